@@ -1,0 +1,437 @@
+"""Decode throughput of the prerouted int4 MoE stack on GB300.
+
+Workload: the 35B-tier 40-layer stack (d=2048, 256 experts, top-4, expert and
+shared intermediate 512, prerouter heads on layers 6-38 with hidden 512, LoRA
+r=16 alpha=32 on the shared expert), batch 1, synthetic seeded weights.  One
+bench step = one decode step = all 40 layers for one token = one launch of the
+persistent engine kernel (edge0_decode_step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  `value` is decode tokens/s with inputs resident in HBM;
+`e2e` the same through the C ABI with pinned host buffers copied in and out
+every step; `roofline` the engine kernel's achieved HBM GB/s against the
+measured copy bandwidth; `cpu_baseline` the CPU oracle on a bounded sample.
+--impl reference times the CPU oracle (the reference arm of this build).
+Multi-GPU runs are independent replicas (no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from int4_routed_expert_prerouter_gb300 import configs  # noqa: E402
+
+METRIC = "decode tokens/s (1 GB300, 35B-tier MoE stack) and achieved HBM GB/s vs roofline"
+CFG = configs.STACK35
+
+
+# ---------------------------------------------------------------- bytes ----
+def algorithmic_bytes_per_token(cfg, own_routed_layers):
+    """Bytes a decode step must read once (int4 experts with scales, shared
+    expert, head dense parts + gathered one-hot columns, LoRA factors, router of
+    each layer that routes itself)."""
+    q4 = configs.q4_bytes
+    expert = configs.expert_bytes(cfg.d, cfg.I)
+    shared = configs.expert_bytes(cfg.d, cfg.Is)
+    head = (cfg.H * cfg.d + cfg.E * cfg.d + cfg.E * cfg.H) * 2 + 2 * cfg.K * (cfg.H + cfg.E) * 2
+    lora = (2 * (cfg.r * cfg.d + cfg.Is * cfg.r) + (cfg.r * cfg.Is + cfg.d * cfg.r)) * 2
+    router = cfg.E * cfg.d * 2
+    n_heads = len(cfg.head_owners())
+    total = cfg.L * (cfg.K * expert + shared + lora) + n_heads * head + own_routed_layers * router
+    del q4
+    return total
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int4_routed_expert_prerouter_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per token of the engine kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "engine_decode_35b_stack_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_token"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------- clocks ----
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in load:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
+
+
+# ------------------------------------------------------------ GPU arm -----
+def run_gpu(args, rank, world):
+    from int4_routed_expert_prerouter_gb300 import binding, inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    cfg = CFG
+    if args.layers or args.experts:
+        # reduced case for profiler captures only (same per-layer shapes)
+        L = args.layers or cfg.L
+        cfg = cfg.with_(L=L, E=args.experts or cfg.E, head_owner_last=min(cfg.head_owner_last, L - 2),
+                        prerouted=tuple(l for l in cfg.prerouted if l < L - 1))
+    model = inputs.make_model(cfg, seed=args.seed, device=dev, small_device=dev)
+    dm = binding.DeviceModel(model, dev)
+    cpu_model = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_model = _host_layers(model, args.cpu_layers)
+    del model
+    torch.cuda.empty_cache()
+    st = binding.DecodeState(cfg, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    B, d = cfg.B, cfg.d
+    # one fresh seeded hidden state per step (each step's h_0), updated in place
+    n_in = args.warmup + 2 * args.steps
+    h_all = torch.empty(n_in, B, d, dtype=torch.float16, device=dev)
+    for i in range(n_in):
+        h_all[i].copy_(inputs.hidden(cfg, i, seed=args.seed, device=dev))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    # warm-up (includes step 0, where every layer routes by its own router)
+    t = 0
+    for _ in range(args.warmup):
+        binding.decode_step(dm, st, h_all[t], t)
+        t += 1
+    barrier()
+    assert st.error() == 0, "kernel error during warm-up"
+
+    if args.trace:
+        st.set_trace(True)
+        binding.decode_step(dm, st, h_all[t], t)
+        t += 1
+        st.set_trace(False)
+        print_trace(st.read_trace(), torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    # device-resident timed region: one event pair per launch for the kernel
+    # duration, one pair around the region for the step time
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            binding.decode_step(dm, st, h_all[t], t)
+            ev[i][1].record(stream)
+            t += 1
+        t_end.record(stream)
+        barrier()
+    assert st.error() == 0, "kernel error in the timed region"
+    region_ms = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # end to end through the C ABI: pinned host input -> device, decode step,
+    # device -> pinned host output, every step
+    h_host_in = torch.empty(args.steps, B, d, dtype=torch.float16).pin_memory()
+    for i in range(args.steps):
+        h_host_in[i].copy_(inputs.hidden(cfg, t + i, seed=args.seed))
+    h_host_out = torch.empty(args.steps, B, d, dtype=torch.float16).pin_memory()
+    h = torch.empty(B, d, dtype=torch.float16, device=dev)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e_start.record(stream)
+    for i in range(args.steps):
+        h.copy_(h_host_in[i], non_blocking=True)
+        binding.decode_step(dm, st, h, t)
+        h_host_out[i].copy_(h, non_blocking=True)
+        t += 1
+    e_end.record(stream)
+    barrier()
+    e2e_ms = e_start.elapsed_time(e_end)
+    assert st.error() == 0
+
+    local = torch.tensor([region_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
+    region_ms, e2e_ms = local.tolist()
+    if rank != 0:
+        return None
+
+    tokens = B * args.steps * world
+    value = tokens / (region_ms / 1e3)
+    e2e_value = tokens / (e2e_ms / 1e3)
+    own = cfg.L - len(cfg.prerouted)
+    bytes_tok = algorithmic_bytes_per_token(cfg, own)
+    mean_kern_s = statistics.mean(kern_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_tok / mean_kern_s / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(region_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4xf16",
+        "data": "synthetic",
+        "config": {
+            "workload": (f"{cfg.name}: {cfg.description}" if cfg is CFG else
+                         f"REDUCED profiling case: {cfg.L} layers, {cfg.E} experts, shapes of {CFG.name}"),
+            "layers": cfg.L, "d_model": cfg.d, "experts": cfg.E, "top_k": cfg.K,
+            "batch": B, "seq_len": 1, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (%.0f MB of weights read per step > 129 MB)" % (bytes_tok / 1e6),
+            "layers_per_s": round(value * cfg.L / world, 1),
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": B * d * 2, "d2h_bytes_per_step": B * d * 2},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None if traffic is None else int(traffic),
+                     "kernel": "edge0::engine_kernel (one launch per decode step)",
+                     "algorithmic_bytes_per_launch": bytes_tok,
+                     "mean_launch_us": round(mean_kern_s * 1e6, 2),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "clocks": clk.summary(),
+    }
+    if cpu_model is not None:
+        line["cpu_baseline"] = cpu_baseline(cpu_model, args)
+    return line
+
+
+def print_trace(tr, nct):
+    """Per-phase split of one traced decode step, averaged over CTAs."""
+    import collections
+    acc = collections.defaultdict(list)
+    for c in range(nct):
+        ev = {}
+        for tag, tm in tr[c].tolist():
+            if tm == 0:
+                break
+            ev[tag] = tm
+        keys = sorted({k >> 4 for k in ev})
+        for k in keys:
+            pts = [ev.get((k << 4) | i) for i in range(4)]
+            if None in pts:
+                continue
+            acc[k].append((pts[1] - pts[0], pts[2] - pts[1], pts[3] - pts[2], pts[3]))
+    tot = [0.0, 0.0, 0.0]
+    lines = []
+    first = min(v[0][3] - sum(v[0][:3]) for v in acc.values()) if acc else 0
+    for k in sorted(acc):
+        v = acc[k]
+        m = [statistics.mean(x[i] for x in v) / 1e3 for i in range(3)]
+        mx = [max(x[i] for x in v) / 1e3 for i in range(3)]
+        tot = [a + b for a, b in zip(tot, m)]
+        lines.append(f"layer {k >> 4:2d} phase {'RAB'[k & 15]}: prologue {m[0]:6.2f} chunks {m[1]:6.2f} "
+                     f"(max {mx[1]:6.2f}) barrier {m[2]:6.2f} us")
+    sys.stderr.write("\n".join(lines) + "\n")
+    sys.stderr.write(f"total (mean over CTAs): prologue {tot[0]:.1f} chunks {tot[1]:.1f} barrier {tot[2]:.1f} us\n")
+
+
+def _host_layers(model, n):
+    """Host copy of layers [6, 6 + n) (a head owner and prerouted layers) for the
+    CPU baseline sample."""
+    from int4_routed_expert_prerouter_gb300 import inputs
+    c = lambda trip: tuple(t.cpu() for t in trip)
+    cfg = model.cfg.with_(L=n, head_owner_first=0, head_owner_last=n - 1, prerouted=tuple(range(n)),
+                          ring=False)
+    m = inputs.Model(cfg, model.seed)
+    for l in range(6, 6 + n):
+        lw = model.layers[l]
+        hd = None if lw.head is None else {k: (v.cpu() if torch.is_tensor(v) else v)
+                                           for k, v in lw.head.items()}
+        if hd is not None:
+            hd["target"] = min(l - 6 + 1, n - 1)
+        m.layers.append(inputs.LayerWeights(c(lw.gate), c(lw.up), c(lw.down), c(lw.sh_gate),
+                                            c(lw.sh_up), c(lw.sh_down), lw.router.cpu(),
+                                            lw.gamma.cpu(), {k: v.cpu() for k, v in lw.lora.items()},
+                                            None, hd, True))
+    return m
+
+
+def cpu_baseline(cpu_model, args):
+    """The CPU oracle (single-threaded C++, fp64) on a bounded sample: decode
+    steps of `cpu_layers` 35B-shaped layers (each with a head, prerouted from
+    the second step), scaled to tokens/s of the 40-layer stack."""
+    import oracle
+    from int4_routed_expert_prerouter_gb300 import inputs
+    cfg = cpu_model.cfg
+    stack = oracle.Stack(cpu_model)
+    per_layer = []
+    for t in range(args.cpu_steps):
+        h = inputs.hidden(cfg, t, seed=args.seed)
+        t0 = time.perf_counter()
+        stack.step(h, t, record=False)
+        per_layer.append((time.perf_counter() - t0) / cfg.L)
+    sec_per_layer = statistics.mean(per_layer[1:] if len(per_layer) > 1 else per_layer)
+    tok_s = 1.0 / (sec_per_layer * CFG.L)
+    return {"value": round(tok_s, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{args.cpu_steps} decode steps of {cfg.L} 35B-tier layers (layers 6..{5 + cfg.L} "
+                      f"of the stack, each with its head; first step excluded), "
+                      f"{sec_per_layer:.3f} s per layer, scaled to {CFG.L} layers per token"}
+
+
+# ------------------------------------------------------ reference arm -----
+def run_reference(args, rank):
+    """The reference arm of this build: the CPU oracle as it stands, on host
+    cores, each bench step one 35B-tier layer of a decode step (a bounded
+    sample), reported in tokens/s of the 40-layer stack."""
+    if rank != 0:
+        return None
+    import oracle
+    from int4_routed_expert_prerouter_gb300 import inputs
+    cfg = CFG.with_(L=2, head_owner_first=0, head_owner_last=0, prerouted=(1,))
+    model = inputs.make_model(cfg, seed=args.seed)
+    stack = oracle.Stack(model)
+    h = inputs.hidden(cfg, 0, seed=args.seed)
+    for t in range(args.warmup):
+        stack.step(h, t, record=False, layers=[t % 2])
+    times = []
+    for i in range(args.steps):
+        t = args.warmup + i
+        t0 = time.perf_counter()
+        stack.step(h, t, record=False, layers=[i % 2])
+        times.append(time.perf_counter() - t0)
+    sec_layer = statistics.mean(times)
+    value = 1.0 / (sec_layer * CFG.L)
+    sample = (f"{args.steps} steps, each one 35B-tier layer (d=2048, E=256, K=4, shared expert, "
+              f"LoRA, head on the first) of a decode step on the CPU oracle, scaled to 40 layers")
+    return {"metric": METRIC, "value": round(value, 5), "unit": "tokens/s", "impl": "reference",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec_layer * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{CFG.name}: {CFG.description}", "batch": 1, "seq_len": 1,
+                       "parallelism": "single host thread"},
+            "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-layers", type=int, default=4)
+    ap.add_argument("--cpu-steps", type=int, default=10)
+    ap.add_argument("--layers", type=int, default=0, help="reduced case for profiler captures")
+    ap.add_argument("--experts", type=int, default=0, help="reduced case for profiler captures")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", action="store_true", help="print a per-phase split of one step")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        args.steps = 12 if args.steps is None else args.steps
+        args.warmup = 3 if args.warmup is None else args.warmup
+        line = run_reference(args, rank)
+    else:
+        args.steps = 512 if args.steps is None else args.steps
+        args.warmup = 8 if args.warmup is None else args.warmup
+        assert args.warmup >= 3
+        if world > 1:
+            torch.distributed.init_process_group("nccl")
+        import __graft_entry__
+        __graft_entry__.build()
+        line = run_gpu(args, rank, world)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+/*
+ * libedge0 -- C ABI of the prerouted int4 MoE decode path on GB300 (sm_103a).
+ *
+ * What the path computes (page titles and sections):
+ *   "The Other Half of the Memory Wall: Serving 35B MoEs from SSD with Trained
+ *    Routing Prediction":
+ *     S3.1 "Math contract"  expert(x) = down(silu(gate(x)) * up(x)), int4 affine
+ *                            group-64 weights;
+ *     S3.2 "Head"           head(feats) = fc2(erf-gelu(fc1 feats)) + linear_init(feats),
+ *                            feats = [x, executed one-hot, previous one-hot],
+ *                            f_in = d_model + 2E; no biases;
+ *     S3.2 "Motivation", "Prediction-as-routing"
+ *                            the head owned by layer N runs at token t and its
+ *                            prediction is layer N+1's routing at t+1;
+ *     S3.3                   unmerged LoRA, y = W_int4 x + (alpha/r) B A x, on the
+ *                            shared-expert projections;
+ *     App. A                 softmax-topk (renormalised) and sigmoid-group routing.
+ *   "Inside Edge0-35B", "Architectural Deep Dive": packed uint32 [E, out, in/8]
+ *    weights with one scale and bias per 64 inputs.
+ *
+ * Conventions for every call
+ *   - Pointers are DEVICE pointers unless the argument says HOST.  The caller
+ *     owns every buffer; the library borrows them for the call, never frees them
+ *     and keeps no global state.
+ *   - fp16 tensors are IEEE binary16 (passed as uint16_t); fp32 as float.
+ *   - Every call enqueues work on `stream` and returns without synchronising.
+ *     Arguments are validated on the host before anything is launched; an
+ *     invalid argument returns EDGE0_EINVAL and launches nothing.
+ *   - Kernels never trap: a wait that runs out of time records EDGE0_ETIMEOUT in
+ *     the route state's control block (read it with edge0_state_error) and the
+ *     kernel returns.
+ *
+ * Weight layouts
+ *   Canonical (the pages'): int4 matrix [out, in] = q uint32 [out, in/8] (nibble i
+ *   of word j is input 8j+i, low nibble first), s and b fp16 [out, in/64],
+ *   w = s*q + b; experts stacked on a leading [E] axis.  Dense fp16 weights are
+ *   nn.Linear [out, in] row-major.
+ *   Packed (this library's HBM layout): rows are taken 16 at a time ("row tile",
+ *   padded with zero rows), inputs 64 at a time ("group"); one (row tile, group)
+ *   "unit" is stored contiguously in the order one warp's tensor-core fragments
+ *   read it, so a warp streams each unit as one 512-byte burst.
+ *     int4 unit: 576 bytes = 512 bytes of nibbles + 64 bytes of scales/biases.
+ *     fp16 unit: 2048 bytes.
+ *   Units run group-fastest within a row tile, row tiles follow each other, and
+ *   experts follow each other.  Use edge0_pack_* to convert canonical weights.
+ */
+#ifndef EDGE0_H
+#define EDGE0_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define EDGE0_OK 0
+#define EDGE0_EINVAL 1      /* bad argument: NULL, shape, K > E, in % 64, misalignment */
+#define EDGE0_ECUDA 2       /* a CUDA runtime call failed */
+#define EDGE0_ETIMEOUT 3    /* a bounded device wait ran out (reported by the kernel) */
+#define EDGE0_EUNSUPPORTED 4/* shape outside what this build handles (see limits) */
+
+const char* edge0_status_string(int status);
+
+/* ---- limits of this build ---- */
+#define EDGE0_MAX_LAYERS 48
+#define EDGE0_MAX_BATCH 4     /* sequences per decode call */
+#define EDGE0_MAX_K 8
+#define EDGE0_MAX_E 512
+
+/* ---- routing rule [App. A] ---- */
+#define EDGE0_ROUTE_SOFTMAX_TOPK 0
+#define EDGE0_ROUTE_SIGMOID_GROUP 1
+typedef struct {
+    int kind;            /* EDGE0_ROUTE_* */
+    int n_groups;        /* sigmoid-group: number of groups n (E % n == 0) */
+    int topk_groups;     /* sigmoid-group: groups kept G */
+    float scale;         /* sigmoid-group: routed scale s */
+    const float* bias;   /* [E] fp32 selection bias or NULL.  softmax-topk adds it to the
+                            logits before softmax and selection; sigmoid-group adds it to
+                            sigmoid(logit) for selection only (weights use raw sigmoid). */
+} edge0_route;
+
+/* ---- routed + shared int4 experts ---- */
+typedef struct {
+    int d, E, K, I, Is;        /* d_model, experts, top-k, expert and shared intermediate */
+    const void* gate;          /* packed int4 [E][I x d]   (edge0_pack_q4)            */
+    const void* up;            /* packed int4 [E][I x d]                               */
+    const void* down;          /* packed int4 [E][d x I]                               */
+    const void* sh_gate;       /* packed int4 [Is x d], or NULL for no shared expert   */
+    const void* sh_up;         /* packed int4 [Is x d]                                 */
+    const void* sh_down;       /* packed int4 [d x Is]                                 */
+    const int32_t* slot_table; /* [E] expert id -> slot in the stacks above, or NULL   */
+    int n_slots;               /* slots in the stacks when slot_table != NULL (a slot
+                                  outside [0, n_slots) makes the kernel record EDGE0_EINVAL) */
+} edge0_moe_desc;
+
+/* ---- one unmerged LoRA projection [S3.3]: y += (alpha/r) B (A v) ---- */
+typedef struct {
+    int r, in, out;
+    float alpha;
+    const void* A;             /* packed fp16 [r x in]  (edge0_pack_f16)               */
+    const uint16_t* B;         /* fp16 [out, r] row-major                              */
+} edge0_lora_desc;
+
+/* ---- prerouter head [S3.2 "Head"] ---- */
+typedef struct {
+    int d, E, H, K;
+    const void* fc1_dense;     /* packed fp16 [H x d]: fc1[:, :d]                      */
+    const uint16_t* fc1_oh_T;  /* fp16 [2E, H]: row j = fc1[:, d + j] (edge0_pack_cols_T) */
+    const void* fc2;           /* packed fp16 [E x H]                                  */
+    const void* linit_dense;   /* packed fp16 [E x d]: linear_init[:, :d]              */
+    const uint16_t* linit_oh_T;/* fp16 [2E, E]: row j = linear_init[:, d + j]          */
+    edge0_route route;         /* routing rule of the layer whose routing it predicts  */
+} edge0_head_desc;
+
+/* ---- one decode layer ---- */
+typedef struct {
+    edge0_moe_desc moe;
+    edge0_lora_desc lora_gate, lora_up, lora_down; /* shared expert; A == NULL: no LoRA */
+    const void* router;        /* packed fp16 [E x d] own router                       */
+    edge0_route route;         /* this layer's routing rule                            */
+    const uint16_t* gamma;     /* [d] RMSNorm gain, or NULL for unit gain              */
+    float eps;                 /* RMSNorm epsilon                                      */
+    int prerouted;             /* 1: at step > 0 route by the upstream head's prediction */
+    int has_head;              /* 1: this layer owns `head`                            */
+    edge0_head_desc head;
+    int head_target;           /* state row the head's prediction is written to        */
+    int index;                 /* this layer's row in the route state                  */
+} edge0_layer_desc;
+
+/* ---- routing state carried across steps and the kernels' scratch ----
+ * pred_ids/pred_w [2][L][B][K]: slot (t & 1) holds the predictions made at step t
+ *   (consumed at t + 1); exec_ids [2][L][B][K]: slot (t & 1) holds the ids each
+ *   layer executed at step t (the head's executed mask at t, previous mask at t+1).
+ * workspace: device scratch of edge0_workspace_bytes(d, E, K, I, Is, H, r, B)
+ *   bytes, zeroed by edge0_state_init before first use; it holds accumulators,
+ *   the residual stream between layers, the grid barrier and the error word.
+ *   Its layout depends on H and r, so the state records them: every layer run on
+ *   this state must have head width H (if it owns a head) and LoRA rank r (if it
+ *   has LoRA).  A workspace belongs to one kind of call (decode on this state,
+ *   edge0_moe_int4_forward, or edge0_prerouter_topk): calls of different kinds
+ *   must not share one. */
+typedef struct {
+    int L, B, K;
+    int H, r;
+    int32_t* pred_ids;
+    float* pred_w;
+    int32_t* exec_ids;
+    void* workspace;
+    size_t workspace_bytes;
+} edge0_route_state;
+
+/* ---- packing (device -> device, enqueued on stream) ---- */
+size_t edge0_q4_packed_bytes(int E, int out, int in);
+/* q [E, out, in/8] uint32, s/b [E, out, in/64] fp16 -> packed int4 units */
+int edge0_pack_q4(const uint32_t* q, const uint16_t* s, const uint16_t* b, int E, int out, int in,
+                  void* packed, cudaStream_t stream);
+size_t edge0_f16_packed_bytes(int out, int in);
+/* W [out, in] fp16 with row stride ld elements (use ld > in for a column slice) */
+int edge0_pack_f16(const uint16_t* W, int out, int in, int ld, void* packed, cudaStream_t stream);
+/* dst [ncols, out] = transpose of W[:, col0 : col0 + ncols] (W row stride ld) */
+int edge0_pack_cols_T(const uint16_t* W, int out, int ld, int col0, int ncols, uint16_t* dst,
+                      cudaStream_t stream);
+
+/* ---- state ---- */
+size_t edge0_workspace_bytes(int d, int E, int K, int I, int Is, int H, int r, int B);
+/* zero pred/exec/workspace; must precede the first decode call on a state */
+int edge0_state_init(edge0_route_state* st, cudaStream_t stream);
+/* HOST call: synchronises `stream`, returns the kernels' recorded status (EDGE0_OK,
+ * EDGE0_ETIMEOUT) in *status and clears it. */
+int edge0_state_error(const edge0_route_state* st, cudaStream_t stream, int* status);
+
+/* ---- the four operations of the path ---- */
+
+/* Prerouter head + top-K [S3.2 "Head", App. A].
+ * x [B, d] fp16 post-attention-norm hidden state; exec_ids [B, K] the experts this
+ * layer executed at this token; prev_ids [B, K] those of the previous token, or
+ * NULL (no previous token: zero mask).  Writes the predicted routing for the
+ * head's target layer: out_ids [B, K] (score-descending, lower id first on ties),
+ * out_w [B, K]; out_logits [B, E] (optional, NULL to skip) the head's fp32 logits.
+ * workspace: scratch of edge0_workspace_bytes(d, E, K, 64, 64, H, 16, B) bytes,
+ * zeroed before its first use (cudaMemset). */
+int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t* x, const int32_t* exec_ids,
+                         const int32_t* prev_ids, int B, int32_t* out_ids, float* out_w,
+                         float* out_logits, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* Routed + shared int4 SwiGLU experts [S3.1 "Math contract"], no LoRA:
+ * y_b = sum_k w[b,k] expert_{ids[b,k]}(x_b) + shared(x_b).
+ * x [B, d] fp16; ids [B, K] int32 (0 <= id < E); w [B, K] fp32; y [B, d] fp16.
+ * workspace as for edge0_prerouter_topk (edge0_workspace_bytes(d, E, K, I, Is, 64, 16, B)). */
+int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t* x, const int32_t* ids,
+                           const float* w, int B, uint16_t* y, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/* Unmerged LoRA delta [S3.3]: y[b] += (alpha/r) B (A v[b]) for v [B, in] fp16,
+ * y [B, out] fp16 (read, add in fp32, round to fp16).  Needs no workspace. */
+int edge0_lora_delta(const edge0_lora_desc* lora, const uint16_t* v, int B, uint16_t* y_inout,
+                     cudaStream_t stream);
+
+/* One decode layer at step `step` for B sequences: h_inout [B, d] fp16 is the
+ * layer input (residual stream) and receives the layer output
+ *   h + routed experts + shared expert (with LoRA),
+ * with routing from the upstream head's prediction (prerouted layers, step > 0)
+ * or the layer's own router; if the layer owns a head, its prediction for
+ * head_target at step + 1 is written to the state.  step < 0 uses and advances
+ * the step counter kept in the workspace. */
+int edge0_decode_layer(const edge0_layer_desc* layer, uint16_t* h_inout, edge0_route_state* st,
+                       int B, int step, cudaStream_t stream);
+
+/* All L layers of one decode step in one persistent launch (same semantics as L
+ * successive edge0_decode_layer calls). */
+int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
+                      edge0_route_state* st, int B, int step, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

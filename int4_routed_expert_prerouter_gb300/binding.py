@@ -1,0 +1,311 @@
+"""ctypes binding of libedge0 (include/edge0.h): argument marshalling only.
+
+PyTorch provides device memory and streams; every step of the decode path runs
+in the library's CUDA kernels.  Importing this module loads the compiled
+library and raises if it is missing -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import build as _build
+from .configs import SIGMOID_GROUP, Config
+
+P = C.c_void_p
+EDGE0_OK, EDGE0_EINVAL, EDGE0_ECUDA, EDGE0_ETIMEOUT, EDGE0_EUNSUPPORTED = 0, 1, 2, 3, 4
+MAX_LAYERS, MAX_BATCH = 48, 4
+
+_lib = None
+
+
+class Edge0Error(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libedge0 is not built ({path}); run __graft_entry__.build()")
+        _lib = C.CDLL(path)
+        _declare(_lib)
+    return _lib
+
+
+# ------------------------------------------------------------- structs ----
+class Route(C.Structure):
+    _fields_ = [("kind", C.c_int), ("n_groups", C.c_int), ("topk_groups", C.c_int),
+                ("scale", C.c_float), ("bias", P)]
+
+
+class MoeDesc(C.Structure):
+    _fields_ = [("d", C.c_int), ("E", C.c_int), ("K", C.c_int), ("I", C.c_int), ("Is", C.c_int),
+                ("gate", P), ("up", P), ("down", P), ("sh_gate", P), ("sh_up", P), ("sh_down", P),
+                ("slot_table", P), ("n_slots", C.c_int)]
+
+
+class LoraDesc(C.Structure):
+    _fields_ = [("r", C.c_int), ("in_", C.c_int), ("out", C.c_int), ("alpha", C.c_float),
+                ("A", P), ("B", P)]
+
+
+class HeadDesc(C.Structure):
+    _fields_ = [("d", C.c_int), ("E", C.c_int), ("H", C.c_int), ("K", C.c_int),
+                ("fc1_dense", P), ("fc1_oh_T", P), ("fc2", P), ("linit_dense", P),
+                ("linit_oh_T", P), ("route", Route)]
+
+
+class LayerDesc(C.Structure):
+    _fields_ = [("moe", MoeDesc), ("lora_gate", LoraDesc), ("lora_up", LoraDesc),
+                ("lora_down", LoraDesc), ("router", P), ("route", Route), ("gamma", P),
+                ("eps", C.c_float), ("prerouted", C.c_int), ("has_head", C.c_int),
+                ("head", HeadDesc), ("head_target", C.c_int), ("index", C.c_int)]
+
+
+class RouteState(C.Structure):
+    _fields_ = [("L", C.c_int), ("B", C.c_int), ("K", C.c_int), ("H", C.c_int), ("r", C.c_int),
+                ("pred_ids", P), ("pred_w", P), ("exec_ids", P), ("workspace", P),
+                ("workspace_bytes", C.c_size_t)]
+
+
+def _declare(L):
+    L.edge0_status_string.argtypes = [C.c_int]
+    L.edge0_status_string.restype = C.c_char_p
+    L.edge0_q4_packed_bytes.argtypes = [C.c_int] * 3
+    L.edge0_q4_packed_bytes.restype = C.c_size_t
+    L.edge0_pack_q4.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, P, P]
+    L.edge0_f16_packed_bytes.argtypes = [C.c_int] * 2
+    L.edge0_f16_packed_bytes.restype = C.c_size_t
+    L.edge0_pack_f16.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
+    L.edge0_pack_cols_T.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, P, P]
+    L.edge0_workspace_bytes.argtypes = [C.c_int] * 8
+    L.edge0_workspace_bytes.restype = C.c_size_t
+    L.edge0_state_init.argtypes = [C.POINTER(RouteState), P]
+    L.edge0_state_error.argtypes = [C.POINTER(RouteState), P, C.POINTER(C.c_int)]
+    L.edge0_prerouter_topk.argtypes = [C.POINTER(HeadDesc), P, P, P, C.c_int, P, P, P, P,
+                                       C.c_size_t, P]
+    L.edge0_moe_int4_forward.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P, C.c_size_t, P]
+    L.edge0_lora_delta.argtypes = [C.POINTER(LoraDesc), P, C.c_int, P, P]
+    L.edge0_decode_layer.argtypes = [C.POINTER(LayerDesc), P, C.POINTER(RouteState), C.c_int,
+                                     C.c_int, P]
+    L.edge0_decode_step.argtypes = [C.POINTER(LayerDesc), C.c_int, P, C.POINTER(RouteState),
+                                    C.c_int, C.c_int, P]
+    for name in ("edge0_pack_q4", "edge0_pack_f16", "edge0_pack_cols_T", "edge0_state_init",
+                 "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
+                 "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step"):
+        getattr(L, name).restype = C.c_int
+
+
+EXPORTED = ["edge0_status_string", "edge0_q4_packed_bytes", "edge0_pack_q4", "edge0_f16_packed_bytes",
+            "edge0_pack_f16", "edge0_pack_cols_T", "edge0_workspace_bytes", "edge0_state_init",
+            "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
+            "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step"]
+
+
+def status_string(code: int) -> str:
+    return lib().edge0_status_string(code).decode()
+
+
+def _check(code, what):
+    if code != EDGE0_OK:
+        raise Edge0Error(code, what)
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------ packing ----
+def pack_q4(q, s, b, stream=None) -> torch.Tensor:
+    """q [E, out, in/8] int32, s/b [E, out, in/64] fp16 (device) -> packed uint8 buffer."""
+    E, out, w8 = q.shape
+    inp = w8 * 8
+    n = lib().edge0_q4_packed_bytes(E, out, inp)
+    dst = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check(lib().edge0_pack_q4(_ptr(q.contiguous()), _ptr(s.contiguous()), _ptr(b.contiguous()),
+                               E, out, inp, _ptr(dst), _stream(stream)), "edge0_pack_q4")
+    return dst
+
+
+def pack_f16(W, ld=None, cols=None, stream=None) -> torch.Tensor:
+    """W [out, ld] fp16 (device); packs W[:, :cols]."""
+    out, full = W.shape
+    inp = cols if cols is not None else full
+    n = lib().edge0_f16_packed_bytes(out, inp)
+    dst = torch.empty(n, dtype=torch.uint8, device=W.device)
+    _check(lib().edge0_pack_f16(_ptr(W.contiguous()), out, inp, full, _ptr(dst), _stream(stream)),
+           "edge0_pack_f16")
+    return dst
+
+
+def pack_cols_T(W, col0, ncols, stream=None) -> torch.Tensor:
+    out, ld = W.shape
+    dst = torch.empty(ncols, out, dtype=torch.float16, device=W.device)
+    _check(lib().edge0_pack_cols_T(_ptr(W.contiguous()), out, ld, col0, ncols, _ptr(dst),
+                                   _stream(stream)), "edge0_pack_cols_T")
+    return dst
+
+
+def workspace_bytes(d, E, K, I, Is, H, r, B) -> int:
+    return int(lib().edge0_workspace_bytes(d, E, K, I, Is, H, r, B))
+
+
+# ------------------------------------------------------------ the model ----
+def _route(cfg: Config, bias) -> Route:
+    if cfg.route_kind == SIGMOID_GROUP:
+        return Route(SIGMOID_GROUP, cfg.n_groups, cfg.topk_groups, cfg.route_scale, _ptr(bias))
+    return Route(0, 1, 1, 1.0, _ptr(bias))
+
+
+class DeviceModel:
+    """A model's weights packed on the GPU plus the layer descriptors that point at them."""
+
+    def __init__(self, model, device="cuda", stream=None):
+        cfg = model.cfg
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.keep = []
+        dev = self.device
+        self.layers = (LayerDesc * cfg.L)()
+        self.biases = []
+        for l, lw in enumerate(model.layers):
+            self.biases.append(None if lw.bias is None else lw.bias.to(dev, torch.float32).contiguous())
+        for l, lw in enumerate(model.layers):
+            self.layers[l] = self._layer(cfg, l, lw, model, stream)
+        torch.cuda.synchronize(dev)
+
+    def _k(self, t):
+        self.keep.append(t)
+        return _ptr(t)
+
+    def _layer(self, cfg, l, lw, model, stream):
+        dev = self.device
+        d, E, K, I, Is, H, r = cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.H, cfg.r
+        g = lambda t: t.to(dev)
+        L = LayerDesc()
+        pq = lambda trip: pack_q4(g(trip[0]), g(trip[1]), g(trip[2]), stream)
+        L.moe = MoeDesc(d, E, K, I, Is, self._k(pq(lw.gate)), self._k(pq(lw.up)), self._k(pq(lw.down)),
+                        self._k(pq(lw.sh_gate)), self._k(pq(lw.sh_up)), self._k(pq(lw.sh_down)),
+                        None, 0)
+        lo = lw.lora
+        alpha = float(cfg.alpha)
+        L.lora_gate = LoraDesc(r, d, Is, alpha, self._k(pack_f16(g(lo["Ag"]), stream=stream)),
+                               self._k(g(lo["Bg"]).contiguous()))
+        L.lora_up = LoraDesc(r, d, Is, alpha, self._k(pack_f16(g(lo["Au"]), stream=stream)),
+                             self._k(g(lo["Bu"]).contiguous()))
+        L.lora_down = LoraDesc(r, Is, d, alpha, self._k(pack_f16(g(lo["Ad"]), stream=stream)),
+                               self._k(g(lo["Bd"]).contiguous()))
+        L.router = self._k(pack_f16(g(lw.router), stream=stream))
+        L.route = _route(cfg, self.biases[l])
+        L.gamma = self._k(g(lw.gamma).contiguous())
+        L.eps = cfg.eps
+        L.prerouted = 1 if lw.prerouted else 0
+        L.index = l
+        if lw.head is not None:
+            hd = lw.head
+            fc1, fc2, linit = g(hd["fc1"]), g(hd["fc2"]), g(hd["linit"])
+            tgt = hd["target"]
+            L.has_head = 1
+            L.head_target = tgt
+            L.head = HeadDesc(d, E, H, K, self._k(pack_f16(fc1, cols=d, stream=stream)),
+                              self._k(pack_cols_T(fc1, d, 2 * E, stream)),
+                              self._k(pack_f16(fc2, stream=stream)),
+                              self._k(pack_f16(linit, cols=d, stream=stream)),
+                              self._k(pack_cols_T(linit, d, 2 * E, stream)),
+                              _route(cfg, self.biases[tgt]))
+        return L
+
+
+class DecodeState:
+    """Routing state + workspace for B sequences over a model's L layers."""
+
+    def __init__(self, cfg: Config, B=None, device="cuda", stream=None):
+        B = cfg.B if B is None else B
+        dev = torch.device(device)
+        self.B = B
+        self.pred_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
+        self.pred_w = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.float32, device=dev)
+        self.exec_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
+        nbytes = workspace_bytes(cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.H, cfg.r, B)
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        self.st = RouteState(cfg.L, B, cfg.K, cfg.H, cfg.r, _ptr(self.pred_ids), _ptr(self.pred_w),
+                             _ptr(self.exec_ids), _ptr(self.workspace), nbytes)
+        _check(lib().edge0_state_init(C.byref(self.st), _stream(stream)), "edge0_state_init")
+
+    TRACE_CTAS, TRACE_SLOTS = 160, 1024
+
+    def set_trace(self, on: bool):
+        """Switch the engine's phase trace on/off (workspace header flag)."""
+        torch.cuda.synchronize(self.workspace.device)
+        flag = torch.tensor([1 if on else 0], dtype=torch.int32)
+        self.workspace[24:28].copy_(flag.view(torch.uint8))
+        if on:
+            self.workspace[-self.TRACE_CTAS * self.TRACE_SLOTS * 8:].zero_()
+        torch.cuda.synchronize(self.workspace.device)
+
+    def read_trace(self):
+        """[CTAs, events, 2] int64: (tag, globaltimer ns) pairs, tag = layer << 8 |
+        phase << 4 | point (0 start, 1 prologue done, 2 chunks done, 3 barrier done)."""
+        torch.cuda.synchronize(self.workspace.device)
+        raw = self.workspace[-self.TRACE_CTAS * self.TRACE_SLOTS * 8:].cpu().view(torch.int64)
+        return raw.view(self.TRACE_CTAS, self.TRACE_SLOTS // 2, 2)
+
+    def error(self, stream=None) -> int:
+        code = C.c_int(0)
+        _check(lib().edge0_state_error(C.byref(self.st), _stream(stream), C.byref(code)),
+               "edge0_state_error")
+        return code.value
+
+
+# ---------------------------------------------------------- operations ----
+def decode_step(dm: DeviceModel, st: DecodeState, h: torch.Tensor, step: int, stream=None):
+    """All layers of one decode step on h [B, d] fp16 (device, in place)."""
+    assert h.is_cuda and h.dtype == torch.float16 and h.is_contiguous()
+    _check(lib().edge0_decode_step(dm.layers, dm.cfg.L, _ptr(h), C.byref(st.st), st.B, step,
+                                   _stream(stream)), "edge0_decode_step")
+
+
+def decode_layer(dm: DeviceModel, l: int, st: DecodeState, h: torch.Tensor, step: int, stream=None):
+    assert h.is_cuda and h.dtype == torch.float16 and h.is_contiguous()
+    _check(lib().edge0_decode_layer(C.byref(dm.layers[l]), _ptr(h), C.byref(st.st), st.B, step,
+                                    _stream(stream)), "edge0_decode_layer")
+
+
+def moe_int4_forward(dm: DeviceModel, l: int, x, ids, w, workspace, stream=None) -> torch.Tensor:
+    B = x.shape[0]
+    y = torch.empty_like(x)
+    _check(lib().edge0_moe_int4_forward(C.byref(dm.layers[l].moe), _ptr(x), _ptr(ids), _ptr(w), B,
+                                        _ptr(y), _ptr(workspace), workspace.numel(),
+                                        _stream(stream)), "edge0_moe_int4_forward")
+    return y
+
+
+def prerouter_topk(dm: DeviceModel, l: int, x, exec_ids, prev_ids, workspace, stream=None):
+    cfg = dm.cfg
+    B = x.shape[0]
+    ids = torch.empty(B, cfg.K, dtype=torch.int32, device=x.device)
+    w = torch.empty(B, cfg.K, dtype=torch.float32, device=x.device)
+    logits = torch.empty(B, cfg.E, dtype=torch.float32, device=x.device)
+    _check(lib().edge0_prerouter_topk(C.byref(dm.layers[l].head), _ptr(x), _ptr(exec_ids),
+                                      _ptr(prev_ids), B, _ptr(ids), _ptr(w), _ptr(logits),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)),
+           "edge0_prerouter_topk")
+    return ids, w, logits
+
+
+def lora_delta(desc: LoraDesc, v, y, stream=None):
+    B = v.shape[0]
+    _check(lib().edge0_lora_delta(C.byref(desc), _ptr(v), B, _ptr(y), _stream(stream)),
+           "edge0_lora_delta")
+    return y

@@ -1,0 +1,353 @@
+// C ABI entry points of libedge0: argument validation on the host, translation
+// of the public descriptors into the engine's kernel parameter block, launch.
+#include <string.h>
+
+#include "internal.cuh"
+
+using namespace edge0;
+
+namespace {
+
+bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+struct Dims {
+    int d, E, K, I, Is, H, r;
+};
+
+int check_route(const edge0_route& r, int E, int K) {
+    if (r.kind == EDGE0_ROUTE_SOFTMAX_TOPK) return EDGE0_OK;
+    if (r.kind != EDGE0_ROUTE_SIGMOID_GROUP) return EDGE0_EINVAL;
+    if (r.n_groups <= 0 || r.n_groups > 32 || E % r.n_groups) return EDGE0_EINVAL;
+    if (E / r.n_groups < 2) return EDGE0_EINVAL;
+    if (r.topk_groups <= 0 || r.topk_groups > r.n_groups) return EDGE0_EINVAL;
+    if (K > r.topk_groups * (E / r.n_groups)) return EDGE0_EINVAL;
+    return EDGE0_OK;
+}
+
+int check_dims(const Dims& D, int B) {
+    if (B <= 0 || B > EDGE0_MAX_BATCH) return EDGE0_EINVAL;
+    if (D.d <= 0 || D.d % kGroup || D.I <= 0 || D.I % kGroup || D.Is <= 0 || D.Is % kGroup)
+        return EDGE0_EINVAL;
+    if (D.H <= 0 || D.H % kGroup) return EDGE0_EINVAL;
+    if (D.E <= 0 || D.E > EDGE0_MAX_E || D.E % 8) return EDGE0_EINVAL;
+    if (D.K <= 0 || D.K > EDGE0_MAX_K || D.K > D.E) return EDGE0_EINVAL;
+    if (D.r <= 0 || D.r > 32) return EDGE0_EINVAL;
+    // what one shared-memory stage must hold
+    if ((long long)D.Is * D.r * 2 > kStageBytes) return EDGE0_EUNSUPPORTED;
+    if (f16_bytes(D.r, D.Is) > kStageBytes) return EDGE0_EUNSUPPORTED;
+    if (2LL * D.K * D.H * 2 > kStageBytes || 2LL * D.K * D.E * 2 > kStageBytes)
+        return EDGE0_EUNSUPPORTED;
+    if (2 * B * D.K + 8 > kMaxSeg) return EDGE0_EUNSUPPORTED;
+    return EDGE0_OK;
+}
+
+void route_into(const edge0_route& r, int* kind, int* ng, int* tg, float* sc, const float** bias) {
+    *kind = r.kind;
+    *ng = r.n_groups > 0 ? r.n_groups : 1;
+    *tg = r.topk_groups > 0 ? r.topk_groups : 1;
+    *sc = r.scale;
+    *bias = r.bias;
+}
+
+int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P) {
+    const edge0_moe_desc& m = Ld.moe;
+    if (m.d != D.d || m.E != D.E || m.K != D.K || m.I != D.I || m.Is != D.Is) return EDGE0_EINVAL;
+    if (!m.gate || !m.up || !m.down || !Ld.router) return EDGE0_EINVAL;
+    if (!al16(m.gate) || !al16(m.up) || !al16(m.down) || !al16(Ld.router)) return EDGE0_EINVAL;
+    if (m.slot_table && m.n_slots <= 0) return EDGE0_EINVAL;
+    memset(&P, 0, sizeof(P));
+    P.gate = (const char*)m.gate;
+    P.up = (const char*)m.up;
+    P.down = (const char*)m.down;
+    P.slot_table = m.slot_table;
+    P.n_slots = m.slot_table ? m.n_slots : m.E;
+    P.router = (const char*)Ld.router;
+    P.gamma = (const __half*)Ld.gamma;
+    P.eps = Ld.eps;
+    int rc = check_route(Ld.route, D.E, D.K);
+    if (rc) return rc;
+    route_into(Ld.route, &P.route_kind, &P.n_groups, &P.topk_groups, &P.route_scale, &P.bias);
+    int flags = 0;
+    if (Ld.prerouted) flags |= LF_PREROUTED;
+    if (m.sh_gate || m.sh_up || m.sh_down) {
+        if (!m.sh_gate || !m.sh_up || !m.sh_down) return EDGE0_EINVAL;
+        if (!al16(m.sh_gate) || !al16(m.sh_up) || !al16(m.sh_down)) return EDGE0_EINVAL;
+        P.sh_gate = (const char*)m.sh_gate;
+        P.sh_up = (const char*)m.sh_up;
+        P.sh_down = (const char*)m.sh_down;
+        flags |= LF_SHARED;
+    }
+    const edge0_lora_desc &lg = Ld.lora_gate, &lu = Ld.lora_up, &ld = Ld.lora_down;
+    if (lg.A || lu.A || ld.A) {
+        if (!(flags & LF_SHARED)) return EDGE0_EINVAL;
+        if (!lg.A || !lu.A || !ld.A || !lg.B || !lu.B || !ld.B) return EDGE0_EINVAL;
+        if (lg.r != D.r || lu.r != D.r || ld.r != D.r) return EDGE0_EINVAL;
+        if (lg.in != D.d || lg.out != D.Is || lu.in != D.d || lu.out != D.Is || ld.in != D.Is ||
+            ld.out != D.d)
+            return EDGE0_EINVAL;
+        if (lg.alpha != lu.alpha || lg.alpha != ld.alpha) return EDGE0_EINVAL;
+        if (!al16(lg.A) || !al16(lu.A) || !al16(ld.A) || !al16(lg.B) || !al16(lu.B) || !al16(ld.B))
+            return EDGE0_EINVAL;
+        P.lora_Ag = (const char*)lg.A;
+        P.lora_Au = (const char*)lu.A;
+        P.lora_Ad = (const char*)ld.A;
+        P.lora_Bg = (const __half*)lg.B;
+        P.lora_Bu = (const __half*)lu.B;
+        P.lora_Bd = (const __half*)ld.B;
+        P.lora_scale = lg.alpha / (float)D.r;
+        flags |= LF_LORA;
+    }
+    if (Ld.has_head) {
+        const edge0_head_desc& h = Ld.head;
+        if (h.d != D.d || h.E != D.E || h.H != D.H || h.K != D.K) return EDGE0_EINVAL;
+        if (!h.fc1_dense || !h.fc1_oh_T || !h.fc2 || !h.linit_dense || !h.linit_oh_T)
+            return EDGE0_EINVAL;
+        if (!al16(h.fc1_dense) || !al16(h.fc1_oh_T) || !al16(h.fc2) || !al16(h.linit_dense) ||
+            !al16(h.linit_oh_T))
+            return EDGE0_EINVAL;
+        if (Ld.head_target < 0 || Ld.head_target >= Lstate) return EDGE0_EINVAL;
+        rc = check_route(h.route, D.E, D.K);
+        if (rc) return rc;
+        P.fc1 = (const char*)h.fc1_dense;
+        P.fc1_oh = (const __half*)h.fc1_oh_T;
+        P.fc2 = (const char*)h.fc2;
+        P.linit = (const char*)h.linit_dense;
+        P.linit_oh = (const __half*)h.linit_oh_T;
+        route_into(h.route, &P.head_route_kind, &P.head_n_groups, &P.head_topk_groups,
+                   &P.head_route_scale, &P.head_bias);
+        P.head_target = Ld.head_target;
+        flags |= LF_HEAD;
+    }
+    if (Ld.index < 0 || Ld.index >= Lstate) return EDGE0_EINVAL;
+    P.sidx = Ld.index;
+    P.flags = flags;
+    return EDGE0_OK;
+}
+
+int launch(const Prog& p, cudaStream_t stream) {
+    int dev = 0, nsm = 0, maxsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EDGE0_ECUDA;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return EDGE0_ECUDA;
+    if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return EDGE0_ECUDA;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, engine_kernel) != cudaSuccess) return EDGE0_ECUDA;
+    const int smem = engine_smem_bytes(p);
+    if (smem + (int)fa.sharedSizeBytes > maxsm) return EDGE0_EUNSUPPORTED;
+    if (cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return EDGE0_ECUDA;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(nsm);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, engine_kernel, p) != cudaSuccess) return EDGE0_ECUDA;
+    return EDGE0_OK;
+}
+
+void set_dims(Prog& p, const Dims& D, int B) {
+    p.B = B;
+    p.d = D.d;
+    p.E = D.E;
+    p.K = D.K;
+    p.I = D.I;
+    p.Is = D.Is;
+    p.H = D.H;
+    p.r = D.r;
+}
+
+int check_ws(const Dims& D, int B, const void* ws, size_t bytes) {
+    if (!ws || !al16(ws)) return EDGE0_EINVAL;
+    if ((long long)bytes < ws_bytes(B, D.K, D.I, D.Is, D.r, D.H, D.E, D.d)) return EDGE0_EINVAL;
+    return EDGE0_OK;
+}
+
+int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_route_state* st, int B,
+                  int step, cudaStream_t stream) {
+    if (!layers || !h || !st || L <= 0 || L > EDGE0_MAX_LAYERS) return EDGE0_EINVAL;
+    if (!st->pred_ids || !st->pred_w || !st->exec_ids) return EDGE0_EINVAL;
+    if (st->B != B || st->L <= 0 || st->K != layers[0].moe.K) return EDGE0_EINVAL;
+    if (!al16(h)) return EDGE0_EINVAL;
+    Dims D;
+    D.d = layers[0].moe.d;
+    D.E = layers[0].moe.E;
+    D.K = layers[0].moe.K;
+    D.I = layers[0].moe.I;
+    D.Is = layers[0].moe.Is;
+    // the workspace layout is fixed by the state's dims, whatever this call runs
+    D.H = st->H;
+    D.r = st->r;
+    for (int l = 0; l < L; ++l) {
+        if (layers[l].has_head && layers[l].head.H != D.H) return EDGE0_EINVAL;
+        if (layers[l].lora_gate.A && layers[l].lora_gate.r != D.r) return EDGE0_EINVAL;
+    }
+    int rc = check_dims(D, B);
+    if (rc) return rc;
+    rc = check_ws(D, B, st->workspace, st->workspace_bytes);
+    if (rc) return rc;
+    static_assert(sizeof(Prog) <= 32000, "kernel parameter block too large");
+    Prog* p = new Prog;
+    memset(p, 0, sizeof(Prog));
+    p->mode = MODE_DECODE;
+    p->L = L;
+    set_dims(*p, D, B);
+    p->step = step;
+    p->h_io = (__half*)h;
+    p->pred_ids = st->pred_ids;
+    p->pred_w = st->pred_w;
+    p->exec_ids = st->exec_ids;
+    p->Ls = st->L;
+    p->ws = (char*)st->workspace;
+    for (int l = 0; l < L && rc == EDGE0_OK; ++l) rc = fill_layer(layers[l], D, st->L, p->layers[l]);
+    if (rc == EDGE0_OK) rc = launch(*p, stream);
+    delete p;
+    return rc;
+}
+
+}  // namespace
+
+extern "C" const char* edge0_status_string(int status) {
+    switch (status) {
+        case EDGE0_OK: return "ok";
+        case EDGE0_EINVAL: return "invalid argument";
+        case EDGE0_ECUDA: return "CUDA runtime error";
+        case EDGE0_ETIMEOUT: return "a bounded device wait timed out";
+        case EDGE0_EUNSUPPORTED: return "shape not supported by this build";
+        default: return "unknown status";
+    }
+}
+
+extern "C" size_t edge0_workspace_bytes(int d, int E, int K, int I, int Is, int H, int r, int B) {
+    if (d <= 0 || E <= 0 || K <= 0 || I <= 0 || Is <= 0 || H <= 0 || r <= 0 || B <= 0) return 0;
+    return (size_t)ws_bytes(B, K, I, Is, r, H, E, d);
+}
+
+extern "C" int edge0_state_init(edge0_route_state* st, cudaStream_t stream) {
+    if (!st || !st->pred_ids || !st->pred_w || !st->exec_ids || !st->workspace) return EDGE0_EINVAL;
+    if (st->L <= 0 || st->B <= 0 || st->K <= 0 || st->H <= 0 || st->r <= 0) return EDGE0_EINVAL;
+    const size_t n = (size_t)2 * st->L * st->B * st->K;
+    if (cudaMemsetAsync(st->pred_ids, 0, n * 4, stream) != cudaSuccess) return EDGE0_ECUDA;
+    if (cudaMemsetAsync(st->pred_w, 0, n * 4, stream) != cudaSuccess) return EDGE0_ECUDA;
+    if (cudaMemsetAsync(st->exec_ids, 0, n * 4, stream) != cudaSuccess) return EDGE0_ECUDA;
+    if (cudaMemsetAsync(st->workspace, 0, st->workspace_bytes, stream) != cudaSuccess)
+        return EDGE0_ECUDA;
+    return EDGE0_OK;
+}
+
+extern "C" int edge0_state_error(const edge0_route_state* st, cudaStream_t stream, int* status) {
+    if (!st || !st->workspace || !status) return EDGE0_EINVAL;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return EDGE0_ECUDA;
+    WsHeader h;
+    if (cudaMemcpy(&h, st->workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return EDGE0_ECUDA;
+    *status = h.error;
+    if (h.error || h.abort) {
+        // clear the error; the barrier counter is re-aligned by the next launch's base
+        // computation only when every CTA left through the same barrier, so reset it too
+        WsHeader z = h;
+        z.error = 0;
+        z.abort = 0;
+        z.barrier = 0;
+        if (cudaMemcpy(st->workspace, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess)
+            return EDGE0_ECUDA;
+    }
+    return EDGE0_OK;
+}
+
+extern "C" int edge0_decode_layer(const edge0_layer_desc* layer, uint16_t* h_inout,
+                                  edge0_route_state* st, int B, int step, cudaStream_t stream) {
+    return decode_common(layer, 1, h_inout, st, B, step, stream);
+}
+
+extern "C" int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
+                                 edge0_route_state* st, int B, int step, cudaStream_t stream) {
+    return decode_common(layers, L, h_inout, st, B, step, stream);
+}
+
+extern "C" int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t* x,
+                                      const int32_t* ids, const float* w, int B, uint16_t* y,
+                                      void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
+    if (!moe || !x || !ids || !w || !y) return EDGE0_EINVAL;
+    if (!moe->gate || !moe->up || !moe->down) return EDGE0_EINVAL;
+    if (!al16(x) || !al16(y)) return EDGE0_EINVAL;
+    Dims D{moe->d, moe->E, moe->K, moe->I, moe->Is > 0 ? moe->Is : 64, 64, 16};
+    int rc = check_dims(D, B);
+    if (rc) return rc;
+    rc = check_ws(D, B, workspace, workspace_bytes);
+    if (rc) return rc;
+    edge0_layer_desc L;
+    memset(&L, 0, sizeof(L));
+    L.moe = *moe;
+    L.moe.Is = D.Is;
+    L.router = moe->gate;     // not used in this mode; satisfies the layer check
+    L.route.kind = EDGE0_ROUTE_SOFTMAX_TOPK;
+    Prog* p = new Prog;
+    memset(p, 0, sizeof(Prog));
+    p->mode = MODE_MOE;
+    p->L = 1;
+    set_dims(*p, D, B);
+    p->step = 0;
+    p->x_in = (const __half*)x;
+    p->ids_in = ids;
+    p->w_in = w;
+    p->y_out = (__half*)y;
+    p->Ls = 1;
+    p->ws = (char*)workspace;
+    rc = fill_layer(L, D, 1, p->layers[0]);
+    if (rc == EDGE0_OK) rc = launch(*p, stream);
+    delete p;
+    return rc;
+}
+
+extern "C" int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t* x,
+                                    const int32_t* exec_ids, const int32_t* prev_ids, int B,
+                                    int32_t* out_ids, float* out_w, float* out_logits,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!head || !x || !exec_ids || !out_ids || !out_w) return EDGE0_EINVAL;
+    if (!al16(x)) return EDGE0_EINVAL;
+    Dims D{head->d, head->E, head->K, 64, 64, head->H, 16};
+    int rc = check_dims(D, B);
+    if (rc) return rc;
+    rc = check_ws(D, B, workspace, workspace_bytes);
+    if (rc) return rc;
+    edge0_layer_desc L;
+    memset(&L, 0, sizeof(L));
+    L.moe.d = D.d;
+    L.moe.E = D.E;
+    L.moe.K = D.K;
+    L.moe.I = D.I;
+    L.moe.Is = D.Is;
+    L.moe.gate = L.moe.up = L.moe.down = head->fc2;   // not used in this mode
+    L.router = head->fc2;
+    L.route.kind = EDGE0_ROUTE_SOFTMAX_TOPK;
+    L.has_head = 1;
+    L.head = *head;
+    L.head_target = 0;
+    Prog* p = new Prog;
+    memset(p, 0, sizeof(Prog));
+    p->mode = MODE_HEAD;
+    p->L = 1;
+    set_dims(*p, D, B);
+    p->step = 0;
+    p->x_in = (const __half*)x;
+    p->exec_in = exec_ids;
+    p->prev_in = prev_ids;
+    p->out_ids = out_ids;
+    p->out_w = out_w;
+    p->out_logits = out_logits;
+    p->Ls = 1;
+    p->ws = (char*)workspace;
+    rc = fill_layer(L, D, 1, p->layers[0]);
+    if (rc == EDGE0_OK) rc = launch(*p, stream);
+    delete p;
+    return rc;
+}

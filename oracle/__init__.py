@@ -86,7 +86,8 @@ class State(C.Structure):
 
 
 class Record(C.Structure):
-    _fields_ = [("x", P), ("ids", P), ("w", P), ("hout", P), ("head_logits", P)]
+    _fields_ = [("x", P), ("ids", P), ("w", P), ("hout", P), ("head_logits", P),
+                ("router_logits", P)]
 
 
 def _declare(L):
@@ -343,8 +344,10 @@ class Stack:
                        ids=torch.zeros(L, B, K, dtype=torch.int32),
                        w=torch.zeros(L, B, K, dtype=torch.float32),
                        hout=torch.zeros(L, B, d, dtype=torch.float16),
-                       head_logits=torch.full((L, B, E), float("nan"), dtype=torch.float32))
-            rec = Record(*[out[k].data_ptr() for k in ("x", "ids", "w", "hout", "head_logits")])
+                       head_logits=torch.full((L, B, E), float("nan"), dtype=torch.float32),
+                       router_logits=torch.full((L, B, E), float("nan"), dtype=torch.float32))
+            rec = Record(*[out[k].data_ptr() for k in ("x", "ids", "w", "hout", "head_logits",
+                                                       "router_logits")])
         if layers is None:
             lib().orc_decode_step(self.layers, C.byref(self.state), _ptr(h), t,
                                   None if rec is None else C.byref(rec))

@@ -323,6 +323,8 @@ void orc_decode_layer(const orc_layer* layers, int l, orc_state* st, uint16_t* h
             orc_f16_matvec(Ly->router, E, d, d, x.data(), lg.data());
             for (int e = 0; e < E; ++e) logits[e] = (float)lg[e];
             orc_apply_route(&Ly->route, logits.data(), E, K, ids, w.data());
+            if (rec && rec->router_logits)
+                std::memcpy(rec->router_logits + ((long)l * B + b) * E, logits.data(), sizeof(float) * E);
         }
 
         routed_one(m, x.data(), ids, w.data(), yr.data());

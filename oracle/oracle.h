@@ -147,9 +147,12 @@ typedef struct {
 
 /* Optional per-layer record of one step (all nullable):
  * x [L][B][d] fp16, ids/w [L][B][K] used by each layer, hout [L][B][d] fp16,
- * head_logits [L][B][E] (rows of layers without a head are left untouched). */
+ * head_logits [L][B][E] (rows of layers without a head are left untouched),
+ * router_logits [L][B][E] (rows of layers that did not run their router are
+ * left untouched). */
 typedef struct {
     uint16_t* x; int32_t* ids; float* w; uint16_t* hout; float* head_logits;
+    float* router_logits;
 } orc_record;
 
 /* run layer l of `layers` at step t on h [B,d] fp16 (in place) */

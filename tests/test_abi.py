@@ -1,0 +1,81 @@
+"""The C-ABI library loads, exports every symbol include/edge0.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from int4_routed_expert_prerouter_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "edge0.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(edge0_[A-Za-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_operations():
+    syms = declared_symbols()
+    for name in ("edge0_prerouter_topk", "edge0_moe_int4_forward", "edge0_lora_delta",
+                 "edge0_decode_layer"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+    assert sorted(binding.EXPORTED) == declared_symbols()
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert binding.status_string(code)
+    assert binding.status_string(0) == "ok"
+
+
+def test_sizes(lib):
+    # packed sizes equal the canonical sizes when rows are a multiple of 16
+    assert lib.edge0_q4_packed_bytes(1, 512, 2048) == 512 * 2048 // 2 + 512 * 32 * 4
+    assert lib.edge0_q4_packed_bytes(256, 512, 2048) * 3 // 256 == 3 * 589824
+    assert lib.edge0_q4_packed_bytes(1, 512, 100) == 0          # in % 64
+    assert lib.edge0_f16_packed_bytes(512, 2048) == 512 * 2048 * 2
+    assert lib.edge0_f16_packed_bytes(4, 128) == 16 * 128 * 2   # rows padded to 16
+    assert binding.workspace_bytes(2048, 256, 4, 512, 512, 512, 16, 1) > 0
+    assert lib.edge0_workspace_bytes(0, 1, 1, 1, 1, 1, 1, 1) == 0
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    E = binding.EDGE0_EINVAL
+    assert lib.edge0_pack_q4(None, None, None, 1, 16, 64, None, None) == E
+    assert lib.edge0_pack_f16(None, 16, 64, 64, None, None) == E
+    assert lib.edge0_pack_cols_T(None, 16, 64, 0, 8, None, None) == E
+    assert lib.edge0_moe_int4_forward(None, None, None, None, 1, None, None, 0, None) == E
+    assert lib.edge0_prerouter_topk(None, None, None, None, 1, None, None, None, None, 0, None) == E
+    assert lib.edge0_lora_delta(None, None, 1, None, None) == E
+    assert lib.edge0_decode_layer(None, None, None, 1, 0, None) == E
+    assert lib.edge0_decode_step(None, 0, None, None, 1, 0, None) == E
+    st = binding.RouteState()
+    assert lib.edge0_state_init(C.byref(st), None) == E
+    # a MoE descriptor with an input width that is not a multiple of the group
+    moe = binding.MoeDesc(100, 16, 2, 128, 128, 16, 16, 16, None, None, None, None, 0)
+    x = C.c_void_p(16)
+    assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 1, x, x, 1 << 20, None) == E
+    # K > E
+    moe = binding.MoeDesc(256, 16, 17, 128, 128, 16, 16, 16, None, None, None, None, 0)
+    assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 1, x, x, 1 << 20, None) == E
+    # batch above the limit
+    moe = binding.MoeDesc(256, 16, 2, 128, 128, 16, 16, 16, None, None, None, None, 0)
+    assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 99, x, x, 1 << 20, None) == E
+    # misaligned input pointer
+    assert lib.edge0_moe_int4_forward(C.byref(moe), C.c_void_p(18), x, x, 1, x, x, 1 << 20, None) == E
+    # workspace too small
+    assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 1, x, x, 64, None) == E

@@ -1,0 +1,424 @@
+"""CUDA path vs the CPU oracle on the same seeded inputs, through the C ABI.
+
+Sizes: small cases the oracle finishes in seconds that still span several row
+tiles and groups plus ragged batches; the 35B single layer and the 40-layer
+35B stack at full size in the launch configuration the bench times (checked on
+the first steps).  Tolerances are in tests/parity_util.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int4_routed_expert_prerouter_gb300 import binding, configs, inputs
+from parity_util import assert_close, routing_matches, selection_scores, weights_by_id
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _cpu_model(model):
+    """Host copy of a model drawn on the device (for the oracle)."""
+    m = inputs.Model(model.cfg, model.seed)
+    for lw in model.layers:
+        c = lambda trip: tuple(t.cpu() for t in trip)
+        m.layers.append(inputs.LayerWeights(c(lw.gate), c(lw.up), c(lw.down), c(lw.sh_gate),
+                                            c(lw.sh_up), c(lw.sh_down), lw.router.cpu(),
+                                            lw.gamma.cpu(), {k: v.cpu() for k, v in lw.lora.items()},
+                                            None if lw.bias is None else lw.bias.cpu(),
+                                            None if lw.head is None else
+                                            {k: (v.cpu() if torch.is_tensor(v) else v)
+                                             for k, v in lw.head.items()},
+                                            lw.prerouted))
+    return m
+
+
+# ------------------------------------------------------------- packing ----
+def _ref_pack_q4(q, s, b):
+    E, out, w8 = q.shape
+    n_rt, ng = (out + 15) // 16, w8 // 8
+    qp = torch.zeros(E, n_rt * 16, w8, dtype=torch.int32)
+    qp[:, :out] = q
+    sp = torch.zeros(E, n_rt * 16, ng, dtype=torch.int16)
+    bp = torch.zeros(E, n_rt * 16, ng, dtype=torch.int16)
+    sp[:, :out] = s.view(torch.int16)
+    bp[:, :out] = b.view(torch.int16)
+    qw = qp.view(E, n_rt, 16, ng, 8)
+    unit = torch.zeros(E, n_rt, ng, 144, dtype=torch.int32)     # 576 bytes
+    for g in range(8):
+        for t in range(4):
+            L = 4 * g + t
+            unit[..., 4 * L + 0] = qw[:, :, g, :, 2 * t]
+            unit[..., 4 * L + 1] = qw[:, :, g, :, 2 * t + 1]
+            unit[..., 4 * L + 2] = qw[:, :, g + 8, :, 2 * t]
+            unit[..., 4 * L + 3] = qw[:, :, g + 8, :, 2 * t + 1]
+    u16 = unit.view(torch.int16).view(E, n_rt, ng, 288)
+    sv = sp.view(E, n_rt, 16, ng).permute(0, 1, 3, 2)
+    bv = bp.view(E, n_rt, 16, ng).permute(0, 1, 3, 2)
+    for g in range(8):
+        u16[..., 256 + 4 * g + 0] = sv[..., g]
+        u16[..., 256 + 4 * g + 1] = bv[..., g]
+        u16[..., 256 + 4 * g + 2] = sv[..., g + 8]
+        u16[..., 256 + 4 * g + 3] = bv[..., g + 8]
+    return unit.view(torch.uint8).reshape(-1)
+
+
+def _ref_pack_f16(W, cols=None):
+    out, ld = W.shape
+    inp = cols or ld
+    n_rt, ng = (out + 15) // 16, inp // 64
+    Wp = torch.zeros(n_rt * 16, inp, dtype=torch.int16)
+    Wp[:out] = W[:, :inp].view(torch.int16)
+    Wv = Wp.view(n_rt, 16, ng, 64)
+    unit = torch.zeros(n_rt, ng, 4, 32, 8, dtype=torch.int16)
+    for m in range(4):
+        for g in range(8):
+            for t in range(4):
+                L = 4 * g + t
+                for j in range(2):
+                    k = 16 * t + (m & 1) + 8 * (m >> 1) + 2 * j
+                    unit[:, :, m, L, 4 * j + 0] = Wv[:, g, :, k]
+                    unit[:, :, m, L, 4 * j + 1] = Wv[:, g, :, k + 4]
+                    unit[:, :, m, L, 4 * j + 2] = Wv[:, g + 8, :, k]
+                    unit[:, :, m, L, 4 * j + 3] = Wv[:, g + 8, :, k + 4]
+    return unit.view(torch.uint8).reshape(-1)
+
+
+@pytest.mark.parametrize("E,out,inp", [(3, 48, 256), (2, 20, 128), (1, 512, 2048)])
+def test_pack_q4_layout(E, out, inp):
+    q, s, b = inputs.int4_stack(5, 1, 1, E, out, inp)
+    got = binding.pack_q4(q.to(DEV), s.to(DEV), b.to(DEV)).cpu()
+    assert torch.equal(got, _ref_pack_q4(q, s, b))
+
+
+@pytest.mark.parametrize("out,inp,cols", [(48, 256, None), (4, 128, None), (64, 288, 256)])
+def test_pack_f16_layout(out, inp, cols):
+    W = (torch.randn(out, inp, generator=torch.Generator().manual_seed(3))).half()
+    got = binding.pack_f16(W.to(DEV), cols=cols).cpu()
+    assert torch.equal(got, _ref_pack_f16(W, cols))
+    T = binding.pack_cols_T(W.to(DEV), 8, 16).cpu()
+    assert torch.equal(T, W[:, 8:24].t().contiguous())
+
+
+# ------------------------------------------------------ standalone ops ----
+def _moe_ws(cfg, B):
+    n = binding.workspace_bytes(cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, 64, 16, B)
+    return torch.zeros(n, dtype=torch.uint8, device=DEV)
+
+
+MOE_CASES = [
+    configs.TOY.with_(B=1),
+    configs.TOY.with_(B=3),
+    configs.STACK35.with_(L=1, E=32, B=1),
+    configs.STACK35.with_(L=1, E=32, B=2),
+    configs.STACK8.with_(L=1, E=32, B=2, zipf=None),
+]
+
+
+@pytest.mark.parametrize("cfg", MOE_CASES, ids=lambda c: f"{c.name}-d{c.d}-E{c.E}-B{c.B}")
+def test_moe_int4_forward(cfg):
+    model = inputs.make_model(cfg.with_(L=1, head_owner_last=-1, prerouted=()), seed=11)
+    lw = model.layers[0]
+    dm = binding.DeviceModel(model, DEV)
+    ws = _moe_ws(cfg, cfg.B)
+    for trial in range(2):
+        x = torch.stack([oracle.rmsnorm(h) for h in inputs.hidden(cfg, trial, seed=11)])
+        ids, w = inputs.routing(cfg, 11, trial)
+        if cfg.B > 1 and trial == 1:
+            ids[1] = ids[0]          # two tokens on the same experts
+        y = binding.moe_int4_forward(dm, 0, x.to(DEV), ids.to(DEV), w.to(DEV), ws)
+        torch.cuda.synchronize()
+        _, y_ref = oracle.moe_forward(cfg, lw, x, ids, w)
+        assert_close(y, y_ref, f"moe y (trial {trial})")
+
+
+@pytest.mark.parametrize("cfg", [configs.TOY.with_(B=2), configs.STACK35.with_(L=2, B=1),
+                                 configs.STACK8.with_(L=2, B=2, head_owner_first=0,
+                                                      head_owner_last=0)],
+                         ids=lambda c: f"{c.name}-B{c.B}")
+@pytest.mark.parametrize("with_prev", [False, True])
+def test_prerouter_topk(cfg, with_prev):
+    cfg = cfg.with_(head_owner_first=0, head_owner_last=0)
+    model = inputs.make_model(cfg, seed=21)
+    dm = binding.DeviceModel(model, DEV)
+    hd = model.layers[0].head
+    tgt_bias = model.layers[hd["target"]].bias
+    n = binding.workspace_bytes(cfg.d, cfg.E, cfg.K, 64, 64, cfg.H, 16, cfg.B)
+    ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    x = torch.stack([oracle.rmsnorm(h) for h in inputs.hidden(cfg, 4, seed=21)])
+    ex, _ = inputs.routing(cfg, 21, 1)
+    pv, _ = inputs.routing(cfg, 21, 2)
+    ids, w, lg = binding.prerouter_topk(dm, 0, x.to(DEV), ex.to(DEV), pv.to(DEV) if with_prev else None, ws)
+    torch.cuda.synchronize()
+    for b in range(cfg.B):
+        ref_lg = oracle.prerouter_logits(hd["fc1"], hd["fc2"], hd["linit"], x[b], ex[b],
+                                         pv[b] if with_prev else None, cfg.d, cfg.E, cfg.H, cfg.K)
+        assert_close(lg[b], ref_lg, f"head logits b={b}")
+        if cfg.route_kind == configs.SIGMOID_GROUP:
+            rid, rw = oracle.route_sigmoid_group(ref_lg, cfg.K, cfg.n_groups, cfg.topk_groups,
+                                                 cfg.route_scale, tgt_bias)
+        else:
+            rid, rw = oracle.route_softmax_topk(ref_lg, cfg.K, tgt_bias)
+        sc = selection_scores(ref_lg.numpy(), cfg.route_kind,
+                              None if tgt_bias is None else tgt_bias.numpy())
+        ok = routing_matches(ids[b].cpu(), rid, sc, cfg.K, cfg.n_groups if cfg.route_kind else None,
+                             cfg.topk_groups if cfg.route_kind else None)
+        if ok is True:
+            assert_close(w[b], rw, f"head weights b={b}")
+
+
+@pytest.mark.parametrize("cfg", [configs.TOY.with_(B=3), configs.STACK35.with_(L=1, E=16, B=2)],
+                         ids=lambda c: c.name)
+def test_lora_delta(cfg):
+    model = inputs.make_model(cfg.with_(L=1, head_owner_last=-1, prerouted=()), seed=31)
+    dm = binding.DeviceModel(model, DEV)
+    lo = model.layers[0].lora
+    g = torch.Generator().manual_seed(31)
+    for name, desc, A, Bm, inp, out in (("gate", dm.layers[0].lora_gate, lo["Ag"], lo["Bg"], cfg.d, cfg.Is),
+                                        ("down", dm.layers[0].lora_down, lo["Ad"], lo["Bd"], cfg.Is, cfg.d)):
+        v = torch.randn(cfg.B, inp, generator=g).half()
+        y0 = (torch.randn(cfg.B, out, generator=g) * 0.1).half()
+        y = y0.to(DEV).contiguous()
+        binding.lora_delta(desc, v.to(DEV).contiguous(), y)
+        torch.cuda.synchronize()
+        for b in range(cfg.B):
+            delta = oracle.lora_delta(A, Bm, cfg.alpha, v[b].double())
+            ref = y0[b].double() + delta
+            # fp16 output: one rounding of y0 + delta on top of the 2e-3 contract
+            err = (y[b].cpu().double() - ref).abs().max().item()
+            tol = 2e-3 * delta.abs().max().item() + 2.0**-11 * ref.abs().max().item()
+            assert err <= tol, f"lora {name} b={b}: {err:.3e} > {tol:.3e}"
+
+
+# ------------------------------------------------------------ decode ----
+def _run_stack(cfg, model, steps, use_layers=False, check_every_layer_state=True):
+    """Decode `steps` steps on GPU and in the oracle; returns the number of steps
+    compared before an allowed near-tie made the two paths diverge."""
+    dm = binding.DeviceModel(model, DEV)
+    st = binding.DecodeState(cfg, device=DEV)
+    ref = oracle.Stack(_cpu_model(model) if model.layers[0].gate[0].is_cuda else model)
+    recs = []
+    for t in range(steps):
+        h0 = inputs.hidden(cfg, t, seed=model.seed)
+        h = h0.to(DEV).contiguous()
+        if use_layers:
+            for l in range(cfg.L):
+                binding.decode_layer(dm, l, st, h, t)
+        else:
+            binding.decode_step(dm, st, h, t)
+        torch.cuda.synchronize()
+        assert st.error() == 0
+        h_ref = h0.clone()
+        rec = ref.step(h_ref, t)
+        recs.append(rec)
+        exec_gpu = st.exec_ids[t & 1].cpu()
+        pred_gpu = st.pred_ids[t & 1].cpu()
+        predw_gpu = st.pred_w[t & 1].cpu()
+        h_err = ((h.cpu().double() - h_ref.double()).abs().max() / h_ref.double().abs().max()).item()
+        tie = False
+        for l in range(cfg.L):
+            lw = model.layers[l]
+            bias = None if lw.bias is None else lw.bias.cpu().numpy()
+            for b in range(cfg.B):
+                if lw.prerouted and t > 0:
+                    lg = recs[t - 1]["head_logits"][l - 1 if not cfg.ring else l, b].numpy()
+                else:
+                    lg = rec["router_logits"][l, b].numpy()
+                sc = selection_scores(lg, cfg.route_kind, bias)
+                try:
+                    r = routing_matches(exec_gpu[l, b], rec["ids"][l, b], sc, cfg.K,
+                                        cfg.n_groups if cfg.route_kind else None,
+                                        cfg.topk_groups if cfg.route_kind else None, ordered=False)
+                except AssertionError as e:
+                    raise AssertionError(f"step {t} layer {l} b {b} executed ids: {e}; "
+                                         f"h rel err after the step {h_err:.2e}") from None
+                tie |= r == "tie"
+            if lw.head is not None and not tie:
+                tg = lw.head["target"]
+                tb = model.layers[tg].bias
+                for b in range(cfg.B):
+                    sc = selection_scores(rec["head_logits"][l, b].numpy(), cfg.route_kind,
+                                          None if tb is None else tb.cpu().numpy())
+                    try:
+                        r = routing_matches(pred_gpu[tg, b], ref.pred_ids[t & 1, tg, b], sc, cfg.K,
+                                            cfg.n_groups if cfg.route_kind else None,
+                                            cfg.topk_groups if cfg.route_kind else None, ordered=False)
+                    except AssertionError as e:
+                        raise AssertionError(f"step {t} head of layer {l} b {b}: {e}; "
+                                             f"h rel err after the step {h_err:.2e}") from None
+                    if r is True:
+                        gw, rw = weights_by_id(pred_gpu[tg, b], predw_gpu[tg, b],
+                                               ref.pred_ids[t & 1, tg, b], ref.pred_w[t & 1, tg, b])
+                        assert_close(gw, rw, f"pred w t={t} l={l}")
+                    tie |= r == "tie"
+            if tie:
+                break
+        print(f"step {t}: h rel err {h_err:.2e}{' (near-tie divergence)' if tie else ''}")
+        if tie:
+            return t
+        assert_close(h.cpu(), h_ref, f"h after step {t}")
+    return steps
+
+
+def test_decode_toy_stack_8_steps():
+    cfg = configs.TOY
+    model = inputs.make_model(cfg, seed=0)
+    assert _run_stack(cfg, model, cfg.steps) >= 6
+
+
+def test_decode_toy_layer_by_layer_matches():
+    cfg = configs.TOY
+    model = inputs.make_model(cfg, seed=1, gamma="random")
+    assert _run_stack(cfg, model, 4, use_layers=True) >= 3
+
+
+def test_decode_toy_ragged_batch():
+    cfg = configs.TOY.with_(B=3)
+    model = inputs.make_model(cfg, seed=2)
+    assert _run_stack(cfg, model, 5) >= 3
+
+
+def test_decode_8b_shapes_small():
+    cfg = configs.STACK8.with_(L=3, E=32, B=2, head_owner_first=0, head_owner_last=1,
+                               prerouted=(1, 2))
+    model = inputs.make_model(cfg, seed=3)
+    assert _run_stack(cfg, model, 4) >= 2
+
+
+def test_decode_35b_layer_ring_full_size():
+    cfg = configs.LAYER35
+    model = inputs.make_model(cfg, seed=0, device=DEV)
+    assert _run_stack(cfg, model, 6) >= 4
+
+
+def test_decode_35b_stack_first_8_layers_full_size():
+    # the timed launch configuration (one persistent launch over consecutive
+    # layers: own-routed 0-6, head owners from 6, prerouted from 7) at full size
+    cfg = configs.STACK35.with_(L=8, head_owner_last=6, prerouted=(7,))
+    model = inputs.make_model(cfg, seed=0, device=DEV)
+    assert _run_stack(cfg, model, 3) >= 2
+
+
+def test_decode_35b_stack_40_layers_full_size_properties():
+    # 40 chained layers drift apart from the oracle by the compounding of
+    # independent fp16 rounding flips (the per-layer contract is checked by the
+    # teacher-forced test below); what holds at any depth is checked here
+    cfg = configs.STACK35
+    model = inputs.make_model(cfg, seed=0, device=DEV)
+    dm = binding.DeviceModel(model, DEV)
+    st = binding.DecodeState(cfg, device=DEV)
+    ref = oracle.Stack(_cpu_model(model))
+    for t in range(3):
+        h0 = inputs.hidden(cfg, t)
+        h = h0.to(DEV).contiguous()
+        binding.decode_step(dm, st, h, t)
+        torch.cuda.synchronize()
+        assert st.error() == 0
+        h_ref = h0.clone()
+        rec = ref.step(h_ref, t)
+        ex = st.exec_ids[t & 1].cpu()
+        for l in range(cfg.L):
+            ids = ex[l, 0].tolist()
+            assert len(set(ids)) == cfg.K and all(0 <= e < cfg.E for e in ids)
+        pr = st.pred_ids[t & 1].cpu()
+        pw = st.pred_w[t & 1].cpu()
+        for l in cfg.head_owners():
+            tg = l + 1
+            assert len(set(pr[tg, 0].tolist())) == cfg.K
+            assert abs(float(pw[tg, 0].sum()) - 1.0) < 1e-5        # renormalised softmax
+        if t > 0:                                                    # consumed as the routing
+            prev_pred = st_prev
+            for l in cfg.prerouted:
+                assert sorted(ex[l, 0].tolist()) == sorted(prev_pred[l, 0].tolist())
+        st_prev = pr.clone()
+        # layer 0 runs on identical inputs: its routing matches the oracle's exactly
+        sc = selection_scores(rec["router_logits"][0, 0].numpy(), cfg.route_kind)
+        assert routing_matches(ex[0, 0], rec["ids"][0, 0], sc, cfg.K, ordered=False)
+        rel = ((h.cpu().double() - h_ref.double()).abs().max() / h_ref.double().abs().max()).item()
+        print(f"step {t}: 40-layer h rel diff {rel:.2e} (free-running, not a parity bound)")
+        assert torch.isfinite(h.float()).all()
+
+
+# ------------------------------------------------- teacher-forced layers ----
+def _teacher_forced(cfg, model, steps, layers=None, verbose=True):
+    """Every layer call on the GPU gets the oracle's h and routing state as input
+    (oracle -> GPU only); each layer's outputs are compared with the oracle's.
+    Returns (compared layer calls, fp16 elements that differ per call)."""
+    dm = binding.DeviceModel(model, DEV)
+    st = binding.DecodeState(cfg, device=DEV)
+    ref = oracle.Stack(_cpu_model(model) if model.layers[0].gate[0].is_cuda else model)
+    layers = list(range(cfg.L)) if layers is None else layers
+    calls, flips, worst = 0, 0, 0.0
+    head_logits_prev = None
+    for t in range(steps):
+        h_ref = inputs.hidden(cfg, t, seed=model.seed)
+        rec_t = {}
+        for l in range(cfg.L):
+            st.pred_ids.copy_(ref.pred_ids)
+            st.pred_w.copy_(ref.pred_w)
+            st.exec_ids.copy_(ref.exec_ids)
+            h_in = h_ref.clone()
+            h = h_in.to(DEV).contiguous()
+            if l in layers:
+                binding.decode_layer(dm, l, st, h, t)
+            rec = ref.step(h_ref, t, layers=[l])
+            rec_t[l] = rec
+            if l not in layers:
+                continue
+            torch.cuda.synchronize()
+            assert st.error() == 0
+            lw = model.layers[l]
+            bias = None if lw.bias is None else lw.bias.cpu().numpy()
+            for b in range(cfg.B):
+                if lw.prerouted and t > 0:
+                    lg = head_logits_prev[l - 1 if not cfg.ring else l][b].numpy()
+                else:
+                    lg = rec["router_logits"][l, b].numpy()
+                r = routing_matches(st.exec_ids[t & 1, l, b].cpu(), rec["ids"][l, b],
+                                    selection_scores(lg, cfg.route_kind, bias), cfg.K,
+                                    cfg.n_groups if cfg.route_kind else None,
+                                    cfg.topk_groups if cfg.route_kind else None, ordered=False)
+                if r == "tie":
+                    continue
+            rel = assert_close(h.cpu(), h_ref, f"h after step {t} layer {l}")
+            worst = max(worst, rel)
+            flips += int((h.cpu() != h_ref).sum())
+            calls += 1
+            if lw.head is not None:
+                tg = lw.head["target"]
+                tb = model.layers[tg].bias
+                for b in range(cfg.B):
+                    sc = selection_scores(rec["head_logits"][l, b].numpy(), cfg.route_kind,
+                                          None if tb is None else tb.cpu().numpy())
+                    gi, gw = st.pred_ids[t & 1, tg, b].cpu(), st.pred_w[t & 1, tg, b].cpu()
+                    ri, rw = ref.pred_ids[t & 1, tg, b], ref.pred_w[t & 1, tg, b]
+                    r = routing_matches(gi, ri, sc, cfg.K, cfg.n_groups if cfg.route_kind else None,
+                                        cfg.topk_groups if cfg.route_kind else None, ordered=False)
+                    if r is True:
+                        gw2, rw2 = weights_by_id(gi, gw, ri, rw)
+                        assert_close(gw2, rw2, f"pred w t={t} l={l}")
+        head_logits_prev = {l: rec_t[l]["head_logits"][l] for l in rec_t}
+    if verbose:
+        print(f"{cfg.name}: {calls} layer calls, worst rel err {worst:.2e}, "
+              f"{flips / max(calls, 1):.2f} fp16 elements differ per call (of {cfg.B * cfg.d})")
+    return calls, flips / max(calls, 1)
+
+
+def test_teacher_forced_35b_stack_full_size():
+    cfg = configs.STACK35
+    model = inputs.make_model(cfg, seed=0, device=DEV)
+    calls, _ = _teacher_forced(cfg, model, steps=3)
+    assert calls >= 100
+
+
+def test_teacher_forced_toy_8_steps():
+    cfg = configs.TOY
+    model = inputs.make_model(cfg, seed=5, gamma="random")
+    calls, _ = _teacher_forced(cfg, model, steps=cfg.steps)
+    assert calls >= 14

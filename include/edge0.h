@@ -216,6 +216,27 @@ int edge0_decode_layer(const edge0_layer_desc* layer, uint16_t* h_inout, edge0_r
 int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
                       edge0_route_state* st, int B, int step, cudaStream_t stream);
 
+/* ---- allocation-free variant (the paper has no counterpart to this call) ----
+ * edge0_moe_int4_forward for callers that cannot allocate memory: code running
+ * in an allocator-free part of a serving loop, code whose memory budget was fixed
+ * at start-up, or hosts that pass this library only buffers they already own.
+ * Same arguments and result as edge0_moe_int4_forward minus the workspace: the
+ * kernel's scratch is a fixed array of EDGE0_NOALLOC_SCRATCH_BYTES bytes inside
+ * the library, present in every GPU that loads it until the process exits.  The
+ * call allocates nothing (no cudaMalloc, no host heap); it clears the part of
+ * the array it uses before launching.
+ *   - Shapes whose scratch would exceed the array return EDGE0_EUNSUPPORTED
+ *     (at d=2048, E=256, K=4, I=Is=512 the need is about 420 KB at B=4).
+ *   - The first call on a device looks up the array's device address for that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - All calls share the array: two calls whose kernels overlap on the GPU (for
+ *     instance on different streams) race and give wrong results. */
+#define EDGE0_NOALLOC_SCRATCH_BYTES (1 << 20)
+int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const uint16_t* x,
+                                   const int32_t* ids, const float* w, int B, uint16_t* y,
+                                   cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

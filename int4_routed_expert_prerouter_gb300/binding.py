@@ -91,6 +91,7 @@ def _declare(L):
     L.edge0_prerouter_topk.argtypes = [C.POINTER(HeadDesc), P, P, P, C.c_int, P, P, P, P,
                                        C.c_size_t, P]
     L.edge0_moe_int4_forward.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P, C.c_size_t, P]
+    L.edge0_moe_int4_forward_noalloc.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P]
     L.edge0_lora_delta.argtypes = [C.POINTER(LoraDesc), P, C.c_int, P, P]
     L.edge0_decode_layer.argtypes = [C.POINTER(LayerDesc), P, C.POINTER(RouteState), C.c_int,
                                      C.c_int, P]
@@ -98,14 +99,16 @@ def _declare(L):
                                     C.c_int, C.c_int, P]
     for name in ("edge0_pack_q4", "edge0_pack_f16", "edge0_pack_cols_T", "edge0_state_init",
                  "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
-                 "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step"):
+                 "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
+                 "edge0_moe_int4_forward_noalloc"):
         getattr(L, name).restype = C.c_int
 
 
 EXPORTED = ["edge0_status_string", "edge0_q4_packed_bytes", "edge0_pack_q4", "edge0_f16_packed_bytes",
             "edge0_pack_f16", "edge0_pack_cols_T", "edge0_workspace_bytes", "edge0_state_init",
             "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
-            "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step"]
+            "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
+            "edge0_moe_int4_forward_noalloc"]
 
 
 def status_string(code: int) -> str:

@@ -1,0 +1,144 @@
+// edge0_moe_int4_forward_noalloc: the routed + shared int4 expert forward for
+// callers that cannot allocate memory.
+//
+// Some callers must not call cudaMalloc (or anything else that allocates) at the
+// point where they run the MoE block: code inside an allocator-free region of a
+// serving loop, code whose memory budget was fixed when the process started, or
+// a host that hands this library only the input and output buffers it already
+// owns.  For them this entry point keeps the kernel's scratch (its accumulators,
+// grid-barrier word and error word) in a fixed array compiled into the library,
+// builds the kernel's parameter block on the stack, and needs nothing from the
+// caller beyond its inputs and outputs.
+//
+// The array is allocated in each GPU's memory when the library is loaded there
+// and stays until the process exits.  Every call on a device uses the same array;
+// two calls whose kernels overlap on the GPU (for instance on two streams) race on
+// it and produce wrong results.
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+
+using namespace edge0;
+
+namespace {
+
+// fixed scratch of the allocation-free entry point
+static __device__ __align__(256) unsigned char g_noalloc_scratch[EDGE0_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a stand-in, so the address is looked up once per device
+// (with that device current) and kept.
+int scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EDGE0_ECUDA;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return EDGE0_ECUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return EDGE0_OK;
+}
+
+bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+}  // namespace
+
+extern "C" int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const uint16_t* x,
+                                              const int32_t* ids, const float* w, int B,
+                                              uint16_t* y, cudaStream_t stream) {
+    // the same argument rules as edge0_moe_int4_forward
+    if (!moe || !x || !ids || !w || !y) return EDGE0_EINVAL;
+    const edge0_moe_desc& m = *moe;
+    if (!m.gate || !m.up || !m.down || !a16(m.gate) || !a16(m.up) || !a16(m.down)) return EDGE0_EINVAL;
+    if (!a16(x) || !a16(y)) return EDGE0_EINVAL;
+    const bool shared = m.sh_gate || m.sh_up || m.sh_down;
+    if (shared && (!m.sh_gate || !m.sh_up || !m.sh_down || !a16(m.sh_gate) || !a16(m.sh_up) ||
+                   !a16(m.sh_down)))
+        return EDGE0_EINVAL;
+    const int Is = m.Is > 0 ? m.Is : 64;
+    if (B <= 0 || B > EDGE0_MAX_BATCH) return EDGE0_EINVAL;
+    if (m.d <= 0 || m.d % kGroup || m.I <= 0 || m.I % kGroup || Is % kGroup) return EDGE0_EINVAL;
+    if (m.E <= 0 || m.E > EDGE0_MAX_E || m.E % 8 || m.K <= 0 || m.K > EDGE0_MAX_K || m.K > m.E)
+        return EDGE0_EINVAL;
+    if (m.slot_table && m.n_slots <= 0) return EDGE0_EINVAL;
+    if (2 * B * m.K + 8 > kMaxSeg) return EDGE0_EUNSUPPORTED;
+    // scratch: header, three accumulator sets and the residual buffers (the trace
+    // area at the end of a workspace is never switched on here)
+    const long long need = ws_bytes(B, m.K, m.I, Is, 16, 64, m.E, m.d) -
+                           (long long)kTraceCtas * kTraceSlots * 8;
+    if (need > (long long)EDGE0_NOALLOC_SCRATCH_BYTES) return EDGE0_EUNSUPPORTED;
+    void* scratch = nullptr;
+    int rc = scratch_address(&scratch);
+    if (rc) return rc;
+    // every call starts from a cleared header and cleared accumulators: the
+    // previous call may have used other shapes
+    if (cudaMemsetAsync(scratch, 0, (size_t)need, stream) != cudaSuccess) return EDGE0_ECUDA;
+
+    Prog p;   // kernel parameter block, on the stack
+    memset(&p, 0, sizeof(p));
+    p.mode = MODE_MOE;
+    p.L = 1;
+    p.B = B;
+    p.d = m.d;
+    p.E = m.E;
+    p.K = m.K;
+    p.I = m.I;
+    p.Is = Is;
+    p.H = 64;
+    p.r = 16;
+    p.step = 0;
+    p.x_in = (const __half*)x;
+    p.ids_in = ids;
+    p.w_in = w;
+    p.y_out = (__half*)y;
+    p.Ls = 1;
+    p.ws = (char*)scratch;
+    LayerP& P = p.layers[0];
+    P.gate = (const char*)m.gate;
+    P.up = (const char*)m.up;
+    P.down = (const char*)m.down;
+    P.slot_table = m.slot_table;
+    P.n_slots = m.slot_table ? m.n_slots : m.E;
+    if (shared) {
+        P.sh_gate = (const char*)m.sh_gate;
+        P.sh_up = (const char*)m.sh_up;
+        P.sh_down = (const char*)m.sh_down;
+        P.flags = LF_SHARED;
+    }
+    P.n_groups = P.topk_groups = P.head_n_groups = P.head_topk_groups = 1;
+
+    int dev = 0, nsm = 0, maxsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EDGE0_ECUDA;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return EDGE0_ECUDA;
+    if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return EDGE0_ECUDA;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, engine_kernel) != cudaSuccess) return EDGE0_ECUDA;
+    const int smem = engine_smem_bytes(p);
+    if (smem + (int)fa.sharedSizeBytes > maxsm) return EDGE0_EUNSUPPORTED;
+    if (cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return EDGE0_ECUDA;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(nsm);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, engine_kernel, p) != cudaSuccess) return EDGE0_ECUDA;
+    return EDGE0_OK;
+}

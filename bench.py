@@ -192,6 +192,22 @@ def run_gpu(args, rank, world):
         t += 1
         st.set_trace(False)
         print_trace(st.read_trace(), torch.cuda.get_device_properties(dev).multi_processor_count)
+    if args.trace_detail is not None:
+        st.set_trace(True, args.trace_detail)
+        binding.decode_step(dm, st, h_all[t], t)
+        t += 1
+        st.set_trace(False)
+        tr = st.read_trace()
+        for cta in (0, 40, 75, 151):
+            t0 = None
+            evs = []
+            for tag, tm in tr[cta].tolist():
+                if tm == 0:
+                    break
+                if t0 is None:
+                    t0 = tm
+                evs.append(f"{tag:#07x}@{(tm - t0) / 1e3:.2f}")
+            sys.stderr.write(f"cta {cta}: " + " ".join(evs) + "\n")
 
     # device-resident timed region: one event pair per launch for the kernel
     # duration, one pair around the region for the step time
@@ -300,22 +316,22 @@ def print_trace(tr, nct):
             ev[tag] = tm
         keys = sorted({k >> 4 for k in ev})
         for k in keys:
-            pts = [ev.get((k << 4) | i) for i in range(4)]
+            pts = [ev.get((k << 4) | i) for i in range(5)]
             if None in pts:
                 continue
-            acc[k].append((pts[1] - pts[0], pts[2] - pts[1], pts[3] - pts[2], pts[3]))
-    tot = [0.0, 0.0, 0.0]
+            acc[k].append(tuple(pts[i + 1] - pts[i] for i in range(4)))
+    names = ("prologue", "chunks", "flush", "barrier")
+    tot = [0.0] * 4
     lines = []
-    first = min(v[0][3] - sum(v[0][:3]) for v in acc.values()) if acc else 0
     for k in sorted(acc):
         v = acc[k]
-        m = [statistics.mean(x[i] for x in v) / 1e3 for i in range(3)]
-        mx = [max(x[i] for x in v) / 1e3 for i in range(3)]
+        m = [statistics.mean(x[i] for x in v) / 1e3 for i in range(4)]
+        mx = [max(x[i] for x in v) / 1e3 for i in range(4)]
         tot = [a + b for a, b in zip(tot, m)]
-        lines.append(f"layer {k >> 4:2d} phase {'RAB'[k & 15]}: prologue {m[0]:6.2f} chunks {m[1]:6.2f} "
-                     f"(max {mx[1]:6.2f}) barrier {m[2]:6.2f} us")
+        lines.append(f"layer {k >> 4:2d} phase {'RAB'[k & 15]}: " +
+                     " ".join(f"{n} {a:6.2f}/{b:6.2f}" for n, a, b in zip(names, m, mx)) + " us (mean/max)")
     sys.stderr.write("\n".join(lines) + "\n")
-    sys.stderr.write(f"total (mean over CTAs): prologue {tot[0]:.1f} chunks {tot[1]:.1f} barrier {tot[2]:.1f} us\n")
+    sys.stderr.write("total (mean over CTAs): " + " ".join(f"{n} {a:.1f}" for n, a in zip(names, tot)) + " us\n")
 
 
 def _host_layers(model, n):
@@ -411,6 +427,8 @@ def main():
     ap.add_argument("--experts", type=int, default=0, help="reduced case for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", action="store_true", help="print a per-phase split of one step")
+    ap.add_argument("--trace-detail", type=int, default=None,
+                    help="print per-chunk stamps of layers N, N+1 for a few CTAs")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

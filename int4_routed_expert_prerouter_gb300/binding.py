@@ -248,10 +248,12 @@ class DecodeState:
 
     TRACE_CTAS, TRACE_SLOTS = 160, 1024
 
-    def set_trace(self, on: bool):
-        """Switch the engine's phase trace on/off (workspace header flag)."""
+    def set_trace(self, on, detail_layer=None):
+        """Switch the engine's phase trace on/off (workspace header flag); with
+        detail_layer, also per-chunk stamps for layers detail_layer, detail_layer + 1."""
         torch.cuda.synchronize(self.workspace.device)
-        flag = torch.tensor([1 if on else 0], dtype=torch.int32)
+        mode = 0 if not on else (1 if detail_layer is None else detail_layer + 2)
+        flag = torch.tensor([mode], dtype=torch.int32)
         self.workspace[24:28].copy_(flag.view(torch.uint8))
         if on:
             self.workspace[-self.TRACE_CTAS * self.TRACE_SLOTS * 8:].zero_()

@@ -8,14 +8,17 @@
 //      down), head fc2 gelu(z) (+ linear_init and the one-hot columns)
 // Every phase's work is a list of "segments" (one packed matrix, or one expert's
 // matrix) cut into 576-byte int4 / 2048-byte fp16 units; each CTA takes a
-// contiguous byte range of the phase.  The producer warp streams the CTA's units
-// (and small auxiliary tensors) into a ring of shared-memory stages with bulk
-// copies as soon as the routing that selects them is known -- for prerouted
-// layers that is at step start, so weight traffic runs ahead across grid
-// barriers.  Consumer warps read each unit once from shared memory and do the
-// dot products on the tensor cores (m16n8k16, fp32 accumulate) with the int4
-// nibbles turned into fp16 subnormals by a single mask (q * 2^-24), then reduce
-// partial sums through shared memory into fp32 accumulators in global memory.
+// contiguous byte range of the phase.  The producer warp builds each phase's
+// segment and chunk list once, publishes it to the consumers through a ring of
+// list slots, and streams the CTA's units (and small auxiliary tensors) into a
+// ring of shared-memory stages with bulk copies as soon as the routing that
+// selects them is known -- for prerouted layers that is at step start, so
+// weight traffic runs ahead across grid barriers.  Consumer warps read each unit
+// once from shared memory and do the dot products on the tensor cores
+// (m16n8k16, fp32 accumulate) with the int4 nibbles turned into fp16 subnormals
+// by a single mask (q * 2^-24); each warp adds its partial sums into a per-phase
+// shared-memory accumulator without CTA-wide synchronisation, and the CTA flushes
+// it to fp32 accumulators in global memory once per phase.
 #include "internal.cuh"
 
 namespace edge0 {
@@ -30,23 +33,37 @@ enum AuxKind : int { AUX_UNITS = 0, AUX_BG, AUX_BU, AUX_AD, AUX_BD, AUX_FC1OH, A
 
 struct Seg {
     const char* base;
-    long long off;     // byte offset of the segment in the phase
+    int off;           // byte offset of the segment in the phase
     int kind;          // 0 int4, 1 fp16
     int n_rt, n_g, rows, ub;
     int src, out, expert, extra;
+    int cu0, cu1;      // this CTA's units of the segment
 };
 
 struct Chunk {
     int aux, seg, u0, u1, tok, bytes;
+    int sacc;          // unit chunks: first accumulator row of the chunk
 };
 
-constexpr int kMaxChunk = 64;
+constexpr int kMaxChunk = 48;
+constexpr int kListSlots = 4;
+constexpr int kSaccRowsPhase = 1024;   // accumulator rows of one CTA in one phase
+constexpr int kBdBytes = 8192;         // LoRA-down B rows of one CTA in one phase
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // bounded waits: 2 s
+
+// one phase's work of this CTA, built by the producer and read by the consumers
+struct PhaseList {
+    int seq;           // phase index + 1 once published
+    int nseg, nch, sacc_rows;
+    int has_sh, has_head, bd_row0, bd_rows;
+    Seg seg[kMaxSeg];
+    Chunk ch[kMaxChunk];
+};
 
 // ------------------------------------------------------------ smem plan ----
 struct Plan {
     int stage, full, empty, xf, xsum, actf, actsum, ashf, ashsum, gf, gsum, ash32, gsh, ush, aacc,
-        v, zsm, linsm, lx, hs, rscr, sacc, segc, segp, chc, chp, ids, wts, ready, red, ctl, total;
+        v, zsm, linsm, lx, hs, rscr, sacc, bd, lists, ids, wts, ready, red, ctl, total;
 };
 
 __host__ __device__ inline int al(int x, int a) { return (x + a - 1) / a * a; }
@@ -79,11 +96,9 @@ __host__ __device__ inline Plan make_plan(int L, int B, int K, int d, int E, int
     p.lx = o;     o += al(B * E * 4, 16);
     p.hs = o;     o += al(B * d * 2, 16);
     p.rscr = o;   o += al(B * 2 * E * 4, 16);
-    p.sacc = o;   o += al(2 * kSaccRows * B * 4, 16);
-    p.segc = o;   o += al(kMaxSeg * (int)sizeof(Seg), 16);
-    p.segp = o;   o += al(kMaxSeg * (int)sizeof(Seg), 16);
-    p.chc = o;    o += al(kMaxChunk * (int)sizeof(Chunk), 16);
-    p.chp = o;    o += al(kMaxChunk * (int)sizeof(Chunk), 16);
+    p.sacc = o;   o += al(kSaccRowsPhase * B * 4, 16);
+    p.bd = o;     o += kBdBytes;
+    p.lists = o;  o += al(kListSlots * (int)sizeof(PhaseList), 16);
     p.ids = o;    o += al(L * B * K * 4, 16);
     p.wts = o;    o += al(L * B * K * 4, 16);
     p.ready = o;  o += al(L * 4, 16);
@@ -108,8 +123,7 @@ struct Ctl {
     int step;
     unsigned pc0;
     int issued;       // chunks issued by the producer
-    int consumed;     // chunks consumed
-    int start;        // producer may start
+    int cdone;        // phases the consumers have finished
 };
 
 __device__ void raise_error(WsHeader* hdr, Ctl* ctl, int code) {
@@ -136,6 +150,23 @@ __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHeader* hdr, Ctl* ct
             }
         }
     }
+}
+
+// spin until *flag >= want (shared memory, written by the other role); bounded
+__device__ bool wait_flag(volatile int* flag, int want, WsHeader* hdr, Ctl* ctl) {
+    if (*flag >= want) return true;
+    const unsigned long long t0 = now_ns();
+    for (unsigned it = 0; *flag < want; ++it) {
+        __nanosleep(32);
+        if ((it & 63) == 63) {
+            if (should_abort(hdr, ctl)) return false;
+            if (now_ns() - t0 > kTimeoutNs) {
+                raise_error(hdr, ctl, EDGE0_ETIMEOUT);
+                return false;
+            }
+        }
+    }
+    return true;
 }
 
 // ---------------------------------------------------------- routing -----
@@ -186,13 +217,11 @@ __device__ void warp_route(const float* logits, int E, int K, int kind, int n_gr
         float gscore = -INFINITY;
         if (lane < n_groups) {
             float a = -INFINITY, b = -INFINITY;
-            int ai = -1;
             for (int j = 0; j < per; ++j) {
                 const float v = sel[lane * per + j];
-                if (v > a) { b = a; a = v; ai = j; }
+                if (v > a) { b = a; a = v; }
                 else if (v > b) { b = v; }
             }
-            (void)ai;
             gscore = a + b;
         }
         // keep the best G groups (lower group index on ties)
@@ -265,6 +294,7 @@ __device__ __forceinline__ unsigned long long* trace_area(const Ctx& c) {
 // record (tag, globaltimer) when tracing is on; consumer thread 0 only
 __device__ __forceinline__ void stamp(const Ctx& c, int tag) {
     if (threadIdx.x != 0 || !c.ctl->trace) return;
+    if (c.ctl->trace >= 2 && (tag & 0xF0000) == 0 && (tag & 0xF) > 4) return;
     const int s = c.ctl->tslot;
     if (s + 2 > kTraceSlots) return;
     unsigned long long* a = trace_area(c);
@@ -273,11 +303,20 @@ __device__ __forceinline__ void stamp(const Ctx& c, int tag) {
     c.ctl->tslot = s + 2;
 }
 
+// detailed stamps for one two-layer window (trace mode >= 2: window starts at layer mode - 2)
+__device__ __forceinline__ void dstamp(const Ctx& c, int l, int tag) {
+    const int m = c.ctl->trace;
+    if (m >= 2 && l >= m - 2 && l <= m - 1) stamp(c, tag);
+}
+
 __device__ __forceinline__ int* sm_ids(const Ctx& c, int l) {
     return reinterpret_cast<int*>(c.sm + c.pl.ids) + l * c.p->B * c.p->K;
 }
 __device__ __forceinline__ float* sm_w(const Ctx& c, int l) {
     return reinterpret_cast<float*>(c.sm + c.pl.wts) + l * c.p->B * c.p->K;
+}
+__device__ __forceinline__ PhaseList* list_slot(const Ctx& c, int pi) {
+    return reinterpret_cast<PhaseList*>(c.sm + c.pl.lists) + (pi % kListSlots);
 }
 
 __device__ __forceinline__ bool has_router_phase(const Prog& p, int l, int step) {
@@ -288,15 +327,19 @@ __device__ __forceinline__ int expert_slot(const LayerP& Ly, int e) {
     return Ly.slot_table ? Ly.slot_table[e] : e;
 }
 
-// Build the segment list of phase `ph` of layer l (deterministic; used by both
-// the producer and the consumers).  Returns the count; *total = phase bytes.
-__device__ int build_segments(const Ctx& c, int l, int ph, const int* ids, Seg* S,
-                              long long* total) {
+__device__ __forceinline__ int units_of(int kind, int bytes) {   // ceil(bytes / unit)
+    return kind ? (bytes + kF16Unit - 1) >> 11 : (bytes + kQ4Unit - 1) / kQ4Unit;
+}
+
+// Build the segment list of phase `ph` of layer l into L->seg (deterministic).
+// Returns the phase's byte total, or -1 for an expert id or slot out of range.
+__device__ int build_segments(const Ctx& c, int l, int ph, const int* ids, PhaseList* Lp) {
     const Prog& p = *c.p;
     const LayerP& Ly = p.layers[l];
     const int B = p.B, K = p.K, d = p.d, E = p.E, I = p.I, Is = p.Is, H = p.H, r = p.r;
     int n = 0;
-    long long off = 0;
+    int off = 0;
+    Seg* S = Lp->seg;
     auto add = [&](const char* base, int kind, int rows, int in, int src, int out, int expert,
                    int extra) {
         if (n >= kMaxSeg) return;
@@ -312,7 +355,7 @@ __device__ int build_segments(const Ctx& c, int l, int ph, const int* ids, Seg* 
         s.expert = expert;
         s.extra = extra;
         s.off = off;
-        off += (long long)s.n_rt * s.n_g * s.ub;
+        off += s.n_rt * s.n_g * s.ub;
     };
     const bool moe_phase = p.mode != MODE_HEAD;
     const bool head = (p.mode == MODE_HEAD) || (p.mode == MODE_DECODE && (Ly.flags & LF_HEAD));
@@ -358,74 +401,77 @@ __device__ int build_segments(const Ctx& c, int l, int ph, const int* ids, Seg* 
             if (head) add(Ly.fc2, 1, E, H, SRC_GELU, OUT_LOGH, -1, EX_HEAD);
         }
     }
-    *total = off;
-    return n;
+    Lp->nseg = n;
+    return off;
 }
 
-// CTA byte range of a phase
-__device__ __forceinline__ void cta_range(long long total, int cta, int nct, long long* lo,
-                                          long long* hi) {
-    *lo = total * cta / nct;
-    *hi = total * (cta + 1) / nct;
-}
-// units of segment s whose start offset lies in [lo, hi)
-__device__ __forceinline__ void seg_units(const Seg& s, long long lo, long long hi, int* u0, int* u1) {
-    const long long n = (long long)s.n_rt * s.n_g;
-    long long a = lo - s.off, b = hi - s.off;
-    a = a <= 0 ? 0 : (a + s.ub - 1) / s.ub;
-    b = b <= 0 ? 0 : (b + s.ub - 1) / s.ub;
-    *u0 = (int)(a < n ? a : n);
-    *u1 = (int)(b < n ? b : n);
-}
-
-// Build the chunk list of a phase for this CTA.  Auxiliary chunks precede the
-// segment that needs them.  n_prev: rows of the previous token's mask (0 or K).
-__device__ int build_chunks(const Ctx& c, const Seg* S, int nseg, long long total, int n_prev,
-                            Chunk* ch) {
+// Build this CTA's chunk list of a phase (after build_segments).  Auxiliary
+// chunks precede the segment that needs them.  n_prev: rows of the previous
+// token's mask (0 or K).  Returns 0, or an EDGE0_* status.
+__device__ int build_chunks(const Ctx& c, int total, int n_prev, PhaseList* Lp) {
     const Prog& p = *c.p;
-    long long lo, hi;
-    cta_range(total, c.cta, c.nct, &lo, &hi);
-    int n = 0;
-    auto push = [&](int aux, int seg, int u0, int u1, int tok, int bytes) {
-        if (n >= kMaxChunk) { n = kMaxChunk + 1; return; }
-        if (n > kMaxChunk) return;
-        Chunk& x = ch[n++];
-        x.aux = aux; x.seg = seg; x.u0 = u0; x.u1 = u1; x.tok = tok; x.bytes = bytes;
+    const int lo = (int)((long long)total * c.cta / c.nct);
+    const int hi = (int)((long long)total * (c.cta + 1) / c.nct);
+    int n = 0, rows = 0;
+    bool over = false;
+    // every chunk is written once, whole
+    auto push = [&](int aux, int seg, int u0, int u1, int tok, int bytes, int sacc_row) {
+        if (n >= kMaxChunk) { over = true; return; }
+        Chunk v;
+        v.aux = aux; v.seg = seg; v.u0 = u0; v.u1 = u1; v.tok = tok; v.bytes = bytes;
+        v.sacc = sacc_row;
+        Lp->ch[n] = v;
+        ++n;
     };
-    const int R16 = c.R16;
-    for (int s = 0; s < nseg; ++s) {
-        int u0, u1;
-        seg_units(S[s], lo, hi, &u0, &u1);
+    Lp->has_sh = 0;
+    Lp->has_head = 0;
+    Lp->bd_row0 = 0;
+    Lp->bd_rows = 0;
+    for (int s = 0; s < Lp->nseg; ++s) {
+        Seg& S = Lp->seg[s];
+        const int nu = S.n_rt * S.n_g;
+        int a = lo - S.off, b = hi - S.off;
+        a = a <= 0 ? 0 : units_of(S.kind, a);
+        b = b <= 0 ? 0 : units_of(S.kind, b);
+        const int u0 = a < nu ? a : nu, u1 = b < nu ? b : nu;
+        S.cu0 = u0;
+        S.cu1 = u1;
         if (u0 >= u1) continue;
-        if (S[s].extra == EX_LORA_DOWN) {
-            push(AUX_BG, s, 0, 0, 0, p.Is * p.r * 2);
-            push(AUX_BU, s, 0, 0, 0, p.Is * p.r * 2);
-            push(AUX_AD, s, 0, 0, 0, (int)f16_bytes(p.r, p.Is));
-        }
-        if (S[s].extra == EX_HEAD) {
-            for (int b = 0; b < p.B; ++b) push(AUX_FC1OH, s, 0, 0, b, (p.K + n_prev) * p.H * 2);
-            for (int b = 0; b < p.B; ++b) push(AUX_LINOH, s, 0, 0, b, (p.K + n_prev) * p.E * 2);
-        }
-        int cap = kStageBytes / S[s].ub;
-        if (cap > 30 * S[s].n_g) cap = 30 * S[s].n_g;     // sacc holds 32 row tiles
-        for (int a = u0; a < u1; a += cap) {
-            const int b = a + cap < u1 ? a + cap : u1;
-            if (S[s].extra == EX_LORA_DOWN) {
-                // B_d rows of the row tiles whose group-0 unit is in [a, b)
-                const int ng = S[s].n_g;
-                const int rt_a = (a + ng - 1) / ng, rt_b = (b - 1) / ng;   // inclusive
-                if (rt_a <= rt_b) {
-                    const int row0 = rt_a * kRowTile;
-                    int row1 = (rt_b + 1) * kRowTile;
-                    if (row1 > p.d) row1 = p.d;
-                    push(AUX_BD, s, rt_a, rt_b + 1, 0, (row1 - row0) * p.r * 2);
-                }
+        if (S.src == SRC_ACTSH) Lp->has_sh = 1;
+        if (S.src == SRC_GELU) Lp->has_head = 1;
+        if (S.extra == EX_LORA_DOWN) {
+            push(AUX_BG, s, 0, 0, 0, p.Is * p.r * 2, 0);
+            push(AUX_BU, s, 0, 0, 0, p.Is * p.r * 2, 0);
+            push(AUX_AD, s, 0, 0, 0, (int)f16_bytes(p.r, p.Is), 0);
+            // B_d rows of the row tiles whose group-0 unit belongs to this CTA
+            const int ng = S.n_g;
+            const int rt_a = (u0 + ng - 1) / ng, rt_b = (u1 - 1) / ng;   // inclusive
+            if (rt_a <= rt_b) {
+                const int row0 = rt_a * kRowTile;
+                int row1 = (rt_b + 1) * kRowTile;
+                if (row1 > p.d) row1 = p.d;
+                if ((row1 - row0) * p.r * 2 > kBdBytes) return EDGE0_EUNSUPPORTED;
+                Lp->bd_row0 = row0;
+                Lp->bd_rows = row1 - row0;
+                push(AUX_BD, s, rt_a, rt_b + 1, 0, (row1 - row0) * p.r * 2, 0);
             }
-            push(AUX_UNITS, s, a, b, 0, (b - a) * S[s].ub);
+        }
+        if (S.extra == EX_HEAD) {
+            for (int t = 0; t < p.B; ++t) push(AUX_FC1OH, s, 0, 0, t, (p.K + n_prev) * p.H * 2, 0);
+            for (int t = 0; t < p.B; ++t) push(AUX_LINOH, s, 0, 0, t, (p.K + n_prev) * p.E * 2, 0);
+        }
+        int cap = kStageBytes / S.ub;
+        if (cap > 30 * S.n_g) cap = 30 * S.n_g;     // a chunk spans at most 32 row tiles
+        for (int x = u0; x < u1; x += cap) {
+            const int y = x + cap < u1 ? x + cap : u1;
+            push(AUX_UNITS, s, x, y, 0, (y - x) * S.ub, rows);
+            rows += ((y - 1) / S.n_g - x / S.n_g + 1) * kRowTile;
         }
     }
-    (void)R16;
-    return n;
+    if (over || rows > kSaccRowsPhase) return EDGE0_EUNSUPPORTED;
+    Lp->nch = n;
+    Lp->sacc_rows = rows;
+    return EDGE0_OK;
 }
 
 // ------------------------------------------------------------ producer -----
@@ -434,35 +480,28 @@ __device__ void producer(Ctx& c) {
     Ctl* ctl = c.ctl;
     uint64_t* full = reinterpret_cast<uint64_t*>(c.sm + c.pl.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(c.sm + c.pl.empty);
-    Seg* S = reinterpret_cast<Seg*>(c.sm + c.pl.segp);
-    Chunk* ch = reinterpret_cast<Chunk*>(c.sm + c.pl.chp);
     volatile int* ready = reinterpret_cast<volatile int*>(c.sm + c.pl.ready);
     const uint64_t pol = policy_evict_first();
     const int step = c.step;
     int stage = 0;
     uint32_t round = 0;
     int issued = 0;
+    int pi = 0;
 
     for (int l = 0; l < p.L; ++l) {
         const LayerP& Ly = p.layers[l];
         for (int ph = PH_R; ph <= PH_B; ++ph) {
             if (ph == PH_R && !has_router_phase(p, l, step)) continue;
+            // the list slot is free once the consumers finished phase pi - kListSlots
+            if (!wait_flag(&ctl->cdone, pi - kListSlots + 1, c.hdr, ctl)) return;
             if (ph != PH_R) {
-                // wait until the consumers have published this layer's routing
-                const unsigned long long t0 = now_ns();
-                for (unsigned it = 0; !ready[l]; ++it) {
-                    __nanosleep(64);
-                    if ((it & 63) == 63) {
-                        if (should_abort(c.hdr, ctl)) return;
-                        if (now_ns() - t0 > kTimeoutNs) { raise_error(c.hdr, ctl, EDGE0_ETIMEOUT); return; }
-                    }
-                }
+                if (!wait_flag(&ready[l], 1, c.hdr, ctl)) return;
                 __threadfence_block();
             }
+            PhaseList* Lp = list_slot(c, pi);
             const int* ids = sm_ids(c, l);
-            long long total;
-            const int nseg = build_segments(c, l, ph, ids, S, &total);
-            if (nseg < 0) { raise_error(c.hdr, ctl, EDGE0_EINVAL); return; }
+            const int total = build_segments(c, l, ph, ids, Lp);
+            if (total < 0) { raise_error(c.hdr, ctl, EDGE0_EINVAL); return; }
             // previous-token mask rows for the head's one-hot columns
             const int32_t* prev = nullptr;
             if (p.mode == MODE_HEAD) prev = p.prev_in;
@@ -474,14 +513,16 @@ __device__ void producer(Ctx& c) {
             if (ph != PH_R)
                 for (int i = 0; i < p.K * p.B; ++i)
                     if (ids[i] < 0 || ids[i] >= p.E) { raise_error(c.hdr, ctl, EDGE0_EINVAL); return; }
-            const int nch = build_chunks(c, S, nseg, total, n_prev, ch);
-            if (nch > kMaxChunk) { raise_error(c.hdr, ctl, EDGE0_EUNSUPPORTED); return; }
-            for (int i = 0; i < nch; ++i) {
-                const Chunk& x = ch[i];
+            const int rc = build_chunks(c, total, n_prev, Lp);
+            if (rc) { raise_error(c.hdr, ctl, rc); return; }
+            __threadfence_block();
+            *(volatile int*)&Lp->seq = pi + 1;
+            for (int i = 0; i < Lp->nch; ++i) {
+                const Chunk& x = Lp->ch[i];
                 if (!mbar_wait(&empty[stage], (round & 1) ^ 1, c.hdr, ctl)) return;
                 char* dst = c.sm + c.pl.stage + stage * kStageBytes;
                 mbar_arrive_expect_tx(&full[stage], (uint32_t)x.bytes);
-                const Seg& s = S[x.seg];
+                const Seg& s = Lp->seg[x.seg];
                 switch (x.aux) {
                     case AUX_UNITS:
                         bulk_g2s(dst, s.base + (long long)x.u0 * s.ub, x.bytes, &full[stage], pol);
@@ -519,18 +560,15 @@ __device__ void producer(Ctx& c) {
                 *(volatile int*)&ctl->issued = issued;
                 if (++stage == kStages) { stage = 0; ++round; }
             }
+            ++pi;
         }
     }
 }
 
 // ------------------------------------------------------------ consumers ----
-struct CState {
-    int stage;
-    uint32_t round;
-    int consumed;
-};
-
 __device__ __forceinline__ void cbar() { named_bar_sync(1, kConsumerThreads); }
+
+__device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile int*)&c.ctl->abort != 0; }
 
 // grid-wide barrier among the consumer warps of all CTAs
 __device__ bool grid_barrier(Ctx& c, unsigned long long& target) {
@@ -552,10 +590,8 @@ __device__ bool grid_barrier(Ctx& c, unsigned long long& target) {
         if (!ok) c.ctl->abort = 1;
     }
     cbar();
-    return !(*(volatile int*)&c.ctl->abort);
+    return !aborted(c);
 }
-
-__device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile int*)&c.ctl->abort != 0; }
 
 // B-fragment / sum pointers of tensor-core column n of segment s (null when
 // inactive).  Column n carries token n / 2: its hi part (n even) or its lo part
@@ -626,103 +662,6 @@ __device__ __forceinline__ float* out_ptr(const Ctx& c, const Seg& s, float* F, 
         case OUT_LOGR: return F + a.logr + (long long)b * p.E + row;
         default: return F + a.logh + (long long)b * p.E + row;
     }
-}
-
-// One warp computes units [ua, ub) of segment s held in `stage` (chunk starting
-// at unit cu0) and adds its per-row partial sums into the chunk accumulator sacc
-// (rows relative to row tile rt0, B columns).
-__device__ void warp_units(const Ctx& c, const Seg& s, int l, const char* stage, int cu0, int ua,
-                           int ub, float* sacc, int rt0) {
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int B = c.p->B;
-    const __half* bf;
-    const float* dummy;
-    col_src(c, s, l, g, &bf, &dummy);
-    const float* sum0;
-    const float* sum1;
-    const __half* f0;
-    const __half* f1;
-    col_src(c, s, l, 2 * t, &f0, &sum0);
-    col_src(c, s, l, 2 * t + 1, &f1, &sum1);
-    const bool q4 = s.kind == 0;
-    int cur = -1;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
-    auto flush = [&](int rt) {
-        float vg, vg8;   // token t: hi column + lo column
-        if (!q4) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { y[i] = lo[i] + 16.0f * hi[i]; lo[i] = 0.f; hi[i] = 0.f; }
-            vg = y[0] + kLoInv * y[1];
-            vg8 = y[2] + kLoInv * y[3];
-        } else {
-            vg = y[0] + y[1];
-            vg8 = y[2] + y[3];
-        }
-        const int r0 = (rt - rt0) * kRowTile + g;
-        if (t < B) {
-            atomicAdd(&sacc[r0 * B + t], vg);
-            atomicAdd(&sacc[(r0 + 8) * B + t], vg8);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) y[i] = 0.f;
-    };
-    for (int u = ua; u < ub; ++u) {
-        const int rt = u / s.n_g, grp = u - rt * s.n_g;
-        if (rt != cur) {
-            if (cur >= 0) flush(cur);
-            cur = rt;
-        }
-        const char* unit = stage + (long long)(u - cu0) * s.ub;
-        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
-        if (bf) {
-            const uint4* bp = reinterpret_cast<const uint4*>(bf + (grp * 4 + t) * 16);
-            b0 = bp[0];
-            b1 = bp[1];
-        }
-        if (q4) {
-            const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
-            const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g);
-            float a4[4] = {0.f, 0.f, 0.f, 0.f};
-            constexpr uint32_t M0 = 0x000F000Fu, M1 = 0x00F000F0u;
-            const uint32_t x8 = wv.x >> 8, z8 = wv.z >> 8, y8 = wv.y >> 8, w8 = wv.w >> 8;
-            uint32_t a[4];
-            a[0] = wv.x & M0; a[1] = wv.z & M0; a[2] = x8 & M0; a[3] = z8 & M0;
-            mma_16816(a4, a, b0.x, b0.y);
-            a[0] = wv.x & M1; a[1] = wv.z & M1; a[2] = x8 & M1; a[3] = z8 & M1;
-            mma_16816(a4, a, b0.z, b0.w);
-            a[0] = wv.y & M0; a[1] = wv.w & M0; a[2] = y8 & M0; a[3] = w8 & M0;
-            mma_16816(a4, a, b1.x, b1.y);
-            a[0] = wv.y & M1; a[1] = wv.w & M1; a[2] = y8 & M1; a[3] = w8 & M1;
-            mma_16816(a4, a, b1.z, b1.w);
-            const __half2 sb0 = *reinterpret_cast<const __half2*>(&sc.x);
-            const __half2 sb1 = *reinterpret_cast<const __half2*>(&sc.y);
-            const float sg = __low2float(sb0) * 16777216.0f, bg = __high2float(sb0);
-            const float sg8 = __low2float(sb1) * 16777216.0f, bg8 = __high2float(sb1);
-            const float xs0 = sum0 ? sum0[grp] : 0.f, xs1 = sum1 ? sum1[grp] : 0.f;
-            // column 2t: hi part of token t; column 2t+1: lo part (scaled by 2^11)
-            y[0] += sg * a4[0] + bg * xs0;
-            y[1] += sg * kLoInv * a4[1] + bg * xs1;
-            y[2] += sg8 * a4[2] + bg8 * xs0;
-            y[3] += sg8 * kLoInv * a4[3] + bg8 * xs1;
-        } else {
-            const uint4 a0 = *reinterpret_cast<const uint4*>(unit + 0 * 512 + 16 * lane);
-            const uint4 a1 = *reinterpret_cast<const uint4*>(unit + 1 * 512 + 16 * lane);
-            const uint4 a2 = *reinterpret_cast<const uint4*>(unit + 2 * 512 + 16 * lane);
-            const uint4 a3 = *reinterpret_cast<const uint4*>(unit + 3 * 512 + 16 * lane);
-            uint32_t a[4];
-            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-            mma_16816(lo, a, b0.x, b0.y);
-            a[0] = a1.x; a[1] = a1.y; a[2] = a1.z; a[3] = a1.w;
-            mma_16816(hi, a, b0.z, b0.w);
-            a[0] = a2.x; a[1] = a2.y; a[2] = a2.z; a[3] = a2.w;
-            mma_16816(lo, a, b1.x, b1.y);
-            a[0] = a3.x; a[1] = a3.y; a[2] = a3.z; a[3] = a3.w;
-            mma_16816(hi, a, b1.z, b1.w);
-        }
-    }
-    if (cur >= 0) flush(cur);
 }
 
 // ----------------------------------------------------------- prologues -----
@@ -819,33 +758,127 @@ __device__ void head_topk(Ctx& c, int l, unsigned pc) {
     }
 }
 
+// One warp computes units [ua, ub) of segment s held in `stage` (chunk starting
+// at unit cu0) and adds its per-row partial sums into the accumulator rows sacc
+// (relative to row tile rt0, B columns).
+__device__ void warp_units(const Ctx& c, const Seg& s, int l, const char* stage, int cu0, int ua,
+                           int ub, float* sacc, int rt0) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int B = c.p->B;
+    const __half* bf;
+    const float* dummy;
+    col_src(c, s, l, g, &bf, &dummy);
+    const float* sum0;
+    const float* sum1;
+    const __half* f0;
+    const __half* f1;
+    col_src(c, s, l, 2 * t, &f0, &sum0);
+    col_src(c, s, l, 2 * t + 1, &f1, &sum1);
+    const bool q4 = s.kind == 0;
+    const int ng = s.n_g;
+    int cur = -1;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+    auto flush = [&](int rt) {
+        float vg, vg8;   // token t: hi column + lo column
+        if (!q4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { y[i] = lo[i] + 16.0f * hi[i]; lo[i] = 0.f; hi[i] = 0.f; }
+            vg = y[0] + kLoInv * y[1];
+            vg8 = y[2] + kLoInv * y[3];
+        } else {
+            vg = y[0] + y[1];
+            vg8 = y[2] + y[3];
+        }
+        const int r0 = (rt - rt0) * kRowTile + g;
+        if (t < B) {
+            atomicAdd(&sacc[r0 * B + t], vg);
+            atomicAdd(&sacc[(r0 + 8) * B + t], vg8);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) y[i] = 0.f;
+    };
+    int rt = ua / ng, grp = ua - rt * ng;
+    for (int u = ua; u < ub; ++u) {
+        if (rt != cur) {
+            if (cur >= 0) flush(cur);
+            cur = rt;
+        }
+        const char* unit = stage + (u - cu0) * s.ub;
+        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
+        if (bf) {
+            const uint4* bp = reinterpret_cast<const uint4*>(bf + (grp * 4 + t) * 16);
+            b0 = bp[0];
+            b1 = bp[1];
+        }
+        if (q4) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+            const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g);
+            float a4[4] = {0.f, 0.f, 0.f, 0.f};
+            constexpr uint32_t M0 = 0x000F000Fu, M1 = 0x00F000F0u;
+            const uint32_t x8 = wv.x >> 8, z8 = wv.z >> 8, y8 = wv.y >> 8, w8 = wv.w >> 8;
+            uint32_t a[4];
+            a[0] = wv.x & M0; a[1] = wv.z & M0; a[2] = x8 & M0; a[3] = z8 & M0;
+            mma_16816(a4, a, b0.x, b0.y);
+            a[0] = wv.x & M1; a[1] = wv.z & M1; a[2] = x8 & M1; a[3] = z8 & M1;
+            mma_16816(a4, a, b0.z, b0.w);
+            a[0] = wv.y & M0; a[1] = wv.w & M0; a[2] = y8 & M0; a[3] = w8 & M0;
+            mma_16816(a4, a, b1.x, b1.y);
+            a[0] = wv.y & M1; a[1] = wv.w & M1; a[2] = y8 & M1; a[3] = w8 & M1;
+            mma_16816(a4, a, b1.z, b1.w);
+            const __half2 sb0 = *reinterpret_cast<const __half2*>(&sc.x);
+            const __half2 sb1 = *reinterpret_cast<const __half2*>(&sc.y);
+            const float sg = __low2float(sb0) * 16777216.0f, bg = __high2float(sb0);
+            const float sg8 = __low2float(sb1) * 16777216.0f, bg8 = __high2float(sb1);
+            const float xs0 = sum0 ? sum0[grp] : 0.f, xs1 = sum1 ? sum1[grp] : 0.f;
+            // column 2t: hi part of token t; column 2t+1: lo part (scaled by 2^11)
+            y[0] += sg * a4[0] + bg * xs0;
+            y[1] += sg * kLoInv * a4[1] + bg * xs1;
+            y[2] += sg8 * a4[2] + bg8 * xs0;
+            y[3] += sg8 * kLoInv * a4[3] + bg8 * xs1;
+        } else {
+            const uint4 a0 = *reinterpret_cast<const uint4*>(unit + 0 * 512 + 16 * lane);
+            const uint4 a1 = *reinterpret_cast<const uint4*>(unit + 1 * 512 + 16 * lane);
+            const uint4 a2 = *reinterpret_cast<const uint4*>(unit + 2 * 512 + 16 * lane);
+            const uint4 a3 = *reinterpret_cast<const uint4*>(unit + 3 * 512 + 16 * lane);
+            uint32_t a[4];
+            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+            mma_16816(lo, a, b0.x, b0.y);
+            a[0] = a1.x; a[1] = a1.y; a[2] = a1.z; a[3] = a1.w;
+            mma_16816(hi, a, b0.z, b0.w);
+            a[0] = a2.x; a[1] = a2.y; a[2] = a2.z; a[3] = a2.w;
+            mma_16816(lo, a, b1.x, b1.y);
+            a[0] = a3.x; a[1] = a3.y; a[2] = a3.z; a[3] = a3.w;
+            mma_16816(hi, a, b1.z, b1.w);
+        }
+        if (++grp == ng) { grp = 0; ++rt; }
+    }
+    if (cur >= 0) flush(cur);
+}
+
 // act = silu(g) u of every routed pair whose down segment has units in this CTA
-__device__ void build_act(Ctx& c, int l, const Seg* S, int nseg, long long total, unsigned pcA) {
+__device__ void build_act(Ctx& c, int l, const PhaseList* Lp, unsigned pcA) {
     const Prog& p = *c.p;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    long long lo, hi;
-    cta_range(total, c.cta, c.nct, &lo, &hi);
     const float* F = acc_set(c, pcA);
     __half* actf = reinterpret_cast<__half*>(c.sm + c.pl.actf);
     float* actsum = reinterpret_cast<float*>(c.sm + c.pl.actsum);
     const int ng = p.I / kGroup;
     const int* ids = sm_ids(c, l);
+    const long long npair = (long long)p.B * p.K;
     for (int it = wid; it < p.B * p.K * ng; it += kConsumerWarps) {
         const int pair = it / ng, grp = it - pair * ng;
         const int e = ids[pair];
         bool need = false;
-        for (int s = 0; s < nseg; ++s)
-            if (S[s].out == OUT_Y && S[s].expert == e) {
-                int u0, u1;
-                seg_units(S[s], lo, hi, &u0, &u1);
-                need = u0 < u1;
-            }
+        for (int s = 0; s < Lp->nseg; ++s)
+            if (Lp->seg[s].out == OUT_Y && Lp->seg[s].expert == e)
+                need = Lp->seg[s].cu0 < Lp->seg[s].cu1;
         if (!need) continue;
         const float* gp = F + c.acc.gu + (long long)pair * 2 * p.I;
         const int i0 = grp * kGroup + lane, i1 = i0 + 32;
         const float a0 = silu_f(gp[i0]) * gp[p.I + i0];
         const float a1 = silu_f(gp[i1]) * gp[p.I + i1];
-        const long long npair = (long long)p.B * p.K;
         put_group(actf + (long long)pair * p.I + grp * kGroup, actsum + pair * ng + grp, a0, a1, lane,
                   actf + (pair + npair) * p.I + grp * kGroup, actsum + (pair + npair) * ng + grp);
     }
@@ -855,9 +888,9 @@ __device__ void build_act(Ctx& c, int l, const Seg* S, int nseg, long long total
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ Prog prog) {
     extern __shared__ __align__(128) char smem[];
     Ctx c;
-    c.p = &prog;
     c.sm = smem;
     c.pl = make_plan(prog.L, prog.B, prog.K, prog.d, prog.E, prog.I, prog.Is, prog.H, prog.r);
+    c.p = &prog;
     c.hdr = reinterpret_cast<WsHeader*>(prog.ws);
     c.ctl = reinterpret_cast<Ctl*>(smem + c.pl.ctl);
     c.acc = acc_layout(prog.B, prog.K, prog.I, prog.Is, prog.r, prog.H, prog.E, prog.d);
@@ -865,15 +898,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     c.cta = blockIdx.x;
     c.R16 = ceil_div(prog.r, 16) * 16;
     const int tid = threadIdx.x;
-    const Prog& p = prog;
+    const Prog& p = *c.p;
 
     if (tid == 0) {
         c.ctl->abort = 0;
         c.ctl->issued = 0;
-        c.ctl->consumed = 0;
+        c.ctl->cdone = 0;
         c.ctl->step = p.step >= 0 ? p.step : ld_volatile_s32(&c.hdr->step);
         c.ctl->pc0 = *(volatile unsigned*)&c.hdr->pc;
-        c.ctl->trace = ld_volatile_s32(&c.hdr->trace) && c.cta < kTraceCtas;
+        c.ctl->trace = c.cta < kTraceCtas ? ld_volatile_s32(&c.hdr->trace) : 0;
         c.ctl->tslot = 0;
         uint64_t* full = reinterpret_cast<uint64_t*>(smem + c.pl.full);
         uint64_t* empty = reinterpret_cast<uint64_t*>(smem + c.pl.empty);
@@ -883,13 +916,17 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         }
         fence_mbar_init();
     }
-    // routing known at launch: predictions (prerouted layers, step > 0) or inputs
     {
         int* ready = reinterpret_cast<int*>(smem + c.pl.ready);
         for (int l = tid; l < p.L; l += kThreads) ready[l] = 0;
+        for (int i = tid; i < kListSlots; i += kThreads)
+            reinterpret_cast<PhaseList*>(smem + c.pl.lists)[i].seq = 0;
+        float* sacc = reinterpret_cast<float*>(smem + c.pl.sacc);
+        for (int i = tid; i < kSaccRowsPhase * p.B; i += kThreads) sacc[i] = 0.f;
     }
     __syncthreads();
     c.step = c.ctl->step;
+    // routing known at launch: predictions (prerouted layers, step > 0) or inputs
     {
         int* ready = reinterpret_cast<int*>(smem + c.pl.ready);
         const int BK = p.B * p.K;
@@ -926,9 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     const int lane = tid & 31, wid = tid >> 5;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + c.pl.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + c.pl.empty);
-    Seg* S = reinterpret_cast<Seg*>(smem + c.pl.segc);
-    Chunk* ch = reinterpret_cast<Chunk*>(smem + c.pl.chc);
-    float* sacc0 = reinterpret_cast<float*>(smem + c.pl.sacc);
+    float* sacc = reinterpret_cast<float*>(smem + c.pl.sacc);
     volatile int* ready = reinterpret_cast<volatile int*>(smem + c.pl.ready);
     const int B = p.B;
     unsigned long long bar_target = 0;
@@ -936,32 +971,33 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         const unsigned long long v = ld_acquire_u64(&c.hdr->barrier);
         bar_target = v - v % (unsigned long long)c.nct;
     }
-    for (int i = tid; i < 2 * kSaccRows * B; i += kConsumerThreads) sacc0[i] = 0.f;
     unsigned pc = c.ctl->pc0;
-    CState cs{0, 0, 0};
-    int sacc_buf = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    int consumed = 0;
+    int pi = 0;
     unsigned pc_prevB = 0;        // phase of the previous layer's B (y, head logits)
     bool prev_head = false;        // previous layer's head logits await top-K
     int prev_layer = -1;
     cbar();
 
-    for (int l = 0; l < p.L; ++l) {
+    for (int l = 0; l < p.L && !aborted(c); ++l) {
         const LayerP& Ly = p.layers[l];
         const bool decode = p.mode == MODE_DECODE;
         unsigned pcR = 0;
+        const bool rphase = has_router_phase(p, l, c.step);
         for (int ph = PH_R; ph <= PH_B; ++ph) {
-            const bool rphase = has_router_phase(p, l, c.step);
             if (ph == PH_R && !rphase) continue;
             // ---------------- prologue
             const int ttag = (l << 8) | (ph << 4);
             stamp(c, ttag | 0);
             zero_set_slice(c, pc + 1);
+            dstamp(c, l, 0x10000 | ttag | 1);
             const bool first_of_layer = (ph == PH_R) || (ph == PH_A && !rphase);
             if (first_of_layer) {
                 if (decode) {
                     const __half* hs = (l <= 1) ? p.h_io : hbuf(c, (l - 1) & 1);
                     const float* ys = l == 0 ? nullptr : acc_set(c, pc_prevB) + c.acc.y;
-                    if (l == 0) hs = p.h_io;
                     build_x(c, hs, ys, l == 0 ? nullptr : hbuf(c, l & 1), Ly.gamma, Ly.eps, true);
                 } else {
                     build_x(c, p.x_in, nullptr, nullptr, nullptr, 0.f, false);
@@ -969,6 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                 if (prev_head && c.cta == c.nct - 1) head_topk(c, prev_layer, pc_prevB);
                 prev_head = false;
             }
+            dstamp(c, l, 0x10000 | ttag | 2);
             if (ph == PH_R) pcR = pc;
             if (ph == PH_A && rphase) {
                 // own routing from the router logits of phase R
@@ -977,9 +1014,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                 for (int b = wid; b < B; b += kConsumerWarps) {
                     __shared__ int rid[EDGE0_MAX_BATCH][EDGE0_MAX_K];
                     __shared__ float rw[EDGE0_MAX_BATCH][EDGE0_MAX_K];
-                    float* mine = scr + (long long)b * 2 * p.E;
                     warp_route(F + c.acc.logr + (long long)b * p.E, p.E, p.K, Ly.route_kind, Ly.n_groups,
-                               Ly.topk_groups, Ly.route_scale, Ly.bias, mine, rid[b], rw[b], lane);
+                               Ly.topk_groups, Ly.route_scale, Ly.bias, scr + (long long)b * 2 * p.E,
+                               rid[b], rw[b], lane);
                     if (lane < p.K) {
                         sm_ids(c, l)[b * p.K + lane] = rid[b][lane];
                         sm_w(c, l)[b * p.K + lane] = rw[b][lane];
@@ -995,47 +1032,19 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                 for (int i = tid; i < B * p.K; i += kConsumerThreads)
                     p.exec_ids[(((long long)(c.step & 1) * p.Ls + Ly.sidx) * B) * p.K + i] = sm_ids(c, l)[i];
             }
+            // this phase's list, published by the producer
+            PhaseList* Lp = list_slot(c, pi);
+            dstamp(c, l, 0x10000 | ttag | 3);
+            if (tid == 0) wait_flag(&Lp->seq, pi + 1, c.hdr, c.ctl);
             cbar();
-            // segment and chunk lists of this phase (consumer copy)
-            long long total = 0;
-            int nseg = 0, nch = 0;
-            __shared__ int s_nseg, s_nch;
-            __shared__ long long s_total;
-            if (tid == 0) {
-                const int* ids = sm_ids(c, l);
-                nseg = build_segments(c, l, ph, ids, S, &total);
-                if (nseg < 0) { s_nseg = -1; s_nch = 0; s_total = 0; }
-                const bool has_prev = (p.mode == MODE_HEAD) ? (p.prev_in != nullptr)
-                                                             : (decode && c.step > 0);
-                nch = nseg < 0 ? 0 : build_chunks(c, S, nseg, total, has_prev ? p.K : 0, ch);
-                s_nseg = nseg;
-                s_nch = nch;
-                s_total = total;
-            }
-            cbar();
-            nseg = s_nseg;
-            nch = s_nch;
-            total = s_total;
-            if (nseg < 0 || nch > kMaxChunk) {
-                if (tid == 0) raise_error(c.hdr, c.ctl, nseg < 0 ? EDGE0_EINVAL : EDGE0_EUNSUPPORTED);
-                cbar();
-                break;
-            }
+            dstamp(c, l, 0x10000 | ttag | 4);
+            if (aborted(c)) break;
+            if (Lp->seq != pi + 1) break;
             float* F = acc_set(c, pc);
             const float* FA = acc_set(c, pc - 1);     // phase A results (valid in phase B)
             if (ph == PH_B) {
-                build_act(c, l, S, nseg, total, pc - 1);
-                // shared expert raw gate/up and LoRA A x, head pre-activations
-                bool need_sh = false, need_head = false;
-                long long lo, hi;
-                cta_range(total, c.cta, c.nct, &lo, &hi);
-                for (int s = 0; s < nseg; ++s) {
-                    int u0, u1;
-                    seg_units(S[s], lo, hi, &u0, &u1);
-                    if (u0 < u1 && S[s].src == SRC_ACTSH) need_sh = true;
-                    if (u0 < u1 && S[s].src == SRC_GELU) need_head = true;
-                }
-                if (need_sh) {
+                build_act(c, l, Lp, pc - 1);
+                if (Lp->has_sh) {
                     float* gsh = reinterpret_cast<float*>(smem + c.pl.gsh);
                     float* ush = reinterpret_cast<float*>(smem + c.pl.ush);
                     float* aacc = reinterpret_cast<float*>(smem + c.pl.aacc);
@@ -1061,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                         }
                     }
                 }
-                if (need_head) {
+                if (Lp->has_head) {
                     float* zsm = reinterpret_cast<float*>(smem + c.pl.zsm);
                     float* linsm = reinterpret_cast<float*>(smem + c.pl.linsm);
                     for (int i = tid; i < B * p.H; i += kConsumerThreads) zsm[i] = FA[c.acc.z + i];
@@ -1073,23 +1082,29 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             stamp(c, ttag | 1);
             const __half* held_bg = nullptr;
             int held_bg_stage = -1;
-            const char* held_bd = nullptr;
-            int held_bd_stage = -1, held_bd_rt0 = 0;
-            for (int i = 0; i < nch && !aborted(c); ++i) {
-                const Chunk x = ch[i];
-                const int st = cs.stage;
-                if (!mbar_wait(&full[st], cs.round & 1, c.hdr, c.ctl)) { c.ctl->abort = 1; }
-                cbar();
-                if (aborted(c)) break;
+            for (int i = 0; i < Lp->nch; ++i) {
+                const Chunk x = Lp->ch[i];
+                const int st = stage;
+                if (!mbar_wait(&full[st], round & 1, c.hdr, c.ctl)) { c.ctl->abort = 1; break; }
+                dstamp(c, l, 0x20000 | (i << 8) | (ph << 4) | x.aux);
                 const char* buf = smem + c.pl.stage + st * kStageBytes;
-                const Seg& s = S[x.seg];
+                const Seg& s = Lp->seg[x.seg];
                 bool release = true;
-                if (x.aux == AUX_BG) {
+                if (x.aux == AUX_UNITS) {
+                    // each warp takes a contiguous share of the chunk's units; no CTA sync
+                    const int n = x.u1 - x.u0;
+                    const int ua = x.u0 + (n * wid) / kConsumerWarps;
+                    const int ub2 = x.u0 + (n * (wid + 1)) / kConsumerWarps;
+                    if (ua < ub2)
+                        warp_units(c, s, l, buf, x.u0, ua, ub2, sacc + x.sacc * B, x.u0 / s.n_g);
+                    __syncwarp();
+                } else if (x.aux == AUX_BG) {
                     held_bg = reinterpret_cast<const __half*>(buf);
                     held_bg_stage = st;
                     release = false;
                 } else if (x.aux == AUX_BU) {
                     // act_s = silu(g + (a/r) Bg ag) * (u + (a/r) Bu au), fp32 copy + fragments
+                    cbar();
                     const __half* Bu = reinterpret_cast<const __half*>(buf);
                     const float* gsh = reinterpret_cast<const float*>(smem + c.pl.gsh);
                     const float* ush = reinterpret_cast<const float*>(smem + c.pl.ush);
@@ -1126,12 +1141,13 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                 } else if (x.aux == AUX_AD) {
                     // v = A_d act_s (r rows), warp 0 on the tensor cores
                     float* v = reinterpret_cast<float*>(smem + c.pl.v);
+                    float* tmp = reinterpret_cast<float*>(smem + c.pl.rscr);   // 16 x B scratch
                     if (wid == 0) {
                         Seg sa;
                         sa.base = nullptr; sa.off = 0; sa.kind = 1;
                         sa.n_rt = ceil_div(p.r, kRowTile); sa.n_g = p.Is / kGroup; sa.rows = p.r;
                         sa.ub = kF16Unit; sa.src = SRC_ACTSH; sa.out = 0; sa.expert = -1; sa.extra = 0;
-                        float* tmp = sacc0 + (1 - sacc_buf) * kSaccRows * B;   // idle buffer
+                        sa.cu0 = 0; sa.cu1 = 0;
                         for (int q = lane; q < kRowTile * sa.n_rt * B; q += 32) tmp[q] = 0.f;
                         __syncwarp();
                         warp_units(c, sa, l, buf, 0, 0, sa.n_rt * sa.n_g, tmp, 0);
@@ -1139,15 +1155,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                         for (int q = lane; q < c.R16 * B; q += 32) {
                             const int row = q / B, b = q - row * B;
                             v[b * c.R16 + row] = row < p.r ? tmp[q] : 0.f;
-                            tmp[q] = 0.f;
                         }
                     }
                     cbar();
                 } else if (x.aux == AUX_BD) {
-                    held_bd = buf;
-                    held_bd_stage = st;
-                    held_bd_rt0 = x.u0;
-                    release = false;
+                    // this CTA's B_d rows, kept for the phase-end flush
+                    const uint4* src = reinterpret_cast<const uint4*>(buf);
+                    uint4* dst = reinterpret_cast<uint4*>(smem + c.pl.bd);
+                    for (int q = tid; q < x.bytes / 16; q += kConsumerThreads) dst[q] = src[q];
+                    cbar();
                 } else if (x.aux == AUX_FC1OH) {
                     // gelu(z + one-hot columns) fragments for token x.tok
                     const __half* rows = reinterpret_cast<const __half*>(buf);
@@ -1181,68 +1197,65 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
                         lx[e] = v;
                     }
                     cbar();
-                } else {
-                    // ---- weight units: split the chunk among the warps
-                    float* sacc = sacc0 + sacc_buf * kSaccRows * B;
-                    const int n = x.u1 - x.u0;
-                    const int rt0 = x.u0 / s.n_g;
-                    const int ua = x.u0 + (int)((long long)n * wid / kConsumerWarps);
-                    const int ub2 = x.u0 + (int)((long long)n * (wid + 1) / kConsumerWarps);
-                    if (ua < ub2) warp_units(c, s, l, buf, x.u0, ua, ub2, sacc, rt0);
-                    cbar();
-                    // flush rows of the touched row tiles to the global accumulators
-                    const int rt1 = (x.u1 - 1) / s.n_g;
-                    const int nrows = (rt1 - rt0 + 1) * kRowTile;
-                    float wcol[EDGE0_MAX_BATCH];
-                    int kcol[EDGE0_MAX_BATCH];
-                    for (int b = 0; b < B; ++b) {
-                        kcol[b] = col_kslot(c, s, l, b);
-                        wcol[b] = (s.out == OUT_Y && s.expert >= 0 && kcol[b] >= 0) ? sm_w(c, l)[b * p.K + kcol[b]] : 1.f;
-                    }
-                    for (int q = tid; q < nrows * B; q += kConsumerThreads) {
-                        const int rl = q / B, b = q - rl * B;
-                        const int rt = rt0 + rl / kRowTile;
-                        const int row = rt * kRowTile + (rl % kRowTile);
-                        float val = sacc[q];
-                        sacc[q] = 0.f;
-                        if (row >= s.rows || kcol[b] < 0) continue;
-                        const bool own0 = (rt * s.n_g >= x.u0) && (rt * s.n_g < x.u1);
-                        if (own0 && s.extra == EX_LORA_DOWN && held_bd) {
-                            const __half* bd = reinterpret_cast<const __half*>(held_bd) +
-                                               (long long)(row - held_bd_rt0 * kRowTile) * p.r;
-                            const float* v = reinterpret_cast<const float*>(smem + c.pl.v) + b * c.R16;
-                            float dsum = 0.f;
-                            for (int j = 0; j < p.r; ++j) dsum += __half2float(bd[j]) * v[j];
-                            val += Ly.lora_scale * dsum;
-                        }
-                        if (own0 && s.extra == EX_HEAD)
-                            val += reinterpret_cast<const float*>(smem + c.pl.lx)[b * p.E + row];
-                        red_add_f32(out_ptr(c, s, F, row, b, kcol[b]), val * wcol[b]);
-                    }
-                    sacc_buf ^= 1;
-                    cbar();
-                    if (held_bd) {
-                        if (lane == 0) mbar_arrive(&empty[held_bd_stage]);
-                        held_bd = nullptr;
-                    }
                 }
                 if (release && lane == 0) mbar_arrive(&empty[st]);
-                if (++cs.stage == kStages) { cs.stage = 0; ++cs.round; }
-                ++cs.consumed;
+                dstamp(c, l, 0x30000 | (i << 8) | (ph << 4) | x.aux);
+                if (++stage == kStages) { stage = 0; ++round; }
+                ++consumed;
             }
+            cbar();
             if (aborted(c)) break;
-            // ---------------- end of phase
+            // ---------------- flush this phase's accumulator rows to global memory
             stamp(c, ttag | 2);
-            if (!grid_barrier(c, bar_target)) break;
+            float wcol[EDGE0_MAX_BATCH];
+            int kcol[EDGE0_MAX_BATCH];
+            for (int i = 0; i < Lp->nch; ++i) {
+                const Chunk& x = Lp->ch[i];
+                if (x.aux != AUX_UNITS) continue;
+                const Seg& s = Lp->seg[x.seg];
+                const int rt0 = x.u0 / s.n_g, rt1 = (x.u1 - 1) / s.n_g;
+                const int nrows = (rt1 - rt0 + 1) * kRowTile;
+                for (int b = 0; b < B; ++b) {
+                    kcol[b] = col_kslot(c, s, l, b);
+                    wcol[b] = (s.out == OUT_Y && s.expert >= 0 && kcol[b] >= 0) ? sm_w(c, l)[b * p.K + kcol[b]] : 1.f;
+                }
+                float* sa = sacc + x.sacc * B;
+                for (int q = tid; q < nrows * B; q += kConsumerThreads) {
+                    const int rl = q / B, b = q - rl * B;
+                    const int rt = rt0 + (rl >> 4);
+                    const int row = rt * kRowTile + (rl & 15);
+                    float val = sa[q];
+                    sa[q] = 0.f;
+                    if (row >= s.rows || kcol[b] < 0) continue;
+                    const bool own0 = (rt * s.n_g >= x.u0) && (rt * s.n_g < x.u1);
+                    if (own0 && s.extra == EX_LORA_DOWN) {
+                        const __half* bd = reinterpret_cast<const __half*>(smem + c.pl.bd) +
+                                           (long long)(row - Lp->bd_row0) * p.r;
+                        const float* v = reinterpret_cast<const float*>(smem + c.pl.v) + b * c.R16;
+                        float dsum = 0.f;
+                        for (int j = 0; j < p.r; ++j) dsum += __half2float(bd[j]) * v[j];
+                        val += Ly.lora_scale * dsum;
+                    }
+                    if (own0 && s.extra == EX_HEAD)
+                        val += reinterpret_cast<const float*>(smem + c.pl.lx)[b * p.E + row];
+                    red_add_f32(out_ptr(c, s, F, row, b, kcol[b]), val * wcol[b]);
+                }
+            }
+            dstamp(c, l, 0x10000 | ttag | 5);
+            cbar();
+            if (tid == 0) *(volatile int*)&c.ctl->cdone = pi + 1;
+            // ---------------- end of phase
             stamp(c, ttag | 3);
+            if (!grid_barrier(c, bar_target)) break;
+            stamp(c, ttag | 4);
             if (ph == PH_B) {
                 pc_prevB = pc;
                 prev_head = (p.mode != MODE_MOE) && (p.mode == MODE_HEAD || (Ly.flags & LF_HEAD));
                 prev_layer = l;
             }
             ++pc;
+            ++pi;
         }
-        if (aborted(c)) break;
     }
 
     if (!aborted(c)) {
@@ -1274,10 +1287,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     } else if (tid == 0) {
         // drain copies still in flight before the CTA exits (bounded)
         const int issued = *(volatile int*)&c.ctl->issued;
-        int stage = cs.stage;
-        uint32_t round = cs.round;
         const unsigned long long t0 = now_ns();
-        for (int k = cs.consumed; k < issued; ++k) {
+        for (int k = consumed; k < issued; ++k) {
             while (!mbar_try_wait(&full[stage], round & 1))
                 if (now_ns() - t0 > 100000000ull) break;
             if (++stage == kStages) { stage = 0; ++round; }
@@ -1285,10 +1296,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     }
 }
 
-}  // namespace edge0
-
-namespace edge0 {
 int engine_smem_bytes(const Prog& p) {
     return make_plan(p.L, p.B, p.K, p.d, p.E, p.I, p.Is, p.H, p.r).total;
 }
+
 }  // namespace edge0

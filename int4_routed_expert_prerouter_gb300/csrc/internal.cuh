@@ -29,7 +29,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kStageBytes = 16384;
 constexpr int kStages = 8;
-constexpr int kMaxSeg = 72;
+constexpr int kMaxSeg = 40;
 constexpr int kSaccRows = 32 * kRowTile;               // rows one chunk can touch
 
 enum Mode : int { MODE_DECODE = 0, MODE_MOE = 1, MODE_HEAD = 2 };

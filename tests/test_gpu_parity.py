@@ -285,7 +285,7 @@ def test_decode_toy_ragged_batch():
 
 
 def test_decode_8b_shapes_small():
-    cfg = configs.STACK8.with_(L=3, E=32, B=2, head_owner_first=0, head_owner_last=1,
+    cfg = configs.STACK8.with_(L=3, E=32, B=1, head_owner_first=0, head_owner_last=1,
                                prerouted=(1, 2))
     model = inputs.make_model(cfg, seed=3)
     assert _run_stack(cfg, model, 4) >= 2

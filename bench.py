@@ -192,23 +192,6 @@ def run_gpu(args, rank, world):
         t += 1
         st.set_trace(False)
         print_trace(st.read_trace(), torch.cuda.get_device_properties(dev).multi_processor_count)
-    if args.trace_detail is not None:
-        st.set_trace(True, args.trace_detail)
-        binding.decode_step(dm, st, h_all[t], t)
-        t += 1
-        st.set_trace(False)
-        tr = st.read_trace()
-        for cta in (0, 40, 75, 151):
-            t0 = None
-            evs = []
-            for tag, tm in tr[cta].tolist():
-                if tm == 0:
-                    break
-                if t0 is None:
-                    t0 = tm
-                evs.append(f"{tag:#07x}@{(tm - t0) / 1e3:.2f}")
-            sys.stderr.write(f"cta {cta}: " + " ".join(evs) + "\n")
-
     # device-resident timed region: one event pair per launch for the kernel
     # duration, one pair around the region for the step time
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -305,8 +288,11 @@ def run_gpu(args, rank, world):
 
 
 def print_trace(tr, nct):
-    """Per-phase split of one traced decode step, averaged over CTAs."""
+    """Per-layer split of one traced decode step, averaged over CTAs: barrier wait
+    and x, own routing, gate/up, pair exchange, act, down (to the barrier
+    arrival), head."""
     import collections
+    names = ("wait+x", "route", "gate/up", "xchg", "act", "down", "head")
     acc = collections.defaultdict(list)
     for c in range(nct):
         ev = {}
@@ -314,22 +300,20 @@ def print_trace(tr, nct):
             if tm == 0:
                 break
             ev[tag] = tm
-        keys = sorted({k >> 4 for k in ev})
-        for k in keys:
-            pts = [ev.get((k << 4) | i) for i in range(5)]
+        for l in sorted({k >> 8 for k in ev}):
+            pts = [ev.get((l << 8) | i) for i in range(8)]
             if None in pts:
                 continue
-            acc[k].append(tuple(pts[i + 1] - pts[i] for i in range(4)))
-    names = ("prologue", "chunks", "flush", "barrier")
-    tot = [0.0] * 4
+            acc[l].append(tuple(pts[i + 1] - pts[i] for i in range(7)))
+    tot = [0.0] * 7
     lines = []
-    for k in sorted(acc):
-        v = acc[k]
-        m = [statistics.mean(x[i] for x in v) / 1e3 for i in range(4)]
-        mx = [max(x[i] for x in v) / 1e3 for i in range(4)]
+    for l in sorted(acc):
+        v = acc[l]
+        m = [statistics.mean(x[i] for x in v) / 1e3 for i in range(7)]
+        mx = [max(x[i] for x in v) / 1e3 for i in range(7)]
         tot = [a + b for a, b in zip(tot, m)]
-        lines.append(f"layer {k >> 4:2d} phase {'RAB'[k & 15]}: " +
-                     " ".join(f"{n} {a:6.2f}/{b:6.2f}" for n, a, b in zip(names, m, mx)) + " us (mean/max)")
+        lines.append(f"layer {l:2d}: " + " ".join(f"{n} {a:5.2f}/{b:5.2f}" for n, a, b in zip(names, m, mx))
+                     + " us (mean/max)")
     sys.stderr.write("\n".join(lines) + "\n")
     sys.stderr.write("total (mean over CTAs): " + " ".join(f"{n} {a:.1f}" for n, a in zip(names, tot)) + " us\n")
 
@@ -427,8 +411,6 @@ def main():
     ap.add_argument("--experts", type=int, default=0, help="reduced case for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", action="store_true", help="print a per-phase split of one step")
-    ap.add_argument("--trace-detail", type=int, default=None,
-                    help="print per-chunk stamps of layers N, N+1 for a few CTAs")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

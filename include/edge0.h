@@ -35,14 +35,20 @@
  *   of word j is input 8j+i, low nibble first), s and b fp16 [out, in/64],
  *   w = s*q + b; experts stacked on a leading [E] axis.  Dense fp16 weights are
  *   nn.Linear [out, in] row-major.
- *   Packed (this library's HBM layout): rows are taken 16 at a time ("row tile",
- *   padded with zero rows), inputs 64 at a time ("group"); one (row tile, group)
- *   "unit" is stored contiguously in the order one warp's tensor-core fragments
- *   read it, so a warp streams each unit as one 512-byte burst.
- *     int4 unit: 576 bytes = 512 bytes of nibbles + 64 bytes of scales/biases.
- *     fp16 unit: 2048 bytes.
- *   Units run group-fastest within a row tile, row tiles follow each other, and
- *   experts follow each other.  Use edge0_pack_* to convert canonical weights.
+ *   Packed (this library's HBM layout, written by edge0_pack_*): rows are taken 16
+ *   at a time ("row tile", padded with zero rows) and inputs 16 at a time
+ *   ("step"); a (row tile, step) block is stored in the order the 32 lanes of a
+ *   warp read it as the A operand of one m16n8k16 tensor-core step (int4: 4
+ *   bytes per lane, 128 bytes; fp16: 16 bytes per lane, 512 bytes).  int4 scale
+ *   and bias pairs of a row tile and group of 64 inputs take 64 bytes.
+ *     gate/up  (edge0_pack_q4_gate_up): one interleaved matrix per expert whose
+ *              row tile j holds gate rows 8j..8j+7 then up rows 8j..8j+7;
+ *              per row tile and group a 576-byte unit (4 step blocks + scales).
+ *     down     (edge0_pack_q4_down): K-major; per group of 64 inputs, the four
+ *              step blocks of every row tile, then the scales of every row tile.
+ *     fp16     (edge0_pack_f16): row-tile major, 2048 bytes per row tile and
+ *              group; (edge0_pack_f16_kmajor): step major.
+ *   Experts follow each other in the stacks.
  */
 #ifndef EDGE0_H
 #define EDGE0_H
@@ -86,12 +92,10 @@ typedef struct {
 /* ---- routed + shared int4 experts ---- */
 typedef struct {
     int d, E, K, I, Is;        /* d_model, experts, top-k, expert and shared intermediate */
-    const void* gate;          /* packed int4 [E][I x d]   (edge0_pack_q4)            */
-    const void* up;            /* packed int4 [E][I x d]                               */
-    const void* down;          /* packed int4 [E][d x I]                               */
-    const void* sh_gate;       /* packed int4 [Is x d], or NULL for no shared expert   */
-    const void* sh_up;         /* packed int4 [Is x d]                                 */
-    const void* sh_down;       /* packed int4 [d x Is]                                 */
+    const void* gate_up;       /* packed int4 [E][gate | up interleaved]  (edge0_pack_q4_gate_up) */
+    const void* down;          /* packed int4 [E][d x I] K-major          (edge0_pack_q4_down)    */
+    const void* sh_gate_up;    /* shared expert, same layouts, or NULL for no shared expert     */
+    const void* sh_down;
     const int32_t* slot_table; /* [E] expert id -> slot in the stacks above, or NULL   */
     int n_slots;               /* slots in the stacks when slot_table != NULL (a slot
                                   outside [0, n_slots) makes the kernel record EDGE0_EINVAL) */
@@ -99,9 +103,12 @@ typedef struct {
 
 /* ---- one unmerged LoRA projection [S3.3]: y += (alpha/r) B (A v) ---- */
 typedef struct {
-    int r, in, out;
+    int r, in, out;            /* rank (at most 16), input and output width            */
     float alpha;
-    const void* A;             /* packed fp16 [r x in]  (edge0_pack_f16)               */
+    const void* A;             /* packed fp16 [r x in]  (edge0_pack_f16); used for the
+                                  shared expert's gate and up projections              */
+    const uint16_t* A_T;       /* fp16 [in, r] = A transposed, row-major; used for the
+                                  shared expert's down projection and edge0_lora_delta */
     const uint16_t* B;         /* fp16 [out, r] row-major                              */
 } edge0_lora_desc;
 
@@ -110,7 +117,7 @@ typedef struct {
     int d, E, H, K;
     const void* fc1_dense;     /* packed fp16 [H x d]: fc1[:, :d]                      */
     const uint16_t* fc1_oh_T;  /* fp16 [2E, H]: row j = fc1[:, d + j] (edge0_pack_cols_T) */
-    const void* fc2;           /* packed fp16 [E x H]                                  */
+    const void* fc2;           /* packed fp16 [E x H] K-major (edge0_pack_f16_kmajor)  */
     const void* linit_dense;   /* packed fp16 [E x d]: linear_init[:, :d]              */
     const uint16_t* linit_oh_T;/* fp16 [2E, E]: row j = linear_init[:, d + j]          */
     edge0_route route;         /* routing rule of the layer whose routing it predicts  */
@@ -135,17 +142,14 @@ typedef struct {
  * pred_ids/pred_w [2][L][B][K]: slot (t & 1) holds the predictions made at step t
  *   (consumed at t + 1); exec_ids [2][L][B][K]: slot (t & 1) holds the ids each
  *   layer executed at step t (the head's executed mask at t, previous mask at t+1).
- * workspace: device scratch of edge0_workspace_bytes(d, E, K, I, Is, H, r, B)
- *   bytes, zeroed by edge0_state_init before first use; it holds accumulators,
- *   the residual stream between layers, the grid barrier and the error word.
- *   Its layout depends on H and r, so the state records them: every layer run on
- *   this state must have head width H (if it owns a head) and LoRA rank r (if it
- *   has LoRA).  A workspace belongs to one kind of call (decode on this state,
+ * workspace: device scratch of edge0_workspace_bytes(L, B, d, E) bytes, zeroed by
+ *   edge0_state_init before first use; it holds the layer-output and logit
+ *   accumulators of two step parities, the grid barrier and the error word.  A
+ *   workspace belongs to one kind of call (decode on this state,
  *   edge0_moe_int4_forward, or edge0_prerouter_topk): calls of different kinds
  *   must not share one. */
 typedef struct {
     int L, B, K;
-    int H, r;
     int32_t* pred_ids;
     float* pred_w;
     int32_t* exec_ids;
@@ -154,19 +158,28 @@ typedef struct {
 } edge0_route_state;
 
 /* ---- packing (device -> device, enqueued on stream) ---- */
-size_t edge0_q4_packed_bytes(int E, int out, int in);
-/* q [E, out, in/8] uint32, s/b [E, out, in/64] fp16 -> packed int4 units */
-int edge0_pack_q4(const uint32_t* q, const uint16_t* s, const uint16_t* b, int E, int out, int in,
-                  void* packed, cudaStream_t stream);
+size_t edge0_q4_gate_up_packed_bytes(int E, int I, int d);
+/* gate and up q [E, I, d/8] uint32, s/b [E, I, d/64] fp16 -> one interleaved matrix per expert */
+int edge0_pack_q4_gate_up(const uint32_t* q_gate, const uint16_t* s_gate, const uint16_t* b_gate,
+                          const uint32_t* q_up, const uint16_t* s_up, const uint16_t* b_up, int E,
+                          int I, int d, void* packed, cudaStream_t stream);
+size_t edge0_q4_down_packed_bytes(int E, int out, int in);
+/* q [E, out, in/8] uint32, s/b [E, out, in/64] fp16 -> K-major packed int4 */
+int edge0_pack_q4_down(const uint32_t* q, const uint16_t* s, const uint16_t* b, int E, int out,
+                       int in, void* packed, cudaStream_t stream);
 size_t edge0_f16_packed_bytes(int out, int in);
 /* W [out, in] fp16 with row stride ld elements (use ld > in for a column slice) */
 int edge0_pack_f16(const uint16_t* W, int out, int in, int ld, void* packed, cudaStream_t stream);
+int edge0_pack_f16_kmajor(const uint16_t* W, int out, int in, int ld, void* packed,
+                          cudaStream_t stream);
 /* dst [ncols, out] = transpose of W[:, col0 : col0 + ncols] (W row stride ld) */
 int edge0_pack_cols_T(const uint16_t* W, int out, int ld, int col0, int ncols, uint16_t* dst,
                       cudaStream_t stream);
 
 /* ---- state ---- */
-size_t edge0_workspace_bytes(int d, int E, int K, int I, int Is, int H, int r, int B);
+/* workspace of a state of L layers (L = 1 for edge0_moe_int4_forward and
+ * edge0_prerouter_topk) for B sequences */
+size_t edge0_workspace_bytes(int L, int B, int d, int E);
 /* zero pred/exec/workspace; must precede the first decode call on a state */
 int edge0_state_init(edge0_route_state* st, cudaStream_t stream);
 /* HOST call: synchronises `stream`, returns the kernels' recorded status (EDGE0_OK,
@@ -181,8 +194,8 @@ int edge0_state_error(const edge0_route_state* st, cudaStream_t stream, int* sta
  * NULL (no previous token: zero mask).  Writes the predicted routing for the
  * head's target layer: out_ids [B, K] (score-descending, lower id first on ties),
  * out_w [B, K]; out_logits [B, E] (optional, NULL to skip) the head's fp32 logits.
- * workspace: scratch of edge0_workspace_bytes(d, E, K, 64, 64, H, 16, B) bytes,
- * zeroed before its first use (cudaMemset). */
+ * workspace: scratch of edge0_workspace_bytes(1, B, d, E) bytes, zeroed before its
+ * first use (cudaMemset). */
 int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t* x, const int32_t* exec_ids,
                          const int32_t* prev_ids, int B, int32_t* out_ids, float* out_w,
                          float* out_logits, void* workspace, size_t workspace_bytes,
@@ -191,13 +204,14 @@ int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t* x, const i
 /* Routed + shared int4 SwiGLU experts [S3.1 "Math contract"], no LoRA:
  * y_b = sum_k w[b,k] expert_{ids[b,k]}(x_b) + shared(x_b).
  * x [B, d] fp16; ids [B, K] int32 (0 <= id < E); w [B, K] fp32; y [B, d] fp16.
- * workspace as for edge0_prerouter_topk (edge0_workspace_bytes(d, E, K, I, Is, 64, 16, B)). */
+ * workspace as for edge0_prerouter_topk (edge0_workspace_bytes(1, B, d, E)). */
 int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t* x, const int32_t* ids,
                            const float* w, int B, uint16_t* y, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
 /* Unmerged LoRA delta [S3.3]: y[b] += (alpha/r) B (A v[b]) for v [B, in] fp16,
- * y [B, out] fp16 (read, add in fp32, round to fp16).  Needs no workspace. */
+ * y [B, out] fp16 (read, add in fp32, round to fp16); reads lora->A_T and lora->B.
+ * Needs no workspace. */
 int edge0_lora_delta(const edge0_lora_desc* lora, const uint16_t* v, int B, uint16_t* y_inout,
                      cudaStream_t stream);
 
@@ -225,14 +239,15 @@ int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
  * the library, present in every GPU that loads it until the process exits.  The
  * call allocates nothing (no cudaMalloc, no host heap); it clears the part of
  * the array it uses before launching.
- *   - Shapes whose scratch would exceed the array return EDGE0_EUNSUPPORTED
- *     (at d=2048, E=256, K=4, I=Is=512 the need is about 420 KB at B=4).
+ *   - The call needs 512 + 8 B d + 16 B E bytes of it (about 80 KB at d=2048,
+ *     E=256, B=4); shapes whose need exceeds the array (d=4096, E=512, B=4)
+ *     return EDGE0_EUNSUPPORTED.
  *   - The first call on a device looks up the array's device address for that
  *     device (cudaGetSymbolAddress); make that first call before any stream
  *     capture.
  *   - All calls share the array: two calls whose kernels overlap on the GPU (for
  *     instance on different streams) race and give wrong results. */
-#define EDGE0_NOALLOC_SCRATCH_BYTES (1 << 20)
+#define EDGE0_NOALLOC_SCRATCH_BYTES (1 << 17)
 int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const uint16_t* x,
                                    const int32_t* ids, const float* w, int B, uint16_t* y,
                                    cudaStream_t stream);

@@ -46,13 +46,13 @@ class Route(C.Structure):
 
 class MoeDesc(C.Structure):
     _fields_ = [("d", C.c_int), ("E", C.c_int), ("K", C.c_int), ("I", C.c_int), ("Is", C.c_int),
-                ("gate", P), ("up", P), ("down", P), ("sh_gate", P), ("sh_up", P), ("sh_down", P),
+                ("gate_up", P), ("down", P), ("sh_gate_up", P), ("sh_down", P),
                 ("slot_table", P), ("n_slots", C.c_int)]
 
 
 class LoraDesc(C.Structure):
     _fields_ = [("r", C.c_int), ("in_", C.c_int), ("out", C.c_int), ("alpha", C.c_float),
-                ("A", P), ("B", P)]
+                ("A", P), ("A_T", P), ("B", P)]
 
 
 class HeadDesc(C.Structure):
@@ -69,7 +69,7 @@ class LayerDesc(C.Structure):
 
 
 class RouteState(C.Structure):
-    _fields_ = [("L", C.c_int), ("B", C.c_int), ("K", C.c_int), ("H", C.c_int), ("r", C.c_int),
+    _fields_ = [("L", C.c_int), ("B", C.c_int), ("K", C.c_int),
                 ("pred_ids", P), ("pred_w", P), ("exec_ids", P), ("workspace", P),
                 ("workspace_bytes", C.c_size_t)]
 
@@ -77,14 +77,18 @@ class RouteState(C.Structure):
 def _declare(L):
     L.edge0_status_string.argtypes = [C.c_int]
     L.edge0_status_string.restype = C.c_char_p
-    L.edge0_q4_packed_bytes.argtypes = [C.c_int] * 3
-    L.edge0_q4_packed_bytes.restype = C.c_size_t
-    L.edge0_pack_q4.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, P, P]
+    L.edge0_q4_gate_up_packed_bytes.argtypes = [C.c_int] * 3
+    L.edge0_q4_gate_up_packed_bytes.restype = C.c_size_t
+    L.edge0_pack_q4_gate_up.argtypes = [P, P, P, P, P, P, C.c_int, C.c_int, C.c_int, P, P]
+    L.edge0_q4_down_packed_bytes.argtypes = [C.c_int] * 3
+    L.edge0_q4_down_packed_bytes.restype = C.c_size_t
+    L.edge0_pack_q4_down.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, P, P]
     L.edge0_f16_packed_bytes.argtypes = [C.c_int] * 2
     L.edge0_f16_packed_bytes.restype = C.c_size_t
     L.edge0_pack_f16.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
+    L.edge0_pack_f16_kmajor.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
     L.edge0_pack_cols_T.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, P, P]
-    L.edge0_workspace_bytes.argtypes = [C.c_int] * 8
+    L.edge0_workspace_bytes.argtypes = [C.c_int] * 4
     L.edge0_workspace_bytes.restype = C.c_size_t
     L.edge0_state_init.argtypes = [C.POINTER(RouteState), P]
     L.edge0_state_error.argtypes = [C.POINTER(RouteState), P, C.POINTER(C.c_int)]
@@ -97,15 +101,18 @@ def _declare(L):
                                      C.c_int, P]
     L.edge0_decode_step.argtypes = [C.POINTER(LayerDesc), C.c_int, P, C.POINTER(RouteState),
                                     C.c_int, C.c_int, P]
-    for name in ("edge0_pack_q4", "edge0_pack_f16", "edge0_pack_cols_T", "edge0_state_init",
+    for name in ("edge0_pack_q4_gate_up", "edge0_pack_q4_down", "edge0_pack_f16",
+                 "edge0_pack_f16_kmajor", "edge0_pack_cols_T", "edge0_state_init",
                  "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
                  "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
                  "edge0_moe_int4_forward_noalloc"):
         getattr(L, name).restype = C.c_int
 
 
-EXPORTED = ["edge0_status_string", "edge0_q4_packed_bytes", "edge0_pack_q4", "edge0_f16_packed_bytes",
-            "edge0_pack_f16", "edge0_pack_cols_T", "edge0_workspace_bytes", "edge0_state_init",
+EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_q4_gate_up",
+            "edge0_q4_down_packed_bytes", "edge0_pack_q4_down", "edge0_f16_packed_bytes",
+            "edge0_pack_f16", "edge0_pack_f16_kmajor", "edge0_pack_cols_T",
+            "edge0_workspace_bytes", "edge0_state_init",
             "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
             "edge0_moe_int4_forward_noalloc"]
@@ -130,38 +137,55 @@ def _stream(stream=None):
 
 
 # ------------------------------------------------------------ packing ----
-def pack_q4(q, s, b, stream=None) -> torch.Tensor:
-    """q [E, out, in/8] int32, s/b [E, out, in/64] fp16 (device) -> packed uint8 buffer."""
-    E, out, w8 = q.shape
-    inp = w8 * 8
-    n = lib().edge0_q4_packed_bytes(E, out, inp)
-    dst = torch.empty(n, dtype=torch.uint8, device=q.device)
-    _check(lib().edge0_pack_q4(_ptr(q.contiguous()), _ptr(s.contiguous()), _ptr(b.contiguous()),
-                               E, out, inp, _ptr(dst), _stream(stream)), "edge0_pack_q4")
+def pack_q4_gate_up(gate, up, stream=None) -> torch.Tensor:
+    """gate, up: (q [E, I, d/8] int32, s, b [E, I, d/64] fp16) on the device ->
+    packed interleaved gate/up (uint8)."""
+    qg, sg, bg = (t.contiguous() for t in gate)
+    qu, su, bu = (t.contiguous() for t in up)
+    E, I, w8 = qg.shape
+    d = w8 * 8
+    n = lib().edge0_q4_gate_up_packed_bytes(E, I, d)
+    dst = torch.empty(n, dtype=torch.uint8, device=qg.device)
+    _check(lib().edge0_pack_q4_gate_up(_ptr(qg), _ptr(sg), _ptr(bg), _ptr(qu), _ptr(su), _ptr(bu),
+                                       E, I, d, _ptr(dst), _stream(stream)), "edge0_pack_q4_gate_up")
     return dst
 
 
-def pack_f16(W, ld=None, cols=None, stream=None) -> torch.Tensor:
-    """W [out, ld] fp16 (device); packs W[:, :cols]."""
+def pack_q4_down(trip, stream=None) -> torch.Tensor:
+    """(q [E, out, in/8] int32, s, b [E, out, in/64] fp16) -> packed K-major int4 (uint8)."""
+    q, s, b = (t.contiguous() for t in trip)
+    E, out, w8 = q.shape
+    inp = w8 * 8
+    n = lib().edge0_q4_down_packed_bytes(E, out, inp)
+    dst = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check(lib().edge0_pack_q4_down(_ptr(q), _ptr(s), _ptr(b), E, out, inp, _ptr(dst), _stream(stream)),
+           "edge0_pack_q4_down")
+    return dst
+
+
+def pack_f16(W, cols=None, stream=None, kmajor=False) -> torch.Tensor:
+    """W [out, ld] fp16 (device); packs W[:, :cols] row-tile major (or K-major)."""
+    W = W.contiguous()
     out, full = W.shape
     inp = cols if cols is not None else full
     n = lib().edge0_f16_packed_bytes(out, inp)
     dst = torch.empty(n, dtype=torch.uint8, device=W.device)
-    _check(lib().edge0_pack_f16(_ptr(W.contiguous()), out, inp, full, _ptr(dst), _stream(stream)),
-           "edge0_pack_f16")
+    fn = lib().edge0_pack_f16_kmajor if kmajor else lib().edge0_pack_f16
+    _check(fn(_ptr(W), out, inp, full, _ptr(dst), _stream(stream)), "edge0_pack_f16")
     return dst
 
 
 def pack_cols_T(W, col0, ncols, stream=None) -> torch.Tensor:
+    W = W.contiguous()
     out, ld = W.shape
     dst = torch.empty(ncols, out, dtype=torch.float16, device=W.device)
-    _check(lib().edge0_pack_cols_T(_ptr(W.contiguous()), out, ld, col0, ncols, _ptr(dst),
-                                   _stream(stream)), "edge0_pack_cols_T")
+    _check(lib().edge0_pack_cols_T(_ptr(W), out, ld, col0, ncols, _ptr(dst), _stream(stream)),
+           "edge0_pack_cols_T")
     return dst
 
 
-def workspace_bytes(d, E, K, I, Is, H, r, B) -> int:
-    return int(lib().edge0_workspace_bytes(d, E, K, I, Is, H, r, B))
+def workspace_bytes(L, B, d, E) -> int:
+    return int(lib().edge0_workspace_bytes(L, B, d, E))
 
 
 # ------------------------------------------------------------ the model ----
@@ -197,18 +221,21 @@ class DeviceModel:
         d, E, K, I, Is, H, r = cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.H, cfg.r
         g = lambda t: t.to(dev)
         L = LayerDesc()
-        pq = lambda trip: pack_q4(g(trip[0]), g(trip[1]), g(trip[2]), stream)
-        L.moe = MoeDesc(d, E, K, I, Is, self._k(pq(lw.gate)), self._k(pq(lw.up)), self._k(pq(lw.down)),
-                        self._k(pq(lw.sh_gate)), self._k(pq(lw.sh_up)), self._k(pq(lw.sh_down)),
+        gt = lambda trip: tuple(g(t) for t in trip)
+        L.moe = MoeDesc(d, E, K, I, Is,
+                        self._k(pack_q4_gate_up(gt(lw.gate), gt(lw.up), stream)),
+                        self._k(pack_q4_down(gt(lw.down), stream)),
+                        self._k(pack_q4_gate_up(gt(lw.sh_gate), gt(lw.sh_up), stream)),
+                        self._k(pack_q4_down(gt(lw.sh_down), stream)),
                         None, 0)
         lo = lw.lora
         alpha = float(cfg.alpha)
-        L.lora_gate = LoraDesc(r, d, Is, alpha, self._k(pack_f16(g(lo["Ag"]), stream=stream)),
-                               self._k(g(lo["Bg"]).contiguous()))
-        L.lora_up = LoraDesc(r, d, Is, alpha, self._k(pack_f16(g(lo["Au"]), stream=stream)),
-                             self._k(g(lo["Bu"]).contiguous()))
-        L.lora_down = LoraDesc(r, Is, d, alpha, self._k(pack_f16(g(lo["Ad"]), stream=stream)),
-                               self._k(g(lo["Bd"]).contiguous()))
+        lora = lambda A, Bm, inp, out: LoraDesc(
+            r, inp, out, alpha, self._k(pack_f16(g(A), stream=stream)),
+            self._k(g(A).t().contiguous()), self._k(g(Bm).contiguous()))
+        L.lora_gate = lora(lo["Ag"], lo["Bg"], d, Is)
+        L.lora_up = lora(lo["Au"], lo["Bu"], d, Is)
+        L.lora_down = lora(lo["Ad"], lo["Bd"], Is, d)
         L.router = self._k(pack_f16(g(lw.router), stream=stream))
         L.route = _route(cfg, self.biases[l])
         L.gamma = self._k(g(lw.gamma).contiguous())
@@ -223,7 +250,7 @@ class DeviceModel:
             L.head_target = tgt
             L.head = HeadDesc(d, E, H, K, self._k(pack_f16(fc1, cols=d, stream=stream)),
                               self._k(pack_cols_T(fc1, d, 2 * E, stream)),
-                              self._k(pack_f16(fc2, stream=stream)),
+                              self._k(pack_f16(fc2, stream=stream, kmajor=True)),
                               self._k(pack_f16(linit, cols=d, stream=stream)),
                               self._k(pack_cols_T(linit, d, 2 * E, stream)),
                               _route(cfg, self.biases[tgt]))
@@ -240,28 +267,27 @@ class DecodeState:
         self.pred_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
         self.pred_w = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.float32, device=dev)
         self.exec_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
-        nbytes = workspace_bytes(cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.H, cfg.r, B)
+        nbytes = workspace_bytes(cfg.L, B, cfg.d, cfg.E)
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
-        self.st = RouteState(cfg.L, B, cfg.K, cfg.H, cfg.r, _ptr(self.pred_ids), _ptr(self.pred_w),
+        self.st = RouteState(cfg.L, B, cfg.K, _ptr(self.pred_ids), _ptr(self.pred_w),
                              _ptr(self.exec_ids), _ptr(self.workspace), nbytes)
         _check(lib().edge0_state_init(C.byref(self.st), _stream(stream)), "edge0_state_init")
 
     TRACE_CTAS, TRACE_SLOTS = 160, 1024
 
-    def set_trace(self, on, detail_layer=None):
-        """Switch the engine's phase trace on/off (workspace header flag); with
-        detail_layer, also per-chunk stamps for layers detail_layer, detail_layer + 1."""
+    def set_trace(self, on):
+        """Switch the engine's per-layer trace on/off (workspace header flag)."""
         torch.cuda.synchronize(self.workspace.device)
-        mode = 0 if not on else (1 if detail_layer is None else detail_layer + 2)
-        flag = torch.tensor([mode], dtype=torch.int32)
+        flag = torch.tensor([1 if on else 0], dtype=torch.int32)
         self.workspace[24:28].copy_(flag.view(torch.uint8))
         if on:
             self.workspace[-self.TRACE_CTAS * self.TRACE_SLOTS * 8:].zero_()
         torch.cuda.synchronize(self.workspace.device)
 
     def read_trace(self):
-        """[CTAs, events, 2] int64: (tag, globaltimer ns) pairs, tag = layer << 8 |
-        phase << 4 | point (0 start, 1 prologue done, 2 chunks done, 3 barrier done)."""
+        """[CTAs, events, 2] int64: (tag, globaltimer ns) pairs, tag = layer << 8 | point
+        (0 start, 1 x built, 2 routed, 3 gate/up done, 4 exchange done, 5 act done,
+        6 down done + barrier arrival, 7 head done)."""
         torch.cuda.synchronize(self.workspace.device)
         raw = self.workspace[-self.TRACE_CTAS * self.TRACE_SLOTS * 8:].cpu().view(torch.int64)
         return raw.view(self.TRACE_CTAS, self.TRACE_SLOTS // 2, 2)

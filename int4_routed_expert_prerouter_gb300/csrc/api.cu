@@ -29,15 +29,9 @@ int check_dims(const Dims& D, int B) {
     if (D.d <= 0 || D.d % kGroup || D.I <= 0 || D.I % kGroup || D.Is <= 0 || D.Is % kGroup)
         return EDGE0_EINVAL;
     if (D.H <= 0 || D.H % kGroup) return EDGE0_EINVAL;
-    if (D.E <= 0 || D.E > EDGE0_MAX_E || D.E % 8) return EDGE0_EINVAL;
+    if (D.E <= 0 || D.E > EDGE0_MAX_E || D.E % 16) return EDGE0_EINVAL;
     if (D.K <= 0 || D.K > EDGE0_MAX_K || D.K > D.E) return EDGE0_EINVAL;
-    if (D.r <= 0 || D.r > 32) return EDGE0_EINVAL;
-    // what one shared-memory stage must hold
-    if ((long long)D.Is * D.r * 2 > kStageBytes) return EDGE0_EUNSUPPORTED;
-    if (f16_bytes(D.r, D.Is) > kStageBytes) return EDGE0_EUNSUPPORTED;
-    if (2LL * D.K * D.H * 2 > kStageBytes || 2LL * D.K * D.E * 2 > kStageBytes)
-        return EDGE0_EUNSUPPORTED;
-    if (2 * B * D.K + 8 > kMaxSeg) return EDGE0_EUNSUPPORTED;
+    if (D.r <= 0 || D.r > 16) return EDGE0_EINVAL;
     return EDGE0_OK;
 }
 
@@ -52,45 +46,44 @@ void route_into(const edge0_route& r, int* kind, int* ng, int* tg, float* sc, co
 int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P) {
     const edge0_moe_desc& m = Ld.moe;
     if (m.d != D.d || m.E != D.E || m.K != D.K || m.I != D.I || m.Is != D.Is) return EDGE0_EINVAL;
-    if (!m.gate || !m.up || !m.down || !Ld.router) return EDGE0_EINVAL;
-    if (!al16(m.gate) || !al16(m.up) || !al16(m.down) || !al16(Ld.router)) return EDGE0_EINVAL;
+    if (!m.gate_up || !m.down || !Ld.router) return EDGE0_EINVAL;
+    if (!al16(m.gate_up) || !al16(m.down) || !al16(Ld.router)) return EDGE0_EINVAL;
     if (m.slot_table && m.n_slots <= 0) return EDGE0_EINVAL;
     memset(&P, 0, sizeof(P));
-    P.gate = (const char*)m.gate;
-    P.up = (const char*)m.up;
+    P.gu = (const char*)m.gate_up;
     P.down = (const char*)m.down;
     P.slot_table = m.slot_table;
     P.n_slots = m.slot_table ? m.n_slots : m.E;
     P.router = (const char*)Ld.router;
     P.gamma = (const __half*)Ld.gamma;
+    if (Ld.gamma && ((uintptr_t)Ld.gamma & 7)) return EDGE0_EINVAL;
     P.eps = Ld.eps;
     int rc = check_route(Ld.route, D.E, D.K);
     if (rc) return rc;
     route_into(Ld.route, &P.route_kind, &P.n_groups, &P.topk_groups, &P.route_scale, &P.bias);
     int flags = 0;
     if (Ld.prerouted) flags |= LF_PREROUTED;
-    if (m.sh_gate || m.sh_up || m.sh_down) {
-        if (!m.sh_gate || !m.sh_up || !m.sh_down) return EDGE0_EINVAL;
-        if (!al16(m.sh_gate) || !al16(m.sh_up) || !al16(m.sh_down)) return EDGE0_EINVAL;
-        P.sh_gate = (const char*)m.sh_gate;
-        P.sh_up = (const char*)m.sh_up;
+    if (m.sh_gate_up || m.sh_down) {
+        if (!m.sh_gate_up || !m.sh_down) return EDGE0_EINVAL;
+        if (!al16(m.sh_gate_up) || !al16(m.sh_down)) return EDGE0_EINVAL;
+        P.sh_gu = (const char*)m.sh_gate_up;
         P.sh_down = (const char*)m.sh_down;
         flags |= LF_SHARED;
     }
     const edge0_lora_desc &lg = Ld.lora_gate, &lu = Ld.lora_up, &ld = Ld.lora_down;
-    if (lg.A || lu.A || ld.A) {
+    if (lg.A || lu.A || ld.A_T) {
         if (!(flags & LF_SHARED)) return EDGE0_EINVAL;
-        if (!lg.A || !lu.A || !ld.A || !lg.B || !lu.B || !ld.B) return EDGE0_EINVAL;
+        if (!lg.A || !lu.A || !ld.A_T || !lg.B || !lu.B || !ld.B) return EDGE0_EINVAL;
         if (lg.r != D.r || lu.r != D.r || ld.r != D.r) return EDGE0_EINVAL;
         if (lg.in != D.d || lg.out != D.Is || lu.in != D.d || lu.out != D.Is || ld.in != D.Is ||
             ld.out != D.d)
             return EDGE0_EINVAL;
         if (lg.alpha != lu.alpha || lg.alpha != ld.alpha) return EDGE0_EINVAL;
-        if (!al16(lg.A) || !al16(lu.A) || !al16(ld.A) || !al16(lg.B) || !al16(lu.B) || !al16(ld.B))
+        if (!al16(lg.A) || !al16(lu.A) || !al16(ld.A_T) || !al16(lg.B) || !al16(lu.B) || !al16(ld.B))
             return EDGE0_EINVAL;
         P.lora_Ag = (const char*)lg.A;
         P.lora_Au = (const char*)lu.A;
-        P.lora_Ad = (const char*)ld.A;
+        P.lora_AdT = (const __half*)ld.A_T;
         P.lora_Bg = (const __half*)lg.B;
         P.lora_Bu = (const __half*)lu.B;
         P.lora_Bd = (const __half*)ld.B;
@@ -124,35 +117,6 @@ int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P)
     return EDGE0_OK;
 }
 
-int launch(const Prog& p, cudaStream_t stream) {
-    int dev = 0, nsm = 0, maxsm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return EDGE0_ECUDA;
-    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return EDGE0_ECUDA;
-    if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-        return EDGE0_ECUDA;
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, engine_kernel) != cudaSuccess) return EDGE0_ECUDA;
-    const int smem = engine_smem_bytes(p);
-    if (smem + (int)fa.sharedSizeBytes > maxsm) return EDGE0_EUNSUPPORTED;
-    if (cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return EDGE0_ECUDA;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(nsm);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, engine_kernel, p) != cudaSuccess) return EDGE0_ECUDA;
-    return EDGE0_OK;
-}
-
 void set_dims(Prog& p, const Dims& D, int B) {
     p.B = B;
     p.d = D.d;
@@ -164,9 +128,9 @@ void set_dims(Prog& p, const Dims& D, int B) {
     p.r = D.r;
 }
 
-int check_ws(const Dims& D, int B, const void* ws, size_t bytes) {
+int check_ws(int Ls, const Dims& D, int B, const void* ws, size_t bytes) {
     if (!ws || !al16(ws)) return EDGE0_EINVAL;
-    if ((long long)bytes < ws_bytes(B, D.K, D.I, D.Is, D.r, D.H, D.E, D.d)) return EDGE0_EINVAL;
+    if ((long long)bytes < ws_layout(Ls, B, D.d, D.E).total) return EDGE0_EINVAL;
     return EDGE0_OK;
 }
 
@@ -182,16 +146,16 @@ int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_rout
     D.K = layers[0].moe.K;
     D.I = layers[0].moe.I;
     D.Is = layers[0].moe.Is;
-    // the workspace layout is fixed by the state's dims, whatever this call runs
-    D.H = st->H;
-    D.r = st->r;
-    for (int l = 0; l < L; ++l) {
-        if (layers[l].has_head && layers[l].head.H != D.H) return EDGE0_EINVAL;
-        if (layers[l].lora_gate.A && layers[l].lora_gate.r != D.r) return EDGE0_EINVAL;
-    }
+    // every head of one call has one width, every LoRA one rank
+    D.H = 64;
+    D.r = 16;
+    for (int l = 0; l < L; ++l)
+        if (layers[l].has_head) { D.H = layers[l].head.H; break; }
+    for (int l = 0; l < L; ++l)
+        if (layers[l].lora_gate.A) { D.r = layers[l].lora_gate.r; break; }
     int rc = check_dims(D, B);
     if (rc) return rc;
-    rc = check_ws(D, B, st->workspace, st->workspace_bytes);
+    rc = check_ws(st->L, D, B, st->workspace, st->workspace_bytes);
     if (rc) return rc;
     static_assert(sizeof(Prog) <= 32000, "kernel parameter block too large");
     Prog* p = new Prog;
@@ -207,7 +171,7 @@ int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_rout
     p->Ls = st->L;
     p->ws = (char*)st->workspace;
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) rc = fill_layer(layers[l], D, st->L, p->layers[l]);
-    if (rc == EDGE0_OK) rc = launch(*p, stream);
+    if (rc == EDGE0_OK) rc = engine_launch(*p, stream);
     delete p;
     return rc;
 }
@@ -225,14 +189,14 @@ extern "C" const char* edge0_status_string(int status) {
     }
 }
 
-extern "C" size_t edge0_workspace_bytes(int d, int E, int K, int I, int Is, int H, int r, int B) {
-    if (d <= 0 || E <= 0 || K <= 0 || I <= 0 || Is <= 0 || H <= 0 || r <= 0 || B <= 0) return 0;
-    return (size_t)ws_bytes(B, K, I, Is, r, H, E, d);
+extern "C" size_t edge0_workspace_bytes(int L, int B, int d, int E) {
+    if (L <= 0 || B <= 0 || d <= 0 || E <= 0) return 0;
+    return (size_t)ws_layout(L, B, d, E).total;
 }
 
 extern "C" int edge0_state_init(edge0_route_state* st, cudaStream_t stream) {
     if (!st || !st->pred_ids || !st->pred_w || !st->exec_ids || !st->workspace) return EDGE0_EINVAL;
-    if (st->L <= 0 || st->B <= 0 || st->K <= 0 || st->H <= 0 || st->r <= 0) return EDGE0_EINVAL;
+    if (st->L <= 0 || st->B <= 0 || st->K <= 0) return EDGE0_EINVAL;
     const size_t n = (size_t)2 * st->L * st->B * st->K;
     if (cudaMemsetAsync(st->pred_ids, 0, n * 4, stream) != cudaSuccess) return EDGE0_ECUDA;
     if (cudaMemsetAsync(st->pred_w, 0, n * 4, stream) != cudaSuccess) return EDGE0_ECUDA;
@@ -277,25 +241,25 @@ extern "C" int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t*
                                       void* workspace, size_t workspace_bytes,
                                       cudaStream_t stream) {
     if (!moe || !x || !ids || !w || !y) return EDGE0_EINVAL;
-    if (!moe->gate || !moe->up || !moe->down) return EDGE0_EINVAL;
+    if (!moe->gate_up || !moe->down) return EDGE0_EINVAL;
     if (!al16(x) || !al16(y)) return EDGE0_EINVAL;
     Dims D{moe->d, moe->E, moe->K, moe->I, moe->Is > 0 ? moe->Is : 64, 64, 16};
     int rc = check_dims(D, B);
     if (rc) return rc;
-    rc = check_ws(D, B, workspace, workspace_bytes);
+    rc = check_ws(1, D, B, workspace, workspace_bytes);
     if (rc) return rc;
     edge0_layer_desc L;
     memset(&L, 0, sizeof(L));
     L.moe = *moe;
     L.moe.Is = D.Is;
-    L.router = moe->gate;     // not used in this mode; satisfies the layer check
+    L.router = moe->gate_up;   // not used in this mode; satisfies the layer check
     L.route.kind = EDGE0_ROUTE_SOFTMAX_TOPK;
     Prog* p = new Prog;
     memset(p, 0, sizeof(Prog));
     p->mode = MODE_MOE;
     p->L = 1;
     set_dims(*p, D, B);
-    p->step = 0;
+    p->step = -1;   // alternate the workspace's parities call by call
     p->x_in = (const __half*)x;
     p->ids_in = ids;
     p->w_in = w;
@@ -303,7 +267,7 @@ extern "C" int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t*
     p->Ls = 1;
     p->ws = (char*)workspace;
     rc = fill_layer(L, D, 1, p->layers[0]);
-    if (rc == EDGE0_OK) rc = launch(*p, stream);
+    if (rc == EDGE0_OK) rc = engine_launch(*p, stream);
     delete p;
     return rc;
 }
@@ -317,7 +281,7 @@ extern "C" int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t*
     Dims D{head->d, head->E, head->K, 64, 64, head->H, 16};
     int rc = check_dims(D, B);
     if (rc) return rc;
-    rc = check_ws(D, B, workspace, workspace_bytes);
+    rc = check_ws(1, D, B, workspace, workspace_bytes);
     if (rc) return rc;
     edge0_layer_desc L;
     memset(&L, 0, sizeof(L));
@@ -326,7 +290,7 @@ extern "C" int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t*
     L.moe.K = D.K;
     L.moe.I = D.I;
     L.moe.Is = D.Is;
-    L.moe.gate = L.moe.up = L.moe.down = head->fc2;   // not used in this mode
+    L.moe.gate_up = L.moe.down = head->fc2;   // not used in this mode
     L.router = head->fc2;
     L.route.kind = EDGE0_ROUTE_SOFTMAX_TOPK;
     L.has_head = 1;
@@ -337,7 +301,7 @@ extern "C" int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t*
     p->mode = MODE_HEAD;
     p->L = 1;
     set_dims(*p, D, B);
-    p->step = 0;
+    p->step = -1;
     p->x_in = (const __half*)x;
     p->exec_in = exec_ids;
     p->prev_in = prev_ids;
@@ -347,7 +311,7 @@ extern "C" int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t*
     p->Ls = 1;
     p->ws = (char*)workspace;
     rc = fill_layer(L, D, 1, p->layers[0]);
-    if (rc == EDGE0_OK) rc = launch(*p, stream);
+    if (rc == EDGE0_OK) rc = engine_launch(*p, stream);
     delete p;
     return rc;
 }

@@ -1,185 +1,469 @@
-// Persistent decode engine: one CTA per SM, 16 consumer warps + 1 producer warp.
+// Persistent decode engine: one CTA per SM in clusters of two ("pairs"); 16
+// consumer warps + 1 producer warp per CTA.
 //
-// A decode step is a sequence of phases separated by grid barriers:
-//   R (own-routed layers, or step 0): router GEMV -> logits
-//   A: gate/up of the routed experts and the shared expert, LoRA A x, head
-//      fc1[:, :d] x and linear_init[:, :d] x
-//   B: down of the routed experts (weighted by w) and the shared expert (+ LoRA
-//      down), head fc2 gelu(z) (+ linear_init and the one-hot columns)
-// Every phase's work is a list of "segments" (one packed matrix, or one expert's
-// matrix) cut into 576-byte int4 / 2048-byte fp16 units; each CTA takes a
-// contiguous byte range of the phase.  The producer warp builds each phase's
-// segment and chunk list once, publishes it to the consumers through a ring of
-// list slots, and streams the CTA's units (and small auxiliary tensors) into a
-// ring of shared-memory stages with bulk copies as soon as the routing that
-// selects them is known -- for prerouted layers that is at step start, so
-// weight traffic runs ahead across grid barriers.  Consumer warps read each unit
-// once from shared memory and do the dot products on the tensor cores
-// (m16n8k16, fp32 accumulate) with the int4 nibbles turned into fp16 subnormals
-// by a single mask (q * 2^-24); each warp adds its partial sums into a per-phase
-// shared-memory accumulator without CTA-wide synchronisation, and the CTA flushes
-// it to fp32 accumulators in global memory once per phase.
+// Dependencies of one decode layer ("The Other Half of the Memory Wall", S3.1
+// "Math contract", S3.2 "Head", S3.3):
+//   x = RMSNorm(h)                         needs all of the previous layer's y
+//   gate/up rows of each expert            need all of x
+//   down rows                              need all of act = silu(gate) * up
+//   y = sum_k w_k down_k act_k + shared    -> next layer
+//   head(x, executed, previous) -> top-K   needed only at the next token
+// The engine takes ONE grid-wide synchronisation per layer (plus one after the
+// router on own-routed layers):
+//   * every expert (and the shared expert) is cut into half-row tiles of 8
+//     act rows ("hr"); the packed gate/up tile of an hr interleaves its 8 gate
+//     rows with its 8 up rows, so one tensor-core row tile yields gate and up of
+//     the same act rows in the same lane;
+//   * each CTA pair owns a contiguous run of hr over the flattened (shared,
+//     routed slot 0, 1, ...) list; the two CTAs split d in halves, compute
+//     partial gate/up sums for all of the pair's rows, swap them through
+//     distributed shared memory (st.async + mbarrier), then each forms act for
+//     all the pair's rows and applies the matching 16-column slices of down
+//     (packed K-major) to its half of the output rows, adding w-weighted
+//     partial sums into y with vector reductions;
+//   * the shared expert's LoRA runs inside the pairs that own shared rows (A x
+//     over the d-halves travels with the partial sums; B_down A_down act is
+//     split linearly over the pairs);
+//   * the prerouter head of layer l runs after the CTA has arrived at layer l's
+//     barrier, in the time the barrier takes; its logits accumulate in global
+//     memory and the last CTA to finish computes the top-K.
+// The producer warp streams each CTA's weight slices into a byte ring of shared
+// memory with bulk copies as soon as the routing that selects them is known
+// (prerouted layers: at step start, so the stream runs ahead across barriers).
+// int4 nibbles enter m16n8k16 tensor-core steps as fp16 subnormals (q * 2^-24)
+// through single masks; activations travel as hi + lo fp16 columns.
+#include <string.h>
+
+#include <mutex>
+
 #include "internal.cuh"
 
 namespace edge0 {
 
-enum PhaseKind : int { PH_R = 0, PH_A = 1, PH_B = 2 };
-enum SrcKind : int { SRC_X = 0, SRC_ACT = 1, SRC_ACTSH = 2, SRC_GELU = 3 };
-enum OutKind : int {
-    OUT_GUG, OUT_GUU, OUT_GUSG, OUT_GUSU, OUT_AG, OUT_AU, OUT_Z, OUT_LIN, OUT_Y, OUT_LOGR, OUT_LOGH
-};
-enum ExtraKind : int { EX_NONE = 0, EX_LORA_DOWN = 1, EX_HEAD = 2 };
-enum AuxKind : int { AUX_UNITS = 0, AUX_BG, AUX_BU, AUX_AD, AUX_BD, AUX_FC1OH, AUX_LINOH };
-
-struct Seg {
-    const char* base;
-    int off;           // byte offset of the segment in the phase
-    int kind;          // 0 int4, 1 fp16
-    int n_rt, n_g, rows, ub;
-    int src, out, expert, extra;
-    int cu0, cu1;      // this CTA's units of the segment
-};
-
-struct Chunk {
-    int aux, seg, u0, u1, tok, bytes;
-    int sacc;          // unit chunks: first accumulator row of the chunk
-};
-
-constexpr int kMaxChunk = 48;
-constexpr int kListSlots = 4;
-constexpr int kSaccRowsPhase = 1024;   // accumulator rows of one CTA in one phase
-constexpr int kBdBytes = 8192;         // LoRA-down B rows of one CTA in one phase
+constexpr int kMaxSegs = 4;        // expert runs in one pair's share of a layer
+constexpr int kMaxItems = 96;      // copy items of one CTA in one layer
+constexpr int kItemMax = 32768;    // bytes of one copy item
+constexpr int kSlots = 256;        // item barriers (>= 2 x kMaxItems)
+constexpr int kTables = 3;         // layer tables in flight
+constexpr int kMaxChunks = 8;      // 4-element chunks of [B, d] per consumer thread
+constexpr int kMaxD = 4096;
+constexpr int kMinRing = 2 * kItemMax;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // bounded waits: 2 s
 
-// one phase's work of this CTA, built by the producer and read by the consumers
-struct PhaseList {
-    int seq;           // phase index + 1 once published
-    int nseg, nch, sacc_rows;
-    int has_sh, has_head, bd_row0, bd_rows;
-    Seg seg[kMaxSeg];
-    Chunk ch[kMaxChunk];
+enum ItemKind : int {
+    IT_ROUTER = 0, IT_GU, IT_LA, IT_LU, IT_BG, IT_BU, IT_DSC, IT_DQ, IT_ADT, IT_BD, IT_FC1, IT_FC2,
+    IT_LINIT
 };
-
-// ------------------------------------------------------------ smem plan ----
-struct Plan {
-    int stage, full, empty, xf, xsum, actf, actsum, ashf, ashsum, gf, gsum, ash32, gsh, ush, aacc,
-        v, zsm, linsm, lx, hs, rscr, sacc, bd, lists, ids, wts, ready, red, ctl, total;
-};
-
-__host__ __device__ inline int al(int x, int a) { return (x + a - 1) / a * a; }
-
-__host__ __device__ inline Plan make_plan(int L, int B, int K, int d, int E, int I, int Is, int H,
-                                          int r) {
-    Plan p;
-    const int R16 = ceil_div(r, 16) * 16;
-    int o = 0;
-    p.stage = o;  o += kStages * kStageBytes;
-    p.full = o;   o += 8 * kStages;
-    p.empty = o;  o += 8 * kStages;
-    o = al(o, 16);
-    p.xf = o;     o += al(B * d * 2, 16);
-    p.xsum = o;   o += al(B * (d / kGroup) * 4, 16);
-    // activation sources keep a hi and a lo fragment array (see put_group)
-    p.actf = o;   o += al(2 * B * K * I * 2, 16);
-    p.actsum = o; o += al(2 * B * K * (I / kGroup) * 4, 16);
-    p.ashf = o;   o += al(2 * B * Is * 2, 16);
-    p.ashsum = o; o += al(2 * B * (Is / kGroup) * 4, 16);
-    p.gf = o;     o += al(2 * B * H * 2, 16);
-    p.gsum = o;   o += al(2 * B * (H / kGroup) * 4, 16);
-    p.ash32 = o;  o += al(B * Is * 4, 16);
-    p.gsh = o;    o += al(B * Is * 4, 16);
-    p.ush = o;    o += al(B * Is * 4, 16);
-    p.aacc = o;   o += al(B * 2 * R16 * 4, 16);
-    p.v = o;      o += al(B * R16 * 4, 16);
-    p.zsm = o;    o += al(B * H * 4, 16);
-    p.linsm = o;  o += al(B * E * 4, 16);
-    p.lx = o;     o += al(B * E * 4, 16);
-    p.hs = o;     o += al(B * d * 2, 16);
-    p.rscr = o;   o += al(B * 2 * E * 4, 16);
-    p.sacc = o;   o += al(kSaccRowsPhase * B * 4, 16);
-    p.bd = o;     o += kBdBytes;
-    p.lists = o;  o += al(kListSlots * (int)sizeof(PhaseList), 16);
-    p.ids = o;    o += al(L * B * K * 4, 16);
-    p.wts = o;    o += al(L * B * K * 4, 16);
-    p.ready = o;  o += al(L * 4, 16);
-    p.red = o;    o += al(B * kConsumerWarps * 4 + 64, 16);
-    p.ctl = o;    o += 64;
-    p.total = o;
-    return p;
+__host__ __device__ inline bool unit_kind(int k) {
+    return k == IT_ROUTER || k == IT_GU || k == IT_LA || k == IT_LU || k == IT_FC1 || k == IT_LINIT;
 }
 
-// ------------------------------------------------------------ helpers -----
+// ------------------------------------------------------------------ plan ----
+struct Seg {
+    int slot;     // -1: shared expert; else routed slot (index into the layer's distinct experts)
+    int hr0, hr1; // half-row tiles [hr0, hr1) of the expert
+    int hoff;     // half-row tiles of the pair before this segment
+    int q0, q1;   // 16-row act quarters [q0, q1) the segment touches
+    int qoff;     // quarters of the pair before this segment
+};
+
+struct PairPlan {
+    int nseg, over;
+    Seg seg[kMaxSegs];
+    int n_hr, n_q;
+    int has_sh;   // the pair owns shared-expert rows
+    int hd0, hd1; // head tasks
+    int ru0, ru1; // router units (in this rank's half of d)
+};
+
+__host__ __device__ inline void split_range(int n, int parts, int i, int* a, int* b) {
+    *a = (int)((long long)n * i / parts);
+    *b = (int)((long long)n * (i + 1) / parts);
+}
+
+struct Shape {
+    int d, I, Is, E, H, r;
+    int n_slots;                      // routed expert slots (0: none)
+    int shared, lora, head, router;   // parts present in the layer
+};
+
+__host__ __device__ inline int shared_pairs(int P, int n_sh, int n_rt, bool lora) {
+    if (n_sh <= 0) return 0;
+    if (n_rt <= 0) return P;
+    // cost in int4-unit equivalents per CTA: an hr is 16 gate/up units + half a
+    // 16-row down slice over half of d; LoRA adds A_gate, A_up over half of d
+    int best = 0x7fffffff, pick = 1;
+    for (int ps = 1; ps < P; ++ps) {
+        const int cs = ceil_div(n_sh, ps) * 24 + (lora ? 40 : 0);
+        const int cr = ceil_div(n_rt, P - ps) * 24;
+        const int cmax = cs > cr ? cs : cr;
+        if (cmax < best) { best = cmax; pick = ps; }
+    }
+    return pick;
+}
+
+__host__ __device__ inline int half_lo(int n, int rank) { return rank ? n / 2 : 0; }
+__host__ __device__ inline int half_hi(int n, int rank) { return rank ? n : n / 2; }
+
+__host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int rank, PairPlan& pp) {
+    pp.nseg = 0;
+    pp.over = 0;
+    pp.n_hr = 0;
+    pp.n_q = 0;
+    pp.has_sh = 0;
+    pp.hd0 = pp.hd1 = 0;
+    pp.ru0 = pp.ru1 = 0;
+    const int hpe = S.I / kHalfRow;
+    const int n_sh = S.shared ? S.Is / kHalfRow : 0;
+    const int n_rt = S.n_slots * hpe;
+    const int Ps = shared_pairs(P, n_sh, n_rt, S.lora != 0);
+    int a, b;
+    if (pair < Ps) {
+        split_range(n_sh, Ps, pair, &a, &b);
+        if (a < b) {
+            Seg& s = pp.seg[pp.nseg++];
+            s.slot = -1; s.hr0 = a; s.hr1 = b; s.hoff = 0; s.q0 = a / 2; s.q1 = (b + 1) / 2; s.qoff = 0;
+            pp.n_hr = b - a;
+            pp.n_q = s.q1 - s.q0;
+            pp.has_sh = 1;
+        }
+    } else if (P > Ps) {
+        split_range(n_rt, P - Ps, pair - Ps, &a, &b);
+        while (a < b) {
+            const int slot = a / hpe;
+            const int end = (slot + 1) * hpe < b ? (slot + 1) * hpe : b;
+            if (pp.nseg >= kMaxSegs) { pp.over = 1; break; }
+            Seg& s = pp.seg[pp.nseg++];
+            s.slot = slot;
+            s.hr0 = a - slot * hpe;
+            s.hr1 = end - slot * hpe;
+            s.hoff = pp.n_hr;
+            s.q0 = s.hr0 / 2;
+            s.q1 = (s.hr1 + 1) / 2;
+            s.qoff = pp.n_q;
+            pp.n_hr += s.hr1 - s.hr0;
+            pp.n_q += s.q1 - s.q0;
+            a = end;
+        }
+    }
+    if (S.head) split_range(S.H / kRowTile + S.E / kRowTile, P, pair, &pp.hd0, &pp.hd1);
+    if (S.router) {
+        const int n_gd = S.d / kGroup;
+        const int ngh = half_hi(n_gd, rank) - half_lo(n_gd, rank);
+        split_range((S.E / kRowTile) * ngh, P, pair, &pp.ru0, &pp.ru1);
+    }
+}
+
+__host__ __device__ inline int head_ctas(const Shape& S, int P) {
+    const int n_ht = S.H / kRowTile + S.E / kRowTile;
+    return 2 * (n_ht < P ? n_ht : P);
+}
+
+// one copy of a contiguous global region into the ring
+struct Item {
+    int kind, seg;
+    int bytes, off;   // size, ring offset
+    int lin;          // linear ring position (off = lin mod ring size)
+    int a, b, n;      // kind-specific position and count
+};
+
+struct LayerTab {
+    int seq;          // layer index + 1 once published
+    int k0, n;        // global index of the first item; items
+    int p1, p2, p3;   // first item of P1 (gate/up), P2 (down), P3 (head); router items from 0
+    PairPlan pl;
+    Item it[kMaxItems];
+};
+
+// this CTA's halves
+struct Halves {
+    int gh0, gh1;   // groups of d
+    int rt0, rt1;   // row tiles of d
+    int e0, e1;     // row tiles of E
+};
+__host__ __device__ inline Halves halves(int d, int E, int rank) {
+    Halves h;
+    h.gh0 = half_lo(d / kGroup, rank);
+    h.gh1 = half_hi(d / kGroup, rank);
+    h.rt0 = half_lo(d / kRowTile, rank);
+    h.rt1 = half_hi(d / kRowTile, rank);
+    h.e0 = half_lo(E / kRowTile, rank);
+    h.e1 = half_hi(E / kRowTile, rank);
+    return h;
+}
+
+// Builds one CTA's copy items of one layer into T (deterministic: the producer
+// issues them, the consumers read them from the published table, the host uses
+// it to check limits).  `lin` is the running linear ring position.  Returns
+// false if a limit is exceeded.
+__host__ __device__ inline bool build_items(const Shape& Sh, int P, int pair, int rank, int ring,
+                                            LayerTab* T, int& lin) {
+    PairPlan& pl = T->pl;
+    pair_plan(Sh, P, pair, rank, pl);
+    if (pl.over) return false;
+    const Halves hv = halves(Sh.d, Sh.E, rank);
+    int n = 0;
+    bool ok = true;
+    auto push = [&](int kind, int seg, int bytes, int a, int b, int cnt) {
+        if (bytes <= 0) return;
+        if (n >= kMaxItems || bytes > kItemMax || bytes > ring) { ok = false; return; }
+        if (lin % ring + bytes > ring) lin += ring - lin % ring;
+        Item& it = T->it[n++];
+        it.kind = kind; it.seg = seg; it.bytes = bytes; it.off = lin % ring; it.lin = lin;
+        it.a = a; it.b = b; it.n = cnt;
+        lin += bytes;
+    };
+    // `units` units of `ub` bytes from unit `first` of position a, at most kItemMax bytes a copy
+    auto push_units = [&](int kind, int seg, int a, int first, int units, int ub) {
+        const int per = kItemMax / ub;
+        for (int j = 0; j < units; j += per) {
+            const int m = units - j < per ? units - j : per;
+            push(kind, seg, m * ub, a, first + j, m);
+        }
+    };
+    const int ngh = hv.gh1 - hv.gh0, nrt = hv.rt1 - hv.rt0, ne = hv.e1 - hv.e0;
+    const int r = Sh.r;
+    // router units: this pair's share of (E row tiles) x (this rank's groups)
+    for (int u = pl.ru0; u < pl.ru1;) {
+        const int tile = u / ngh, j = u % ngh;
+        const int m = (ngh - j) < (pl.ru1 - u) ? (ngh - j) : (pl.ru1 - u);
+        push_units(IT_ROUTER, 0, tile, j, m, kF16Unit);
+        u += m;
+    }
+    T->p1 = n;
+    for (int s = 0; s < pl.nseg; ++s) {
+        const Seg& g = pl.seg[s];
+        for (int hr = g.hr0; hr < g.hr1; ++hr) push_units(IT_GU, s, hr, 0, ngh, kQ4Unit);
+        if (g.slot < 0 && Sh.lora) {
+            push_units(IT_LA, s, 0, 0, ngh, kF16Unit);
+            push_units(IT_LU, s, 0, 0, ngh, kF16Unit);
+            const int rows = (g.hr1 - g.hr0) * kHalfRow;
+            push(IT_BG, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            push(IT_BU, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+        }
+    }
+    T->p2 = n;
+    for (int s = 0; s < pl.nseg; ++s) {
+        const Seg& g = pl.seg[s];
+        for (int gg = g.q0 / 4; gg <= (g.q1 - 1) / 4; ++gg) {
+            push(IT_DSC, s, nrt * kQ4Scales, gg, 0, nrt);
+            const int qa = g.q0 > 4 * gg ? g.q0 : 4 * gg, qb = g.q1 < 4 * gg + 4 ? g.q1 : 4 * gg + 4;
+            for (int Q = qa; Q < qb; ++Q) push(IT_DQ, s, nrt * kQ4Quarter, Q, 0, nrt);
+        }
+        if (g.slot < 0 && Sh.lora) {
+            const int rows = (g.hr1 - g.hr0) * kHalfRow;
+            push(IT_ADT, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            const int per = kItemMax / (r * 2);
+            for (int row = hv.rt0 * kRowTile; row < hv.rt1 * kRowTile; row += per) {
+                const int m = hv.rt1 * kRowTile - row < per ? hv.rt1 * kRowTile - row : per;
+                push(IT_BD, s, m * r * 2, row, 0, m);
+            }
+        }
+    }
+    T->p3 = n;
+    const int nH = Sh.H / kRowTile;
+    for (int t = pl.hd0; t < pl.hd1; ++t) {
+        if (t < nH) {
+            push_units(IT_FC1, 0, t, 0, ngh, kF16Unit);
+            push(IT_FC2, 0, ne * kF16Step, t, hv.e0, ne);
+        } else {
+            push_units(IT_LINIT, 0, t - nH, 0, ngh, kF16Unit);
+        }
+    }
+    T->n = n;
+    return ok;
+}
+
+// ------------------------------------------------------------ smem plan ----
+struct Ctl {
+    int trace, tslot, abort, step, cdone, issued, last, pad;
+};
+
+struct Plan {
+    int ring, full, empty, xch, lin, tabs, xf, xsum, hs, part, recv, act32, af, qsum, vlo, zpart,
+        zrecv, gf, ids, wts, dist, ndist, prv, nprv, ready, rscr, red, ctl, total;
+};
+
+__host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
+
+__host__ __device__ inline int msg_floats(const Prog& p) { return (p.hr_max * 16 + 32) * p.B; }
+
+__host__ __device__ inline Plan make_plan(const Prog& p) {
+    Plan s;
+    const int B = p.B, K = p.K, L = p.L;
+    const int n_gd = p.d / kGroup, ngh = n_gd - n_gd / 2;
+    int o = 0;
+    s.full = o;   o += kSlots * 8;
+    s.empty = o;  o += kSlots * 8;
+    s.xch = o;    o += 2 * 8;
+    o = al16(o);
+    s.lin = o;    o += kSlots * 4;
+    s.tabs = o;   o += al16(kTables * (int)sizeof(LayerTab));
+    s.xf = o;     o += al16(ngh * 4 * B * 4 * 8);
+    s.xsum = o;   o += al16(ngh * B * 4);
+    s.hs = o;     o += al16(B * p.d * 2);
+    s.part = o;   o += al16(msg_floats(p) * 4);
+    s.recv = o;   o += al16(msg_floats(p) * 4);
+    s.act32 = o;  o += al16(p.hr_max * 8 * B * 4);
+    s.af = o;     o += al16(p.q_max * B * 2 * 4 * 8);
+    s.qsum = o;   o += al16(p.q_max * B * 4);
+    s.vlo = o;    o += al16(16 * B * 4);
+    s.zpart = o;  o += al16(16 * B * 4);
+    s.zrecv = o;  o += al16(2 * 16 * B * 4);
+    s.gf = o;     o += al16(B * 2 * 4 * 8);
+    s.ids = o;    o += al16(L * B * K * 4);
+    s.wts = o;    o += al16(L * B * K * 4);
+    s.dist = o;   o += al16(L * (p.slots_max > 0 ? p.slots_max : 1) * 4);
+    s.ndist = o;  o += al16(L * 4);
+    s.prv = o;    o += al16(L * B * K * 4);
+    s.nprv = o;   o += al16(L * 4);
+    s.ready = o;  o += al16(L * 4);
+    s.rscr = o;   o += al16(B * 3 * p.E * 4);
+    s.red = o;    o += al16((B * kConsumerWarps + 64) * 4);
+    s.ctl = o;    o += al16((int)sizeof(Ctl));
+    o = (o + 127) & ~127;
+    s.ring = o;
+    s.total = o + p.ring_bytes;
+    return s;
+}
+
+// ------------------------------------------------------------- context ----
+struct Ctx {
+    const Prog* p;
+    char* sm;
+    Plan pl;
+    WsHeader* hdr;
+    Ctl* ctl;
+    WsLayout ws;
+    Halves hv;
+    int nct, cta, pair, rank, P;
+    int step, par;
+};
+
 __device__ __forceinline__ unsigned long long now_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// shared control words
-struct Ctl {
-    int trace;        // record phase timestamps
-    int tslot;        // next trace slot
-    int abort;        // CTA-local: give up
-    int step;
-    unsigned pc0;
-    int issued;       // chunks issued by the producer
-    int cdone;        // phases the consumers have finished
-};
-
-__device__ void raise_error(WsHeader* hdr, Ctl* ctl, int code) {
-    atomicCAS(&hdr->error, 0, code);
-    atomicExch(&hdr->abort, 1);
-    ctl->abort = 1;
+__device__ void raise_error(const Ctx& c, int code) {
+    atomicCAS(&c.hdr->error, 0, code);
+    atomicExch(&c.hdr->abort, 1);
+    *(volatile int*)&c.ctl->abort = 1;
 }
-
-__device__ __forceinline__ bool should_abort(WsHeader* hdr, Ctl* ctl) {
-    return *(volatile int*)&ctl->abort || ld_volatile_s32(&hdr->abort);
+__device__ __forceinline__ bool should_abort(const Ctx& c) {
+    return *(volatile int*)&c.ctl->abort || ld_volatile_s32(&c.hdr->abort);
 }
+__device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile int*)&c.ctl->abort != 0; }
 
 // wait on an mbarrier phase with a time bound; false on abort/timeout
-__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHeader* hdr, Ctl* ctl) {
+__device__ bool mbar_wait(const Ctx& c, uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = now_ns();
     for (unsigned it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 63) {
-            if (should_abort(hdr, ctl)) return false;
-            if (now_ns() - t0 > kTimeoutNs) {
-                raise_error(hdr, ctl, EDGE0_ETIMEOUT);
-                return false;
-            }
+            if (should_abort(c)) return false;
+            if (now_ns() - t0 > kTimeoutNs) { raise_error(c, EDGE0_ETIMEOUT); return false; }
         }
     }
 }
 
 // spin until *flag >= want (shared memory, written by the other role); bounded
-__device__ bool wait_flag(volatile int* flag, int want, WsHeader* hdr, Ctl* ctl) {
+__device__ bool wait_flag(const Ctx& c, volatile int* flag, int want) {
     if (*flag >= want) return true;
     const unsigned long long t0 = now_ns();
     for (unsigned it = 0; *flag < want; ++it) {
         __nanosleep(32);
         if ((it & 63) == 63) {
-            if (should_abort(hdr, ctl)) return false;
-            if (now_ns() - t0 > kTimeoutNs) {
-                raise_error(hdr, ctl, EDGE0_ETIMEOUT);
-                return false;
-            }
+            if (should_abort(c)) return false;
+            if (now_ns() - t0 > kTimeoutNs) { raise_error(c, EDGE0_ETIMEOUT); return false; }
         }
     }
     return true;
 }
 
+template <class T>
+__device__ __forceinline__ T* SM(const Ctx& c, int off) { return reinterpret_cast<T*>(c.sm + off); }
+
+__device__ __forceinline__ uint64_t* full_bar(const Ctx& c, int k) { return SM<uint64_t>(c, c.pl.full) + (k % kSlots); }
+__device__ __forceinline__ uint64_t* empty_bar(const Ctx& c, int k) { return SM<uint64_t>(c, c.pl.empty) + (k % kSlots); }
+__device__ __forceinline__ uint32_t item_parity(int k) { return (uint32_t)((k / kSlots) & 1); }
+__device__ __forceinline__ LayerTab* tab_of(const Ctx& c, int l) { return SM<LayerTab>(c, c.pl.tabs) + (l % kTables); }
+__device__ __forceinline__ int* ids_of(const Ctx& c, int l) { return SM<int>(c, c.pl.ids) + l * c.p->B * c.p->K; }
+__device__ __forceinline__ float* w_of(const Ctx& c, int l) { return SM<float>(c, c.pl.wts) + l * c.p->B * c.p->K; }
+__device__ __forceinline__ int* dist_of(const Ctx& c, int l) {
+    return SM<int>(c, c.pl.dist) + l * (c.p->slots_max > 0 ? c.p->slots_max : 1);
+}
+__device__ __forceinline__ int* prev_of(const Ctx& c, int l) { return SM<int>(c, c.pl.prv) + l * c.p->B * c.p->K; }
+__device__ __forceinline__ const char* ring_at(const Ctx& c, const Item& it) { return c.sm + c.pl.ring + it.off; }
+
+__device__ __forceinline__ float* ws_f(const Ctx& c, long long off) { return reinterpret_cast<float*>(c.p->ws + off); }
+__device__ __forceinline__ float* y_buf(const Ctx& c, int par, int sidx) {
+    return ws_f(c, c.ws.y) + ((long long)par * c.p->Ls + sidx) * c.p->B * c.p->d;
+}
+__device__ __forceinline__ float* logr_buf(const Ctx& c, int par, int sidx) {
+    return ws_f(c, c.ws.logr) + ((long long)par * c.p->Ls + sidx) * c.p->B * c.p->E;
+}
+__device__ __forceinline__ float* logh_buf(const Ctx& c, int par, int sidx) {
+    return ws_f(c, c.ws.logh) + ((long long)par * c.p->Ls + sidx) * c.p->B * c.p->E;
+}
+__device__ __forceinline__ unsigned* cnt_buf(const Ctx& c, int par, int sidx) {
+    return reinterpret_cast<unsigned*>(c.p->ws + c.ws.cnt) + par * c.p->Ls + sidx;
+}
+
+// optional trace: (tag, globaltimer) pairs per CTA, written by consumer thread 0
+__device__ __forceinline__ void stamp(const Ctx& c, int tag) {
+    if (threadIdx.x != 0 || !c.ctl->trace) return;
+    const int s = c.ctl->tslot;
+    if (s + 2 > kTraceSlots) return;
+    unsigned long long* a =
+        reinterpret_cast<unsigned long long*>(c.p->ws + c.ws.trace) + (long long)c.cta * kTraceSlots;
+    a[s] = (unsigned long long)tag;
+    a[s + 1] = now_ns();
+    c.ctl->tslot = s + 2;
+}
+
+__host__ __device__ inline bool has_router_phase(const Prog& p, int l, int step) {
+    return p.mode == MODE_DECODE && (!(p.layers[l].flags & LF_PREROUTED) || step == 0);
+}
+
+__host__ __device__ inline Shape layer_shape(const Prog& p, int l, bool router) {
+    const LayerP& Ly = p.layers[l];
+    Shape S;
+    S.d = p.d; S.I = p.I; S.Is = p.Is; S.E = p.E; S.H = p.H; S.r = p.r;
+    S.n_slots = p.mode == MODE_HEAD ? 0 : p.slots_max;
+    S.shared = (p.mode != MODE_HEAD && (Ly.flags & LF_SHARED)) ? 1 : 0;
+    S.lora = (S.shared && p.mode == MODE_DECODE && (Ly.flags & LF_LORA)) ? 1 : 0;
+    S.head = (p.mode == MODE_HEAD || (p.mode == MODE_DECODE && (Ly.flags & LF_HEAD))) ? 1 : 0;
+    S.router = router ? 1 : 0;
+    return S;
+}
+
+__device__ __forceinline__ void cbar() { named_bar_sync(1, kConsumerThreads); }
+// consumer barrier that also returns the OR of `v` over the consumer threads
+__device__ __forceinline__ bool cbar_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(kConsumerThreads)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------- routing -----
-// top-K over `score` (E values in shared/global memory) by one warp, value
-// descending, lower index first on ties; masked entries are -inf.
+// top-K over `score` (E values) by one warp, value descending, lower index first
+// on ties; masked entries are -inf.
 __device__ void warp_topk(const float* score, int E, int K, int* ids, int lane) {
-    unsigned taken[16];
+    unsigned taken[EDGE0_MAX_E / 32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) taken[i] = 0;
+    for (int i = 0; i < EDGE0_MAX_E / 32; ++i) taken[i] = 0;
     for (int k = 0; k < K; ++k) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < EDGE0_MAX_E / 32; ++i) {
             const int e = lane + 32 * i;
             if (e >= E || taken[i]) continue;
             const float v = score[e];
@@ -198,8 +482,8 @@ __device__ void warp_topk(const float* score, int E, int K, int* ids, int lane) 
     }
 }
 
-// Routing rule of App. A, one token per warp.  logits: E fp32 (global or shared);
-// scratch: 2 * E floats of shared memory for this warp.
+// Routing rule of App. A, one token per warp.  logits: E fp32 in shared memory;
+// scratch: 2 E floats of shared memory for this warp.
 __device__ void warp_route(const float* logits, int E, int K, int kind, int n_groups, int G,
                            float scale, const float* bias, float* scratch, int* ids, float* w,
                            int lane) {
@@ -213,7 +497,7 @@ __device__ void warp_route(const float* logits, int E, int K, int kind, int n_gr
         }
         __syncwarp();
         const int per = E / n_groups;
-        // group scores: sum of the two largest selection scores of each group
+        // group score: sum of the two largest selection scores of the group
         float gscore = -INFINITY;
         if (lane < n_groups) {
             float a = -INFINITY, b = -INFINITY;
@@ -225,8 +509,7 @@ __device__ void warp_route(const float* logits, int E, int K, int kind, int n_gr
             gscore = a + b;
         }
         // keep the best G groups (lower group index on ties)
-        unsigned keep = 0;
-        unsigned gtaken = 0;
+        unsigned keep = 0, gtaken = 0;
         for (int k = 0; k < G; ++k) {
             float bv = (lane < n_groups && !((gtaken >> lane) & 1)) ? gscore : -INFINITY;
             int bi = (lane < n_groups && !((gtaken >> lane) & 1)) ? lane : 0x7fffffff;
@@ -264,1040 +547,1178 @@ __device__ void warp_route(const float* logits, int E, int K, int kind, int n_gr
     __syncwarp();
 }
 
-// ------------------------------------------------------------ context -----
-struct Ctx {
-    const Prog* p;
-    char* sm;
-    Plan pl;
-    WsHeader* hdr;
-    Ctl* ctl;
-    AccLayout acc;
-    int nct, cta;
-    int step;
-    int R16;
-};
-
-__device__ __forceinline__ float* acc_set(const Ctx& c, unsigned pc) {
-    return reinterpret_cast<float*>(c.p->ws + kWsHeaderBytes) + (long long)(pc % 3) * c.acc.total;
-}
-__device__ __forceinline__ __half* hbuf(const Ctx& c, int i) {
-    return reinterpret_cast<__half*>(c.p->ws + kWsHeaderBytes + 3 * c.acc.total * 4) +
-           (long long)i * c.p->B * c.p->d;
-}
-
-// optional phase trace: slot i of this CTA <- globaltimer (thread 0 only)
-__device__ __forceinline__ unsigned long long* trace_area(const Ctx& c) {
-    const char* base = c.p->ws + kWsHeaderBytes + 3 * c.acc.total * 4 + 2LL * c.p->B * c.p->d * 2 + 256;
-    return reinterpret_cast<unsigned long long*>(const_cast<char*>(base)) + (long long)c.cta * kTraceSlots;
-}
-
-// record (tag, globaltimer) when tracing is on; consumer thread 0 only
-__device__ __forceinline__ void stamp(const Ctx& c, int tag) {
-    if (threadIdx.x != 0 || !c.ctl->trace) return;
-    if (c.ctl->trace >= 2 && (tag & 0xF0000) == 0 && (tag & 0xF) > 4) return;
-    const int s = c.ctl->tslot;
-    if (s + 2 > kTraceSlots) return;
-    unsigned long long* a = trace_area(c);
-    a[s] = (unsigned long long)tag;
-    a[s + 1] = now_ns();
-    c.ctl->tslot = s + 2;
-}
-
-// detailed stamps for one two-layer window (trace mode >= 2: window starts at layer mode - 2)
-__device__ __forceinline__ void dstamp(const Ctx& c, int l, int tag) {
-    const int m = c.ctl->trace;
-    if (m >= 2 && l >= m - 2 && l <= m - 1) stamp(c, tag);
-}
-
-__device__ __forceinline__ int* sm_ids(const Ctx& c, int l) {
-    return reinterpret_cast<int*>(c.sm + c.pl.ids) + l * c.p->B * c.p->K;
-}
-__device__ __forceinline__ float* sm_w(const Ctx& c, int l) {
-    return reinterpret_cast<float*>(c.sm + c.pl.wts) + l * c.p->B * c.p->K;
-}
-__device__ __forceinline__ PhaseList* list_slot(const Ctx& c, int pi) {
-    return reinterpret_cast<PhaseList*>(c.sm + c.pl.lists) + (pi % kListSlots);
-}
-
-__device__ __forceinline__ bool has_router_phase(const Prog& p, int l, int step) {
-    return p.mode == MODE_DECODE && (!(p.layers[l].flags & LF_PREROUTED) || step == 0);
-}
-
-__device__ __forceinline__ int expert_slot(const LayerP& Ly, int e) {
-    return Ly.slot_table ? Ly.slot_table[e] : e;
-}
-
-__device__ __forceinline__ int units_of(int kind, int bytes) {   // ceil(bytes / unit)
-    return kind ? (bytes + kF16Unit - 1) >> 11 : (bytes + kQ4Unit - 1) / kQ4Unit;
-}
-
-// Build the segment list of phase `ph` of layer l into L->seg (deterministic).
-// Returns the phase's byte total, or -1 for an expert id or slot out of range.
-__device__ int build_segments(const Ctx& c, int l, int ph, const int* ids, PhaseList* Lp) {
+// distinct experts of a layer's routing in order of first appearance; false if
+// an id is out of range (single thread)
+__device__ bool make_dist(const Ctx& c, int l) {
     const Prog& p = *c.p;
-    const LayerP& Ly = p.layers[l];
-    const int B = p.B, K = p.K, d = p.d, E = p.E, I = p.I, Is = p.Is, H = p.H, r = p.r;
+    const int* ids = ids_of(c, l);
+    int* dist = dist_of(c, l);
     int n = 0;
-    int off = 0;
-    Seg* S = Lp->seg;
-    auto add = [&](const char* base, int kind, int rows, int in, int src, int out, int expert,
-                   int extra) {
-        if (n >= kMaxSeg) return;
-        Seg& s = S[n++];
-        s.base = base;
-        s.kind = kind;
-        s.n_rt = ceil_div(rows, kRowTile);
-        s.n_g = in / kGroup;
-        s.rows = rows;
-        s.ub = kind ? kF16Unit : kQ4Unit;
-        s.src = src;
-        s.out = out;
-        s.expert = expert;
-        s.extra = extra;
-        s.off = off;
-        off += s.n_rt * s.n_g * s.ub;
-    };
-    const bool moe_phase = p.mode != MODE_HEAD;
-    const bool head = (p.mode == MODE_HEAD) || (p.mode == MODE_DECODE && (Ly.flags & LF_HEAD));
-    const bool lora = p.mode == MODE_DECODE && (Ly.flags & LF_LORA);
-    const bool shared = moe_phase && (Ly.flags & LF_SHARED);
-    if (ph == PH_R) {
-        add(Ly.router, 1, E, d, SRC_X, OUT_LOGR, -1, EX_NONE);
-    } else {
-        // distinct routed experts in order of first appearance over (b, k)
-        if (moe_phase) {
-            for (int i = 0; i < B * K; ++i) {
-                const int e = ids[i];
-                bool seen = false;
-                for (int j = 0; j < i; ++j) seen |= (ids[j] == e);
-                if (seen) continue;
-                if (e < 0 || e >= E) return -1;
-                const long long slot = expert_slot(Ly, e);
-                if (slot < 0 || slot >= Ly.n_slots) return -1;
-                if (ph == PH_A) {
-                    add(Ly.gate + slot * q4_bytes(I, d), 0, I, d, SRC_X, OUT_GUG, e, EX_NONE);
-                    add(Ly.up + slot * q4_bytes(I, d), 0, I, d, SRC_X, OUT_GUU, e, EX_NONE);
-                } else {
-                    add(Ly.down + slot * q4_bytes(d, I), 0, d, I, SRC_ACT, OUT_Y, e, EX_NONE);
-                }
-            }
-        }
-        if (ph == PH_A) {
-            if (shared) {
-                add(Ly.sh_gate, 0, Is, d, SRC_X, OUT_GUSG, -1, EX_NONE);
-                add(Ly.sh_up, 0, Is, d, SRC_X, OUT_GUSU, -1, EX_NONE);
-            }
-            if (shared && lora) {
-                add(Ly.lora_Ag, 1, r, d, SRC_X, OUT_AG, -1, EX_NONE);
-                add(Ly.lora_Au, 1, r, d, SRC_X, OUT_AU, -1, EX_NONE);
-            }
-            if (head) {
-                add(Ly.fc1, 1, H, d, SRC_X, OUT_Z, -1, EX_NONE);
-                add(Ly.linit, 1, E, d, SRC_X, OUT_LIN, -1, EX_NONE);
-            }
-        } else {
-            if (shared)
-                add(Ly.sh_down, 0, d, Is, SRC_ACTSH, OUT_Y, -1, lora ? EX_LORA_DOWN : EX_NONE);
-            if (head) add(Ly.fc2, 1, E, H, SRC_GELU, OUT_LOGH, -1, EX_HEAD);
-        }
+    bool ok = true;
+    for (int i = 0; i < p.B * p.K; ++i) {
+        const int e = ids[i];
+        if (e < 0 || e >= p.E) { ok = false; continue; }
+        bool seen = false;
+        for (int j = 0; j < n; ++j) seen |= dist[j] == e;
+        if (!seen && n < p.slots_max) dist[n++] = e;
     }
-    Lp->nseg = n;
-    return off;
-}
-
-// Build this CTA's chunk list of a phase (after build_segments).  Auxiliary
-// chunks precede the segment that needs them.  n_prev: rows of the previous
-// token's mask (0 or K).  Returns 0, or an EDGE0_* status.
-__device__ int build_chunks(const Ctx& c, int total, int n_prev, PhaseList* Lp) {
-    const Prog& p = *c.p;
-    const int lo = (int)((long long)total * c.cta / c.nct);
-    const int hi = (int)((long long)total * (c.cta + 1) / c.nct);
-    int n = 0, rows = 0;
-    bool over = false;
-    // every chunk is written once, whole
-    auto push = [&](int aux, int seg, int u0, int u1, int tok, int bytes, int sacc_row) {
-        if (n >= kMaxChunk) { over = true; return; }
-        Chunk v;
-        v.aux = aux; v.seg = seg; v.u0 = u0; v.u1 = u1; v.tok = tok; v.bytes = bytes;
-        v.sacc = sacc_row;
-        Lp->ch[n] = v;
-        ++n;
-    };
-    Lp->has_sh = 0;
-    Lp->has_head = 0;
-    Lp->bd_row0 = 0;
-    Lp->bd_rows = 0;
-    for (int s = 0; s < Lp->nseg; ++s) {
-        Seg& S = Lp->seg[s];
-        const int nu = S.n_rt * S.n_g;
-        int a = lo - S.off, b = hi - S.off;
-        a = a <= 0 ? 0 : units_of(S.kind, a);
-        b = b <= 0 ? 0 : units_of(S.kind, b);
-        const int u0 = a < nu ? a : nu, u1 = b < nu ? b : nu;
-        S.cu0 = u0;
-        S.cu1 = u1;
-        if (u0 >= u1) continue;
-        if (S.src == SRC_ACTSH) Lp->has_sh = 1;
-        if (S.src == SRC_GELU) Lp->has_head = 1;
-        if (S.extra == EX_LORA_DOWN) {
-            push(AUX_BG, s, 0, 0, 0, p.Is * p.r * 2, 0);
-            push(AUX_BU, s, 0, 0, 0, p.Is * p.r * 2, 0);
-            push(AUX_AD, s, 0, 0, 0, (int)f16_bytes(p.r, p.Is), 0);
-            // B_d rows of the row tiles whose group-0 unit belongs to this CTA
-            const int ng = S.n_g;
-            const int rt_a = (u0 + ng - 1) / ng, rt_b = (u1 - 1) / ng;   // inclusive
-            if (rt_a <= rt_b) {
-                const int row0 = rt_a * kRowTile;
-                int row1 = (rt_b + 1) * kRowTile;
-                if (row1 > p.d) row1 = p.d;
-                if ((row1 - row0) * p.r * 2 > kBdBytes) return EDGE0_EUNSUPPORTED;
-                Lp->bd_row0 = row0;
-                Lp->bd_rows = row1 - row0;
-                push(AUX_BD, s, rt_a, rt_b + 1, 0, (row1 - row0) * p.r * 2, 0);
-            }
-        }
-        if (S.extra == EX_HEAD) {
-            for (int t = 0; t < p.B; ++t) push(AUX_FC1OH, s, 0, 0, t, (p.K + n_prev) * p.H * 2, 0);
-            for (int t = 0; t < p.B; ++t) push(AUX_LINOH, s, 0, 0, t, (p.K + n_prev) * p.E * 2, 0);
-        }
-        int cap = kStageBytes / S.ub;
-        if (cap > 30 * S.n_g) cap = 30 * S.n_g;     // a chunk spans at most 32 row tiles
-        for (int x = u0; x < u1; x += cap) {
-            const int y = x + cap < u1 ? x + cap : u1;
-            push(AUX_UNITS, s, x, y, 0, (y - x) * S.ub, rows);
-            rows += ((y - 1) / S.n_g - x / S.n_g + 1) * kRowTile;
-        }
-    }
-    if (over || rows > kSaccRowsPhase) return EDGE0_EUNSUPPORTED;
-    Lp->nch = n;
-    Lp->sacc_rows = rows;
-    return EDGE0_OK;
+    SM<int>(c, c.pl.ndist)[l] = n;
+    return ok;
 }
 
 // ------------------------------------------------------------ producer -----
+// global source of an item; null: nothing to copy (a routed slot no token uses);
+// (const char*)1: an expert slot outside the stacks
+__device__ const char* item_src(const Ctx& c, int l, const LayerTab* T, const Item& it) {
+    const Prog& p = *c.p;
+    const LayerP& Ly = p.layers[l];
+    const int n_gd = p.d / kGroup, r = p.r, n_rtd = p.d / kRowTile, gh0 = c.hv.gh0, rt0 = c.hv.rt0;
+    const char* gu = nullptr;
+    const char* dn = nullptr;
+    if (it.kind == IT_GU || it.kind == IT_DSC || it.kind == IT_DQ) {
+        const Seg& g = T->pl.seg[it.seg];
+        if (g.slot < 0) {
+            gu = Ly.sh_gu;
+            dn = Ly.sh_down;
+        } else {
+            if (g.slot >= SM<int>(c, c.pl.ndist)[l]) return nullptr;
+            const int e = dist_of(c, l)[g.slot];
+            const int slot = Ly.slot_table ? Ly.slot_table[e] : e;
+            if (slot < 0 || slot >= Ly.n_slots) return reinterpret_cast<const char*>(1);
+            gu = Ly.gu + (long long)slot * q4_bytes(2 * p.I, p.d);
+            dn = Ly.down + (long long)slot * q4_bytes(p.d, p.I);
+        }
+    }
+    switch (it.kind) {
+        case IT_ROUTER: return Ly.router + ((long long)it.a * n_gd + gh0 + it.b) * kF16Unit;
+        case IT_GU: return gu + ((long long)it.a * n_gd + gh0 + it.b) * kQ4Unit;
+        case IT_LA: return Ly.lora_Ag + (long long)(gh0 + it.b) * kF16Unit;
+        case IT_LU: return Ly.lora_Au + (long long)(gh0 + it.b) * kF16Unit;
+        case IT_BG: return reinterpret_cast<const char*>(Ly.lora_Bg + (long long)it.a * r);
+        case IT_BU: return reinterpret_cast<const char*>(Ly.lora_Bu + (long long)it.a * r);
+        case IT_DSC:
+            return dn + (long long)it.a * n_rtd * kQ4Unit + 4LL * n_rtd * kQ4Quarter + (long long)rt0 * kQ4Scales;
+        case IT_DQ:
+            return dn + (long long)(it.a / 4) * n_rtd * kQ4Unit + ((long long)(it.a % 4) * n_rtd + rt0) * kQ4Quarter;
+        case IT_ADT: return reinterpret_cast<const char*>(Ly.lora_AdT + (long long)it.a * r);
+        case IT_BD: return reinterpret_cast<const char*>(Ly.lora_Bd + (long long)it.a * r);
+        case IT_FC1: return Ly.fc1 + ((long long)it.a * n_gd + gh0 + it.b) * kF16Unit;
+        case IT_FC2: return Ly.fc2 + ((long long)it.a * (p.E / kRowTile) + it.b) * kF16Step;
+        default: return Ly.linit + ((long long)it.a * n_gd + gh0 + it.b) * kF16Unit;
+    }
+}
+
 __device__ void producer(Ctx& c) {
     const Prog& p = *c.p;
     Ctl* ctl = c.ctl;
-    uint64_t* full = reinterpret_cast<uint64_t*>(c.sm + c.pl.full);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(c.sm + c.pl.empty);
-    volatile int* ready = reinterpret_cast<volatile int*>(c.sm + c.pl.ready);
+    volatile int* ready = SM<volatile int>(c, c.pl.ready);
+    int* lstart = SM<int>(c, c.pl.lin);   // linear start of the item in each slot
     const uint64_t pol = policy_evict_first();
-    const int step = c.step;
-    int stage = 0;
-    uint32_t round = 0;
-    int issued = 0;
-    int pi = 0;
-
+    char* ring = c.sm + c.pl.ring;
+    int lin = 0;      // linear ring position of the next item
+    int k = 0;        // global index of the next item
+    int front = 0;    // oldest item not known to be released
     for (int l = 0; l < p.L; ++l) {
-        const LayerP& Ly = p.layers[l];
-        for (int ph = PH_R; ph <= PH_B; ++ph) {
-            if (ph == PH_R && !has_router_phase(p, l, step)) continue;
-            // the list slot is free once the consumers finished phase pi - kListSlots
-            if (!wait_flag(&ctl->cdone, pi - kListSlots + 1, c.hdr, ctl)) return;
-            if (ph != PH_R) {
-                if (!wait_flag(&ready[l], 1, c.hdr, ctl)) return;
+        // the table slot is free once the consumers finished layer l - kTables
+        if (!wait_flag(c, &ctl->cdone, l - kTables + 1)) return;
+        LayerTab* T = tab_of(c, l);
+        T->k0 = k;
+        const Shape Sh = layer_shape(p, l, has_router_phase(p, l, c.step));
+        if (!build_items(Sh, c.P, c.pair, c.rank, p.ring_bytes, T, lin)) {
+            raise_error(c, EDGE0_EUNSUPPORTED);
+            return;
+        }
+        __threadfence_block();
+        *(volatile int*)&T->seq = l + 1;
+        bool have_routing = false;
+        for (int i = 0; i < T->n; ++i, ++k) {
+            const Item& it = T->it[i];
+            if (!have_routing && (it.kind == IT_GU || it.kind == IT_DSC || it.kind == IT_DQ) &&
+                T->pl.seg[it.seg].slot >= 0) {
+                if (!wait_flag(c, &ready[l], 1)) return;
                 __threadfence_block();
+                have_routing = true;
             }
-            PhaseList* Lp = list_slot(c, pi);
-            const int* ids = sm_ids(c, l);
-            const int total = build_segments(c, l, ph, ids, Lp);
-            if (total < 0) { raise_error(c.hdr, ctl, EDGE0_EINVAL); return; }
-            // previous-token mask rows for the head's one-hot columns
-            const int32_t* prev = nullptr;
-            if (p.mode == MODE_HEAD) prev = p.prev_in;
-            else if (p.mode == MODE_DECODE && step > 0)
-                prev = p.exec_ids + (((long long)((step - 1) & 1) * p.Ls + Ly.sidx) * p.B) * p.K;
-            const int n_prev = prev ? p.K : 0;
-            for (int i = 0; i < n_prev * p.B; ++i)
-                if (prev[i] < 0 || prev[i] >= p.E) { raise_error(c.hdr, ctl, EDGE0_EINVAL); return; }
-            if (ph != PH_R)
-                for (int i = 0; i < p.K * p.B; ++i)
-                    if (ids[i] < 0 || ids[i] >= p.E) { raise_error(c.hdr, ctl, EDGE0_EINVAL); return; }
-            const int rc = build_chunks(c, total, n_prev, Lp);
-            if (rc) { raise_error(c.hdr, ctl, rc); return; }
-            __threadfence_block();
-            *(volatile int*)&Lp->seq = pi + 1;
-            for (int i = 0; i < Lp->nch; ++i) {
-                const Chunk& x = Lp->ch[i];
-                if (!mbar_wait(&empty[stage], (round & 1) ^ 1, c.hdr, ctl)) return;
-                char* dst = c.sm + c.pl.stage + stage * kStageBytes;
-                mbar_arrive_expect_tx(&full[stage], (uint32_t)x.bytes);
-                const Seg& s = Lp->seg[x.seg];
-                switch (x.aux) {
-                    case AUX_UNITS:
-                        bulk_g2s(dst, s.base + (long long)x.u0 * s.ub, x.bytes, &full[stage], pol);
-                        break;
-                    case AUX_BG:
-                        bulk_g2s(dst, Ly.lora_Bg, x.bytes, &full[stage], pol);
-                        break;
-                    case AUX_BU:
-                        bulk_g2s(dst, Ly.lora_Bu, x.bytes, &full[stage], pol);
-                        break;
-                    case AUX_AD:
-                        bulk_g2s(dst, Ly.lora_Ad, x.bytes, &full[stage], pol);
-                        break;
-                    case AUX_BD:
-                        bulk_g2s(dst, Ly.lora_Bd + (long long)x.u0 * kRowTile * p.r, x.bytes,
-                                 &full[stage], pol);
-                        break;
-                    case AUX_FC1OH:
-                    case AUX_LINOH: {
-                        const bool f = x.aux == AUX_FC1OH;
-                        const int rowlen = f ? p.H : p.E;
-                        const __half* tab = f ? Ly.fc1_oh : Ly.linit_oh;
-                        const int* ex = ids + x.tok * p.K;
-                        for (int k = 0; k < p.K; ++k)
-                            bulk_g2s(dst + k * rowlen * 2, tab + (long long)ex[k] * rowlen,
-                                     rowlen * 2, &full[stage], pol);
-                        for (int k = 0; k < n_prev; ++k)
-                            bulk_g2s(dst + (p.K + k) * rowlen * 2,
-                                     tab + (long long)(p.E + prev[x.tok * p.K + k]) * rowlen,
-                                     rowlen * 2, &full[stage], pol);
-                        break;
-                    }
-                }
-                ++issued;
-                *(volatile int*)&ctl->issued = issued;
-                if (++stage == kStages) { stage = 0; ++round; }
+            const char* src = item_src(c, l, T, it);
+            if (src == reinterpret_cast<const char*>(1)) { raise_error(c, EDGE0_EINVAL); return; }
+            // wait until slot k is free and the item's ring bytes no longer hold live items
+            while (front < k && (front <= k - kSlots || it.lin + it.bytes - lstart[front % kSlots] > p.ring_bytes)) {
+                if (!mbar_wait(c, empty_bar(c, front), item_parity(front))) return;
+                ++front;
             }
-            ++pi;
+            lstart[k % kSlots] = it.lin;
+            uint64_t* fb = full_bar(c, k);
+            if (src) {
+                mbar_arrive_expect_tx(fb, (uint32_t)it.bytes);
+                bulk_g2s(ring + it.off, src, (uint32_t)it.bytes, fb, pol);
+            } else {
+                mbar_arrive(fb);
+            }
+            *(volatile int*)&ctl->issued = k + 1;
         }
     }
 }
 
 // ------------------------------------------------------------ consumers ----
-__device__ __forceinline__ void cbar() { named_bar_sync(1, kConsumerThreads); }
+__device__ __forceinline__ bool wait_item(const Ctx& c, const LayerTab* T, int i) {
+    return mbar_wait(c, full_bar(c, T->k0 + i), item_parity(T->k0 + i));
+}
+__device__ __forceinline__ void release_item(const Ctx& c, const LayerTab* T, int i) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar(c, T->k0 + i));
+}
 
-__device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile int*)&c.ctl->abort != 0; }
-
-// grid-wide barrier among the consumer warps of all CTAs
-__device__ bool grid_barrier(Ctx& c, unsigned long long& target) {
-    cbar();
-    bool ok = true;
+// grid barrier: arrive (after the caller's cbar) and wait
+__device__ void bar_arrive(const Ctx& c) {
     if (threadIdx.x == 0) {
         __threadfence();
         red_release_add_u64(&c.hdr->barrier, 1ull);
+    }
+}
+__device__ bool bar_wait(const Ctx& c, unsigned long long& target) {
+    if (threadIdx.x == 0) {
         target += (unsigned long long)c.nct;
         if (ld_acquire_u64(&c.hdr->barrier) < target) {
             const unsigned long long t0 = now_ns();
             for (unsigned it = 0; ld_acquire_u64(&c.hdr->barrier) < target; ++it) {
                 if ((it & 15) == 15) {
-                    if (should_abort(c.hdr, c.ctl)) { ok = false; break; }
-                    if (now_ns() - t0 > kTimeoutNs) { raise_error(c.hdr, c.ctl, EDGE0_ETIMEOUT); ok = false; break; }
+                    if (should_abort(c)) { *(volatile int*)&c.ctl->abort = 1; break; }
+                    if (now_ns() - t0 > kTimeoutNs) { raise_error(c, EDGE0_ETIMEOUT); break; }
                 }
             }
         }
-        if (!ok) c.ctl->abort = 1;
+    }
+    return !cbar_or(aborted(c));
+}
+
+// send nfloats (multiple of 4) from this CTA's `src` into the peer's copy of
+// `dst`, and wait for the peer's data in this CTA's `dst` (exchange barrier `which`)
+__device__ bool exchange(const Ctx& c, int which, const float* src, float* dst, int nfloats,
+                         uint32_t& phase) {
+    uint64_t* bar = SM<uint64_t>(c, c.pl.xch) + which;
+    const uint32_t peer = c.rank ^ 1u;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nfloats * 4));
+    const uint32_t rbar = mapa_shared(smem_u32(bar), peer);
+    const uint32_t rdst = mapa_shared(smem_u32(dst), peer);
+    for (int i = threadIdx.x; i < nfloats / 4; i += kConsumerThreads)
+        st_async_v4(rdst + 16u * i, reinterpret_cast<const uint4*>(src)[i], rbar);
+    const bool ok = mbar_wait(c, bar, phase & 1u);
+    ++phase;
+    return ok;
+}
+
+// B fragment of the x source for lane (g, t): token g / 2 in the even columns
+struct XFrag {
+    const uint2* base;
+    int stride;   // uint2 per 16-input step
+    bool live;
+};
+__device__ __forceinline__ XFrag xfrag(const Ctx& c) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, tok = g >> 1;
+    XFrag f;
+    f.live = !(g & 1) && tok < c.p->B;
+    f.base = SM<uint2>(c, c.pl.xf) + (f.live ? tok : 0) * 4 + t;
+    f.stride = c.p->B * 4;
+    return f;
+}
+
+__device__ __forceinline__ void q4_masks(uint32_t w, uint32_t A[4]) {
+    const uint32_t w8 = w >> 8;
+    A[0] = w & 0x000F000Fu;    // row g,   k 2t | 2t+1
+    A[1] = w & 0x00F000F0u;    // row g+8, k 2t | 2t+1   (x16)
+    A[2] = w8 & 0x000F000Fu;   // row g,   k 2t+8 | 2t+9
+    A[3] = w8 & 0x00F000F0u;   // row g+8, k 2t+8 | 2t+9 (x16)
+}
+
+// int4 units [a, b) of a run whose unit j is local group gl0 + j of one row
+// tile: adds s 2^24 acc + b xsum per unit to rows g (r0) and g + 8 (r1), token t
+__device__ __forceinline__ void q4_run(const Ctx& c, const char* base, int a, int b, int gl0,
+                                       float& r0, float& r1) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int B = c.p->B;
+    const XFrag xf = xfrag(c);
+    const float* xs = SM<float>(c, c.pl.xsum);
+    for (int j = a; j < b; ++j) {
+        const char* unit = base + (long long)j * kQ4Unit;
+        const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+        const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g);
+        const int gl = gl0 + j;
+        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            uint2 bb = make_uint2(0u, 0u);
+            if (xf.live) bb = xf.base[(gl * 4 + s) * xf.stride];
+            uint32_t A[4];
+            q4_masks(w[s], A);
+            mma_16816(acc, A, bb.x, bb.y);
+        }
+        const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) of row g
+        const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) of row g + 8
+        const float x = t < B ? xs[gl * B + t] : 0.f;
+        r0 += __low2float(s0) * kTwo24 * acc[0] + __high2float(s0) * x;
+        r1 += __low2float(s1) * (kTwo24 / 16.0f) * acc[2] + __high2float(s1) * x;
+    }
+}
+
+// fp16 units [a, b) (x source) accumulated into acc (rows g, g + 8; column 2t = token t)
+__device__ __forceinline__ void f16_run(const Ctx& c, const char* base, int a, int b, int gl0, float acc[4]) {
+    const int lane = threadIdx.x & 31;
+    const XFrag xf = xfrag(c);
+    for (int j = a; j < b; ++j) {
+        const char* unit = base + (long long)j * kF16Unit;
+        const int gl = gl0 + j;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const uint4 av = *reinterpret_cast<const uint4*>(unit + s * kF16Step + 16 * lane);
+            uint2 bb = make_uint2(0u, 0u);
+            if (xf.live) bb = xf.base[(gl * 4 + s) * xf.stride];
+            const uint32_t A[4] = {av.x, av.y, av.z, av.w};
+            mma_16816(acc, A, bb.x, bb.y);
+        }
+    }
+}
+
+// ------------------------------------------------------------ prologue ----
+// x = fp16(RMSNorm(h) * gamma) for all tokens (decode; h updated by the previous
+// layer's y first) or x = x_in; B fragments and group sums for this CTA's half
+// of d.  The residual h stays in shared memory.
+__device__ void build_x(Ctx& c, int l) {
+    const Prog& p = *c.p;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int B = p.B, d = p.d, n4 = B * d / 4;
+    const bool decode = p.mode == MODE_DECODE;
+    const LayerP& Ly = p.layers[l];
+    __half* hs = SM<__half>(c, c.pl.hs);
+    const float* y = (decode && l > 0) ? y_buf(c, c.par, p.layers[l - 1].sidx) : nullptr;
+    const __half* hsrc = decode ? (l == 0 ? p.h_io : hs) : p.x_in;
+    const __half* gam = decode ? Ly.gamma : nullptr;
+    uint2 hv[kMaxChunks], gv[kMaxChunks];
+    float4 yv[kMaxChunks];
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j) {
+        const int i = tid + j * kConsumerThreads;
+        if (i < n4) {
+            hv[j] = *reinterpret_cast<const uint2*>(hsrc + 4 * i);
+            yv[j] = y ? __ldcg(reinterpret_cast<const float4*>(y + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[j] = gam ? __ldg(reinterpret_cast<const uint2*>(gam + (4 * i) % d)) : make_uint2(0x3C003C00u, 0x3C003C00u);
+        }
+    }
+    float hf[kMaxChunks][4];
+    float ss[EDGE0_MAX_BATCH] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j) {
+        const int i = tid + j * kConsumerThreads;
+        if (i < n4) {
+            const __half2 h01 = *reinterpret_cast<const __half2*>(&hv[j].x);
+            const __half2 h23 = *reinterpret_cast<const __half2*>(&hv[j].y);
+            float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
+            if (y) {
+                v[0] = __half2float(__float2half_rn(v[0] + yv[j].x));
+                v[1] = __half2float(__float2half_rn(v[1] + yv[j].y));
+                v[2] = __half2float(__float2half_rn(v[2] + yv[j].z));
+                v[3] = __half2float(__float2half_rn(v[3] + yv[j].w));
+            }
+            if (decode) {
+                __half2 o01 = __floats2half2_rn(v[0], v[1]), o23 = __floats2half2_rn(v[2], v[3]);
+                uint2 o;
+                o.x = *reinterpret_cast<uint32_t*>(&o01);
+                o.y = *reinterpret_cast<uint32_t*>(&o23);
+                *reinterpret_cast<uint2*>(hs + 4 * i) = o;
+            }
+            const int b = (4 * i) / d;
+            const float q = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+            for (int bb = 0; bb < EDGE0_MAX_BATCH; ++bb) if (bb == b) ss[bb] += q;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hf[j][e] = v[e];
+        }
+    }
+    float* red = SM<float>(c, c.pl.red);
+    float* rs = red + B * kConsumerWarps;
+    if (decode) {
+        for (int b = 0; b < B; ++b) {
+            const float s = warp_sum(ss[b]);
+            if (lane == 0) red[b * kConsumerWarps + wid] = s;
+        }
+        cbar();
+        if (tid < B) {
+            float s = 0.f;
+            for (int w = 0; w < kConsumerWarps; ++w) s += red[tid * kConsumerWarps + w];
+            rs[tid] = rsqrtf(s / (float)d + Ly.eps);
+        }
+        cbar();
+    }
+    uint32_t* xf = SM<uint32_t>(c, c.pl.xf);
+    float* xsum = SM<float>(c, c.pl.xsum);
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j) {
+        const int i = tid + j * kConsumerThreads;
+        if (j * kConsumerThreads >= n4) break;   // uniform over the CTA
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        int b = 0, k = 0;
+        if (i < n4) {
+            b = (4 * i) / d;
+            k = (4 * i) % d;
+            const __half2 g01 = *reinterpret_cast<const __half2*>(&gv[j].x);
+            const __half2 g23 = *reinterpret_cast<const __half2*>(&gv[j].y);
+            const float gg[4] = {__low2float(g01), __high2float(g01), __low2float(g23), __high2float(g23)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                x[e] = decode ? __half2float(__float2half_rn(hf[j][e] * rs[b] * gg[e])) : hf[j][e];
+        }
+        // group sum over the 16 threads that hold one group
+        float s4 = x[0] + x[1] + x[2] + x[3];
+#pragma unroll
+        for (int m = 8; m; m >>= 1) s4 += __shfl_xor_sync(0xffffffffu, s4, m);
+        const int grp = k / kGroup;
+        if (i < n4 && grp >= c.hv.gh0 && grp < c.hv.gh1) {
+            const int kk = k % kGroup;
+            const int sl = (grp - c.hv.gh0) * 4 + kk / 16;
+            const int k1 = kk % 16, t1 = (k1 & 7) >> 1, w = k1 >> 3;
+            const __half2 x01 = __floats2half2_rn(x[0], x[1]), x23 = __floats2half2_rn(x[2], x[3]);
+            xf[((sl * B + b) * 4 + t1) * 2 + w] = *reinterpret_cast<const uint32_t*>(&x01);
+            xf[((sl * B + b) * 4 + t1 + 1) * 2 + w] = *reinterpret_cast<const uint32_t*>(&x23);
+            if ((lane & 15) == 0) xsum[(grp - c.hv.gh0) * B + b] = s4;
+        }
     }
     cbar();
-    return !aborted(c);
 }
 
-// B-fragment / sum pointers of tensor-core column n of segment s (null when
-// inactive).  Column n carries token n / 2: its hi part (n even) or its lo part
-// (n odd, activation sources only; x is exactly fp16 and has no lo part).
-__device__ __forceinline__ void col_src(const Ctx& c, const Seg& s, int l, int n, const __half** f,
-                                        const float** sum) {
+// ------------------------------------------------------------- phases -----
+// units of the unit items in [ia, ib) split over the warps; f(item, local unit
+// range) runs on items the warp has units in; every item is released by every warp
+template <class F>
+__device__ bool warp_units(const Ctx& c, const LayerTab* T, int ia, int ib, F&& f) {
+    const int wid = threadIdx.x >> 5;
+    int tot = 0;
+    for (int i = ia; i < ib; ++i)
+        if (unit_kind(T->it[i].kind)) tot += T->it[i].n;
+    int ua, ub;
+    split_range(tot, kConsumerWarps, wid, &ua, &ub);
+    int u = 0;
+    bool ok = true;
+    for (int i = ia; i < ib; ++i) {
+        const Item& it = T->it[i];
+        if (!unit_kind(it.kind)) continue;
+        const int a = ua - u > 0 ? ua - u : 0, b = ub - u < it.n ? ub - u : it.n;
+        u += it.n;
+        if (a < b && ok) {
+            if (!wait_item(c, T, i)) ok = false;
+            else f(it, a, b);
+        }
+        release_item(c, T, i);
+    }
+    return ok;
+}
+
+__device__ __forceinline__ bool seg_live(const Ctx& c, int l, const Seg& s) {
+    return s.slot < 0 || s.slot < SM<int>(c, c.pl.ndist)[l];
+}
+
+// own router: partial logits of this CTA's units, into the layer's logits
+__device__ bool phase_router(Ctx& c, int l, const LayerTab* T) {
     const Prog& p = *c.p;
-    *f = nullptr;
-    *sum = nullptr;
-    const int b = n >> 1, part = n & 1;
-    if (b >= p.B) return;
-    const char* sm = c.sm;
-    switch (s.src) {
-        case SRC_X:
-            if (part) return;
-            *f = reinterpret_cast<const __half*>(sm + c.pl.xf) + (long long)b * p.d;
-            *sum = reinterpret_cast<const float*>(sm + c.pl.xsum) + b * (p.d / kGroup);
-            break;
-        case SRC_ACT: {
-            const int* ids = sm_ids(c, l) + b * p.K;
-            const long long npair = (long long)p.B * p.K;
-            for (int k = 0; k < p.K; ++k)
-                if (ids[k] == s.expert) {
-                    const long long pr = b * p.K + k + part * npair;
-                    *f = reinterpret_cast<const __half*>(sm + c.pl.actf) + pr * p.I;
-                    *sum = reinterpret_cast<const float*>(sm + c.pl.actsum) + pr * (p.I / kGroup);
-                    break;
-                }
-            break;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    float* lg = logr_buf(c, c.par, p.layers[l].sidx);
+    return warp_units(c, T, 0, T->p1, [&](const Item& it, int a, int b) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        f16_run(c, ring_at(c, it), a, b, it.b, acc);
+        const int row = it.a * kRowTile + g;
+        if (t < p.B) {
+            if (row < p.E) red_add_f32(lg + t * p.E + row, acc[0]);
+            if (row + 8 < p.E) red_add_f32(lg + t * p.E + row + 8, acc[2]);
         }
-        case SRC_ACTSH: {
-            const long long r = b + part * p.B;
-            *f = reinterpret_cast<const __half*>(sm + c.pl.ashf) + r * p.Is;
-            *sum = reinterpret_cast<const float*>(sm + c.pl.ashsum) + r * (p.Is / kGroup);
-            break;
-        }
-        default: {
-            const long long r = b + part * p.B;
-            *f = reinterpret_cast<const __half*>(sm + c.pl.gf) + r * p.H;
-            *sum = reinterpret_cast<const float*>(sm + c.pl.gsum) + r * (p.H / kGroup);
-            break;
+    });
+}
+
+// routing of an own-routed layer from its complete router logits
+__device__ void route_layer(Ctx& c, int l) {
+    const Prog& p = *c.p;
+    const LayerP& Ly = p.layers[l];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    float* scr = SM<float>(c, c.pl.rscr);
+    const float* lg = logr_buf(c, c.par, Ly.sidx);
+    for (int i = tid; i < p.B * p.E; i += kConsumerThreads) {
+        const int b = i / p.E, e = i - b * p.E;
+        scr[b * 3 * p.E + e] = __ldcg(lg + i);
+    }
+    cbar();
+    for (int b = wid; b < p.B; b += kConsumerWarps) {
+        __shared__ int rid[EDGE0_MAX_BATCH][EDGE0_MAX_K];
+        __shared__ float rw[EDGE0_MAX_BATCH][EDGE0_MAX_K];
+        warp_route(scr + b * 3 * p.E, p.E, p.K, Ly.route_kind, Ly.n_groups, Ly.topk_groups,
+                   Ly.route_scale, Ly.bias, scr + b * 3 * p.E + p.E, rid[b], rw[b], lane);
+        if (lane < p.K) {
+            ids_of(c, l)[b * p.K + lane] = rid[b][lane];
+            w_of(c, l)[b * p.K + lane] = rw[b][lane];
         }
     }
+    cbar();
+    if (tid == 0) {
+        if (!make_dist(c, l)) raise_error(c, EDGE0_EINVAL);
+        __threadfence_block();
+        SM<volatile int>(c, c.pl.ready)[l] = 1;
+    }
+    cbar();
 }
 
-// k slot of token b for routed segment s (-1: token does not use this expert)
-__device__ __forceinline__ int col_kslot(const Ctx& c, const Seg& s, int l, int b) {
-    if (s.expert < 0) return 0;
-    const int* ids = sm_ids(c, l) + b * c.p->K;
-    for (int k = 0; k < c.p->K; ++k)
-        if (ids[k] == s.expert) return k;
+// P1: partial gate/up (+ LoRA A x) sums of the pair's rows over this CTA's half of d
+__device__ bool phase1(Ctx& c, int l, const LayerTab* T) {
+    const int B = c.p->B;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    float* part = SM<float>(c, c.pl.part);
+    const int nlp = T->pl.n_hr * 16 * B;
+    return warp_units(c, T, T->p1, T->p2, [&](const Item& it, int a, int b) {
+        const Seg& sg = T->pl.seg[it.seg];
+        if (!seg_live(c, l, sg)) return;
+        if (it.kind == IT_GU) {
+            float r0 = 0.f, r1 = 0.f;
+            q4_run(c, ring_at(c, it), a, b, it.b, r0, r1);
+            const int hl = sg.hoff + it.a - sg.hr0;
+            if (t < B) {
+                atomicAdd(&part[(hl * 16 + g) * B + t], r0);
+                atomicAdd(&part[(hl * 16 + 8 + g) * B + t], r1);
+            }
+        } else {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            f16_run(c, ring_at(c, it), a, b, it.b, acc);
+            const int m = it.kind == IT_LA ? 0 : 1;
+            if (t < B) {
+                atomicAdd(&part[nlp + (m * 16 + g) * B + t], acc[0]);
+                atomicAdd(&part[nlp + (m * 16 + 8 + g) * B + t], acc[2]);
+            }
+        }
+    });
+}
+
+// index of the first item of `kind` for segment s in [ia, ib), or -1
+__device__ __forceinline__ int find_item(const LayerTab* T, int ia, int ib, int kind, int s) {
+    for (int i = ia; i < ib; ++i)
+        if (T->it[i].kind == kind && T->it[i].seg == s) return i;
     return -1;
 }
 
-__device__ __forceinline__ float* out_ptr(const Ctx& c, const Seg& s, float* F, int row, int b, int k) {
-    const Prog& p = *c.p;
-    const AccLayout& a = c.acc;
-    switch (s.out) {
-        case OUT_GUG: return F + a.gu + ((long long)(b * p.K + k) * 2 + 0) * p.I + row;
-        case OUT_GUU: return F + a.gu + ((long long)(b * p.K + k) * 2 + 1) * p.I + row;
-        case OUT_GUSG: return F + a.gus + ((long long)b * 2 + 0) * p.Is + row;
-        case OUT_GUSU: return F + a.gus + ((long long)b * 2 + 1) * p.Is + row;
-        case OUT_AG: return F + a.aacc + ((long long)b * 2 + 0) * c.R16 + row;
-        case OUT_AU: return F + a.aacc + ((long long)b * 2 + 1) * c.R16 + row;
-        case OUT_Z: return F + a.z + (long long)b * p.H + row;
-        case OUT_LIN: return F + a.lin + (long long)b * p.E + row;
-        case OUT_Y: return F + a.y + (long long)b * p.d + row;
-        case OUT_LOGR: return F + a.logr + (long long)b * p.E + row;
-        default: return F + a.logh + (long long)b * p.E + row;
-    }
-}
-
-// ----------------------------------------------------------- prologues -----
-// x = fp16(h rsqrt(mean h^2 + eps) gamma) for all tokens, written as B fragments.
-// hsrc: fp16 [B, d]; ysrc: fp32 [B, d] added first (h = fp16(hsrc + ysrc)), or null.
-// hdst: where CTA 0 stores the updated h (or null).  norm=false: x = hsrc.
-__device__ void build_x(Ctx& c, const __half* hsrc, const float* ysrc, __half* hdst,
-                        const __half* gamma, float eps, bool norm) {
-    const Prog& p = *c.p;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int B = p.B, d = p.d;
-    __half* xf = reinterpret_cast<__half*>(c.sm + c.pl.xf);
-    float* xsum = reinterpret_cast<float*>(c.sm + c.pl.xsum);
-    float* red = reinterpret_cast<float*>(c.sm + c.pl.red);
-    __half* hs = reinterpret_cast<__half*>(c.sm + c.pl.hs);   // the (updated) h, fp16
-    float ss[EDGE0_MAX_BATCH];
-#pragma unroll
-    for (int b = 0; b < EDGE0_MAX_BATCH; ++b) ss[b] = 0.f;
-    for (int i = tid; i < B * d; i += kConsumerThreads) {
-        float v = __half2float(hsrc[i]);
-        if (ysrc) v += ysrc[i];
-        const __half hv = __float2half_rn(v);
-        hs[i] = hv;
-        if (hdst && c.cta == 0) hdst[i] = hv;
-        const float f = __half2float(hv);
-        const int b = i / d;
-#pragma unroll
-        for (int bb = 0; bb < EDGE0_MAX_BATCH; ++bb)
-            if (bb == b) ss[bb] += f * f;
-    }
-    if (norm) {
-        for (int b = 0; b < B; ++b) {
-            float s = ss[b];
-#pragma unroll
-            for (int k = 16; k; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
-            if (lane == 0) red[b * kConsumerWarps + wid] = s;
-        }
-    }
-    cbar();
-    float* rs = red + B * kConsumerWarps;
-    if (norm && tid < B) {
-        float s = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) s += red[tid * kConsumerWarps + w];
-        rs[tid] = rsqrtf(s / (float)d + eps);
-    }
-    cbar();
-    const int ng = d / kGroup;
-    for (int it = wid; it < B * ng; it += kConsumerWarps) {
-        const int b = it / ng, grp = it - b * ng;
-        const int i0 = grp * kGroup + lane, i1 = i0 + 32;
-        float v0 = __half2float(hs[b * d + i0]), v1 = __half2float(hs[b * d + i1]);
-        if (norm) {
-            const float r = rs[b];
-            v0 = __half2float(__float2half_rn(v0 * r * (gamma ? __half2float(gamma[i0]) : 1.0f)));
-            v1 = __half2float(__float2half_rn(v1 * r * (gamma ? __half2float(gamma[i1]) : 1.0f)));
-        }
-        put_group(xf + (long long)b * d + grp * kGroup, xsum + b * ng + grp, v0, v1, lane);
-    }
-    cbar();
-}
-
-// zero this CTA's slice of accumulator set (pc % 3)
-__device__ void zero_set_slice(const Ctx& c, unsigned pc) {
-    float* F = acc_set(c, pc);
-    const long long n = c.acc.total;
-    const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
-    for (long long i = a + threadIdx.x; i < b; i += kConsumerThreads) F[i] = 0.f;
-}
-
-// top-K of a finished head: logits in set `pc`, written to pred[step & 1][target]
-__device__ void head_topk(Ctx& c, int l, unsigned pc) {
+// act = silu(gate) * up of all the pair's rows (partials of both CTAs, LoRA B
+// terms for shared rows) -> hi/lo B fragments per 16-row quarter and their sums;
+// v = A_down act for the shared rows (LoRA).  Every consumer thread runs every
+// barrier here; the result is CTA-uniform.
+__device__ bool compute_act(Ctx& c, int l, const LayerTab* T, bool lora) {
     const Prog& p = *c.p;
     const LayerP& Ly = p.layers[l];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    float* F = acc_set(c, pc);
-    float* scr = reinterpret_cast<float*>(c.sm + c.pl.rscr);   // 2E floats per token
-    for (int b = wid; b < p.B; b += kConsumerWarps) {
-        __shared__ int tids[EDGE0_MAX_BATCH][EDGE0_MAX_K];
-        __shared__ float tw[EDGE0_MAX_BATCH][EDGE0_MAX_K];
-        warp_route(F + c.acc.logh + (long long)b * p.E, p.E, p.K, Ly.head_route_kind, Ly.head_n_groups,
-                   Ly.head_topk_groups, Ly.head_route_scale, Ly.head_bias,
-                   scr + (long long)b * 2 * p.E, tids[b], tw[b], lane);
-        if (lane < p.K) {
-            if (p.mode == MODE_HEAD) {
-                p.out_ids[b * p.K + lane] = tids[b][lane];
-                p.out_w[b * p.K + lane] = tw[b][lane];
-            } else {
-                const long long o = (((long long)(c.step & 1) * p.Ls + Ly.head_target) * p.B + b) * p.K + lane;
-                p.pred_ids[o] = tids[b][lane];
-                p.pred_w[o] = tw[b][lane];
+    const int B = p.B, r = p.r, tid = threadIdx.x;
+    const PairPlan& pl = T->pl;
+    const float* part = SM<float>(c, c.pl.part);
+    const float* recv = SM<float>(c, c.pl.recv);
+    float* act32 = SM<float>(c, c.pl.act32);
+    __half* af = SM<__half>(c, c.pl.af);
+    float* qsum = SM<float>(c, c.pl.qsum);
+    float* vlo = SM<float>(c, c.pl.vlo);
+    const int nlp = pl.n_hr * 16 * B;
+    // LoRA items of the shared segment (segment 0 of a pair that owns shared rows)
+    int ibg = -1, ibu = -1, iadt = -1, ssh = -1;
+    bool ok = true;
+    if (lora && pl.has_sh) {
+        ssh = 0;
+        ibg = find_item(T, T->p1, T->p2, IT_BG, ssh);
+        ibu = find_item(T, T->p1, T->p2, IT_BU, ssh);
+        iadt = find_item(T, T->p2, T->p3, IT_ADT, ssh);
+        ok = ibg >= 0 && ibu >= 0 && iadt >= 0;
+        if (!ok && tid == 0) raise_error(c, EDGE0_EINVAL);
+        ok = ok && wait_item(c, T, ibg) && wait_item(c, T, ibu) && wait_item(c, T, iadt);
+    }
+    for (int i = tid; i < pl.n_q * B * 2 * 4 * 4; i += kConsumerThreads) af[i] = __float2half_rn(0.f);
+    for (int i = tid; i < pl.n_q * B; i += kConsumerThreads) qsum[i] = 0.f;
+    ok = !cbar_or(!ok);
+    for (int i = tid; ok && i < pl.n_hr * 8 * B; i += kConsumerThreads) {
+        const int hl = i / (8 * B), g = (i / B) % 8, b = i % B;
+        int s = 0;
+        while (s + 1 < pl.nseg && hl >= pl.seg[s + 1].hoff) ++s;
+        const Seg& sg = pl.seg[s];
+        float a = 0.f;
+        if (seg_live(c, l, sg)) {
+            const int row = (sg.hr0 + hl - sg.hoff) * kHalfRow + g;   // act row of the expert
+            float gate = part[(hl * 16 + g) * B + b] + recv[(hl * 16 + g) * B + b];
+            float up = part[(hl * 16 + 8 + g) * B + b] + recv[(hl * 16 + 8 + g) * B + b];
+            if (s == ssh) {
+                const int rl = row - sg.hr0 * kHalfRow;
+                const __half* bg = reinterpret_cast<const __half*>(ring_at(c, T->it[ibg])) + rl * r;
+                const __half* bu = reinterpret_cast<const __half*>(ring_at(c, T->it[ibu])) + rl * r;
+                float dg = 0.f, du = 0.f;
+                for (int q = 0; q < r; ++q) {
+                    dg += __half2float(bg[q]) * (part[nlp + q * B + b] + recv[nlp + q * B + b]);
+                    du += __half2float(bu[q]) * (part[nlp + (16 + q) * B + b] + recv[nlp + (16 + q) * B + b]);
+                }
+                gate += Ly.lora_scale * dg;
+                up += Ly.lora_scale * du;
+            }
+            a = silu_f(gate) * up;
+            const int Ql = sg.qoff + row / 16 - sg.q0;
+            const int k1 = row % 16, t1 = (k1 & 7) >> 1, w = k1 >> 3, sub = k1 & 1;
+            const __half hi = __float2half_rn(a);
+            const __half lo = __float2half_rn((a - __half2float(hi)) * kLoScale);
+            af[(((Ql * B + b) * 2 + 0) * 4 + t1) * 4 + w * 2 + sub] = hi;
+            af[(((Ql * B + b) * 2 + 1) * 4 + t1) * 4 + w * 2 + sub] = lo;
+            atomicAdd(&qsum[Ql * B + b], a);
+        }
+        act32[(hl * 8 + g) * B + b] = a;
+    }
+    cbar();
+    if (ok && ssh >= 0) {
+        // v[q][b] = sum over the pair's shared act rows of A_down[q][row] act[row][b]
+        const Seg& sg = pl.seg[ssh];
+        const __half* adt = reinterpret_cast<const __half*>(ring_at(c, T->it[iadt]));
+        const int rows = (sg.hr1 - sg.hr0) * kHalfRow;
+        for (int i = tid; i < r * B; i += kConsumerThreads) {
+            const int q = i / B, b = i % B;
+            float v = 0.f;
+            for (int j = 0; j < rows; ++j) v += __half2float(adt[j * r + q]) * act32[(sg.hoff * 8 + j) * B + b];
+            vlo[q * B + b] = v;
+        }
+    }
+    // the non-unit P1 items (LoRA B rows of gate/up) are no longer needed
+    for (int i = T->p1; i < T->p2; ++i)
+        if (!unit_kind(T->it[i].kind)) release_item(c, T, i);
+    return !cbar_or(!ok);
+}
+
+// P2: down rows of this CTA's half of d over the pair's act quarters -> y
+__device__ bool phase2(Ctx& c, int l, const LayerTab* T, bool lora) {
+    const Prog& p = *c.p;
+    const LayerP& Ly = p.layers[l];
+    const int B = p.B, K = p.K, r = p.r, d = p.d;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    const PairPlan& pl = T->pl;
+    bool ok = true;
+    for (int i = T->p2; i < T->p3 && ok; ++i) ok = wait_item(c, T, i);
+    if (ok && pl.n_hr > 0) {
+        const uint2* afr = SM<uint2>(c, c.pl.af);
+        const float* qsum = SM<float>(c, c.pl.qsum);
+        const float* vlo = SM<float>(c, c.pl.vlo);
+        const int tok = g >> 1, part = g & 1;
+        const bool blive = tok < B;
+        // per-segment token weights (lane's token t)
+        float wt[kMaxSegs];
+        for (int s = 0; s < pl.nseg; ++s) {
+            const Seg& sg = pl.seg[s];
+            wt[s] = 0.f;
+            if (t >= B || !seg_live(c, l, sg)) continue;
+            if (sg.slot < 0) { wt[s] = 1.f; continue; }
+            const int e = dist_of(c, l)[sg.slot];
+            for (int k = 0; k < K; ++k)
+                if (ids_of(c, l)[t * K + k] == e) wt[s] += w_of(c, l)[t * K + k];
+        }
+        // LoRA down rows
+        const int ibd = (lora && pl.has_sh) ? find_item(T, T->p2, T->p3, IT_BD, 0) : -1;
+        const int nrt = c.hv.rt1 - c.hv.rt0;
+        int w0, w1;
+        split_range(nrt, kConsumerWarps, wid, &w0, &w1);
+        float* y = y_buf(c, c.par, Ly.sidx);
+        for (int i = w0; i < w1; ++i) {
+            float y0 = 0.f, y1 = 0.f;
+            for (int s = 0; s < pl.nseg; ++s) {
+                const Seg& sg = pl.seg[s];
+                if (!seg_live(c, l, sg)) continue;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                int gcur = -1;
+                uint2 sc = make_uint2(0u, 0u);
+                auto epilogue = [&]() {
+                    if (gcur < 0) return;
+                    const int qa = sg.q0 > 4 * gcur ? sg.q0 : 4 * gcur;
+                    const int qb = sg.q1 < 4 * gcur + 4 ? sg.q1 : 4 * gcur + 4;
+                    float qs = 0.f;
+                    if (t < B)
+                        for (int Q = qa; Q < qb; ++Q) qs += qsum[(sg.qoff + Q - sg.q0) * B + t];
+                    const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);
+                    const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);
+                    y0 += wt[s] * (__low2float(s0) * kTwo24 * (acc[0] + acc[1] * kLoInv) + __high2float(s0) * qs);
+                    y1 += wt[s] * (__low2float(s1) * (kTwo24 / 16.0f) * (acc[2] + acc[3] * kLoInv) +
+                                   __high2float(s1) * qs);
+                };
+                for (int j = T->p2; j < T->p3; ++j) {
+                    const Item& it = T->it[j];
+                    if (it.seg != s) continue;
+                    if (it.kind == IT_DSC) {
+                        epilogue();
+                        gcur = it.a;
+                        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                        sc = *reinterpret_cast<const uint2*>(ring_at(c, it) + i * kQ4Scales + 8 * g);
+                    } else if (it.kind == IT_DQ) {
+                        const uint32_t wq = *reinterpret_cast<const uint32_t*>(ring_at(c, it) + i * kQ4Quarter + 4 * lane);
+                        const int Ql = sg.qoff + it.a - sg.q0;
+                        uint2 bb = make_uint2(0u, 0u);
+                        if (blive) bb = afr[((Ql * B + tok) * 2 + part) * 4 + t];
+                        uint32_t A[4];
+                        q4_masks(wq, A);
+                        mma_16816(acc, A, bb.x, bb.y);
+                    }
+                }
+                epilogue();
+            }
+            const int row = (c.hv.rt0 + i) * kRowTile + g;
+            if (ibd >= 0 && t < B) {
+                // rows of this CTA's half are split over consecutive BD items
+                const int per = kItemMax / (r * 2);
+                const int rel = row - c.hv.rt0 * kRowTile;
+                const __half* bd0 = reinterpret_cast<const __half*>(ring_at(c, T->it[ibd + rel / per])) + (rel % per) * r;
+                const __half* bd1 = reinterpret_cast<const __half*>(ring_at(c, T->it[ibd + (rel + 8) / per])) + ((rel + 8) % per) * r;
+                float d0 = 0.f, d1 = 0.f;
+                for (int q = 0; q < r; ++q) {
+                    d0 += __half2float(bd0[q]) * vlo[q * B + t];
+                    d1 += __half2float(bd1[q]) * vlo[q * B + t];
+                }
+                y0 += Ly.lora_scale * d0;
+                y1 += Ly.lora_scale * d1;
+            }
+            // rows g..g+3 of lanes with g % 4 == 0 as one vector reduction
+            const float a1 = __shfl_down_sync(0xffffffffu, y0, 4), a2 = __shfl_down_sync(0xffffffffu, y0, 8),
+                        a3 = __shfl_down_sync(0xffffffffu, y0, 12);
+            const float b1 = __shfl_down_sync(0xffffffffu, y1, 4), b2 = __shfl_down_sync(0xffffffffu, y1, 8),
+                        b3 = __shfl_down_sync(0xffffffffu, y1, 12);
+            if (t < B && (g & 3) == 0) {
+                red_add_v4_f32(y + (long long)t * d + row, y0, a1, a2, a3);
+                red_add_v4_f32(y + (long long)t * d + row + 8, y1, b1, b2, b3);
             }
         }
-        __syncwarp();
     }
+    for (int i = T->p2; i < T->p3; ++i) release_item(c, T, i);
+    return ok;
 }
 
-// One warp computes units [ua, ub) of segment s held in `stage` (chunk starting
-// at unit cu0) and adds its per-row partial sums into the accumulator rows sacc
-// (relative to row tile rt0, B columns).
-__device__ void warp_units(const Ctx& c, const Seg& s, int l, const char* stage, int cu0, int ua,
-                           int ub, float* sacc, int rt0) {
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int B = c.p->B;
-    const __half* bf;
-    const float* dummy;
-    col_src(c, s, l, g, &bf, &dummy);
-    const float* sum0;
-    const float* sum1;
-    const __half* f0;
-    const __half* f1;
-    col_src(c, s, l, 2 * t, &f0, &sum0);
-    col_src(c, s, l, 2 * t + 1, &f1, &sum1);
-    const bool q4 = s.kind == 0;
-    const int ng = s.n_g;
-    int cur = -1;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-    float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
-    auto flush = [&](int rt) {
-        float vg, vg8;   // token t: hi column + lo column
-        if (!q4) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { y[i] = lo[i] + 16.0f * hi[i]; lo[i] = 0.f; hi[i] = 0.f; }
-            vg = y[0] + kLoInv * y[1];
-            vg8 = y[2] + kLoInv * y[3];
-        } else {
-            vg = y[0] + y[1];
-            vg8 = y[2] + y[3];
-        }
-        const int r0 = (rt - rt0) * kRowTile + g;
-        if (t < B) {
-            atomicAdd(&sacc[r0 * B + t], vg);
-            atomicAdd(&sacc[(r0 + 8) * B + t], vg8);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) y[i] = 0.f;
-    };
-    int rt = ua / ng, grp = ua - rt * ng;
-    for (int u = ua; u < ub; ++u) {
-        if (rt != cur) {
-            if (cur >= 0) flush(cur);
-            cur = rt;
-        }
-        const char* unit = stage + (u - cu0) * s.ub;
-        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
-        if (bf) {
-            const uint4* bp = reinterpret_cast<const uint4*>(bf + (grp * 4 + t) * 16);
-            b0 = bp[0];
-            b1 = bp[1];
-        }
-        if (q4) {
-            const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
-            const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g);
-            float a4[4] = {0.f, 0.f, 0.f, 0.f};
-            constexpr uint32_t M0 = 0x000F000Fu, M1 = 0x00F000F0u;
-            const uint32_t x8 = wv.x >> 8, z8 = wv.z >> 8, y8 = wv.y >> 8, w8 = wv.w >> 8;
-            uint32_t a[4];
-            a[0] = wv.x & M0; a[1] = wv.z & M0; a[2] = x8 & M0; a[3] = z8 & M0;
-            mma_16816(a4, a, b0.x, b0.y);
-            a[0] = wv.x & M1; a[1] = wv.z & M1; a[2] = x8 & M1; a[3] = z8 & M1;
-            mma_16816(a4, a, b0.z, b0.w);
-            a[0] = wv.y & M0; a[1] = wv.w & M0; a[2] = y8 & M0; a[3] = w8 & M0;
-            mma_16816(a4, a, b1.x, b1.y);
-            a[0] = wv.y & M1; a[1] = wv.w & M1; a[2] = y8 & M1; a[3] = w8 & M1;
-            mma_16816(a4, a, b1.z, b1.w);
-            const __half2 sb0 = *reinterpret_cast<const __half2*>(&sc.x);
-            const __half2 sb1 = *reinterpret_cast<const __half2*>(&sc.y);
-            const float sg = __low2float(sb0) * 16777216.0f, bg = __high2float(sb0);
-            const float sg8 = __low2float(sb1) * 16777216.0f, bg8 = __high2float(sb1);
-            const float xs0 = sum0 ? sum0[grp] : 0.f, xs1 = sum1 ? sum1[grp] : 0.f;
-            // column 2t: hi part of token t; column 2t+1: lo part (scaled by 2^11)
-            y[0] += sg * a4[0] + bg * xs0;
-            y[1] += sg * kLoInv * a4[1] + bg * xs1;
-            y[2] += sg8 * a4[2] + bg8 * xs0;
-            y[3] += sg8 * kLoInv * a4[3] + bg8 * xs1;
-        } else {
-            const uint4 a0 = *reinterpret_cast<const uint4*>(unit + 0 * 512 + 16 * lane);
-            const uint4 a1 = *reinterpret_cast<const uint4*>(unit + 1 * 512 + 16 * lane);
-            const uint4 a2 = *reinterpret_cast<const uint4*>(unit + 2 * 512 + 16 * lane);
-            const uint4 a3 = *reinterpret_cast<const uint4*>(unit + 3 * 512 + 16 * lane);
-            uint32_t a[4];
-            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
-            mma_16816(lo, a, b0.x, b0.y);
-            a[0] = a1.x; a[1] = a1.y; a[2] = a1.z; a[3] = a1.w;
-            mma_16816(hi, a, b0.z, b0.w);
-            a[0] = a2.x; a[1] = a2.y; a[2] = a2.z; a[3] = a2.w;
-            mma_16816(lo, a, b1.x, b1.y);
-            a[0] = a3.x; a[1] = a3.y; a[2] = a3.z; a[3] = a3.w;
-            mma_16816(hi, a, b1.z, b1.w);
-        }
-        if (++grp == ng) { grp = 0; ++rt; }
-    }
-    if (cur >= 0) flush(cur);
-}
-
-// act = silu(g) u of every routed pair whose down segment has units in this CTA
-__device__ void build_act(Ctx& c, int l, const PhaseList* Lp, unsigned pcA) {
+// top-K of a head whose logits are complete (the last CTA to finish its head work)
+__device__ void head_topk(Ctx& c, int l) {
     const Prog& p = *c.p;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const float* F = acc_set(c, pcA);
-    __half* actf = reinterpret_cast<__half*>(c.sm + c.pl.actf);
-    float* actsum = reinterpret_cast<float*>(c.sm + c.pl.actsum);
-    const int ng = p.I / kGroup;
-    const int* ids = sm_ids(c, l);
-    const long long npair = (long long)p.B * p.K;
-    for (int it = wid; it < p.B * p.K * ng; it += kConsumerWarps) {
-        const int pair = it / ng, grp = it - pair * ng;
-        const int e = ids[pair];
-        bool need = false;
-        for (int s = 0; s < Lp->nseg; ++s)
-            if (Lp->seg[s].out == OUT_Y && Lp->seg[s].expert == e)
-                need = Lp->seg[s].cu0 < Lp->seg[s].cu1;
-        if (!need) continue;
-        const float* gp = F + c.acc.gu + (long long)pair * 2 * p.I;
-        const int i0 = grp * kGroup + lane, i1 = i0 + 32;
-        const float a0 = silu_f(gp[i0]) * gp[p.I + i0];
-        const float a1 = silu_f(gp[i1]) * gp[p.I + i1];
-        put_group(actf + (long long)pair * p.I + grp * kGroup, actsum + pair * ng + grp, a0, a1, lane,
-                  actf + (pair + npair) * p.I + grp * kGroup, actsum + (pair + npair) * ng + grp);
+    const LayerP& Ly = p.layers[l];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    float* scr = SM<float>(c, c.pl.rscr);
+    const float* lg = logh_buf(c, c.par, Ly.sidx);
+    for (int i = tid; i < p.B * p.E; i += kConsumerThreads) {
+        const int b = i / p.E, e = i - b * p.E;
+        const float v = __ldcg(lg + i);
+        scr[b * 3 * p.E + e] = v;
+        if (p.mode == MODE_HEAD && p.out_logits) p.out_logits[i] = v;
     }
+    cbar();
+    for (int b = wid; b < p.B; b += kConsumerWarps) {
+        __shared__ int tid_[EDGE0_MAX_BATCH][EDGE0_MAX_K];
+        __shared__ float tw_[EDGE0_MAX_BATCH][EDGE0_MAX_K];
+        warp_route(scr + b * 3 * p.E, p.E, p.K, Ly.head_route_kind, Ly.head_n_groups, Ly.head_topk_groups,
+                   Ly.head_route_scale, Ly.head_bias, scr + b * 3 * p.E + p.E, tid_[b], tw_[b], lane);
+        if (lane < p.K) {
+            if (p.mode == MODE_HEAD) {
+                p.out_ids[b * p.K + lane] = tid_[b][lane];
+                p.out_w[b * p.K + lane] = tw_[b][lane];
+            } else {
+                const long long o = (((long long)c.par * p.Ls + Ly.head_target) * p.B + b) * p.K + lane;
+                p.pred_ids[o] = tid_[b][lane];
+                p.pred_w[o] = tw_[b][lane];
+            }
+        }
+    }
+    cbar();
+}
+
+// P3: this pair's head tasks of layer l (fc1 row tiles with their fc2 columns, or
+// linear_init row tiles), then the arrival count; the last CTA does the top-K.
+// Every consumer thread runs every barrier; the result is CTA-uniform.
+__device__ bool phase3(Ctx& c, int l, const LayerTab* T, uint32_t& xph) {
+    const Prog& p = *c.p;
+    const LayerP& Ly = p.layers[l];
+    const int B = p.B, K = p.K, E = p.E, H = p.H;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
+    const PairPlan& pl = T->pl;
+    const int nH = H / kRowTile;
+    const int* ids = ids_of(c, l);
+    const int* prv = prev_of(c, l);
+    const int nprev = SM<int>(c, c.pl.nprv)[l];   // previous-token ids present (0 or K)
+    float* lg = logh_buf(c, c.par, Ly.sidx);
+    float* zpart = SM<float>(c, c.pl.zpart);
+    float* zrecv = SM<float>(c, c.pl.zrecv);
+    __half* gf = SM<__half>(c, c.pl.gf);
+    bool ok = true;
+    int i = T->p3;
+    for (int task = pl.hd0; task < pl.hd1; ++task) {
+        const bool fc1 = task < nH;
+        const int pos = fc1 ? task : task - nH;
+        int j = i;
+        while (j < T->n && T->it[j].kind == (fc1 ? IT_FC1 : IT_LINIT) && T->it[j].a == pos) ++j;
+        if (fc1) {
+            // z partial of H rows 16 pos .. + 15 over this CTA's half of d
+            for (int q = tid; q < 16 * B; q += kConsumerThreads) zpart[q] = 0.f;
+            cbar();
+            ok = warp_units(c, T, i, j, [&](const Item& it, int a, int b) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                f16_run(c, ring_at(c, it), a, b, it.b, acc);
+                if (t < B) {
+                    atomicAdd(&zpart[g * B + t], acc[0]);
+                    atomicAdd(&zpart[(g + 8) * B + t], acc[2]);
+                }
+            }) && ok;
+            // one-hot columns: fc1[:, d + e] for executed e, fc1[:, d + E + e] for previous e
+            float oh = 0.f;
+            const int rr = tid / B, bb = tid % B;
+            if (tid < 16 * B) {
+                const int hrow = pos * kRowTile + rr;
+                for (int k = 0; k < K; ++k) oh += __half2float(Ly.fc1_oh[(long long)ids[bb * K + k] * H + hrow]);
+                for (int k = 0; k < nprev; ++k)
+                    oh += __half2float(Ly.fc1_oh[(long long)(E + prv[bb * K + k]) * H + hrow]);
+            }
+            ok = !cbar_or(!ok || aborted(c));
+            float* zr = zrecv + (xph & 1) * 16 * B;
+            if (ok) ok = exchange(c, 1, zpart, zr, 16 * B, xph);
+            if (ok && tid < 16 * B) {
+                const float z = zpart[rr * B + bb] + zr[rr * B + bb] + oh;
+                const float gl = 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+                const int t1 = (rr & 7) >> 1, w = rr >> 3, sub = rr & 1;
+                const __half hi = __float2half_rn(gl);
+                const __half lo = __float2half_rn((gl - __half2float(hi)) * kLoScale);
+                gf[((bb * 2 + 0) * 4 + t1) * 4 + w * 2 + sub] = hi;
+                gf[((bb * 2 + 1) * 4 + t1) * 4 + w * 2 + sub] = lo;
+            }
+            ok = !cbar_or(!ok);
+            // fc2 columns 16 pos .. + 15 for this CTA's half of the E rows
+            if (j < T->n && T->it[j].kind == IT_FC2 && T->it[j].a == pos) {
+                const Item& it2 = T->it[j];
+                if (ok) ok = wait_item(c, T, j);
+                if (ok) {
+                    const uint2* gfr = SM<uint2>(c, c.pl.gf);
+                    const int tok = g >> 1, prt = g & 1;
+                    for (int e = wid; e < it2.n; e += kConsumerWarps) {
+                        const uint4 av = *reinterpret_cast<const uint4*>(ring_at(c, it2) + e * kF16Step + 16 * lane);
+                        uint2 bq = make_uint2(0u, 0u);
+                        if (tok < B) bq = gfr[(tok * 2 + prt) * 4 + t];
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        const uint32_t A[4] = {av.x, av.y, av.z, av.w};
+                        mma_16816(acc, A, bq.x, bq.y);
+                        const int row = (it2.b + e) * kRowTile + g;
+                        if (t < B) {
+                            red_add_f32(lg + t * E + row, acc[0] + acc[1] * kLoInv);
+                            red_add_f32(lg + t * E + row + 8, acc[2] + acc[3] * kLoInv);
+                        }
+                    }
+                }
+                release_item(c, T, j);
+                ++j;
+            }
+            ok = !cbar_or(!ok);
+        } else {
+            ok = warp_units(c, T, i, j, [&](const Item& it, int a, int b) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                f16_run(c, ring_at(c, it), a, b, it.b, acc);
+                const int row = pos * kRowTile + g;
+                if (t < B) {
+                    red_add_f32(lg + t * E + row, acc[0]);
+                    red_add_f32(lg + t * E + row + 8, acc[2]);
+                }
+            }) && ok;
+            if (c.rank == 0 && tid < 16 * B) {
+                // linear_init one-hot columns of these 16 logits
+                const int rr = tid / B, bb = tid % B, row = pos * kRowTile + rr;
+                float oh = 0.f;
+                for (int k = 0; k < K; ++k) oh += __half2float(Ly.linit_oh[(long long)ids[bb * K + k] * E + row]);
+                for (int k = 0; k < nprev; ++k)
+                    oh += __half2float(Ly.linit_oh[(long long)(E + prv[bb * K + k]) * E + row]);
+                red_add_f32(lg + bb * E + row, oh);
+            }
+            ok = !cbar_or(!ok);
+        }
+        i = j;
+        if (!ok) break;   // uniform
+    }
+    if (ok && pl.hd1 > pl.hd0) {
+        __threadfence();
+        cbar();
+        const Shape Sh = layer_shape(p, l, false);
+        if (tid == 0) {
+            const unsigned old = atom_acq_rel_add_u32(cnt_buf(c, c.par, Ly.sidx), 1u);
+            c.ctl->last = old == (unsigned)(head_ctas(Sh, c.P) - 1);
+        }
+        cbar();
+        if (c.ctl->last) head_topk(c, l);
+    }
+    return !cbar_or(!ok);
 }
 
 // ------------------------------------------------------------ the kernel ---
-__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ Prog prog) {
-    extern __shared__ __align__(128) char smem[];
-    Ctx c;
-    c.sm = smem;
-    c.pl = make_plan(prog.L, prog.B, prog.K, prog.d, prog.E, prog.I, prog.Is, prog.H, prog.r);
-    c.p = &prog;
-    c.hdr = reinterpret_cast<WsHeader*>(prog.ws);
-    c.ctl = reinterpret_cast<Ctl*>(smem + c.pl.ctl);
-    c.acc = acc_layout(prog.B, prog.K, prog.I, prog.Is, prog.r, prog.H, prog.E, prog.d);
-    c.nct = gridDim.x;
-    c.cta = blockIdx.x;
-    c.R16 = ceil_div(prog.r, 16) * 16;
-    const int tid = threadIdx.x;
+__device__ void consumer(Ctx& c) {
     const Prog& p = *c.p;
-
-    if (tid == 0) {
-        c.ctl->abort = 0;
-        c.ctl->issued = 0;
-        c.ctl->cdone = 0;
-        c.ctl->step = p.step >= 0 ? p.step : ld_volatile_s32(&c.hdr->step);
-        c.ctl->pc0 = *(volatile unsigned*)&c.hdr->pc;
-        c.ctl->trace = c.cta < kTraceCtas ? ld_volatile_s32(&c.hdr->trace) : 0;
-        c.ctl->tslot = 0;
-        uint64_t* full = reinterpret_cast<uint64_t*>(smem + c.pl.full);
-        uint64_t* empty = reinterpret_cast<uint64_t*>(smem + c.pl.empty);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
-        }
-        fence_mbar_init();
-    }
-    {
-        int* ready = reinterpret_cast<int*>(smem + c.pl.ready);
-        for (int l = tid; l < p.L; l += kThreads) ready[l] = 0;
-        for (int i = tid; i < kListSlots; i += kThreads)
-            reinterpret_cast<PhaseList*>(smem + c.pl.lists)[i].seq = 0;
-        float* sacc = reinterpret_cast<float*>(smem + c.pl.sacc);
-        for (int i = tid; i < kSaccRowsPhase * p.B; i += kThreads) sacc[i] = 0.f;
-    }
-    __syncthreads();
-    c.step = c.ctl->step;
-    // routing known at launch: predictions (prerouted layers, step > 0) or inputs
-    {
-        int* ready = reinterpret_cast<int*>(smem + c.pl.ready);
-        const int BK = p.B * p.K;
-        for (int l = 0; l < p.L; ++l) {
-            const LayerP& Ly = p.layers[l];
-            const int* src_i = nullptr;
-            const float* src_w = nullptr;
-            if (p.mode == MODE_DECODE && (Ly.flags & LF_PREROUTED) && c.step > 0) {
-                const long long o = (((long long)((c.step - 1) & 1) * p.Ls + Ly.sidx) * p.B) * p.K;
-                src_i = p.pred_ids + o;
-                src_w = p.pred_w + o;
-            } else if (p.mode == MODE_MOE) {
-                src_i = p.ids_in;
-                src_w = p.w_in;
-            } else if (p.mode == MODE_HEAD) {
-                src_i = p.exec_in;
-            }
-            if (!src_i) continue;
-            for (int i = tid; i < BK; i += kThreads) {
-                sm_ids(c, l)[i] = src_i[i];
-                sm_w(c, l)[i] = src_w ? src_w[i] : 0.f;
-            }
-            if (tid == 0) ready[l] = 1;
-        }
-    }
-    __syncthreads();
-
-    if (tid >= kConsumerThreads) {
-        if (tid == kConsumerThreads) producer(c);
-        return;
-    }
-
-    // ------------------------------------------------------ consumer side --
-    const int lane = tid & 31, wid = tid >> 5;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + c.pl.full);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + c.pl.empty);
-    float* sacc = reinterpret_cast<float*>(smem + c.pl.sacc);
-    volatile int* ready = reinterpret_cast<volatile int*>(smem + c.pl.ready);
-    const int B = p.B;
+    const int tid = threadIdx.x;
+    const int B = p.B, d = p.d;
     unsigned long long bar_target = 0;
     if (tid == 0) {
         const unsigned long long v = ld_acquire_u64(&c.hdr->barrier);
         bar_target = v - v % (unsigned long long)c.nct;
     }
-    unsigned pc = c.ctl->pc0;
-    int stage = 0;
-    uint32_t round = 0;
-    int consumed = 0;
-    int pi = 0;
-    unsigned pc_prevB = 0;        // phase of the previous layer's B (y, head logits)
-    bool prev_head = false;        // previous layer's head logits await top-K
-    int prev_layer = -1;
-    cbar();
-
-    for (int l = 0; l < p.L && !aborted(c); ++l) {
+    uint32_t xph1 = 0, xph3 = 0;
+    volatile int* ready = SM<volatile int>(c, c.pl.ready);
+    float* part = SM<float>(c, c.pl.part);
+    // every decision to leave the loop is taken from a barrier reduction, so all
+    // consumer threads leave together
+    for (int l = 0; l < p.L; ++l) {
         const LayerP& Ly = p.layers[l];
-        const bool decode = p.mode == MODE_DECODE;
-        unsigned pcR = 0;
-        const bool rphase = has_router_phase(p, l, c.step);
-        for (int ph = PH_R; ph <= PH_B; ++ph) {
-            if (ph == PH_R && !rphase) continue;
-            // ---------------- prologue
-            const int ttag = (l << 8) | (ph << 4);
-            stamp(c, ttag | 0);
-            zero_set_slice(c, pc + 1);
-            dstamp(c, l, 0x10000 | ttag | 1);
-            const bool first_of_layer = (ph == PH_R) || (ph == PH_A && !rphase);
-            if (first_of_layer) {
-                if (decode) {
-                    const __half* hs = (l <= 1) ? p.h_io : hbuf(c, (l - 1) & 1);
-                    const float* ys = l == 0 ? nullptr : acc_set(c, pc_prevB) + c.acc.y;
-                    build_x(c, hs, ys, l == 0 ? nullptr : hbuf(c, l & 1), Ly.gamma, Ly.eps, true);
-                } else {
-                    build_x(c, p.x_in, nullptr, nullptr, nullptr, 0.f, false);
-                }
-                if (prev_head && c.cta == c.nct - 1) head_topk(c, prev_layer, pc_prevB);
-                prev_head = false;
-            }
-            dstamp(c, l, 0x10000 | ttag | 2);
-            if (ph == PH_R) pcR = pc;
-            if (ph == PH_A && rphase) {
-                // own routing from the router logits of phase R
-                const float* F = acc_set(c, pcR);
-                float* scr = reinterpret_cast<float*>(smem + c.pl.rscr);
-                for (int b = wid; b < B; b += kConsumerWarps) {
-                    __shared__ int rid[EDGE0_MAX_BATCH][EDGE0_MAX_K];
-                    __shared__ float rw[EDGE0_MAX_BATCH][EDGE0_MAX_K];
-                    warp_route(F + c.acc.logr + (long long)b * p.E, p.E, p.K, Ly.route_kind, Ly.n_groups,
-                               Ly.topk_groups, Ly.route_scale, Ly.bias, scr + (long long)b * 2 * p.E,
-                               rid[b], rw[b], lane);
-                    if (lane < p.K) {
-                        sm_ids(c, l)[b * p.K + lane] = rid[b][lane];
-                        sm_w(c, l)[b * p.K + lane] = rw[b][lane];
-                    }
-                }
-                cbar();
-                if (tid == 0) {
-                    __threadfence_block();
-                    ready[l] = 1;
-                }
-            }
-            if (ph == PH_A && decode && c.cta == 0) {
-                for (int i = tid; i < B * p.K; i += kConsumerThreads)
-                    p.exec_ids[(((long long)(c.step & 1) * p.Ls + Ly.sidx) * B) * p.K + i] = sm_ids(c, l)[i];
-            }
-            // this phase's list, published by the producer
-            PhaseList* Lp = list_slot(c, pi);
-            dstamp(c, l, 0x10000 | ttag | 3);
-            if (tid == 0) wait_flag(&Lp->seq, pi + 1, c.hdr, c.ctl);
-            cbar();
-            dstamp(c, l, 0x10000 | ttag | 4);
-            if (aborted(c)) break;
-            if (Lp->seq != pi + 1) break;
-            float* F = acc_set(c, pc);
-            const float* FA = acc_set(c, pc - 1);     // phase A results (valid in phase B)
-            if (ph == PH_B) {
-                build_act(c, l, Lp, pc - 1);
-                if (Lp->has_sh) {
-                    float* gsh = reinterpret_cast<float*>(smem + c.pl.gsh);
-                    float* ush = reinterpret_cast<float*>(smem + c.pl.ush);
-                    float* aacc = reinterpret_cast<float*>(smem + c.pl.aacc);
-                    for (int i = tid; i < B * p.Is; i += kConsumerThreads) {
-                        const int b = i / p.Is, j = i - b * p.Is;
-                        gsh[i] = FA[c.acc.gus + ((long long)b * 2) * p.Is + j];
-                        ush[i] = FA[c.acc.gus + ((long long)b * 2 + 1) * p.Is + j];
-                    }
-                    for (int i = tid; i < B * 2 * c.R16; i += kConsumerThreads) aacc[i] = FA[c.acc.aacc + i];
-                    const bool lora = decode && (Ly.flags & LF_LORA);
-                    if (!lora) {
-                        cbar();
-                        __half* ashf = reinterpret_cast<__half*>(smem + c.pl.ashf);
-                        float* ashsum = reinterpret_cast<float*>(smem + c.pl.ashsum);
-                        const int ng = p.Is / kGroup;
-                        for (int it = wid; it < B * ng; it += kConsumerWarps) {
-                            const int b = it / ng, grp = it - b * ng;
-                            const int i0 = b * p.Is + grp * kGroup + lane, i1 = i0 + 32;
-                            put_group(ashf + (long long)b * p.Is + grp * kGroup, ashsum + b * ng + grp,
-                                      silu_f(gsh[i0]) * ush[i0], silu_f(gsh[i1]) * ush[i1], lane,
-                                      ashf + (long long)(b + B) * p.Is + grp * kGroup,
-                                      ashsum + (b + B) * ng + grp);
-                        }
-                    }
-                }
-                if (Lp->has_head) {
-                    float* zsm = reinterpret_cast<float*>(smem + c.pl.zsm);
-                    float* linsm = reinterpret_cast<float*>(smem + c.pl.linsm);
-                    for (int i = tid; i < B * p.H; i += kConsumerThreads) zsm[i] = FA[c.acc.z + i];
-                    for (int i = tid; i < B * p.E; i += kConsumerThreads) linsm[i] = FA[c.acc.lin + i];
-                }
-                cbar();
-            }
-            // ---------------- chunk loop
-            stamp(c, ttag | 1);
-            const __half* held_bg = nullptr;
-            int held_bg_stage = -1;
-            for (int i = 0; i < Lp->nch; ++i) {
-                const Chunk x = Lp->ch[i];
-                const int st = stage;
-                if (!mbar_wait(&full[st], round & 1, c.hdr, c.ctl)) { c.ctl->abort = 1; break; }
-                dstamp(c, l, 0x20000 | (i << 8) | (ph << 4) | x.aux);
-                const char* buf = smem + c.pl.stage + st * kStageBytes;
-                const Seg& s = Lp->seg[x.seg];
-                bool release = true;
-                if (x.aux == AUX_UNITS) {
-                    // each warp takes a contiguous share of the chunk's units; no CTA sync
-                    const int n = x.u1 - x.u0;
-                    const int ua = x.u0 + (n * wid) / kConsumerWarps;
-                    const int ub2 = x.u0 + (n * (wid + 1)) / kConsumerWarps;
-                    if (ua < ub2)
-                        warp_units(c, s, l, buf, x.u0, ua, ub2, sacc + x.sacc * B, x.u0 / s.n_g);
-                    __syncwarp();
-                } else if (x.aux == AUX_BG) {
-                    held_bg = reinterpret_cast<const __half*>(buf);
-                    held_bg_stage = st;
-                    release = false;
-                } else if (x.aux == AUX_BU) {
-                    // act_s = silu(g + (a/r) Bg ag) * (u + (a/r) Bu au), fp32 copy + fragments
-                    cbar();
-                    const __half* Bu = reinterpret_cast<const __half*>(buf);
-                    const float* gsh = reinterpret_cast<const float*>(smem + c.pl.gsh);
-                    const float* ush = reinterpret_cast<const float*>(smem + c.pl.ush);
-                    const float* aacc = reinterpret_cast<const float*>(smem + c.pl.aacc);
-                    float* ash32 = reinterpret_cast<float*>(smem + c.pl.ash32);
-                    for (int j = tid; j < B * p.Is; j += kConsumerThreads) {
-                        const int b = j / p.Is, row = j - b * p.Is;
-                        const float* ag = aacc + (b * 2) * c.R16;
-                        const float* au = aacc + (b * 2 + 1) * c.R16;
-                        float dg = 0.f, du = 0.f;
-                        for (int q = 0; q < p.r; ++q) {
-                            dg += __half2float(held_bg[row * p.r + q]) * ag[q];
-                            du += __half2float(Bu[row * p.r + q]) * au[q];
-                        }
-                        const float gg = gsh[j] + Ly.lora_scale * dg;
-                        const float uu = ush[j] + Ly.lora_scale * du;
-                        ash32[j] = silu_f(gg) * uu;
-                    }
-                    cbar();
-                    __half* ashf = reinterpret_cast<__half*>(smem + c.pl.ashf);
-                    float* ashsum = reinterpret_cast<float*>(smem + c.pl.ashsum);
-                    const int ng = p.Is / kGroup;
-                    for (int it = wid; it < B * ng; it += kConsumerWarps) {
-                        const int b = it / ng, grp = it - b * ng;
-                        const int i0 = b * p.Is + grp * kGroup + lane;
-                        put_group(ashf + (long long)b * p.Is + grp * kGroup, ashsum + b * ng + grp,
-                                  ash32[i0], ash32[i0 + 32], lane,
-                                  ashf + (long long)(b + B) * p.Is + grp * kGroup,
-                                  ashsum + (b + B) * ng + grp);
-                    }
-                    cbar();
-                    if (lane == 0) mbar_arrive(&empty[held_bg_stage]);
-                    held_bg = nullptr;
-                } else if (x.aux == AUX_AD) {
-                    // v = A_d act_s (r rows), warp 0 on the tensor cores
-                    float* v = reinterpret_cast<float*>(smem + c.pl.v);
-                    float* tmp = reinterpret_cast<float*>(smem + c.pl.rscr);   // 16 x B scratch
-                    if (wid == 0) {
-                        Seg sa;
-                        sa.base = nullptr; sa.off = 0; sa.kind = 1;
-                        sa.n_rt = ceil_div(p.r, kRowTile); sa.n_g = p.Is / kGroup; sa.rows = p.r;
-                        sa.ub = kF16Unit; sa.src = SRC_ACTSH; sa.out = 0; sa.expert = -1; sa.extra = 0;
-                        sa.cu0 = 0; sa.cu1 = 0;
-                        for (int q = lane; q < kRowTile * sa.n_rt * B; q += 32) tmp[q] = 0.f;
-                        __syncwarp();
-                        warp_units(c, sa, l, buf, 0, 0, sa.n_rt * sa.n_g, tmp, 0);
-                        __syncwarp();
-                        for (int q = lane; q < c.R16 * B; q += 32) {
-                            const int row = q / B, b = q - row * B;
-                            v[b * c.R16 + row] = row < p.r ? tmp[q] : 0.f;
-                        }
-                    }
-                    cbar();
-                } else if (x.aux == AUX_BD) {
-                    // this CTA's B_d rows, kept for the phase-end flush
-                    const uint4* src = reinterpret_cast<const uint4*>(buf);
-                    uint4* dst = reinterpret_cast<uint4*>(smem + c.pl.bd);
-                    for (int q = tid; q < x.bytes / 16; q += kConsumerThreads) dst[q] = src[q];
-                    cbar();
-                } else if (x.aux == AUX_FC1OH) {
-                    // gelu(z + one-hot columns) fragments for token x.tok
-                    const __half* rows = reinterpret_cast<const __half*>(buf);
-                    const int nrows = x.bytes / (p.H * 2);
-                    const float* zsm = reinterpret_cast<const float*>(smem + c.pl.zsm) + x.tok * p.H;
-                    __half* gf = reinterpret_cast<__half*>(smem + c.pl.gf) + (long long)x.tok * p.H;
-                    float* gsum = reinterpret_cast<float*>(smem + c.pl.gsum) + x.tok * (p.H / kGroup);
-                    __half* gfl = gf + (long long)B * p.H;
-                    float* gsuml = gsum + B * (p.H / kGroup);
-                    for (int grp = wid; grp < p.H / kGroup; grp += kConsumerWarps) {
-                        const int i0 = grp * kGroup + lane, i1 = i0 + 32;
-                        float z0 = zsm[i0], z1 = zsm[i1];
-                        for (int q = 0; q < nrows; ++q) {
-                            z0 += __half2float(rows[q * p.H + i0]);
-                            z1 += __half2float(rows[q * p.H + i1]);
-                        }
-                        const float g0 = 0.5f * z0 * (1.0f + erff(z0 * 0.70710678118654752f));
-                        const float g1 = 0.5f * z1 * (1.0f + erff(z1 * 0.70710678118654752f));
-                        put_group(gf + grp * kGroup, gsum + grp, g0, g1, lane, gfl + grp * kGroup,
-                                  gsuml + grp);
-                    }
-                    cbar();
-                } else if (x.aux == AUX_LINOH) {
-                    const __half* rows = reinterpret_cast<const __half*>(buf);
-                    const int nrows = x.bytes / (p.E * 2);
-                    const float* linsm = reinterpret_cast<const float*>(smem + c.pl.linsm) + x.tok * p.E;
-                    float* lx = reinterpret_cast<float*>(smem + c.pl.lx) + x.tok * p.E;
-                    for (int e = tid; e < p.E; e += kConsumerThreads) {
-                        float v = linsm[e];
-                        for (int q = 0; q < nrows; ++q) v += __half2float(rows[q * p.E + e]);
-                        lx[e] = v;
-                    }
-                    cbar();
-                }
-                if (release && lane == 0) mbar_arrive(&empty[st]);
-                dstamp(c, l, 0x30000 | (i << 8) | (ph << 4) | x.aux);
-                if (++stage == kStages) { stage = 0; ++round; }
-                ++consumed;
-            }
-            cbar();
-            if (aborted(c)) break;
-            // ---------------- flush this phase's accumulator rows to global memory
-            stamp(c, ttag | 2);
-            float wcol[EDGE0_MAX_BATCH];
-            int kcol[EDGE0_MAX_BATCH];
-            for (int i = 0; i < Lp->nch; ++i) {
-                const Chunk& x = Lp->ch[i];
-                if (x.aux != AUX_UNITS) continue;
-                const Seg& s = Lp->seg[x.seg];
-                const int rt0 = x.u0 / s.n_g, rt1 = (x.u1 - 1) / s.n_g;
-                const int nrows = (rt1 - rt0 + 1) * kRowTile;
-                for (int b = 0; b < B; ++b) {
-                    kcol[b] = col_kslot(c, s, l, b);
-                    wcol[b] = (s.out == OUT_Y && s.expert >= 0 && kcol[b] >= 0) ? sm_w(c, l)[b * p.K + kcol[b]] : 1.f;
-                }
-                float* sa = sacc + x.sacc * B;
-                for (int q = tid; q < nrows * B; q += kConsumerThreads) {
-                    const int rl = q / B, b = q - rl * B;
-                    const int rt = rt0 + (rl >> 4);
-                    const int row = rt * kRowTile + (rl & 15);
-                    float val = sa[q];
-                    sa[q] = 0.f;
-                    if (row >= s.rows || kcol[b] < 0) continue;
-                    const bool own0 = (rt * s.n_g >= x.u0) && (rt * s.n_g < x.u1);
-                    if (own0 && s.extra == EX_LORA_DOWN) {
-                        const __half* bd = reinterpret_cast<const __half*>(smem + c.pl.bd) +
-                                           (long long)(row - Lp->bd_row0) * p.r;
-                        const float* v = reinterpret_cast<const float*>(smem + c.pl.v) + b * c.R16;
-                        float dsum = 0.f;
-                        for (int j = 0; j < p.r; ++j) dsum += __half2float(bd[j]) * v[j];
-                        val += Ly.lora_scale * dsum;
-                    }
-                    if (own0 && s.extra == EX_HEAD)
-                        val += reinterpret_cast<const float*>(smem + c.pl.lx)[b * p.E + row];
-                    red_add_f32(out_ptr(c, s, F, row, b, kcol[b]), val * wcol[b]);
-                }
-            }
-            dstamp(c, l, 0x10000 | ttag | 5);
-            cbar();
-            if (tid == 0) *(volatile int*)&c.ctl->cdone = pi + 1;
-            // ---------------- end of phase
-            stamp(c, ttag | 3);
-            if (!grid_barrier(c, bar_target)) break;
-            stamp(c, ttag | 4);
-            if (ph == PH_B) {
-                pc_prevB = pc;
-                prev_head = (p.mode != MODE_MOE) && (p.mode == MODE_HEAD || (Ly.flags & LF_HEAD));
-                prev_layer = l;
-            }
-            ++pc;
-            ++pi;
+        LayerTab* T = tab_of(c, l);
+        stamp(c, (l << 8) | 0);
+        if (tid == 0) wait_flag(c, &T->seq, l + 1);
+        if (cbar_or(aborted(c))) break;
+        const bool router = has_router_phase(p, l, c.step);
+        const Shape Sh = layer_shape(p, l, router);
+        for (int q = tid; q < (T->pl.n_hr * 16 + 32) * B; q += kConsumerThreads) part[q] = 0.f;
+        // ---------------- input x
+        if (p.mode == MODE_DECODE && l > 0)
+            if (!bar_wait(c, bar_target)) break;
+        if (p.mode == MODE_DECODE || l == 0) build_x(c, l);
+        stamp(c, (l << 8) | 1);
+        // ---------------- own routing
+        if (router) {
+            const bool ok = phase_router(c, l, T);
+            if (cbar_or(!ok || aborted(c))) break;
+            bar_arrive(c);
+            if (!bar_wait(c, bar_target)) break;
+            route_layer(c, l);
         }
+        if (p.mode == MODE_DECODE && c.cta == 0) {
+            for (int i = tid; i < B * p.K; i += kConsumerThreads)
+                p.exec_ids[(((long long)c.par * p.Ls + Ly.sidx) * B) * p.K + i] = ids_of(c, l)[i];
+        }
+        if (ready[l] != 1) {
+            if (tid == 0) raise_error(c, EDGE0_EINVAL);
+            cbar();
+            break;
+        }
+        stamp(c, (l << 8) | 2);
+        // ---------------- P1: gate/up partials, swap with the peer, act
+        bool ok = phase1(c, l, T);
+        if (cbar_or(!ok || aborted(c))) break;
+        stamp(c, (l << 8) | 3);
+        if (T->pl.n_hr > 0) {
+            const int nmsg = (T->pl.n_hr * 16 + (Sh.lora && T->pl.has_sh ? 32 : 0)) * B;
+            ok = exchange(c, 0, part, SM<float>(c, c.pl.recv), nmsg, xph1);
+            if (cbar_or(!ok)) break;
+        }
+        stamp(c, (l << 8) | 4);
+        if (!compute_act(c, l, T, Sh.lora != 0)) break;
+        stamp(c, (l << 8) | 5);
+        // ---------------- P2: down -> y, then this layer's barrier
+        ok = phase2(c, l, T, Sh.lora != 0);
+        if (cbar_or(!ok || aborted(c))) break;
+        bar_arrive(c);
+        stamp(c, (l << 8) | 6);
+        // ---------------- P3: head, while the barrier completes
+        if (Sh.head)
+            if (!phase3(c, l, T, xph3)) break;
+        stamp(c, (l << 8) | 7);
+        if (cbar_or(aborted(c))) break;
+        if (tid == 0) *(volatile int*)&c.ctl->cdone = l + 1;
     }
-
-    if (!aborted(c)) {
-        // ---------------- tail
-        const float* Y = acc_set(c, pc_prevB) + c.acc.y;
-        if (p.mode == MODE_DECODE) {
-            const __half* hs = (p.L <= 1) ? p.h_io : hbuf(c, (p.L - 1) & 1);
-            const long long n = (long long)B * p.d;
-            const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
-            // h_L = fp16(h_{L-1} + y); h_{L-1} of a single-layer call is h_io itself
-            for (long long i = a + tid; i < b; i += kConsumerThreads)
-                p.h_io[i] = __float2half_rn(__half2float(hs[i]) + Y[i]);
-        } else if (p.mode == MODE_MOE) {
-            const long long n = (long long)B * p.d;
-            const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
-            for (long long i = a + tid; i < b; i += kConsumerThreads) p.y_out[i] = __float2half_rn(Y[i]);
-        }
-        if (p.mode == MODE_HEAD && p.out_logits) {
-            const float* Lg = acc_set(c, pc_prevB) + c.acc.logh;
-            const long long n = (long long)B * p.E;
-            const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
-            for (long long i = a + tid; i < b; i += kConsumerThreads) p.out_logits[i] = Lg[i];
-        }
-        if (prev_head && c.cta == c.nct - 1) head_topk(c, prev_layer, pc_prevB);
-        if (c.cta == 0 && tid == 0) {
-            c.hdr->pc = pc;
-            if (p.step < 0) c.hdr->step = c.step + 1;
-        }
-    } else if (tid == 0) {
-        // drain copies still in flight before the CTA exits (bounded)
-        const int issued = *(volatile int*)&c.ctl->issued;
-        const unsigned long long t0 = now_ns();
-        for (int k = consumed; k < issued; ++k) {
-            while (!mbar_try_wait(&full[stage], round & 1))
-                if (now_ns() - t0 > 100000000ull) break;
-            if (++stage == kStages) { stage = 0; ++round; }
-        }
+    if (cbar_or(aborted(c))) return;
+    // ---------------- tail: the last layer's y is complete after its barrier
+    if (!bar_wait(c, bar_target)) return;
+    const float* Y = y_buf(c, c.par, p.layers[p.L - 1].sidx);
+    const long long n = (long long)B * d;
+    const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
+    if (p.mode == MODE_DECODE) {
+        const __half* hs = SM<__half>(c, c.pl.hs);
+        for (long long i = a + tid; i < b; i += kConsumerThreads)
+            p.h_io[i] = __float2half_rn(__half2float(hs[i]) + __ldcg(Y + i));
+    } else if (p.mode == MODE_MOE) {
+        for (long long i = a + tid; i < b; i += kConsumerThreads) p.y_out[i] = __float2half_rn(__ldcg(Y + i));
     }
+    if (c.cta == 0 && tid == 0 && p.step < 0) c.hdr->step = c.step + 1;
 }
 
-int engine_smem_bytes(const Prog& p) {
-    return make_plan(p.L, p.B, p.K, p.d, p.E, p.I, p.Is, p.H, p.r).total;
+__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ Prog prog) {
+    extern __shared__ __align__(128) char smem[];
+    Ctx c;
+    c.p = &prog;
+    c.sm = smem;
+    c.pl = make_plan(prog);
+    c.hdr = reinterpret_cast<WsHeader*>(prog.ws);
+    c.ctl = reinterpret_cast<Ctl*>(smem + c.pl.ctl);
+    c.ws = ws_layout(prog.Ls, prog.B, prog.d, prog.E);
+    c.nct = gridDim.x;
+    c.cta = blockIdx.x;
+    c.rank = (int)cluster_ctarank();
+    c.pair = c.cta / kClusterCtas;
+    c.P = c.nct / kClusterCtas;
+    c.hv = halves(prog.d, prog.E, c.rank);
+    const int tid = threadIdx.x;
+    const Prog& p = prog;
+
+    if (tid == 0) {
+        Ctl* ctl = c.ctl;
+        ctl->abort = 0;
+        ctl->cdone = 0;
+        ctl->issued = 0;
+        ctl->last = 0;
+        ctl->step = p.step >= 0 ? p.step : ld_volatile_s32(&c.hdr->step);
+        ctl->trace = c.cta < kTraceCtas ? ld_volatile_s32(&c.hdr->trace) : 0;
+        ctl->tslot = 0;
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(SM<uint64_t>(c, c.pl.full) + s, 1);
+            mbar_init(SM<uint64_t>(c, c.pl.empty) + s, kConsumerWarps);
+        }
+        mbar_init(SM<uint64_t>(c, c.pl.xch) + 0, 1);
+        mbar_init(SM<uint64_t>(c, c.pl.xch) + 1, 1);
+        fence_mbar_init();
+    }
+    for (int i = tid; i < kTables; i += kThreads) tab_of(c, i)->seq = 0;
+    __syncthreads();
+    c.step = c.ctl->step;
+    c.par = c.step & 1;
+    // clear the other step parity of this launch's layers for the next step
+    {
+        const int op = c.par ^ 1;
+        const long long per_y = (long long)p.B * p.d, per_l = (long long)p.B * p.E;
+        const long long tot = (long long)p.L * (per_y + 2 * per_l);
+        const long long a = tot * c.cta / c.nct, b = tot * (c.cta + 1) / c.nct;
+        for (long long i = a + tid; i < b; i += kThreads) {
+            const long long l = i / (per_y + 2 * per_l), o = i % (per_y + 2 * per_l);
+            const int sidx = p.layers[l].sidx;
+            if (o < per_y) y_buf(c, op, sidx)[o] = 0.f;
+            else if (o < per_y + per_l) logr_buf(c, op, sidx)[o - per_y] = 0.f;
+            else logh_buf(c, op, sidx)[o - per_y - per_l] = 0.f;
+        }
+        if (c.cta == 0)
+            for (int l = tid; l < p.L; l += kThreads) *cnt_buf(c, op, p.layers[l].sidx) = 0u;
+    }
+    // routing known at launch: predictions (prerouted layers, step > 0) or inputs;
+    // previous-token ids of head layers
+    for (int l = tid; l < p.L; l += kThreads) {
+        const LayerP& Ly = p.layers[l];
+        const int BK = p.B * p.K;
+        const int32_t* src_i = nullptr;
+        const float* src_w = nullptr;
+        if (p.mode == MODE_DECODE && (Ly.flags & LF_PREROUTED) && c.step > 0) {
+            const long long o = (((long long)((c.step - 1) & 1) * p.Ls + Ly.sidx) * p.B) * p.K;
+            src_i = p.pred_ids + o;
+            src_w = p.pred_w + o;
+        } else if (p.mode == MODE_MOE) {
+            src_i = p.ids_in;
+            src_w = p.w_in;
+        } else if (p.mode == MODE_HEAD) {
+            src_i = p.exec_in;
+        }
+        int flag = 0;
+        if (src_i) {
+            for (int i = 0; i < BK; ++i) {
+                ids_of(c, l)[i] = src_i[i];
+                w_of(c, l)[i] = src_w ? src_w[i] : 0.f;
+            }
+            if (!make_dist(c, l)) raise_error(c, EDGE0_EINVAL);
+            flag = 1;
+        }
+        const int32_t* pv = nullptr;
+        if (p.mode == MODE_HEAD) pv = p.prev_in;
+        else if (p.mode == MODE_DECODE && (Ly.flags & LF_HEAD) && c.step > 0)
+            pv = p.exec_ids + (((long long)((c.step - 1) & 1) * p.Ls + Ly.sidx) * p.B) * p.K;
+        if (pv) {
+            for (int i = 0; i < BK; ++i) {
+                const int e = pv[i];
+                if (e < 0 || e >= p.E) raise_error(c, EDGE0_EINVAL);
+                prev_of(c, l)[i] = e < 0 || e >= p.E ? 0 : e;
+            }
+        }
+        SM<int>(c, c.pl.nprv)[l] = pv ? p.K : 0;
+        SM<volatile int>(c, c.pl.ready)[l] = flag;
+    }
+    __syncthreads();
+    // the peer's barriers exist before any exchange
+    cluster_sync_all();
+
+    if (tid >= kConsumerThreads) {
+        if (tid == kConsumerThreads && !aborted(c)) producer(c);
+        __syncwarp();
+    } else {
+        consumer(c);
+    }
+    __syncthreads();
+    if (tid == 0 && aborted(c)) {
+        // let copies still in flight into this CTA's ring land before it exits (bounded)
+        const int issued = *(volatile int*)&c.ctl->issued;
+        const unsigned long long t0 = now_ns();
+        for (int k = issued > kSlots ? issued - kSlots : 0; k < issued; ++k)
+            while (!mbar_try_wait(full_bar(c, k), item_parity(k)))
+                if (now_ns() - t0 > 100000000ull) break;
+        while (now_ns() - t0 < 20000ull) {}   // stores from the peer still in flight
+    }
+    __syncthreads();
+    // neither CTA of a pair leaves while the other may still write into it
+    cluster_sync_all();
+}
+
+// ------------------------------------------------------------------ host ---
+namespace {
+std::mutex g_grid_mutex;
+int g_grid[64] = {};
+int g_smem_max[64] = {};
+}  // namespace
+
+int engine_grid(int* nct) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return EDGE0_ECUDA;
+    std::lock_guard<std::mutex> lock(g_grid_mutex);
+    if (!g_grid[dev]) {
+        int maxsm = 0;
+        if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return EDGE0_ECUDA;
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, engine_kernel) != cudaSuccess) return EDGE0_ECUDA;
+        const int dyn = maxsm - (int)fa.sharedSizeBytes;
+        if (cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
+            return EDGE0_ECUDA;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(kClusterCtas);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = dyn;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = kClusterCtas;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int ncl = 0;
+        if (cudaOccupancyMaxActiveClusters(&ncl, (void*)engine_kernel, &cfg) != cudaSuccess || ncl < 2)
+            return EDGE0_ECUDA;
+        g_grid[dev] = ncl * kClusterCtas;
+        g_smem_max[dev] = dyn;
+    }
+    *nct = g_grid[dev];
+    return EDGE0_OK;
+}
+
+// Derived launch fields for one set of shapes and grid: the pair-plan maxima over
+// every kind of layer (shared expert, LoRA, head, own router: all 16
+// combinations) and the ring that fits next to the fixed buffers.
+struct Derived {
+    int mode, B, K, d, E, I, Is, H, r, nct, smem_max;
+    int rc, slots_max, hr_max, q_max, ring_bytes, smem;
+};
+
+static int derive(Derived& D) {
+    Prog p;
+    memset(&p, 0, sizeof(p));
+    p.mode = D.mode; p.L = 1; p.B = D.B; p.K = D.K; p.d = D.d; p.E = D.E; p.I = D.I; p.Is = D.Is;
+    p.H = D.H; p.r = D.r;
+    if (D.nct < 2 * kClusterCtas || D.nct % kClusterCtas) return EDGE0_EUNSUPPORTED;
+    if (p.B <= 0 || p.B > EDGE0_MAX_BATCH) return EDGE0_EINVAL;
+    if (p.d % 128 || p.d > kMaxD || p.E % kRowTile || p.H % 64 || p.I % 64 || p.Is % 64)
+        return EDGE0_EUNSUPPORTED;
+    if ((long long)p.B * p.d / 4 > (long long)kMaxChunks * kConsumerThreads) return EDGE0_EUNSUPPORTED;
+    if (p.r <= 0 || p.r > 16) return EDGE0_EUNSUPPORTED;
+    p.slots_max = p.mode == MODE_HEAD ? 0 : (p.B * p.K < p.E ? p.B * p.K : p.E);
+    const int P = D.nct / kClusterCtas;
+    p.hr_max = 1;
+    p.q_max = 1;
+    LayerTab T;   // scratch on the stack: the allocation-free entry point comes here too
+    // one layer per combination of parts, in both passes (maxima, then ring capacity)
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int combo = 0; combo < 16; ++combo) {
+            p.layers[0].flags = ((combo & 1) ? LF_SHARED : 0) | ((combo & 2) ? LF_LORA : 0) |
+                                ((combo & 4) ? LF_HEAD : 0);
+            const bool router = (combo & 8) && p.mode == MODE_DECODE;
+            const Shape S = layer_shape(p, 0, router);
+            for (int pair = 0; pair < P; ++pair)
+                for (int rank = 0; rank < kClusterCtas; ++rank) {
+                    int lin = 0;
+                    if (!build_items(S, P, pair, rank, 1 << 30, &T, lin)) return EDGE0_EUNSUPPORTED;
+                    if (pass == 0) {
+                        if (T.pl.n_hr > p.hr_max) p.hr_max = T.pl.n_hr;
+                        if (T.pl.n_q > p.q_max) p.q_max = T.pl.n_q;
+                    } else {
+                        // the consumers hold all down items of a layer (and the LoRA B
+                        // rows) at once: they must fit in the ring next to one item of
+                        // slack for the wrap-around
+                        long long held = 0;
+                        for (int i = T.p1; i < T.p3; ++i)
+                            if (!unit_kind(T.it[i].kind)) held += T.it[i].bytes;
+                        if (held + kItemMax > p.ring_bytes) return EDGE0_EUNSUPPORTED;
+                    }
+                }
+        }
+        if (pass == 0) {
+            p.L = EDGE0_MAX_LAYERS;   // the fixed buffers of the largest call
+            p.ring_bytes = 0;
+            const int fixed = make_plan(p).total;
+            p.ring_bytes = ((D.smem_max - fixed) / 16) * 16;
+            if (p.ring_bytes < kMinRing) return EDGE0_EUNSUPPORTED;
+        }
+    }
+    D.slots_max = p.slots_max;
+    D.hr_max = p.hr_max;
+    D.q_max = p.q_max;
+    D.ring_bytes = p.ring_bytes;
+    D.smem = make_plan(p).total;
+    return EDGE0_OK;
+}
+
+namespace {
+constexpr int kDerivedCache = 16;
+Derived g_derived[kDerivedCache];
+int g_derived_n = 0, g_derived_next = 0;
+}  // namespace
+
+// Fills the derived fields of p for a grid of nct CTAs and checks the shapes
+// against the engine's limits (cached per shape set; allocates nothing).
+int engine_check(Prog& p, int nct, int smem_max, int* smem_bytes) {
+    if (p.L <= 0 || p.L > EDGE0_MAX_LAYERS) return EDGE0_EINVAL;
+    Derived key;
+    memset(&key, 0, sizeof(key));
+    key.mode = p.mode; key.B = p.B; key.K = p.K; key.d = p.d; key.E = p.E; key.I = p.I;
+    key.Is = p.Is; key.H = p.H; key.r = p.r; key.nct = nct; key.smem_max = smem_max;
+    std::lock_guard<std::mutex> lock(g_grid_mutex);
+    int hit = -1;
+    for (int i = 0; i < g_derived_n; ++i) {
+        const Derived& d = g_derived[i];
+        if (d.mode == key.mode && d.B == key.B && d.K == key.K && d.d == key.d && d.E == key.E &&
+            d.I == key.I && d.Is == key.Is && d.H == key.H && d.r == key.r && d.nct == key.nct &&
+            d.smem_max == key.smem_max) { hit = i; break; }
+    }
+    if (hit < 0) {
+        key.rc = derive(key);
+        hit = g_derived_next;
+        g_derived[hit] = key;
+        g_derived_next = (g_derived_next + 1) % kDerivedCache;
+        if (g_derived_n < kDerivedCache) ++g_derived_n;
+    }
+    const Derived& d = g_derived[hit];
+    if (d.rc) return d.rc;
+    p.slots_max = d.slots_max;
+    p.hr_max = d.hr_max;
+    p.q_max = d.q_max;
+    p.ring_bytes = d.ring_bytes;
+    // the fixed buffers of this call's L are no larger than those the ring was sized with
+    *smem_bytes = make_plan(p).total;
+    return EDGE0_OK;
+}
+
+int engine_launch(Prog& p, cudaStream_t stream) {
+    int nct = 0;
+    int rc = engine_grid(&nct);
+    if (rc) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int smem = 0;
+    rc = engine_check(p, nct, g_smem_max[dev], &smem);
+    if (rc) return rc;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(nct);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kClusterCtas;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeCooperative;
+    at[1].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, engine_kernel, p) != cudaSuccess) return EDGE0_ECUDA;
+    return EDGE0_OK;
 }
 
 }  // namespace edge0

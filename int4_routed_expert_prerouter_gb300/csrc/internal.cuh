@@ -12,25 +12,27 @@ namespace edge0 {
 constexpr int kGroup = 64;           // inputs per affine group (int4 group-64)
 constexpr int kRowTile = 16;         // rows per tensor-core row tile
 constexpr int kQ4Unit = 576;         // int4 unit: 512 B nibbles + 64 B scale/bias pairs
+constexpr int kQ4Quarter = 128;      // int4 block of one 16-input step of one row tile
+constexpr int kQ4Scales = 64;        // scale/bias pairs of one row tile and group
 constexpr int kF16Unit = 2048;       // fp16 unit: 16 rows x 64 inputs
-constexpr int kFragPerGroup = 64;    // halves of one token's B fragments per group
+constexpr int kF16Step = 512;        // fp16 block of one 16-input step of one row tile
+constexpr int kHalfRow = 8;          // act rows per interleaved gate/up tile
 
 inline __host__ __device__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+// packed bytes of an int4 matrix [out, in] (row tiles x groups x 576)
 inline __host__ __device__ long long q4_bytes(int out, int in) {
     return (long long)ceil_div(out, kRowTile) * (in / kGroup) * kQ4Unit;
 }
+// packed bytes of an fp16 matrix [out, in] (row tiles x 16-input steps x 512)
 inline __host__ __device__ long long f16_bytes(int out, int in) {
-    return (long long)ceil_div(out, kRowTile) * (in / kGroup) * kF16Unit;
+    return (long long)ceil_div(out, kRowTile) * (in / 16) * kF16Step;
 }
 
 // --------------------------------------------------------------- engine ----
 constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kStageBytes = 16384;
-constexpr int kStages = 8;
-constexpr int kMaxSeg = 40;
-constexpr int kSaccRows = 32 * kRowTile;               // rows one chunk can touch
+constexpr int kClusterCtas = 2;                        // CTA pairs share gate/up partial sums
 
 enum Mode : int { MODE_DECODE = 0, MODE_MOE = 1, MODE_HEAD = 2 };
 
@@ -42,37 +44,35 @@ enum LayerFlags : int {
 };
 
 struct LayerP {
-    const char* gate;       // packed int4 stacks (expert stride q4_bytes)
-    const char* up;
-    const char* down;
-    const char* sh_gate;
-    const char* sh_up;
+    const char* gu;          // packed interleaved gate/up, experts stacked (stride q4_bytes(2I, d))
+    const char* down;        // packed K-major down, experts stacked (stride q4_bytes(d, I))
+    const char* sh_gu;       // shared expert, same layouts
     const char* sh_down;
-    const int* slot_table;
+    const int* slot_table;   // expert id -> slot of the stacks (or null: slot = id)
     int n_slots;
-    const char* router;     // packed fp16 [E x d]
-    const char* lora_Ag;    // packed fp16 [r x d]
+    const char* router;      // packed fp16 [E x d]
+    const char* lora_Ag;     // packed fp16 [r x d] (one row tile)
     const char* lora_Au;
-    const char* lora_Ad;    // packed fp16 [r x Is]
-    const __half* lora_Bg;  // [Is, r]
+    const __half* lora_AdT;  // [Is, r]: A_down transposed
+    const __half* lora_Bg;   // [Is, r]
     const __half* lora_Bu;
-    const __half* lora_Bd;  // [d, r]
-    const char* fc1;        // packed fp16 [H x d]
-    const __half* fc1_oh;   // [2E, H]
-    const char* fc2;        // packed fp16 [E x H]
-    const char* linit;      // packed fp16 [E x d]
-    const __half* linit_oh; // [2E, E]
+    const __half* lora_Bd;   // [d, r]
+    const char* fc1;         // packed fp16 [H x d]
+    const __half* fc1_oh;    // [2E, H]
+    const char* fc2;         // packed fp16 K-major [E x H]
+    const char* linit;       // packed fp16 [E x d]
+    const __half* linit_oh;  // [2E, E]
     const __half* gamma;
-    const float* bias;      // this layer's routing bias (or null)
-    const float* head_bias; // head target's routing bias (or null)
+    const float* bias;       // this layer's routing bias (or null)
+    const float* head_bias;  // head target's routing bias (or null)
     float eps;
-    float lora_scale;       // alpha / r
+    float lora_scale;        // alpha / r
     float route_scale, head_route_scale;
     int route_kind, n_groups, topk_groups;
     int head_route_kind, head_n_groups, head_topk_groups;
     int flags;
-    int head_target;        // state row
-    int sidx;               // state row of this layer
+    int head_target;         // state row
+    int sidx;                // state row of this layer
 };
 
 struct Prog {
@@ -97,47 +97,45 @@ struct Prog {
     float* out_logits;
     // workspace
     char* ws;
-    long long ws_set_floats;  // floats per accumulator set
+    // derived by engine_check for the launch's grid
+    int slots_max;            // routed expert slots of a layer: min(B K, E)
+    int hr_max, q_max;        // most half-row tiles / act quarters one CTA pair owns
+    int ring_bytes;           // shared-memory ring of streamed weights
     LayerP layers[EDGE0_MAX_LAYERS];
 };
 
 // Workspace header (first 256 bytes)
 struct WsHeader {
     unsigned long long barrier;   // monotonically increasing arrival counter
-    unsigned int pc;              // phase counter (accumulator ring position)
+    unsigned int spare;
     int step;                     // auto step counter
     int error;                    // EDGE0_* status recorded by a kernel
     int abort;                    // set with error: every wait gives up
     int trace;                    // non-zero: record phase timestamps in the trace area
 };
 constexpr int kWsHeaderBytes = 256;
-// trace area (after the residual buffers): per CTA kTraceSlots u64 globaltimer stamps
+// trace area (at the end of the workspace): per CTA kTraceSlots u64
 constexpr int kTraceCtas = 160;
 constexpr int kTraceSlots = 1024;   // (tag, time) pairs
 
-// Accumulator set layout (floats), per token b:
-struct AccLayout {
-    long long gu, gus, aacc, z, lin, y, logr, logh, total;   // offsets of [B] blocks
+// Workspace after the header, per step parity p in {0, 1} and state row s:
+//   y        [2][Ls][B][d]  fp32  layer output accumulators (red.add)
+//   logits_r [2][Ls][B][E]  fp32  own-router logits
+//   logits_h [2][Ls][B][E]  fp32  head logits (row of the head's owner)
+//   count    [2][Ls]        u32   head-work arrivals
+struct WsLayout {
+    long long y, logr, logh, cnt, trace, total;   // byte offsets
 };
-inline __host__ __device__ AccLayout acc_layout(int B, int K, int I, int Is, int r, int H, int E, int d) {
-    AccLayout a;
-    long long o = 0;
-    a.gu = o;   o += (long long)B * K * 2 * I;
-    a.gus = o;  o += (long long)B * 2 * Is;
-    a.aacc = o; o += (long long)B * 2 * ceil_div(r, 16) * 16;
-    a.z = o;    o += (long long)B * H;
-    a.lin = o;  o += (long long)B * E;
-    a.y = o;    o += (long long)B * d;
-    a.logr = o; o += (long long)B * E;
-    a.logh = o; o += (long long)B * E;
-    a.total = (o + 63) / 64 * 64;
-    return a;
-}
-// workspace: header | 3 accumulator sets | 2 residual buffers [B, d] fp16
-inline __host__ __device__ long long ws_bytes(int B, int K, int I, int Is, int r, int H, int E, int d) {
-    AccLayout a = acc_layout(B, K, I, Is, r, H, E, d);
-    return kWsHeaderBytes + 3 * a.total * 4 + 2LL * B * d * 2 + 256 +
-           (long long)kTraceCtas * kTraceSlots * 8;
+inline __host__ __device__ WsLayout ws_layout(int Ls, int B, int d, int E) {
+    WsLayout w;
+    long long o = kWsHeaderBytes;
+    w.y = o;     o += 2LL * Ls * B * d * 4;
+    w.logr = o;  o += 2LL * Ls * B * E * 4;
+    w.logh = o;  o += 2LL * Ls * B * E * 4;
+    w.cnt = o;   o += (2LL * Ls * 4 + 255) / 256 * 256;
+    w.trace = o; o += (long long)kTraceCtas * kTraceSlots * 8;
+    w.total = o;
+    return w;
 }
 
 // --------------------------------------------------------------- PTX -----
@@ -157,7 +155,7 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
 }
 __device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(
@@ -169,10 +167,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar))
                  : "memory");
 }
+// parity wait with cluster-scope acquire: also orders the data that the other CTA
+// of the cluster wrote with st.async before completing the transaction
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -194,12 +194,51 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
     return p;
 }
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+
+// ---- thread-block cluster (CTA pairs) ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// 16-byte store into another CTA's shared memory that completes `bytes` on its mbarrier
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];\n"
+        ::"r"(raddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
+        : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" :::
+                     "memory");
+}
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
     asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;\n" ::"l"(p), "f"(v) : "memory");
 }
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1,%2,%3,%4};\n" ::"l"(p), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
 __device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_acq_rel_add_u32(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
@@ -217,53 +256,28 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-// position of group-local input o (0..15 within a 16-input quarter) in the
-// lane's 16 B-fragment halves; the map is its own inverse
-__device__ __forceinline__ int frag_pos(int o) {
-    const int lo = o & 7;
-    const int m = (lo == 1) ? 4 : (lo == 4) ? 1 : (lo == 3) ? 6 : (lo == 6) ? 3 : lo;
-    return (o & 8) | m;
-}
-
-// Write one group (64 inputs) of B fragments: lane holds inputs lane and lane+32.
-// Odd inputs (those the int4 masks deliver as 16 q 2^-24) are stored divided by 16.
-// With `lo` non-null the value is split v = hi + lo * 2^-11 (hi = fp16(v), lo =
-// fp16((v - hi) * 2^11)); the two halves go to two tensor-core columns so the
-// products keep ~22 bits of the fp32 activation.  Sums are of the represented
-// values (hi, and v - hi).
-constexpr float kLoScale = 2048.0f;
-constexpr float kLoInv = 1.0f / 2048.0f;
-
-__device__ __forceinline__ void put_one(__half* frag, int j, __half h) {
-    const int o = j & 15;
-    frag[(j >> 4) * 16 + frag_pos(o)] = (o & 1) ? __float2half_rn(__half2float(h) * 0.0625f) : h;
-}
-
 __device__ __forceinline__ float warp_sum(float s) {
 #pragma unroll
     for (int k = 16; k; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
     return s;
 }
 
-__device__ __forceinline__ void put_group(__half* frag, float* sum_out, float v0, float v1,
-                                          int lane, __half* lo = nullptr,
-                                          float* lo_sum_out = nullptr) {
-    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-    put_one(frag, lane, h0);
-    put_one(frag, lane + 32, h1);
-    const float s = warp_sum(__half2float(h0) + __half2float(h1));
-    if (lane == 0) *sum_out = s;
-    if (lo) {
-        const float r0 = v0 - __half2float(h0), r1 = v1 - __half2float(h1);
-        put_one(lo, lane, __float2half_rn(r0 * kLoScale));
-        put_one(lo, lane + 32, __float2half_rn(r1 * kLoScale));
-        const float sl = warp_sum(r0 + r1);
-        if (lane == 0) *lo_sum_out = sl;
-    }
-}
+// Activation sources are split v = hi + lo * 2^-11 (hi = fp16(v), lo =
+// fp16((v - hi) * 2^11)) and the halves go to two tensor-core columns, so the
+// products keep ~22 bits of the fp32 value.
+constexpr float kLoScale = 2048.0f;
+constexpr float kLoInv = 1.0f / 2048.0f;
+constexpr float kTwo24 = 16777216.0f;   // int4 nibbles enter the tensor cores as q * 2^-24
 
-// engine entry (engine.cu)
+// engine (engine.cu)
 __global__ void engine_kernel(const __grid_constant__ Prog prog);
-int engine_smem_bytes(const Prog& p);
+// grid size (CTAs, a multiple of the cluster size) the engine runs with on the current device
+int engine_grid(int* nct);
+// fills p's derived fields for a grid of nct CTAs and checks the shapes against the
+// engine's limits; *smem_bytes <- dynamic shared memory.  0 or an EDGE0_* status.
+int engine_check(Prog& p, int nct, int smem_max, int* smem_bytes);
+// launch the engine for `p` on `stream` (cooperative, CTA pairs); fills p's derived
+// fields.  Allocates nothing.
+int engine_launch(Prog& p, cudaStream_t stream);
 
 }  // namespace edge0

@@ -57,23 +57,21 @@ extern "C" int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const u
     // the same argument rules as edge0_moe_int4_forward
     if (!moe || !x || !ids || !w || !y) return EDGE0_EINVAL;
     const edge0_moe_desc& m = *moe;
-    if (!m.gate || !m.up || !m.down || !a16(m.gate) || !a16(m.up) || !a16(m.down)) return EDGE0_EINVAL;
+    if (!m.gate_up || !m.down || !a16(m.gate_up) || !a16(m.down)) return EDGE0_EINVAL;
     if (!a16(x) || !a16(y)) return EDGE0_EINVAL;
-    const bool shared = m.sh_gate || m.sh_up || m.sh_down;
-    if (shared && (!m.sh_gate || !m.sh_up || !m.sh_down || !a16(m.sh_gate) || !a16(m.sh_up) ||
-                   !a16(m.sh_down)))
+    const bool shared = m.sh_gate_up || m.sh_down;
+    if (shared && (!m.sh_gate_up || !m.sh_down || !a16(m.sh_gate_up) || !a16(m.sh_down)))
         return EDGE0_EINVAL;
     const int Is = m.Is > 0 ? m.Is : 64;
     if (B <= 0 || B > EDGE0_MAX_BATCH) return EDGE0_EINVAL;
     if (m.d <= 0 || m.d % kGroup || m.I <= 0 || m.I % kGroup || Is % kGroup) return EDGE0_EINVAL;
-    if (m.E <= 0 || m.E > EDGE0_MAX_E || m.E % 8 || m.K <= 0 || m.K > EDGE0_MAX_K || m.K > m.E)
+    if (m.E <= 0 || m.E > EDGE0_MAX_E || m.E % 16 || m.K <= 0 || m.K > EDGE0_MAX_K || m.K > m.E)
         return EDGE0_EINVAL;
     if (m.slot_table && m.n_slots <= 0) return EDGE0_EINVAL;
-    if (2 * B * m.K + 8 > kMaxSeg) return EDGE0_EUNSUPPORTED;
-    // scratch: header, three accumulator sets and the residual buffers (the trace
-    // area at the end of a workspace is never switched on here)
-    const long long need = ws_bytes(B, m.K, m.I, Is, 16, 64, m.E, m.d) -
-                           (long long)kTraceCtas * kTraceSlots * 8;
+    // scratch: header and the accumulators of one layer in two step parities (the
+    // trace area at the end of a workspace is never switched on here)
+    const WsLayout wl = ws_layout(1, B, m.d, m.E);
+    const long long need = wl.trace;
     if (need > (long long)EDGE0_NOALLOC_SCRATCH_BYTES) return EDGE0_EUNSUPPORTED;
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
@@ -102,43 +100,15 @@ extern "C" int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const u
     p.Ls = 1;
     p.ws = (char*)scratch;
     LayerP& P = p.layers[0];
-    P.gate = (const char*)m.gate;
-    P.up = (const char*)m.up;
+    P.gu = (const char*)m.gate_up;
     P.down = (const char*)m.down;
     P.slot_table = m.slot_table;
     P.n_slots = m.slot_table ? m.n_slots : m.E;
     if (shared) {
-        P.sh_gate = (const char*)m.sh_gate;
-        P.sh_up = (const char*)m.sh_up;
+        P.sh_gu = (const char*)m.sh_gate_up;
         P.sh_down = (const char*)m.sh_down;
         P.flags = LF_SHARED;
     }
     P.n_groups = P.topk_groups = P.head_n_groups = P.head_topk_groups = 1;
-
-    int dev = 0, nsm = 0, maxsm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return EDGE0_ECUDA;
-    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return EDGE0_ECUDA;
-    if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-        return EDGE0_ECUDA;
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, engine_kernel) != cudaSuccess) return EDGE0_ECUDA;
-    const int smem = engine_smem_bytes(p);
-    if (smem + (int)fa.sharedSizeBytes > maxsm) return EDGE0_EUNSUPPORTED;
-    if (cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return EDGE0_ECUDA;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(nsm);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, engine_kernel, p) != cudaSuccess) return EDGE0_ECUDA;
-    return EDGE0_OK;
+    return engine_launch(p, stream);
 }

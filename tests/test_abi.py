@@ -43,20 +43,26 @@ def test_status_strings(lib):
 
 
 def test_sizes(lib):
-    # packed sizes equal the canonical sizes when rows are a multiple of 16
-    assert lib.edge0_q4_packed_bytes(1, 512, 2048) == 512 * 2048 // 2 + 512 * 32 * 4
-    assert lib.edge0_q4_packed_bytes(256, 512, 2048) * 3 // 256 == 3 * 589824
-    assert lib.edge0_q4_packed_bytes(1, 512, 100) == 0          # in % 64
+    # packed sizes equal the canonical sizes when rows are a multiple of 16:
+    # 1,769,472 bytes per 35B-tier expert (gate + up + down at d=2048, I=512)
+    gu = lib.edge0_q4_gate_up_packed_bytes(1, 512, 2048)
+    dn = lib.edge0_q4_down_packed_bytes(1, 2048, 512)
+    assert gu == 2 * (512 * 2048 // 2 + 512 * 32 * 4)
+    assert gu + dn == 1769472
+    assert lib.edge0_q4_gate_up_packed_bytes(256, 512, 2048) == 256 * gu
+    assert lib.edge0_q4_down_packed_bytes(1, 512, 100) == 0     # in % 64
     assert lib.edge0_f16_packed_bytes(512, 2048) == 512 * 2048 * 2
     assert lib.edge0_f16_packed_bytes(4, 128) == 16 * 128 * 2   # rows padded to 16
-    assert binding.workspace_bytes(2048, 256, 4, 512, 512, 512, 16, 1) > 0
-    assert lib.edge0_workspace_bytes(0, 1, 1, 1, 1, 1, 1, 1) == 0
+    assert binding.workspace_bytes(40, 1, 2048, 256) > 0
+    assert lib.edge0_workspace_bytes(0, 1, 2048, 256) == 0
 
 
 def test_host_validation_rejects_bad_arguments(lib):
     E = binding.EDGE0_EINVAL
-    assert lib.edge0_pack_q4(None, None, None, 1, 16, 64, None, None) == E
+    assert lib.edge0_pack_q4_gate_up(None, None, None, None, None, None, 1, 64, 64, None, None) == E
+    assert lib.edge0_pack_q4_down(None, None, None, 1, 16, 64, None, None) == E
     assert lib.edge0_pack_f16(None, 16, 64, 64, None, None) == E
+    assert lib.edge0_pack_f16_kmajor(None, 16, 64, 64, None, None) == E
     assert lib.edge0_pack_cols_T(None, 16, 64, 0, 8, None, None) == E
     assert lib.edge0_moe_int4_forward(None, None, None, None, 1, None, None, 0, None) == E
     assert lib.edge0_prerouter_topk(None, None, None, None, 1, None, None, None, None, 0, None) == E
@@ -66,14 +72,14 @@ def test_host_validation_rejects_bad_arguments(lib):
     st = binding.RouteState()
     assert lib.edge0_state_init(C.byref(st), None) == E
     # a MoE descriptor with an input width that is not a multiple of the group
-    moe = binding.MoeDesc(100, 16, 2, 128, 128, 16, 16, 16, None, None, None, None, 0)
+    moe = binding.MoeDesc(100, 16, 2, 128, 128, 16, 16, None, None, None, 0)
     x = C.c_void_p(16)
     assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 1, x, x, 1 << 20, None) == E
     # K > E
-    moe = binding.MoeDesc(256, 16, 17, 128, 128, 16, 16, 16, None, None, None, None, 0)
+    moe = binding.MoeDesc(256, 16, 17, 128, 128, 16, 16, None, None, None, 0)
     assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 1, x, x, 1 << 20, None) == E
     # batch above the limit
-    moe = binding.MoeDesc(256, 16, 2, 128, 128, 16, 16, 16, None, None, None, None, 0)
+    moe = binding.MoeDesc(256, 16, 2, 128, 128, 16, 16, None, None, None, 0)
     assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 99, x, x, 1 << 20, None) == E
     # misaligned input pointer
     assert lib.edge0_moe_int4_forward(C.byref(moe), C.c_void_p(18), x, x, 1, x, x, 1 << 20, None) == E

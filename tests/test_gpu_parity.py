@@ -40,75 +40,126 @@ def _cpu_model(model):
 
 
 # ------------------------------------------------------------- packing ----
-def _ref_pack_q4(q, s, b):
+# Reference packers written from the layout description in include/edge0.h:
+# lane L = 4g + t of a row tile's 16-input step holds rows g and g + 8 at
+# step-local inputs {2t, 2t+1, 2t+8, 2t+9}.
+_NIB = [(0, 0), (1, 0), (0, 8), (1, 8), (0, 1), (1, 1), (0, 9), (1, 9)]   # (row + 8?, k offset) of nibble p
+
+
+def _nibbles(q):
+    """q [..., in/8] int32 -> [..., in] int64 nibble values (input 8j+i = nibble i of word j)."""
+    w = q.to(torch.int64) & 0xFFFFFFFF
+    return torch.stack([(w >> (4 * i)) & 0xF for i in range(8)], dim=-1).flatten(-2)
+
+
+def _q4_units(N, S, Bq):
+    """N [..., 16, in] nibbles of one row tile, S/Bq [..., 16, in/64] fp16 ->
+    words [..., in/64, 4, 32] (step, lane) int64 and scales [..., in/64, 8, 4] int16."""
+    inp = N.shape[-1]
+    ng = inp // 64
+    Nv = N.reshape(*N.shape[:-1], ng, 4, 16)            # [..., 16 rows, group, step, k]
+    words = torch.zeros(*N.shape[:-2], ng, 4, 32, dtype=torch.int64)
+    for g in range(8):
+        for t in range(4):
+            w = torch.zeros(*N.shape[:-2], ng, 4, dtype=torch.int64)
+            for pos, (hi, ko) in enumerate(_NIB):
+                w |= Nv[..., g + 8 * hi, :, :, 2 * t + ko] << (4 * pos)
+            words[..., 4 * g + t] = w
+    sv = S.view(torch.int16).transpose(-1, -2)          # [..., group, 16 rows]
+    bv = Bq.view(torch.int16).transpose(-1, -2)
+    sc = torch.stack([sv[..., :8], bv[..., :8], sv[..., 8:], bv[..., 8:]], dim=-1)   # [..., group, 8, 4]
+    return words, sc
+
+
+def _to_u8(words, sc):
+    """unit bytes: 4 step words per lane (lane-major, 16 B each) then 64 B of scales."""
+    w32 = words.to(torch.int32)                          # wraps to the same bits
+    lane_major = w32.transpose(-1, -2).contiguous()      # [..., group, 32 lanes, 4 steps]
+    a = lane_major.view(torch.uint8).flatten(-3)         # [..., group * 512]
+    return a, sc.contiguous().view(torch.uint8)
+
+
+def _ref_pack_gate_up(gate, up):
+    qg, sg, bg = gate
+    qu, su, bu = up
+    E, I, w8 = qg.shape
+    Ng, Nu = _nibbles(qg), _nibbles(qu)                  # [E, I, d]
+    rows = torch.cat([Ng.view(E, I // 8, 8, -1), Nu.view(E, I // 8, 8, -1)], dim=2)   # [E, tiles, 16, d]
+    S = torch.cat([sg.view(E, I // 8, 8, -1), su.view(E, I // 8, 8, -1)], dim=2)
+    Bq = torch.cat([bg.view(E, I // 8, 8, -1), bu.view(E, I // 8, 8, -1)], dim=2)
+    words, sc = _q4_units(rows, S, Bq)                   # [E, tiles, ng, 4, 32], [E, tiles, ng, 8, 4]
+    w32 = words.to(torch.int32).transpose(-1, -2).contiguous()              # [E, tiles, ng, 32, 4]
+    units = torch.cat([w32.view(torch.uint8).flatten(-2), sc.contiguous().view(torch.uint8).flatten(-2)], -1)
+    return units.reshape(-1)
+
+
+def _ref_pack_down(trip):
+    q, s, b = trip
     E, out, w8 = q.shape
-    n_rt, ng = (out + 15) // 16, w8 // 8
-    qp = torch.zeros(E, n_rt * 16, w8, dtype=torch.int32)
-    qp[:, :out] = q
-    sp = torch.zeros(E, n_rt * 16, ng, dtype=torch.int16)
-    bp = torch.zeros(E, n_rt * 16, ng, dtype=torch.int16)
-    sp[:, :out] = s.view(torch.int16)
-    bp[:, :out] = b.view(torch.int16)
-    qw = qp.view(E, n_rt, 16, ng, 8)
-    unit = torch.zeros(E, n_rt, ng, 144, dtype=torch.int32)     # 576 bytes
+    n_rt = (out + 15) // 16
+    N = torch.zeros(E, n_rt * 16, w8 * 8, dtype=torch.int64)
+    N[:, :out] = _nibbles(q)
+    S = torch.zeros(E, n_rt * 16, s.shape[-1], dtype=torch.float16)
+    Bq = torch.zeros_like(S)
+    S[:, :out] = s
+    Bq[:, :out] = b
+    words, sc = _q4_units(N.view(E, n_rt, 16, -1), S.view(E, n_rt, 16, -1), Bq.view(E, n_rt, 16, -1))
+    # words [E, rt, g, 4 steps, 32 lanes] -> per group: [4 steps][rt][32 lanes] words, then [rt] scales
+    w = words.to(torch.int32).permute(0, 2, 3, 1, 4).contiguous()           # [E, g, 4, rt, 32]
+    scv = sc.permute(0, 2, 1, 3, 4).contiguous()                            # [E, g, rt, 8, 4]
+    ng = w.shape[1]
+    per_g = torch.cat([w.view(torch.uint8).view(E, ng, -1), scv.view(torch.uint8).view(E, ng, -1)], -1)
+    return per_g.reshape(-1)
+
+
+def _ref_pack_f16(W, cols=None, kmajor=False):
+    out, ld = W.shape
+    inp = cols or ld
+    n_rt, ns = (out + 15) // 16, inp // 16
+    Wp = torch.zeros(n_rt * 16, inp, dtype=torch.int16)
+    Wp[:out] = W[:, :inp].view(torch.int16)
+    Wv = Wp.view(n_rt, 16, ns, 16)                       # [rt, row, step, k]
+    blk = torch.zeros(n_rt, ns, 32, 8, dtype=torch.int16)
     for g in range(8):
         for t in range(4):
             L = 4 * g + t
-            unit[..., 4 * L + 0] = qw[:, :, g, :, 2 * t]
-            unit[..., 4 * L + 1] = qw[:, :, g, :, 2 * t + 1]
-            unit[..., 4 * L + 2] = qw[:, :, g + 8, :, 2 * t]
-            unit[..., 4 * L + 3] = qw[:, :, g + 8, :, 2 * t + 1]
-    u16 = unit.view(torch.int16).view(E, n_rt, ng, 288)
-    sv = sp.view(E, n_rt, 16, ng).permute(0, 1, 3, 2)
-    bv = bp.view(E, n_rt, 16, ng).permute(0, 1, 3, 2)
-    for g in range(8):
-        u16[..., 256 + 4 * g + 0] = sv[..., g]
-        u16[..., 256 + 4 * g + 1] = bv[..., g]
-        u16[..., 256 + 4 * g + 2] = sv[..., g + 8]
-        u16[..., 256 + 4 * g + 3] = bv[..., g + 8]
-    return unit.view(torch.uint8).reshape(-1)
+            order = [(g, 2 * t), (g, 2 * t + 1), (g + 8, 2 * t), (g + 8, 2 * t + 1),
+                     (g, 2 * t + 8), (g, 2 * t + 9), (g + 8, 2 * t + 8), (g + 8, 2 * t + 9)]
+            for j, (row, k) in enumerate(order):
+                blk[:, :, L, j] = Wv[:, row, :, k]
+    if kmajor:
+        blk = blk.transpose(0, 1).contiguous()
+    return blk.view(torch.uint8).reshape(-1)
 
 
-def _ref_pack_f16(W, cols=None):
-    out, ld = W.shape
-    inp = cols or ld
-    n_rt, ng = (out + 15) // 16, inp // 64
-    Wp = torch.zeros(n_rt * 16, inp, dtype=torch.int16)
-    Wp[:out] = W[:, :inp].view(torch.int16)
-    Wv = Wp.view(n_rt, 16, ng, 64)
-    unit = torch.zeros(n_rt, ng, 4, 32, 8, dtype=torch.int16)
-    for m in range(4):
-        for g in range(8):
-            for t in range(4):
-                L = 4 * g + t
-                for j in range(2):
-                    k = 16 * t + (m & 1) + 8 * (m >> 1) + 2 * j
-                    unit[:, :, m, L, 4 * j + 0] = Wv[:, g, :, k]
-                    unit[:, :, m, L, 4 * j + 1] = Wv[:, g, :, k + 4]
-                    unit[:, :, m, L, 4 * j + 2] = Wv[:, g + 8, :, k]
-                    unit[:, :, m, L, 4 * j + 3] = Wv[:, g + 8, :, k + 4]
-    return unit.view(torch.uint8).reshape(-1)
+@pytest.mark.parametrize("E,I,d", [(3, 64, 256), (2, 128, 128), (1, 512, 2048)])
+def test_pack_q4_gate_up_layout(E, I, d):
+    gate = inputs.int4_stack(5, 1, 1, E, I, d)
+    up = inputs.int4_stack(5, 1, 2, E, I, d)
+    got = binding.pack_q4_gate_up(tuple(t.to(DEV) for t in gate), tuple(t.to(DEV) for t in up)).cpu()
+    assert torch.equal(got, _ref_pack_gate_up(gate, up))
 
 
-@pytest.mark.parametrize("E,out,inp", [(3, 48, 256), (2, 20, 128), (1, 512, 2048)])
-def test_pack_q4_layout(E, out, inp):
-    q, s, b = inputs.int4_stack(5, 1, 1, E, out, inp)
-    got = binding.pack_q4(q.to(DEV), s.to(DEV), b.to(DEV)).cpu()
-    assert torch.equal(got, _ref_pack_q4(q, s, b))
+@pytest.mark.parametrize("E,out,inp", [(3, 48, 256), (2, 20, 128), (1, 2048, 512)])
+def test_pack_q4_down_layout(E, out, inp):
+    trip = inputs.int4_stack(6, 1, 3, E, out, inp)
+    got = binding.pack_q4_down(tuple(t.to(DEV) for t in trip)).cpu()
+    assert torch.equal(got, _ref_pack_down(trip))
 
 
 @pytest.mark.parametrize("out,inp,cols", [(48, 256, None), (4, 128, None), (64, 288, 256)])
-def test_pack_f16_layout(out, inp, cols):
+@pytest.mark.parametrize("kmajor", [False, True])
+def test_pack_f16_layout(out, inp, cols, kmajor):
     W = (torch.randn(out, inp, generator=torch.Generator().manual_seed(3))).half()
-    got = binding.pack_f16(W.to(DEV), cols=cols).cpu()
-    assert torch.equal(got, _ref_pack_f16(W, cols))
+    got = binding.pack_f16(W.to(DEV), cols=cols, kmajor=kmajor).cpu()
+    assert torch.equal(got, _ref_pack_f16(W, cols, kmajor))
     T = binding.pack_cols_T(W.to(DEV), 8, 16).cpu()
     assert torch.equal(T, W[:, 8:24].t().contiguous())
 
 
 # ------------------------------------------------------ standalone ops ----
 def _moe_ws(cfg, B):
-    n = binding.workspace_bytes(cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, 64, 16, B)
+    n = binding.workspace_bytes(1, B, cfg.d, cfg.E)
     return torch.zeros(n, dtype=torch.uint8, device=DEV)
 
 
@@ -149,7 +200,7 @@ def test_prerouter_topk(cfg, with_prev):
     dm = binding.DeviceModel(model, DEV)
     hd = model.layers[0].head
     tgt_bias = model.layers[hd["target"]].bias
-    n = binding.workspace_bytes(cfg.d, cfg.E, cfg.K, 64, 64, cfg.H, 16, cfg.B)
+    n = binding.workspace_bytes(1, cfg.B, cfg.d, cfg.E)
     ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
     x = torch.stack([oracle.rmsnorm(h) for h in inputs.hidden(cfg, 4, seed=21)])
     ex, _ = inputs.routing(cfg, 21, 1)

@@ -33,7 +33,7 @@ def _built():
 def test_noalloc_matches_the_workspace_entry_point_two_calls_in_a_row(cfg):
     model = inputs.make_model(cfg.with_(L=1), seed=41)
     dm = binding.DeviceModel(model, DEV)
-    ws = torch.zeros(binding.workspace_bytes(cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, 64, 16, cfg.B),
+    ws = torch.zeros(binding.workspace_bytes(1, cfg.B, cfg.d, cfg.E),
                      dtype=torch.uint8, device=DEV)
     lib = binding.lib()
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -54,7 +54,9 @@ def test_noalloc_matches_the_workspace_entry_point_two_calls_in_a_row(cfg):
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = binding.lib()
     x = C.c_void_p(256)
-    # d = 16384 with 512 experts of intermediate 4096 needs more than the fixed array
-    moe = binding.MoeDesc(16384, 512, 8, 4096, 4096, 256, 256, 256, None, None, None, None, 0)
+    # d = 4096 with 512 experts at B = 4 needs 256 + 8 B d + 16 B E + 256 = 164,352
+    # bytes of scratch, more than the fixed array holds
+    moe = binding.MoeDesc(4096, 512, 8, 512, 512, 256, 256, None, None, None, 0)
+    assert binding.lib().edge0_workspace_bytes(1, 4, 4096, 512) - 160 * 1024 * 8 > 128 * 1024
     rc = lib.edge0_moe_int4_forward_noalloc(C.byref(moe), x, x, x, 4, x, None)
     assert rc == binding.EDGE0_EUNSUPPORTED

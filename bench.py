@@ -184,7 +184,8 @@ def run_gpu(args, rank, world):
         binding.decode_step(dm, st, h_all[t], t)
         t += 1
     barrier()
-    assert st.error() == 0, "kernel error during warm-up"
+    err = st.error()
+    assert err == 0, f"kernel error during warm-up: {binding.status_string(err)}"
 
     if args.trace:
         st.set_trace(True)
@@ -208,7 +209,8 @@ def run_gpu(args, rank, world):
             t += 1
         t_end.record(stream)
         barrier()
-    assert st.error() == 0, "kernel error in the timed region"
+    err = st.error()
+    assert err == 0, f"kernel error in the timed region: {binding.status_string(err)}"
     region_ms = t_start.elapsed_time(t_end)
     kern_ms = [a.elapsed_time(b) for a, b in ev]
 
@@ -287,33 +289,57 @@ def run_gpu(args, rank, world):
     return line
 
 
-def print_trace(tr, nct):
-    """Per-layer split of one traced decode step, averaged over CTAs: barrier wait
-    and x, own routing, gate/up, pair exchange, act, down (to the barrier
-    arrival), head."""
+def print_trace(tr, nct, sm_mhz=2070.0):
+    """Per-layer split of one traced decode step, averaged over CTAs (durations
+    from each SM's cycle counter): barrier wait and x, own routing, gate/up,
+    pair exchange, act, down (to the barrier arrival), head; the act and down
+    phases split further; and the producer's timeline relative to the
+    consumer's layer start (globaltimer)."""
     import collections
+    cons, prod = tr
     names = ("wait+x", "route", "gate/up", "xchg", "act", "down", "head")
     acc = collections.defaultdict(list)
+    sub = collections.defaultdict(list)
+    rel = collections.defaultdict(list)
+    us = lambda cyc: cyc / sm_mhz
     for c in range(nct):
-        ev = {}
-        for tag, tm in tr[c].tolist():
-            if tm == 0:
-                break
-            ev[tag] = tm
+        ev, evt = {}, {}
+        for tag, tm, cy in cons[c].tolist():
+            if tm != 0:
+                ev[tag] = cy
+                evt[tag] = tm
+        pev = {}
+        for tag, tm, cy in prod[c].tolist():
+            if tm != 0:
+                pev[tag] = tm
         for l in sorted({k >> 8 for k in ev}):
             pts = [ev.get((l << 8) | i) for i in range(8)]
             if None in pts:
                 continue
-            acc[l].append(tuple(pts[i + 1] - pts[i] for i in range(7)))
+            acc[l].append(tuple(us(pts[i + 1] - pts[i]) for i in range(7)))
+            x = [ev.get((l << 8) | k) for k in (4, 10, 11, 5, 9, 12, 6)]
+            if None not in x:
+                sub[l].append(tuple(us(x[i + 1] - x[i]) for i in range(6)))
+            t0 = evt[(l << 8) | 0]
+            r = [pev.get((l << 8) | k) for k in (0x80, 0x81, 0x83)]
+            if None not in r:
+                rel[l].append(tuple((v - t0) / 1e3 for v in r))
     tot = [0.0] * 7
     lines = []
+    subn = ("act:zero", "act:rows", "act:tail", "dn:wait", "dn:rows", "dn:release")
     for l in sorted(acc):
         v = acc[l]
-        m = [statistics.mean(x[i] for x in v) / 1e3 for i in range(7)]
-        mx = [max(x[i] for x in v) / 1e3 for i in range(7)]
+        m = [statistics.mean(x[i] for x in v) for i in range(7)]
+        mx = [max(x[i] for x in v) for i in range(7)]
         tot = [a + b for a, b in zip(tot, m)]
+        extra = ""
+        if sub[l]:
+            extra += " | " + " ".join(f"{n} {statistics.mean(x[i] for x in sub[l]):.2f}" for i, n in enumerate(subn))
+        if rel[l]:
+            extra += " | producer " + " ".join(f"{n} {statistics.mean(x[i] for x in rel[l]):+.1f}"
+                                              for i, n in enumerate(("tab0", "tab1", "issued")))
         lines.append(f"layer {l:2d}: " + " ".join(f"{n} {a:5.2f}/{b:5.2f}" for n, a, b in zip(names, m, mx))
-                     + " us (mean/max)")
+                     + " us (mean/max)" + extra)
     sys.stderr.write("\n".join(lines) + "\n")
     sys.stderr.write("total (mean over CTAs): " + " ".join(f"{n} {a:.1f}" for n, a in zip(names, tot)) + " us\n")
 

@@ -273,7 +273,7 @@ class DecodeState:
                              _ptr(self.exec_ids), _ptr(self.workspace), nbytes)
         _check(lib().edge0_state_init(C.byref(self.st), _stream(stream)), "edge0_state_init")
 
-    TRACE_CTAS, TRACE_SLOTS = 160, 1024
+    TRACE_CTAS, TRACE_SLOTS, TRACE_PRODUCER = 160, 4096, 3072
 
     def set_trace(self, on):
         """Switch the engine's per-layer trace on/off (workspace header flag)."""
@@ -285,12 +285,18 @@ class DecodeState:
         torch.cuda.synchronize(self.workspace.device)
 
     def read_trace(self):
-        """[CTAs, events, 2] int64: (tag, globaltimer ns) pairs, tag = layer << 8 | point
-        (0 start, 1 x built, 2 routed, 3 gate/up done, 4 exchange done, 5 act done,
-        6 down done + barrier arrival, 7 head done)."""
+        """(consumer, producer): [CTAs, events, 3] int64 (tag, globaltimer ns, SM clock)
+        triples; consumer tags are layer << 8 | point (0 start, 1 x built, 2 routed,
+        3 gate/up done, 4 exchange done, 5 act done, 6 down done + barrier arrival,
+        7 head done, 8 gate/up data seen, 9 down data seen, 10-12 inside act/down),
+        producer tags layer << 8 | 0x80 + point (table started, built, routing
+        known, items issued)."""
         torch.cuda.synchronize(self.workspace.device)
         raw = self.workspace[-self.TRACE_CTAS * self.TRACE_SLOTS * 8:].cpu().view(torch.int64)
-        return raw.view(self.TRACE_CTAS, self.TRACE_SLOTS // 2, 2)
+        raw = raw.view(self.TRACE_CTAS, self.TRACE_SLOTS)
+        cons = raw[:, :self.TRACE_PRODUCER // 3 * 3].reshape(self.TRACE_CTAS, -1, 3)
+        prod = raw[:, self.TRACE_PRODUCER:self.TRACE_PRODUCER + (self.TRACE_SLOTS - self.TRACE_PRODUCER) // 3 * 3].reshape(self.TRACE_CTAS, -1, 3)
+        return cons, prod
 
     def error(self, stream=None) -> int:
         code = C.c_int(0)

@@ -45,14 +45,20 @@ constexpr int kMaxItems = 96;      // copy items of one CTA in one layer
 constexpr int kItemMax = 32768;    // bytes of one copy item
 constexpr int kSlots = 256;        // item barriers (>= 2 x kMaxItems)
 constexpr int kTables = 3;         // layer tables in flight
-constexpr int kMaxChunks = 8;      // 4-element chunks of [B, d] per consumer thread
+constexpr int kMaxChunks = 4;      // 4-element chunks of [B, d] per consumer thread
 constexpr int kMaxD = 4096;
 constexpr int kMinRing = 2 * kItemMax;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // bounded waits: 2 s
 
+// Copy items.  Unit items (router, gate/up, LoRA A, fc1, linear_init) copy a run
+// of n consecutive units of the CTA's half of the input groups, from unit b of
+// the half (the run may cross row tiles).  Down items copy n consecutive 16-row
+// steps (from step b of group a) over the CTA's half of the output rows (DQ),
+// those followed by the group's scales (DQS, when the run ends at step 3), or the
+// scales alone (DSC).
 enum ItemKind : int {
-    IT_ROUTER = 0, IT_GU, IT_LA, IT_LU, IT_BG, IT_BU, IT_DSC, IT_DQ, IT_ADT, IT_BD, IT_FC1, IT_FC2,
-    IT_LINIT
+    IT_ROUTER = 0, IT_GU, IT_LA, IT_LU, IT_BG, IT_BU, IT_DSC, IT_DQ, IT_DQS, IT_ADT, IT_BD, IT_FC1,
+    IT_FC2, IT_LINIT
 };
 __host__ __device__ inline bool unit_kind(int k) {
     return k == IT_ROUTER || k == IT_GU || k == IT_LA || k == IT_LU || k == IT_FC1 || k == IT_LINIT;
@@ -76,15 +82,18 @@ struct PairPlan {
     int ru0, ru1; // router units (in this rank's half of d)
 };
 
+// [n i / parts, n (i + 1) / parts): 32-bit arithmetic (n * parts < 2^31 for
+// every split the engine makes; the host checks the shapes)
 __host__ __device__ inline void split_range(int n, int parts, int i, int* a, int* b) {
-    *a = (int)((long long)n * i / parts);
-    *b = (int)((long long)n * (i + 1) / parts);
+    *a = n * i / parts;
+    *b = n * (i + 1) / parts;
 }
 
 struct Shape {
     int d, I, Is, E, H, r;
     int n_slots;                      // routed expert slots (0: none)
     int shared, lora, head, router;   // parts present in the layer
+    int ps;                           // pairs that own shared-expert rows
 };
 
 __host__ __device__ inline int shared_pairs(int P, int n_sh, int n_rt, bool lora) {
@@ -116,7 +125,7 @@ __host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int r
     const int hpe = S.I / kHalfRow;
     const int n_sh = S.shared ? S.Is / kHalfRow : 0;
     const int n_rt = S.n_slots * hpe;
-    const int Ps = shared_pairs(P, n_sh, n_rt, S.lora != 0);
+    const int Ps = S.ps;
     int a, b;
     if (pair < Ps) {
         split_range(n_sh, Ps, pair, &a, &b);
@@ -192,92 +201,110 @@ __host__ __device__ inline Halves halves(int d, int E, int rank) {
     return h;
 }
 
+// appends one item (or, for a run of units, as many items of at most kItemMax
+// bytes as it takes) to T, placing it in the ring at the running position `lin`
+struct ItemSink {
+    LayerTab* T;
+    int n, lin, pos, ring;   // pos = lin mod ring
+    bool ok;
+};
+__host__ __device__ __noinline__ void push_item(ItemSink& k, int kind, int seg, int bytes, int a, int b,
+                                                int cnt) {
+    if (bytes <= 0) return;
+    if (k.n >= kMaxItems || bytes > kItemMax || bytes > k.ring) { k.ok = false; return; }
+    if (k.pos + bytes > k.ring) { k.lin += k.ring - k.pos; k.pos = 0; }   // no item wraps
+    Item& it = k.T->it[k.n++];
+    it.kind = kind; it.seg = seg; it.bytes = bytes; it.off = k.pos; it.lin = k.lin;
+    it.a = a; it.b = b; it.n = cnt;
+    k.lin += bytes;
+    k.pos += bytes;
+}
+__host__ __device__ __noinline__ void push_units(ItemSink& k, int kind, int seg, int a, int first,
+                                                 int units, int ub) {
+    const int per = kItemMax / ub;
+    for (int j = 0; j < units; j += per) {
+        const int m = units - j < per ? units - j : per;
+        push_item(k, kind, seg, m * ub, a, first + j, m);
+    }
+}
+
 // Builds one CTA's copy items of one layer into T (deterministic: the producer
 // issues them, the consumers read them from the published table, the host uses
 // it to check limits).  `lin` is the running linear ring position.  Returns
 // false if a limit is exceeded.
-__host__ __device__ inline bool build_items(const Shape& Sh, int P, int pair, int rank, int ring,
-                                            LayerTab* T, int& lin) {
+__host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pair, int rank, int ring,
+                                                  LayerTab* T, int& lin) {
     PairPlan& pl = T->pl;
     pair_plan(Sh, P, pair, rank, pl);
     if (pl.over) return false;
     const Halves hv = halves(Sh.d, Sh.E, rank);
-    int n = 0;
-    bool ok = true;
-    auto push = [&](int kind, int seg, int bytes, int a, int b, int cnt) {
-        if (bytes <= 0) return;
-        if (n >= kMaxItems || bytes > kItemMax || bytes > ring) { ok = false; return; }
-        if (lin % ring + bytes > ring) lin += ring - lin % ring;
-        Item& it = T->it[n++];
-        it.kind = kind; it.seg = seg; it.bytes = bytes; it.off = lin % ring; it.lin = lin;
-        it.a = a; it.b = b; it.n = cnt;
-        lin += bytes;
-    };
-    // `units` units of `ub` bytes from unit `first` of position a, at most kItemMax bytes a copy
-    auto push_units = [&](int kind, int seg, int a, int first, int units, int ub) {
-        const int per = kItemMax / ub;
-        for (int j = 0; j < units; j += per) {
-            const int m = units - j < per ? units - j : per;
-            push(kind, seg, m * ub, a, first + j, m);
-        }
-    };
+    ItemSink k{T, 0, lin, lin % ring, ring, true};
     const int ngh = hv.gh1 - hv.gh0, nrt = hv.rt1 - hv.rt0, ne = hv.e1 - hv.e0;
     const int r = Sh.r;
     // router units: this pair's share of (E row tiles) x (this rank's groups)
-    for (int u = pl.ru0; u < pl.ru1;) {
-        const int tile = u / ngh, j = u % ngh;
-        const int m = (ngh - j) < (pl.ru1 - u) ? (ngh - j) : (pl.ru1 - u);
-        push_units(IT_ROUTER, 0, tile, j, m, kF16Unit);
-        u += m;
-    }
-    T->p1 = n;
+    push_units(k, IT_ROUTER, 0, 0, pl.ru0, pl.ru1 - pl.ru0, kF16Unit);
+    T->p1 = k.n;
     for (int s = 0; s < pl.nseg; ++s) {
         const Seg& g = pl.seg[s];
-        for (int hr = g.hr0; hr < g.hr1; ++hr) push_units(IT_GU, s, hr, 0, ngh, kQ4Unit);
+        push_units(k, IT_GU, s, 0, g.hr0 * ngh, (g.hr1 - g.hr0) * ngh, kQ4Unit);
         if (g.slot < 0 && Sh.lora) {
-            push_units(IT_LA, s, 0, 0, ngh, kF16Unit);
-            push_units(IT_LU, s, 0, 0, ngh, kF16Unit);
+            push_units(k, IT_LA, s, 0, 0, ngh, kF16Unit);
+            push_units(k, IT_LU, s, 0, 0, ngh, kF16Unit);
             const int rows = (g.hr1 - g.hr0) * kHalfRow;
-            push(IT_BG, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
-            push(IT_BU, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            push_item(k, IT_BG, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            push_item(k, IT_BU, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
         }
     }
-    T->p2 = n;
+    T->p2 = k.n;
     for (int s = 0; s < pl.nseg; ++s) {
         const Seg& g = pl.seg[s];
+        const int qbytes = nrt * kQ4Quarter, sbytes = nrt * kQ4Scales;
+        const int qper = kItemMax / qbytes > 0 ? kItemMax / qbytes : 1;
         for (int gg = g.q0 / 4; gg <= (g.q1 - 1) / 4; ++gg) {
-            push(IT_DSC, s, nrt * kQ4Scales, gg, 0, nrt);
             const int qa = g.q0 > 4 * gg ? g.q0 : 4 * gg, qb = g.q1 < 4 * gg + 4 ? g.q1 : 4 * gg + 4;
-            for (int Q = qa; Q < qb; ++Q) push(IT_DQ, s, nrt * kQ4Quarter, Q, 0, nrt);
+            // runs of steps (at most kItemMax bytes), the scales merged into the last
+            // run when the group's steps and scales are adjacent and fit
+            for (int q = qa; q < qb; q += qper) {
+                const int m = qb - q < qper ? qb - q : qper;
+                const bool last = q + m == qb;
+                if (last && qb == 4 * gg + 4 && m * qbytes + sbytes <= kItemMax) {
+                    push_item(k, IT_DQS, s, m * qbytes + sbytes, gg, q - 4 * gg, m);
+                } else {
+                    push_item(k, IT_DQ, s, m * qbytes, gg, q - 4 * gg, m);
+                    if (last) push_item(k, IT_DSC, s, sbytes, gg, 0, nrt);
+                }
+            }
         }
         if (g.slot < 0 && Sh.lora) {
             const int rows = (g.hr1 - g.hr0) * kHalfRow;
-            push(IT_ADT, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            push_item(k, IT_ADT, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
             const int per = kItemMax / (r * 2);
             for (int row = hv.rt0 * kRowTile; row < hv.rt1 * kRowTile; row += per) {
                 const int m = hv.rt1 * kRowTile - row < per ? hv.rt1 * kRowTile - row : per;
-                push(IT_BD, s, m * r * 2, row, 0, m);
+                push_item(k, IT_BD, s, m * r * 2, row, 0, m);
             }
         }
     }
-    T->p3 = n;
+    T->p3 = k.n;
     const int nH = Sh.H / kRowTile;
     for (int t = pl.hd0; t < pl.hd1; ++t) {
         if (t < nH) {
-            push_units(IT_FC1, 0, t, 0, ngh, kF16Unit);
-            push(IT_FC2, 0, ne * kF16Step, t, hv.e0, ne);
+            push_units(k, IT_FC1, 0, t, t * ngh, ngh, kF16Unit);
+            push_item(k, IT_FC2, 0, ne * kF16Step, t, hv.e0, ne);
         } else {
-            push_units(IT_LINIT, 0, t - nH, 0, ngh, kF16Unit);
+            push_units(k, IT_LINIT, 0, t - nH, (t - nH) * ngh, ngh, kF16Unit);
         }
     }
-    T->n = n;
-    return ok;
+    T->n = k.n;
+    lin = k.lin;
+    return k.ok;
 }
 
 // ------------------------------------------------------------ smem plan ----
 struct Ctl {
-    int trace, tslot, abort, step, cdone, issued, last, pad;
+    int trace, tslot, abort, step, cdone, issued, last, ptslot;
 };
+constexpr int kTraceProducer = 3072;   // first trace word of the producer's stamps
 
 struct Plan {
     int ring, full, empty, xch, lin, tabs, xf, xsum, hs, part, recv, act32, af, qsum, vlo, zpart,
@@ -288,11 +315,12 @@ __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 
 __host__ __device__ inline int msg_floats(const Prog& p) { return (p.hr_max * 16 + 32) * p.B; }
 
-__host__ __device__ inline Plan make_plan(const Prog& p) {
+// base: bytes at the start of shared memory taken by the parameter copy and the context
+__host__ __device__ inline Plan make_plan(const Prog& p, int base) {
     Plan s;
     const int B = p.B, K = p.K, L = p.L;
     const int n_gd = p.d / kGroup, ngh = n_gd - n_gd / 2;
-    int o = 0;
+    int o = base;
     s.full = o;   o += kSlots * 8;
     s.empty = o;  o += kSlots * 8;
     s.xch = o;    o += 2 * 8;
@@ -328,9 +356,10 @@ __host__ __device__ inline Plan make_plan(const Prog& p) {
 }
 
 // ------------------------------------------------------------- context ----
+// Per-CTA context.  It and a copy of the kernel parameters live at fixed places
+// at the start of dynamic shared memory (every function reads them there: no
+// context is passed around, nothing of it is kept in local memory).
 struct Ctx {
-    const Prog* p;
-    char* sm;
     Plan pl;
     WsHeader* hdr;
     Ctl* ctl;
@@ -340,88 +369,135 @@ struct Ctx {
     int step, par;
 };
 
+extern __shared__ __align__(128) char g_smem[];
+constexpr int kProgOff = 0;
+constexpr int kCtxOff = (int)((sizeof(Prog) + 127) / 128 * 128);
+constexpr int kCtxBytes = (int)((sizeof(Ctx) + 127) / 128 * 128);
+__device__ __forceinline__ Ctx& ctx() { return *reinterpret_cast<Ctx*>(g_smem + kCtxOff); }
+__device__ __forceinline__ const Prog& prg() { return *reinterpret_cast<const Prog*>(g_smem + kProgOff); }
+
 __device__ __forceinline__ unsigned long long now_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-__device__ void raise_error(const Ctx& c, int code) {
+__device__ __noinline__ void raise_error(int code) {
+    const Ctx& c = ctx();
     atomicCAS(&c.hdr->error, 0, code);
     atomicExch(&c.hdr->abort, 1);
     *(volatile int*)&c.ctl->abort = 1;
 }
-__device__ __forceinline__ bool should_abort(const Ctx& c) {
+__device__ __forceinline__ bool should_abort() {
+    const Ctx& c = ctx();
     return *(volatile int*)&c.ctl->abort || ld_volatile_s32(&c.hdr->abort);
 }
-__device__ __forceinline__ bool aborted(const Ctx& c) { return *(volatile int*)&c.ctl->abort != 0; }
+__device__ __forceinline__ bool aborted() {
+    const Ctx& c = ctx(); return *(volatile int*)&c.ctl->abort != 0; }
 
 // wait on an mbarrier phase with a time bound; false on abort/timeout
-__device__ bool mbar_wait(const Ctx& c, uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
+    const Ctx& c = ctx();
     const unsigned long long t0 = now_ns();
     for (unsigned it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 63) {
-            if (should_abort(c)) return false;
-            if (now_ns() - t0 > kTimeoutNs) { raise_error(c, EDGE0_ETIMEOUT); return false; }
+            if (should_abort()) return false;
+            if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); return false; }
         }
     }
 }
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const Ctx& c = ctx();
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
+}
 
 // spin until *flag >= want (shared memory, written by the other role); bounded
-__device__ bool wait_flag(const Ctx& c, volatile int* flag, int want) {
+__device__ __noinline__ bool wait_flag(volatile int* flag, int want) {
+    const Ctx& c = ctx();
     if (*flag >= want) return true;
     const unsigned long long t0 = now_ns();
     for (unsigned it = 0; *flag < want; ++it) {
         __nanosleep(32);
         if ((it & 63) == 63) {
-            if (should_abort(c)) return false;
-            if (now_ns() - t0 > kTimeoutNs) { raise_error(c, EDGE0_ETIMEOUT); return false; }
+            if (should_abort()) return false;
+            if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); return false; }
         }
     }
     return true;
 }
 
 template <class T>
-__device__ __forceinline__ T* SM(const Ctx& c, int off) { return reinterpret_cast<T*>(c.sm + off); }
+__device__ __forceinline__ T* SM(int off) {
+    const Ctx& c = ctx(); return reinterpret_cast<T*>(g_smem + off); }
 
-__device__ __forceinline__ uint64_t* full_bar(const Ctx& c, int k) { return SM<uint64_t>(c, c.pl.full) + (k % kSlots); }
-__device__ __forceinline__ uint64_t* empty_bar(const Ctx& c, int k) { return SM<uint64_t>(c, c.pl.empty) + (k % kSlots); }
+__device__ __forceinline__ uint64_t* full_bar(int k) {
+    const Ctx& c = ctx(); return SM<uint64_t>(c.pl.full) + (k % kSlots); }
+__device__ __forceinline__ uint64_t* empty_bar(int k) {
+    const Ctx& c = ctx(); return SM<uint64_t>(c.pl.empty) + (k % kSlots); }
 __device__ __forceinline__ uint32_t item_parity(int k) { return (uint32_t)((k / kSlots) & 1); }
-__device__ __forceinline__ LayerTab* tab_of(const Ctx& c, int l) { return SM<LayerTab>(c, c.pl.tabs) + (l % kTables); }
-__device__ __forceinline__ int* ids_of(const Ctx& c, int l) { return SM<int>(c, c.pl.ids) + l * c.p->B * c.p->K; }
-__device__ __forceinline__ float* w_of(const Ctx& c, int l) { return SM<float>(c, c.pl.wts) + l * c.p->B * c.p->K; }
-__device__ __forceinline__ int* dist_of(const Ctx& c, int l) {
-    return SM<int>(c, c.pl.dist) + l * (c.p->slots_max > 0 ? c.p->slots_max : 1);
+__device__ __forceinline__ LayerTab* tab_of(int l) {
+    const Ctx& c = ctx(); return SM<LayerTab>(c.pl.tabs) + (l % kTables); }
+__device__ __forceinline__ int* ids_of(int l) {
+    const Ctx& c = ctx(); return SM<int>(c.pl.ids) + l * prg().B * prg().K; }
+__device__ __forceinline__ float* w_of(int l) {
+    const Ctx& c = ctx(); return SM<float>(c.pl.wts) + l * prg().B * prg().K; }
+__device__ __forceinline__ int* dist_of(int l) {
+    const Ctx& c = ctx();
+    return SM<int>(c.pl.dist) + l * (prg().slots_max > 0 ? prg().slots_max : 1);
 }
-__device__ __forceinline__ int* prev_of(const Ctx& c, int l) { return SM<int>(c, c.pl.prv) + l * c.p->B * c.p->K; }
-__device__ __forceinline__ const char* ring_at(const Ctx& c, const Item& it) { return c.sm + c.pl.ring + it.off; }
+__device__ __forceinline__ int* prev_of(int l) {
+    const Ctx& c = ctx(); return SM<int>(c.pl.prv) + l * prg().B * prg().K; }
+__device__ __forceinline__ const char* ring_at(const Item& it) {
+    const Ctx& c = ctx(); return g_smem + c.pl.ring + it.off; }
 
-__device__ __forceinline__ float* ws_f(const Ctx& c, long long off) { return reinterpret_cast<float*>(c.p->ws + off); }
-__device__ __forceinline__ float* y_buf(const Ctx& c, int par, int sidx) {
-    return ws_f(c, c.ws.y) + ((long long)par * c.p->Ls + sidx) * c.p->B * c.p->d;
+__device__ __forceinline__ float* ws_f(long long off) {
+    const Ctx& c = ctx(); return reinterpret_cast<float*>(prg().ws + off); }
+__device__ __forceinline__ float* y_buf(int par, int sidx) {
+    const Ctx& c = ctx();
+    return ws_f(c.ws.y) + ((long long)par * prg().Ls + sidx) * prg().B * prg().d;
 }
-__device__ __forceinline__ float* logr_buf(const Ctx& c, int par, int sidx) {
-    return ws_f(c, c.ws.logr) + ((long long)par * c.p->Ls + sidx) * c.p->B * c.p->E;
+__device__ __forceinline__ float* logr_buf(int par, int sidx) {
+    const Ctx& c = ctx();
+    return ws_f(c.ws.logr) + ((long long)par * prg().Ls + sidx) * prg().B * prg().E;
 }
-__device__ __forceinline__ float* logh_buf(const Ctx& c, int par, int sidx) {
-    return ws_f(c, c.ws.logh) + ((long long)par * c.p->Ls + sidx) * c.p->B * c.p->E;
+__device__ __forceinline__ float* logh_buf(int par, int sidx) {
+    const Ctx& c = ctx();
+    return ws_f(c.ws.logh) + ((long long)par * prg().Ls + sidx) * prg().B * prg().E;
 }
-__device__ __forceinline__ unsigned* cnt_buf(const Ctx& c, int par, int sidx) {
-    return reinterpret_cast<unsigned*>(c.p->ws + c.ws.cnt) + par * c.p->Ls + sidx;
+__device__ __forceinline__ unsigned* cnt_buf(int par, int sidx) {
+    const Ctx& c = ctx();
+    return reinterpret_cast<unsigned*>(prg().ws + c.ws.cnt) + par * prg().Ls + sidx;
 }
 
 // optional trace: (tag, globaltimer) pairs per CTA, written by consumer thread 0
-__device__ __forceinline__ void stamp(const Ctx& c, int tag) {
-    if (threadIdx.x != 0 || !c.ctl->trace) return;
+__device__ __noinline__ void stamp_slow(int tag) {
+    const Ctx& c = ctx();
     const int s = c.ctl->tslot;
-    if (s + 2 > kTraceSlots) return;
+    if (s + 3 > kTraceProducer) return;
     unsigned long long* a =
-        reinterpret_cast<unsigned long long*>(c.p->ws + c.ws.trace) + (long long)c.cta * kTraceSlots;
+        reinterpret_cast<unsigned long long*>(prg().ws + c.ws.trace) + (long long)c.cta * kTraceSlots;
     a[s] = (unsigned long long)tag;
     a[s + 1] = now_ns();
-    c.ctl->tslot = s + 2;
+    a[s + 2] = clock64();
+    c.ctl->tslot = s + 3;
+}
+__device__ __forceinline__ void stamp(int tag) {
+    const Ctx& c = ctx();
+    if (threadIdx.x == 0 && c.ctl->trace) stamp_slow(tag);
+}
+// the producer's stamps (slots from kTraceProducer on)
+__device__ __noinline__ void stamp_producer(int tag) {
+    const Ctx& c = ctx();
+    if (!c.ctl->trace) return;
+    const int s = c.ctl->ptslot;
+    if (s + 3 > kTraceSlots) return;
+    unsigned long long* a =
+        reinterpret_cast<unsigned long long*>(prg().ws + c.ws.trace) + (long long)c.cta * kTraceSlots;
+    a[s] = (unsigned long long)tag;
+    a[s + 1] = now_ns();
+    a[s + 2] = clock64();
+    c.ctl->ptslot = s + 3;
 }
 
 __host__ __device__ inline bool has_router_phase(const Prog& p, int l, int step) {
@@ -437,6 +513,7 @@ __host__ __device__ inline Shape layer_shape(const Prog& p, int l, bool router) 
     S.lora = (S.shared && p.mode == MODE_DECODE && (Ly.flags & LF_LORA)) ? 1 : 0;
     S.head = (p.mode == MODE_HEAD || (p.mode == MODE_DECODE && (Ly.flags & LF_HEAD))) ? 1 : 0;
     S.router = router ? 1 : 0;
+    S.ps = S.shared ? p.ps[S.lora] : 0;
     return S;
 }
 
@@ -454,48 +531,46 @@ __device__ __forceinline__ bool cbar_or(bool v) {
 }
 
 // ---------------------------------------------------------- routing -----
-// top-K over `score` (E values) by one warp, value descending, lower index first
-// on ties; masked entries are -inf.
-__device__ void warp_topk(const float* score, int E, int K, int* ids, int lane) {
-    unsigned taken[EDGE0_MAX_E / 32];
-#pragma unroll
-    for (int i = 0; i < EDGE0_MAX_E / 32; ++i) taken[i] = 0;
+// top-K over `score` (E values, E <= 512) by one warp, value descending, lower
+// index first on ties; masked entries are -inf.  Lane l owns entries l + 32 i.
+__device__ __noinline__ void warp_topk(const float* score, int E, int K, int* ids, int lane) {
+    unsigned taken = 0;   // bit i: entry lane + 32 i already selected
     for (int k = 0; k < K; ++k) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        for (int i = 0; i < EDGE0_MAX_E / 32; ++i) {
-            const int e = lane + 32 * i;
-            if (e >= E || taken[i]) continue;
+        for (int i = 0, e = lane; e < E; ++i, e += 32) {
+            if ((taken >> i) & 1u) continue;
             const float v = score[e];
-            if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+            if (v > bv) { bv = v; bi = e; }   // e increases: ties keep the lower index
         }
-#pragma unroll
         for (int s = 16; s; s >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
             const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
             if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
         }
         if (bi == 0x7fffffff) bi = 0;   // fewer than K candidates (not reachable for valid shapes)
-        if ((bi & 31) == lane) taken[bi >> 5] = 1;
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         if (lane == 0) ids[k] = bi;
-        __syncwarp();
     }
+    __syncwarp();
 }
 
 // Routing rule of App. A, one token per warp.  logits: E fp32 in shared memory;
 // scratch: 2 E floats of shared memory for this warp.
-__device__ void warp_route(const float* logits, int E, int K, int kind, int n_groups, int G,
-                           float scale, const float* bias, float* scratch, int* ids, float* w,
-                           int lane) {
+__device__ __noinline__ void warp_route(const float* logits, int E, int K, int kind, int n_groups,
+                                        int G, float scale, const float* bias, float* scratch,
+                                        int* ids, float* w, int lane) {
     float* sel = scratch;
     float* sig = scratch + E;
-    if (kind == EDGE0_ROUTE_SIGMOID_GROUP) {
-        for (int e = lane; e < E; e += 32) {
-            const float s = 1.0f / (1.0f + expf(-logits[e]));
-            sig[e] = s;
-            sel[e] = bias ? s + bias[e] : s;
-        }
-        __syncwarp();
+    const bool group = kind == EDGE0_ROUTE_SIGMOID_GROUP;
+    for (int e = lane; e < E; e += 32) {
+        const float l = logits[e];
+        const float s = group ? 1.0f / (1.0f + expf(-l)) : l;
+        sig[e] = s;
+        sel[e] = bias ? s + bias[e] : s;
+    }
+    __syncwarp();
+    if (group) {
         const int per = E / n_groups;
         // group score: sum of the two largest selection scores of the group
         float gscore = -INFINITY;
@@ -509,35 +584,29 @@ __device__ void warp_route(const float* logits, int E, int K, int kind, int n_gr
             gscore = a + b;
         }
         // keep the best G groups (lower group index on ties)
-        unsigned keep = 0, gtaken = 0;
+        unsigned keep = 0;
         for (int k = 0; k < G; ++k) {
-            float bv = (lane < n_groups && !((gtaken >> lane) & 1)) ? gscore : -INFINITY;
-            int bi = (lane < n_groups && !((gtaken >> lane) & 1)) ? lane : 0x7fffffff;
-#pragma unroll
+            const bool cand = lane < n_groups && !((keep >> lane) & 1u);
+            float bv = cand ? gscore : -INFINITY;
+            int bi = cand ? lane : 0x7fffffff;
             for (int s = 16; s; s >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
                 if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
             }
-            if (bi < 32) { gtaken |= 1u << bi; keep |= 1u << bi; }
+            if (bi < 32) keep |= 1u << bi;
         }
-        __syncwarp();
         for (int e = lane; e < E; e += 32)
-            if (!((keep >> (e / per)) & 1)) sel[e] = -INFINITY;
+            if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
         __syncwarp();
-        warp_topk(sel, E, K, ids, lane);
-        __syncwarp();
-        if (lane == 0) {
+    }
+    warp_topk(sel, E, K, ids, lane);
+    if (lane == 0) {
+        if (group) {
             float sum = 0.0f;
             for (int k = 0; k < K; ++k) sum += sig[ids[k]];
             for (int k = 0; k < K; ++k) w[k] = scale * sig[ids[k]] / (sum + 1e-20f);
-        }
-    } else {
-        for (int e = lane; e < E; e += 32) sel[e] = bias ? logits[e] + bias[e] : logits[e];
-        __syncwarp();
-        warp_topk(sel, E, K, ids, lane);
-        __syncwarp();
-        if (lane == 0) {
+        } else {
             const float mx = sel[ids[0]];
             float sum = 0.0f;
             for (int k = 0; k < K; ++k) sum += expf(sel[ids[k]] - mx);
@@ -549,10 +618,11 @@ __device__ void warp_route(const float* logits, int E, int K, int kind, int n_gr
 
 // distinct experts of a layer's routing in order of first appearance; false if
 // an id is out of range (single thread)
-__device__ bool make_dist(const Ctx& c, int l) {
-    const Prog& p = *c.p;
-    const int* ids = ids_of(c, l);
-    int* dist = dist_of(c, l);
+__device__ bool make_dist(int l) {
+    const Ctx& c = ctx();
+    const Prog& p = prg();
+    const int* ids = ids_of(l);
+    int* dist = dist_of(l);
     int n = 0;
     bool ok = true;
     for (int i = 0; i < p.B * p.K; ++i) {
@@ -562,147 +632,204 @@ __device__ bool make_dist(const Ctx& c, int l) {
         for (int j = 0; j < n; ++j) seen |= dist[j] == e;
         if (!seen && n < p.slots_max) dist[n++] = e;
     }
-    SM<int>(c, c.pl.ndist)[l] = n;
+    SM<int>(c.pl.ndist)[l] = n;
     return ok;
 }
 
 // ------------------------------------------------------------ producer -----
 // global source of an item; null: nothing to copy (a routed slot no token uses);
 // (const char*)1: an expert slot outside the stacks
-__device__ const char* item_src(const Ctx& c, int l, const LayerTab* T, const Item& it) {
-    const Prog& p = *c.p;
+__device__ __noinline__ const char* item_src(int l, const LayerTab* T, const Item& it) {
+    const Ctx& c = ctx();
+    const Prog& p = prg();
     const LayerP& Ly = p.layers[l];
-    const int n_gd = p.d / kGroup, r = p.r, n_rtd = p.d / kRowTile, gh0 = c.hv.gh0, rt0 = c.hv.rt0;
+    const int n_gd = p.d / kGroup, r = p.r, n_rtd = p.d / kRowTile;
+    const int h = c.rank, hn0 = n_gd / 2;
+    // first unit of this CTA's half of a row-tile-major matrix with `tiles` row tiles
+    auto half0 = [&](int tiles) { return (long long)h * tiles * hn0; };
     const char* gu = nullptr;
     const char* dn = nullptr;
-    if (it.kind == IT_GU || it.kind == IT_DSC || it.kind == IT_DQ) {
+    int I = p.I;
+    if (it.kind == IT_GU || it.kind == IT_DSC || it.kind == IT_DQ || it.kind == IT_DQS) {
         const Seg& g = T->pl.seg[it.seg];
         if (g.slot < 0) {
             gu = Ly.sh_gu;
             dn = Ly.sh_down;
+            I = p.Is;
         } else {
-            if (g.slot >= SM<int>(c, c.pl.ndist)[l]) return nullptr;
-            const int e = dist_of(c, l)[g.slot];
+            if (g.slot >= SM<int>(c.pl.ndist)[l]) return nullptr;
+            const int e = dist_of(l)[g.slot];
             const int slot = Ly.slot_table ? Ly.slot_table[e] : e;
             if (slot < 0 || slot >= Ly.n_slots) return reinterpret_cast<const char*>(1);
             gu = Ly.gu + (long long)slot * q4_bytes(2 * p.I, p.d);
             dn = Ly.down + (long long)slot * q4_bytes(p.d, p.I);
         }
     }
+    // down: group a, this CTA's half of the row tiles
+    const int nrt = c.hv.rt1 - c.hv.rt0;
+    const char* dgrp = dn ? dn + (long long)it.a * n_rtd * kQ4Unit + (long long)h * (n_rtd / 2) * kQ4Unit : nullptr;
     switch (it.kind) {
-        case IT_ROUTER: return Ly.router + ((long long)it.a * n_gd + gh0 + it.b) * kF16Unit;
-        case IT_GU: return gu + ((long long)it.a * n_gd + gh0 + it.b) * kQ4Unit;
-        case IT_LA: return Ly.lora_Ag + (long long)(gh0 + it.b) * kF16Unit;
-        case IT_LU: return Ly.lora_Au + (long long)(gh0 + it.b) * kF16Unit;
+        case IT_ROUTER: return Ly.router + (half0(p.E / kRowTile) + it.b) * kF16Unit;
+        case IT_GU: return gu + (half0(I / kHalfRow) + it.b) * kQ4Unit;
+        case IT_LA: return Ly.lora_Ag + (half0(1) + it.b) * kF16Unit;
+        case IT_LU: return Ly.lora_Au + (half0(1) + it.b) * kF16Unit;
         case IT_BG: return reinterpret_cast<const char*>(Ly.lora_Bg + (long long)it.a * r);
         case IT_BU: return reinterpret_cast<const char*>(Ly.lora_Bu + (long long)it.a * r);
-        case IT_DSC:
-            return dn + (long long)it.a * n_rtd * kQ4Unit + 4LL * n_rtd * kQ4Quarter + (long long)rt0 * kQ4Scales;
         case IT_DQ:
-            return dn + (long long)(it.a / 4) * n_rtd * kQ4Unit + ((long long)(it.a % 4) * n_rtd + rt0) * kQ4Quarter;
+        case IT_DQS: return dgrp + (long long)it.b * nrt * kQ4Quarter;
+        case IT_DSC: return dgrp + 4LL * nrt * kQ4Quarter;
         case IT_ADT: return reinterpret_cast<const char*>(Ly.lora_AdT + (long long)it.a * r);
         case IT_BD: return reinterpret_cast<const char*>(Ly.lora_Bd + (long long)it.a * r);
-        case IT_FC1: return Ly.fc1 + ((long long)it.a * n_gd + gh0 + it.b) * kF16Unit;
+        case IT_FC1: return Ly.fc1 + (half0(p.H / kRowTile) + it.b) * kF16Unit;
         case IT_FC2: return Ly.fc2 + ((long long)it.a * (p.E / kRowTile) + it.b) * kF16Step;
-        default: return Ly.linit + ((long long)it.a * n_gd + gh0 + it.b) * kF16Unit;
+        default: return Ly.linit + (half0(p.E / kRowTile) + it.b) * kF16Unit;
     }
 }
 
-__device__ void producer(Ctx& c) {
-    const Prog& p = *c.p;
+// The producer warp (all 32 lanes call this; it uses warp-wide shuffles): lane 0
+// builds each layer's item table and decides how many of the next items can go
+// (routing known, ring bytes and barrier slots free); the lanes then issue those
+// copies in parallel.
+__device__ void producer() {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     Ctl* ctl = c.ctl;
-    volatile int* ready = SM<volatile int>(c, c.pl.ready);
-    int* lstart = SM<int>(c, c.pl.lin);   // linear start of the item in each slot
+    const int lane = threadIdx.x & 31;
+    volatile int* ready = SM<volatile int>(c.pl.ready);
+    int* lstart = SM<int>(c.pl.lin);   // linear start of the item in each slot
     const uint64_t pol = policy_evict_first();
-    char* ring = c.sm + c.pl.ring;
-    int lin = 0;      // linear ring position of the next item
+    char* ring = g_smem + c.pl.ring;
+    int lin = 0;      // linear ring position of the next item (lane 0)
     int k = 0;        // global index of the next item
-    int front = 0;    // oldest item not known to be released
+    int front = 0;    // oldest item not known to be released (lane 0)
+    if (__shfl_sync(0xffffffffu, lane == 0 ? (int)aborted() : 0, 0)) return;
     for (int l = 0; l < p.L; ++l) {
-        // the table slot is free once the consumers finished layer l - kTables
-        if (!wait_flag(c, &ctl->cdone, l - kTables + 1)) return;
-        LayerTab* T = tab_of(c, l);
-        T->k0 = k;
-        const Shape Sh = layer_shape(p, l, has_router_phase(p, l, c.step));
-        if (!build_items(Sh, c.P, c.pair, c.rank, p.ring_bytes, T, lin)) {
-            raise_error(c, EDGE0_EUNSUPPORTED);
-            return;
+        LayerTab* T = tab_of(l);
+        int fail = 0;
+        if (lane == 0) {
+            // the table slot is free once the consumers finished layer l - kTables
+            if (!wait_flag(&ctl->cdone, l - kTables + 1)) fail = 1;
+            if (!fail) {
+                stamp_producer((l << 8) | 0x80);
+                T->k0 = k;
+                const Shape Sh = layer_shape(p, l, has_router_phase(p, l, c.step));
+                if (!build_items(Sh, c.P, c.pair, c.rank, p.ring_bytes, T, lin)) {
+                    raise_error(EDGE0_EUNSUPPORTED);
+                    fail = 1;
+                } else {
+                    __threadfence_block();
+                    *(volatile int*)&T->seq = l + 1;
+                    stamp_producer((l << 8) | 0x81);
+                }
+            }
         }
-        __threadfence_block();
-        *(volatile int*)&T->seq = l + 1;
+        if (__shfl_sync(0xffffffffu, fail, 0)) return;
+        __syncwarp();
+        const int n = T->n;
         bool have_routing = false;
-        for (int i = 0; i < T->n; ++i, ++k) {
-            const Item& it = T->it[i];
-            if (!have_routing && (it.kind == IT_GU || it.kind == IT_DSC || it.kind == IT_DQ) &&
-                T->pl.seg[it.seg].slot >= 0) {
-                if (!wait_flag(c, &ready[l], 1)) return;
-                __threadfence_block();
-                have_routing = true;
+        for (int i = 0; i < n;) {
+            int m = 0;
+            if (lane == 0) {
+                // items i .. i + m - 1 can go now; wait only for the first one
+                for (; m < 32 && i + m < n; ++m) {
+                    const Item& it = T->it[i + m];
+                    const int kk = k + m;
+                    const bool routed = (it.kind == IT_GU || it.kind == IT_DSC || it.kind == IT_DQ ||
+                                         it.kind == IT_DQS) && T->pl.seg[it.seg].slot >= 0;
+                    if (routed && !have_routing) {
+                        if (m > 0 && ready[l] != 1) break;
+                        if (!wait_flag(&ready[l], 1)) { fail = 1; break; }
+                        __threadfence_block();
+                        have_routing = true;
+                        stamp_producer((l << 8) | 0x82);
+                    }
+                    // slot kk and the item's ring bytes must be free
+                    while (front < kk && (front <= kk - kSlots || it.lin + it.bytes - lstart[front % kSlots] > p.ring_bytes)) {
+                        if (m > 0) break;
+                        if (!mbar_wait(empty_bar(front), item_parity(front))) { fail = 1; break; }
+                        ++front;
+                    }
+                    if (fail) break;
+                    if (front < kk && (front <= kk - kSlots || it.lin + it.bytes - lstart[front % kSlots] > p.ring_bytes)) break;
+                    lstart[kk % kSlots] = it.lin;
+                }
             }
-            const char* src = item_src(c, l, T, it);
-            if (src == reinterpret_cast<const char*>(1)) { raise_error(c, EDGE0_EINVAL); return; }
-            // wait until slot k is free and the item's ring bytes no longer hold live items
-            while (front < k && (front <= k - kSlots || it.lin + it.bytes - lstart[front % kSlots] > p.ring_bytes)) {
-                if (!mbar_wait(c, empty_bar(c, front), item_parity(front))) return;
-                ++front;
+            fail = __shfl_sync(0xffffffffu, fail, 0);
+            m = __shfl_sync(0xffffffffu, m, 0);
+            if (fail) return;
+            __syncwarp();
+            if (lane < m) {
+                const Item& it = T->it[i + lane];
+                const char* src = item_src(l, T, it);
+                uint64_t* fb = full_bar(k + lane);
+                if (src == reinterpret_cast<const char*>(1)) {
+                    raise_error(EDGE0_EINVAL);
+                    mbar_arrive(fb);
+                } else if (src) {
+                    mbar_arrive_expect_tx(fb, (uint32_t)it.bytes);
+                    bulk_g2s(ring + it.off, src, (uint32_t)it.bytes, fb, pol);
+                } else {
+                    mbar_arrive(fb);
+                }
             }
-            lstart[k % kSlots] = it.lin;
-            uint64_t* fb = full_bar(c, k);
-            if (src) {
-                mbar_arrive_expect_tx(fb, (uint32_t)it.bytes);
-                bulk_g2s(ring + it.off, src, (uint32_t)it.bytes, fb, pol);
-            } else {
-                mbar_arrive(fb);
-            }
-            *(volatile int*)&ctl->issued = k + 1;
+            __syncwarp();
+            i += m;
+            k += m;
+            if (lane == 0) *(volatile int*)&ctl->issued = k;
         }
+        if (lane == 0) stamp_producer((l << 8) | 0x83);
     }
 }
 
 // ------------------------------------------------------------ consumers ----
-__device__ __forceinline__ bool wait_item(const Ctx& c, const LayerTab* T, int i) {
-    return mbar_wait(c, full_bar(c, T->k0 + i), item_parity(T->k0 + i));
+__device__ __forceinline__ bool wait_item(const LayerTab* T, int i) {
+    const Ctx& c = ctx();
+    return mbar_wait(full_bar(T->k0 + i), item_parity(T->k0 + i));
 }
-__device__ __forceinline__ void release_item(const Ctx& c, const LayerTab* T, int i) {
+__device__ __forceinline__ void release_item(const LayerTab* T, int i) {
+    const Ctx& c = ctx();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar(c, T->k0 + i));
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar(T->k0 + i));
 }
 
 // grid barrier: arrive (after the caller's cbar) and wait
-__device__ void bar_arrive(const Ctx& c) {
+__device__ void bar_arrive() {
+    const Ctx& c = ctx();
     if (threadIdx.x == 0) {
         __threadfence();
         red_release_add_u64(&c.hdr->barrier, 1ull);
     }
 }
-__device__ bool bar_wait(const Ctx& c, unsigned long long& target) {
+__device__ __noinline__ bool bar_wait(unsigned long long& target) {
+    const Ctx& c = ctx();
     if (threadIdx.x == 0) {
         target += (unsigned long long)c.nct;
         if (ld_acquire_u64(&c.hdr->barrier) < target) {
             const unsigned long long t0 = now_ns();
             for (unsigned it = 0; ld_acquire_u64(&c.hdr->barrier) < target; ++it) {
                 if ((it & 15) == 15) {
-                    if (should_abort(c)) { *(volatile int*)&c.ctl->abort = 1; break; }
-                    if (now_ns() - t0 > kTimeoutNs) { raise_error(c, EDGE0_ETIMEOUT); break; }
+                    if (should_abort()) { *(volatile int*)&c.ctl->abort = 1; break; }
+                    if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); break; }
                 }
             }
         }
     }
-    return !cbar_or(aborted(c));
+    return !cbar_or(aborted());
 }
 
 // send nfloats (multiple of 4) from this CTA's `src` into the peer's copy of
 // `dst`, and wait for the peer's data in this CTA's `dst` (exchange barrier `which`)
-__device__ bool exchange(const Ctx& c, int which, const float* src, float* dst, int nfloats,
+__device__ __noinline__ bool exchange(int which, const float* src, float* dst, int nfloats,
                          uint32_t& phase) {
-    uint64_t* bar = SM<uint64_t>(c, c.pl.xch) + which;
+    const Ctx& c = ctx();
+    uint64_t* bar = SM<uint64_t>(c.pl.xch) + which;
     const uint32_t peer = c.rank ^ 1u;
     if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nfloats * 4));
     const uint32_t rbar = mapa_shared(smem_u32(bar), peer);
     const uint32_t rdst = mapa_shared(smem_u32(dst), peer);
     for (int i = threadIdx.x; i < nfloats / 4; i += kConsumerThreads)
         st_async_v4(rdst + 16u * i, reinterpret_cast<const uint4*>(src)[i], rbar);
-    const bool ok = mbar_wait(c, bar, phase & 1u);
+    const bool ok = mbar_wait(bar, phase & 1u);
     ++phase;
     return ok;
 }
@@ -713,12 +840,13 @@ struct XFrag {
     int stride;   // uint2 per 16-input step
     bool live;
 };
-__device__ __forceinline__ XFrag xfrag(const Ctx& c) {
+__device__ __forceinline__ XFrag xfrag() {
+    const Ctx& c = ctx();
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, tok = g >> 1;
     XFrag f;
-    f.live = !(g & 1) && tok < c.p->B;
-    f.base = SM<uint2>(c, c.pl.xf) + (f.live ? tok : 0) * 4 + t;
-    f.stride = c.p->B * 4;
+    f.live = !(g & 1) && tok < prg().B;
+    f.base = SM<uint2>(c.pl.xf) + (f.live ? tok : 0) * 4 + t;
+    f.stride = prg().B * 4;
     return f;
 }
 
@@ -732,12 +860,13 @@ __device__ __forceinline__ void q4_masks(uint32_t w, uint32_t A[4]) {
 
 // int4 units [a, b) of a run whose unit j is local group gl0 + j of one row
 // tile: adds s 2^24 acc + b xsum per unit to rows g (r0) and g + 8 (r1), token t
-__device__ __forceinline__ void q4_run(const Ctx& c, const char* base, int a, int b, int gl0,
+__device__ __forceinline__ void q4_run(const char* base, int a, int b, int gl0,
                                        float& r0, float& r1) {
+    const Ctx& c = ctx();
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int B = c.p->B;
-    const XFrag xf = xfrag(c);
-    const float* xs = SM<float>(c, c.pl.xsum);
+    const int B = prg().B;
+    const XFrag xf = xfrag();
+    const float* xs = SM<float>(c.pl.xsum);
     for (int j = a; j < b; ++j) {
         const char* unit = base + (long long)j * kQ4Unit;
         const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
@@ -762,9 +891,10 @@ __device__ __forceinline__ void q4_run(const Ctx& c, const char* base, int a, in
 }
 
 // fp16 units [a, b) (x source) accumulated into acc (rows g, g + 8; column 2t = token t)
-__device__ __forceinline__ void f16_run(const Ctx& c, const char* base, int a, int b, int gl0, float acc[4]) {
+__device__ __forceinline__ void f16_run(const char* base, int a, int b, int gl0, float acc[4]) {
+    const Ctx& c = ctx();
     const int lane = threadIdx.x & 31;
-    const XFrag xf = xfrag(c);
+    const XFrag xf = xfrag();
     for (int j = a; j < b; ++j) {
         const char* unit = base + (long long)j * kF16Unit;
         const int gl = gl0 + j;
@@ -782,94 +912,96 @@ __device__ __forceinline__ void f16_run(const Ctx& c, const char* base, int a, i
 // ------------------------------------------------------------ prologue ----
 // x = fp16(RMSNorm(h) * gamma) for all tokens (decode; h updated by the previous
 // layer's y first) or x = x_in; B fragments and group sums for this CTA's half
-// of d.  The residual h stays in shared memory.
-__device__ void build_x(Ctx& c, int l) {
-    const Prog& p = *c.p;
+// of d.  The residual h stays in shared memory.  All global loads of a thread
+// are issued before any is used (one round trip after the barrier).
+__device__ __noinline__ void build_x(int l) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int B = p.B, d = p.d, n4 = B * d / 4;
     const bool decode = p.mode == MODE_DECODE;
     const LayerP& Ly = p.layers[l];
-    __half* hs = SM<__half>(c, c.pl.hs);
-    const float* y = (decode && l > 0) ? y_buf(c, c.par, p.layers[l - 1].sidx) : nullptr;
+    __half* hs = SM<__half>(c.pl.hs);
+    const float* y = (decode && l > 0) ? y_buf(c.par, p.layers[l - 1].sidx) : nullptr;
     const __half* hsrc = decode ? (l == 0 ? p.h_io : hs) : p.x_in;
-    const __half* gam = decode ? Ly.gamma : nullptr;
-    uint2 hv[kMaxChunks], gv[kMaxChunks];
+    uint2 hv[kMaxChunks];
     float4 yv[kMaxChunks];
 #pragma unroll
     for (int j = 0; j < kMaxChunks; ++j) {
         const int i = tid + j * kConsumerThreads;
         if (i < n4) {
             hv[j] = *reinterpret_cast<const uint2*>(hsrc + 4 * i);
-            yv[j] = y ? __ldcg(reinterpret_cast<const float4*>(y + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            gv[j] = gam ? __ldg(reinterpret_cast<const uint2*>(gam + (4 * i) % d)) : make_uint2(0x3C003C00u, 0x3C003C00u);
+            if (y) yv[j] = __ldcg(reinterpret_cast<const float4*>(y + 4 * i));
         }
     }
-    float hf[kMaxChunks][4];
+    // h = fp16(h + y) into shared memory, sums of squares per token
     float ss[EDGE0_MAX_BATCH] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < kMaxChunks; ++j) {
         const int i = tid + j * kConsumerThreads;
         if (i < n4) {
-            const __half2 h01 = *reinterpret_cast<const __half2*>(&hv[j].x);
-            const __half2 h23 = *reinterpret_cast<const __half2*>(&hv[j].y);
-            float v[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
+            __half2 h01 = *reinterpret_cast<const __half2*>(&hv[j].x);
+            __half2 h23 = *reinterpret_cast<const __half2*>(&hv[j].y);
             if (y) {
-                v[0] = __half2float(__float2half_rn(v[0] + yv[j].x));
-                v[1] = __half2float(__float2half_rn(v[1] + yv[j].y));
-                v[2] = __half2float(__float2half_rn(v[2] + yv[j].z));
-                v[3] = __half2float(__float2half_rn(v[3] + yv[j].w));
+                h01 = __floats2half2_rn(__low2float(h01) + yv[j].x, __high2float(h01) + yv[j].y);
+                h23 = __floats2half2_rn(__low2float(h23) + yv[j].z, __high2float(h23) + yv[j].w);
             }
-            if (decode) {
-                __half2 o01 = __floats2half2_rn(v[0], v[1]), o23 = __floats2half2_rn(v[2], v[3]);
-                uint2 o;
-                o.x = *reinterpret_cast<uint32_t*>(&o01);
-                o.y = *reinterpret_cast<uint32_t*>(&o23);
-                *reinterpret_cast<uint2*>(hs + 4 * i) = o;
-            }
+            uint2 o;
+            o.x = *reinterpret_cast<uint32_t*>(&h01);
+            o.y = *reinterpret_cast<uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(hs + 4 * i) = o;
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            const float q = f01.x * f01.x + f01.y * f01.y + f23.x * f23.x + f23.y * f23.y;
             const int b = (4 * i) / d;
-            const float q = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
 #pragma unroll
             for (int bb = 0; bb < EDGE0_MAX_BATCH; ++bb) if (bb == b) ss[bb] += q;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) hf[j][e] = v[e];
         }
     }
-    float* red = SM<float>(c, c.pl.red);
+    float* red = SM<float>(c.pl.red);
     float* rs = red + B * kConsumerWarps;
     if (decode) {
         for (int b = 0; b < B; ++b) {
-            const float s = warp_sum(ss[b]);
-            if (lane == 0) red[b * kConsumerWarps + wid] = s;
+            const float sum = warp_sum(ss[b]);
+            if (lane == 0) red[b * kConsumerWarps + wid] = sum;
         }
-        cbar();
-        if (tid < B) {
-            float s = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) s += red[tid * kConsumerWarps + w];
-            rs[tid] = rsqrtf(s / (float)d + Ly.eps);
-        }
-        cbar();
     }
-    uint32_t* xf = SM<uint32_t>(c, c.pl.xf);
-    float* xsum = SM<float>(c, c.pl.xsum);
-#pragma unroll
-    for (int j = 0; j < kMaxChunks; ++j) {
+    cbar();
+    if (decode && tid < B) {
+        float sum = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) sum += red[tid * kConsumerWarps + w];
+        rs[tid] = rsqrtf(sum / (float)d + Ly.eps);
+    }
+    cbar();
+    // x fragments and group sums of this CTA's half (the 16 threads of a group
+    // are the 16 lanes of a half-warp)
+    uint32_t* xf = SM<uint32_t>(c.pl.xf);
+    float* xsum = SM<float>(c.pl.xsum);
+    const __half* gam = decode ? Ly.gamma : nullptr;
+#pragma unroll 1
+    for (int j = 0; j * kConsumerThreads < n4; ++j) {
         const int i = tid + j * kConsumerThreads;
-        if (j * kConsumerThreads >= n4) break;   // uniform over the CTA
         float x[4] = {0.f, 0.f, 0.f, 0.f};
         int b = 0, k = 0;
         if (i < n4) {
             b = (4 * i) / d;
             k = (4 * i) % d;
-            const __half2 g01 = *reinterpret_cast<const __half2*>(&gv[j].x);
-            const __half2 g23 = *reinterpret_cast<const __half2*>(&gv[j].y);
-            const float gg[4] = {__low2float(g01), __high2float(g01), __low2float(g23), __high2float(g23)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                x[e] = decode ? __half2float(__float2half_rn(hf[j][e] * rs[b] * gg[e])) : hf[j][e];
+            const uint2 hh = *reinterpret_cast<const uint2*>(hs + 4 * i);
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&hh.x));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&hh.y));
+            x[0] = f01.x; x[1] = f01.y; x[2] = f23.x; x[3] = f23.y;
+            if (decode) {
+                float g4[4] = {1.f, 1.f, 1.f, 1.f};
+                if (gam) {
+                    const uint2 gg = __ldg(reinterpret_cast<const uint2*>(gam + k));
+                    const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&gg.x));
+                    const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&gg.y));
+                    g4[0] = g01.x; g4[1] = g01.y; g4[2] = g23.x; g4[3] = g23.y;
+                }
+                const float r = rs[b];
+                for (int e = 0; e < 4; ++e) x[e] = __half2float(__float2half_rn(x[e] * r * g4[e]));
+            }
         }
-        // group sum over the 16 threads that hold one group
         float s4 = x[0] + x[1] + x[2] + x[3];
-#pragma unroll
         for (int m = 8; m; m >>= 1) s4 += __shfl_xor_sync(0xffffffffu, s4, m);
         const int grp = k / kGroup;
         if (i < n4 && grp >= c.hv.gh0 && grp < c.hv.gh1) {
@@ -886,10 +1018,26 @@ __device__ void build_x(Ctx& c, int l) {
 }
 
 // ------------------------------------------------------------- phases -----
+// g(tile, j0, j1, gl0) for each run of the units [a, b) of a unit item that lies
+// in one row tile: units j0..j1-1 of the item, unit j is local group gl0 + j
+template <class G>
+__device__ __forceinline__ void tile_runs(const Item& it, int a, int b, G&& g) {
+    const Ctx& c = ctx();
+    const int ngh = c.hv.gh1 - c.hv.gh0;
+    int j = a;
+    while (j < b) {
+        const int u = it.b + j, tile = u / ngh, grp = u - tile * ngh;
+        const int e = b < j + (ngh - grp) ? b : j + (ngh - grp);
+        g(tile, j, e, grp - j);
+        j = e;
+    }
+}
+
 // units of the unit items in [ia, ib) split over the warps; f(item, local unit
 // range) runs on items the warp has units in; every item is released by every warp
 template <class F>
-__device__ bool warp_units(const Ctx& c, const LayerTab* T, int ia, int ib, F&& f) {
+__device__ bool warp_units(const LayerTab* T, int ia, int ib, F&& f, int wait_tag = -1) {
+    const Ctx& c = ctx();
     const int wid = threadIdx.x >> 5;
     int tot = 0;
     for (int i = ia; i < ib; ++i)
@@ -904,41 +1052,49 @@ __device__ bool warp_units(const Ctx& c, const LayerTab* T, int ia, int ib, F&& 
         const int a = ua - u > 0 ? ua - u : 0, b = ub - u < it.n ? ub - u : it.n;
         u += it.n;
         if (a < b && ok) {
-            if (!wait_item(c, T, i)) ok = false;
-            else f(it, a, b);
+            if (!wait_item(T, i)) ok = false;
+            else {
+                if (wait_tag >= 0) { stamp(wait_tag); wait_tag = -1; }
+                f(it, a, b);
+            }
         }
-        release_item(c, T, i);
+        release_item(T, i);
     }
     return ok;
 }
 
-__device__ __forceinline__ bool seg_live(const Ctx& c, int l, const Seg& s) {
-    return s.slot < 0 || s.slot < SM<int>(c, c.pl.ndist)[l];
+__device__ __forceinline__ bool seg_live(int l, const Seg& s) {
+    const Ctx& c = ctx();
+    return s.slot < 0 || s.slot < SM<int>(c.pl.ndist)[l];
 }
 
 // own router: partial logits of this CTA's units, into the layer's logits
-__device__ bool phase_router(Ctx& c, int l, const LayerTab* T) {
-    const Prog& p = *c.p;
+__device__ bool phase_router(int l, const LayerTab* T) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    float* lg = logr_buf(c, c.par, p.layers[l].sidx);
-    return warp_units(c, T, 0, T->p1, [&](const Item& it, int a, int b) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        f16_run(c, ring_at(c, it), a, b, it.b, acc);
-        const int row = it.a * kRowTile + g;
-        if (t < p.B) {
-            if (row < p.E) red_add_f32(lg + t * p.E + row, acc[0]);
-            if (row + 8 < p.E) red_add_f32(lg + t * p.E + row + 8, acc[2]);
-        }
+    float* lg = logr_buf(c.par, p.layers[l].sidx);
+    return warp_units(T, 0, T->p1, [&](const Item& it, int a, int b) {
+        tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            f16_run(ring_at(it), j0, j1, gl0, acc);
+            const int row = tile * kRowTile + g;
+            if (t < p.B) {
+                if (row < p.E) red_add_f32(lg + t * p.E + row, acc[0]);
+                if (row + 8 < p.E) red_add_f32(lg + t * p.E + row + 8, acc[2]);
+            }
+        });
     });
 }
 
 // routing of an own-routed layer from its complete router logits
-__device__ void route_layer(Ctx& c, int l) {
-    const Prog& p = *c.p;
+__device__ __noinline__ void route_layer(int l) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const LayerP& Ly = p.layers[l];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    float* scr = SM<float>(c, c.pl.rscr);
-    const float* lg = logr_buf(c, c.par, Ly.sidx);
+    float* scr = SM<float>(c.pl.rscr);
+    const float* lg = logr_buf(c.par, Ly.sidx);
     for (int i = tid; i < p.B * p.E; i += kConsumerThreads) {
         const int b = i / p.E, e = i - b * p.E;
         scr[b * 3 * p.E + e] = __ldcg(lg + i);
@@ -950,46 +1106,49 @@ __device__ void route_layer(Ctx& c, int l) {
         warp_route(scr + b * 3 * p.E, p.E, p.K, Ly.route_kind, Ly.n_groups, Ly.topk_groups,
                    Ly.route_scale, Ly.bias, scr + b * 3 * p.E + p.E, rid[b], rw[b], lane);
         if (lane < p.K) {
-            ids_of(c, l)[b * p.K + lane] = rid[b][lane];
-            w_of(c, l)[b * p.K + lane] = rw[b][lane];
+            ids_of(l)[b * p.K + lane] = rid[b][lane];
+            w_of(l)[b * p.K + lane] = rw[b][lane];
         }
     }
     cbar();
     if (tid == 0) {
-        if (!make_dist(c, l)) raise_error(c, EDGE0_EINVAL);
+        if (!make_dist(l)) raise_error(EDGE0_EINVAL);
         __threadfence_block();
-        SM<volatile int>(c, c.pl.ready)[l] = 1;
+        SM<volatile int>(c.pl.ready)[l] = 1;
     }
     cbar();
 }
 
 // P1: partial gate/up (+ LoRA A x) sums of the pair's rows over this CTA's half of d
-__device__ bool phase1(Ctx& c, int l, const LayerTab* T) {
-    const int B = c.p->B;
+__device__ bool phase1(int l, const LayerTab* T) {
+    Ctx& c = ctx();
+    const int B = prg().B;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    float* part = SM<float>(c, c.pl.part);
+    float* part = SM<float>(c.pl.part);
     const int nlp = T->pl.n_hr * 16 * B;
-    return warp_units(c, T, T->p1, T->p2, [&](const Item& it, int a, int b) {
+    return warp_units(T, T->p1, T->p2, [&](const Item& it, int a, int b) {
         const Seg& sg = T->pl.seg[it.seg];
-        if (!seg_live(c, l, sg)) return;
-        if (it.kind == IT_GU) {
-            float r0 = 0.f, r1 = 0.f;
-            q4_run(c, ring_at(c, it), a, b, it.b, r0, r1);
-            const int hl = sg.hoff + it.a - sg.hr0;
-            if (t < B) {
-                atomicAdd(&part[(hl * 16 + g) * B + t], r0);
-                atomicAdd(&part[(hl * 16 + 8 + g) * B + t], r1);
+        if (!seg_live(l, sg)) return;
+        tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
+            if (it.kind == IT_GU) {
+                float r0 = 0.f, r1 = 0.f;
+                q4_run(ring_at(it), j0, j1, gl0, r0, r1);
+                const int hl = sg.hoff + tile - sg.hr0;
+                if (t < B) {
+                    atomicAdd(&part[(hl * 16 + g) * B + t], r0);
+                    atomicAdd(&part[(hl * 16 + 8 + g) * B + t], r1);
+                }
+            } else {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                f16_run(ring_at(it), j0, j1, gl0, acc);
+                const int m = it.kind == IT_LA ? 0 : 1;
+                if (t < B) {
+                    atomicAdd(&part[nlp + (m * 16 + g) * B + t], acc[0]);
+                    atomicAdd(&part[nlp + (m * 16 + 8 + g) * B + t], acc[2]);
+                }
             }
-        } else {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            f16_run(c, ring_at(c, it), a, b, it.b, acc);
-            const int m = it.kind == IT_LA ? 0 : 1;
-            if (t < B) {
-                atomicAdd(&part[nlp + (m * 16 + g) * B + t], acc[0]);
-                atomicAdd(&part[nlp + (m * 16 + 8 + g) * B + t], acc[2]);
-            }
-        }
-    });
+        });
+    }, (l << 8) | 8);
 }
 
 // index of the first item of `kind` for segment s in [ia, ib), or -1
@@ -1003,17 +1162,18 @@ __device__ __forceinline__ int find_item(const LayerTab* T, int ia, int ib, int 
 // terms for shared rows) -> hi/lo B fragments per 16-row quarter and their sums;
 // v = A_down act for the shared rows (LoRA).  Every consumer thread runs every
 // barrier here; the result is CTA-uniform.
-__device__ bool compute_act(Ctx& c, int l, const LayerTab* T, bool lora) {
-    const Prog& p = *c.p;
+__device__ bool compute_act(int l, const LayerTab* T, bool lora) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const LayerP& Ly = p.layers[l];
     const int B = p.B, r = p.r, tid = threadIdx.x;
     const PairPlan& pl = T->pl;
-    const float* part = SM<float>(c, c.pl.part);
-    const float* recv = SM<float>(c, c.pl.recv);
-    float* act32 = SM<float>(c, c.pl.act32);
-    __half* af = SM<__half>(c, c.pl.af);
-    float* qsum = SM<float>(c, c.pl.qsum);
-    float* vlo = SM<float>(c, c.pl.vlo);
+    const float* part = SM<float>(c.pl.part);
+    const float* recv = SM<float>(c.pl.recv);
+    float* act32 = SM<float>(c.pl.act32);
+    __half* af = SM<__half>(c.pl.af);
+    float* qsum = SM<float>(c.pl.qsum);
+    float* vlo = SM<float>(c.pl.vlo);
     const int nlp = pl.n_hr * 16 * B;
     // LoRA items of the shared segment (segment 0 of a pair that owns shared rows)
     int ibg = -1, ibu = -1, iadt = -1, ssh = -1;
@@ -1024,26 +1184,27 @@ __device__ bool compute_act(Ctx& c, int l, const LayerTab* T, bool lora) {
         ibu = find_item(T, T->p1, T->p2, IT_BU, ssh);
         iadt = find_item(T, T->p2, T->p3, IT_ADT, ssh);
         ok = ibg >= 0 && ibu >= 0 && iadt >= 0;
-        if (!ok && tid == 0) raise_error(c, EDGE0_EINVAL);
-        ok = ok && wait_item(c, T, ibg) && wait_item(c, T, ibu) && wait_item(c, T, iadt);
+        if (!ok && tid == 0) raise_error(EDGE0_EINVAL);
+        ok = ok && wait_item(T, ibg) && wait_item(T, ibu) && wait_item(T, iadt);
     }
     for (int i = tid; i < pl.n_q * B * 2 * 4 * 4; i += kConsumerThreads) af[i] = __float2half_rn(0.f);
     for (int i = tid; i < pl.n_q * B; i += kConsumerThreads) qsum[i] = 0.f;
     ok = !cbar_or(!ok);
+    stamp((l << 8) | 10);
     for (int i = tid; ok && i < pl.n_hr * 8 * B; i += kConsumerThreads) {
         const int hl = i / (8 * B), g = (i / B) % 8, b = i % B;
         int s = 0;
         while (s + 1 < pl.nseg && hl >= pl.seg[s + 1].hoff) ++s;
         const Seg& sg = pl.seg[s];
         float a = 0.f;
-        if (seg_live(c, l, sg)) {
+        if (seg_live(l, sg)) {
             const int row = (sg.hr0 + hl - sg.hoff) * kHalfRow + g;   // act row of the expert
             float gate = part[(hl * 16 + g) * B + b] + recv[(hl * 16 + g) * B + b];
             float up = part[(hl * 16 + 8 + g) * B + b] + recv[(hl * 16 + 8 + g) * B + b];
             if (s == ssh) {
                 const int rl = row - sg.hr0 * kHalfRow;
-                const __half* bg = reinterpret_cast<const __half*>(ring_at(c, T->it[ibg])) + rl * r;
-                const __half* bu = reinterpret_cast<const __half*>(ring_at(c, T->it[ibu])) + rl * r;
+                const __half* bg = reinterpret_cast<const __half*>(ring_at(T->it[ibg])) + rl * r;
+                const __half* bu = reinterpret_cast<const __half*>(ring_at(T->it[ibu])) + rl * r;
                 float dg = 0.f, du = 0.f;
                 for (int q = 0; q < r; ++q) {
                     dg += __half2float(bg[q]) * (part[nlp + q * B + b] + recv[nlp + q * B + b]);
@@ -1064,10 +1225,11 @@ __device__ bool compute_act(Ctx& c, int l, const LayerTab* T, bool lora) {
         act32[(hl * 8 + g) * B + b] = a;
     }
     cbar();
+    stamp((l << 8) | 11);
     if (ok && ssh >= 0) {
         // v[q][b] = sum over the pair's shared act rows of A_down[q][row] act[row][b]
         const Seg& sg = pl.seg[ssh];
-        const __half* adt = reinterpret_cast<const __half*>(ring_at(c, T->it[iadt]));
+        const __half* adt = reinterpret_cast<const __half*>(ring_at(T->it[iadt]));
         const int rows = (sg.hr1 - sg.hr0) * kHalfRow;
         for (int i = tid; i < r * B; i += kConsumerThreads) {
             const int q = i / B, b = i % B;
@@ -1078,47 +1240,49 @@ __device__ bool compute_act(Ctx& c, int l, const LayerTab* T, bool lora) {
     }
     // the non-unit P1 items (LoRA B rows of gate/up) are no longer needed
     for (int i = T->p1; i < T->p2; ++i)
-        if (!unit_kind(T->it[i].kind)) release_item(c, T, i);
+        if (!unit_kind(T->it[i].kind)) release_item(T, i);
     return !cbar_or(!ok);
 }
 
 // P2: down rows of this CTA's half of d over the pair's act quarters -> y
-__device__ bool phase2(Ctx& c, int l, const LayerTab* T, bool lora) {
-    const Prog& p = *c.p;
+__device__ bool phase2(int l, const LayerTab* T, bool lora) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const LayerP& Ly = p.layers[l];
     const int B = p.B, K = p.K, r = p.r, d = p.d;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const PairPlan& pl = T->pl;
     bool ok = true;
-    for (int i = T->p2; i < T->p3 && ok; ++i) ok = wait_item(c, T, i);
+    for (int i = T->p2; i < T->p3 && ok; ++i) ok = wait_item(T, i);
+    stamp((l << 8) | 9);
     if (ok && pl.n_hr > 0) {
-        const uint2* afr = SM<uint2>(c, c.pl.af);
-        const float* qsum = SM<float>(c, c.pl.qsum);
-        const float* vlo = SM<float>(c, c.pl.vlo);
+        const uint2* afr = SM<uint2>(c.pl.af);
+        const float* qsum = SM<float>(c.pl.qsum);
+        const float* vlo = SM<float>(c.pl.vlo);
         const int tok = g >> 1, part = g & 1;
         const bool blive = tok < B;
+        const int nrt = c.hv.rt1 - c.hv.rt0;
         // per-segment token weights (lane's token t)
         float wt[kMaxSegs];
         for (int s = 0; s < pl.nseg; ++s) {
             const Seg& sg = pl.seg[s];
             wt[s] = 0.f;
-            if (t >= B || !seg_live(c, l, sg)) continue;
+            if (t >= B || !seg_live(l, sg)) continue;
             if (sg.slot < 0) { wt[s] = 1.f; continue; }
-            const int e = dist_of(c, l)[sg.slot];
+            const int e = dist_of(l)[sg.slot];
             for (int k = 0; k < K; ++k)
-                if (ids_of(c, l)[t * K + k] == e) wt[s] += w_of(c, l)[t * K + k];
+                if (ids_of(l)[t * K + k] == e) wt[s] += w_of(l)[t * K + k];
         }
         // LoRA down rows
         const int ibd = (lora && pl.has_sh) ? find_item(T, T->p2, T->p3, IT_BD, 0) : -1;
-        const int nrt = c.hv.rt1 - c.hv.rt0;
         int w0, w1;
         split_range(nrt, kConsumerWarps, wid, &w0, &w1);
-        float* y = y_buf(c, c.par, Ly.sidx);
+        float* y = y_buf(c.par, Ly.sidx);
         for (int i = w0; i < w1; ++i) {
             float y0 = 0.f, y1 = 0.f;
             for (int s = 0; s < pl.nseg; ++s) {
                 const Seg& sg = pl.seg[s];
-                if (!seg_live(c, l, sg)) continue;
+                if (!seg_live(l, sg)) continue;
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 int gcur = -1;
                 uint2 sc = make_uint2(0u, 0u);
@@ -1138,30 +1302,42 @@ __device__ bool phase2(Ctx& c, int l, const LayerTab* T, bool lora) {
                 for (int j = T->p2; j < T->p3; ++j) {
                     const Item& it = T->it[j];
                     if (it.seg != s) continue;
-                    if (it.kind == IT_DSC) {
+                    if (it.kind == IT_DQ || it.kind == IT_DQS) {
+                        // steps b .. b + n - 1 of group a over this CTA's row tiles
+                        if (gcur != it.a) {
+                            gcur = it.a;
+                            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                        }
+                        for (int qi = 0; qi < it.n; ++qi) {
+                            const uint32_t wq = *reinterpret_cast<const uint32_t*>(
+                                ring_at(it) + (qi * nrt + i) * kQ4Quarter + 4 * lane);
+                            const int Ql = sg.qoff + 4 * gcur + it.b + qi - sg.q0;
+                            uint2 bb = make_uint2(0u, 0u);
+                            if (blive) bb = afr[((Ql * B + tok) * 2 + part) * 4 + t];
+                            uint32_t A[4];
+                            q4_masks(wq, A);
+                            mma_16816(acc, A, bb.x, bb.y);
+                        }
+                        if (it.kind == IT_DQS) {
+                            sc = *reinterpret_cast<const uint2*>(ring_at(it) + it.n * nrt * kQ4Quarter +
+                                                                 i * kQ4Scales + 8 * g);
+                            epilogue();
+                            gcur = -1;
+                        }
+                    } else if (it.kind == IT_DSC) {
+                        sc = *reinterpret_cast<const uint2*>(ring_at(it) + i * kQ4Scales + 8 * g);
                         epilogue();
-                        gcur = it.a;
-                        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-                        sc = *reinterpret_cast<const uint2*>(ring_at(c, it) + i * kQ4Scales + 8 * g);
-                    } else if (it.kind == IT_DQ) {
-                        const uint32_t wq = *reinterpret_cast<const uint32_t*>(ring_at(c, it) + i * kQ4Quarter + 4 * lane);
-                        const int Ql = sg.qoff + it.a - sg.q0;
-                        uint2 bb = make_uint2(0u, 0u);
-                        if (blive) bb = afr[((Ql * B + tok) * 2 + part) * 4 + t];
-                        uint32_t A[4];
-                        q4_masks(wq, A);
-                        mma_16816(acc, A, bb.x, bb.y);
+                        gcur = -1;
                     }
                 }
-                epilogue();
             }
             const int row = (c.hv.rt0 + i) * kRowTile + g;
             if (ibd >= 0 && t < B) {
                 // rows of this CTA's half are split over consecutive BD items
                 const int per = kItemMax / (r * 2);
                 const int rel = row - c.hv.rt0 * kRowTile;
-                const __half* bd0 = reinterpret_cast<const __half*>(ring_at(c, T->it[ibd + rel / per])) + (rel % per) * r;
-                const __half* bd1 = reinterpret_cast<const __half*>(ring_at(c, T->it[ibd + (rel + 8) / per])) + ((rel + 8) % per) * r;
+                const __half* bd0 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + rel / per])) + (rel % per) * r;
+                const __half* bd1 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + (rel + 8) / per])) + ((rel + 8) % per) * r;
                 float d0 = 0.f, d1 = 0.f;
                 for (int q = 0; q < r; ++q) {
                     d0 += __half2float(bd0[q]) * vlo[q * B + t];
@@ -1181,17 +1357,19 @@ __device__ bool phase2(Ctx& c, int l, const LayerTab* T, bool lora) {
             }
         }
     }
-    for (int i = T->p2; i < T->p3; ++i) release_item(c, T, i);
+    stamp((l << 8) | 12);
+    for (int i = T->p2; i < T->p3; ++i) release_item(T, i);
     return ok;
 }
 
 // top-K of a head whose logits are complete (the last CTA to finish its head work)
-__device__ void head_topk(Ctx& c, int l) {
-    const Prog& p = *c.p;
+__device__ __noinline__ void head_topk(int l) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const LayerP& Ly = p.layers[l];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    float* scr = SM<float>(c, c.pl.rscr);
-    const float* lg = logh_buf(c, c.par, Ly.sidx);
+    float* scr = SM<float>(c.pl.rscr);
+    const float* lg = logh_buf(c.par, Ly.sidx);
     for (int i = tid; i < p.B * p.E; i += kConsumerThreads) {
         const int b = i / p.E, e = i - b * p.E;
         const float v = __ldcg(lg + i);
@@ -1221,20 +1399,21 @@ __device__ void head_topk(Ctx& c, int l) {
 // P3: this pair's head tasks of layer l (fc1 row tiles with their fc2 columns, or
 // linear_init row tiles), then the arrival count; the last CTA does the top-K.
 // Every consumer thread runs every barrier; the result is CTA-uniform.
-__device__ bool phase3(Ctx& c, int l, const LayerTab* T, uint32_t& xph) {
-    const Prog& p = *c.p;
+__device__ bool phase3(int l, const LayerTab* T, uint32_t& xph) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const LayerP& Ly = p.layers[l];
     const int B = p.B, K = p.K, E = p.E, H = p.H;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
     const PairPlan& pl = T->pl;
     const int nH = H / kRowTile;
-    const int* ids = ids_of(c, l);
-    const int* prv = prev_of(c, l);
-    const int nprev = SM<int>(c, c.pl.nprv)[l];   // previous-token ids present (0 or K)
-    float* lg = logh_buf(c, c.par, Ly.sidx);
-    float* zpart = SM<float>(c, c.pl.zpart);
-    float* zrecv = SM<float>(c, c.pl.zrecv);
-    __half* gf = SM<__half>(c, c.pl.gf);
+    const int* ids = ids_of(l);
+    const int* prv = prev_of(l);
+    const int nprev = SM<int>(c.pl.nprv)[l];   // previous-token ids present (0 or K)
+    float* lg = logh_buf(c.par, Ly.sidx);
+    float* zpart = SM<float>(c.pl.zpart);
+    float* zrecv = SM<float>(c.pl.zrecv);
+    __half* gf = SM<__half>(c.pl.gf);
     bool ok = true;
     int i = T->p3;
     for (int task = pl.hd0; task < pl.hd1; ++task) {
@@ -1246,13 +1425,15 @@ __device__ bool phase3(Ctx& c, int l, const LayerTab* T, uint32_t& xph) {
             // z partial of H rows 16 pos .. + 15 over this CTA's half of d
             for (int q = tid; q < 16 * B; q += kConsumerThreads) zpart[q] = 0.f;
             cbar();
-            ok = warp_units(c, T, i, j, [&](const Item& it, int a, int b) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                f16_run(c, ring_at(c, it), a, b, it.b, acc);
-                if (t < B) {
-                    atomicAdd(&zpart[g * B + t], acc[0]);
-                    atomicAdd(&zpart[(g + 8) * B + t], acc[2]);
-                }
+            ok = warp_units(T, i, j, [&](const Item& it, int a, int b) {
+                tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    f16_run(ring_at(it), j0, j1, gl0, acc);
+                    if (t < B) {
+                        atomicAdd(&zpart[g * B + t], acc[0]);
+                        atomicAdd(&zpart[(g + 8) * B + t], acc[2]);
+                    }
+                });
             }) && ok;
             // one-hot columns: fc1[:, d + e] for executed e, fc1[:, d + E + e] for previous e
             float oh = 0.f;
@@ -1263,9 +1444,9 @@ __device__ bool phase3(Ctx& c, int l, const LayerTab* T, uint32_t& xph) {
                 for (int k = 0; k < nprev; ++k)
                     oh += __half2float(Ly.fc1_oh[(long long)(E + prv[bb * K + k]) * H + hrow]);
             }
-            ok = !cbar_or(!ok || aborted(c));
+            ok = !cbar_or(!ok || aborted());
             float* zr = zrecv + (xph & 1) * 16 * B;
-            if (ok) ok = exchange(c, 1, zpart, zr, 16 * B, xph);
+            if (ok) ok = exchange(1, zpart, zr, 16 * B, xph);
             if (ok && tid < 16 * B) {
                 const float z = zpart[rr * B + bb] + zr[rr * B + bb] + oh;
                 const float gl = 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
@@ -1279,12 +1460,12 @@ __device__ bool phase3(Ctx& c, int l, const LayerTab* T, uint32_t& xph) {
             // fc2 columns 16 pos .. + 15 for this CTA's half of the E rows
             if (j < T->n && T->it[j].kind == IT_FC2 && T->it[j].a == pos) {
                 const Item& it2 = T->it[j];
-                if (ok) ok = wait_item(c, T, j);
+                if (ok) ok = wait_item(T, j);
                 if (ok) {
-                    const uint2* gfr = SM<uint2>(c, c.pl.gf);
+                    const uint2* gfr = SM<uint2>(c.pl.gf);
                     const int tok = g >> 1, prt = g & 1;
                     for (int e = wid; e < it2.n; e += kConsumerWarps) {
-                        const uint4 av = *reinterpret_cast<const uint4*>(ring_at(c, it2) + e * kF16Step + 16 * lane);
+                        const uint4 av = *reinterpret_cast<const uint4*>(ring_at(it2) + e * kF16Step + 16 * lane);
                         uint2 bq = make_uint2(0u, 0u);
                         if (tok < B) bq = gfr[(tok * 2 + prt) * 4 + t];
                         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1297,19 +1478,21 @@ __device__ bool phase3(Ctx& c, int l, const LayerTab* T, uint32_t& xph) {
                         }
                     }
                 }
-                release_item(c, T, j);
+                release_item(T, j);
                 ++j;
             }
             ok = !cbar_or(!ok);
         } else {
-            ok = warp_units(c, T, i, j, [&](const Item& it, int a, int b) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                f16_run(c, ring_at(c, it), a, b, it.b, acc);
-                const int row = pos * kRowTile + g;
-                if (t < B) {
-                    red_add_f32(lg + t * E + row, acc[0]);
-                    red_add_f32(lg + t * E + row + 8, acc[2]);
-                }
+            ok = warp_units(T, i, j, [&](const Item& it, int a, int b) {
+                tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    f16_run(ring_at(it), j0, j1, gl0, acc);
+                    const int row = tile * kRowTile + g;
+                    if (t < B) {
+                        red_add_f32(lg + t * E + row, acc[0]);
+                        red_add_f32(lg + t * E + row + 8, acc[2]);
+                    }
+                });
             }) && ok;
             if (c.rank == 0 && tid < 16 * B) {
                 // linear_init one-hot columns of these 16 logits
@@ -1330,18 +1513,19 @@ __device__ bool phase3(Ctx& c, int l, const LayerTab* T, uint32_t& xph) {
         cbar();
         const Shape Sh = layer_shape(p, l, false);
         if (tid == 0) {
-            const unsigned old = atom_acq_rel_add_u32(cnt_buf(c, c.par, Ly.sidx), 1u);
+            const unsigned old = atom_acq_rel_add_u32(cnt_buf(c.par, Ly.sidx), 1u);
             c.ctl->last = old == (unsigned)(head_ctas(Sh, c.P) - 1);
         }
         cbar();
-        if (c.ctl->last) head_topk(c, l);
+        if (c.ctl->last) head_topk(l);
     }
     return !cbar_or(!ok);
 }
 
 // ------------------------------------------------------------ the kernel ---
-__device__ void consumer(Ctx& c) {
-    const Prog& p = *c.p;
+__device__ void consumer() {
+    Ctx& c = ctx();
+    const Prog& p = prg();
     const int tid = threadIdx.x;
     const int B = p.B, d = p.d;
     unsigned long long bar_target = 0;
@@ -1350,74 +1534,74 @@ __device__ void consumer(Ctx& c) {
         bar_target = v - v % (unsigned long long)c.nct;
     }
     uint32_t xph1 = 0, xph3 = 0;
-    volatile int* ready = SM<volatile int>(c, c.pl.ready);
-    float* part = SM<float>(c, c.pl.part);
+    volatile int* ready = SM<volatile int>(c.pl.ready);
+    float* part = SM<float>(c.pl.part);
     // every decision to leave the loop is taken from a barrier reduction, so all
     // consumer threads leave together
     for (int l = 0; l < p.L; ++l) {
         const LayerP& Ly = p.layers[l];
-        LayerTab* T = tab_of(c, l);
-        stamp(c, (l << 8) | 0);
-        if (tid == 0) wait_flag(c, &T->seq, l + 1);
-        if (cbar_or(aborted(c))) break;
+        LayerTab* T = tab_of(l);
+        stamp((l << 8) | 0);
+        if (tid == 0) wait_flag(&T->seq, l + 1);
+        if (cbar_or(aborted())) break;
         const bool router = has_router_phase(p, l, c.step);
         const Shape Sh = layer_shape(p, l, router);
         for (int q = tid; q < (T->pl.n_hr * 16 + 32) * B; q += kConsumerThreads) part[q] = 0.f;
         // ---------------- input x
         if (p.mode == MODE_DECODE && l > 0)
-            if (!bar_wait(c, bar_target)) break;
-        if (p.mode == MODE_DECODE || l == 0) build_x(c, l);
-        stamp(c, (l << 8) | 1);
+            if (!bar_wait(bar_target)) break;
+        if (p.mode == MODE_DECODE || l == 0) build_x(l);
+        stamp((l << 8) | 1);
         // ---------------- own routing
         if (router) {
-            const bool ok = phase_router(c, l, T);
-            if (cbar_or(!ok || aborted(c))) break;
-            bar_arrive(c);
-            if (!bar_wait(c, bar_target)) break;
-            route_layer(c, l);
+            const bool ok = phase_router(l, T);
+            if (cbar_or(!ok || aborted())) break;
+            bar_arrive();
+            if (!bar_wait(bar_target)) break;
+            route_layer(l);
         }
         if (p.mode == MODE_DECODE && c.cta == 0) {
             for (int i = tid; i < B * p.K; i += kConsumerThreads)
-                p.exec_ids[(((long long)c.par * p.Ls + Ly.sidx) * B) * p.K + i] = ids_of(c, l)[i];
+                p.exec_ids[(((long long)c.par * p.Ls + Ly.sidx) * B) * p.K + i] = ids_of(l)[i];
         }
         if (ready[l] != 1) {
-            if (tid == 0) raise_error(c, EDGE0_EINVAL);
+            if (tid == 0) raise_error(EDGE0_EINVAL);
             cbar();
             break;
         }
-        stamp(c, (l << 8) | 2);
+        stamp((l << 8) | 2);
         // ---------------- P1: gate/up partials, swap with the peer, act
-        bool ok = phase1(c, l, T);
-        if (cbar_or(!ok || aborted(c))) break;
-        stamp(c, (l << 8) | 3);
+        bool ok = phase1(l, T);
+        if (cbar_or(!ok || aborted())) break;
+        stamp((l << 8) | 3);
         if (T->pl.n_hr > 0) {
             const int nmsg = (T->pl.n_hr * 16 + (Sh.lora && T->pl.has_sh ? 32 : 0)) * B;
-            ok = exchange(c, 0, part, SM<float>(c, c.pl.recv), nmsg, xph1);
+            ok = exchange(0, part, SM<float>(c.pl.recv), nmsg, xph1);
             if (cbar_or(!ok)) break;
         }
-        stamp(c, (l << 8) | 4);
-        if (!compute_act(c, l, T, Sh.lora != 0)) break;
-        stamp(c, (l << 8) | 5);
+        stamp((l << 8) | 4);
+        if (!compute_act(l, T, Sh.lora != 0)) break;
+        stamp((l << 8) | 5);
         // ---------------- P2: down -> y, then this layer's barrier
-        ok = phase2(c, l, T, Sh.lora != 0);
-        if (cbar_or(!ok || aborted(c))) break;
-        bar_arrive(c);
-        stamp(c, (l << 8) | 6);
+        ok = phase2(l, T, Sh.lora != 0);
+        if (cbar_or(!ok || aborted())) break;
+        bar_arrive();
+        stamp((l << 8) | 6);
         // ---------------- P3: head, while the barrier completes
         if (Sh.head)
-            if (!phase3(c, l, T, xph3)) break;
-        stamp(c, (l << 8) | 7);
-        if (cbar_or(aborted(c))) break;
+            if (!phase3(l, T, xph3)) break;
+        stamp((l << 8) | 7);
+        if (cbar_or(aborted())) break;
         if (tid == 0) *(volatile int*)&c.ctl->cdone = l + 1;
     }
-    if (cbar_or(aborted(c))) return;
+    if (cbar_or(aborted())) return;
     // ---------------- tail: the last layer's y is complete after its barrier
-    if (!bar_wait(c, bar_target)) return;
-    const float* Y = y_buf(c, c.par, p.layers[p.L - 1].sidx);
+    if (!bar_wait(bar_target)) return;
+    const float* Y = y_buf(c.par, p.layers[p.L - 1].sidx);
     const long long n = (long long)B * d;
     const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
     if (p.mode == MODE_DECODE) {
-        const __half* hs = SM<__half>(c, c.pl.hs);
+        const __half* hs = SM<__half>(c.pl.hs);
         for (long long i = a + tid; i < b; i += kConsumerThreads)
             p.h_io[i] = __float2half_rn(__half2float(hs[i]) + __ldcg(Y + i));
     } else if (p.mode == MODE_MOE) {
@@ -1427,22 +1611,43 @@ __device__ void consumer(Ctx& c) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ Prog prog) {
-    extern __shared__ __align__(128) char smem[];
-    Ctx c;
-    c.p = &prog;
-    c.sm = smem;
-    c.pl = make_plan(prog);
-    c.hdr = reinterpret_cast<WsHeader*>(prog.ws);
-    c.ctl = reinterpret_cast<Ctl*>(smem + c.pl.ctl);
-    c.ws = ws_layout(prog.Ls, prog.B, prog.d, prog.E);
-    c.nct = gridDim.x;
-    c.cta = blockIdx.x;
-    c.rank = (int)cluster_ctarank();
-    c.pair = c.cta / kClusterCtas;
-    c.P = c.nct / kClusterCtas;
-    c.hv = halves(prog.d, prog.E, c.rank);
     const int tid = threadIdx.x;
-    const Prog& p = prog;
+    // parameters and context into shared memory
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(&prog);
+        uint4* dst = reinterpret_cast<uint4*>(g_smem + kProgOff);
+        for (int i = tid; i < (int)(sizeof(Prog) / 16); i += kThreads) dst[i] = src[i];
+        if (tid == 0) {
+            const char* s8 = reinterpret_cast<const char*>(&prog);
+            for (int i = (int)(sizeof(Prog) / 16) * 16; i < (int)sizeof(Prog); ++i) g_smem[kProgOff + i] = s8[i];
+            Ctx& cc = ctx();
+            cc.pl = make_plan(prog, kCtxOff + kCtxBytes);
+            cc.hdr = reinterpret_cast<WsHeader*>(prog.ws);
+            cc.ctl = reinterpret_cast<Ctl*>(g_smem + cc.pl.ctl);
+            cc.ws = ws_layout(prog.Ls, prog.B, prog.d, prog.E);
+            cc.nct = gridDim.x;
+            cc.cta = blockIdx.x;
+            cc.rank = (int)cluster_ctarank();
+            cc.pair = cc.cta / kClusterCtas;
+            cc.P = cc.nct / kClusterCtas;
+            cc.hv = halves(prog.d, prog.E, cc.rank);
+        }
+        __syncthreads();
+    }
+    Ctx& c = ctx();
+    const Prog& p = prg();
+
+    // the pair exchange addresses the other CTA of a two-CTA cluster: a launch
+    // without that cluster shape records an error and touches no other CTA
+    uint32_t ncl;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncl));
+    if (ncl != (uint32_t)kClusterCtas || gridDim.x % kClusterCtas) {
+        if (tid == 0) {
+            atomicCAS(&c.hdr->error, 0, EDGE0_EUNSUPPORTED);
+            atomicExch(&c.hdr->abort, 1);
+        }
+        return;
+    }
 
     if (tid == 0) {
         Ctl* ctl = c.ctl;
@@ -1453,15 +1658,16 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         ctl->step = p.step >= 0 ? p.step : ld_volatile_s32(&c.hdr->step);
         ctl->trace = c.cta < kTraceCtas ? ld_volatile_s32(&c.hdr->trace) : 0;
         ctl->tslot = 0;
+        ctl->ptslot = kTraceProducer;
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(SM<uint64_t>(c, c.pl.full) + s, 1);
-            mbar_init(SM<uint64_t>(c, c.pl.empty) + s, kConsumerWarps);
+            mbar_init(SM<uint64_t>(c.pl.full) + s, 1);
+            mbar_init(SM<uint64_t>(c.pl.empty) + s, kConsumerWarps);
         }
-        mbar_init(SM<uint64_t>(c, c.pl.xch) + 0, 1);
-        mbar_init(SM<uint64_t>(c, c.pl.xch) + 1, 1);
+        mbar_init(SM<uint64_t>(c.pl.xch) + 0, 1);
+        mbar_init(SM<uint64_t>(c.pl.xch) + 1, 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < kTables; i += kThreads) tab_of(c, i)->seq = 0;
+    for (int i = tid; i < kTables; i += kThreads) tab_of(i)->seq = 0;
     __syncthreads();
     c.step = c.ctl->step;
     c.par = c.step & 1;
@@ -1474,12 +1680,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         for (long long i = a + tid; i < b; i += kThreads) {
             const long long l = i / (per_y + 2 * per_l), o = i % (per_y + 2 * per_l);
             const int sidx = p.layers[l].sidx;
-            if (o < per_y) y_buf(c, op, sidx)[o] = 0.f;
-            else if (o < per_y + per_l) logr_buf(c, op, sidx)[o - per_y] = 0.f;
-            else logh_buf(c, op, sidx)[o - per_y - per_l] = 0.f;
+            if (o < per_y) y_buf(op, sidx)[o] = 0.f;
+            else if (o < per_y + per_l) logr_buf(op, sidx)[o - per_y] = 0.f;
+            else logh_buf(op, sidx)[o - per_y - per_l] = 0.f;
         }
         if (c.cta == 0)
-            for (int l = tid; l < p.L; l += kThreads) *cnt_buf(c, op, p.layers[l].sidx) = 0u;
+            for (int l = tid; l < p.L; l += kThreads) *cnt_buf(op, p.layers[l].sidx) = 0u;
     }
     // routing known at launch: predictions (prerouted layers, step > 0) or inputs;
     // previous-token ids of head layers
@@ -1501,10 +1707,10 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         int flag = 0;
         if (src_i) {
             for (int i = 0; i < BK; ++i) {
-                ids_of(c, l)[i] = src_i[i];
-                w_of(c, l)[i] = src_w ? src_w[i] : 0.f;
+                ids_of(l)[i] = src_i[i];
+                w_of(l)[i] = src_w ? src_w[i] : 0.f;
             }
-            if (!make_dist(c, l)) raise_error(c, EDGE0_EINVAL);
+            if (!make_dist(l)) raise_error(EDGE0_EINVAL);
             flag = 1;
         }
         const int32_t* pv = nullptr;
@@ -1514,30 +1720,30 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         if (pv) {
             for (int i = 0; i < BK; ++i) {
                 const int e = pv[i];
-                if (e < 0 || e >= p.E) raise_error(c, EDGE0_EINVAL);
-                prev_of(c, l)[i] = e < 0 || e >= p.E ? 0 : e;
+                if (e < 0 || e >= p.E) raise_error(EDGE0_EINVAL);
+                prev_of(l)[i] = e < 0 || e >= p.E ? 0 : e;
             }
         }
-        SM<int>(c, c.pl.nprv)[l] = pv ? p.K : 0;
-        SM<volatile int>(c, c.pl.ready)[l] = flag;
+        SM<int>(c.pl.nprv)[l] = pv ? p.K : 0;
+        SM<volatile int>(c.pl.ready)[l] = flag;
     }
     __syncthreads();
     // the peer's barriers exist before any exchange
     cluster_sync_all();
 
     if (tid >= kConsumerThreads) {
-        if (tid == kConsumerThreads && !aborted(c)) producer(c);
+        producer();   // the whole producer warp
         __syncwarp();
     } else {
-        consumer(c);
+        consumer();
     }
     __syncthreads();
-    if (tid == 0 && aborted(c)) {
+    if (tid == 0 && aborted()) {
         // let copies still in flight into this CTA's ring land before it exits (bounded)
         const int issued = *(volatile int*)&c.ctl->issued;
         const unsigned long long t0 = now_ns();
         for (int k = issued > kSlots ? issued - kSlots : 0; k < issued; ++k)
-            while (!mbar_try_wait(full_bar(c, k), item_parity(k)))
+            while (!mbar_try_wait(full_bar(k), item_parity(k)))
                 if (now_ns() - t0 > 100000000ull) break;
         while (now_ns() - t0 < 20000ull) {}   // stores from the peer still in flight
     }
@@ -1593,7 +1799,7 @@ int engine_grid(int* nct) {
 // combinations) and the ring that fits next to the fixed buffers.
 struct Derived {
     int mode, B, K, d, E, I, Is, H, r, nct, smem_max;
-    int rc, slots_max, hr_max, q_max, ring_bytes, smem;
+    int rc, slots_max, ps0, ps1, hr_max, q_max, ring_bytes, smem;
 };
 
 static int derive(Derived& D) {
@@ -1609,6 +1815,10 @@ static int derive(Derived& D) {
     if (p.r <= 0 || p.r > 16) return EDGE0_EUNSUPPORTED;
     p.slots_max = p.mode == MODE_HEAD ? 0 : (p.B * p.K < p.E ? p.B * p.K : p.E);
     const int P = D.nct / kClusterCtas;
+    // the plan's 32-bit splits: n * parts stays below 2^31
+    if ((long long)(p.slots_max * (p.I / kHalfRow) + p.Is) * P >= (1LL << 31)) return EDGE0_EUNSUPPORTED;
+    p.ps[0] = shared_pairs(P, p.Is / kHalfRow, p.slots_max * (p.I / kHalfRow), false);
+    p.ps[1] = shared_pairs(P, p.Is / kHalfRow, p.slots_max * (p.I / kHalfRow), true);
     p.hr_max = 1;
     p.q_max = 1;
     LayerTab T;   // scratch on the stack: the allocation-free entry point comes here too
@@ -1640,16 +1850,18 @@ static int derive(Derived& D) {
         if (pass == 0) {
             p.L = EDGE0_MAX_LAYERS;   // the fixed buffers of the largest call
             p.ring_bytes = 0;
-            const int fixed = make_plan(p).total;
+            const int fixed = make_plan(p, kCtxOff + kCtxBytes).total;
             p.ring_bytes = ((D.smem_max - fixed) / 16) * 16;
             if (p.ring_bytes < kMinRing) return EDGE0_EUNSUPPORTED;
         }
     }
     D.slots_max = p.slots_max;
+    D.ps0 = p.ps[0];
+    D.ps1 = p.ps[1];
     D.hr_max = p.hr_max;
     D.q_max = p.q_max;
     D.ring_bytes = p.ring_bytes;
-    D.smem = make_plan(p).total;
+    D.smem = make_plan(p, kCtxOff + kCtxBytes).total;
     return EDGE0_OK;
 }
 
@@ -1685,11 +1897,13 @@ int engine_check(Prog& p, int nct, int smem_max, int* smem_bytes) {
     const Derived& d = g_derived[hit];
     if (d.rc) return d.rc;
     p.slots_max = d.slots_max;
+    p.ps[0] = d.ps0;
+    p.ps[1] = d.ps1;
     p.hr_max = d.hr_max;
     p.q_max = d.q_max;
     p.ring_bytes = d.ring_bytes;
     // the fixed buffers of this call's L are no larger than those the ring was sized with
-    *smem_bytes = make_plan(p).total;
+    *smem_bytes = make_plan(p, kCtxOff + kCtxBytes).total;
     return EDGE0_OK;
 }
 

@@ -99,6 +99,7 @@ struct Prog {
     char* ws;
     // derived by engine_check for the launch's grid
     int slots_max;            // routed expert slots of a layer: min(B K, E)
+    int ps[2];                // CTA pairs that own shared-expert rows (without, with LoRA)
     int hr_max, q_max;        // most half-row tiles / act quarters one CTA pair owns
     int ring_bytes;           // shared-memory ring of streamed weights
     LayerP layers[EDGE0_MAX_LAYERS];
@@ -116,7 +117,7 @@ struct WsHeader {
 constexpr int kWsHeaderBytes = 256;
 // trace area (at the end of the workspace): per CTA kTraceSlots u64
 constexpr int kTraceCtas = 160;
-constexpr int kTraceSlots = 1024;   // (tag, time) pairs
+constexpr int kTraceSlots = 4096;   // u64 words: (tag, globaltimer, clock) triples
 
 // Workspace after the header, per step parity p in {0, 1} and state row s:
 //   y        [2][Ls][B][d]  fp32  layer output accumulators (red.add)

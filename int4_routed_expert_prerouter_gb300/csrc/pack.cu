@@ -14,15 +14,20 @@
 // fp16 step block (16 bytes per lane, 512 per row tile and step): the lane's A
 // registers a0..a3 = (g, 2t|2t+1), (g+8, 2t|2t+1), (g, 2t+8|2t+9), (g+8, 2t+8|2t+9).
 //
-// Packed matrices:
-//   gate/up  [E][I/8 tiles][d/64 groups][576]: tile j interleaves gate rows
-//            8j..8j+7 (tile rows 0..7) with up rows 8j..8j+7 (tile rows 8..15); a
-//            576-byte unit = 4 step words per lane (512 B) + (s, b) of rows g and
-//            g + 8 at 512 + 8 g.
-//   down     [E][I/64 groups][4 steps][d/16 row tiles][128] then, per group,
-//            [d/16 row tiles][64] scale/bias pairs: one 16-input slice of the
-//            intermediate is contiguous over all output rows.
-//   fp16     [out/16 row tiles][in/64 groups][4 steps][512] (row-tile major) or
+// Packed matrices.  The decode engine splits the input groups of a matrix that
+// multiplies x, and the output rows of down, into two halves (half 0: the first
+// n/2, half 1: the rest), one per CTA of a pair; each half is stored contiguously
+// so that a CTA's share of consecutive row tiles is one run of bytes.
+//   gate/up  [E][half][I/8 tiles][groups of the half][576]: tile j interleaves
+//            gate rows 8j..8j+7 (tile rows 0..7) with up rows 8j..8j+7 (tile rows
+//            8..15); a 576-byte unit = 4 step words per lane (512 B) + (s, b) of
+//            rows g and g + 8 at 512 + 8 g.
+//   down     [E][I/64 groups][half of the d/16 row tiles]: 4 step blocks of 128 B
+//            per row tile of the half (step major), then the half's 64-byte
+//            scale/bias blocks; one 16-input slice of the intermediate over a
+//            half of the output rows is contiguous.
+//   fp16     [half][out/16 row tiles][groups of the half][4 steps][512] (row
+//            tiles x input groups; every matrix that multiplies x) or
 //            [in/16 steps][out/16 row tiles][512] (K-major, for the head's fc2).
 #include "internal.cuh"
 
@@ -66,7 +71,10 @@ __global__ void pack_gu_kernel(const uint32_t* __restrict__ qg, const uint16_t* 
     v.y = step_word(rg, ru, kGroup * c + 16, t);
     v.z = step_word(rg, ru, kGroup * c + 32, t);
     v.w = step_word(rg, ru, kGroup * c + 48, t);
-    char* u = dst + unit * kQ4Unit;
+    // half-major position of unit (j, c) of expert e
+    const int n0 = n_g / 2, h = c >= n0 ? 1 : 0, nh = h ? n_g - n0 : n0;
+    const long long pos = (long long)e * n_t * n_g + (long long)h * n_t * n0 + (long long)j * nh + (c - h * n0);
+    char* u = dst + pos * kQ4Unit;
     *reinterpret_cast<uint4*>(u + 16 * lane) = v;
     if (t == 0) {
         const long long o = ((long long)e * I + row) * gpr + c;
@@ -97,9 +105,11 @@ __global__ void pack_down_kernel(const uint32_t* __restrict__ q, const uint16_t*
     const long long wpr = in / 8, gpr = in / kGroup;
     const uint32_t* w0 = r0 < out ? q + ((long long)e * out + r0) * wpr : nullptr;
     const uint32_t* w1 = r1 < out ? q + ((long long)e * out + r1) * wpr : nullptr;
-    char* base = dst + ((long long)e * n_g + c) * n_rt * kQ4Unit;
+    // half h of the row tiles: [4 steps][row tiles of the half][128] then [row tiles of the half][64]
+    const int n0 = n_rt / 2, h = i >= n0 ? 1 : 0, nh = h ? n_rt - n0 : n0, il = i - h * n0;
+    char* base = dst + ((long long)e * n_g + c) * n_rt * kQ4Unit + (long long)h * n0 * kQ4Unit;
     for (int st = 0; st < 4; ++st)
-        *reinterpret_cast<uint32_t*>(base + ((long long)st * n_rt + i) * kQ4Quarter + 4 * lane) =
+        *reinterpret_cast<uint32_t*>(base + ((long long)st * nh + il) * kQ4Quarter + 4 * lane) =
             step_word(w0, w1, kGroup * c + 16 * st, t);
     if (t == 0) {
         ushort4 sb;
@@ -108,7 +118,7 @@ __global__ void pack_down_kernel(const uint32_t* __restrict__ q, const uint16_t*
         sb.y = r0 < out ? b[o0] : 0;
         sb.z = r1 < out ? s[o1] : 0;
         sb.w = r1 < out ? b[o1] : 0;
-        *reinterpret_cast<ushort4*>(base + 4LL * n_rt * kQ4Quarter + (long long)i * kQ4Scales + 8 * g) = sb;
+        *reinterpret_cast<ushort4*>(base + 4LL * nh * kQ4Quarter + (long long)il * kQ4Scales + 8 * g) = sb;
     }
 }
 
@@ -134,9 +144,18 @@ __global__ void pack_f16_kernel(const uint16_t* __restrict__ W, int out, int in,
     const int lane = (int)(tid & 31);
     const long long blk = tid >> 5;
     int i, st;
-    if (kmajor) { i = (int)(blk % n_rt); st = (int)(blk / n_rt); }
-    else { st = (int)(blk % n_s); i = (int)(blk / n_s); }
-    *reinterpret_cast<uint4*>(dst + blk * kF16Step + 16 * lane) =
+    long long pos = blk;
+    if (kmajor) {
+        i = (int)(blk % n_rt);
+        st = (int)(blk / n_rt);
+    } else {
+        // half-major over the input groups: [half][row tile][group of the half][step]
+        st = (int)(blk % n_s);
+        i = (int)(blk / n_s);
+        const int n_g = n_s / 4, n0 = n_g / 2, c = st / 4, h = c >= n0 ? 1 : 0, nh = h ? n_g - n0 : n0;
+        pos = ((long long)h * n_rt * n0 + (long long)i * nh + (c - h * n0)) * 4 + st % 4;
+    }
+    *reinterpret_cast<uint4*>(dst + pos * kF16Step + 16 * lane) =
         f16_block(W, out, ld, i, 16 * st, lane >> 2, lane & 3);
 }
 

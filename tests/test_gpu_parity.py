@@ -42,7 +42,9 @@ def _cpu_model(model):
 # ------------------------------------------------------------- packing ----
 # Reference packers written from the layout description in include/edge0.h:
 # lane L = 4g + t of a row tile's 16-input step holds rows g and g + 8 at
-# step-local inputs {2t, 2t+1, 2t+8, 2t+9}.
+# step-local inputs {2t, 2t+1, 2t+8, 2t+9}; matrices that multiply x are stored
+# by halves of their input groups, down by halves of its output row tiles
+# (half 0: the first n // 2).
 _NIB = [(0, 0), (1, 0), (0, 8), (1, 8), (0, 1), (1, 1), (0, 9), (1, 9)]   # (row + 8?, k offset) of nibble p
 
 
@@ -90,7 +92,9 @@ def _ref_pack_gate_up(gate, up):
     words, sc = _q4_units(rows, S, Bq)                   # [E, tiles, ng, 4, 32], [E, tiles, ng, 8, 4]
     w32 = words.to(torch.int32).transpose(-1, -2).contiguous()              # [E, tiles, ng, 32, 4]
     units = torch.cat([w32.view(torch.uint8).flatten(-2), sc.contiguous().view(torch.uint8).flatten(-2)], -1)
-    return units.reshape(-1)
+    n0 = units.shape[2] // 2                             # [E, tiles, ng, 576] -> [E, half, tiles, groups, 576]
+    halves = [units[:, :, :n0].reshape(E, -1), units[:, :, n0:].reshape(E, -1)]
+    return torch.cat(halves, dim=1).reshape(-1)
 
 
 def _ref_pack_down(trip):
@@ -104,12 +108,17 @@ def _ref_pack_down(trip):
     S[:, :out] = s
     Bq[:, :out] = b
     words, sc = _q4_units(N.view(E, n_rt, 16, -1), S.view(E, n_rt, 16, -1), Bq.view(E, n_rt, 16, -1))
-    # words [E, rt, g, 4 steps, 32 lanes] -> per group: [4 steps][rt][32 lanes] words, then [rt] scales
+    # words [E, rt, g, 4 steps, 32 lanes] -> per group and half of the row tiles:
+    # [4 steps][rt of the half][32 lanes] words, then [rt of the half] scales
     w = words.to(torch.int32).permute(0, 2, 3, 1, 4).contiguous()           # [E, g, 4, rt, 32]
     scv = sc.permute(0, 2, 1, 3, 4).contiguous()                            # [E, g, rt, 8, 4]
     ng = w.shape[1]
-    per_g = torch.cat([w.view(torch.uint8).view(E, ng, -1), scv.view(torch.uint8).view(E, ng, -1)], -1)
-    return per_g.reshape(-1)
+    n0 = n_rt // 2
+    parts = []
+    for lo, hi in ((0, n0), (n0, n_rt)):
+        parts.append(w[:, :, :, lo:hi].contiguous().view(torch.uint8).view(E, ng, -1))
+        parts.append(scv[:, :, lo:hi].contiguous().view(torch.uint8).view(E, ng, -1))
+    return torch.cat(parts, -1).reshape(-1)
 
 
 def _ref_pack_f16(W, cols=None, kmajor=False):
@@ -128,11 +137,14 @@ def _ref_pack_f16(W, cols=None, kmajor=False):
             for j, (row, k) in enumerate(order):
                 blk[:, :, L, j] = Wv[:, row, :, k]
     if kmajor:
-        blk = blk.transpose(0, 1).contiguous()
-    return blk.view(torch.uint8).reshape(-1)
+        return blk.transpose(0, 1).contiguous().view(torch.uint8).reshape(-1)
+    ng = ns // 4
+    n0 = ng // 2                                         # [rt, step, ...] -> [half, rt, groups, 4 steps, ...]
+    blk = blk.view(n_rt, ng, 4, 32, 8)
+    return torch.cat([blk[:, :n0].reshape(-1), blk[:, n0:].reshape(-1)]).view(torch.uint8).reshape(-1)
 
 
-@pytest.mark.parametrize("E,I,d", [(3, 64, 256), (2, 128, 128), (1, 512, 2048)])
+@pytest.mark.parametrize("E,I,d", [(3, 64, 256), (2, 128, 128), (1, 512, 2048), (2, 64, 192)])
 def test_pack_q4_gate_up_layout(E, I, d):
     gate = inputs.int4_stack(5, 1, 1, E, I, d)
     up = inputs.int4_stack(5, 1, 2, E, I, d)
@@ -140,14 +152,14 @@ def test_pack_q4_gate_up_layout(E, I, d):
     assert torch.equal(got, _ref_pack_gate_up(gate, up))
 
 
-@pytest.mark.parametrize("E,out,inp", [(3, 48, 256), (2, 20, 128), (1, 2048, 512)])
+@pytest.mark.parametrize("E,out,inp", [(3, 48, 256), (2, 20, 128), (1, 2048, 512), (2, 80, 192)])
 def test_pack_q4_down_layout(E, out, inp):
     trip = inputs.int4_stack(6, 1, 3, E, out, inp)
     got = binding.pack_q4_down(tuple(t.to(DEV) for t in trip)).cpu()
     assert torch.equal(got, _ref_pack_down(trip))
 
 
-@pytest.mark.parametrize("out,inp,cols", [(48, 256, None), (4, 128, None), (64, 288, 256)])
+@pytest.mark.parametrize("out,inp,cols", [(48, 256, None), (4, 128, None), (64, 288, 256), (32, 192, None)])
 @pytest.mark.parametrize("kmajor", [False, True])
 def test_pack_f16_layout(out, inp, cols, kmajor):
     W = (torch.randn(out, inp, generator=torch.Generator().manual_seed(3))).half()

@@ -57,6 +57,6 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     # d = 4096 with 512 experts at B = 4 needs 256 + 8 B d + 16 B E + 256 = 164,352
     # bytes of scratch, more than the fixed array holds
     moe = binding.MoeDesc(4096, 512, 8, 512, 512, 256, 256, None, None, None, 0)
-    assert binding.lib().edge0_workspace_bytes(1, 4, 4096, 512) - 160 * 1024 * 8 > 128 * 1024
+    assert binding.lib().edge0_workspace_bytes(1, 4, 4096, 512) - 160 * 4096 * 8 > 128 * 1024
     rc = lib.edge0_moe_int4_forward_noalloc(C.byref(moe), x, x, x, 4, x, None)
     assert rc == binding.EDGE0_EUNSUPPORTED

@@ -29,6 +29,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from int4_routed_expert_prerouter_gb300 import configs  # noqa: E402
@@ -192,7 +193,10 @@ def run_gpu(args, rank, world):
         binding.decode_step(dm, st, h_all[t], t)
         t += 1
         st.set_trace(False)
-        print_trace(st.read_trace(), torch.cuda.get_device_properties(dev).multi_processor_count)
+        tr = st.read_trace()
+        print_trace(tr, torch.cuda.get_device_properties(dev).multi_processor_count)
+        if args.trace_file:
+            np.savez_compressed(args.trace_file, consumer=tr[0].numpy(), producer=tr[1].numpy())
     # device-resident timed region: one event pair per launch for the kernel
     # duration, one pair around the region for the step time
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -437,6 +441,7 @@ def main():
     ap.add_argument("--experts", type=int, default=0, help="reduced case for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", action="store_true", help="print a per-phase split of one step")
+    ap.add_argument("--trace-file", default=None, help="with --trace: save the raw per-CTA trace (.npz)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -41,12 +41,12 @@
 namespace edge0 {
 
 constexpr int kMaxSegs = 4;        // expert runs in one pair's share of a layer
-constexpr int kMaxItems = 96;      // copy items of one CTA in one layer
-constexpr int kItemMax = 32768;    // bytes of one copy item
+constexpr int kMaxItems = 64;      // copy items of one CTA in one layer
+constexpr int kItemMax = 16384;    // bytes of one copy item (copies of 16 KB reach full HBM rate)
 constexpr int kSlots = 256;        // item barriers (>= 2 x kMaxItems)
 constexpr int kTables = 3;         // layer tables in flight
 constexpr int kMaxChunks = 4;      // 4-element chunks of [B, d] per consumer thread
-constexpr int kMaxD = 4096;
+constexpr int kMaxD = 2048;
 constexpr int kMinRing = 2 * kItemMax;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // bounded waits: 2 s
 
@@ -176,11 +176,23 @@ struct Item {
     int a, b, n;      // kind-specific position and count
 };
 
+// one K-group of down rows a segment touches: where its 16-row steps and scales
+// sit in the ring (offsets of row tile 0 of this CTA's half) and which act
+// quarters they multiply
+constexpr int kMaxDg = 12;
+struct DGroup {
+    int seg, nq, ql0;   // segment, steps, act quarter (in the pair's list) of the first step
+    int soff;           // ring offset of the scales
+    int qoff[4];        // ring offset of each step
+};
+
 struct LayerTab {
     int seq;          // layer index + 1 once published
     int k0, n;        // global index of the first item; items
     int p1, p2, p3;   // first item of P1 (gate/up), P2 (down), P3 (head); router items from 0
+    int ndg;          // down groups
     PairPlan pl;
+    DGroup dg[kMaxDg];
     Item it[kMaxItems];
 };
 
@@ -239,6 +251,7 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
     if (pl.over) return false;
     const Halves hv = halves(Sh.d, Sh.E, rank);
     ItemSink k{T, 0, lin, lin % ring, ring, true};
+    T->ndg = 0;
     const int ngh = hv.gh1 - hv.gh0, nrt = hv.rt1 - hv.rt0, ne = hv.e1 - hv.e0;
     const int r = Sh.r;
     // router units: this pair's share of (E row tiles) x (this rank's groups)
@@ -262,17 +275,33 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
         const int qper = kItemMax / qbytes > 0 ? kItemMax / qbytes : 1;
         for (int gg = g.q0 / 4; gg <= (g.q1 - 1) / 4; ++gg) {
             const int qa = g.q0 > 4 * gg ? g.q0 : 4 * gg, qb = g.q1 < 4 * gg + 4 ? g.q1 : 4 * gg + 4;
+            DGroup* D = nullptr;
+            if (T->ndg < kMaxDg) {
+                D = &T->dg[T->ndg++];
+                D->seg = s;
+                D->nq = qb - qa;
+                D->ql0 = g.qoff + qa - g.q0;
+            } else {
+                k.ok = false;
+            }
             // runs of steps (at most kItemMax bytes), the scales merged into the last
             // run when the group's steps and scales are adjacent and fit
             for (int q = qa; q < qb; q += qper) {
                 const int m = qb - q < qper ? qb - q : qper;
                 const bool last = q + m == qb;
+                const int n0 = k.n;
                 if (last && qb == 4 * gg + 4 && m * qbytes + sbytes <= kItemMax) {
                     push_item(k, IT_DQS, s, m * qbytes + sbytes, gg, q - 4 * gg, m);
+                    if (D && k.n > n0) D->soff = T->it[n0].off + m * qbytes;
                 } else {
                     push_item(k, IT_DQ, s, m * qbytes, gg, q - 4 * gg, m);
-                    if (last) push_item(k, IT_DSC, s, sbytes, gg, 0, nrt);
+                    if (last) {
+                        push_item(k, IT_DSC, s, sbytes, gg, 0, nrt);
+                        if (D && k.n > n0 + 1) D->soff = T->it[n0 + 1].off;
+                    }
                 }
+                if (D && k.n > n0)
+                    for (int qi = 0; qi < m; ++qi) D->qoff[q - qa + qi] = T->it[n0].off + qi * qbytes;
             }
         }
         if (g.slot < 0 && Sh.lora) {
@@ -867,6 +896,7 @@ __device__ __forceinline__ void q4_run(const char* base, int a, int b, int gl0,
     const int B = prg().B;
     const XFrag xf = xfrag();
     const float* xs = SM<float>(c.pl.xsum);
+#pragma unroll 2
     for (int j = a; j < b; ++j) {
         const char* unit = base + (long long)j * kQ4Unit;
         const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
@@ -1187,8 +1217,7 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
         if (!ok && tid == 0) raise_error(EDGE0_EINVAL);
         ok = ok && wait_item(T, ibg) && wait_item(T, ibu) && wait_item(T, iadt);
     }
-    for (int i = tid; i < pl.n_q * B * 2 * 4 * 4; i += kConsumerThreads) af[i] = __float2half_rn(0.f);
-    for (int i = tid; i < pl.n_q * B; i += kConsumerThreads) qsum[i] = 0.f;
+    // af and qsum were cleared at the start of the layer
     ok = !cbar_or(!ok);
     stamp((l << 8) | 10);
     for (int i = tid; ok && i < pl.n_hr * 8 * B; i += kConsumerThreads) {
@@ -1244,7 +1273,11 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
     return !cbar_or(!ok);
 }
 
-// P2: down rows of this CTA's half of d over the pair's act quarters -> y
+// P2: down rows of this CTA's half of d over the pair's act quarters -> y.  Each
+// warp owns up to kMaxRtw consecutive row tiles and walks the layer's down groups
+// once: the group's act fragments are loaded once, then every row tile of the
+// warp runs its own accumulator chain.
+constexpr int kMaxRtw = 4;   // row tiles of one warp (d <= kMaxD = 2048)
 __device__ bool phase2(int l, const LayerTab* T, bool lora) {
     Ctx& c = ctx();
     const Prog& p = prg();
@@ -1259,101 +1292,95 @@ __device__ bool phase2(int l, const LayerTab* T, bool lora) {
         const uint2* afr = SM<uint2>(c.pl.af);
         const float* qsum = SM<float>(c.pl.qsum);
         const float* vlo = SM<float>(c.pl.vlo);
+        const char* ring = g_smem + c.pl.ring;
         const int tok = g >> 1, part = g & 1;
         const bool blive = tok < B;
         const int nrt = c.hv.rt1 - c.hv.rt0;
-        // per-segment token weights (lane's token t)
-        float wt[kMaxSegs];
-        for (int s = 0; s < pl.nseg; ++s) {
-            const Seg& sg = pl.seg[s];
-            wt[s] = 0.f;
-            if (t >= B || !seg_live(l, sg)) continue;
-            if (sg.slot < 0) { wt[s] = 1.f; continue; }
-            const int e = dist_of(l)[sg.slot];
-            for (int k = 0; k < K; ++k)
-                if (ids_of(l)[t * K + k] == e) wt[s] += w_of(l)[t * K + k];
-        }
-        // LoRA down rows
-        const int ibd = (lora && pl.has_sh) ? find_item(T, T->p2, T->p3, IT_BD, 0) : -1;
-        int w0, w1;
-        split_range(nrt, kConsumerWarps, wid, &w0, &w1);
-        float* y = y_buf(c.par, Ly.sidx);
-        for (int i = w0; i < w1; ++i) {
-            float y0 = 0.f, y1 = 0.f;
-            for (int s = 0; s < pl.nseg; ++s) {
-                const Seg& sg = pl.seg[s];
-                if (!seg_live(l, sg)) continue;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                int gcur = -1;
-                uint2 sc = make_uint2(0u, 0u);
-                auto epilogue = [&]() {
-                    if (gcur < 0) return;
-                    const int qa = sg.q0 > 4 * gcur ? sg.q0 : 4 * gcur;
-                    const int qb = sg.q1 < 4 * gcur + 4 ? sg.q1 : 4 * gcur + 4;
-                    float qs = 0.f;
-                    if (t < B)
-                        for (int Q = qa; Q < qb; ++Q) qs += qsum[(sg.qoff + Q - sg.q0) * B + t];
-                    const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);
-                    const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);
-                    y0 += wt[s] * (__low2float(s0) * kTwo24 * (acc[0] + acc[1] * kLoInv) + __high2float(s0) * qs);
-                    y1 += wt[s] * (__low2float(s1) * (kTwo24 / 16.0f) * (acc[2] + acc[3] * kLoInv) +
-                                   __high2float(s1) * qs);
-                };
-                for (int j = T->p2; j < T->p3; ++j) {
-                    const Item& it = T->it[j];
-                    if (it.seg != s) continue;
-                    if (it.kind == IT_DQ || it.kind == IT_DQS) {
-                        // steps b .. b + n - 1 of group a over this CTA's row tiles
-                        if (gcur != it.a) {
-                            gcur = it.a;
-                            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-                        }
-                        for (int qi = 0; qi < it.n; ++qi) {
+        const int per = (nrt + kConsumerWarps - 1) / kConsumerWarps;
+        const int i0 = wid * per;
+        float y0[kMaxRtw], y1[kMaxRtw];
+#pragma unroll
+        for (int q = 0; q < kMaxRtw; ++q) y0[q] = y1[q] = 0.f;
+        for (int di = 0; di < T->ndg; ++di) {
+            const DGroup D = T->dg[di];
+            const Seg& sg = pl.seg[D.seg];
+            if (!seg_live(l, sg)) continue;
+            // weight of the lane's token t for this segment's expert
+            float w = 0.f;
+            if (t < B) {
+                if (sg.slot < 0) {
+                    w = 1.f;
+                } else {
+                    const int e = dist_of(l)[sg.slot];
+                    for (int k = 0; k < K; ++k)
+                        if (ids_of(l)[t * K + k] == e) w += w_of(l)[t * K + k];
+                }
+            }
+            uint2 bb[4];
+            float qs = 0.f;
+#pragma unroll
+            for (int qi = 0; qi < 4; ++qi) {
+                bb[qi] = make_uint2(0u, 0u);
+                if (qi < D.nq) {
+                    if (blive) bb[qi] = afr[(((D.ql0 + qi) * B + tok) * 2 + part) * 4 + t];
+                    if (t < B) qs += qsum[(D.ql0 + qi) * B + t];
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < kMaxRtw; ++rr) {
+                const int i = i0 + rr;
+                if (rr < per && i < nrt) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int qi = 0; qi < 4; ++qi) {
+                        if (qi < D.nq) {
                             const uint32_t wq = *reinterpret_cast<const uint32_t*>(
-                                ring_at(it) + (qi * nrt + i) * kQ4Quarter + 4 * lane);
-                            const int Ql = sg.qoff + 4 * gcur + it.b + qi - sg.q0;
-                            uint2 bb = make_uint2(0u, 0u);
-                            if (blive) bb = afr[((Ql * B + tok) * 2 + part) * 4 + t];
+                                ring + D.qoff[qi] + i * kQ4Quarter + 4 * lane);
                             uint32_t A[4];
                             q4_masks(wq, A);
-                            mma_16816(acc, A, bb.x, bb.y);
+                            mma_16816(acc, A, bb[qi].x, bb[qi].y);
                         }
-                        if (it.kind == IT_DQS) {
-                            sc = *reinterpret_cast<const uint2*>(ring_at(it) + it.n * nrt * kQ4Quarter +
-                                                                 i * kQ4Scales + 8 * g);
-                            epilogue();
-                            gcur = -1;
-                        }
-                    } else if (it.kind == IT_DSC) {
-                        sc = *reinterpret_cast<const uint2*>(ring_at(it) + i * kQ4Scales + 8 * g);
-                        epilogue();
-                        gcur = -1;
                     }
+                    const uint2 sc = *reinterpret_cast<const uint2*>(ring + D.soff + i * kQ4Scales + 8 * g);
+                    const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);
+                    const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);
+                    y0[rr] += w * (__low2float(s0) * kTwo24 * (acc[0] + acc[1] * kLoInv) + __high2float(s0) * qs);
+                    y1[rr] += w * (__low2float(s1) * (kTwo24 / 16.0f) * (acc[2] + acc[3] * kLoInv) +
+                                   __high2float(s1) * qs);
                 }
             }
-            const int row = (c.hv.rt0 + i) * kRowTile + g;
-            if (ibd >= 0 && t < B) {
-                // rows of this CTA's half are split over consecutive BD items
-                const int per = kItemMax / (r * 2);
-                const int rel = row - c.hv.rt0 * kRowTile;
-                const __half* bd0 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + rel / per])) + (rel % per) * r;
-                const __half* bd1 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + (rel + 8) / per])) + ((rel + 8) % per) * r;
-                float d0 = 0.f, d1 = 0.f;
-                for (int q = 0; q < r; ++q) {
-                    d0 += __half2float(bd0[q]) * vlo[q * B + t];
-                    d1 += __half2float(bd1[q]) * vlo[q * B + t];
+        }
+        // LoRA down rows (pairs with shared rows), then one vector reduction per 4 rows
+        const int ibd = (lora && pl.has_sh) ? find_item(T, T->p2, T->p3, IT_BD, 0) : -1;
+        const int bper = kItemMax / (r * 2);
+        float* y = y_buf(c.par, Ly.sidx);
+#pragma unroll
+        for (int rr = 0; rr < kMaxRtw; ++rr) {
+            const int i = i0 + rr;
+            if (rr < per && i < nrt) {
+                const int row = (c.hv.rt0 + i) * kRowTile + g;
+                float a0 = y0[rr], a1v = y1[rr];
+                if (ibd >= 0 && t < B) {
+                    const int rel = row - c.hv.rt0 * kRowTile;
+                    const __half* bd0 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + rel / bper])) + (rel % bper) * r;
+                    const __half* bd1 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + (rel + 8) / bper])) + ((rel + 8) % bper) * r;
+                    float d0 = 0.f, d1 = 0.f;
+                    for (int q = 0; q < r; ++q) {
+                        d0 += __half2float(bd0[q]) * vlo[q * B + t];
+                        d1 += __half2float(bd1[q]) * vlo[q * B + t];
+                    }
+                    a0 += Ly.lora_scale * d0;
+                    a1v += Ly.lora_scale * d1;
                 }
-                y0 += Ly.lora_scale * d0;
-                y1 += Ly.lora_scale * d1;
-            }
-            // rows g..g+3 of lanes with g % 4 == 0 as one vector reduction
-            const float a1 = __shfl_down_sync(0xffffffffu, y0, 4), a2 = __shfl_down_sync(0xffffffffu, y0, 8),
-                        a3 = __shfl_down_sync(0xffffffffu, y0, 12);
-            const float b1 = __shfl_down_sync(0xffffffffu, y1, 4), b2 = __shfl_down_sync(0xffffffffu, y1, 8),
-                        b3 = __shfl_down_sync(0xffffffffu, y1, 12);
-            if (t < B && (g & 3) == 0) {
-                red_add_v4_f32(y + (long long)t * d + row, y0, a1, a2, a3);
-                red_add_v4_f32(y + (long long)t * d + row + 8, y1, b1, b2, b3);
+                // rows g..g+3 of lanes with g % 4 == 0 as one vector reduction
+                const float u1 = __shfl_down_sync(0xffffffffu, a0, 4), u2 = __shfl_down_sync(0xffffffffu, a0, 8),
+                            u3 = __shfl_down_sync(0xffffffffu, a0, 12);
+                const float v1 = __shfl_down_sync(0xffffffffu, a1v, 4), v2 = __shfl_down_sync(0xffffffffu, a1v, 8),
+                            v3 = __shfl_down_sync(0xffffffffu, a1v, 12);
+                if (t < B && (g & 3) == 0) {
+                    red_add_v4_f32(y + (long long)t * d + row, a0, u1, u2, u3);
+                    red_add_v4_f32(y + (long long)t * d + row + 8, a1v, v1, v2, v3);
+                }
             }
         }
     }
@@ -1547,6 +1574,13 @@ __device__ void consumer() {
         const bool router = has_router_phase(p, l, c.step);
         const Shape Sh = layer_shape(p, l, router);
         for (int q = tid; q < (T->pl.n_hr * 16 + 32) * B; q += kConsumerThreads) part[q] = 0.f;
+        {
+            // act fragments and quarter sums of this layer start at zero (partial quarters)
+            uint32_t* af = SM<uint32_t>(c.pl.af);
+            float* qsum = SM<float>(c.pl.qsum);
+            for (int q = tid; q < T->pl.n_q * B * 2 * 4 * 2; q += kConsumerThreads) af[q] = 0u;
+            for (int q = tid; q < T->pl.n_q * B; q += kConsumerThreads) qsum[q] = 0.f;
+        }
         // ---------------- input x
         if (p.mode == MODE_DECODE && l > 0)
             if (!bar_wait(bar_target)) break;

@@ -80,6 +80,8 @@ struct PairPlan {
     int has_sh;   // the pair owns shared-expert rows
     int hd0, hd1; // head tasks
     int ru0, ru1; // router units (in this rank's half of d)
+    int la0, la1; // LoRA A units (A_gate then A_up groups of this rank's half of d)
+    int bd0, bd1; // LoRA B_down row tiles (of this rank's half of the output rows)
 };
 
 // [n i / parts, n (i + 1) / parts): 32-bit arithmetic (n * parts < 2^31 for
@@ -96,17 +98,25 @@ struct Shape {
     int ps;                           // pairs that own shared-expert rows
 };
 
-__host__ __device__ inline int shared_pairs(int P, int n_sh, int n_rt, bool lora) {
+// The shared expert's LoRA runs once per layer, split over the pairs that own
+// shared rows (not repeated by each): they compute A_gate x and A_up x (split over
+// d) into a small global accumulator, wait for it to be complete before their act,
+// add v = A_down act of their rows into a second one, and after their down rows
+// apply B_down (split over the output rows) to the complete v.  Head tasks go to
+// the other pairs.
+
+__host__ __device__ inline int shared_pairs(int P, int n_sh, int n_rt, bool lora, bool head) {
     if (n_sh <= 0) return 0;
     if (n_rt <= 0) return P;
     // cost in int4-unit equivalents per CTA: an hr is 16 gate/up units + half a
-    // 16-row down slice over half of d; LoRA adds A_gate, A_up over half of d
+    // 16-row down slice over half of d; shared pairs carry the LoRA terms and
+    // their waits, routed pairs the head tasks
     int best = 0x7fffffff, pick = 1;
     for (int ps = 1; ps < P; ++ps) {
-        const int cs = ceil_div(n_sh, ps) * 24 + (lora ? 40 : 0);
-        const int cr = ceil_div(n_rt, P - ps) * 24;
+        const int cs = ceil_div(n_sh, ps) * 24 + (lora ? 16 : 0);
+        const int cr = ceil_div(n_rt, P - ps) * 24 + (head ? 16 : 0);
         const int cmax = cs > cr ? cs : cr;
-        if (cmax < best) { best = cmax; pick = ps; }
+        if (cmax <= best) { best = cmax; pick = ps; }   // ties: more shared pairs
     }
     return pick;
 }
@@ -122,6 +132,8 @@ __host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int r
     pp.has_sh = 0;
     pp.hd0 = pp.hd1 = 0;
     pp.ru0 = pp.ru1 = 0;
+    pp.la0 = pp.la1 = 0;
+    pp.bd0 = pp.bd1 = 0;
     const int hpe = S.I / kHalfRow;
     const int n_sh = S.shared ? S.Is / kHalfRow : 0;
     const int n_rt = S.n_slots * hpe;
@@ -155,7 +167,16 @@ __host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int r
             a = end;
         }
     }
-    if (S.head) split_range(S.H / kRowTile + S.E / kRowTile, P, pair, &pp.hd0, &pp.hd1);
+    // head tasks: routed pairs (all pairs if there are none)
+    const int Pr = P > Ps ? P - Ps : P, ir = P > Ps ? pair - Ps : pair;
+    if (ir >= 0 && S.head) split_range(S.H / kRowTile + S.E / kRowTile, Pr, ir, &pp.hd0, &pp.hd1);
+    // LoRA (implies a shared expert, so Ps >= 1): the shared pairs
+    if (S.lora && pair < Ps) {
+        const int n_gd = S.d / kGroup, ngh = half_hi(n_gd, rank) - half_lo(n_gd, rank);
+        const int n_rtd = S.d / kRowTile, nrt = half_hi(n_rtd, rank) - half_lo(n_rtd, rank);
+        split_range(2 * ngh, Ps, pair, &pp.la0, &pp.la1);
+        split_range(nrt, Ps, pair, &pp.bd0, &pp.bd1);
+    }
     if (S.router) {
         const int n_gd = S.d / kGroup;
         const int ngh = half_hi(n_gd, rank) - half_lo(n_gd, rank);
@@ -163,9 +184,11 @@ __host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int r
     }
 }
 
+// CTAs that do head work in a layer (the head's arrival-counter target)
 __host__ __device__ inline int head_ctas(const Shape& S, int P) {
     const int n_ht = S.H / kRowTile + S.E / kRowTile;
-    return 2 * (n_ht < P ? n_ht : P);
+    const int Pr = P > S.ps ? P - S.ps : P;
+    return 2 * (n_ht < Pr ? n_ht : Pr);
 }
 
 // one copy of a contiguous global region into the ring
@@ -257,15 +280,24 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
     // router units: this pair's share of (E row tiles) x (this rank's groups)
     push_units(k, IT_ROUTER, 0, 0, pl.ru0, pl.ru1 - pl.ru0, kF16Unit);
     T->p1 = k.n;
+    // LoRA A units first (every shared pair waits for the sums of all of them):
+    // A_gate groups [la0, la1) n [0, ngh), then A_up groups
+    if (pl.la0 < ngh && pl.la0 < pl.la1) {
+        const int e = pl.la1 < ngh ? pl.la1 : ngh;
+        push_units(k, IT_LA, 0, 0, pl.la0, e - pl.la0, kF16Unit);
+    }
+    if (pl.la1 > ngh) {
+        const int b0 = pl.la0 > ngh ? pl.la0 : ngh;
+        push_units(k, IT_LU, 0, 0, b0 - ngh, pl.la1 - b0, kF16Unit);
+    }
     for (int s = 0; s < pl.nseg; ++s) {
         const Seg& g = pl.seg[s];
         push_units(k, IT_GU, s, 0, g.hr0 * ngh, (g.hr1 - g.hr0) * ngh, kQ4Unit);
         if (g.slot < 0 && Sh.lora) {
-            push_units(k, IT_LA, s, 0, 0, ngh, kF16Unit);
-            push_units(k, IT_LU, s, 0, 0, ngh, kF16Unit);
             const int rows = (g.hr1 - g.hr0) * kHalfRow;
             push_item(k, IT_BG, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
             push_item(k, IT_BU, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            push_item(k, IT_ADT, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
         }
     }
     T->p2 = k.n;
@@ -304,14 +336,13 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
                     for (int qi = 0; qi < m; ++qi) D->qoff[q - qa + qi] = T->it[n0].off + qi * qbytes;
             }
         }
-        if (g.slot < 0 && Sh.lora) {
-            const int rows = (g.hr1 - g.hr0) * kHalfRow;
-            push_item(k, IT_ADT, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
-            const int per = kItemMax / (r * 2);
-            for (int row = hv.rt0 * kRowTile; row < hv.rt1 * kRowTile; row += per) {
-                const int m = hv.rt1 * kRowTile - row < per ? hv.rt1 * kRowTile - row : per;
-                push_item(k, IT_BD, s, m * r * 2, row, 0, m);
-            }
+    }
+    // LoRA B_down rows: row tiles [bd0, bd1) of this rank's half
+    {
+        const int per = kItemMax / (r * 2);
+        for (int row = (hv.rt0 + pl.bd0) * kRowTile; row < (hv.rt0 + pl.bd1) * kRowTile; row += per) {
+            const int m = (hv.rt0 + pl.bd1) * kRowTile - row < per ? (hv.rt0 + pl.bd1) * kRowTile - row : per;
+            push_item(k, IT_BD, 0, m * r * 2, row, 0, m);
         }
     }
     T->p3 = k.n;
@@ -342,7 +373,7 @@ struct Plan {
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 
-__host__ __device__ inline int msg_floats(const Prog& p) { return (p.hr_max * 16 + 32) * p.B; }
+__host__ __device__ inline int msg_floats(const Prog& p) { return p.hr_max * 16 * p.B; }
 
 // base: bytes at the start of shared memory taken by the parameter copy and the context
 __host__ __device__ inline Plan make_plan(const Prog& p, int base) {
@@ -364,7 +395,7 @@ __host__ __device__ inline Plan make_plan(const Prog& p, int base) {
     s.act32 = o;  o += al16(p.hr_max * 8 * B * 4);
     s.af = o;     o += al16(p.q_max * B * 2 * 4 * 8);
     s.qsum = o;   o += al16(p.q_max * B * 4);
-    s.vlo = o;    o += al16(16 * B * 4);
+    s.vlo = o;    o += al16(32 * B * 4);
     s.zpart = o;  o += al16(16 * B * 4);
     s.zrecv = o;  o += al16(2 * 16 * B * 4);
     s.gf = o;     o += al16(B * 2 * 4 * 8);
@@ -494,9 +525,15 @@ __device__ __forceinline__ float* logh_buf(int par, int sidx) {
     const Ctx& c = ctx();
     return ws_f(c.ws.logh) + ((long long)par * prg().Ls + sidx) * prg().B * prg().E;
 }
-__device__ __forceinline__ unsigned* cnt_buf(int par, int sidx) {
+// the LoRA sums of a layer: A_gate x at [q B + b], A_up x at [(16 + q) B + b],
+// v = A_down act at [(32 + q) B + b]
+__device__ __forceinline__ float* lora_buf(int par, int sidx) {
     const Ctx& c = ctx();
-    return reinterpret_cast<unsigned*>(prg().ws + c.ws.cnt) + par * prg().Ls + sidx;
+    return ws_f(c.ws.lora) + ((long long)par * prg().Ls + sidx) * prg().B * kLoraAcc;
+}
+__device__ __forceinline__ unsigned* cnt_buf(int par, int sidx, int which) {
+    const Ctx& c = ctx();
+    return reinterpret_cast<unsigned*>(prg().ws + c.ws.cnt) + (par * prg().Ls + sidx) * kLayerCounters + which;
 }
 
 // optional trace: (tag, globaltimer) pairs per CTA, written by consumer thread 0
@@ -542,7 +579,7 @@ __host__ __device__ inline Shape layer_shape(const Prog& p, int l, bool router) 
     S.lora = (S.shared && p.mode == MODE_DECODE && (Ly.flags & LF_LORA)) ? 1 : 0;
     S.head = (p.mode == MODE_HEAD || (p.mode == MODE_DECODE && (Ly.flags & LF_HEAD))) ? 1 : 0;
     S.router = router ? 1 : 0;
-    S.ps = S.shared ? p.ps[S.lora] : 0;
+    S.ps = S.shared ? p.ps[S.lora + 2 * S.head] : 0;
     return S;
 }
 
@@ -1149,36 +1186,57 @@ __device__ __noinline__ void route_layer(int l) {
     cbar();
 }
 
-// P1: partial gate/up (+ LoRA A x) sums of the pair's rows over this CTA's half of d
+// P1: partial gate/up sums of the pair's rows over this CTA's half of d; LoRA A
+// units go straight into the layer's global sums, each warp counting the units it
+// finished
 __device__ bool phase1(int l, const LayerTab* T) {
     Ctx& c = ctx();
-    const int B = prg().B;
+    const Prog& p = prg();
+    const int B = p.B;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     float* part = SM<float>(c.pl.part);
-    const int nlp = T->pl.n_hr * 16 * B;
     return warp_units(T, T->p1, T->p2, [&](const Item& it, int a, int b) {
+        if (it.kind == IT_LA || it.kind == IT_LU) {
+            float* la = lora_buf(c.par, p.layers[l].sidx) + (it.kind == IT_LA ? 0 : 16 * B);
+            tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                f16_run(ring_at(it), j0, j1, gl0, acc);
+                if (t < B) {
+                    red_add_f32(la + g * B + t, acc[0]);
+                    red_add_f32(la + (g + 8) * B + t, acc[2]);
+                }
+            });
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atom_acq_rel_add_u32(cnt_buf(c.par, p.layers[l].sidx, CNT_LORA_A), (unsigned)(b - a));
+            return;
+        }
         const Seg& sg = T->pl.seg[it.seg];
         if (!seg_live(l, sg)) return;
         tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
-            if (it.kind == IT_GU) {
-                float r0 = 0.f, r1 = 0.f;
-                q4_run(ring_at(it), j0, j1, gl0, r0, r1);
-                const int hl = sg.hoff + tile - sg.hr0;
-                if (t < B) {
-                    atomicAdd(&part[(hl * 16 + g) * B + t], r0);
-                    atomicAdd(&part[(hl * 16 + 8 + g) * B + t], r1);
-                }
-            } else {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                f16_run(ring_at(it), j0, j1, gl0, acc);
-                const int m = it.kind == IT_LA ? 0 : 1;
-                if (t < B) {
-                    atomicAdd(&part[nlp + (m * 16 + g) * B + t], acc[0]);
-                    atomicAdd(&part[nlp + (m * 16 + 8 + g) * B + t], acc[2]);
-                }
+            float r0 = 0.f, r1 = 0.f;
+            q4_run(ring_at(it), j0, j1, gl0, r0, r1);
+            const int hl = sg.hoff + tile - sg.hr0;
+            if (t < B) {
+                atomicAdd(&part[(hl * 16 + g) * B + t], r0);
+                atomicAdd(&part[(hl * 16 + 8 + g) * B + t], r1);
             }
         });
     }, (l << 8) | 8);
+}
+
+// bounded wait (one thread) until a layer counter reaches `want`; false on
+// abort or timeout
+__device__ __noinline__ bool wait_count(const unsigned* cnt, unsigned want) {
+    if (ld_acquire_u32(cnt) >= want) return true;
+    const unsigned long long t0 = now_ns();
+    for (unsigned it = 0; ld_acquire_u32(cnt) < want; ++it) {
+        if ((it & 15) == 15) {
+            if (should_abort()) return false;
+            if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); return false; }
+        }
+    }
+    return true;
 }
 
 // index of the first item of `kind` for segment s in [ia, ib), or -1
@@ -1190,8 +1248,9 @@ __device__ __forceinline__ int find_item(const LayerTab* T, int ia, int ib, int 
 
 // act = silu(gate) * up of all the pair's rows (partials of both CTAs, LoRA B
 // terms for shared rows) -> hi/lo B fragments per 16-row quarter and their sums;
-// v = A_down act for the shared rows (LoRA).  Every consumer thread runs every
-// barrier here; the result is CTA-uniform.
+// for shared rows with LoRA, this CTA's half of the r entries of A_down act is
+// added to the layer's v.  Every consumer thread runs every barrier here; the
+// result is CTA-uniform.
 __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
     Ctx& c = ctx();
     const Prog& p = prg();
@@ -1203,8 +1262,8 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
     float* act32 = SM<float>(c.pl.act32);
     __half* af = SM<__half>(c.pl.af);
     float* qsum = SM<float>(c.pl.qsum);
-    float* vlo = SM<float>(c.pl.vlo);
-    const int nlp = pl.n_hr * 16 * B;
+    float* lsum = SM<float>(c.pl.vlo);   // A_gate x, A_up x of the layer (2 x 16 x B)
+    float* lora_g = lora_buf(c.par, Ly.sidx);
     // LoRA items of the shared segment (segment 0 of a pair that owns shared rows)
     int ibg = -1, ibu = -1, iadt = -1, ssh = -1;
     bool ok = true;
@@ -1212,10 +1271,14 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
         ssh = 0;
         ibg = find_item(T, T->p1, T->p2, IT_BG, ssh);
         ibu = find_item(T, T->p1, T->p2, IT_BU, ssh);
-        iadt = find_item(T, T->p2, T->p3, IT_ADT, ssh);
+        iadt = find_item(T, T->p1, T->p2, IT_ADT, ssh);
         ok = ibg >= 0 && ibu >= 0 && iadt >= 0;
         if (!ok && tid == 0) raise_error(EDGE0_EINVAL);
         ok = ok && wait_item(T, ibg) && wait_item(T, ibu) && wait_item(T, iadt);
+        // every LoRA A unit of the layer has been added to the global sums
+        if (tid == 0 && ok) ok = wait_count(cnt_buf(c.par, Ly.sidx, CNT_LORA_A), 2u * (unsigned)(p.d / kGroup));
+        ok = !cbar_or(!ok);
+        for (int i = tid; ok && i < 32 * B; i += kConsumerThreads) lsum[i] = __ldcg(lora_g + i);
     }
     // af and qsum were cleared at the start of the layer
     ok = !cbar_or(!ok);
@@ -1236,8 +1299,8 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
                 const __half* bu = reinterpret_cast<const __half*>(ring_at(T->it[ibu])) + rl * r;
                 float dg = 0.f, du = 0.f;
                 for (int q = 0; q < r; ++q) {
-                    dg += __half2float(bg[q]) * (part[nlp + q * B + b] + recv[nlp + q * B + b]);
-                    du += __half2float(bu[q]) * (part[nlp + (16 + q) * B + b] + recv[nlp + (16 + q) * B + b]);
+                    dg += __half2float(bg[q]) * lsum[q * B + b];
+                    du += __half2float(bu[q]) * lsum[(16 + q) * B + b];
                 }
                 gate += Ly.lora_scale * dg;
                 up += Ly.lora_scale * du;
@@ -1256,16 +1319,21 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
     cbar();
     stamp((l << 8) | 11);
     if (ok && ssh >= 0) {
-        // v[q][b] = sum over the pair's shared act rows of A_down[q][row] act[row][b]
+        // v[q][b] += sum over the pair's shared act rows of A_down[q][row] act[row][b],
+        // q in this CTA's half of [0, r); then count this CTA's shared rows
         const Seg& sg = pl.seg[ssh];
         const __half* adt = reinterpret_cast<const __half*>(ring_at(T->it[iadt]));
         const int rows = (sg.hr1 - sg.hr0) * kHalfRow;
-        for (int i = tid; i < r * B; i += kConsumerThreads) {
-            const int q = i / B, b = i % B;
+        const int q0 = c.rank ? r / 2 : 0, q1 = c.rank ? r : r / 2;
+        for (int i = tid; i < (q1 - q0) * B; i += kConsumerThreads) {
+            const int q = q0 + i / B, b = i % B;
             float v = 0.f;
             for (int j = 0; j < rows; ++j) v += __half2float(adt[j * r + q]) * act32[(sg.hoff * 8 + j) * B + b];
-            vlo[q * B + b] = v;
+            red_add_f32(lora_g + (32 + q) * B + b, v);
         }
+        __threadfence();
+        cbar();
+        if (tid == 0) atom_acq_rel_add_u32(cnt_buf(c.par, Ly.sidx, CNT_LORA_V), (unsigned)(sg.hr1 - sg.hr0));
     }
     // the non-unit P1 items (LoRA B rows of gate/up) are no longer needed
     for (int i = T->p1; i < T->p2; ++i)
@@ -1291,7 +1359,6 @@ __device__ bool phase2(int l, const LayerTab* T, bool lora) {
     if (ok && pl.n_hr > 0) {
         const uint2* afr = SM<uint2>(c.pl.af);
         const float* qsum = SM<float>(c.pl.qsum);
-        const float* vlo = SM<float>(c.pl.vlo);
         const char* ring = g_smem + c.pl.ring;
         const int tok = g >> 1, part = g & 1;
         const bool blive = tok < B;
@@ -1350,28 +1417,14 @@ __device__ bool phase2(int l, const LayerTab* T, bool lora) {
                 }
             }
         }
-        // LoRA down rows (pairs with shared rows), then one vector reduction per 4 rows
-        const int ibd = (lora && pl.has_sh) ? find_item(T, T->p2, T->p3, IT_BD, 0) : -1;
-        const int bper = kItemMax / (r * 2);
+        // one vector reduction per 4 rows
         float* y = y_buf(c.par, Ly.sidx);
 #pragma unroll
         for (int rr = 0; rr < kMaxRtw; ++rr) {
             const int i = i0 + rr;
             if (rr < per && i < nrt) {
                 const int row = (c.hv.rt0 + i) * kRowTile + g;
-                float a0 = y0[rr], a1v = y1[rr];
-                if (ibd >= 0 && t < B) {
-                    const int rel = row - c.hv.rt0 * kRowTile;
-                    const __half* bd0 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + rel / bper])) + (rel % bper) * r;
-                    const __half* bd1 = reinterpret_cast<const __half*>(ring_at(T->it[ibd + (rel + 8) / bper])) + ((rel + 8) % bper) * r;
-                    float d0 = 0.f, d1 = 0.f;
-                    for (int q = 0; q < r; ++q) {
-                        d0 += __half2float(bd0[q]) * vlo[q * B + t];
-                        d1 += __half2float(bd1[q]) * vlo[q * B + t];
-                    }
-                    a0 += Ly.lora_scale * d0;
-                    a1v += Ly.lora_scale * d1;
-                }
+                const float a0 = y0[rr], a1v = y1[rr];
                 // rows g..g+3 of lanes with g % 4 == 0 as one vector reduction
                 const float u1 = __shfl_down_sync(0xffffffffu, a0, 4), u2 = __shfl_down_sync(0xffffffffu, a0, 8),
                             u3 = __shfl_down_sync(0xffffffffu, a0, 12);
@@ -1385,6 +1438,31 @@ __device__ bool phase2(int l, const LayerTab* T, bool lora) {
         }
     }
     stamp((l << 8) | 12);
+    // LoRA B_down rows of this CTA, once v is complete:
+    // y[row] += scale * sum_q B_down[row][q] v[q]
+    const int ibd = lora ? find_item(T, T->p2, T->p3, IT_BD, 0) : -1;
+    if (ibd >= 0) {
+        float* vs = SM<float>(c.pl.vlo);
+        const int tid = threadIdx.x;
+        const int n_sh = p.Is / kHalfRow;
+        if (tid == 0 && ok) ok = wait_count(cnt_buf(c.par, Ly.sidx, CNT_LORA_V), 2u * (unsigned)n_sh);
+        ok = !cbar_or(!ok);
+        const float* vg = lora_buf(c.par, Ly.sidx) + 32 * B;
+        for (int i = tid; ok && i < r * B; i += kConsumerThreads) vs[i] = __ldcg(vg + i);
+        cbar();
+        float* y = y_buf(c.par, Ly.sidx);
+        for (int ii = ibd; ok && ii < T->p3; ++ii) {
+            const Item& it = T->it[ii];
+            if (it.kind != IT_BD) continue;
+            const __half* bd = reinterpret_cast<const __half*>(ring_at(it));
+            for (int i = tid; i < it.n * B; i += kConsumerThreads) {
+                const int j = i / B, b = i % B;
+                float s = 0.f;
+                for (int q = 0; q < r; ++q) s += __half2float(bd[j * r + q]) * vs[q * B + b];
+                red_add_f32(y + (long long)b * d + it.a + j, Ly.lora_scale * s);
+            }
+        }
+    }
     for (int i = T->p2; i < T->p3; ++i) release_item(T, i);
     return ok;
 }
@@ -1472,8 +1550,10 @@ __device__ bool phase3(int l, const LayerTab* T, uint32_t& xph) {
                     oh += __half2float(Ly.fc1_oh[(long long)(E + prv[bb * K + k]) * H + hrow]);
             }
             ok = !cbar_or(!ok || aborted());
+            stamp((l << 8) | 13);
             float* zr = zrecv + (xph & 1) * 16 * B;
             if (ok) ok = exchange(1, zpart, zr, 16 * B, xph);
+            stamp((l << 8) | 14);
             if (ok && tid < 16 * B) {
                 const float z = zpart[rr * B + bb] + zr[rr * B + bb] + oh;
                 const float gl = 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
@@ -1509,6 +1589,7 @@ __device__ bool phase3(int l, const LayerTab* T, uint32_t& xph) {
                 ++j;
             }
             ok = !cbar_or(!ok);
+            stamp((l << 8) | 15);
         } else {
             ok = warp_units(T, i, j, [&](const Item& it, int a, int b) {
                 tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
@@ -1531,6 +1612,7 @@ __device__ bool phase3(int l, const LayerTab* T, uint32_t& xph) {
                 red_add_f32(lg + bb * E + row, oh);
             }
             ok = !cbar_or(!ok);
+            stamp((l << 8) | 16);
         }
         i = j;
         if (!ok) break;   // uniform
@@ -1540,10 +1622,11 @@ __device__ bool phase3(int l, const LayerTab* T, uint32_t& xph) {
         cbar();
         const Shape Sh = layer_shape(p, l, false);
         if (tid == 0) {
-            const unsigned old = atom_acq_rel_add_u32(cnt_buf(c.par, Ly.sidx), 1u);
+            const unsigned old = atom_acq_rel_add_u32(cnt_buf(c.par, Ly.sidx, CNT_HEAD), 1u);
             c.ctl->last = old == (unsigned)(head_ctas(Sh, c.P) - 1);
         }
         cbar();
+        stamp((l << 8) | 17);
         if (c.ctl->last) head_topk(l);
     }
     return !cbar_or(!ok);
@@ -1573,7 +1656,7 @@ __device__ void consumer() {
         if (cbar_or(aborted())) break;
         const bool router = has_router_phase(p, l, c.step);
         const Shape Sh = layer_shape(p, l, router);
-        for (int q = tid; q < (T->pl.n_hr * 16 + 32) * B; q += kConsumerThreads) part[q] = 0.f;
+        for (int q = tid; q < T->pl.n_hr * 16 * B; q += kConsumerThreads) part[q] = 0.f;
         {
             // act fragments and quarter sums of this layer start at zero (partial quarters)
             uint32_t* af = SM<uint32_t>(c.pl.af);
@@ -1609,7 +1692,7 @@ __device__ void consumer() {
         if (cbar_or(!ok || aborted())) break;
         stamp((l << 8) | 3);
         if (T->pl.n_hr > 0) {
-            const int nmsg = (T->pl.n_hr * 16 + (Sh.lora && T->pl.has_sh ? 32 : 0)) * B;
+            const int nmsg = T->pl.n_hr * 16 * B;
             ok = exchange(0, part, SM<float>(c.pl.recv), nmsg, xph1);
             if (cbar_or(!ok)) break;
         }
@@ -1708,18 +1791,21 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     // clear the other step parity of this launch's layers for the next step
     {
         const int op = c.par ^ 1;
-        const long long per_y = (long long)p.B * p.d, per_l = (long long)p.B * p.E;
-        const long long tot = (long long)p.L * (per_y + 2 * per_l);
+        const long long per_y = (long long)p.B * p.d, per_l = (long long)p.B * p.E,
+                        per_a = (long long)p.B * kLoraAcc, per = per_y + 2 * per_l + per_a;
+        const long long tot = (long long)p.L * per;
         const long long a = tot * c.cta / c.nct, b = tot * (c.cta + 1) / c.nct;
         for (long long i = a + tid; i < b; i += kThreads) {
-            const long long l = i / (per_y + 2 * per_l), o = i % (per_y + 2 * per_l);
+            const long long l = i / per, o = i % per;
             const int sidx = p.layers[l].sidx;
             if (o < per_y) y_buf(op, sidx)[o] = 0.f;
             else if (o < per_y + per_l) logr_buf(op, sidx)[o - per_y] = 0.f;
-            else logh_buf(op, sidx)[o - per_y - per_l] = 0.f;
+            else if (o < per_y + 2 * per_l) logh_buf(op, sidx)[o - per_y - per_l] = 0.f;
+            else lora_buf(op, sidx)[o - per_y - 2 * per_l] = 0.f;
         }
         if (c.cta == 0)
-            for (int l = tid; l < p.L; l += kThreads) *cnt_buf(op, p.layers[l].sidx) = 0u;
+            for (int i = tid; i < p.L * kLayerCounters; i += kThreads)
+                cnt_buf(op, p.layers[i / kLayerCounters].sidx, 0)[i % kLayerCounters] = 0u;
     }
     // routing known at launch: predictions (prerouted layers, step > 0) or inputs;
     // previous-token ids of head layers
@@ -1833,7 +1919,7 @@ int engine_grid(int* nct) {
 // combinations) and the ring that fits next to the fixed buffers.
 struct Derived {
     int mode, B, K, d, E, I, Is, H, r, nct, smem_max;
-    int rc, slots_max, ps0, ps1, hr_max, q_max, ring_bytes, smem;
+    int rc, slots_max, ps[4], hr_max, q_max, ring_bytes, smem;
 };
 
 static int derive(Derived& D) {
@@ -1851,8 +1937,8 @@ static int derive(Derived& D) {
     const int P = D.nct / kClusterCtas;
     // the plan's 32-bit splits: n * parts stays below 2^31
     if ((long long)(p.slots_max * (p.I / kHalfRow) + p.Is) * P >= (1LL << 31)) return EDGE0_EUNSUPPORTED;
-    p.ps[0] = shared_pairs(P, p.Is / kHalfRow, p.slots_max * (p.I / kHalfRow), false);
-    p.ps[1] = shared_pairs(P, p.Is / kHalfRow, p.slots_max * (p.I / kHalfRow), true);
+    for (int f = 0; f < 4; ++f)
+        p.ps[f] = shared_pairs(P, p.Is / kHalfRow, p.slots_max * (p.I / kHalfRow), f & 1, f & 2);
     p.hr_max = 1;
     p.q_max = 1;
     LayerTab T;   // scratch on the stack: the allocation-free entry point comes here too
@@ -1890,8 +1976,7 @@ static int derive(Derived& D) {
         }
     }
     D.slots_max = p.slots_max;
-    D.ps0 = p.ps[0];
-    D.ps1 = p.ps[1];
+    for (int f = 0; f < 4; ++f) D.ps[f] = p.ps[f];
     D.hr_max = p.hr_max;
     D.q_max = p.q_max;
     D.ring_bytes = p.ring_bytes;
@@ -1931,8 +2016,7 @@ int engine_check(Prog& p, int nct, int smem_max, int* smem_bytes) {
     const Derived& d = g_derived[hit];
     if (d.rc) return d.rc;
     p.slots_max = d.slots_max;
-    p.ps[0] = d.ps0;
-    p.ps[1] = d.ps1;
+    for (int f = 0; f < 4; ++f) p.ps[f] = d.ps[f];
     p.hr_max = d.hr_max;
     p.q_max = d.q_max;
     p.ring_bytes = d.ring_bytes;

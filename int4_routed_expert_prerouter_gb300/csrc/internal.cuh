@@ -99,7 +99,7 @@ struct Prog {
     char* ws;
     // derived by engine_check for the launch's grid
     int slots_max;            // routed expert slots of a layer: min(B K, E)
-    int ps[2];                // CTA pairs that own shared-expert rows (without, with LoRA)
+    int ps[4];                // CTA pairs that own shared-expert rows (index: LoRA + 2 head)
     int hr_max, q_max;        // most half-row tiles / act quarters one CTA pair owns
     int ring_bytes;           // shared-memory ring of streamed weights
     LayerP layers[EDGE0_MAX_LAYERS];
@@ -124,8 +124,15 @@ constexpr int kTraceSlots = 4096;   // u64 words: (tag, globaltimer, clock) trip
 //   logits_r [2][Ls][B][E]  fp32  own-router logits
 //   logits_h [2][Ls][B][E]  fp32  head logits (row of the head's owner)
 //   count    [2][Ls]        u32   head-work arrivals
+// per layer and step parity: the shared expert's LoRA sums (A_gate x, A_up x:
+// 2 x 16 values, v = A_down act: 16 values, per token) and the arrival counters
+// (head CTAs, LoRA A units, shared act rows)
+constexpr int kLoraAcc = 48;
+constexpr int kLayerCounters = 4;
+enum { CNT_HEAD = 0, CNT_LORA_A = 1, CNT_LORA_V = 2 };
+
 struct WsLayout {
-    long long y, logr, logh, cnt, trace, total;   // byte offsets
+    long long y, logr, logh, lora, cnt, trace, total;   // byte offsets
 };
 inline __host__ __device__ WsLayout ws_layout(int Ls, int B, int d, int E) {
     WsLayout w;
@@ -133,7 +140,8 @@ inline __host__ __device__ WsLayout ws_layout(int Ls, int B, int d, int E) {
     w.y = o;     o += 2LL * Ls * B * d * 4;
     w.logr = o;  o += 2LL * Ls * B * E * 4;
     w.logh = o;  o += 2LL * Ls * B * E * 4;
-    w.cnt = o;   o += (2LL * Ls * 4 + 255) / 256 * 256;
+    w.lora = o;  o += 2LL * Ls * B * kLoraAcc * 4;
+    w.cnt = o;   o += (2LL * Ls * kLayerCounters * 4 + 255) / 256 * 256;
     w.trace = o; o += (long long)kTraceCtas * kTraceSlots * 8;
     w.total = o;
     return w;
@@ -244,6 +252,11 @@ __device__ __forceinline__ unsigned atom_acq_rel_add_u32(unsigned* p, unsigned v
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 __device__ __forceinline__ int ld_volatile_s32(const int* p) {

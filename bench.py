@@ -296,15 +296,17 @@ def run_gpu(args, rank, world):
 def print_trace(tr, nct, sm_mhz=2070.0):
     """Per-layer split of one traced decode step, averaged over CTAs (durations
     from each SM's cycle counter): barrier wait and x, own routing, gate/up,
-    pair exchange, act, down (to the barrier arrival), head; the act and down
-    phases split further; and the producer's timeline relative to the
-    consumer's layer start (globaltimer)."""
+    pair exchange, act, down (to the barrier arrival); the act and down phases
+    split further; the producer's timeline relative to the consumer's layer
+    start (globaltimer); then the head flush after the last layer (x fragments,
+    fc1/linear_init units, fc2, count and top-K, summed over a CTA's tables)."""
     import collections
     cons, prod = tr
-    names = ("wait+x", "route", "gate/up", "xchg", "act", "down", "head")
+    names = ("wait+x", "route", "gate/up", "xchg", "act", "down")
     acc = collections.defaultdict(list)
     sub = collections.defaultdict(list)
     rel = collections.defaultdict(list)
+    flush = []
     us = lambda cyc: cyc / sm_mhz
     for c in range(nct):
         ev, evt = {}, {}
@@ -316,11 +318,11 @@ def print_trace(tr, nct, sm_mhz=2070.0):
         for tag, tm, cy in prod[c].tolist():
             if tm != 0:
                 pev[tag] = tm
-        for l in sorted({k >> 8 for k in ev}):
-            pts = [ev.get((l << 8) | i) for i in range(8)]
+        for l in sorted({k >> 8 for k in ev if (k & 0xFF) == 0}):
+            pts = [ev.get((l << 8) | i) for i in range(7)]
             if None in pts:
                 continue
-            acc[l].append(tuple(us(pts[i + 1] - pts[i]) for i in range(7)))
+            acc[l].append(tuple(us(pts[i + 1] - pts[i]) for i in range(6)))
             x = [ev.get((l << 8) | k) for k in (4, 10, 11, 5, 9, 12, 6)]
             if None not in x:
                 sub[l].append(tuple(us(x[i + 1] - x[i]) for i in range(6)))
@@ -328,13 +330,26 @@ def print_trace(tr, nct, sm_mhz=2070.0):
             r = [pev.get((l << 8) | k) for k in (0x80, 0x81, 0x83)]
             if None not in r:
                 rel[l].append(tuple((v - t0) / 1e3 for v in r))
-    tot = [0.0] * 7
+        tails = [k for k in ev if (k & 0xFF) == 7]
+        tabs = sorted({k >> 8 for k in ev if (k & 0xFF) == 23})
+        if tails and tabs:
+            prev = ev[max(tails)]
+            parts = [0.0] * 4
+            for t in tabs:
+                pts = [ev.get((t << 8) | k) for k in (20, 21, 22, 23)]
+                if None in pts:
+                    continue
+                seg = [pts[0] - prev] + [pts[i + 1] - pts[i] for i in range(3)]
+                parts = [a + us(b) for a, b in zip(parts, seg)]
+                prev = pts[3]
+            flush.append(parts + [sum(parts)])
+    tot = [0.0] * 6
     lines = []
     subn = ("act:zero", "act:rows", "act:tail", "dn:wait", "dn:rows", "dn:release")
     for l in sorted(acc):
         v = acc[l]
-        m = [statistics.mean(x[i] for x in v) for i in range(7)]
-        mx = [max(x[i] for x in v) for i in range(7)]
+        m = [statistics.mean(x[i] for x in v) for i in range(6)]
+        mx = [max(x[i] for x in v) for i in range(6)]
         tot = [a + b for a, b in zip(tot, m)]
         extra = ""
         if sub[l]:
@@ -344,6 +359,11 @@ def print_trace(tr, nct, sm_mhz=2070.0):
                                               for i, n in enumerate(("tab0", "tab1", "issued")))
         lines.append(f"layer {l:2d}: " + " ".join(f"{n} {a:5.2f}/{b:5.2f}" for n, a, b in zip(names, m, mx))
                      + " us (mean/max)" + extra)
+    if flush:
+        fn = ("x", "units", "fc2", "count+topk", "total")
+        lines.append("head flush: " + " ".join(
+            f"{n} {statistics.mean(f[i] for f in flush):5.2f}/{max(f[i] for f in flush):5.2f}"
+            for i, n in enumerate(fn)) + " us (mean/max over CTAs)")
     sys.stderr.write("\n".join(lines) + "\n")
     sys.stderr.write("total (mean over CTAs): " + " ".join(f"{n} {a:.1f}" for n, a in zip(names, tot)) + " us\n")
 

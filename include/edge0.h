@@ -239,7 +239,7 @@ int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
  * the library, present in every GPU that loads it until the process exits.  The
  * call allocates nothing (no cudaMalloc, no host heap); it clears the part of
  * the array it uses before launching.
- *   - The call needs 512 + 8 B d + 16 B E + 384 B bytes of it (about 82 KB at d=2048,
+ *   - The call needs 512 + 10 B d + 16 B E + 384 B bytes of it (about 98 KB at d=2048,
  *     E=256, B=4); shapes whose need exceeds the array (d=4096, E=512, B=4)
  *     return EDGE0_EUNSUPPORTED.
  *   - The first call on a device looks up the array's device address for that

@@ -78,7 +78,7 @@ struct PairPlan {
     Seg seg[kMaxSegs];
     int n_hr, n_q;
     int has_sh;   // the pair owns shared-expert rows
-    int hd0, hd1; // head tasks
+    int hd0, hd1; // head tasks (tables of the head flush)
     int ru0, ru1; // router units (in this rank's half of d)
     int la0, la1; // LoRA A units (A_gate then A_up groups of this rank's half of d)
     int bd0, bd1; // LoRA B_down row tiles (of this rank's half of the output rows)
@@ -93,28 +93,27 @@ __host__ __device__ inline void split_range(int n, int parts, int i, int* a, int
 
 struct Shape {
     int d, I, Is, E, H, r;
-    int n_slots;                      // routed expert slots (0: none)
-    int shared, lora, head, router;   // parts present in the layer
-    int ps;                           // pairs that own shared-expert rows
+    int n_slots;                // routed expert slots (0: none)
+    int shared, lora, router;   // parts present in the layer
+    int ps;                     // pairs that own shared-expert rows
 };
 
-// The shared expert's LoRA runs once per layer, split over the pairs that own
-// shared rows (not repeated by each): they compute A_gate x and A_up x (split over
-// d) into a small global accumulator, wait for it to be complete before their act,
-// add v = A_down act of their rows into a second one, and after their down rows
-// apply B_down (split over the output rows) to the complete v.  Head tasks go to
-// the other pairs.
+// The shared expert's LoRA runs once per layer, not repeated by each pair that
+// owns shared rows: those pairs compute A_gate x and A_up x (split over d) into a
+// small global accumulator, wait for it to be complete before their act, and add
+// v = A_down act of their rows into a second one; the other pairs, after their
+// down rows, apply B_down (split over the output rows) to the complete v.
 
-__host__ __device__ inline int shared_pairs(int P, int n_sh, int n_rt, bool lora, bool head) {
+__host__ __device__ inline int shared_pairs(int P, int n_sh, int n_rt, bool lora) {
     if (n_sh <= 0) return 0;
     if (n_rt <= 0) return P;
     // cost in int4-unit equivalents per CTA: an hr is 16 gate/up units + half a
-    // 16-row down slice over half of d; shared pairs carry the LoRA terms and
-    // their waits, routed pairs the head tasks
+    // 16-row down slice over half of d; shared pairs carry the LoRA A and v terms
+    // and the wait for the A sums, routed pairs the B_down rows
     int best = 0x7fffffff, pick = 1;
     for (int ps = 1; ps < P; ++ps) {
         const int cs = ceil_div(n_sh, ps) * 24 + (lora ? 16 : 0);
-        const int cr = ceil_div(n_rt, P - ps) * 24 + (head ? 16 : 0);
+        const int cr = ceil_div(n_rt, P - ps) * 24 + (lora ? 4 : 0);
         const int cmax = cs > cr ? cs : cr;
         if (cmax <= best) { best = cmax; pick = ps; }   // ties: more shared pairs
     }
@@ -167,15 +166,14 @@ __host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int r
             a = end;
         }
     }
-    // head tasks: routed pairs (all pairs if there are none)
-    const int Pr = P > Ps ? P - Ps : P, ir = P > Ps ? pair - Ps : pair;
-    if (ir >= 0 && S.head) split_range(S.H / kRowTile + S.E / kRowTile, Pr, ir, &pp.hd0, &pp.hd1);
-    // LoRA (implies a shared expert, so Ps >= 1): the shared pairs
-    if (S.lora && pair < Ps) {
+    // LoRA (implies a shared expert, so Ps >= 1): A units on the shared pairs,
+    // B_down rows on the routed pairs (on all pairs if there are none)
+    if (S.lora) {
         const int n_gd = S.d / kGroup, ngh = half_hi(n_gd, rank) - half_lo(n_gd, rank);
         const int n_rtd = S.d / kRowTile, nrt = half_hi(n_rtd, rank) - half_lo(n_rtd, rank);
-        split_range(2 * ngh, Ps, pair, &pp.la0, &pp.la1);
-        split_range(nrt, Ps, pair, &pp.bd0, &pp.bd1);
+        if (pair < Ps) split_range(2 * ngh, Ps, pair, &pp.la0, &pp.la1);
+        const int Pr = P > Ps ? P - Ps : P, ir = P > Ps ? pair - Ps : pair;
+        if (ir >= 0) split_range(nrt, Pr, ir, &pp.bd0, &pp.bd1);
     }
     if (S.router) {
         const int n_gd = S.d / kGroup;
@@ -184,12 +182,49 @@ __host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int r
     }
 }
 
-// CTAs that do head work in a layer (the head's arrival-counter target)
-__host__ __device__ inline int head_ctas(const Shape& S, int P) {
-    const int n_ht = S.H / kRowTile + S.E / kRowTile;
-    const int Pr = P > S.ps ? P - S.ps : P;
-    return 2 * (n_ht < Pr ? n_ht : Pr);
+// ---- head flush.  A head depends only on its layer's x and routing, and its
+// prediction is consumed one token later, so every head of a launch runs in one
+// phase after the last layer (one flush per decode step).  The heads' tasks (per
+// head: H/16 fc1 row tiles with their fc2 columns, then E/16 linear_init row
+// tiles) form one list, split contiguously over the CTAs; each CTA does its tasks
+// over all of d (no pair exchange), in tables of at most p.ft tasks of one head.
+__host__ __device__ inline bool is_head_layer(const Prog& p, int l) {
+    return p.mode == MODE_HEAD || (p.mode == MODE_DECODE && (p.layers[l].flags & LF_HEAD));
 }
+__host__ __device__ inline int n_heads(const Prog& p) {
+    if (p.mode == MODE_HEAD) return 1;
+    int n = 0;
+    for (int l = 0; l < p.L; ++l) n += is_head_layer(p, l) ? 1 : 0;
+    return n;
+}
+__host__ __device__ inline int head_layer(const Prog& p, int hi) {
+    for (int l = 0; l < p.L; ++l)
+        if (is_head_layer(p, l) && hi-- == 0) return l;
+    return 0;
+}
+__host__ __device__ inline int head_tasks(const Prog& p) { return p.H / kRowTile + p.E / kRowTile; }
+// table j of CTA `cta` of an nct grid: head layer *hl, tasks [*t0, *t1); false
+// past the CTA's last table
+__host__ __device__ inline bool flush_table(const Prog& p, int nct, int cta, int j, int* hl, int* t0, int* t1) {
+    const int nt = head_tasks(p);
+    int g, g1;
+    split_range(n_heads(p) * nt, nct, cta, &g, &g1);
+    for (int i = 0; g < g1; ++i) {
+        const int hi = g / nt, t = g - hi * nt;
+        int e = t + p.ft < nt ? t + p.ft : nt;
+        if (hi * nt + e > g1) e = g1 - hi * nt;
+        if (i == j) {
+            *hl = head_layer(p, hi);
+            *t0 = t;
+            *t1 = e;
+            return true;
+        }
+        g = hi * nt + e;
+    }
+    return false;
+}
+// layers of the launch that have item tables before the flush
+__host__ __device__ inline int n_layer_tabs(const Prog& p) { return p.mode == MODE_HEAD ? 0 : p.L; }
 
 // one copy of a contiguous global region into the ring
 struct Item {
@@ -210,7 +245,8 @@ struct DGroup {
 };
 
 struct LayerTab {
-    int seq;          // layer index + 1 once published
+    int seq;          // table index + 1 once published
+    int hl;           // head layer of a flush table, -1 for a layer table
     int k0, n;        // global index of the first item; items
     int p1, p2, p3;   // first item of P1 (gate/up), P2 (down), P3 (head); router items from 0
     int ndg;          // down groups
@@ -243,8 +279,8 @@ struct ItemSink {
     int n, lin, pos, ring;   // pos = lin mod ring
     bool ok;
 };
-__host__ __device__ __noinline__ void push_item(ItemSink& k, int kind, int seg, int bytes, int a, int b,
-                                                int cnt) {
+__host__ __device__ __forceinline__ void push_item(ItemSink& k, int kind, int seg, int bytes, int a, int b,
+                                                   int cnt) {
     if (bytes <= 0) return;
     if (k.n >= kMaxItems || bytes > kItemMax || bytes > k.ring) { k.ok = false; return; }
     if (k.pos + bytes > k.ring) { k.lin += k.ring - k.pos; k.pos = 0; }   // no item wraps
@@ -254,8 +290,8 @@ __host__ __device__ __noinline__ void push_item(ItemSink& k, int kind, int seg, 
     k.lin += bytes;
     k.pos += bytes;
 }
-__host__ __device__ __noinline__ void push_units(ItemSink& k, int kind, int seg, int a, int first,
-                                                 int units, int ub) {
+__host__ __device__ __forceinline__ void push_units(ItemSink& k, int kind, int seg, int a, int first,
+                                                    int units, int ub) {
     const int per = kItemMax / ub;
     for (int j = 0; j < units; j += per) {
         const int m = units - j < per ? units - j : per;
@@ -275,7 +311,8 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
     const Halves hv = halves(Sh.d, Sh.E, rank);
     ItemSink k{T, 0, lin, lin % ring, ring, true};
     T->ndg = 0;
-    const int ngh = hv.gh1 - hv.gh0, nrt = hv.rt1 - hv.rt0, ne = hv.e1 - hv.e0;
+    T->hl = -1;
+    const int ngh = hv.gh1 - hv.gh0, nrt = hv.rt1 - hv.rt0;
     const int r = Sh.r;
     // router units: this pair's share of (E row tiles) x (this rank's groups)
     push_units(k, IT_ROUTER, 0, 0, pl.ru0, pl.ru1 - pl.ru0, kF16Unit);
@@ -346,15 +383,34 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
         }
     }
     T->p3 = k.n;
-    const int nH = Sh.H / kRowTile;
-    for (int t = pl.hd0; t < pl.hd1; ++t) {
-        if (t < nH) {
-            push_units(k, IT_FC1, 0, t, t * ngh, ngh, kF16Unit);
-            push_item(k, IT_FC2, 0, ne * kF16Step, t, hv.e0, ne);
-        } else {
-            push_units(k, IT_LINIT, 0, t - nH, (t - nH) * ngh, ngh, kF16Unit);
+    T->n = k.n;
+    lin = k.lin;
+    return k.ok;
+}
+
+// Items of one head-flush table (tasks [t0, t1) of head layer hl, over all of
+// d): the fc1 and linear_init units of both halves of d (seg = half), then one
+// fc2 column block over all E rows per fc1 task.  p1 = 0, p2 = first fc2 item.
+__host__ __device__ __noinline__ bool build_flush_items(const Prog& p, int hl, int t0, int t1, int ring,
+                                                        LayerTab* T, int& lin) {
+    ItemSink k{T, 0, lin, lin % ring, ring, true};
+    PairPlan& pl = T->pl;
+    pl.nseg = 0; pl.over = 0; pl.n_hr = 0; pl.n_q = 0; pl.has_sh = 0;
+    pl.ru0 = pl.ru1 = pl.la0 = pl.la1 = pl.bd0 = pl.bd1 = 0;
+    pl.hd0 = t0;
+    pl.hd1 = t1;
+    T->hl = hl;
+    T->ndg = 0;
+    T->p1 = 0;
+    const int nH = p.H / kRowTile, hn0 = p.d / kGroup / 2, nE = p.E / kRowTile;
+    for (int t = t0; t < t1; ++t)
+        for (int h = 0; h < 2; ++h) {
+            if (t < nH) push_units(k, IT_FC1, h, t, t * hn0, hn0, kF16Unit);
+            else push_units(k, IT_LINIT, h, t - nH, (t - nH) * hn0, hn0, kF16Unit);
         }
-    }
+    T->p2 = k.n;
+    for (int t = t0; t < t1 && t < nH; ++t) push_item(k, IT_FC2, 0, nE * kF16Step, t, 0, nE);
+    T->p3 = k.n;
     T->n = k.n;
     lin = k.lin;
     return k.ok;
@@ -368,10 +424,15 @@ constexpr int kTraceProducer = 3072;   // first trace word of the producer's sta
 
 struct Plan {
     int ring, full, empty, xch, lin, tabs, xf, xsum, hs, part, recv, act32, af, qsum, vlo, zpart,
-        zrecv, gf, ids, wts, dist, ndist, prv, nprv, ready, rscr, red, ctl, total;
+        gf, ids, wts, dist, ndist, prv, nprv, ready, rscr, red, ctl, total;
 };
 
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
+// head-flush tasks per table: at most 12, and one consumer thread per (task, row, token)
+__host__ __device__ inline int flush_tasks_max(int B) {
+    const int t = kConsumerThreads / (kRowTile * B);
+    return t < 12 ? t : 12;
+}
 
 __host__ __device__ inline int msg_floats(const Prog& p) { return p.hr_max * 16 * p.B; }
 
@@ -380,6 +441,7 @@ __host__ __device__ inline Plan make_plan(const Prog& p, int base) {
     Plan s;
     const int B = p.B, K = p.K, L = p.L;
     const int n_gd = p.d / kGroup, ngh = n_gd - n_gd / 2;
+    const int ft = flush_tasks_max(B);
     int o = base;
     s.full = o;   o += kSlots * 8;
     s.empty = o;  o += kSlots * 8;
@@ -387,7 +449,7 @@ __host__ __device__ inline Plan make_plan(const Prog& p, int base) {
     o = al16(o);
     s.lin = o;    o += kSlots * 4;
     s.tabs = o;   o += al16(kTables * (int)sizeof(LayerTab));
-    s.xf = o;     o += al16(ngh * 4 * B * 4 * 8);
+    s.xf = o;     o += al16(n_gd * 4 * B * 4 * 8);   // all of d (head flush), else this CTA's half
     s.xsum = o;   o += al16(ngh * B * 4);
     s.hs = o;     o += al16(B * p.d * 2);
     s.part = o;   o += al16(msg_floats(p) * 4);
@@ -396,9 +458,8 @@ __host__ __device__ inline Plan make_plan(const Prog& p, int base) {
     s.af = o;     o += al16(p.q_max * B * 2 * 4 * 8);
     s.qsum = o;   o += al16(p.q_max * B * 4);
     s.vlo = o;    o += al16(32 * B * 4);
-    s.zpart = o;  o += al16(16 * B * 4);
-    s.zrecv = o;  o += al16(2 * 16 * B * 4);
-    s.gf = o;     o += al16(B * 2 * 4 * 8);
+    s.zpart = o;  o += al16(ft * 16 * B * 4);
+    s.gf = o;     o += al16(ft * B * 2 * 4 * 8);
     s.ids = o;    o += al16(L * B * K * 4);
     s.wts = o;    o += al16(L * B * K * 4);
     s.dist = o;   o += al16(L * (p.slots_max > 0 ? p.slots_max : 1) * 4);
@@ -531,6 +592,11 @@ __device__ __forceinline__ float* lora_buf(int par, int sidx) {
     const Ctx& c = ctx();
     return ws_f(c.ws.lora) + ((long long)par * prg().Ls + sidx) * prg().B * kLoraAcc;
 }
+// x of a head layer (fp16 [B][d]), kept for the head flush
+__device__ __forceinline__ __half* xs_buf(int sidx) {
+    const Ctx& c = ctx();
+    return reinterpret_cast<__half*>(prg().ws + c.ws.xs) + (long long)sidx * prg().B * prg().d;
+}
 __device__ __forceinline__ unsigned* cnt_buf(int par, int sidx, int which) {
     const Ctx& c = ctx();
     return reinterpret_cast<unsigned*>(prg().ws + c.ws.cnt) + (par * prg().Ls + sidx) * kLayerCounters + which;
@@ -577,9 +643,8 @@ __host__ __device__ inline Shape layer_shape(const Prog& p, int l, bool router) 
     S.n_slots = p.mode == MODE_HEAD ? 0 : p.slots_max;
     S.shared = (p.mode != MODE_HEAD && (Ly.flags & LF_SHARED)) ? 1 : 0;
     S.lora = (S.shared && p.mode == MODE_DECODE && (Ly.flags & LF_LORA)) ? 1 : 0;
-    S.head = (p.mode == MODE_HEAD || (p.mode == MODE_DECODE && (Ly.flags & LF_HEAD))) ? 1 : 0;
     S.router = router ? 1 : 0;
-    S.ps = S.shared ? p.ps[S.lora + 2 * S.head] : 0;
+    S.ps = S.shared ? p.ps[S.lora] : 0;
     return S;
 }
 
@@ -746,9 +811,10 @@ __device__ __noinline__ const char* item_src(int l, const LayerTab* T, const Ite
         case IT_DSC: return dgrp + 4LL * nrt * kQ4Quarter;
         case IT_ADT: return reinterpret_cast<const char*>(Ly.lora_AdT + (long long)it.a * r);
         case IT_BD: return reinterpret_cast<const char*>(Ly.lora_Bd + (long long)it.a * r);
-        case IT_FC1: return Ly.fc1 + (half0(p.H / kRowTile) + it.b) * kF16Unit;
+        // head flush: both halves of d (seg = half)
+        case IT_FC1: return Ly.fc1 + ((long long)it.seg * (p.H / kRowTile) * hn0 + it.b) * kF16Unit;
         case IT_FC2: return Ly.fc2 + ((long long)it.a * (p.E / kRowTile) + it.b) * kF16Step;
-        default: return Ly.linit + (half0(p.E / kRowTile) + it.b) * kF16Unit;
+        default: return Ly.linit + ((long long)it.seg * (p.E / kRowTile) * hn0 + it.b) * kF16Unit;
     }
 }
 
@@ -769,17 +835,23 @@ __device__ void producer() {
     int k = 0;        // global index of the next item
     int front = 0;    // oldest item not known to be released (lane 0)
     if (__shfl_sync(0xffffffffu, lane == 0 ? (int)aborted() : 0, 0)) return;
-    for (int l = 0; l < p.L; ++l) {
+    // the layers' tables, then this CTA's tables of the head flush
+    const int nl = n_layer_tabs(p);
+    for (int l = 0;; ++l) {
+        int hl = -1, t0 = 0, t1 = 0;
+        if (l >= nl && !flush_table(p, c.nct, c.cta, l - nl, &hl, &t0, &t1)) break;
         LayerTab* T = tab_of(l);
         int fail = 0;
         if (lane == 0) {
-            // the table slot is free once the consumers finished layer l - kTables
+            // the table slot is free once the consumers finished table l - kTables
             if (!wait_flag(&ctl->cdone, l - kTables + 1)) fail = 1;
             if (!fail) {
                 stamp_producer((l << 8) | 0x80);
                 T->k0 = k;
-                const Shape Sh = layer_shape(p, l, has_router_phase(p, l, c.step));
-                if (!build_items(Sh, c.P, c.pair, c.rank, p.ring_bytes, T, lin)) {
+                const bool built = l < nl ? build_items(layer_shape(p, l, has_router_phase(p, l, c.step)), c.P,
+                                                        c.pair, c.rank, p.ring_bytes, T, lin)
+                                          : build_flush_items(p, hl, t0, t1, p.ring_bytes, T, lin);
+                if (!built) {
                     raise_error(EDGE0_EUNSUPPORTED);
                     fail = 1;
                 } else {
@@ -809,10 +881,15 @@ __device__ void producer() {
                         have_routing = true;
                         stamp_producer((l << 8) | 0x82);
                     }
-                    // slot kk and the item's ring bytes must be free
+                    // slot kk and the item's ring bytes must be free: move `front` past the
+                    // released items (waiting only for the batch's first item)
                     while (front < kk && (front <= kk - kSlots || it.lin + it.bytes - lstart[front % kSlots] > p.ring_bytes)) {
-                        if (m > 0) break;
-                        if (!mbar_wait(empty_bar(front), item_parity(front))) { fail = 1; break; }
+                        if (m > 0) {
+                            if (!mbar_try_wait(empty_bar(front), item_parity(front))) break;
+                        } else if (!mbar_wait(empty_bar(front), item_parity(front))) {
+                            fail = 1;
+                            break;
+                        }
                         ++front;
                     }
                     if (fail) break;
@@ -826,7 +903,7 @@ __device__ void producer() {
             __syncwarp();
             if (lane < m) {
                 const Item& it = T->it[i + lane];
-                const char* src = item_src(l, T, it);
+                const char* src = item_src(l < nl ? l : T->hl, T, it);
                 uint64_t* fb = full_bar(k + lane);
                 if (src == reinterpret_cast<const char*>(1)) {
                     raise_error(EDGE0_EINVAL);
@@ -839,6 +916,7 @@ __device__ void producer() {
                 }
             }
             __syncwarp();
+            if (lane == 0 && l >= nl && i < 64) stamp_producer((l << 8) | (0x90 + i));   // flush: batch issued
             i += m;
             k += m;
             if (lane == 0) *(volatile int*)&ctl->issued = k;
@@ -1044,6 +1122,8 @@ __device__ __noinline__ void build_x(int l) {
     uint32_t* xf = SM<uint32_t>(c.pl.xf);
     float* xsum = SM<float>(c.pl.xsum);
     const __half* gam = decode ? Ly.gamma : nullptr;
+    // one CTA keeps x of a head layer for the head flush
+    __half* xs_out = (decode && c.cta == 0 && is_head_layer(p, l)) ? xs_buf(Ly.sidx) : nullptr;
 #pragma unroll 1
     for (int j = 0; j * kConsumerThreads < n4; ++j) {
         const int i = tid + j * kConsumerThreads;
@@ -1067,6 +1147,13 @@ __device__ __noinline__ void build_x(int l) {
                 const float r = rs[b];
                 for (int e = 0; e < 4; ++e) x[e] = __half2float(__float2half_rn(x[e] * r * g4[e]));
             }
+        }
+        if (xs_out && i < n4) {
+            const __half2 x01 = __floats2half2_rn(x[0], x[1]), x23 = __floats2half2_rn(x[2], x[3]);
+            uint2 o;
+            o.x = *reinterpret_cast<const uint32_t*>(&x01);
+            o.y = *reinterpret_cast<const uint32_t*>(&x23);
+            *reinterpret_cast<uint2*>(xs_out + 4 * i) = o;
         }
         float s4 = x[0] + x[1] + x[2] + x[3];
         for (int m = 8; m; m >>= 1) s4 += __shfl_xor_sync(0xffffffffu, s4, m);
@@ -1125,6 +1212,32 @@ __device__ bool warp_units(const LayerTab* T, int ia, int ib, F&& f, int wait_ta
                 f(it, a, b);
             }
         }
+        release_item(T, i);
+    }
+    return ok;
+}
+
+// the units of the unit items in [ia, ib) dealt to the warps one at a time in
+// turn, so that all warps move through the items together and a table longer
+// than the ring streams through it; f(item, j, j + 1) per unit
+// (trace: warp 0 stamps tag_base + item when an item it works on has arrived)
+template <class F>
+__device__ bool warp_units_rr(const LayerTab* T, int ia, int ib, F&& f, int tag_base = -1) {
+    const int wid = threadIdx.x >> 5;
+    int u = 0;
+    bool ok = true;
+    for (int i = ia; i < ib; ++i) {
+        const Item& it = T->it[i];
+        if (!unit_kind(it.kind)) continue;
+        int j = ((wid - u) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+        if (j < it.n && ok) {
+            if (!wait_item(T, i)) ok = false;
+            else {
+                if (tag_base >= 0 && i < 64) stamp(tag_base + i);
+                for (; j < it.n; j += kConsumerWarps) f(it, j, j + 1);
+            }
+        }
+        u += it.n;
         release_item(T, i);
     }
     return ok;
@@ -1501,134 +1614,138 @@ __device__ __noinline__ void head_topk(int l) {
     cbar();
 }
 
-// P3: this pair's head tasks of layer l (fc1 row tiles with their fc2 columns, or
-// linear_init row tiles), then the arrival count; the last CTA does the top-K.
-// Every consumer thread runs every barrier; the result is CTA-uniform.
-__device__ bool phase3(int l, const LayerTab* T, uint32_t& xph) {
+// x of head layer l over all of d as B fragments (the kept copy, or the input of
+// a head-only call)
+__device__ __noinline__ void load_x_full(int l) {
     Ctx& c = ctx();
     const Prog& p = prg();
+    const int B = p.B, d = p.d, n4 = B * d / 4;
+    const __half* src = p.mode == MODE_HEAD ? p.x_in : xs_buf(p.layers[l].sidx);
+    uint32_t* xf = SM<uint32_t>(c.pl.xf);
+    for (int i = threadIdx.x; i < n4; i += kConsumerThreads) {
+        const int b = (4 * i) / d, k = (4 * i) % d;
+        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(src + 4 * i));
+        const int sl = (k / kGroup) * 4 + (k % kGroup) / 16;
+        const int k1 = k % 16, t1 = (k1 & 7) >> 1, w = k1 >> 3;
+        xf[((sl * B + b) * 4 + t1) * 2 + w] = v.x;
+        xf[((sl * B + b) * 4 + t1 + 1) * 2 + w] = v.y;
+    }
+    cbar();
+}
+
+// One table of the head flush: tasks [t0, t1) of head layer T->hl over all of d.
+//   z = fc1 x + sum over executed e of fc1[:, d + e] + sum over previous e of
+//       fc1[:, d + E + e]                       (16 rows per fc1 task)
+//   logits += fc2[:, tile] GELU(z[tile])        (all E rows, per fc1 task)
+//   logits += linear_init x + its one-hot columns  (16 rows per linear_init task)
+// then the task count of the head; the CTA that completes it does the top-K.
+// Every consumer thread runs every barrier; the result is CTA-uniform.
+__device__ bool run_flush(int tl, const LayerTab* T, int& xl) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
+    const int l = T->hl;
     const LayerP& Ly = p.layers[l];
     const int B = p.B, K = p.K, E = p.E, H = p.H;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
-    const PairPlan& pl = T->pl;
-    const int nH = H / kRowTile;
-    const int* ids = ids_of(l);
-    const int* prv = prev_of(l);
-    const int nprev = SM<int>(c.pl.nprv)[l];   // previous-token ids present (0 or K)
+    const int nH = H / kRowTile, hn0 = p.d / kGroup / 2;
+    const int t0 = T->pl.hd0, t1 = T->pl.hd1;
     float* lg = logh_buf(c.par, Ly.sidx);
-    float* zpart = SM<float>(c.pl.zpart);
-    float* zrecv = SM<float>(c.pl.zrecv);
+    float* zp = SM<float>(c.pl.zpart);   // [task][16][B]: z rows (fc1), logit rows (linear_init)
+    if (xl != l) {
+        load_x_full(l);
+        xl = l;
+    }
+    stamp((tl << 8) | 20);
+    for (int q = tid; q < (t1 - t0) * 16 * B; q += kConsumerThreads) zp[q] = 0.f;
+    // one-hot columns of (task, row, token) = thread: loads issued before the units
+    const int ti = tid / (16 * B), rr = (tid / B) % 16, bb = tid % B;
+    const int task = t0 + ti;
+    const bool mine = task < t1;
+    float oh = 0.f;
+    if (mine) {
+        const int nprev = SM<int>(c.pl.nprv)[l];
+        const int* ids = ids_of(l);
+        const int* prv = prev_of(l);
+        const __half* col = task < nH ? Ly.fc1_oh : Ly.linit_oh;
+        const int stride = task < nH ? H : E;
+        const int row = (task < nH ? task : task - nH) * kRowTile + rr;
+        float v[2 * EDGE0_MAX_K];
+#pragma unroll
+        for (int k = 0; k < EDGE0_MAX_K; ++k) {
+            v[k] = k < K ? __half2float(col[(long long)ids[bb * K + k] * stride + row]) : 0.f;
+            v[EDGE0_MAX_K + k] = k < nprev ? __half2float(col[(long long)(E + prv[bb * K + k]) * stride + row]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 2 * EDGE0_MAX_K; ++k) oh += v[k];
+    }
+    cbar();
+    // fc1 and linear_init units of both halves of d
+    bool ok = warp_units_rr(T, 0, T->p2, [&](const Item& it, int a, int b) {
+        tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            f16_run(ring_at(it), j0, j1, gl0 + it.seg * hn0, acc);
+            const int tk = (it.kind == IT_FC1 ? tile : tile + nH) - t0;
+            if (t < B) {
+                atomicAdd(&zp[(tk * 16 + g) * B + t], acc[0]);
+                atomicAdd(&zp[(tk * 16 + 8 + g) * B + t], acc[2]);
+            }
+        });
+    }, (tl << 8) | 0x40);
+    ok = !cbar_or(!ok || aborted());
+    stamp((tl << 8) | 21);
+    // GELU (erf form) of the fc1 rows -> hi/lo B fragments per fc1 task; the
+    // linear_init rows (with their one-hot columns) go into the logits
     __half* gf = SM<__half>(c.pl.gf);
-    bool ok = true;
-    int i = T->p3;
-    for (int task = pl.hd0; task < pl.hd1; ++task) {
-        const bool fc1 = task < nH;
-        const int pos = fc1 ? task : task - nH;
-        int j = i;
-        while (j < T->n && T->it[j].kind == (fc1 ? IT_FC1 : IT_LINIT) && T->it[j].a == pos) ++j;
-        if (fc1) {
-            // z partial of H rows 16 pos .. + 15 over this CTA's half of d
-            for (int q = tid; q < 16 * B; q += kConsumerThreads) zpart[q] = 0.f;
-            cbar();
-            ok = warp_units(T, i, j, [&](const Item& it, int a, int b) {
-                tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    f16_run(ring_at(it), j0, j1, gl0, acc);
-                    if (t < B) {
-                        atomicAdd(&zpart[g * B + t], acc[0]);
-                        atomicAdd(&zpart[(g + 8) * B + t], acc[2]);
-                    }
-                });
-            }) && ok;
-            // one-hot columns: fc1[:, d + e] for executed e, fc1[:, d + E + e] for previous e
-            float oh = 0.f;
-            const int rr = tid / B, bb = tid % B;
-            if (tid < 16 * B) {
-                const int hrow = pos * kRowTile + rr;
-                for (int k = 0; k < K; ++k) oh += __half2float(Ly.fc1_oh[(long long)ids[bb * K + k] * H + hrow]);
-                for (int k = 0; k < nprev; ++k)
-                    oh += __half2float(Ly.fc1_oh[(long long)(E + prv[bb * K + k]) * H + hrow]);
-            }
-            ok = !cbar_or(!ok || aborted());
-            stamp((l << 8) | 13);
-            float* zr = zrecv + (xph & 1) * 16 * B;
-            if (ok) ok = exchange(1, zpart, zr, 16 * B, xph);
-            stamp((l << 8) | 14);
-            if (ok && tid < 16 * B) {
-                const float z = zpart[rr * B + bb] + zr[rr * B + bb] + oh;
-                const float gl = 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
-                const int t1 = (rr & 7) >> 1, w = rr >> 3, sub = rr & 1;
-                const __half hi = __float2half_rn(gl);
-                const __half lo = __float2half_rn((gl - __half2float(hi)) * kLoScale);
-                gf[((bb * 2 + 0) * 4 + t1) * 4 + w * 2 + sub] = hi;
-                gf[((bb * 2 + 1) * 4 + t1) * 4 + w * 2 + sub] = lo;
-            }
-            ok = !cbar_or(!ok);
-            // fc2 columns 16 pos .. + 15 for this CTA's half of the E rows
-            if (j < T->n && T->it[j].kind == IT_FC2 && T->it[j].a == pos) {
-                const Item& it2 = T->it[j];
-                if (ok) ok = wait_item(T, j);
-                if (ok) {
-                    const uint2* gfr = SM<uint2>(c.pl.gf);
-                    const int tok = g >> 1, prt = g & 1;
-                    for (int e = wid; e < it2.n; e += kConsumerWarps) {
-                        const uint4 av = *reinterpret_cast<const uint4*>(ring_at(it2) + e * kF16Step + 16 * lane);
-                        uint2 bq = make_uint2(0u, 0u);
-                        if (tok < B) bq = gfr[(tok * 2 + prt) * 4 + t];
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                        const uint32_t A[4] = {av.x, av.y, av.z, av.w};
-                        mma_16816(acc, A, bq.x, bq.y);
-                        const int row = (it2.b + e) * kRowTile + g;
-                        if (t < B) {
-                            red_add_f32(lg + t * E + row, acc[0] + acc[1] * kLoInv);
-                            red_add_f32(lg + t * E + row + 8, acc[2] + acc[3] * kLoInv);
-                        }
-                    }
-                }
-                release_item(T, j);
-                ++j;
-            }
-            ok = !cbar_or(!ok);
-            stamp((l << 8) | 15);
+    if (ok && mine) {
+        if (task < nH) {
+            const float z = zp[(ti * 16 + rr) * B + bb] + oh;
+            const float gl = 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+            const int t1f = (rr & 7) >> 1, w = rr >> 3, sub = rr & 1;
+            const __half hi = __float2half_rn(gl);
+            const __half lo = __float2half_rn((gl - __half2float(hi)) * kLoScale);
+            gf[(((ti * B + bb) * 2 + 0) * 4 + t1f) * 4 + w * 2 + sub] = hi;
+            gf[(((ti * B + bb) * 2 + 1) * 4 + t1f) * 4 + w * 2 + sub] = lo;
         } else {
-            ok = warp_units(T, i, j, [&](const Item& it, int a, int b) {
-                tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    f16_run(ring_at(it), j0, j1, gl0, acc);
-                    const int row = tile * kRowTile + g;
-                    if (t < B) {
-                        red_add_f32(lg + t * E + row, acc[0]);
-                        red_add_f32(lg + t * E + row + 8, acc[2]);
-                    }
-                });
-            }) && ok;
-            if (c.rank == 0 && tid < 16 * B) {
-                // linear_init one-hot columns of these 16 logits
-                const int rr = tid / B, bb = tid % B, row = pos * kRowTile + rr;
-                float oh = 0.f;
-                for (int k = 0; k < K; ++k) oh += __half2float(Ly.linit_oh[(long long)ids[bb * K + k] * E + row]);
-                for (int k = 0; k < nprev; ++k)
-                    oh += __half2float(Ly.linit_oh[(long long)(E + prv[bb * K + k]) * E + row]);
-                red_add_f32(lg + bb * E + row, oh);
+            red_add_f32(lg + bb * E + (task - nH) * kRowTile + rr, zp[(ti * 16 + rr) * B + bb] + oh);
+        }
+    }
+    cbar();
+    // fc2: the column block of each fc1 task over all E rows
+    for (int i = T->p2; i < T->n; ++i) {
+        const Item& it2 = T->it[i];
+        if (ok) ok = wait_item(T, i);
+        if (ok) {
+            const uint2* gfr = SM<uint2>(c.pl.gf) + (it2.a - t0) * B * 8;
+            const int tok = g >> 1, prt = g & 1;
+            uint2 bq = make_uint2(0u, 0u);
+            if (tok < B) bq = gfr[(tok * 2 + prt) * 4 + t];
+            for (int e = wid; e < it2.n; e += kConsumerWarps) {
+                const uint4 av = *reinterpret_cast<const uint4*>(ring_at(it2) + e * kF16Step + 16 * lane);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t A[4] = {av.x, av.y, av.z, av.w};
+                mma_16816(acc, A, bq.x, bq.y);
+                const int row = (it2.b + e) * kRowTile + g;
+                if (t < B) {
+                    red_add_f32(lg + t * E + row, acc[0] + acc[1] * kLoInv);
+                    red_add_f32(lg + t * E + row + 8, acc[2] + acc[3] * kLoInv);
+                }
             }
-            ok = !cbar_or(!ok);
-            stamp((l << 8) | 16);
         }
-        i = j;
-        if (!ok) break;   // uniform
+        release_item(T, i);
     }
-    if (ok && pl.hd1 > pl.hd0) {
-        __threadfence();
-        cbar();
-        const Shape Sh = layer_shape(p, l, false);
-        if (tid == 0) {
-            const unsigned old = atom_acq_rel_add_u32(cnt_buf(c.par, Ly.sidx, CNT_HEAD), 1u);
-            c.ctl->last = old == (unsigned)(head_ctas(Sh, c.P) - 1);
-        }
-        cbar();
-        stamp((l << 8) | 17);
-        if (c.ctl->last) head_topk(l);
+    ok = !cbar_or(!ok);
+    stamp((tl << 8) | 22);
+    // count this table's tasks; the CTA that completes the head does its top-K
+    __threadfence();
+    cbar();
+    if (tid == 0) {
+        const unsigned n = (unsigned)(t1 - t0);
+        const unsigned old = atom_acq_rel_add_u32(cnt_buf(c.par, Ly.sidx, CNT_HEAD), n);
+        c.ctl->last = ok && old + n == (unsigned)head_tasks(p);
     }
+    cbar();
+    if (c.ctl->last) head_topk(l);
+    stamp((tl << 8) | 23);
     return !cbar_or(!ok);
 }
 
@@ -1643,12 +1760,13 @@ __device__ void consumer() {
         const unsigned long long v = ld_acquire_u64(&c.hdr->barrier);
         bar_target = v - v % (unsigned long long)c.nct;
     }
-    uint32_t xph1 = 0, xph3 = 0;
+    uint32_t xph1 = 0;
     volatile int* ready = SM<volatile int>(c.pl.ready);
     float* part = SM<float>(c.pl.part);
     // every decision to leave the loop is taken from a barrier reduction, so all
     // consumer threads leave together
-    for (int l = 0; l < p.L; ++l) {
+    const int nl = n_layer_tabs(p);
+    for (int l = 0; l < nl; ++l) {
         const LayerP& Ly = p.layers[l];
         LayerTab* T = tab_of(l);
         stamp((l << 8) | 0);
@@ -1704,25 +1822,36 @@ __device__ void consumer() {
         if (cbar_or(!ok || aborted())) break;
         bar_arrive();
         stamp((l << 8) | 6);
-        // ---------------- P3: head, while the barrier completes
-        if (Sh.head)
-            if (!phase3(l, T, xph3)) break;
-        stamp((l << 8) | 7);
         if (cbar_or(aborted())) break;
         if (tid == 0) *(volatile int*)&c.ctl->cdone = l + 1;
     }
     if (cbar_or(aborted())) return;
-    // ---------------- tail: the last layer's y is complete after its barrier
-    if (!bar_wait(bar_target)) return;
-    const float* Y = y_buf(c.par, p.layers[p.L - 1].sidx);
-    const long long n = (long long)B * d;
-    const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
-    if (p.mode == MODE_DECODE) {
-        const __half* hs = SM<__half>(c.pl.hs);
-        for (long long i = a + tid; i < b; i += kConsumerThreads)
-            p.h_io[i] = __float2half_rn(__half2float(hs[i]) + __ldcg(Y + i));
-    } else if (p.mode == MODE_MOE) {
-        for (long long i = a + tid; i < b; i += kConsumerThreads) p.y_out[i] = __float2half_rn(__ldcg(Y + i));
+    if (nl > 0) {
+        // ---------------- tail: the last layer's y is complete after its barrier
+        if (!bar_wait(bar_target)) return;
+        stamp((nl << 8) | 7);
+        const float* Y = y_buf(c.par, p.layers[p.L - 1].sidx);
+        const long long n = (long long)B * d;
+        const long long a = n * c.cta / c.nct, b = n * (c.cta + 1) / c.nct;
+        if (p.mode == MODE_DECODE) {
+            const __half* hs = SM<__half>(c.pl.hs);
+            for (long long i = a + tid; i < b; i += kConsumerThreads)
+                p.h_io[i] = __float2half_rn(__half2float(hs[i]) + __ldcg(Y + i));
+        } else if (p.mode == MODE_MOE) {
+            for (long long i = a + tid; i < b; i += kConsumerThreads) p.y_out[i] = __float2half_rn(__ldcg(Y + i));
+        }
+    }
+    // ---------------- head flush: every head layer's x and routing are final here
+    int xl = -1;
+    for (int j = 0;; ++j) {
+        int hl, t0, t1;
+        if (!flush_table(p, c.nct, c.cta, j, &hl, &t0, &t1)) break;
+        const int tl = nl + j;
+        LayerTab* T = tab_of(tl);
+        if (tid == 0) wait_flag(&T->seq, tl + 1);
+        if (cbar_or(aborted())) return;
+        if (!run_flush(tl, T, xl)) return;
+        if (tid == 0) *(volatile int*)&c.ctl->cdone = tl + 1;
     }
     if (c.cta == 0 && tid == 0 && p.step < 0) c.hdr->step = c.step + 1;
 }
@@ -1915,11 +2044,11 @@ int engine_grid(int* nct) {
 }
 
 // Derived launch fields for one set of shapes and grid: the pair-plan maxima over
-// every kind of layer (shared expert, LoRA, head, own router: all 16
-// combinations) and the ring that fits next to the fixed buffers.
+// every kind of layer (shared expert, LoRA, own router: all 8 combinations), the
+// ring that fits next to the fixed buffers, and the head flush's table size.
 struct Derived {
     int mode, B, K, d, E, I, Is, H, r, nct, smem_max;
-    int rc, slots_max, ps[4], hr_max, q_max, ring_bytes, smem;
+    int rc, slots_max, ps[2], hr_max, q_max, ring_bytes, ft, smem;
 };
 
 static int derive(Derived& D) {
@@ -1937,17 +2066,17 @@ static int derive(Derived& D) {
     const int P = D.nct / kClusterCtas;
     // the plan's 32-bit splits: n * parts stays below 2^31
     if ((long long)(p.slots_max * (p.I / kHalfRow) + p.Is) * P >= (1LL << 31)) return EDGE0_EUNSUPPORTED;
-    for (int f = 0; f < 4; ++f)
-        p.ps[f] = shared_pairs(P, p.Is / kHalfRow, p.slots_max * (p.I / kHalfRow), f & 1, f & 2);
+    for (int f = 0; f < 2; ++f) p.ps[f] = shared_pairs(P, p.Is / kHalfRow, p.slots_max * (p.I / kHalfRow), f);
+    p.ft = flush_tasks_max(p.B);
+    if ((long long)EDGE0_MAX_LAYERS * head_tasks(p) * D.nct >= (1LL << 31)) return EDGE0_EUNSUPPORTED;
     p.hr_max = 1;
     p.q_max = 1;
     LayerTab T;   // scratch on the stack: the allocation-free entry point comes here too
     // one layer per combination of parts, in both passes (maxima, then ring capacity)
     for (int pass = 0; pass < 2; ++pass) {
-        for (int combo = 0; combo < 16; ++combo) {
-            p.layers[0].flags = ((combo & 1) ? LF_SHARED : 0) | ((combo & 2) ? LF_LORA : 0) |
-                                ((combo & 4) ? LF_HEAD : 0);
-            const bool router = (combo & 8) && p.mode == MODE_DECODE;
+        for (int combo = 0; combo < 8; ++combo) {
+            p.layers[0].flags = ((combo & 1) ? LF_SHARED : 0) | ((combo & 2) ? LF_LORA : 0);
+            const bool router = (combo & 4) && p.mode == MODE_DECODE;
             const Shape S = layer_shape(p, 0, router);
             for (int pair = 0; pair < P; ++pair)
                 for (int rank = 0; rank < kClusterCtas; ++rank) {
@@ -1975,8 +2104,27 @@ static int derive(Derived& D) {
             if (p.ring_bytes < kMinRing) return EDGE0_EUNSUPPORTED;
         }
     }
+    // head flush tables: the fc2 items of a table are held until its fc2 step, next
+    // to one item of slack; fewer tasks per table where the ring is short
+    if (p.mode != MODE_MOE) {
+        const int fc2b = (p.E / kRowTile) * kF16Step;
+        if (fc2b > kItemMax) return EDGE0_EUNSUPPORTED;
+        const int fit = (p.ring_bytes - kItemMax) / fc2b;
+        if (fit < 1) return EDGE0_EUNSUPPORTED;
+        if (p.ft > fit) p.ft = fit;
+        const int nt = head_tasks(p);
+        for (int t0 = 0; t0 < nt; t0 += p.ft) {
+            const int t1 = t0 + p.ft < nt ? t0 + p.ft : nt;
+            int lin = 0;
+            if (!build_flush_items(p, 0, t0, t1, 1 << 30, &T, lin)) return EDGE0_EUNSUPPORTED;
+            long long held = 0;
+            for (int i = T.p2; i < T.n; ++i) held += T.it[i].bytes;
+            if (held + kItemMax > p.ring_bytes) return EDGE0_EUNSUPPORTED;
+        }
+    }
     D.slots_max = p.slots_max;
-    for (int f = 0; f < 4; ++f) D.ps[f] = p.ps[f];
+    for (int f = 0; f < 2; ++f) D.ps[f] = p.ps[f];
+    D.ft = p.ft;
     D.hr_max = p.hr_max;
     D.q_max = p.q_max;
     D.ring_bytes = p.ring_bytes;
@@ -2016,7 +2164,8 @@ int engine_check(Prog& p, int nct, int smem_max, int* smem_bytes) {
     const Derived& d = g_derived[hit];
     if (d.rc) return d.rc;
     p.slots_max = d.slots_max;
-    for (int f = 0; f < 4; ++f) p.ps[f] = d.ps[f];
+    for (int f = 0; f < 2; ++f) p.ps[f] = d.ps[f];
+    p.ft = d.ft;
     p.hr_max = d.hr_max;
     p.q_max = d.q_max;
     p.ring_bytes = d.ring_bytes;

@@ -99,9 +99,10 @@ struct Prog {
     char* ws;
     // derived by engine_check for the launch's grid
     int slots_max;            // routed expert slots of a layer: min(B K, E)
-    int ps[4];                // CTA pairs that own shared-expert rows (index: LoRA + 2 head)
+    int ps[2];                // CTA pairs that own shared-expert rows (without, with LoRA)
     int hr_max, q_max;        // most half-row tiles / act quarters one CTA pair owns
     int ring_bytes;           // shared-memory ring of streamed weights
+    int ft;                   // most head tasks in one table of the head flush
     LayerP layers[EDGE0_MAX_LAYERS];
 };
 
@@ -120,19 +121,20 @@ constexpr int kTraceCtas = 160;
 constexpr int kTraceSlots = 4096;   // u64 words: (tag, globaltimer, clock) triples
 
 // Workspace after the header, per step parity p in {0, 1} and state row s:
-//   y        [2][Ls][B][d]  fp32  layer output accumulators (red.add)
-//   logits_r [2][Ls][B][E]  fp32  own-router logits
-//   logits_h [2][Ls][B][E]  fp32  head logits (row of the head's owner)
-//   count    [2][Ls]        u32   head-work arrivals
-// per layer and step parity: the shared expert's LoRA sums (A_gate x, A_up x:
-// 2 x 16 values, v = A_down act: 16 values, per token) and the arrival counters
-// (head CTAs, LoRA A units, shared act rows)
+//   y        [2][Ls][B][d]   fp32  layer output accumulators (red.add)
+//   logits_r [2][Ls][B][E]   fp32  own-router logits
+//   logits_h [2][Ls][B][E]   fp32  head logits (row of the head's owner)
+//   lora     [2][Ls][B][48]  fp32  the shared expert's LoRA sums: A_gate x, A_up x
+//                                  (2 x 16 per token), v = A_down act (16)
+//   count    [2][Ls][4]      u32   arrival counters: head tasks, LoRA A units,
+//                                  shared act rows
+//   xs       [Ls][B][d]      fp16  x of each head layer, for the head flush
 constexpr int kLoraAcc = 48;
 constexpr int kLayerCounters = 4;
 enum { CNT_HEAD = 0, CNT_LORA_A = 1, CNT_LORA_V = 2 };
 
 struct WsLayout {
-    long long y, logr, logh, lora, cnt, trace, total;   // byte offsets
+    long long y, logr, logh, lora, cnt, xs, trace, total;   // byte offsets
 };
 inline __host__ __device__ WsLayout ws_layout(int Ls, int B, int d, int E) {
     WsLayout w;
@@ -142,6 +144,7 @@ inline __host__ __device__ WsLayout ws_layout(int Ls, int B, int d, int E) {
     w.logh = o;  o += 2LL * Ls * B * E * 4;
     w.lora = o;  o += 2LL * Ls * B * kLoraAcc * 4;
     w.cnt = o;   o += (2LL * Ls * kLayerCounters * 4 + 255) / 256 * 256;
+    w.xs = o;    o += ((long long)Ls * B * d * 2 + 255) / 256 * 256;
     w.trace = o; o += (long long)kTraceCtas * kTraceSlots * 8;
     w.total = o;
     return w;

@@ -54,7 +54,7 @@ def test_noalloc_matches_the_workspace_entry_point_two_calls_in_a_row(cfg):
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = binding.lib()
     x = C.c_void_p(256)
-    # d = 4096 with 512 experts at B = 4 needs 256 + 8 B d + 16 B E + 384 B + 256 = 165,888
+    # d = 4096 with 512 experts at B = 4 needs 512 + 10 B d + 16 B E + 384 B = 198,656
     # bytes of scratch, more than the fixed array holds
     moe = binding.MoeDesc(4096, 512, 8, 512, 512, 256, 256, None, None, None, 0)
     assert binding.lib().edge0_workspace_bytes(1, 4, 4096, 512) - 160 * 4096 * 8 > 128 * 1024

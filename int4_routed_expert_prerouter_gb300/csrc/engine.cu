@@ -250,6 +250,7 @@ struct LayerTab {
     int k0, n;        // global index of the first item; items
     int p1, p2, p3;   // first item of P1 (gate/up), P2 (down), P3 (head); router items from 0
     int ndg;          // down groups
+    int ibg, ibu, iadt, ibd;   // first item of the LoRA B_gate, B_up, A_down^T, B_down rows (or -1)
     PairPlan pl;
     DGroup dg[kMaxDg];
     Item it[kMaxItems];
@@ -312,6 +313,7 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
     ItemSink k{T, 0, lin, lin % ring, ring, true};
     T->ndg = 0;
     T->hl = -1;
+    T->ibg = T->ibu = T->iadt = T->ibd = -1;
     const int ngh = hv.gh1 - hv.gh0, nrt = hv.rt1 - hv.rt0;
     const int r = Sh.r;
     // router units: this pair's share of (E row tiles) x (this rank's groups)
@@ -332,8 +334,11 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
         push_units(k, IT_GU, s, 0, g.hr0 * ngh, (g.hr1 - g.hr0) * ngh, kQ4Unit);
         if (g.slot < 0 && Sh.lora) {
             const int rows = (g.hr1 - g.hr0) * kHalfRow;
+            T->ibg = k.n;
             push_item(k, IT_BG, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            T->ibu = k.n;
             push_item(k, IT_BU, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
+            T->iadt = k.n;
             push_item(k, IT_ADT, s, rows * r * 2, g.hr0 * kHalfRow, 0, rows);
         }
     }
@@ -375,7 +380,8 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
         }
     }
     // LoRA B_down rows: row tiles [bd0, bd1) of this rank's half
-    {
+    if (pl.bd1 > pl.bd0) {
+        T->ibd = k.n;
         const int per = kItemMax / (r * 2);
         for (int row = (hv.rt0 + pl.bd0) * kRowTile; row < (hv.rt0 + pl.bd1) * kRowTile; row += per) {
             const int m = (hv.rt0 + pl.bd1) * kRowTile - row < per ? (hv.rt0 + pl.bd1) * kRowTile - row : per;
@@ -401,6 +407,7 @@ __host__ __device__ __noinline__ bool build_flush_items(const Prog& p, int hl, i
     pl.hd1 = t1;
     T->hl = hl;
     T->ndg = 0;
+    T->ibg = T->ibu = T->iadt = T->ibd = -1;
     T->p1 = 0;
     const int nH = p.H / kRowTile, hn0 = p.d / kGroup / 2, nE = p.E / kRowTile;
     for (int t = t0; t < t1; ++t)
@@ -886,9 +893,13 @@ __device__ void producer() {
                     while (front < kk && (front <= kk - kSlots || it.lin + it.bytes - lstart[front % kSlots] > p.ring_bytes)) {
                         if (m > 0) {
                             if (!mbar_try_wait(empty_bar(front), item_parity(front))) break;
-                        } else if (!mbar_wait(empty_bar(front), item_parity(front))) {
-                            fail = 1;
-                            break;
+                        } else {
+                            if (l >= nl && !mbar_try_wait(empty_bar(front), item_parity(front)))
+                                stamp_producer((l << 8) | 0xE0 | ((front - T->k0 + 1024) << 20));
+                            if (!mbar_wait(empty_bar(front), item_parity(front))) {
+                                fail = 1;
+                                break;
+                            }
                         }
                         ++front;
                     }
@@ -916,7 +927,8 @@ __device__ void producer() {
                 }
             }
             __syncwarp();
-            if (lane == 0 && l >= nl && i < 64) stamp_producer((l << 8) | (0x90 + i));   // flush: batch issued
+            if (lane == 0 && l >= nl && i < 64)   // flush: batch issued, with the front item
+                stamp_producer((l << 8) | (0x90 + i) | ((front - T->k0 + 1024) << 20));
             i += m;
             k += m;
             if (lane == 0) *(volatile int*)&ctl->issued = k;
@@ -1002,44 +1014,15 @@ __device__ __forceinline__ void q4_masks(uint32_t w, uint32_t A[4]) {
     A[3] = w8 & 0x00F000F0u;   // row g+8, k 2t+8 | 2t+9 (x16)
 }
 
-// int4 units [a, b) of a run whose unit j is local group gl0 + j of one row
-// tile: adds s 2^24 acc + b xsum per unit to rows g (r0) and g + 8 (r1), token t
-__device__ __forceinline__ void q4_run(const char* base, int a, int b, int gl0,
-                                       float& r0, float& r1) {
-    const Ctx& c = ctx();
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int B = prg().B;
-    const XFrag xf = xfrag();
-    const float* xs = SM<float>(c.pl.xsum);
-#pragma unroll 2
-    for (int j = a; j < b; ++j) {
-        const char* unit = base + (long long)j * kQ4Unit;
-        const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
-        const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g);
-        const int gl = gl0 + j;
-        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            uint2 bb = make_uint2(0u, 0u);
-            if (xf.live) bb = xf.base[(gl * 4 + s) * xf.stride];
-            uint32_t A[4];
-            q4_masks(w[s], A);
-            mma_16816(acc, A, bb.x, bb.y);
-        }
-        const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) of row g
-        const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) of row g + 8
-        const float x = t < B ? xs[gl * B + t] : 0.f;
-        r0 += __low2float(s0) * kTwo24 * acc[0] + __high2float(s0) * x;
-        r1 += __low2float(s1) * (kTwo24 / 16.0f) * acc[2] + __high2float(s1) * x;
-    }
-}
-
 // fp16 units [a, b) (x source) accumulated into acc (rows g, g + 8; column 2t = token t)
 __device__ __forceinline__ void f16_run(const char* base, int a, int b, int gl0, float acc[4]) {
     const Ctx& c = ctx();
     const int lane = threadIdx.x & 31;
     const XFrag xf = xfrag();
+    // one accumulator per 16-input step: consecutive MMAs do not wait on each other
+    float as[4][4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) as[s][0] = as[s][1] = as[s][2] = as[s][3] = 0.f;
     for (int j = a; j < b; ++j) {
         const char* unit = base + (long long)j * kF16Unit;
         const int gl = gl0 + j;
@@ -1049,9 +1032,11 @@ __device__ __forceinline__ void f16_run(const char* base, int a, int b, int gl0,
             uint2 bb = make_uint2(0u, 0u);
             if (xf.live) bb = xf.base[(gl * 4 + s) * xf.stride];
             const uint32_t A[4] = {av.x, av.y, av.z, av.w};
-            mma_16816(acc, A, bb.x, bb.y);
+            mma_16816(as[s], A, bb.x, bb.y);
         }
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] += (as[0][e] + as[1][e]) + (as[2][e] + as[3][e]);
 }
 
 // ------------------------------------------------------------ prologue ----
@@ -1217,32 +1202,6 @@ __device__ bool warp_units(const LayerTab* T, int ia, int ib, F&& f, int wait_ta
     return ok;
 }
 
-// the units of the unit items in [ia, ib) dealt to the warps one at a time in
-// turn, so that all warps move through the items together and a table longer
-// than the ring streams through it; f(item, j, j + 1) per unit
-// (trace: warp 0 stamps tag_base + item when an item it works on has arrived)
-template <class F>
-__device__ bool warp_units_rr(const LayerTab* T, int ia, int ib, F&& f, int tag_base = -1) {
-    const int wid = threadIdx.x >> 5;
-    int u = 0;
-    bool ok = true;
-    for (int i = ia; i < ib; ++i) {
-        const Item& it = T->it[i];
-        if (!unit_kind(it.kind)) continue;
-        int j = ((wid - u) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-        if (j < it.n && ok) {
-            if (!wait_item(T, i)) ok = false;
-            else {
-                if (tag_base >= 0 && i < 64) stamp(tag_base + i);
-                for (; j < it.n; j += kConsumerWarps) f(it, j, j + 1);
-            }
-        }
-        u += it.n;
-        release_item(T, i);
-    }
-    return ok;
-}
-
 __device__ __forceinline__ bool seg_live(int l, const Seg& s) {
     const Ctx& c = ctx();
     return s.slot < 0 || s.slot < SM<int>(c.pl.ndist)[l];
@@ -1299,45 +1258,6 @@ __device__ __noinline__ void route_layer(int l) {
     cbar();
 }
 
-// P1: partial gate/up sums of the pair's rows over this CTA's half of d; LoRA A
-// units go straight into the layer's global sums, each warp counting the units it
-// finished
-__device__ bool phase1(int l, const LayerTab* T) {
-    Ctx& c = ctx();
-    const Prog& p = prg();
-    const int B = p.B;
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    float* part = SM<float>(c.pl.part);
-    return warp_units(T, T->p1, T->p2, [&](const Item& it, int a, int b) {
-        if (it.kind == IT_LA || it.kind == IT_LU) {
-            float* la = lora_buf(c.par, p.layers[l].sidx) + (it.kind == IT_LA ? 0 : 16 * B);
-            tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                f16_run(ring_at(it), j0, j1, gl0, acc);
-                if (t < B) {
-                    red_add_f32(la + g * B + t, acc[0]);
-                    red_add_f32(la + (g + 8) * B + t, acc[2]);
-                }
-            });
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) atom_acq_rel_add_u32(cnt_buf(c.par, p.layers[l].sidx, CNT_LORA_A), (unsigned)(b - a));
-            return;
-        }
-        const Seg& sg = T->pl.seg[it.seg];
-        if (!seg_live(l, sg)) return;
-        tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
-            float r0 = 0.f, r1 = 0.f;
-            q4_run(ring_at(it), j0, j1, gl0, r0, r1);
-            const int hl = sg.hoff + tile - sg.hr0;
-            if (t < B) {
-                atomicAdd(&part[(hl * 16 + g) * B + t], r0);
-                atomicAdd(&part[(hl * 16 + 8 + g) * B + t], r1);
-            }
-        });
-    }, (l << 8) | 8);
-}
-
 // bounded wait (one thread) until a layer counter reaches `want`; false on
 // abort or timeout
 __device__ __noinline__ bool wait_count(const unsigned* cnt, unsigned want) {
@@ -1352,11 +1272,134 @@ __device__ __noinline__ bool wait_count(const unsigned* cnt, unsigned want) {
     return true;
 }
 
-// index of the first item of `kind` for segment s in [ia, ib), or -1
-__device__ __forceinline__ int find_item(const LayerTab* T, int ia, int ib, int kind, int s) {
+// P1: partial gate/up sums of the pair's rows over this CTA's half of d; LoRA A
+// units go straight into the layer's global sums, each warp counting the units it
+// finished.  The warps take contiguous shares of the units; addresses come from
+// registers (the table's constants loaded once, each item's fields once).  With
+// LoRA on a shared pair, the last warp then waits for every LoRA A unit of the
+// layer and loads the sums (A_gate x, A_up x) for the act.
+__device__ bool phase1(int l, const LayerTab* T, bool lora_wait) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
+    const LayerP& Ly = p.layers[l];
+    const int B = p.B;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    float* part = SM<float>(c.pl.part);
+    const char* ringb = g_smem + c.pl.ring;
+    const int tok = g >> 1;
+    const bool live = !(g & 1) && tok < B;
+    const uint2* xfb = SM<uint2>(c.pl.xf) + (live ? tok : 0) * 4 + t;
+    const int xstride = B * 4;
+    const float* xs = SM<float>(c.pl.xsum);
+    const int ngh = c.hv.gh1 - c.hv.gh0;
+    const int k0 = T->k0, ia = T->p1, ib = T->p2;
+    const int ndist = SM<int>(c.pl.ndist)[l];
+    float* lora_g = lora_buf(c.par, Ly.sidx);
+    int tot = 0;
     for (int i = ia; i < ib; ++i)
-        if (T->it[i].kind == kind && T->it[i].seg == s) return i;
-    return -1;
+        if (unit_kind(T->it[i].kind)) tot += T->it[i].n;
+    int ua, ub;
+    split_range(tot, kConsumerWarps, wid, &ua, &ub);
+    int u = 0;
+    bool ok = true, first = true;
+    for (int i = ia; i < ib; ++i) {
+        const int kind = T->it[i].kind;
+        if (!unit_kind(kind)) continue;
+        const int in = T->it[i].n;
+        const int a = ua - u > 0 ? ua - u : 0, b = ub - u < in ? ub - u : in;
+        u += in;
+        if (a < b && ok) {
+            if (!mbar_wait(full_bar(k0 + i), item_parity(k0 + i))) {
+                ok = false;
+            } else {
+                if (first) { stamp((l << 8) | 8); first = false; }
+                const int ibase = T->it[i].b, seg = T->it[i].seg;
+                const char* base = ringb + T->it[i].off;
+                if (kind == IT_LA || kind == IT_LU) {
+                    // one row tile (r <= 16 rows): units are groups ibase + j of this half
+                    float as[4][4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) as[q][0] = as[q][1] = as[q][2] = as[q][3] = 0.f;
+                    for (int j = a; j < b; ++j) {
+                        const char* unit = base + j * kF16Unit;
+                        const int gl = ibase + j;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 av = *reinterpret_cast<const uint4*>(unit + q * kF16Step + 16 * lane);
+                            uint2 bb = make_uint2(0u, 0u);
+                            if (live) bb = xfb[(gl * 4 + q) * xstride];
+                            const uint32_t A[4] = {av.x, av.y, av.z, av.w};
+                            mma_16816(as[q], A, bb.x, bb.y);
+                        }
+                    }
+                    float* la = lora_g + (kind == IT_LA ? 0 : 16 * B);
+                    if (t < B) {
+                        red_add_f32(la + g * B + t, (as[0][0] + as[1][0]) + (as[2][0] + as[3][0]));
+                        red_add_f32(la + (g + 8) * B + t, (as[0][2] + as[1][2]) + (as[2][2] + as[3][2]));
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) red_release_add_u32(cnt_buf(c.par, Ly.sidx, CNT_LORA_A), (unsigned)(b - a));
+                } else {
+                    const int slot = T->pl.seg[seg].slot, hr0 = T->pl.seg[seg].hr0, hoff = T->pl.seg[seg].hoff;
+                    if (slot < 0 || slot < ndist) {
+                        // runs of units that lie in one row tile
+                        int j = a;
+                        while (j < b) {
+                            const int uu = ibase + j, tile = uu / ngh, grp = uu - tile * ngh;
+                            const int e = b < j + (ngh - grp) ? b : j + (ngh - grp);
+                            const int gl0 = grp - j;
+                            float r0 = 0.f, r1 = 0.f;
+#pragma unroll 2
+                            for (int jj = j; jj < e; ++jj) {
+                                const char* unit = base + jj * kQ4Unit;
+                                const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+                                const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g);
+                                const int gl = gl0 + jj;
+                                const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+                                float as[4][4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    uint2 bb = make_uint2(0u, 0u);
+                                    if (live) bb = xfb[(gl * 4 + q) * xstride];
+                                    uint32_t A[4];
+                                    q4_masks(w[q], A);
+                                    as[q][0] = as[q][1] = as[q][2] = as[q][3] = 0.f;
+                                    mma_16816(as[q], A, bb.x, bb.y);
+                                }
+                                const float a0 = (as[0][0] + as[1][0]) + (as[2][0] + as[3][0]);
+                                const float a2 = (as[0][2] + as[1][2]) + (as[2][2] + as[3][2]);
+                                const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);
+                                const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);
+                                const float xv = t < B ? xs[gl * B + t] : 0.f;
+                                r0 += __low2float(s0) * kTwo24 * a0 + __high2float(s0) * xv;
+                                r1 += __low2float(s1) * (kTwo24 / 16.0f) * a2 + __high2float(s1) * xv;
+                            }
+                            const int hl = hoff + tile - hr0;
+                            if (t < B) {
+                                atomicAdd(&part[(hl * 16 + g) * B + t], r0);
+                                atomicAdd(&part[(hl * 16 + 8 + g) * B + t], r1);
+                            }
+                            j = e;
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(k0 + i));
+    }
+    if (lora_wait && wid == kConsumerWarps - 1) {
+        // every LoRA A unit of the layer is in the global sums: load them
+        bool w = true;
+        if (lane == 0 && ok) w = wait_count(cnt_buf(c.par, Ly.sidx, CNT_LORA_A), 2u * (unsigned)(p.d / kGroup));
+        w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        float* lsum = SM<float>(c.pl.vlo);
+        if (ok && w)
+            for (int q = lane; q < 32 * B; q += 32) lsum[q] = __ldcg(lora_g + q);
+        ok = ok && w;
+    }
+    return ok;
 }
 
 // act = silu(gate) * up of all the pair's rows (partials of both CTAs, LoRA B
@@ -1382,16 +1425,13 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
     bool ok = true;
     if (lora && pl.has_sh) {
         ssh = 0;
-        ibg = find_item(T, T->p1, T->p2, IT_BG, ssh);
-        ibu = find_item(T, T->p1, T->p2, IT_BU, ssh);
-        iadt = find_item(T, T->p1, T->p2, IT_ADT, ssh);
+        ibg = T->ibg;
+        ibu = T->ibu;
+        iadt = T->iadt;
         ok = ibg >= 0 && ibu >= 0 && iadt >= 0;
         if (!ok && tid == 0) raise_error(EDGE0_EINVAL);
+        // (the LoRA A sums were loaded into lsum at the end of P1)
         ok = ok && wait_item(T, ibg) && wait_item(T, ibu) && wait_item(T, iadt);
-        // every LoRA A unit of the layer has been added to the global sums
-        if (tid == 0 && ok) ok = wait_count(cnt_buf(c.par, Ly.sidx, CNT_LORA_A), 2u * (unsigned)(p.d / kGroup));
-        ok = !cbar_or(!ok);
-        for (int i = tid; ok && i < 32 * B; i += kConsumerThreads) lsum[i] = __ldcg(lora_g + i);
     }
     // af and qsum were cleared at the start of the layer
     ok = !cbar_or(!ok);
@@ -1434,19 +1474,25 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
     if (ok && ssh >= 0) {
         // v[q][b] += sum over the pair's shared act rows of A_down[q][row] act[row][b],
         // q in this CTA's half of [0, r); then count this CTA's shared rows
+        // one warp per output (q, b), its lanes splitting the rows
         const Seg& sg = pl.seg[ssh];
         const __half* adt = reinterpret_cast<const __half*>(ring_at(T->it[iadt]));
         const int rows = (sg.hr1 - sg.hr0) * kHalfRow;
         const int q0 = c.rank ? r / 2 : 0, q1 = c.rank ? r : r / 2;
-        for (int i = tid; i < (q1 - q0) * B; i += kConsumerThreads) {
-            const int q = q0 + i / B, b = i % B;
+        const int lane = tid & 31, wid = tid >> 5;
+        const float* a32 = act32 + sg.hoff * 8 * B;
+        for (int o = wid; o < (q1 - q0) * B; o += kConsumerWarps) {
+            const int q = q0 + o / B, b = o % B;
             float v = 0.f;
-            for (int j = 0; j < rows; ++j) v += __half2float(adt[j * r + q]) * act32[(sg.hoff * 8 + j) * B + b];
-            red_add_f32(lora_g + (32 + q) * B + b, v);
+            for (int j = lane; j < rows; j += 32) v += __half2float(adt[j * r + q]) * a32[j * B + b];
+            v = warp_sum(v);
+            if (lane == 0) red_add_f32(lora_g + (32 + q) * B + b, v);
         }
-        __threadfence();
         cbar();
-        if (tid == 0) atom_acq_rel_add_u32(cnt_buf(c.par, Ly.sidx, CNT_LORA_V), (unsigned)(sg.hr1 - sg.hr0));
+        if (tid == 0) {
+            __threadfence();
+            red_release_add_u32(cnt_buf(c.par, Ly.sidx, CNT_LORA_V), (unsigned)(sg.hr1 - sg.hr0));
+        }
     }
     // the non-unit P1 items (LoRA B rows of gate/up) are no longer needed
     for (int i = T->p1; i < T->p2; ++i)
@@ -1553,7 +1599,7 @@ __device__ bool phase2(int l, const LayerTab* T, bool lora) {
     stamp((l << 8) | 12);
     // LoRA B_down rows of this CTA, once v is complete:
     // y[row] += scale * sum_q B_down[row][q] v[q]
-    const int ibd = lora ? find_item(T, T->p2, T->p3, IT_BD, 0) : -1;
+    const int ibd = lora ? T->ibd : -1;
     if (ibd >= 0) {
         float* vs = SM<float>(c.pl.vlo);
         const int tid = threadIdx.x;
@@ -1679,18 +1725,61 @@ __device__ bool run_flush(int tl, const LayerTab* T, int& xl) {
         for (int k = 0; k < 2 * EDGE0_MAX_K; ++k) oh += v[k];
     }
     cbar();
-    // fc1 and linear_init units of both halves of d
-    bool ok = warp_units_rr(T, 0, T->p2, [&](const Item& it, int a, int b) {
-        tile_runs(it, a, b, [&](int tile, int j0, int j1, int gl0) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            f16_run(ring_at(it), j0, j1, gl0 + it.seg * hn0, acc);
-            const int tk = (it.kind == IT_FC1 ? tile : tile + nH) - t0;
-            if (t < B) {
-                atomicAdd(&zp[(tk * 16 + g) * B + t], acc[0]);
-                atomicAdd(&zp[(tk * 16 + 8 + g) * B + t], acc[2]);
+    // fc1 and linear_init units of both halves of d, dealt to the warps one at a
+    // time in turn (all warps move through the items together, so a table longer
+    // than the ring streams through it).  Addresses come from registers: the
+    // table's constants are loaded once, each item's fields once.
+    bool ok = true;
+    {
+        const char* ringb = g_smem + c.pl.ring;
+        const int tok = g >> 1;
+        const bool live = !(g & 1) && tok < B;
+        const uint2* xfb = SM<uint2>(c.pl.xf) + (live ? tok : 0) * 4 + t;
+        const int xstride = B * 4;
+        const int k0 = T->k0, n_units_items = T->p2;
+        int u = 0;
+        int cur = -1;   // task of the warp's running sum
+        float s0 = 0.f, s2 = 0.f;
+        for (int i = 0; i < n_units_items; ++i) {
+            const int kind = T->it[i].kind, seg = T->it[i].seg, off = T->it[i].off, ib = T->it[i].b, in = T->it[i].n;
+            int j = ((wid - u) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+            if (j < in && ok) {
+                if (!mbar_wait(full_bar(k0 + i), item_parity(k0 + i))) ok = false;
+                for (; ok && j < in; j += kConsumerWarps) {
+                    const int uu = ib + j, tile = uu / hn0, gl = uu - tile * hn0 + seg * hn0;
+                    const int tk = (kind == IT_FC1 ? tile : tile + nH) - t0;
+                    if (tk != cur) {
+                        if (cur >= 0 && t < B) {
+                            atomicAdd(&zp[(cur * 16 + g) * B + t], s0);
+                            atomicAdd(&zp[(cur * 16 + 8 + g) * B + t], s2);
+                        }
+                        cur = tk;
+                        s0 = s2 = 0.f;
+                    }
+                    const char* unit = ringb + off + j * kF16Unit;
+                    float as[4][4];
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint4 av = *reinterpret_cast<const uint4*>(unit + s * kF16Step + 16 * lane);
+                        uint2 bb = make_uint2(0u, 0u);
+                        if (live) bb = xfb[(gl * 4 + s) * xstride];
+                        const uint32_t A[4] = {av.x, av.y, av.z, av.w};
+                        as[s][0] = as[s][1] = as[s][2] = as[s][3] = 0.f;
+                        mma_16816(as[s], A, bb.x, bb.y);
+                    }
+                    s0 += (as[0][0] + as[1][0]) + (as[2][0] + as[3][0]);
+                    s2 += (as[0][2] + as[1][2]) + (as[2][2] + as[3][2]);
+                }
             }
-        });
-    }, (tl << 8) | 0x40);
+            u += in;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(k0 + i));
+        }
+        if (cur >= 0 && t < B) {
+            atomicAdd(&zp[(cur * 16 + g) * B + t], s0);
+            atomicAdd(&zp[(cur * 16 + 8 + g) * B + t], s2);
+        }
+    }
     ok = !cbar_or(!ok || aborted());
     stamp((tl << 8) | 21);
     // GELU (erf form) of the fc1 rows -> hi/lo B fragments per fc1 task; the
@@ -1806,7 +1895,7 @@ __device__ void consumer() {
         }
         stamp((l << 8) | 2);
         // ---------------- P1: gate/up partials, swap with the peer, act
-        bool ok = phase1(l, T);
+        bool ok = phase1(l, T, Sh.lora && T->pl.has_sh);
         if (cbar_or(!ok || aborted())) break;
         stamp((l << 8) | 3);
         if (T->pl.n_hr > 0) {

@@ -72,7 +72,8 @@ const char* edge0_status_string(int status);
 
 /* ---- limits of this build ---- */
 #define EDGE0_MAX_LAYERS 48
-#define EDGE0_MAX_BATCH 4     /* sequences per decode call */
+#define EDGE0_MAX_BATCH 4     /* sequences per call of the persistent batch-1 engine */
+#define EDGE0_MAX_BATCHED 256 /* sequences per decode call on the batched path */
 #define EDGE0_MAX_K 8
 #define EDGE0_MAX_E 512
 
@@ -178,8 +179,13 @@ int edge0_pack_cols_T(const uint16_t* W, int out, int ld, int col0, int ncols, u
 
 /* ---- state ---- */
 /* workspace of a state of L layers (L = 1 for edge0_moe_int4_forward and
- * edge0_prerouter_topk) for B sequences */
+ * edge0_prerouter_topk) for B <= EDGE0_MAX_BATCH sequences */
 size_t edge0_workspace_bytes(int L, int B, int d, int E);
+/* workspace of a decode state of L layers for any B <= EDGE0_MAX_BATCHED:
+ * edge0_workspace_bytes for B <= EDGE0_MAX_BATCH, else the batched path's
+ * (layer output, x of every layer, dispatch lists, act of every (token, expert)
+ * pair); K top-k, I and Is the expert and shared intermediate, H the head width */
+size_t edge0_decode_workspace_bytes(int L, int B, int d, int E, int K, int I, int Is, int H);
 /* zero pred/exec/workspace; must precede the first decode call on a state */
 int edge0_state_init(edge0_route_state* st, cudaStream_t stream);
 /* HOST call: synchronises `stream`, returns the kernels' recorded status (EDGE0_OK,
@@ -225,8 +231,12 @@ int edge0_lora_delta(const edge0_lora_desc* lora, const uint16_t* v, int B, uint
 int edge0_decode_layer(const edge0_layer_desc* layer, uint16_t* h_inout, edge0_route_state* st,
                        int B, int step, cudaStream_t stream);
 
-/* All L layers of one decode step in one persistent launch (same semantics as L
- * successive edge0_decode_layer calls). */
+/* All L layers of one decode step (same semantics as L successive
+ * edge0_decode_layer calls).  B <= EDGE0_MAX_BATCH: one persistent launch;
+ * EDGE0_MAX_BATCH < B <= EDGE0_MAX_BATCHED: the batched path, a sequence of
+ * kernels per layer in which every active expert's weights are read once for
+ * all of its tokens, then every head of the step; it needs step >= 0 and a
+ * workspace of edge0_decode_workspace_bytes. */
 int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
                       edge0_route_state* st, int B, int step, cudaStream_t stream);
 

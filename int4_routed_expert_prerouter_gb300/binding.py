@@ -16,7 +16,7 @@ from .configs import SIGMOID_GROUP, Config
 
 P = C.c_void_p
 EDGE0_OK, EDGE0_EINVAL, EDGE0_ECUDA, EDGE0_ETIMEOUT, EDGE0_EUNSUPPORTED = 0, 1, 2, 3, 4
-MAX_LAYERS, MAX_BATCH = 48, 4
+MAX_LAYERS, MAX_BATCH, MAX_BATCHED = 48, 4, 256
 
 _lib = None
 
@@ -90,6 +90,8 @@ def _declare(L):
     L.edge0_pack_cols_T.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, P, P]
     L.edge0_workspace_bytes.argtypes = [C.c_int] * 4
     L.edge0_workspace_bytes.restype = C.c_size_t
+    L.edge0_decode_workspace_bytes.argtypes = [C.c_int] * 8
+    L.edge0_decode_workspace_bytes.restype = C.c_size_t
     L.edge0_state_init.argtypes = [C.POINTER(RouteState), P]
     L.edge0_state_error.argtypes = [C.POINTER(RouteState), P, C.POINTER(C.c_int)]
     L.edge0_prerouter_topk.argtypes = [C.POINTER(HeadDesc), P, P, P, C.c_int, P, P, P, P,
@@ -112,7 +114,7 @@ def _declare(L):
 EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_q4_gate_up",
             "edge0_q4_down_packed_bytes", "edge0_pack_q4_down", "edge0_f16_packed_bytes",
             "edge0_pack_f16", "edge0_pack_f16_kmajor", "edge0_pack_cols_T",
-            "edge0_workspace_bytes", "edge0_state_init",
+            "edge0_workspace_bytes", "edge0_decode_workspace_bytes", "edge0_state_init",
             "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
             "edge0_moe_int4_forward_noalloc"]
@@ -186,6 +188,11 @@ def pack_cols_T(W, col0, ncols, stream=None) -> torch.Tensor:
 
 def workspace_bytes(L, B, d, E) -> int:
     return int(lib().edge0_workspace_bytes(L, B, d, E))
+
+
+def decode_workspace_bytes(cfg: Config, B: int) -> int:
+    """Workspace of a decode state for B sequences (either path)."""
+    return int(lib().edge0_decode_workspace_bytes(cfg.L, B, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is, cfg.H))
 
 
 # ------------------------------------------------------------ the model ----
@@ -267,7 +274,8 @@ class DecodeState:
         self.pred_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
         self.pred_w = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.float32, device=dev)
         self.exec_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
-        nbytes = workspace_bytes(cfg.L, B, cfg.d, cfg.E)
+        nbytes = decode_workspace_bytes(cfg, B)
+        assert nbytes > 0, f"no decode path for B = {B}"
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         self.st = RouteState(cfg.L, B, cfg.K, _ptr(self.pred_ids), _ptr(self.pred_w),
                              _ptr(self.exec_ids), _ptr(self.workspace), nbytes)

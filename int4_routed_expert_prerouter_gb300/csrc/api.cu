@@ -24,8 +24,8 @@ int check_route(const edge0_route& r, int E, int K) {
     return EDGE0_OK;
 }
 
-int check_dims(const Dims& D, int B) {
-    if (B <= 0 || B > EDGE0_MAX_BATCH) return EDGE0_EINVAL;
+int check_dims(const Dims& D, int B, int max_b = EDGE0_MAX_BATCH) {
+    if (B <= 0 || B > max_b) return EDGE0_EINVAL;
     if (D.d <= 0 || D.d % kGroup || D.I <= 0 || D.I % kGroup || D.Is <= 0 || D.Is % kGroup)
         return EDGE0_EINVAL;
     if (D.H <= 0 || D.H % kGroup) return EDGE0_EINVAL;
@@ -153,10 +153,20 @@ int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_rout
         if (layers[l].has_head) { D.H = layers[l].head.H; break; }
     for (int l = 0; l < L; ++l)
         if (layers[l].lora_gate.A) { D.r = layers[l].lora_gate.r; break; }
-    int rc = check_dims(D, B);
+    const bool batched = B > EDGE0_MAX_BATCH;
+    int rc = check_dims(D, B, batched ? EDGE0_MAX_BATCHED : EDGE0_MAX_BATCH);
     if (rc) return rc;
-    rc = check_ws(st->L, D, B, st->workspace, st->workspace_bytes);
-    if (rc) return rc;
+    if (batched) {
+        // the batched path: explicit steps, d in halves of whole groups
+        if (step < 0 || D.d % 128) return EDGE0_EINVAL;
+        const int Imax = D.I > D.Is ? D.I : D.Is;
+        if (!st->workspace || !al16(st->workspace) ||
+            (long long)st->workspace_bytes < batch_ws_layout(st->L, B, D.d, D.E, D.K, Imax, D.H).total)
+            return EDGE0_EINVAL;
+    } else {
+        rc = check_ws(st->L, D, B, st->workspace, st->workspace_bytes);
+        if (rc) return rc;
+    }
     static_assert(sizeof(Prog) <= 32000, "kernel parameter block too large");
     Prog* p = new Prog;
     memset(p, 0, sizeof(Prog));
@@ -171,7 +181,7 @@ int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_rout
     p->Ls = st->L;
     p->ws = (char*)st->workspace;
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) rc = fill_layer(layers[l], D, st->L, p->layers[l]);
-    if (rc == EDGE0_OK) rc = engine_launch(*p, stream);
+    if (rc == EDGE0_OK) rc = batched ? batch_decode(*p, stream) : engine_launch(*p, stream);
     delete p;
     return rc;
 }
@@ -192,6 +202,13 @@ extern "C" const char* edge0_status_string(int status) {
 extern "C" size_t edge0_workspace_bytes(int L, int B, int d, int E) {
     if (L <= 0 || B <= 0 || d <= 0 || E <= 0) return 0;
     return (size_t)ws_layout(L, B, d, E).total;
+}
+
+extern "C" size_t edge0_decode_workspace_bytes(int L, int B, int d, int E, int K, int I, int Is, int H) {
+    if (L <= 0 || B <= 0 || d <= 0 || E <= 0 || K <= 0 || I <= 0 || Is <= 0 || H <= 0) return 0;
+    if (B <= EDGE0_MAX_BATCH) return (size_t)ws_layout(L, B, d, E).total;
+    if (B > EDGE0_MAX_BATCHED) return 0;
+    return (size_t)batch_ws_layout(L, B, d, E, K, I > Is ? I : Is, H).total;
 }
 
 extern "C" int edge0_state_init(edge0_route_state* st, cudaStream_t stream) {

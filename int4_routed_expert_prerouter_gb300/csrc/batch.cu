@@ -1,0 +1,667 @@
+// Batched decode path: one decode step for many independent sequences (B from
+// EDGE0_MAX_BATCH + 1 up to EDGE0_MAX_BATCHED), the shape of the batched
+// configurations (64 sequences on the 8B tier, 256 on the 35B tier).
+//
+// Per layer ("The Other Half of the Memory Wall", S3.1 "Math contract", S3.2
+// "Prediction-as-routing", S3.3, App. A), as stream-ordered kernels:
+//   k_norm      h = fp16(h + y_prev), x = fp16(RMSNorm(h) gamma), x group sums
+//   routing     prediction (prerouted layers, step > 0) or own router
+//               (k_dense + k_route)
+//   k_dispatch  tokens grouped by expert: the active experts in id order, each
+//               with its token list and routing weights
+//   k_dense     LoRA A_gate x, A_up x (shared expert)
+//   k_gu        gate/up of every active expert and the shared expert, once per
+//               expert for all of its tokens -> act = silu(g) up (fp32)
+//   k_down      down of the same -> y += w act (fp32 reductions)
+//   k_lora_vd   y += (alpha/r) B_down (A_down act_shared)
+// and after the last layer h = fp16(h + y), then every head of the step (one
+// flush per step: a head's prediction is consumed only at the next token):
+//   z = fc1 x + executed / previous one-hot columns, GELU, logits = fc2 g +
+//   linear_init x + its one-hot columns, top-K -> prediction for the next step.
+//
+// The weights are the same packed layouts as the persistent engine's (int4
+// nibbles enter mma.sync as fp16 subnormals q 2^-24, the epilogue rescales by
+// s 2^24 and adds b times the group sum of the input; fp32 inputs enter as a
+// hi + lo pair of fp16).  An expert's weights are read once per step however
+// many tokens it serves: the contraction becomes a skinny GEMM over its tokens.
+#include <string.h>
+
+#include "internal.cuh"
+#include "common.cuh"
+
+namespace edge0 {
+
+// ---------------------------------------------------------------- layout ----
+BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
+    BatchWs w;
+    auto al = [](long long x) { return (x + 255) / 256 * 256; };
+    long long o = kWsHeaderBytes;
+    w.y = o;     o += al((long long)B * d * 4);
+    w.xs = o;    o += al((long long)L * B * d * 2);
+    w.xsum = o;  o += al((long long)B * (d / kGroup) * 4);
+    w.lg = o;    o += al((long long)B * E * 4);
+    w.z = o;     o += al((long long)B * H * 4);
+    w.la = o;    o += al((long long)B * 32 * 4);
+    w.wsel = o;  o += al((long long)B * K * 4);
+    w.disp = o;  o += al((long long)(4 * (EDGE0_MAX_E + 1) + 1) * 4);
+    w.tok = o;   o += al((long long)B * K * 4);
+    w.wt = o;    o += al((long long)B * K * 4);
+    w.act = o;   o += al((long long)(B * K + B) * I * 4);
+    w.total = o;
+    return w;
+}
+
+namespace {
+
+struct Disp {   // dispatch of one layer (device)
+    int nact;
+    int sexp[EDGE0_MAX_E + 1];
+    int soff[EDGE0_MAX_E + 1];
+    int scnt[EDGE0_MAX_E + 1];
+};
+
+__device__ __forceinline__ void record_error(WsHeader* hdr, int code) {
+    atomicCAS(&hdr->error, 0, code);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------- k_norm -------
+// One CTA per token.  add_y: h = fp16(h + y) and y = 0 (the previous layer's
+// output); want_x: x = fp16(h rsqrt(mean h^2 + eps) gamma) into x_out and the
+// sums of each 64-input group of x into xsum.
+__global__ void __launch_bounds__(256) k_norm(__half* h, float* y, int add_y, const __half* gamma, float eps,
+                                              int d, __half* x_out, float* xsum, int want_x) {
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    __half* hb = h + (long long)b * d;
+    float* yb = y + (long long)b * d;
+    float ss = 0.f;
+    for (int i = 2 * tid; i < d; i += 512) {
+        __half2 hv = *reinterpret_cast<const __half2*>(hb + i);
+        if (add_y) {
+            const float2 f = __half22float2(hv);
+            const float2 yv = *reinterpret_cast<const float2*>(yb + i);
+            hv = __floats2half2_rn(f.x + yv.x, f.y + yv.y);
+            *reinterpret_cast<__half2*>(hb + i) = hv;
+            *reinterpret_cast<float2*>(yb + i) = make_float2(0.f, 0.f);
+        }
+        const float2 f = __half22float2(hv);
+        ss += f.x * f.x + f.y * f.y;
+    }
+    if (!want_x) return;
+    __shared__ float red[8];
+    __shared__ float rs;
+    ss = warp_sum(ss);
+    if (lane == 0) red[wid] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < 8; ++w) s += red[w];
+        rs = rsqrtf(s / (float)d + eps);
+    }
+    __syncthreads();
+    const float r = rs;
+    // 512 inputs per pass: warp w covers inputs [64 w, 64 w + 64) of the pass,
+    // exactly one group
+    for (int i = 2 * tid; i < d; i += 512) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(hb + i));
+        float g0 = 1.f, g1 = 1.f;
+        if (gamma) {
+            const float2 gg = __half22float2(*reinterpret_cast<const __half2*>(gamma + i));
+            g0 = gg.x;
+            g1 = gg.y;
+        }
+        const __half2 xv = __floats2half2_rn(f.x * r * g0, f.y * r * g1);
+        *reinterpret_cast<__half2*>(x_out + (long long)b * d + i) = xv;
+        const float2 xf = __half22float2(xv);
+        const float s = warp_sum(xf.x + xf.y);
+        if (lane == 0) xsum[(long long)b * (d / kGroup) + i / kGroup] = s;
+    }
+}
+
+// ------------------------------------------------------------- k_dense ------
+// out[b][o] (=, or += with accumulate) sum_k W[o][k] X[b][k] for rows o < N and
+// tokens b < B.  W packed fp16: kmajor = 0: [half][16-row tile][group of the
+// half][4 steps x 512 B] (2 KB units); kmajor = 1: [16-input step][row tile] x
+// 512 B.  X: fp16 [B][ldx] (xh) or fp32 (xf, entered as hi + lo fp16).  One CTA
+// per (row tile, 32 tokens); its 4 warps split the inputs.
+template <bool F32IN>
+__global__ void __launch_bounds__(128) k_dense(const char* __restrict__ W, int kmajor, int N, int Kin,
+                                               const __half* __restrict__ xh, const float* __restrict__ xf,
+                                               int ldx, int B, float* out, int ldo, int accumulate) {
+    const int rt = blockIdx.x, tb = blockIdx.y * 32;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
+    const int nks = Kin / 16, RT = (N + 15) / 16, hn = Kin / kGroup / 2;
+    float acc[4][4], accl[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] = accl[n][e] = 0.f;
+    for (int ks = wid; ks < nks; ks += 4) {
+        const char* ap;
+        if (kmajor) {
+            ap = W + ((long long)ks * RT + rt) * kF16Step;
+        } else {
+            const int gg = ks >> 2, s = ks & 3, h = gg / hn, gl = gg - h * hn;
+            ap = W + ((long long)(h * RT + rt) * hn + gl) * kF16Unit + s * kF16Step;
+        }
+        const uint4 av = __ldg(reinterpret_cast<const uint4*>(ap + 16 * lane));
+        const uint32_t A[4] = {av.x, av.y, av.z, av.w};
+        const int k0 = ks * 16 + 2 * t;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int tok = tb + n * 8 + g;
+            uint32_t b0 = 0u, b1 = 0u, l0 = 0u, l1 = 0u;
+            if (tok < B) {
+                if (!F32IN) {
+                    b0 = __ldg(reinterpret_cast<const uint32_t*>(xh + (long long)tok * ldx + k0));
+                    b1 = __ldg(reinterpret_cast<const uint32_t*>(xh + (long long)tok * ldx + k0 + 8));
+                } else {
+                    const float2 f0 = __ldg(reinterpret_cast<const float2*>(xf + (long long)tok * ldx + k0));
+                    const float2 f1 = __ldg(reinterpret_cast<const float2*>(xf + (long long)tok * ldx + k0 + 8));
+                    const __half2 h0 = __floats2half2_rn(f0.x, f0.y), h1 = __floats2half2_rn(f1.x, f1.y);
+                    const float2 r0 = __half22float2(h0), r1 = __half22float2(h1);
+                    b0 = *reinterpret_cast<const uint32_t*>(&h0);
+                    b1 = *reinterpret_cast<const uint32_t*>(&h1);
+                    l0 = pack_h2((f0.x - r0.x) * kLoScale, (f0.y - r0.y) * kLoScale);
+                    l1 = pack_h2((f1.x - r1.x) * kLoScale, (f1.y - r1.y) * kLoScale);
+                }
+            }
+            mma_16816(acc[n], A, b0, b1);
+            if (F32IN) mma_16816(accl[n], A, l0, l1);
+        }
+    }
+    __shared__ float red[4][16][33];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = F32IN ? acc[n][e] + accl[n][e] * kLoInv : acc[n][e];
+        red[wid][g][n * 8 + 2 * t] = v[0];
+        red[wid][g][n * 8 + 2 * t + 1] = v[1];
+        red[wid][g + 8][n * 8 + 2 * t] = v[2];
+        red[wid][g + 8][n * 8 + 2 * t + 1] = v[3];
+    }
+    __syncthreads();
+    for (int i = tid; i < 16 * 32; i += 128) {
+        const int r = i >> 5, c = i & 31;
+        const int row = rt * 16 + r, tok = tb + c;
+        if (row < N && tok < B) {
+            const float s = (red[0][r][c] + red[1][r][c]) + (red[2][r][c] + red[3][r][c]);
+            float* o = out + (long long)tok * ldo + row;
+            *o = accumulate ? *o + s : s;
+        }
+    }
+}
+
+// ----------------------------------------------------------- k_onehot -------
+// z[b][n] += sum over executed e of M[e][n] + sum over previous e of M[E + e][n]
+// (M = [2E][N] fp16: the one-hot columns of a head matrix, transposed), then
+// GELU (erf form) if `gelu`.
+__global__ void k_onehot(float* z, int ldz, int N, const __half* __restrict__ M, const int32_t* ids,
+                         const int32_t* prev, int K, int E, int gelu) {
+    const int b = blockIdx.y, n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    // (ids outside [0, E) were recorded as errors by the dispatch; read column 0)
+    auto col = [E](int e) { return e >= 0 && e < E ? e : 0; };
+    float oh = 0.f;
+    for (int k = 0; k < K; ++k) oh += __half2float(M[(long long)col(ids[b * K + k]) * N + n]);
+    if (prev)
+        for (int k = 0; k < K; ++k) oh += __half2float(M[(long long)(E + col(prev[b * K + k])) * N + n]);
+    float v = z[(long long)b * ldz + n] + oh;
+    if (gelu) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    z[(long long)b * ldz + n] = v;
+}
+
+// ------------------------------------------------------------ k_route -------
+// Routing rule of App. A, one token per warp, 8 warps per CTA.
+__global__ void __launch_bounds__(256) k_route(const float* logits, int ldl, int B, int E, int K, int kind,
+                                               int ng, int G, float scale, const float* bias, int32_t* ids_out,
+                                               float* w_out) {
+    extern __shared__ float sm[];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, b = blockIdx.x * 8 + wid;
+    float* lg = sm + wid * 3 * E;
+    int* rid = reinterpret_cast<int*>(sm + 8 * 3 * E) + wid * EDGE0_MAX_K;
+    float* rw = sm + 8 * 3 * E + 8 * EDGE0_MAX_K + wid * EDGE0_MAX_K;
+    if (b >= B) return;
+    for (int e = lane; e < E; e += 32) lg[e] = logits[(long long)b * ldl + e];
+    __syncwarp();
+    warp_route(lg, E, K, kind, ng, G, scale, bias, lg + E, rid, rw, lane);
+    if (lane < K) {
+        ids_out[b * K + lane] = rid[lane];
+        w_out[b * K + lane] = rw[lane];
+    }
+}
+
+// --------------------------------------------------------- k_dispatch -------
+// The active experts of a layer in id order, each with the positions of its
+// (token, weight) pairs; one CTA.  An id outside [0, E) records EDGE0_EINVAL
+// and counts as expert 0.
+__global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const float* w, int B, int K, int E,
+                                                   Disp* D, int* tok, float* wt, WsHeader* hdr) {
+    __shared__ int cnt[EDGE0_MAX_E], off[EDGE0_MAX_E], fill[EDGE0_MAX_E];
+    const int tid = threadIdx.x, n = B * K;
+    for (int e = tid; e < E; e += blockDim.x) cnt[e] = fill[e] = 0;
+    __syncthreads();
+    for (int p = tid; p < n; p += blockDim.x) {
+        int e = ids[p];
+        if (e < 0 || e >= E) { record_error(hdr, EDGE0_EINVAL); e = 0; }
+        atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0, a = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = run;
+            if (cnt[e] > 0) {
+                D->sexp[a] = e;
+                D->soff[a] = run;
+                D->scnt[a] = cnt[e];
+                ++a;
+            }
+            run += cnt[e];
+        }
+        D->nact = a;
+    }
+    __syncthreads();
+    for (int p = tid; p < n; p += blockDim.x) {
+        int e = ids[p];
+        if (e < 0 || e >= E) e = 0;
+        const int pos = off[e] + atomicAdd(&fill[e], 1);
+        tok[pos] = p / K;
+        wt[pos] = w[p];
+    }
+}
+
+// One expert of a layer for a CTA: blockIdx.y < nact is a routed expert (its
+// weights through the slot table), blockIdx.y == nact the shared expert (every
+// token, weight 1).  False: nothing to do.
+struct Slot {
+    const char* gu;
+    const char* dn;
+    int I, m, pos0;
+    const int* toks;     // token of each position (null: position = token)
+    const float* wts;    // weight of each position (null: 1)
+    bool shared;
+};
+__device__ __forceinline__ bool slot_of(int j, const Disp* D, const LayerP& Ly, int B, int K, int d, int I,
+                                        int Is, const int* tok, const float* wt, WsHeader* hdr, Slot& s) {
+    const int nact = D->nact;
+    if (j < nact) {
+        const int e = D->sexp[j];
+        const int sl = Ly.slot_table ? Ly.slot_table[e] : e;
+        if (sl < 0 || sl >= Ly.n_slots) {
+            if (threadIdx.x == 0) record_error(hdr, EDGE0_EINVAL);
+            return false;
+        }
+        s.gu = Ly.gu + (long long)sl * q4_bytes(2 * I, d);
+        s.dn = Ly.down + (long long)sl * q4_bytes(d, I);
+        s.I = I;
+        s.m = D->scnt[j];
+        s.pos0 = D->soff[j];
+        s.toks = tok + s.pos0;
+        s.wts = wt + s.pos0;
+        s.shared = false;
+        return true;
+    }
+    if (j == nact && Ly.sh_gu) {
+        s.gu = Ly.sh_gu;
+        s.dn = Ly.sh_down;
+        s.I = Is;
+        s.m = B;
+        s.pos0 = B * K;
+        s.toks = nullptr;
+        s.wts = nullptr;
+        s.shared = true;
+        return true;
+    }
+    return false;
+}
+
+// --------------------------------------------------------------- k_gu -------
+// gate/up of one expert for all of its tokens: warp w of CTA x takes the
+// interleaved 16-row tile 4 x + w (gate rows 8 x' .. + 7 and the same up rows)
+// over all of d; tokens in blocks of 32 (4 mma column tiles of 8 tokens).
+// act[position][row] = silu(gate) up (the shared expert's gate and up with their
+// LoRA terms (alpha/r) B (A x), A x precomputed in la).
+__global__ void __launch_bounds__(128) k_gu(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
+                                            const __half* __restrict__ x, const float* __restrict__ xsum,
+                                            const float* la, int lora, int r, int B, int K, int d, int I, int Is,
+                                            int Imax, float* act, WsHeader* hdr) {
+    Slot S;
+    if (!slot_of(blockIdx.y, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    const int rt = blockIdx.x * 4 + wid;
+    if (rt * kHalfRow >= S.I) return;
+    const int n_gd = d / kGroup, hn = n_gd / 2, RTI = S.I / kHalfRow;
+    for (int tb = 0; tb < S.m; tb += 32) {
+        int tk[4];   // token of the lane's B column in each column tile
+        int tc[4][2];   // tokens of the lane's C columns 2t, 2t + 1
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int p = tb + n * 8 + g;
+            tk[n] = p < S.m ? (S.toks ? S.toks[p] : p) : -1;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int q = tb + n * 8 + 2 * t + c;
+                tc[n][c] = q < S.m ? (S.toks ? S.toks[q] : q) : -1;
+            }
+        }
+        float racc[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) racc[n][e] = 0.f;
+        for (int gg = 0; gg < n_gd; ++gg) {
+            const int h = gg / hn, gl = gg - h * hn;
+            const char* unit = S.gu + ((long long)(h * RTI + rt) * hn + gl) * kQ4Unit;
+            const uint4 wv = __ldg(reinterpret_cast<const uint4*>(unit + 16 * lane));
+            const uint2 sc = __ldg(reinterpret_cast<const uint2*>(unit + 512 + 8 * g));
+            const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+            float acc[4][4];
+#pragma unroll
+            for (int n = 0; n < 4; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                uint32_t A[4];
+                q4_masks(wq[s], A);
+                const int k0 = gg * kGroup + s * 16 + 2 * t;
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    uint32_t b0 = 0u, b1 = 0u;
+                    if (tk[n] >= 0) {
+                        const __half* xr = x + (long long)tk[n] * d + k0;
+                        b0 = __ldg(reinterpret_cast<const uint32_t*>(xr));
+                        b1 = __ldg(reinterpret_cast<const uint32_t*>(xr + 8));
+                    }
+                    mma_16816(acc[n], A, b0, b1);
+                }
+            }
+            const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) of row g
+            const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) of row g + 8
+            const float sg0 = __low2float(s0) * kTwo24, bg0 = __high2float(s0);
+            const float sg1 = __low2float(s1) * (kTwo24 / 16.0f), bg1 = __high2float(s1);
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                const float xs0 = tc[n][0] >= 0 ? __ldg(xsum + (long long)tc[n][0] * n_gd + gg) : 0.f;
+                const float xs1 = tc[n][1] >= 0 ? __ldg(xsum + (long long)tc[n][1] * n_gd + gg) : 0.f;
+                racc[n][0] += sg0 * acc[n][0] + bg0 * xs0;
+                racc[n][1] += sg0 * acc[n][1] + bg0 * xs1;
+                racc[n][2] += sg1 * acc[n][2] + bg1 * xs0;
+                racc[n][3] += sg1 * acc[n][3] + bg1 * xs1;
+            }
+        }
+        const int arow = rt * kHalfRow + g;
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int q = tb + n * 8 + 2 * t + c;
+                if (q >= S.m) continue;
+                float gate = racc[n][c], up = racc[n][2 + c];
+                if (S.shared && lora) {
+                    const int b = tc[n][c];
+                    const __half* bg = Ly.lora_Bg + (long long)arow * r;
+                    const __half* bu = Ly.lora_Bu + (long long)arow * r;
+                    float dg = 0.f, du = 0.f;
+                    for (int qq = 0; qq < r; ++qq) {
+                        dg += __half2float(bg[qq]) * la[b * 32 + qq];
+                        du += __half2float(bu[qq]) * la[b * 32 + 16 + qq];
+                    }
+                    gate += Ly.lora_scale * dg;
+                    up += Ly.lora_scale * du;
+                }
+                act[(long long)(S.pos0 + q) * Imax + arow] = silu_f(gate) * up;
+            }
+    }
+}
+
+// ------------------------------------------------------------- k_down -------
+// down of one expert for all of its tokens: warp w of CTA x takes the 16 output
+// rows of row tile 4 x + w over all of the expert's act rows; tokens in blocks of
+// 16 (4 mma column tiles of 4 tokens x hi/lo); y[token] += w act_out (fp32
+// reductions).
+__global__ void __launch_bounds__(128) k_down(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
+                                              const float* __restrict__ act, int B, int K, int d, int I, int Is,
+                                              int Imax, float* y, WsHeader* hdr) {
+    Slot S;
+    if (!slot_of(blockIdx.y, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    const int rt = blockIdx.x * 4 + wid, n_rtd = d / kRowTile, nh = n_rtd / 2;
+    if (rt >= n_rtd) return;
+    const int h = rt >= nh ? 1 : 0, i = rt - h * nh;
+    const int ngi = S.I / kGroup;
+    const int tokc = g >> 1, part = g & 1;
+    for (int tb = 0; tb < S.m; tb += 16) {
+        int pb[4];   // position of the lane's B column token in each column tile
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int p = tb + n * 4 + tokc;
+            pb[n] = p < S.m ? S.pos0 + p : -1;
+        }
+        float o[4][2];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) o[n][0] = o[n][1] = 0.f;
+        for (int gg = 0; gg < ngi; ++gg) {
+            const char* grp = S.dn + (long long)gg * n_rtd * kQ4Unit + (long long)h * nh * kQ4Unit;
+            const uint2 sc = __ldg(reinterpret_cast<const uint2*>(grp + 4 * nh * kQ4Quarter + i * kQ4Scales + 8 * g));
+            float acc[4][4], qs[4];
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                qs[n] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+            }
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t wq = __ldg(reinterpret_cast<const uint32_t*>(grp + (s * nh + i) * kQ4Quarter + 4 * lane));
+                uint32_t A[4];
+                q4_masks(wq, A);
+                const int k0 = gg * kGroup + s * 16 + 2 * t;
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    uint32_t b0 = 0u, b1 = 0u;
+                    if (pb[n] >= 0) {
+                        const float* ar = act + (long long)pb[n] * Imax + k0;
+                        const float2 a0 = *reinterpret_cast<const float2*>(ar);
+                        const float2 a1 = *reinterpret_cast<const float2*>(ar + 8);
+                        qs[n] += (a0.x + a0.y) + (a1.x + a1.y);
+                        const __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a1.x, a1.y);
+                        if (!part) {
+                            b0 = *reinterpret_cast<const uint32_t*>(&h0);
+                            b1 = *reinterpret_cast<const uint32_t*>(&h1);
+                        } else {
+                            const float2 r0 = __half22float2(h0), r1 = __half22float2(h1);
+                            b0 = pack_h2((a0.x - r0.x) * kLoScale, (a0.y - r0.y) * kLoScale);
+                            b1 = pack_h2((a1.x - r1.x) * kLoScale, (a1.y - r1.y) * kLoScale);
+                        }
+                    }
+                    mma_16816(acc[n], A, b0, b1);
+                }
+            }
+            const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);
+            const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);
+            const float sg0 = __low2float(s0) * kTwo24, bg0 = __high2float(s0);
+            const float sg1 = __low2float(s1) * (kTwo24 / 16.0f), bg1 = __high2float(s1);
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+                // group sum of act for the token of column tile n's lane group g:
+                // the 4 lanes of g hold 16 inputs each; lane (2 t) 4 holds token t
+                float q = qs[n];
+                q += __shfl_xor_sync(0xffffffffu, q, 1);
+                q += __shfl_xor_sync(0xffffffffu, q, 2);
+                const float qt = __shfl_sync(0xffffffffu, q, (2 * t) * 4);
+                o[n][0] += sg0 * (acc[n][0] + acc[n][1] * kLoInv) + bg0 * qt;
+                o[n][1] += sg1 * (acc[n][2] + acc[n][3] * kLoInv) + bg1 * qt;
+            }
+        }
+        const int row = rt * kRowTile + g;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int p = tb + n * 4 + t;
+            if (p >= S.m) continue;
+            const int b = S.toks ? S.toks[p] : p;
+            const float w = S.wts ? S.wts[p] : 1.f;
+            red_add_f32(y + (long long)b * d + row, w * o[n][0]);
+            red_add_f32(y + (long long)b * d + row + 8, w * o[n][1]);
+        }
+    }
+}
+
+// ---------------------------------------------------------- k_lora_vd -------
+// One CTA per token: v = A_down act_shared (r values), y += (alpha/r) B_down v.
+__global__ void __launch_bounds__(256) k_lora_vd(const float* act, int Imax, int pos0, const __half* AdT,
+                                                 const __half* Bd, int r, int Is, int d, float scale, float* y) {
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    __shared__ float red[8][16];
+    __shared__ float vs[16];
+    float acc[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+    const float* a = act + (long long)(pos0 + b) * Imax;
+    for (int k = tid; k < Is; k += 256) {
+        const float av = a[k];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (q < r) acc[q] += __half2float(AdT[(long long)k * r + q]) * av;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const float s = warp_sum(acc[q]);
+        if (lane == 0) red[wid][q] = s;
+    }
+    __syncthreads();
+    if (tid < 16) {
+        float s = 0.f;
+        for (int w = 0; w < 8; ++w) s += red[w][tid];
+        vs[tid] = s;
+    }
+    __syncthreads();
+    for (int row = tid; row < d; row += 256) {
+        float s = 0.f;
+        for (int q = 0; q < r; ++q) s += __half2float(Bd[(long long)row * r + q]) * vs[q];
+        y[(long long)b * d + row] += scale * s;
+    }
+}
+
+// launch helpers
+template <bool F32IN>
+int dense(const char* W, int kmajor, int N, int Kin, const __half* xh, const float* xf, int ldx, int B,
+          float* out, int ldo, int accumulate, cudaStream_t st) {
+    const dim3 grid((N + 15) / 16, (B + 31) / 32);
+    k_dense<F32IN><<<grid, 128, 0, st>>>(W, kmajor, N, Kin, xh, xf, ldx, B, out, ldo, accumulate);
+    return cudaGetLastError() == cudaSuccess ? EDGE0_OK : EDGE0_ECUDA;
+}
+
+int route(const float* lg, int B, int E, int K, int kind, int ng, int G, float scale, const float* bias,
+          int32_t* ids, float* w, cudaStream_t st) {
+    const size_t smem = (size_t)8 * 3 * E * 4 + 2 * 8 * EDGE0_MAX_K * 4;
+    if (smem > 48 * 1024) {   // E > 496: opt in to more dynamic shared memory
+        static int done = 0;
+        if (!done) {
+            if (cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                return EDGE0_ECUDA;
+            done = 1;
+        }
+    }
+    k_route<<<(B + 7) / 8, 256, smem, st>>>(lg, E, B, E, K, kind, ng, G, scale, bias, ids, w);
+    return cudaGetLastError() == cudaSuccess ? EDGE0_OK : EDGE0_ECUDA;
+}
+
+}  // namespace
+
+// One decode step of L layers for B > EDGE0_MAX_BATCH sequences (host: validates
+// nothing beyond what the caller checked; enqueues on `st`).
+int batch_decode(const Prog& p, cudaStream_t st) {
+    const int L = p.L, B = p.B, K = p.K, d = p.d, E = p.E, I = p.I, Is = p.Is, H = p.H, r = p.r;
+    const int Imax = I > Is ? I : Is;
+    const BatchWs W = batch_ws_layout(p.Ls, B, d, E, K, Imax, H);
+    char* ws = p.ws;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    float* y = reinterpret_cast<float*>(ws + W.y);
+    __half* xs = reinterpret_cast<__half*>(ws + W.xs);
+    float* xsum = reinterpret_cast<float*>(ws + W.xsum);
+    float* lg = reinterpret_cast<float*>(ws + W.lg);
+    float* z = reinterpret_cast<float*>(ws + W.z);
+    float* la = reinterpret_cast<float*>(ws + W.la);
+    float* wsel = reinterpret_cast<float*>(ws + W.wsel);
+    Disp* D = reinterpret_cast<Disp*>(ws + W.disp);
+    int* tok = reinterpret_cast<int*>(ws + W.tok);
+    float* wt = reinterpret_cast<float*>(ws + W.wt);
+    float* act = reinterpret_cast<float*>(ws + W.act);
+    const int step = p.step, par = step & 1;
+    const int slots = (B * K < E ? B * K : E) + 1;
+    auto ok = [] { return cudaGetLastError() == cudaSuccess; };
+    int rc = EDGE0_OK;
+    for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
+        const LayerP& Ly = p.layers[l];
+        const long long srow = (long long)Ly.sidx * B * K;
+        __half* x = xs + (long long)Ly.sidx * B * d;
+        k_norm<<<B, 256, 0, st>>>(p.h_io, y, l > 0, Ly.gamma, Ly.eps, d, x, xsum, 1);
+        if (!ok()) return EDGE0_ECUDA;
+        int32_t* exec = p.exec_ids + (long long)par * p.Ls * B * K + srow;
+        const float* w;
+        if ((Ly.flags & LF_PREROUTED) && step > 0) {
+            const long long o = (long long)(par ^ 1) * p.Ls * B * K + srow;
+            if (cudaMemcpyAsync(exec, p.pred_ids + o, (size_t)B * K * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return EDGE0_ECUDA;
+            w = p.pred_w + o;
+        } else {
+            rc = dense<false>(Ly.router, 0, E, d, x, nullptr, d, B, lg, E, 0, st);
+            if (rc == EDGE0_OK)
+                rc = route(lg, B, E, K, Ly.route_kind, Ly.n_groups, Ly.topk_groups, Ly.route_scale, Ly.bias, exec,
+                           wsel, st);
+            w = wsel;
+        }
+        if (rc) return rc;
+        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, D, tok, wt, hdr);
+        if (!ok()) return EDGE0_ECUDA;
+        const int lora = (Ly.flags & LF_LORA) ? 1 : 0;
+        if (lora) {
+            rc = dense<false>(Ly.lora_Ag, 0, r, d, x, nullptr, d, B, la, 32, 0, st);
+            if (rc == EDGE0_OK) rc = dense<false>(Ly.lora_Au, 0, r, d, x, nullptr, d, B, la + 16, 32, 0, st);
+            if (rc) return rc;
+        }
+        k_gu<<<dim3((Imax / kHalfRow + 3) / 4, slots), 128, 0, st>>>(Ly, D, tok, wt, x, xsum, la, lora, r, B, K, d,
+                                                                     I, Is, Imax, act, hdr);
+        if (!ok()) return EDGE0_ECUDA;
+        k_down<<<dim3(d / kRowTile / 4, slots), 128, 0, st>>>(Ly, D, tok, wt, act, B, K, d, I, Is, Imax, y, hdr);
+        if (!ok()) return EDGE0_ECUDA;
+        if (lora) {
+            k_lora_vd<<<B, 256, 0, st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is, d, Ly.lora_scale, y);
+            if (!ok()) return EDGE0_ECUDA;
+        }
+    }
+    // the last layer's output
+    k_norm<<<B, 256, 0, st>>>(p.h_io, y, 1, nullptr, 0.f, d, nullptr, nullptr, 0);
+    if (!ok()) return EDGE0_ECUDA;
+    // head flush: every head of the step, from its layer's x and routing
+    for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
+        const LayerP& Ly = p.layers[l];
+        if (!(Ly.flags & LF_HEAD)) continue;
+        const long long srow = (long long)Ly.sidx * B * K;
+        const __half* x = xs + (long long)Ly.sidx * B * d;
+        const int32_t* exec = p.exec_ids + (long long)par * p.Ls * B * K + srow;
+        const int32_t* prev = step > 0 ? p.exec_ids + (long long)(par ^ 1) * p.Ls * B * K + srow : nullptr;
+        rc = dense<false>(Ly.fc1, 0, H, d, x, nullptr, d, B, z, H, 0, st);
+        if (rc) break;
+        k_onehot<<<dim3((H + 127) / 128, B), 128, 0, st>>>(z, H, H, Ly.fc1_oh, exec, prev, K, E, 1);
+        if (!ok()) return EDGE0_ECUDA;
+        rc = dense<true>(Ly.fc2, 1, E, H, nullptr, z, H, B, lg, E, 0, st);
+        if (rc == EDGE0_OK) rc = dense<false>(Ly.linit, 0, E, d, x, nullptr, d, B, lg, E, 1, st);
+        if (rc) break;
+        k_onehot<<<dim3((E + 127) / 128, B), 128, 0, st>>>(lg, E, E, Ly.linit_oh, exec, prev, K, E, 0);
+        if (!ok()) return EDGE0_ECUDA;
+        const long long o = (long long)par * p.Ls * B * K + (long long)Ly.head_target * B * K;
+        rc = route(lg, B, E, K, Ly.head_route_kind, Ly.head_n_groups, Ly.head_topk_groups, Ly.head_route_scale,
+                   Ly.head_bias, p.pred_ids + o, p.pred_w + o, st);
+    }
+    return rc;
+}
+
+}  // namespace edge0

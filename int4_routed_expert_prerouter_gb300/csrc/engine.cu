@@ -37,6 +37,7 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "common.cuh"
 
 namespace edge0 {
 
@@ -668,92 +669,6 @@ __device__ __forceinline__ bool cbar_or(bool v) {
     return r != 0;
 }
 
-// ---------------------------------------------------------- routing -----
-// top-K over `score` (E values, E <= 512) by one warp, value descending, lower
-// index first on ties; masked entries are -inf.  Lane l owns entries l + 32 i.
-__device__ __noinline__ void warp_topk(const float* score, int E, int K, int* ids, int lane) {
-    unsigned taken = 0;   // bit i: entry lane + 32 i already selected
-    for (int k = 0; k < K; ++k) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int i = 0, e = lane; e < E; ++i, e += 32) {
-            if ((taken >> i) & 1u) continue;
-            const float v = score[e];
-            if (v > bv) { bv = v; bi = e; }   // e increases: ties keep the lower index
-        }
-        for (int s = 16; s; s >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if (bi == 0x7fffffff) bi = 0;   // fewer than K candidates (not reachable for valid shapes)
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == 0) ids[k] = bi;
-    }
-    __syncwarp();
-}
-
-// Routing rule of App. A, one token per warp.  logits: E fp32 in shared memory;
-// scratch: 2 E floats of shared memory for this warp.
-__device__ __noinline__ void warp_route(const float* logits, int E, int K, int kind, int n_groups,
-                                        int G, float scale, const float* bias, float* scratch,
-                                        int* ids, float* w, int lane) {
-    float* sel = scratch;
-    float* sig = scratch + E;
-    const bool group = kind == EDGE0_ROUTE_SIGMOID_GROUP;
-    for (int e = lane; e < E; e += 32) {
-        const float l = logits[e];
-        const float s = group ? 1.0f / (1.0f + expf(-l)) : l;
-        sig[e] = s;
-        sel[e] = bias ? s + bias[e] : s;
-    }
-    __syncwarp();
-    if (group) {
-        const int per = E / n_groups;
-        // group score: sum of the two largest selection scores of the group
-        float gscore = -INFINITY;
-        if (lane < n_groups) {
-            float a = -INFINITY, b = -INFINITY;
-            for (int j = 0; j < per; ++j) {
-                const float v = sel[lane * per + j];
-                if (v > a) { b = a; a = v; }
-                else if (v > b) { b = v; }
-            }
-            gscore = a + b;
-        }
-        // keep the best G groups (lower group index on ties)
-        unsigned keep = 0;
-        for (int k = 0; k < G; ++k) {
-            const bool cand = lane < n_groups && !((keep >> lane) & 1u);
-            float bv = cand ? gscore : -INFINITY;
-            int bi = cand ? lane : 0x7fffffff;
-            for (int s = 16; s; s >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            if (bi < 32) keep |= 1u << bi;
-        }
-        for (int e = lane; e < E; e += 32)
-            if (!((keep >> (e / per)) & 1u)) sel[e] = -INFINITY;
-        __syncwarp();
-    }
-    warp_topk(sel, E, K, ids, lane);
-    if (lane == 0) {
-        if (group) {
-            float sum = 0.0f;
-            for (int k = 0; k < K; ++k) sum += sig[ids[k]];
-            for (int k = 0; k < K; ++k) w[k] = scale * sig[ids[k]] / (sum + 1e-20f);
-        } else {
-            const float mx = sel[ids[0]];
-            float sum = 0.0f;
-            for (int k = 0; k < K; ++k) sum += expf(sel[ids[k]] - mx);
-            for (int k = 0; k < K; ++k) w[k] = expf(sel[ids[k]] - mx) / sum;
-        }
-    }
-    __syncwarp();
-}
-
 // distinct experts of a layer's routing in order of first appearance; false if
 // an id is out of range (single thread)
 __device__ bool make_dist(int l) {
@@ -1004,14 +919,6 @@ __device__ __forceinline__ XFrag xfrag() {
     f.base = SM<uint2>(c.pl.xf) + (f.live ? tok : 0) * 4 + t;
     f.stride = prg().B * 4;
     return f;
-}
-
-__device__ __forceinline__ void q4_masks(uint32_t w, uint32_t A[4]) {
-    const uint32_t w8 = w >> 8;
-    A[0] = w & 0x000F000Fu;    // row g,   k 2t | 2t+1
-    A[1] = w & 0x00F000F0u;    // row g+8, k 2t | 2t+1   (x16)
-    A[2] = w8 & 0x000F000Fu;   // row g,   k 2t+8 | 2t+9
-    A[3] = w8 & 0x00F000F0u;   // row g+8, k 2t+8 | 2t+9 (x16)
 }
 
 // fp16 units [a, b) (x source) accumulated into acc (rows g, g + 8; column 2t = token t)

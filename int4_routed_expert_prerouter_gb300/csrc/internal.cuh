@@ -150,6 +150,16 @@ inline __host__ __device__ WsLayout ws_layout(int Ls, int B, int d, int E) {
     return w;
 }
 
+// Workspace of the batched decode path (B > EDGE0_MAX_BATCH), after the header:
+//   y [B][d] fp32 layer output, xs [Ls][B][d] fp16 x of every layer (heads),
+//   xsum [B][d/64] group sums of x, lg [B][E] logits, z [B][H] head hidden,
+//   la [B][32] LoRA A x, wsel [B][K] own-router weights, disp (dispatch of a
+//   layer), tok / wt [B K] (token, weight) per position, act [B K + B][Imax].
+struct BatchWs {
+    long long y, xs, xsum, lg, z, la, wsel, disp, tok, wt, act, total;
+};
+BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H);
+
 // --------------------------------------------------------------- PTX -----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -299,5 +309,9 @@ int engine_check(Prog& p, int nct, int smem_max, int* smem_bytes);
 // launch the engine for `p` on `stream` (cooperative, CTA pairs); fills p's derived
 // fields.  Allocates nothing.
 int engine_launch(Prog& p, cudaStream_t stream);
+
+// the batched decode path (batch.cu): one step of p.L layers for p.B sequences
+struct Prog;
+int batch_decode(const Prog& p, cudaStream_t stream);
 
 }  // namespace edge0

@@ -85,3 +85,33 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.edge0_moe_int4_forward(C.byref(moe), C.c_void_p(18), x, x, 1, x, x, 1 << 20, None) == E
     # workspace too small
     assert lib.edge0_moe_int4_forward(C.byref(moe), x, x, x, 1, x, x, 64, None) == E
+
+
+def test_batched_path_sizes_and_host_validation(lib):
+    from int4_routed_expert_prerouter_gb300 import configs
+    c = configs.STACK8
+    size = lambda B: lib.edge0_decode_workspace_bytes(c.L, B, c.d, c.E, c.K, c.I, c.Is, c.H)
+    # B <= 4: the persistent engine's workspace
+    assert size(4) == lib.edge0_workspace_bytes(c.L, 4, c.d, c.E)
+    # B > 4: at least the layer output, x of every layer and act of every
+    # (token, expert) pair of the batched path
+    B = 64
+    assert size(B) >= 256 + B * c.d * 4 + c.L * B * c.d * 2 + (B * c.K + B) * c.I * 4
+    assert size(256) > size(64) > 0
+    assert size(257) == 0
+    # decode calls on the batched path that the host rejects before any launch
+    E = binding.EDGE0_EINVAL
+    p = C.c_void_p(256)
+    layer = binding.LayerDesc()
+    layer.moe = binding.MoeDesc(c.d, c.E, c.K, c.I, c.Is, p, p, None, None, None, 0)
+    layer.router = p
+
+    def state(B, nbytes):
+        return binding.RouteState(c.L, B, c.K, p, p, p, p, nbytes)
+
+    st = state(257, 1 << 40)
+    assert lib.edge0_decode_step(C.byref(layer), 1, p, C.byref(st), 257, 0, None) == E   # B above the limit
+    st = state(64, 1 << 40)
+    assert lib.edge0_decode_step(C.byref(layer), 1, p, C.byref(st), 64, -1, None) == E   # step counter: engine only
+    st = state(64, 4096)
+    assert lib.edge0_decode_step(C.byref(layer), 1, p, C.byref(st), 64, 0, None) == E    # workspace too small

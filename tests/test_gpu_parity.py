@@ -408,6 +408,51 @@ def test_decode_35b_stack_40_layers_full_size_properties():
         assert torch.isfinite(h.float()).all()
 
 
+# ------------------------------------------------ batched decode path ----
+# B > 4 sequences run on the batched path (experts grouped by token lists).
+def test_batched_toy_ragged_batch():
+    cfg = configs.TOY.with_(B=7)
+    model = inputs.make_model(cfg, seed=6, gamma="random")
+    assert _run_stack(cfg, model, 5) >= 3
+
+
+def test_batched_toy_layer_by_layer():
+    cfg = configs.TOY.with_(B=5)
+    model = inputs.make_model(cfg, seed=8)
+    assert _run_stack(cfg, model, 4, use_layers=True) >= 3
+
+
+def test_batched_8b_shapes_small():
+    # sigmoid-group routing with the Zipf selection bias, K = 8
+    cfg = configs.STACK8.with_(L=3, E=32, B=16, head_owner_first=0, head_owner_last=1,
+                               prerouted=(1, 2))
+    model = inputs.make_model(cfg, seed=7)
+    assert _run_stack(cfg, model, 4) >= 2
+
+
+def test_batched_35b_shapes_small_zipf():
+    # softmax-topK with the Zipf logit bias: a few experts take most tokens
+    cfg = configs.HOST35.with_(L=3, E=64, B=37, head_owner_first=0, head_owner_last=1,
+                               prerouted=(1, 2), pool_frac=None)
+    model = inputs.make_model(cfg, seed=9)
+    assert _run_stack(cfg, model, 3) >= 2
+
+
+def test_batched_8b_full_shapes_64_sequences_teacher_forced():
+    cfg = configs.STACK8.with_(L=3, head_owner_first=0, head_owner_last=1, prerouted=(1, 2))
+    model = inputs.make_model(cfg, seed=0, device=DEV)
+    calls, _ = _teacher_forced(cfg, model, steps=2)
+    assert calls >= 4
+
+
+def test_batched_35b_full_shapes_256_sequences_teacher_forced():
+    cfg = configs.HOST35.with_(L=2, head_owner_first=0, head_owner_last=0, prerouted=(1,),
+                               pool_frac=None)
+    model = inputs.make_model(cfg, seed=0, device=DEV)
+    calls, _ = _teacher_forced(cfg, model, steps=2)
+    assert calls >= 3
+
+
 # ------------------------------------------------- teacher-forced layers ----
 def _teacher_forced(cfg, model, steps, layers=None, verbose=True):
     """Every layer call on the GPU gets the oracle's h and routing state as input

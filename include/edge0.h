@@ -99,7 +99,13 @@ typedef struct {
     const void* sh_down;
     const int32_t* slot_table; /* [E] expert id -> slot in the stacks above, or NULL   */
     int n_slots;               /* slots in the stacks when slot_table != NULL (a slot
-                                  outside [0, n_slots) makes the kernel record EDGE0_EINVAL) */
+                                  outside [0, n_slots) makes the kernel record EDGE0_EINVAL,
+                                  except -1 with a host tier below)                    */
+    const void* host_gate_up;  /* host tier (batched decode path only): all E experts'
+                                  packed gate/up and down stacks in pinned host memory the
+                                  device can read; an expert whose slot_table entry is -1
+                                  is read from here.  NULL: no host tier.              */
+    const void* host_down;
 } edge0_moe_desc;
 
 /* ---- one unmerged LoRA projection [S3.3]: y += (alpha/r) B (A v) ---- */
@@ -137,6 +143,8 @@ typedef struct {
     edge0_head_desc head;
     int head_target;           /* state row the head's prediction is written to        */
     int index;                 /* this layer's row in the route state                  */
+    cudaEvent_t ready;         /* batched path: the layer's kernels wait for this event
+                                  (e.g. its expert-pool prefetch) when not NULL        */
 } edge0_layer_desc;
 
 /* ---- routing state carried across steps and the kernels' scratch ----
@@ -239,6 +247,39 @@ int edge0_decode_layer(const edge0_layer_desc* layer, uint16_t* h_inout, edge0_r
  * workspace of edge0_decode_workspace_bytes. */
 int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
                       edge0_route_state* st, int B, int step, cudaStream_t stream);
+
+/* ---- expert pool with a host tier [S3.1 "SSD Streaming Expert Layers", S3.2
+ * "Motivation", S5.3]: n_slots device slots per layer in front of every
+ * expert's packed weights in pinned host memory.  The device slot table
+ * (edge0_moe_desc.slot_table, [E] int32) maps an expert to its slot or -1 (read
+ * from the host tier).  Host-side object; not thread-safe.
+ *   edge0_pool_create      L layers of E experts; one expert's packed gate/up and
+ *                          down take gu_bytes and dn_bytes.
+ *   edge0_pool_set_layer   the layer's host stacks [E][..] (pinned), its device
+ *                          slot stacks [n_slots][..] and its device slot table.
+ *   edge0_pool_plan        marks ids[0..n) (duplicates allowed) as requested and
+ *                          assigns each requested expert that is not resident a
+ *                          slot: a free one, else the least recently requested
+ *                          slot whose expert is not requested now; experts left
+ *                          without a slot stay in the host tier.  Returns the
+ *                          copies to make (expert, slot) without making them.
+ *   edge0_pool_prefetch    plan + one cudaMemcpyAsync per copied matrix on
+ *                          `stream`, then the slot table; *copied = experts
+ *                          copied.  Kernels that read the layer must not run
+ *                          between this call and the completion of its copies:
+ *                          record an event on `stream` after it and pass it as
+ *                          the layer's `ready` event.
+ *   edge0_pool_stats       requested experts found resident / copied, so far. */
+typedef struct edge0_pool edge0_pool;
+int edge0_pool_create(int L, int E, int n_slots, size_t gu_bytes, size_t dn_bytes, edge0_pool** out);
+int edge0_pool_set_layer(edge0_pool* pool, int l, const void* host_gu, const void* host_dn, void* dev_gu,
+                         void* dev_dn, int32_t* dev_slot_table);
+int edge0_pool_plan(edge0_pool* pool, int l, const int32_t* ids, int n, int32_t* out_expert,
+                    int32_t* out_slot, int* n_copy);
+int edge0_pool_prefetch(edge0_pool* pool, int l, const int32_t* ids, int n, cudaStream_t stream,
+                        int* copied);
+int edge0_pool_stats(const edge0_pool* pool, long long* hits, long long* copies);
+void edge0_pool_destroy(edge0_pool* pool);
 
 /* ---- allocation-free variant (the paper has no counterpart to this call) ----
  * edge0_moe_int4_forward for callers that cannot allocate memory: code running

@@ -47,7 +47,7 @@ class Route(C.Structure):
 class MoeDesc(C.Structure):
     _fields_ = [("d", C.c_int), ("E", C.c_int), ("K", C.c_int), ("I", C.c_int), ("Is", C.c_int),
                 ("gate_up", P), ("down", P), ("sh_gate_up", P), ("sh_down", P),
-                ("slot_table", P), ("n_slots", C.c_int)]
+                ("slot_table", P), ("n_slots", C.c_int), ("host_gate_up", P), ("host_down", P)]
 
 
 class LoraDesc(C.Structure):
@@ -65,7 +65,7 @@ class LayerDesc(C.Structure):
     _fields_ = [("moe", MoeDesc), ("lora_gate", LoraDesc), ("lora_up", LoraDesc),
                 ("lora_down", LoraDesc), ("router", P), ("route", Route), ("gamma", P),
                 ("eps", C.c_float), ("prerouted", C.c_int), ("has_head", C.c_int),
-                ("head", HeadDesc), ("head_target", C.c_int), ("index", C.c_int)]
+                ("head", HeadDesc), ("head_target", C.c_int), ("index", C.c_int), ("ready", P)]
 
 
 class RouteState(C.Structure):
@@ -92,6 +92,13 @@ def _declare(L):
     L.edge0_workspace_bytes.restype = C.c_size_t
     L.edge0_decode_workspace_bytes.argtypes = [C.c_int] * 8
     L.edge0_decode_workspace_bytes.restype = C.c_size_t
+    L.edge0_pool_create.argtypes = [C.c_int, C.c_int, C.c_int, C.c_size_t, C.c_size_t, C.POINTER(P)]
+    L.edge0_pool_set_layer.argtypes = [P, C.c_int, P, P, P, P, P]
+    L.edge0_pool_plan.argtypes = [P, C.c_int, P, C.c_int, P, P, C.POINTER(C.c_int)]
+    L.edge0_pool_prefetch.argtypes = [P, C.c_int, P, C.c_int, P, C.POINTER(C.c_int)]
+    L.edge0_pool_stats.argtypes = [P, C.POINTER(C.c_longlong), C.POINTER(C.c_longlong)]
+    L.edge0_pool_destroy.argtypes = [P]
+    L.edge0_pool_destroy.restype = None
     L.edge0_state_init.argtypes = [C.POINTER(RouteState), P]
     L.edge0_state_error.argtypes = [C.POINTER(RouteState), P, C.POINTER(C.c_int)]
     L.edge0_prerouter_topk.argtypes = [C.POINTER(HeadDesc), P, P, P, C.c_int, P, P, P, P,
@@ -117,7 +124,8 @@ EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_
             "edge0_workspace_bytes", "edge0_decode_workspace_bytes", "edge0_state_init",
             "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
-            "edge0_moe_int4_forward_noalloc"]
+            "edge0_moe_int4_forward_noalloc", "edge0_pool_create", "edge0_pool_set_layer",
+            "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_destroy"]
 
 
 def status_string(code: int) -> str:
@@ -212,6 +220,7 @@ class DeviceModel:
         self.keep = []
         dev = self.device
         self.layers = (LayerDesc * cfg.L)()
+        self.stacks = [None] * cfg.L   # packed routed (gate/up, down) stacks per layer
         self.biases = []
         for l, lw in enumerate(model.layers):
             self.biases.append(None if lw.bias is None else lw.bias.to(dev, torch.float32).contiguous())
@@ -229,9 +238,10 @@ class DeviceModel:
         g = lambda t: t.to(dev)
         L = LayerDesc()
         gt = lambda trip: tuple(g(t) for t in trip)
+        self.stacks[l] = (pack_q4_gate_up(gt(lw.gate), gt(lw.up), stream), pack_q4_down(gt(lw.down), stream))
         L.moe = MoeDesc(d, E, K, I, Is,
-                        self._k(pack_q4_gate_up(gt(lw.gate), gt(lw.up), stream)),
-                        self._k(pack_q4_down(gt(lw.down), stream)),
+                        _ptr(self.stacks[l][0]),
+                        _ptr(self.stacks[l][1]),
                         self._k(pack_q4_gate_up(gt(lw.sh_gate), gt(lw.sh_up), stream)),
                         self._k(pack_q4_down(gt(lw.sh_down), stream)),
                         None, 0)
@@ -311,6 +321,73 @@ class DecodeState:
         _check(lib().edge0_state_error(C.byref(self.st), _stream(stream), C.byref(code)),
                "edge0_state_error")
         return code.value
+
+
+class ExpertPool:
+    """Host tier for a DeviceModel's routed experts (edge0_pool_*): every layer's
+    packed experts move to pinned host memory the device can read, and the layer
+    keeps `n_slots` device slots, filled by copy-engine prefetch from the
+    prerouter's prediction one token ahead.  The model's descriptors are pointed
+    at the slots, the slot table and the host stacks; the full device stacks are
+    released."""
+
+    def __init__(self, dm: "DeviceModel", n_slots: int, copy_stream=None):
+        cfg = dm.cfg
+        self.dm, self.n_slots = dm, n_slots
+        dev = dm.device
+        self.gu_bytes = int(lib().edge0_q4_gate_up_packed_bytes(1, cfg.I, cfg.d))
+        self.dn_bytes = int(lib().edge0_q4_down_packed_bytes(1, cfg.d, cfg.I))
+        self.pool = C.c_void_p()
+        _check(lib().edge0_pool_create(cfg.L, cfg.E, n_slots, self.gu_bytes, self.dn_bytes,
+                                       C.byref(self.pool)), "edge0_pool_create")
+        self.copy_stream = copy_stream or torch.cuda.Stream(dev)
+        self.events = [torch.cuda.Event() for _ in range(cfg.L)]
+        self.keep = []
+        for l in range(cfg.L):
+            gu, dn = dm.stacks[l]
+            hg = torch.empty(gu.numel(), dtype=torch.uint8, pin_memory=True)
+            hd = torch.empty(dn.numel(), dtype=torch.uint8, pin_memory=True)
+            hg.copy_(gu)
+            hd.copy_(dn)
+            sg = torch.empty(n_slots * self.gu_bytes, dtype=torch.uint8, device=dev)
+            sd = torch.empty(n_slots * self.dn_bytes, dtype=torch.uint8, device=dev)
+            tb = torch.full((cfg.E,), -1, dtype=torch.int32, device=dev)
+            _check(lib().edge0_pool_set_layer(self.pool, l, _ptr(hg), _ptr(hd), _ptr(sg), _ptr(sd), _ptr(tb)),
+                   "edge0_pool_set_layer")
+            m = dm.layers[l].moe
+            m.gate_up, m.down, m.slot_table, m.n_slots = _ptr(sg), _ptr(sd), _ptr(tb), n_slots
+            m.host_gate_up, m.host_down = _ptr(hg), _ptr(hd)
+            self.keep += [hg, hd, sg, sd, tb]
+            dm.stacks[l] = None
+        torch.cuda.synchronize(dev)
+
+    def prefetch(self, st: "DecodeState", t: int, layers):
+        """After step t has completed: make resident, per layer in `layers`, the
+        experts its prediction for step t + 1 names (union over the batch), on the
+        copy stream; the layer's next decode waits for its copies.  Returns the
+        number of experts copied."""
+        pred = st.pred_ids[t & 1].cpu()
+        total = 0
+        for l in layers:
+            ids = torch.unique(pred[l]).to(torch.int32).contiguous()
+            n = C.c_int(0)
+            _check(lib().edge0_pool_prefetch(self.pool, l, C.c_void_p(ids.data_ptr()), ids.numel(),
+                                             C.c_void_p(self.copy_stream.cuda_stream), C.byref(n)),
+                   "edge0_pool_prefetch")
+            self.events[l].record(self.copy_stream)
+            self.dm.layers[l].ready = C.c_void_p(self.events[l].cuda_event)
+            total += n.value
+        return total
+
+    def stats(self):
+        hits, copies = C.c_longlong(0), C.c_longlong(0)
+        _check(lib().edge0_pool_stats(self.pool, C.byref(hits), C.byref(copies)), "edge0_pool_stats")
+        return hits.value, copies.value
+
+    def __del__(self):
+        if getattr(self, "pool", None):
+            lib().edge0_pool_destroy(self.pool)
+            self.pool = None
 
 
 # ---------------------------------------------------------- operations ----

@@ -54,6 +54,11 @@ int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P)
     P.down = (const char*)m.down;
     P.slot_table = m.slot_table;
     P.n_slots = m.slot_table ? m.n_slots : m.E;
+    if ((m.host_gate_up != nullptr) != (m.host_down != nullptr)) return EDGE0_EINVAL;
+    if (m.host_gate_up && (!m.slot_table || !al16(m.host_gate_up) || !al16(m.host_down))) return EDGE0_EINVAL;
+    P.gu_host = (const char*)m.host_gate_up;
+    P.down_host = (const char*)m.host_down;
+    P.ready = (void*)Ld.ready;
     P.router = (const char*)Ld.router;
     P.gamma = (const __half*)Ld.gamma;
     if (Ld.gamma && ((uintptr_t)Ld.gamma & 7)) return EDGE0_EINVAL;

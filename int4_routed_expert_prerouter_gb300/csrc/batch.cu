@@ -293,12 +293,17 @@ __device__ __forceinline__ bool slot_of(int j, const Disp* D, const LayerP& Ly, 
     if (j < nact) {
         const int e = D->sexp[j];
         const int sl = Ly.slot_table ? Ly.slot_table[e] : e;
-        if (sl < 0 || sl >= Ly.n_slots) {
+        if (sl == -1 && Ly.gu_host) {
+            // host tier: the expert's weights are read from pinned host memory
+            s.gu = Ly.gu_host + (long long)e * q4_bytes(2 * I, d);
+            s.dn = Ly.down_host + (long long)e * q4_bytes(d, I);
+        } else if (sl < 0 || sl >= Ly.n_slots) {
             if (threadIdx.x == 0) record_error(hdr, EDGE0_EINVAL);
             return false;
+        } else {
+            s.gu = Ly.gu + (long long)sl * q4_bytes(2 * I, d);
+            s.dn = Ly.down + (long long)sl * q4_bytes(d, I);
         }
-        s.gu = Ly.gu + (long long)sl * q4_bytes(2 * I, d);
-        s.dn = Ly.down + (long long)sl * q4_bytes(d, I);
         s.I = I;
         s.m = D->scnt[j];
         s.pos0 = D->soff[j];
@@ -602,6 +607,7 @@ int batch_decode(const Prog& p, cudaStream_t st) {
         const LayerP& Ly = p.layers[l];
         const long long srow = (long long)Ly.sidx * B * K;
         __half* x = xs + (long long)Ly.sidx * B * d;
+        if (Ly.ready && cudaStreamWaitEvent(st, (cudaEvent_t)Ly.ready, 0) != cudaSuccess) return EDGE0_ECUDA;
         k_norm<<<B, 256, 0, st>>>(p.h_io, y, l > 0, Ly.gamma, Ly.eps, d, x, xsum, 1);
         if (!ok()) return EDGE0_ECUDA;
         int32_t* exec = p.exec_ids + (long long)par * p.Ls * B * K + srow;

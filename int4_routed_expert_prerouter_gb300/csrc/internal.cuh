@@ -50,6 +50,9 @@ struct LayerP {
     const char* sh_down;
     const int* slot_table;   // expert id -> slot of the stacks (or null: slot = id)
     int n_slots;
+    const char* gu_host;     // host tier: all experts (slot -1), batched path only
+    const char* down_host;
+    void* ready;             // host: event the batched path waits for before the layer
     const char* router;      // packed fp16 [E x d]
     const char* lora_Ag;     // packed fp16 [r x d] (one row tile)
     const char* lora_Au;

@@ -260,11 +260,17 @@ def test_lora_delta(cfg):
 
 
 # ------------------------------------------------------------ decode ----
-def _run_stack(cfg, model, steps, use_layers=False, check_every_layer_state=True):
+def _run_stack(cfg, model, steps, use_layers=False, check_every_layer_state=True, pool_slots=None,
+               on_pool=None):
     """Decode `steps` steps on GPU and in the oracle; returns the number of steps
-    compared before an allowed near-tie made the two paths diverge."""
+    compared before an allowed near-tie made the two paths diverge.  pool_slots:
+    run the routed experts from a host tier with that many device slots per
+    layer, prefetched after each step from the predictions (on_pool(pool) at the
+    end)."""
     dm = binding.DeviceModel(model, DEV)
     st = binding.DecodeState(cfg, device=DEV)
+    pool = binding.ExpertPool(dm, pool_slots) if pool_slots else None
+    prerouted = [l for l in range(cfg.L) if model.layers[l].prerouted]
     ref = oracle.Stack(_cpu_model(model) if model.layers[0].gate[0].is_cuda else model)
     recs = []
     for t in range(steps):
@@ -277,6 +283,8 @@ def _run_stack(cfg, model, steps, use_layers=False, check_every_layer_state=True
             binding.decode_step(dm, st, h, t)
         torch.cuda.synchronize()
         assert st.error() == 0
+        if pool is not None:
+            pool.prefetch(st, t, prerouted)
         h_ref = h0.clone()
         rec = ref.step(h_ref, t)
         recs.append(rec)
@@ -324,9 +332,11 @@ def _run_stack(cfg, model, steps, use_layers=False, check_every_layer_state=True
                 break
         print(f"step {t}: h rel err {h_err:.2e}{' (near-tie divergence)' if tie else ''}")
         if tie:
-            return t
+            break
         assert_close(h.cpu(), h_ref, f"h after step {t}")
-    return steps
+    if on_pool is not None:
+        on_pool(pool)
+    return t if tie else steps
 
 
 def test_decode_toy_stack_8_steps():
@@ -436,6 +446,20 @@ def test_batched_35b_shapes_small_zipf():
                                prerouted=(1, 2), pool_frac=None)
     model = inputs.make_model(cfg, seed=9)
     assert _run_stack(cfg, model, 3) >= 2
+
+
+def test_host_tier_batched_decode_matches_oracle():
+    # 16 device slots for 64 experts: predicted experts are copied in ahead of
+    # their layer, the rest (and own-routed layers) are read from host memory
+    cfg = configs.HOST35.with_(L=3, E=64, B=24, head_owner_first=0, head_owner_last=1,
+                               prerouted=(1, 2), pool_frac=0.25)
+    model = inputs.make_model(cfg, seed=11)
+    seen = {}
+    n = _run_stack(cfg, model, 4, pool_slots=16, on_pool=lambda p: seen.update(stats=p.stats()))
+    assert n >= 2
+    hits, copies = seen["stats"]
+    print(f"pool: {hits} hits, {copies} experts copied")
+    assert copies > 0 and hits > 0
 
 
 def test_batched_8b_full_shapes_64_sequences_teacher_forced():

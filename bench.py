@@ -152,7 +152,7 @@ def run_gpu(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    cfg = CFG
+    cfg = configs.CONFIGS[args.config]
     if args.layers or args.experts:
         # reduced case for profiler captures only (same per-layer shapes)
         L = args.layers or cfg.L
@@ -269,7 +269,7 @@ def run_gpu(args, rank, world):
         "dtype": "int4xf16",
         "data": "synthetic",
         "config": {
-            "workload": (f"{cfg.name}: {cfg.description}" if cfg is CFG else
+            "workload": (f"{cfg.name}: {cfg.description}" if not (args.layers or args.experts) else
                          f"REDUCED profiling case: {cfg.L} layers, {cfg.E} experts, shapes of {CFG.name}"),
             "layers": cfg.L, "d_model": cfg.d, "experts": cfg.E, "top_k": cfg.K,
             "batch": B, "seq_len": 1, "parallelism": f"replicas x{world}",
@@ -290,6 +290,164 @@ def run_gpu(args, rank, world):
     }
     if cpu_model is not None:
         line["cpu_baseline"] = cpu_baseline(cpu_model, args)
+    return line
+
+
+def batched_bytes_per_step(cfg, exec_ids, own_routed):
+    """Algorithmic bytes of one batched decode step: each layer's distinct routed
+    experts once (however many tokens they serve), the shared expert and LoRA
+    factors, every head's dense parts once and its gathered one-hot columns per
+    token, and the router of each layer that routes itself.  exec_ids: [L, B, K]
+    of the step."""
+    expert = configs.expert_bytes(cfg.d, cfg.I)
+    shared = configs.expert_bytes(cfg.d, cfg.Is)
+    lora = (2 * (cfg.r * cfg.d + cfg.Is * cfg.r) + (cfg.r * cfg.Is + cfg.d * cfg.r)) * 2
+    head_dense = (cfg.H * cfg.d + cfg.E * cfg.d + cfg.E * cfg.H) * 2
+    head_cols = 2 * cfg.K * (cfg.H + cfg.E) * 2
+    total = 0
+    for l in range(cfg.L):
+        total += len(np.unique(exec_ids[l])) * expert + shared + lora
+    total += len(cfg.head_owners()) * (head_dense + cfg.B * head_cols) + own_routed * cfg.E * cfg.d * 2
+    return total
+
+
+def run_batched(args, rank, world, cfg):
+    """The batched decode path (cfg.B > 4 sequences): one bench step = one decode
+    step of all sequences; with a host tier (cfg.pool_frac), the experts each
+    prerouted layer's prediction names are prefetched after every step (part of
+    the timed step: it waits for that step's predictions)."""
+    from int4_routed_expert_prerouter_gb300 import binding, inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    model = inputs.make_model(cfg, seed=args.seed, device=dev, small_device=dev)
+    dm = binding.DeviceModel(model, dev)
+    del model
+    torch.cuda.empty_cache()
+    pool = binding.ExpertPool(dm, int(cfg.E * cfg.pool_frac)) if cfg.pool_frac else None
+    torch.cuda.empty_cache()
+    st = binding.DecodeState(cfg, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    B, d = cfg.B, cfg.d
+    prerouted = list(cfg.prerouted)
+    n_in = args.warmup + 3 * args.steps
+    h_all = torch.empty(n_in, B, d, dtype=torch.float16, device=dev)
+    for i in range(n_in):
+        h_all[i].copy_(inputs.hidden(cfg, i, seed=args.seed, device=dev))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    def step(t, prefetch=True):
+        binding.decode_step(dm, st, h_all[t], t)
+        if pool is not None and prefetch:
+            pool.prefetch(st, t, prerouted)
+
+    t = 0
+    for _ in range(args.warmup):
+        step(t)
+        t += 1
+    barrier()
+    err = st.error()
+    assert err == 0, f"kernel error during warm-up: {binding.status_string(err)}"
+
+    def timed(prefetch=True):
+        nonlocal t
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        a.record(stream)
+        for _ in range(args.steps):
+            step(t, prefetch)
+            t += 1
+        b.record(stream)
+        barrier()
+        return a.elapsed_time(b)
+
+    hits0, copies0 = pool.stats() if pool is not None else (0, 0)
+    with ClockSampler(dev.index) as clk:
+        region_ms = timed()
+    err = st.error()
+    assert err == 0, f"kernel error in the timed region: {binding.status_string(err)}"
+    hits1, copies1 = pool.stats() if pool is not None else (0, 0)
+    # bytes from the routing of the last two timed steps
+    ex = st.exec_ids.cpu().numpy()
+    own = cfg.L - len(cfg.prerouted)
+    step_bytes = statistics.mean(batched_bytes_per_step(cfg, ex[p], own) for p in (0, 1))
+    off_ms = timed(prefetch=False) if pool is not None else None
+
+    # end to end: pinned host input -> device, decode step, device -> host, every step
+    h_host = torch.empty(args.steps, B, d, dtype=torch.float16).pin_memory()
+    for i in range(args.steps):
+        h_host[i].copy_(inputs.hidden(cfg, t + i, seed=args.seed))
+    h = torch.empty(B, d, dtype=torch.float16, device=dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    a.record(stream)
+    for i in range(args.steps):
+        h.copy_(h_host[i], non_blocking=True)
+        binding.decode_step(dm, st, h, t)
+        if pool is not None:
+            pool.prefetch(st, t, prerouted)
+        h_host[i].copy_(h, non_blocking=True)
+        t += 1
+    b.record(stream)
+    barrier()
+    e2e_ms = a.elapsed_time(b)
+    assert st.error() == 0
+
+    local = torch.tensor([region_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
+    region_ms, e2e_ms = local.tolist()
+    if rank != 0:
+        return None
+    tokens = B * args.steps * world
+    value = tokens / (region_ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (region_ms / args.steps / 1e3) / 1e9
+    line = {
+        "metric": f"decode tokens/s (1 GB300, {cfg.name}, {B} sequences) and achieved HBM GB/s vs roofline",
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(region_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4xf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{cfg.name}: {cfg.description}",
+            "layers": cfg.L, "d_model": d, "experts": cfg.E, "top_k": cfg.K, "batch": B, "seq_len": 1,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (%.0f MB of weights read per step > 129 MB)" % (step_bytes / 1e6),
+            "layers_per_s": round(value / B * cfg.L / world, 1),
+        },
+        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": B * d * 2, "d2h_bytes_per_step": B * d * 2},
+        # per layer: norm, dispatch, gate/up, down, LoRA A (2), LoRA down; + router
+        # and top-K on own-routed layers; final residual; per head: fc1, one-hot +
+        # GELU, fc2, linear_init, one-hot, top-K
+        "gpu_launches": args.steps * (7 * cfg.L + 2 * own + 1 + 6 * len(cfg.head_owners())),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "batched decode step (per layer: norm, routing, dispatch, gate/up, down, LoRA; "
+                               "head flush), algorithmic bytes from the step's routing over the step time",
+                     "algorithmic_bytes_per_step": int(step_bytes),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "clocks": clk.summary(),
+    }
+    if pool is not None:
+        req = (hits1 - hits0) + (copies1 - copies0)
+        line["pool"] = {"slots_per_layer": pool.n_slots, "experts": cfg.E,
+                        "prefetch_hit_rate": round((hits1 - hits0) / max(req, 1), 4),
+                        "experts_copied_per_step": round((copies1 - copies0) / args.steps, 2),
+                        "prefetch_off_tokens_per_s": round(tokens / (off_ms / 1e3), 2),
+                        "prefetch_off": "no copies: resident set frozen, misses read from host memory"}
     return line
 
 
@@ -462,6 +620,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", action="store_true", help="print a per-phase split of one step")
     ap.add_argument("--trace-file", default=None, help="with --trace: save the raw per-CTA trace (.npz)")
+    ap.add_argument("--config", default=CFG.name, choices=sorted(configs.CONFIGS),
+                    help="workload; the batched configurations (B > 4) run the batched path")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -477,7 +637,13 @@ def main():
             torch.distributed.init_process_group("nccl")
         import __graft_entry__
         __graft_entry__.build()
-        line = run_gpu(args, rank, world)
+        cfg = configs.CONFIGS[args.config]
+        if cfg.B > 4:
+            if args.steps == 512:
+                args.steps = 16
+            line = run_batched(args, rank, world, cfg)
+        else:
+            line = run_gpu(args, rank, world)
         if world > 1:
             torch.distributed.destroy_process_group()
     if line is not None:

@@ -32,6 +32,8 @@
 namespace edge0 {
 
 // ---------------------------------------------------------------- layout ----
+// work items of the expert kernels in the dispatch record (see Disp)
+constexpr int kDispItems = EDGE0_MAX_BATCHED * EDGE0_MAX_K / 8 + EDGE0_MAX_E + EDGE0_MAX_BATCHED / 8 + 2;
 BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
     BatchWs w;
     auto al = [](long long x) { return (x + 255) / 256 * 256; };
@@ -43,7 +45,7 @@ BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
     w.z = o;     o += al((long long)B * H * 4);
     w.la = o;    o += al((long long)B * 32 * 4);
     w.wsel = o;  o += al((long long)B * K * 4);
-    w.disp = o;  o += al((long long)(4 * (EDGE0_MAX_E + 1) + 1) * 4);
+    w.disp = o;  o += al((long long)(4 * (EDGE0_MAX_E + 1) + 4 + 4 * kDispItems) * 4);
     w.tok = o;   o += al((long long)B * K * 4);
     w.wt = o;    o += al((long long)B * K * 4);
     w.act = o;   o += al((long long)(B * K + B) * I * 4);
@@ -53,11 +55,17 @@ BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
 
 namespace {
 
-struct Disp {   // dispatch of one layer (device)
+// work items of the expert kernels: (slot, first token of a block); at most
+// B K / blk + (active experts) + B / blk + 1 per kernel
+constexpr int kMaxItems = kDispItems;
+
+struct Disp {   // dispatch of one layer (device); fits the workspace's dispatch record
     int nact;
     int sexp[EDGE0_MAX_E + 1];
     int soff[EDGE0_MAX_E + 1];
     int scnt[EDGE0_MAX_E + 1];
+    int n_gu, n_dn;                   // work items of k_gu / k_down
+    int2 it_gu[kMaxItems], it_dn[kMaxItems];
 };
 
 __device__ __forceinline__ void record_error(WsHeader* hdr, int code) {
@@ -123,24 +131,26 @@ __global__ void __launch_bounds__(256) k_norm(__half* h, float* y, int add_y, co
 }
 
 // ------------------------------------------------------------- k_dense ------
-// out[b][o] (=, or += with accumulate) sum_k W[o][k] X[b][k] for rows o < N and
-// tokens b < B.  W packed fp16: kmajor = 0: [half][16-row tile][group of the
-// half][4 steps x 512 B] (2 KB units); kmajor = 1: [16-input step][row tile] x
-// 512 B.  X: fp16 [B][ldx] (xh) or fp32 (xf, entered as hi + lo fp16).  One CTA
-// per (row tile, 32 tokens); its 4 warps split the inputs.
+// out[b][o] += sum_k W[o][k] X[b][k] for rows o < N and tokens b < B (the caller
+// zeroes `out` where it does not accumulate).  W packed fp16: kmajor = 0:
+// [half][16-row tile][group of the half][4 steps x 512 B] (2 KB units);
+// kmajor = 1: [16-input step][row tile] x 512 B.  X: fp16 [B][ldx] (xh) or fp32
+// (xf, entered as hi + lo fp16).  One CTA per (row tile, 32 tokens, 256-input
+// chunk); its 4 warps split the chunk's 16 steps; fp32 reductions into out.
 template <bool F32IN>
 __global__ void __launch_bounds__(128) k_dense(const char* __restrict__ W, int kmajor, int N, int Kin,
                                                const __half* __restrict__ xh, const float* __restrict__ xf,
-                                               int ldx, int B, float* out, int ldo, int accumulate) {
-    const int rt = blockIdx.x, tb = blockIdx.y * 32;
+                                               int ldx, int B, float* out, int ldo) {
+    const int rt = blockIdx.x, tb = blockIdx.y * 32, kc = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
     const int nks = Kin / 16, RT = (N + 15) / 16, hn = Kin / kGroup / 2;
+    const int ks1 = nks < kc * 16 + 16 ? nks : kc * 16 + 16;
     float acc[4][4], accl[4][4];
 #pragma unroll
     for (int n = 0; n < 4; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[n][e] = accl[n][e] = 0.f;
-    for (int ks = wid; ks < nks; ks += 4) {
+    for (int ks = kc * 16 + wid; ks < ks1; ks += 4) {
         const char* ap;
         if (kmajor) {
             ap = W + ((long long)ks * RT + rt) * kF16Step;
@@ -189,11 +199,8 @@ __global__ void __launch_bounds__(128) k_dense(const char* __restrict__ W, int k
     for (int i = tid; i < 16 * 32; i += 128) {
         const int r = i >> 5, c = i & 31;
         const int row = rt * 16 + r, tok = tb + c;
-        if (row < N && tok < B) {
-            const float s = (red[0][r][c] + red[1][r][c]) + (red[2][r][c] + red[3][r][c]);
-            float* o = out + (long long)tok * ldo + row;
-            *o = accumulate ? *o + s : s;
-        }
+        if (row < N && tok < B)
+            red_add_f32(out + (long long)tok * ldo + row, (red[0][r][c] + red[1][r][c]) + (red[2][r][c] + red[3][r][c]));
     }
 }
 
@@ -241,7 +248,8 @@ __global__ void __launch_bounds__(256) k_route(const float* logits, int ldl, int
 // (token, weight) pairs; one CTA.  An id outside [0, E) records EDGE0_EINVAL
 // and counts as expert 0.
 __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const float* w, int B, int K, int E,
-                                                   Disp* D, int* tok, float* wt, WsHeader* hdr) {
+                                                   int shared, int blk_gu, int blk_dn, Disp* D, int* tok, float* wt,
+                                                   WsHeader* hdr) {
     __shared__ int cnt[EDGE0_MAX_E], off[EDGE0_MAX_E], fill[EDGE0_MAX_E];
     const int tid = threadIdx.x, n = B * K;
     for (int e = tid; e < E; e += blockDim.x) cnt[e] = fill[e] = 0;
@@ -265,6 +273,15 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const flo
             run += cnt[e];
         }
         D->nact = a;
+        // one work item per block of tokens of each active expert (and the shared expert)
+        int ng = 0, nd = 0;
+        for (int j = 0; j <= a; ++j) {
+            const int m = j < a ? D->scnt[j] : (shared ? B : 0);
+            for (int tb = 0; tb < m; tb += blk_gu) D->it_gu[ng++] = make_int2(j, tb);
+            for (int tb = 0; tb < m; tb += blk_dn) D->it_dn[nd++] = make_int2(j, tb);
+        }
+        D->n_gu = ng;
+        D->n_dn = nd;
     }
     __syncthreads();
     for (int p = tid; p < n; p += blockDim.x) {
@@ -286,6 +303,7 @@ struct Slot {
     const int* toks;     // token of each position (null: position = token)
     const float* wts;    // weight of each position (null: 1)
     bool shared;
+    bool host;           // weights in the host tier
 };
 __device__ __forceinline__ bool slot_of(int j, const Disp* D, const LayerP& Ly, int B, int K, int d, int I,
                                         int Is, const int* tok, const float* wt, WsHeader* hdr, Slot& s) {
@@ -293,10 +311,12 @@ __device__ __forceinline__ bool slot_of(int j, const Disp* D, const LayerP& Ly, 
     if (j < nact) {
         const int e = D->sexp[j];
         const int sl = Ly.slot_table ? Ly.slot_table[e] : e;
+        s.host = false;
         if (sl == -1 && Ly.gu_host) {
             // host tier: the expert's weights are read from pinned host memory
             s.gu = Ly.gu_host + (long long)e * q4_bytes(2 * I, d);
             s.dn = Ly.down_host + (long long)e * q4_bytes(d, I);
+            s.host = true;
         } else if (sl < 0 || sl >= Ly.n_slots) {
             if (threadIdx.x == 0) record_error(hdr, EDGE0_EINVAL);
             return false;
@@ -321,51 +341,224 @@ __device__ __forceinline__ bool slot_of(int j, const Disp* D, const LayerP& Ly, 
         s.toks = nullptr;
         s.wts = nullptr;
         s.shared = true;
+        s.host = false;
         return true;
     }
     return false;
 }
 
+// Experts run in CTAs of 8 warps, one 16-row tile each, over blocks of tokens
+// of one expert: the block's B operand (x rows, or act fragments as hi + lo
+// fp16) is staged in shared memory once per CTA; each warp streams its tile's
+// 576-byte int4 slices group by group through a 4-stage ring in shared memory
+// (cp.async for device-resident experts, plain loads for host-tier ones), three
+// groups in flight.
+constexpr int kExpWarps = 8;
+constexpr int kGuTok = 8;     // tokens per gate/up block (one mma column tile)
+constexpr int kDnTok = 16;    // tokens per down block (4 tiles of 4 tokens x hi/lo)
+constexpr int kStages = 4;
+constexpr int kSlice = 576;   // one group of one row tile: 512 B of nibbles + 64 B of (s, b)
+
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_2() { asm volatile("cp.async.wait_group 2;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// one 16-byte piece of a slice into the ring: asynchronous from device memory,
+// a plain load + store from the host tier
+__device__ __forceinline__ void piece(void* dst, const char* src, bool host) {
+    if (!host) cp16(dst, src);
+    else *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+}
+
 // --------------------------------------------------------------- k_gu -------
 // gate/up of one expert for all of its tokens: warp w of CTA x takes the
-// interleaved 16-row tile 4 x + w (gate rows 8 x' .. + 7 and the same up rows)
-// over all of d; tokens in blocks of 32 (4 mma column tiles of 8 tokens).
-// act[position][row] = silu(gate) up (the shared expert's gate and up with their
-// LoRA terms (alpha/r) B (A x), A x precomputed in la).
-__global__ void __launch_bounds__(128) k_gu(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
+// interleaved 16-row tile 8 x + w (gate rows of act rows 8 (8 x + w) .. + 7 and
+// the same up rows) over all of d, 8 tokens per block.  act[position][row] =
+// silu(gate) up (the shared expert's gate and up with their LoRA terms
+// (alpha/r) B (A x), A x precomputed in la).
+// Dynamic shared memory: x rows [kGuTok][d + 8] fp16 (padded: conflict-free
+// fragment reads), x group sums [kGuTok][d/64], ring [8 warps][4][576 B].
+__global__ void __launch_bounds__(256) k_gu(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
                                             const __half* __restrict__ x, const float* __restrict__ xsum,
                                             const float* la, int lora, int r, int B, int K, int d, int I, int Is,
                                             int Imax, float* act, WsHeader* hdr) {
+    extern __shared__ __align__(16) char gsm[];
+    if ((int)blockIdx.y >= D->n_gu) return;   // CTA-uniform
+    const int2 item = D->it_gu[blockIdx.y];
     Slot S;
-    if (!slot_of(blockIdx.y, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const int rt = blockIdx.x * 4 + wid;
-    if (rt * kHalfRow >= S.I) return;
-    const int n_gd = d / kGroup, hn = n_gd / 2, RTI = S.I / kHalfRow;
-    for (int tb = 0; tb < S.m; tb += 32) {
-        int tk[4];   // token of the lane's B column in each column tile
-        int tc[4][2];   // tokens of the lane's C columns 2t, 2t + 1
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-            const int p = tb + n * 8 + g;
-            tk[n] = p < S.m ? (S.toks ? S.toks[p] : p) : -1;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int q = tb + n * 8 + 2 * t + c;
-                tc[n][c] = q < S.m ? (S.toks ? S.toks[q] : q) : -1;
-            }
+    if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
+    const int n_gd = d / kGroup, hn = n_gd / 2, RTI = S.I / kHalfRow, ld = d + 8;
+    __half* xrow = reinterpret_cast<__half*>(gsm);
+    float* xss = reinterpret_cast<float*>(gsm + kGuTok * ld * 2);
+    char* ring = gsm + kGuTok * ld * 2 + kGuTok * n_gd * 4 + wid * kStages * kSlice;
+    const int rt = blockIdx.x * kExpWarps + wid;
+    const bool live = rt < RTI;
+    auto unit_of = [&](int gg) {
+        const int h = gg / hn, gl = gg - h * hn;
+        return S.gu + ((long long)(h * RTI + rt) * hn + gl) * kQ4Unit;
+    };
+    auto fill = [&](int gg) {
+        if (gg < n_gd) {
+            char* dst = ring + (gg & (kStages - 1)) * kSlice;
+            const char* src = unit_of(gg);
+            piece(dst + 16 * lane, src + 16 * lane, S.host);
+            if (lane < 4) piece(dst + 512 + 16 * lane, src + 512 + 16 * lane, S.host);
         }
-        float racc[4][4];
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) racc[n][e] = 0.f;
+        cp_commit();
+    };
+    {
+        const int tb = item.y;
+        for (int e = tid; e < kGuTok * (d / 8); e += 256) {
+            const int q = e / (d / 8), c = e - q * (d / 8), p = tb + q;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (p < S.m) v = __ldg(reinterpret_cast<const uint4*>(x + (long long)(S.toks ? S.toks[p] : p) * d) + c);
+            *reinterpret_cast<uint4*>(xrow + q * ld + c * 8) = v;
+        }
+        for (int e = tid; e < kGuTok * n_gd; e += 256) {
+            const int q = e / n_gd, gg = e - q * n_gd, p = tb + q;
+            xss[e] = p < S.m ? __ldg(xsum + (long long)(S.toks ? S.toks[p] : p) * n_gd + gg) : 0.f;
+        }
+        __syncthreads();
+        if (!live) return;
+        float racc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < kStages - 1; ++j) fill(j);
+        const __half* xg = xrow + g * ld + 2 * t;
         for (int gg = 0; gg < n_gd; ++gg) {
-            const int h = gg / hn, gl = gg - h * hn;
-            const char* unit = S.gu + ((long long)(h * RTI + rt) * hn + gl) * kQ4Unit;
-            const uint4 wv = __ldg(reinterpret_cast<const uint4*>(unit + 16 * lane));
-            const uint2 sc = __ldg(reinterpret_cast<const uint2*>(unit + 512 + 8 * g));
+            cp_wait_2();
+            __syncwarp();
+            const char* u = ring + (gg & (kStages - 1)) * kSlice;
+            const uint4 wv = *reinterpret_cast<const uint4*>(u + 16 * lane);
+            const uint2 sc = *reinterpret_cast<const uint2*>(u + 512 + 8 * g);
+            __syncwarp();
+            fill(gg + kStages - 1);
             const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                uint32_t A[4];
+                q4_masks(wq[s], A);
+                const __half* xp = xg + gg * kGroup + s * 16;
+                mma_16816(acc, A, *reinterpret_cast<const uint32_t*>(xp), *reinterpret_cast<const uint32_t*>(xp + 8));
+            }
+            const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) of row g
+            const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) of row g + 8
+            const float xs0 = xss[(2 * t) * n_gd + gg], xs1 = xss[(2 * t + 1) * n_gd + gg];
+            racc[0] += __low2float(s0) * kTwo24 * acc[0] + __high2float(s0) * xs0;
+            racc[1] += __low2float(s0) * kTwo24 * acc[1] + __high2float(s0) * xs1;
+            racc[2] += __low2float(s1) * (kTwo24 / 16.0f) * acc[2] + __high2float(s1) * xs0;
+            racc[3] += __low2float(s1) * (kTwo24 / 16.0f) * acc[3] + __high2float(s1) * xs1;
+        }
+        cp_wait_0();
+        const int arow = rt * kHalfRow + g;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int q = tb + 2 * t + c;
+            if (q >= S.m) continue;
+            float gate = racc[c], up = racc[2 + c];
+            if (S.shared && lora) {
+                const int b = S.toks ? S.toks[q] : q;
+                const __half* bg = Ly.lora_Bg + (long long)arow * r;
+                const __half* bu = Ly.lora_Bu + (long long)arow * r;
+                float dg = 0.f, du = 0.f;
+                for (int qq = 0; qq < r; ++qq) {
+                    dg += __half2float(bg[qq]) * la[b * 32 + qq];
+                    du += __half2float(bu[qq]) * la[b * 32 + 16 + qq];
+                }
+                gate += Ly.lora_scale * dg;
+                up += Ly.lora_scale * du;
+            }
+            act[(long long)(S.pos0 + q) * Imax + arow] = silu_f(gate) * up;
+        }
+    }
+}
+
+// ------------------------------------------------------------- k_down -------
+// down of one expert for all of its tokens: warp w of CTA x takes the 16 output
+// rows of row tile 8 x + w over all of the expert's act rows, 16 tokens per
+// block (4 mma column tiles of 4 tokens x hi/lo); y[token] += w act_out (fp32
+// reductions).  A warp's slice of group gg (its 4 step blocks of 128 B and its
+// 64 B of scales) is gathered into the ring in the unit layout of gate/up.
+// Dynamic shared memory: act fragments [I/64][4 steps][4 tiles][32 lanes] uint2,
+// act group sums [kDnTok][I/64], ring [8 warps][4][576 B].
+__global__ void __launch_bounds__(256) k_down(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
+                                              const float* __restrict__ act, int B, int K, int d, int I, int Is,
+                                              int Imax, float* y, WsHeader* hdr) {
+    extern __shared__ __align__(16) char dsm[];
+    if ((int)blockIdx.y >= D->n_dn) return;   // CTA-uniform
+    const int2 item = D->it_dn[blockIdx.y];
+    Slot S;
+    if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
+    const int n_rtd = d / kRowTile, nh = n_rtd / 2, ngi = S.I / kGroup, ngmax = Imax / kGroup;
+    uint2* afr = reinterpret_cast<uint2*>(dsm);
+    float* qsm = reinterpret_cast<float*>(dsm + ngmax * 512 * 8);
+    char* ring = dsm + ngmax * 512 * 8 + kDnTok * ngmax * 4 + wid * kStages * kSlice;
+    const int rt = blockIdx.x * kExpWarps + wid;
+    const bool live = rt < n_rtd;
+    const int h = rt >= nh ? 1 : 0, i = rt - h * nh;
+    auto fill = [&](int gg) {
+        if (gg < ngi) {
+            char* dst = ring + (gg & (kStages - 1)) * kSlice;
+            const char* grp = S.dn + (long long)gg * n_rtd * kQ4Unit + (long long)h * nh * kQ4Unit;
+            piece(dst + 16 * lane, grp + ((lane >> 3) * nh + i) * kQ4Quarter + 16 * (lane & 7), S.host);
+            if (lane < 4) piece(dst + 512 + 16 * lane, grp + 4 * nh * kQ4Quarter + i * kQ4Scales + 16 * lane, S.host);
+        }
+        cp_commit();
+    };
+    {
+        const int tb = item.y;
+        for (int e = tid; e < ngi * 512; e += 256) {
+            const int ln = e & 31, n = (e >> 5) & 3, s = (e >> 7) & 3, gg = e >> 9;
+            const int p = tb + n * 4 + (ln >> 3), part = (ln >> 2) & 1;
+            uint2 v = make_uint2(0u, 0u);
+            if (p < S.m) {
+                const float* ar = act + (long long)(S.pos0 + p) * Imax + gg * kGroup + s * 16 + 2 * (ln & 3);
+                const float2 a0 = *reinterpret_cast<const float2*>(ar);
+                const float2 a1 = *reinterpret_cast<const float2*>(ar + 8);
+                const __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a1.x, a1.y);
+                if (!part) {
+                    v.x = *reinterpret_cast<const uint32_t*>(&h0);
+                    v.y = *reinterpret_cast<const uint32_t*>(&h1);
+                } else {
+                    const float2 r0 = __half22float2(h0), r1 = __half22float2(h1);
+                    v.x = pack_h2((a0.x - r0.x) * kLoScale, (a0.y - r0.y) * kLoScale);
+                    v.y = pack_h2((a1.x - r1.x) * kLoScale, (a1.y - r1.y) * kLoScale);
+                }
+            }
+            afr[e] = v;
+        }
+        for (int e = tid; e < kDnTok * ngi; e += 256) {
+            const int q = e / ngi, gg = e - q * ngi, p = tb + q;
+            float sum = 0.f;
+            if (p < S.m) {
+                const float4* ar = reinterpret_cast<const float4*>(act + (long long)(S.pos0 + p) * Imax + gg * kGroup);
+                for (int k = 0; k < kGroup / 4; ++k) {
+                    const float4 a = ar[k];
+                    sum += (a.x + a.y) + (a.z + a.w);
+                }
+            }
+            qsm[e] = sum;
+        }
+        __syncthreads();
+        if (!live) return;
+        float o[4][2];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) o[n][0] = o[n][1] = 0.f;
+        for (int j = 0; j < kStages - 1; ++j) fill(j);
+        for (int gg = 0; gg < ngi; ++gg) {
+            cp_wait_2();
+            __syncwarp();
+            const char* u = ring + (gg & (kStages - 1)) * kSlice;
+            uint32_t wq[4];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) wq[s] = *reinterpret_cast<const uint32_t*>(u + s * kQ4Quarter + 4 * lane);
+            const uint2 sc = *reinterpret_cast<const uint2*>(u + 512 + 8 * g);
+            __syncwarp();
+            fill(gg + kStages - 1);
             float acc[4][4];
 #pragma unroll
             for (int n = 0; n < 4; ++n)
@@ -375,118 +568,10 @@ __global__ void __launch_bounds__(128) k_gu(const LayerP Ly, const Disp* D, cons
             for (int s = 0; s < 4; ++s) {
                 uint32_t A[4];
                 q4_masks(wq[s], A);
-                const int k0 = gg * kGroup + s * 16 + 2 * t;
 #pragma unroll
                 for (int n = 0; n < 4; ++n) {
-                    uint32_t b0 = 0u, b1 = 0u;
-                    if (tk[n] >= 0) {
-                        const __half* xr = x + (long long)tk[n] * d + k0;
-                        b0 = __ldg(reinterpret_cast<const uint32_t*>(xr));
-                        b1 = __ldg(reinterpret_cast<const uint32_t*>(xr + 8));
-                    }
-                    mma_16816(acc[n], A, b0, b1);
-                }
-            }
-            const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) of row g
-            const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) of row g + 8
-            const float sg0 = __low2float(s0) * kTwo24, bg0 = __high2float(s0);
-            const float sg1 = __low2float(s1) * (kTwo24 / 16.0f), bg1 = __high2float(s1);
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const float xs0 = tc[n][0] >= 0 ? __ldg(xsum + (long long)tc[n][0] * n_gd + gg) : 0.f;
-                const float xs1 = tc[n][1] >= 0 ? __ldg(xsum + (long long)tc[n][1] * n_gd + gg) : 0.f;
-                racc[n][0] += sg0 * acc[n][0] + bg0 * xs0;
-                racc[n][1] += sg0 * acc[n][1] + bg0 * xs1;
-                racc[n][2] += sg1 * acc[n][2] + bg1 * xs0;
-                racc[n][3] += sg1 * acc[n][3] + bg1 * xs1;
-            }
-        }
-        const int arow = rt * kHalfRow + g;
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int q = tb + n * 8 + 2 * t + c;
-                if (q >= S.m) continue;
-                float gate = racc[n][c], up = racc[n][2 + c];
-                if (S.shared && lora) {
-                    const int b = tc[n][c];
-                    const __half* bg = Ly.lora_Bg + (long long)arow * r;
-                    const __half* bu = Ly.lora_Bu + (long long)arow * r;
-                    float dg = 0.f, du = 0.f;
-                    for (int qq = 0; qq < r; ++qq) {
-                        dg += __half2float(bg[qq]) * la[b * 32 + qq];
-                        du += __half2float(bu[qq]) * la[b * 32 + 16 + qq];
-                    }
-                    gate += Ly.lora_scale * dg;
-                    up += Ly.lora_scale * du;
-                }
-                act[(long long)(S.pos0 + q) * Imax + arow] = silu_f(gate) * up;
-            }
-    }
-}
-
-// ------------------------------------------------------------- k_down -------
-// down of one expert for all of its tokens: warp w of CTA x takes the 16 output
-// rows of row tile 4 x + w over all of the expert's act rows; tokens in blocks of
-// 16 (4 mma column tiles of 4 tokens x hi/lo); y[token] += w act_out (fp32
-// reductions).
-__global__ void __launch_bounds__(128) k_down(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
-                                              const float* __restrict__ act, int B, int K, int d, int I, int Is,
-                                              int Imax, float* y, WsHeader* hdr) {
-    Slot S;
-    if (!slot_of(blockIdx.y, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const int rt = blockIdx.x * 4 + wid, n_rtd = d / kRowTile, nh = n_rtd / 2;
-    if (rt >= n_rtd) return;
-    const int h = rt >= nh ? 1 : 0, i = rt - h * nh;
-    const int ngi = S.I / kGroup;
-    const int tokc = g >> 1, part = g & 1;
-    for (int tb = 0; tb < S.m; tb += 16) {
-        int pb[4];   // position of the lane's B column token in each column tile
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-            const int p = tb + n * 4 + tokc;
-            pb[n] = p < S.m ? S.pos0 + p : -1;
-        }
-        float o[4][2];
-#pragma unroll
-        for (int n = 0; n < 4; ++n) o[n][0] = o[n][1] = 0.f;
-        for (int gg = 0; gg < ngi; ++gg) {
-            const char* grp = S.dn + (long long)gg * n_rtd * kQ4Unit + (long long)h * nh * kQ4Unit;
-            const uint2 sc = __ldg(reinterpret_cast<const uint2*>(grp + 4 * nh * kQ4Quarter + i * kQ4Scales + 8 * g));
-            float acc[4][4], qs[4];
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                qs[n] = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-            }
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t wq = __ldg(reinterpret_cast<const uint32_t*>(grp + (s * nh + i) * kQ4Quarter + 4 * lane));
-                uint32_t A[4];
-                q4_masks(wq, A);
-                const int k0 = gg * kGroup + s * 16 + 2 * t;
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    uint32_t b0 = 0u, b1 = 0u;
-                    if (pb[n] >= 0) {
-                        const float* ar = act + (long long)pb[n] * Imax + k0;
-                        const float2 a0 = *reinterpret_cast<const float2*>(ar);
-                        const float2 a1 = *reinterpret_cast<const float2*>(ar + 8);
-                        qs[n] += (a0.x + a0.y) + (a1.x + a1.y);
-                        const __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a1.x, a1.y);
-                        if (!part) {
-                            b0 = *reinterpret_cast<const uint32_t*>(&h0);
-                            b1 = *reinterpret_cast<const uint32_t*>(&h1);
-                        } else {
-                            const float2 r0 = __half22float2(h0), r1 = __half22float2(h1);
-                            b0 = pack_h2((a0.x - r0.x) * kLoScale, (a0.y - r0.y) * kLoScale);
-                            b1 = pack_h2((a1.x - r1.x) * kLoScale, (a1.y - r1.y) * kLoScale);
-                        }
-                    }
-                    mma_16816(acc[n], A, b0, b1);
+                    const uint2 bb = afr[((gg * 4 + s) * 4 + n) * 32 + lane];
+                    mma_16816(acc[n], A, bb.x, bb.y);
                 }
             }
             const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);
@@ -495,16 +580,12 @@ __global__ void __launch_bounds__(128) k_down(const LayerP Ly, const Disp* D, co
             const float sg1 = __low2float(s1) * (kTwo24 / 16.0f), bg1 = __high2float(s1);
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
-                // group sum of act for the token of column tile n's lane group g:
-                // the 4 lanes of g hold 16 inputs each; lane (2 t) 4 holds token t
-                float q = qs[n];
-                q += __shfl_xor_sync(0xffffffffu, q, 1);
-                q += __shfl_xor_sync(0xffffffffu, q, 2);
-                const float qt = __shfl_sync(0xffffffffu, q, (2 * t) * 4);
+                const float qt = qsm[(n * 4 + t) * ngi + gg];   // group sum of the lane's C-column token
                 o[n][0] += sg0 * (acc[n][0] + acc[n][1] * kLoInv) + bg0 * qt;
                 o[n][1] += sg1 * (acc[n][2] + acc[n][3] * kLoInv) + bg1 * qt;
             }
         }
+        cp_wait_0();
         const int row = rt * kRowTile + g;
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
@@ -555,12 +636,23 @@ __global__ void __launch_bounds__(256) k_lora_vd(const float* act, int Imax, int
 }
 
 // launch helpers
+// out [B][ldo] += W X^T (zero out first unless accumulating into it)
 template <bool F32IN>
 int dense(const char* W, int kmajor, int N, int Kin, const __half* xh, const float* xf, int ldx, int B,
-          float* out, int ldo, int accumulate, cudaStream_t st) {
-    const dim3 grid((N + 15) / 16, (B + 31) / 32);
-    k_dense<F32IN><<<grid, 128, 0, st>>>(W, kmajor, N, Kin, xh, xf, ldx, B, out, ldo, accumulate);
+          float* out, int ldo, bool zero, cudaStream_t st) {
+    if (zero && cudaMemsetAsync(out, 0, (size_t)B * ldo * 4, st) != cudaSuccess) return EDGE0_ECUDA;
+    const dim3 grid((N + 15) / 16, (B + 31) / 32, (Kin / 16 + 15) / 16);
+    k_dense<F32IN><<<grid, 128, 0, st>>>(W, kmajor, N, Kin, xh, xf, ldx, B, out, ldo);
     return cudaGetLastError() == cudaSuccess ? EDGE0_OK : EDGE0_ECUDA;
+}
+
+// opt in to `smem` bytes of dynamic shared memory for `f` (once per size reached)
+template <class F>
+bool smem_opt_in(F f, size_t smem, size_t* done) {
+    if (smem <= 48 * 1024 || smem <= *done) return true;
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
+    *done = smem;
+    return true;
 }
 
 int route(const float* lg, int B, int E, int K, int kind, int ng, int G, float scale, const float* bias,
@@ -601,7 +693,15 @@ int batch_decode(const Prog& p, cudaStream_t st) {
     float* act = reinterpret_cast<float*>(ws + W.act);
     const int step = p.step, par = step & 1;
     const int slots = (B * K < E ? B * K : E) + 1;
+    const int items_gu = (B * K + kGuTok - 1) / kGuTok + slots + (B + kGuTok - 1) / kGuTok;
+    const int items_dn = (B * K + kDnTok - 1) / kDnTok + slots + (B + kDnTok - 1) / kDnTok;
     auto ok = [] { return cudaGetLastError() == cudaSuccess; };
+    // staged B fragments (+ group sums) of one token block
+    const size_t ring = (size_t)kExpWarps * kStages * kSlice;
+    const size_t smem_gu = (size_t)kGuTok * (d + 8) * 2 + (size_t)kGuTok * (d / kGroup) * 4 + ring;
+    const size_t smem_dn = (size_t)(Imax / kGroup) * 512 * 8 + (size_t)kDnTok * (Imax / kGroup) * 4 + ring;
+    static size_t done_gu = 0, done_dn = 0;
+    if (!smem_opt_in(k_gu, smem_gu, &done_gu) || !smem_opt_in(k_down, smem_dn, &done_dn)) return EDGE0_ECUDA;
     int rc = EDGE0_OK;
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
         const LayerP& Ly = p.layers[l];
@@ -618,25 +718,27 @@ int batch_decode(const Prog& p, cudaStream_t st) {
                 return EDGE0_ECUDA;
             w = p.pred_w + o;
         } else {
-            rc = dense<false>(Ly.router, 0, E, d, x, nullptr, d, B, lg, E, 0, st);
+            rc = dense<false>(Ly.router, 0, E, d, x, nullptr, d, B, lg, E, true, st);
             if (rc == EDGE0_OK)
                 rc = route(lg, B, E, K, Ly.route_kind, Ly.n_groups, Ly.topk_groups, Ly.route_scale, Ly.bias, exec,
                            wsel, st);
             w = wsel;
         }
         if (rc) return rc;
-        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, D, tok, wt, hdr);
+        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, kGuTok, kDnTok, D, tok, wt, hdr);
         if (!ok()) return EDGE0_ECUDA;
         const int lora = (Ly.flags & LF_LORA) ? 1 : 0;
         if (lora) {
-            rc = dense<false>(Ly.lora_Ag, 0, r, d, x, nullptr, d, B, la, 32, 0, st);
-            if (rc == EDGE0_OK) rc = dense<false>(Ly.lora_Au, 0, r, d, x, nullptr, d, B, la + 16, 32, 0, st);
+            if (cudaMemsetAsync(la, 0, (size_t)B * 32 * 4, st) != cudaSuccess) return EDGE0_ECUDA;
+            rc = dense<false>(Ly.lora_Ag, 0, r, d, x, nullptr, d, B, la, 32, false, st);
+            if (rc == EDGE0_OK) rc = dense<false>(Ly.lora_Au, 0, r, d, x, nullptr, d, B, la + 16, 32, false, st);
             if (rc) return rc;
         }
-        k_gu<<<dim3((Imax / kHalfRow + 3) / 4, slots), 128, 0, st>>>(Ly, D, tok, wt, x, xsum, la, lora, r, B, K, d,
-                                                                     I, Is, Imax, act, hdr);
+        k_gu<<<dim3((Imax / kHalfRow + kExpWarps - 1) / kExpWarps, items_gu), 256, smem_gu, st>>>(
+            Ly, D, tok, wt, x, xsum, la, lora, r, B, K, d, I, Is, Imax, act, hdr);
         if (!ok()) return EDGE0_ECUDA;
-        k_down<<<dim3(d / kRowTile / 4, slots), 128, 0, st>>>(Ly, D, tok, wt, act, B, K, d, I, Is, Imax, y, hdr);
+        k_down<<<dim3((d / kRowTile + kExpWarps - 1) / kExpWarps, items_dn), 256, smem_dn, st>>>(
+            Ly, D, tok, wt, act, B, K, d, I, Is, Imax, y, hdr);
         if (!ok()) return EDGE0_ECUDA;
         if (lora) {
             k_lora_vd<<<B, 256, 0, st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is, d, Ly.lora_scale, y);
@@ -654,12 +756,12 @@ int batch_decode(const Prog& p, cudaStream_t st) {
         const __half* x = xs + (long long)Ly.sidx * B * d;
         const int32_t* exec = p.exec_ids + (long long)par * p.Ls * B * K + srow;
         const int32_t* prev = step > 0 ? p.exec_ids + (long long)(par ^ 1) * p.Ls * B * K + srow : nullptr;
-        rc = dense<false>(Ly.fc1, 0, H, d, x, nullptr, d, B, z, H, 0, st);
+        rc = dense<false>(Ly.fc1, 0, H, d, x, nullptr, d, B, z, H, true, st);
         if (rc) break;
         k_onehot<<<dim3((H + 127) / 128, B), 128, 0, st>>>(z, H, H, Ly.fc1_oh, exec, prev, K, E, 1);
         if (!ok()) return EDGE0_ECUDA;
-        rc = dense<true>(Ly.fc2, 1, E, H, nullptr, z, H, B, lg, E, 0, st);
-        if (rc == EDGE0_OK) rc = dense<false>(Ly.linit, 0, E, d, x, nullptr, d, B, lg, E, 1, st);
+        rc = dense<true>(Ly.fc2, 1, E, H, nullptr, z, H, B, lg, E, true, st);
+        if (rc == EDGE0_OK) rc = dense<false>(Ly.linit, 0, E, d, x, nullptr, d, B, lg, E, false, st);
         if (rc) break;
         k_onehot<<<dim3((E + 127) / 128, B), 128, 0, st>>>(lg, E, E, Ly.linit_oh, exec, prev, K, E, 0);
         if (!ok()) return EDGE0_ECUDA;

@@ -396,8 +396,9 @@ __host__ __device__ __noinline__ bool build_items(const Shape& Sh, int P, int pa
 }
 
 // Items of one head-flush table (tasks [t0, t1) of head layer hl, over all of
-// d): the fc1 and linear_init units of both halves of d (seg = half), then one
-// fc2 column block over all E rows per fc1 task.  p1 = 0, p2 = first fc2 item.
+// d): the fc1 and linear_init units of both halves of d (seg = half).  The fc2
+// column blocks are small and read directly from global memory (held in the
+// ring they would halve its streaming depth).  p1 = 0, p2 = p3 = n.
 __host__ __device__ __noinline__ bool build_flush_items(const Prog& p, int hl, int t0, int t1, int ring,
                                                         LayerTab* T, int& lin) {
     ItemSink k{T, 0, lin, lin % ring, ring, true};
@@ -417,10 +418,10 @@ __host__ __device__ __noinline__ bool build_flush_items(const Prog& p, int hl, i
             else push_units(k, IT_LINIT, h, t - nH, (t - nH) * hn0, hn0, kF16Unit);
         }
     T->p2 = k.n;
-    for (int t = t0; t < t1 && t < nH; ++t) push_item(k, IT_FC2, 0, nE * kF16Step, t, 0, nE);
     T->p3 = k.n;
     T->n = k.n;
     lin = k.lin;
+    (void)nE;
     return k.ok;
 }
 
@@ -626,6 +627,19 @@ __device__ __forceinline__ void stamp(int tag) {
     const Ctx& c = ctx();
     if (threadIdx.x == 0 && c.ctl->trace) stamp_slow(tag);
 }
+// a value in place of the time (thread 0, when tracing)
+__device__ __noinline__ void stamp_value(int tag, unsigned long long v) {
+    const Ctx& c = ctx();
+    if (threadIdx.x != 0 || !c.ctl->trace) return;
+    const int s = c.ctl->tslot;
+    if (s + 3 > kTraceProducer) return;
+    unsigned long long* a =
+        reinterpret_cast<unsigned long long*>(prg().ws + c.ws.trace) + (long long)c.cta * kTraceSlots;
+    a[s] = (unsigned long long)tag;
+    a[s + 1] = v;
+    a[s + 2] = clock64();
+    c.ctl->tslot = s + 3;
+}
 // the producer's stamps (slots from kTraceProducer on)
 __device__ __noinline__ void stamp_producer(int tag) {
     const Ctx& c = ctx();
@@ -757,33 +771,44 @@ __device__ void producer() {
     int k = 0;        // global index of the next item
     int front = 0;    // oldest item not known to be released (lane 0)
     if (__shfl_sync(0xffffffffu, lane == 0 ? (int)aborted() : 0, 0)) return;
-    // the layers' tables, then this CTA's tables of the head flush
+    // the layers' tables, then this CTA's tables of the head flush.  Lane 0
+    // builds tables in order, one ahead of the table being issued whenever that
+    // table's slot is already free (a build never waits behind the ring).
     const int nl = n_layer_tabs(p);
-    for (int l = 0;; ++l) {
+    int nb = 0, kb = 0;   // lane 0: next table to build, global index of its first item
+    auto build_next = [&](bool wait, int* fail) -> bool {
         int hl = -1, t0 = 0, t1 = 0;
-        if (l >= nl && !flush_table(p, c.nct, c.cta, l - nl, &hl, &t0, &t1)) break;
-        LayerTab* T = tab_of(l);
-        int fail = 0;
+        if (nb >= nl && !flush_table(p, c.nct, c.cta, nb - nl, &hl, &t0, &t1)) return false;
+        // the table slot is free once the consumers finished table nb - kTables
+        if (!wait && *(volatile int*)&ctl->cdone < nb - kTables + 1) return false;
+        if (wait && !wait_flag(&ctl->cdone, nb - kTables + 1)) { *fail = 1; return false; }
+        LayerTab* T = tab_of(nb);
+        stamp_producer((nb << 8) | 0x80);
+        T->k0 = kb;
+        const bool built = nb < nl ? build_items(layer_shape(p, nb, has_router_phase(p, nb, c.step)), c.P,
+                                                 c.pair, c.rank, p.ring_bytes, T, lin)
+                                   : build_flush_items(p, hl, t0, t1, p.ring_bytes, T, lin);
+        if (!built) {
+            raise_error(EDGE0_EUNSUPPORTED);
+            *fail = 1;
+            return false;
+        }
+        __threadfence_block();
+        *(volatile int*)&T->seq = nb + 1;
+        stamp_producer((nb << 8) | 0x81);
+        kb += T->n;
+        ++nb;
+        return true;
+    };
+    for (int l = 0;; ++l) {
+        int fail = 0, have = 1;
         if (lane == 0) {
-            // the table slot is free once the consumers finished table l - kTables
-            if (!wait_flag(&ctl->cdone, l - kTables + 1)) fail = 1;
-            if (!fail) {
-                stamp_producer((l << 8) | 0x80);
-                T->k0 = k;
-                const bool built = l < nl ? build_items(layer_shape(p, l, has_router_phase(p, l, c.step)), c.P,
-                                                        c.pair, c.rank, p.ring_bytes, T, lin)
-                                          : build_flush_items(p, hl, t0, t1, p.ring_bytes, T, lin);
-                if (!built) {
-                    raise_error(EDGE0_EUNSUPPORTED);
-                    fail = 1;
-                } else {
-                    __threadfence_block();
-                    *(volatile int*)&T->seq = l + 1;
-                    stamp_producer((l << 8) | 0x81);
-                }
-            }
+            if (nb <= l && !build_next(true, &fail)) have = 0;   // table l
+            if (have && !fail && nb == l + 1) build_next(false, &fail);
         }
         if (__shfl_sync(0xffffffffu, fail, 0)) return;
+        if (!__shfl_sync(0xffffffffu, have, 0)) break;
+        LayerTab* T = tab_of(l);
         __syncwarp();
         const int n = T->n;
         bool have_routing = false;
@@ -1632,10 +1657,11 @@ __device__ bool run_flush(int tl, const LayerTab* T, int& xl) {
         for (int k = 0; k < 2 * EDGE0_MAX_K; ++k) oh += v[k];
     }
     cbar();
-    // fc1 and linear_init units of both halves of d, dealt to the warps one at a
-    // time in turn (all warps move through the items together, so a table longer
-    // than the ring streams through it).  Addresses come from registers: the
-    // table's constants are loaded once, each item's fields once.
+    // fc1 and linear_init units of both halves of d.  Whole items are dealt to
+    // the warps in turn (item i to warp i mod 16): the warps work on 16
+    // consecutive items at once, so a table longer than the ring streams through
+    // it, and each item's units (one row tile of one task) share one running sum.
+    // The warp that processed an item releases it for all warps.
     bool ok = true;
     {
         const char* ringb = g_smem + c.pl.ring;
@@ -1644,48 +1670,40 @@ __device__ bool run_flush(int tl, const LayerTab* T, int& xl) {
         const uint2* xfb = SM<uint2>(c.pl.xf) + (live ? tok : 0) * 4 + t;
         const int xstride = B * 4;
         const int k0 = T->k0, n_units_items = T->p2;
-        int u = 0;
-        int cur = -1;   // task of the warp's running sum
-        float s0 = 0.f, s2 = 0.f;
-        for (int i = 0; i < n_units_items; ++i) {
+        long long waited = 0, t_begin = clock64();   // trace: warp 0's waits and total
+        for (int i = wid; i < n_units_items && ok; i += kConsumerWarps) {
             const int kind = T->it[i].kind, seg = T->it[i].seg, off = T->it[i].off, ib = T->it[i].b, in = T->it[i].n;
-            int j = ((wid - u) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-            if (j < in && ok) {
-                if (!mbar_wait(full_bar(k0 + i), item_parity(k0 + i))) ok = false;
-                for (; ok && j < in; j += kConsumerWarps) {
-                    const int uu = ib + j, tile = uu / hn0, gl = uu - tile * hn0 + seg * hn0;
-                    const int tk = (kind == IT_FC1 ? tile : tile + nH) - t0;
-                    if (tk != cur) {
-                        if (cur >= 0 && t < B) {
-                            atomicAdd(&zp[(cur * 16 + g) * B + t], s0);
-                            atomicAdd(&zp[(cur * 16 + 8 + g) * B + t], s2);
-                        }
-                        cur = tk;
-                        s0 = s2 = 0.f;
-                    }
-                    const char* unit = ringb + off + j * kF16Unit;
-                    float as[4][4];
+            const long long w0 = clock64();
+            ok = mbar_wait(full_bar(k0 + i), item_parity(k0 + i));
+            waited += clock64() - w0;
+            if (ok) {
+                // an item lies within one row tile of one half of d
+                const int tile = ib / hn0, gl0 = ib - tile * hn0 + seg * hn0;
+                const int tk = (kind == IT_FC1 ? tile : tile + nH) - t0;
+                float as[4][4];
+#pragma unroll
+                for (int s = 0; s < 4; ++s) as[s][0] = as[s][1] = as[s][2] = as[s][3] = 0.f;
+                const char* unit = ringb + off;
+                for (int j = 0; j < in; ++j, unit += kF16Unit) {
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         const uint4 av = *reinterpret_cast<const uint4*>(unit + s * kF16Step + 16 * lane);
                         uint2 bb = make_uint2(0u, 0u);
-                        if (live) bb = xfb[(gl * 4 + s) * xstride];
+                        if (live) bb = xfb[((gl0 + j) * 4 + s) * xstride];
                         const uint32_t A[4] = {av.x, av.y, av.z, av.w};
-                        as[s][0] = as[s][1] = as[s][2] = as[s][3] = 0.f;
                         mma_16816(as[s], A, bb.x, bb.y);
                     }
-                    s0 += (as[0][0] + as[1][0]) + (as[2][0] + as[3][0]);
-                    s2 += (as[0][2] + as[1][2]) + (as[2][2] + as[3][2]);
+                }
+                if (t < B) {
+                    atomicAdd(&zp[(tk * 16 + g) * B + t], (as[0][0] + as[1][0]) + (as[2][0] + as[3][0]));
+                    atomicAdd(&zp[(tk * 16 + 8 + g) * B + t], (as[0][2] + as[1][2]) + (as[2][2] + as[3][2]));
                 }
             }
-            u += in;
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(k0 + i));
+            if (lane == 0) mbar_arrive_n(empty_bar(k0 + i), kConsumerWarps);
         }
-        if (cur >= 0 && t < B) {
-            atomicAdd(&zp[(cur * 16 + g) * B + t], s0);
-            atomicAdd(&zp[(cur * 16 + 8 + g) * B + t], s2);
-        }
+        stamp_value((tl << 8) | 0x3E, (unsigned long long)(clock64() - t_begin));
+        stamp_value((tl << 8) | 0x3F, (unsigned long long)waited);
     }
     ok = !cbar_or(!ok || aborted());
     stamp((tl << 8) | 21);
@@ -1706,28 +1724,28 @@ __device__ bool run_flush(int tl, const LayerTab* T, int& xl) {
         }
     }
     cbar();
-    // fc2: the column block of each fc1 task over all E rows
-    for (int i = T->p2; i < T->n; ++i) {
-        const Item& it2 = T->it[i];
-        if (ok) ok = wait_item(T, i);
-        if (ok) {
-            const uint2* gfr = SM<uint2>(c.pl.gf) + (it2.a - t0) * B * 8;
-            const int tok = g >> 1, prt = g & 1;
-            uint2 bq = make_uint2(0u, 0u);
-            if (tok < B) bq = gfr[(tok * 2 + prt) * 4 + t];
-            for (int e = wid; e < it2.n; e += kConsumerWarps) {
-                const uint4 av = *reinterpret_cast<const uint4*>(ring_at(it2) + e * kF16Step + 16 * lane);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // fc2: the column block of each fc1 task over all E rows, from global memory
+    // (K-major: block `task`, row tile e at (task E/16 + e) 512 B); one (task, row
+    // tile) per warp in turn, the sum over tasks kept per row tile
+    {
+        const int nE = E / kRowTile, nf = (t1 < nH ? t1 : nH) - t0;
+        const int tok = g >> 1, prt = g & 1;
+        for (int e = wid; ok && nf > 0 && e < nE; e += kConsumerWarps) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int f = 0; f < nf; ++f) {
+                const uint4 av = __ldg(reinterpret_cast<const uint4*>(
+                    Ly.fc2 + ((long long)(t0 + f) * nE + e) * kF16Step + 16 * lane));
+                uint2 bq = make_uint2(0u, 0u);
+                if (tok < B) bq = SM<uint2>(c.pl.gf)[(f * B + tok) * 8 + prt * 4 + t];
                 const uint32_t A[4] = {av.x, av.y, av.z, av.w};
                 mma_16816(acc, A, bq.x, bq.y);
-                const int row = (it2.b + e) * kRowTile + g;
-                if (t < B) {
-                    red_add_f32(lg + t * E + row, acc[0] + acc[1] * kLoInv);
-                    red_add_f32(lg + t * E + row + 8, acc[2] + acc[3] * kLoInv);
-                }
+            }
+            const int row = e * kRowTile + g;
+            if (t < B) {
+                red_add_f32(lg + t * E + row, acc[0] + acc[1] * kLoInv);
+                red_add_f32(lg + t * E + row + 8, acc[2] + acc[3] * kLoInv);
             }
         }
-        release_item(T, i);
     }
     ok = !cbar_or(!ok);
     stamp((tl << 8) | 22);

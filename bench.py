@@ -146,6 +146,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
 
 
+# ------------------------------------------------------ multi-replica -----
+def job_times(times_ms, world, device):
+    """Replicas (one process per GPU, no collective on the data path) time
+    their own regions; the job takes as long as the slowest: the max over ranks
+    of each time."""
+    local = torch.tensor(times_ms, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
+    return local.tolist()
+
+
+def job_throughput(tokens_all_ranks, region_ms):
+    """Whole-job throughput: the tokens every rank decoded over the job's time."""
+    return tokens_all_ranks / (region_ms / 1e3)
+
+
 # ------------------------------------------------------------ GPU arm -----
 def run_gpu(args, rank, world):
     from int4_routed_expert_prerouter_gb300 import binding, inputs
@@ -239,15 +255,12 @@ def run_gpu(args, rank, world):
     e2e_ms = e_start.elapsed_time(e_end)
     assert st.error() == 0
 
-    local = torch.tensor([region_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
-    region_ms, e2e_ms = local.tolist()
+    region_ms, e2e_ms = job_times([region_ms, e2e_ms], world, dev)
     if rank != 0:
         return None
 
     tokens = B * args.steps * world
-    value = tokens / (region_ms / 1e3)
+    value = job_throughput(tokens, region_ms)
     e2e_value = tokens / (e2e_ms / 1e3)
     own = cfg.L - len(cfg.prerouted)
     bytes_tok = algorithmic_bytes_per_token(cfg, own)
@@ -397,14 +410,11 @@ def run_batched(args, rank, world, cfg):
     e2e_ms = a.elapsed_time(b)
     assert st.error() == 0
 
-    local = torch.tensor([region_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
-    region_ms, e2e_ms = local.tolist()
+    region_ms, e2e_ms = job_times([region_ms, e2e_ms], world, dev)
     if rank != 0:
         return None
     tokens = B * args.steps * world
-    value = tokens / (region_ms / 1e3)
+    value = job_throughput(tokens, region_ms)
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (region_ms / args.steps / 1e3) / 1e9
     line = {

@@ -260,26 +260,61 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const flo
         atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-        int run = 0, a = 0;
-        for (int e = 0; e < E; ++e) {
-            off[e] = run;
-            if (cnt[e] > 0) {
-                D->sexp[a] = e;
-                D->soff[a] = run;
-                D->scnt[a] = cnt[e];
-                ++a;
+    // exclusive scans over the experts (thread e owns expert e): position offset,
+    // slot index, and the first work item of each kernel
+    __shared__ int sc_wsum[4][32];
+    const int e = tid;
+    const int c_e = e < E ? cnt[e] : 0;
+    int v[4] = {c_e, c_e > 0 ? 1 : 0, (c_e + blk_gu - 1) / blk_gu, (c_e + blk_dn - 1) / blk_dn};
+    int incl[4];
+    const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        int x = v[q];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        incl[q] = x;
+        if (lane == 31) sc_wsum[q][wid] = x;
+    }
+    __syncthreads();
+    if (wid == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            int x = lane < (int)(blockDim.x >> 5) ? sc_wsum[q][lane] : 0;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
             }
-            run += cnt[e];
+            sc_wsum[q][lane] = x;   // inclusive over warps
+        }
+    }
+    __syncthreads();
+    int ex[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) ex[q] = incl[q] - v[q] + (wid > 0 ? sc_wsum[q][wid - 1] : 0);
+    const int nwarps = blockDim.x >> 5;
+    const int a = sc_wsum[1][nwarps - 1];   // active experts
+    if (e < E) {
+        off[e] = ex[0];
+        if (c_e > 0) {
+            const int j = ex[1];
+            D->sexp[j] = e;
+            D->soff[j] = ex[0];
+            D->scnt[j] = c_e;
+            for (int i = 0; i < v[2]; ++i) D->it_gu[ex[2] + i] = make_int2(j, i * blk_gu);
+            for (int i = 0; i < v[3]; ++i) D->it_dn[ex[3] + i] = make_int2(j, i * blk_dn);
+        }
+    }
+    if (tid == 0) {
+        // the shared expert's work items after the routed ones (slot a)
+        int ng = sc_wsum[2][nwarps - 1], nd = sc_wsum[3][nwarps - 1];
+        if (shared) {
+            for (int tb = 0; tb < B; tb += blk_gu) D->it_gu[ng++] = make_int2(a, tb);
+            for (int tb = 0; tb < B; tb += blk_dn) D->it_dn[nd++] = make_int2(a, tb);
         }
         D->nact = a;
-        // one work item per block of tokens of each active expert (and the shared expert)
-        int ng = 0, nd = 0;
-        for (int j = 0; j <= a; ++j) {
-            const int m = j < a ? D->scnt[j] : (shared ? B : 0);
-            for (int tb = 0; tb < m; tb += blk_gu) D->it_gu[ng++] = make_int2(j, tb);
-            for (int tb = 0; tb < m; tb += blk_dn) D->it_dn[nd++] = make_int2(j, tb);
-        }
         D->n_gu = ng;
         D->n_dn = nd;
     }
@@ -600,7 +635,8 @@ __global__ void __launch_bounds__(256) k_down(const LayerP Ly, const Disp* D, co
 }
 
 // ---------------------------------------------------------- k_lora_vd -------
-// One CTA per token: v = A_down act_shared (r values), y += (alpha/r) B_down v.
+// One CTA per (token, 256 output rows): v = A_down act_shared (r values, each
+// CTA of the token recomputes them), y += (alpha/r) B_down v for its rows.
 __global__ void __launch_bounds__(256) k_lora_vd(const float* act, int Imax, int pos0, const __half* AdT,
                                                  const __half* Bd, int r, int Is, int d, float scale, float* y) {
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -628,7 +664,7 @@ __global__ void __launch_bounds__(256) k_lora_vd(const float* act, int Imax, int
         vs[tid] = s;
     }
     __syncthreads();
-    for (int row = tid; row < d; row += 256) {
+    for (int row = blockIdx.y * 256 + tid; row < d && row < (int)(blockIdx.y + 1) * 256; row += 256) {
         float s = 0.f;
         for (int q = 0; q < r; ++q) s += __half2float(Bd[(long long)row * r + q]) * vs[q];
         y[(long long)b * d + row] += scale * s;
@@ -741,7 +777,8 @@ int batch_decode(const Prog& p, cudaStream_t st) {
             Ly, D, tok, wt, act, B, K, d, I, Is, Imax, y, hdr);
         if (!ok()) return EDGE0_ECUDA;
         if (lora) {
-            k_lora_vd<<<B, 256, 0, st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is, d, Ly.lora_scale, y);
+            k_lora_vd<<<dim3(B, (d + 255) / 256), 256, 0, st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is, d,
+                                                               Ly.lora_scale, y);
             if (!ok()) return EDGE0_ECUDA;
         }
     }

@@ -428,6 +428,7 @@ __host__ __device__ __noinline__ bool build_flush_items(const Prog& p, int hl, i
 // ------------------------------------------------------------ smem plan ----
 struct Ctl {
     int trace, tslot, abort, step, cdone, issued, last, ptslot;
+    unsigned long long bar_seen;   // grid-barrier count right after this CTA's last arrival
 };
 constexpr int kTraceProducer = 3072;   // first trace word of the producer's stamps
 
@@ -889,18 +890,21 @@ __device__ __forceinline__ void release_item(const LayerTab* T, int i) {
 }
 
 // grid barrier: arrive (after the caller's cbar) and wait
+// The arrival is an atomic that returns the count: the CTA whose arrival
+// completes a barrier learns it at once instead of polling for its own update
+// (the last to arrive is the one the whole grid waits for).
 __device__ void bar_arrive() {
     const Ctx& c = ctx();
     if (threadIdx.x == 0) {
         __threadfence();
-        red_release_add_u64(&c.hdr->barrier, 1ull);
+        c.ctl->bar_seen = atom_acq_rel_add_u64(&c.hdr->barrier, 1ull) + 1ull;
     }
 }
 __device__ __noinline__ bool bar_wait(unsigned long long& target) {
     const Ctx& c = ctx();
     if (threadIdx.x == 0) {
         target += (unsigned long long)c.nct;
-        if (ld_acquire_u64(&c.hdr->barrier) < target) {
+        if (c.ctl->bar_seen < target && ld_acquire_u64(&c.hdr->barrier) < target) {
             const unsigned long long t0 = now_ns();
             for (unsigned it = 0; ld_acquire_u64(&c.hdr->barrier) < target; ++it) {
                 if ((it & 15) == 15) {
@@ -1776,6 +1780,11 @@ __device__ void consumer() {
     }
     uint32_t xph1 = 0;
     volatile int* ready = SM<volatile int>(c.pl.ready);
+    {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        stamp_value(0xFFF00, smid);   // trace: the SM this CTA runs on
+    }
     float* part = SM<float>(c.pl.part);
     // every decision to leave the loop is taken from a barrier reduction, so all
     // consumer threads leave together
@@ -1799,6 +1808,7 @@ __device__ void consumer() {
         // ---------------- input x
         if (p.mode == MODE_DECODE && l > 0)
             if (!bar_wait(bar_target)) break;
+        stamp((l << 8) | 24);   // the previous layer's grid barrier seen
         if (p.mode == MODE_DECODE || l == 0) build_x(l);
         stamp((l << 8) | 1);
         // ---------------- own routing
@@ -1915,6 +1925,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         ctl->cdone = 0;
         ctl->issued = 0;
         ctl->last = 0;
+        ctl->bar_seen = 0;
         ctl->step = p.step >= 0 ? p.step : ld_volatile_s32(&c.hdr->step);
         ctl->trace = c.cta < kTraceCtas ? ld_volatile_s32(&c.hdr->trace) : 0;
         ctl->tslot = 0;

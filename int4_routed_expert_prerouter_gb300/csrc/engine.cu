@@ -21,9 +21,9 @@
 //     all the pair's rows and applies the matching 16-column slices of down
 //     (packed K-major) to its half of the output rows, adding w-weighted
 //     partial sums into y with vector reductions;
-//   * the shared expert's LoRA runs inside the pairs that own shared rows (A x
-//     over the d-halves travels with the partial sums; B_down A_down act is
-//     split linearly over the pairs);
+//   * the shared expert's LoRA runs inside the pairs that own shared rows: A x
+//     and v = A_down act are summed in small global accumulators, and the
+//     same pairs apply B_down (split over the output rows) once v is complete;
 //   * the prerouter head of layer l runs after the CTA has arrived at layer l's
 //     barrier, in the time the barrier takes; its logits accumulate in global
 //     memory and the last CTA to finish computes the top-K.
@@ -47,6 +47,7 @@ constexpr int kItemMax = 16384;    // bytes of one copy item (copies of 16 KB re
 constexpr int kSlots = 256;        // item barriers (>= 2 x kMaxItems)
 constexpr int kTables = 3;         // layer tables in flight
 constexpr int kMaxChunks = 4;      // 4-element chunks of [B, d] per consumer thread
+constexpr int kVWarp = 15;         // consumer warp that forms the LoRA v of a CTA with shared rows
 constexpr int kMaxD = 2048;
 constexpr int kMinRing = 2 * kItemMax;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // bounded waits: 2 s
@@ -102,19 +103,20 @@ struct Shape {
 // The shared expert's LoRA runs once per layer, not repeated by each pair that
 // owns shared rows: those pairs compute A_gate x and A_up x (split over d) into a
 // small global accumulator, wait for it to be complete before their act, and add
-// v = A_down act of their rows into a second one; the other pairs, after their
-// down rows, apply B_down (split over the output rows) to the complete v.
+// v = A_down act of their rows into a second one (one warp, while the others run
+// the down rows); after their down rows they apply B_down (split over the output
+// rows) to the complete v.  The routed pairs carry no LoRA work.
 
 __host__ __device__ inline int shared_pairs(int P, int n_sh, int n_rt, bool lora) {
     if (n_sh <= 0) return 0;
     if (n_rt <= 0) return P;
     // cost in int4-unit equivalents per CTA: an hr is 16 gate/up units + half a
     // 16-row down slice over half of d; shared pairs carry the LoRA A and v terms
-    // and the wait for the A sums, routed pairs the B_down rows
+    // and the wait for the A sums and the B_down rows
     int best = 0x7fffffff, pick = 1;
     for (int ps = 1; ps < P; ++ps) {
-        const int cs = ceil_div(n_sh, ps) * 24 + (lora ? 16 : 0);
-        const int cr = ceil_div(n_rt, P - ps) * 24 + (lora ? 4 : 0);
+        const int cs = ceil_div(n_sh, ps) * 24 + (lora ? 20 : 0);
+        const int cr = ceil_div(n_rt, P - ps) * 24;
         const int cmax = cs > cr ? cs : cr;
         if (cmax <= best) { best = cmax; pick = ps; }   // ties: more shared pairs
     }
@@ -167,14 +169,13 @@ __host__ __device__ inline void pair_plan(const Shape& S, int P, int pair, int r
             a = end;
         }
     }
-    // LoRA (implies a shared expert, so Ps >= 1): A units on the shared pairs,
-    // B_down rows on the routed pairs (on all pairs if there are none)
-    if (S.lora) {
+    // LoRA (implies a shared expert, so Ps >= 1): A units and B_down rows on the
+    // shared pairs
+    if (S.lora && pair < Ps) {
         const int n_gd = S.d / kGroup, ngh = half_hi(n_gd, rank) - half_lo(n_gd, rank);
         const int n_rtd = S.d / kRowTile, nrt = half_hi(n_rtd, rank) - half_lo(n_rtd, rank);
-        if (pair < Ps) split_range(2 * ngh, Ps, pair, &pp.la0, &pp.la1);
-        const int Pr = P > Ps ? P - Ps : P, ir = P > Ps ? pair - Ps : pair;
-        if (ir >= 0) split_range(nrt, Pr, ir, &pp.bd0, &pp.bd1);
+        split_range(2 * ngh, Ps, pair, &pp.la0, &pp.la1);
+        split_range(nrt, Ps, pair, &pp.bd0, &pp.bd1);
     }
     if (S.router) {
         const int n_gd = S.d / kGroup;
@@ -433,7 +434,7 @@ struct Ctl {
 constexpr int kTraceProducer = 3072;   // first trace word of the producer's stamps
 
 struct Plan {
-    int ring, full, empty, xch, lin, tabs, xf, xsum, hs, part, recv, act32, af, qsum, vlo, zpart,
+    int ring, full, empty, xch, lin, tabs, xf, xsum, hs, gam, part, recv, act32, af, qsum, vlo, zpart,
         gf, ids, wts, dist, ndist, prv, nprv, ready, rscr, red, ctl, total;
 };
 
@@ -462,6 +463,7 @@ __host__ __device__ inline Plan make_plan(const Prog& p, int base) {
     s.xf = o;     o += al16(n_gd * 4 * B * 4 * 8);   // all of d (head flush), else this CTA's half
     s.xsum = o;   o += al16(ngh * B * 4);
     s.hs = o;     o += al16(B * p.d * 2);
+    s.gam = o;    o += al16(p.d * 2);   // RMSNorm gain of the next decode layer
     s.part = o;   o += al16(msg_floats(p) * 4);
     s.recv = o;   o += al16(msg_floats(p) * 4);
     s.act32 = o;  o += al16(p.hr_max * 8 * B * 4);
@@ -976,6 +978,19 @@ __device__ __forceinline__ void f16_run(const char* base, int a, int b, int gl0,
 }
 
 // ------------------------------------------------------------ prologue ----
+// RMSNorm gain of decode layer l into shared memory with cp.async (no registers
+// held; it lands while the CTA still works on the layer before); build_x waits
+// for its own copies, and its consumer barriers publish them.
+__device__ __forceinline__ void prefetch_gamma(int l) {
+    const Prog& p = prg();
+    if (p.mode != MODE_DECODE || l >= p.L || !p.layers[l].gamma) return;
+    __half* g = SM<__half>(ctx().pl.gam);
+    const __half* src = p.layers[l].gamma;
+    for (int i = threadIdx.x; i < p.d / 4; i += kConsumerThreads)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(g + 4 * i)), "l"(src + 4 * i)
+                     : "memory");
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
 // x = fp16(RMSNorm(h) * gamma) for all tokens (decode; h updated by the previous
 // layer's y first) or x = x_in; B fragments and group sums for this CTA's half
 // of d.  The residual h stays in shared memory.  All global loads of a thread
@@ -990,6 +1005,7 @@ __device__ __noinline__ void build_x(int l) {
     __half* hs = SM<__half>(c.pl.hs);
     const float* y = (decode && l > 0) ? y_buf(c.par, p.layers[l - 1].sidx) : nullptr;
     const __half* hsrc = decode ? (l == 0 ? p.h_io : hs) : p.x_in;
+    asm volatile("cp.async.wait_all;\n" ::: "memory");   // this thread's part of the gain
     uint2 hv[kMaxChunks];
     float4 yv[kMaxChunks];
 #pragma unroll
@@ -1042,7 +1058,7 @@ __device__ __noinline__ void build_x(int l) {
     // are the 16 lanes of a half-warp)
     uint32_t* xf = SM<uint32_t>(c.pl.xf);
     float* xsum = SM<float>(c.pl.xsum);
-    const __half* gam = decode ? Ly.gamma : nullptr;
+    const __half* gam = (decode && Ly.gamma) ? SM<__half>(c.pl.gam) : nullptr;
     // one CTA keeps x of a head layer for the head flush
     __half* xs_out = (decode && c.cta == 0 && is_head_layer(p, l)) ? xs_buf(Ly.sidx) : nullptr;
 #pragma unroll 1
@@ -1060,7 +1076,7 @@ __device__ __noinline__ void build_x(int l) {
             if (decode) {
                 float g4[4] = {1.f, 1.f, 1.f, 1.f};
                 if (gam) {
-                    const uint2 gg = __ldg(reinterpret_cast<const uint2*>(gam + k));
+                    const uint2 gg = *reinterpret_cast<const uint2*>(gam + k);
                     const float2 g01 = __half22float2(*reinterpret_cast<const __half2*>(&gg.x));
                     const float2 g23 = __half22float2(*reinterpret_cast<const __half2*>(&gg.y));
                     g4[0] = g01.x; g4[1] = g01.y; g4[2] = g23.x; g4[3] = g23.y;
@@ -1407,33 +1423,55 @@ __device__ bool compute_act(int l, const LayerTab* T, bool lora) {
     }
     cbar();
     stamp((l << 8) | 11);
-    if (ok && ssh >= 0) {
-        // v[q][b] += sum over the pair's shared act rows of A_down[q][row] act[row][b],
-        // q in this CTA's half of [0, r); then count this CTA's shared rows
-        // one warp per output (q, b), its lanes splitting the rows
-        const Seg& sg = pl.seg[ssh];
-        const __half* adt = reinterpret_cast<const __half*>(ring_at(T->it[iadt]));
-        const int rows = (sg.hr1 - sg.hr0) * kHalfRow;
-        const int q0 = c.rank ? r / 2 : 0, q1 = c.rank ? r : r / 2;
-        const int lane = tid & 31, wid = tid >> 5;
-        const float* a32 = act32 + sg.hoff * 8 * B;
-        for (int o = wid; o < (q1 - q0) * B; o += kConsumerWarps) {
-            const int q = q0 + o / B, b = o % B;
-            float v = 0.f;
-            for (int j = lane; j < rows; j += 32) v += __half2float(adt[j * r + q]) * a32[j * B + b];
-            v = warp_sum(v);
-            if (lane == 0) red_add_f32(lora_g + (32 + q) * B + b, v);
-        }
-        cbar();
-        if (tid == 0) {
-            __threadfence();
-            red_release_add_u32(cnt_buf(c.par, Ly.sidx, CNT_LORA_V), (unsigned)(sg.hr1 - sg.hr0));
-        }
-    }
-    // the non-unit P1 items (LoRA B rows of gate/up) are no longer needed
+    // the non-unit P1 items (LoRA B rows of gate/up) are no longer needed; the
+    // v warp keeps A_down^T until it has formed v (phase2)
+    const bool vw = ssh >= 0 && (tid >> 5) == kVWarp;
     for (int i = T->p1; i < T->p2; ++i)
-        if (!unit_kind(T->it[i].kind)) release_item(T, i);
+        if (!unit_kind(T->it[i].kind) && !(vw && i == iadt)) release_item(T, i);
     return !cbar_or(!ok);
+}
+
+// v[q][b] += sum over the pair's shared act rows of A_down[q][row] act[row][b]
+// for q in this CTA's half of [0, r), by one warp (kVWarp) of a CTA that owns
+// shared rows, while the other warps start the down rows; then the warp counts
+// this CTA's shared rows and releases A_down^T.  Lane = (row phase js, output
+// qi): each lane sums every fourth row of one q, two shuffles join the phases.
+__device__ void lora_v_warp(int l, const LayerTab* T) {
+    Ctx& c = ctx();
+    const Prog& p = prg();
+    const LayerP& Ly = p.layers[l];
+    const int B = p.B, r = p.r, lane = threadIdx.x & 31;
+    const PairPlan& pl = T->pl;
+    const Seg& sg = pl.seg[0];
+    const __half* adt = reinterpret_cast<const __half*>(ring_at(T->it[T->iadt]));
+    const float* a32 = SM<float>(c.pl.act32) + sg.hoff * 8 * B;
+    float* vg = lora_buf(c.par, Ly.sidx) + 32 * B;
+    const int rows = (sg.hr1 - sg.hr0) * kHalfRow;
+    const int q0 = c.rank ? r / 2 : 0, q1 = c.rank ? r : r / 2;
+    const int qi = lane & 7, js = lane >> 3, q = q0 + qi;
+    float acc[EDGE0_MAX_BATCH] = {0.f, 0.f, 0.f, 0.f};
+    if (q < q1)
+        for (int j = js; j < rows; j += 4) {
+            const float a = __half2float(adt[j * r + q]);
+#pragma unroll
+            for (int b = 0; b < EDGE0_MAX_BATCH; ++b)
+                if (b < B) acc[b] += a * a32[j * B + b];
+        }
+#pragma unroll
+    for (int b = 0; b < EDGE0_MAX_BATCH; ++b) {
+        acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 8);
+        acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], 16);
+    }
+    if (js == 0 && q < q1)
+#pragma unroll
+        for (int b = 0; b < EDGE0_MAX_BATCH; ++b)
+            if (b < B) red_add_f32(vg + q * B + b, acc[b]);
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        red_release_add_u32(cnt_buf(c.par, Ly.sidx, CNT_LORA_V), (unsigned)(sg.hr1 - sg.hr0));
+    }
+    release_item(T, T->iadt);
 }
 
 // P2: down rows of this CTA's half of d over the pair's act quarters -> y.  Each
@@ -1449,6 +1487,7 @@ __device__ bool phase2(int l, const LayerTab* T, bool lora) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const PairPlan& pl = T->pl;
     bool ok = true;
+    if (lora && pl.has_sh && wid == kVWarp) lora_v_warp(l, T);
     for (int i = T->p2; i < T->p3 && ok; ++i) ok = wait_item(T, i);
     stamp((l << 8) | 9);
     if (ok && pl.n_hr > 0) {
@@ -1786,6 +1825,7 @@ __device__ void consumer() {
         stamp_value(0xFFF00, smid);   // trace: the SM this CTA runs on
     }
     float* part = SM<float>(c.pl.part);
+    prefetch_gamma(0);
     // every decision to leave the loop is taken from a barrier reduction, so all
     // consumer threads leave together
     const int nl = n_layer_tabs(p);
@@ -1810,6 +1850,7 @@ __device__ void consumer() {
             if (!bar_wait(bar_target)) break;
         stamp((l << 8) | 24);   // the previous layer's grid barrier seen
         if (p.mode == MODE_DECODE || l == 0) build_x(l);
+        prefetch_gamma(l + 1);   // build_x(l) is done with the gain of layer l
         stamp((l << 8) | 1);
         // ---------------- own routing
         if (router) {
@@ -2010,6 +2051,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         __syncwarp();
     } else {
         consumer();
+        asm volatile("cp.async.wait_all;\n" ::: "memory");   // no gain copy outlives the CTA
     }
     __syncthreads();
     if (tid == 0 && aborted()) {

@@ -234,7 +234,13 @@ __global__ void __launch_bounds__(256) k_route(const float* logits, int ldl, int
     int* rid = reinterpret_cast<int*>(sm + 8 * 3 * E) + wid * EDGE0_MAX_K;
     float* rw = sm + 8 * 3 * E + 8 * EDGE0_MAX_K + wid * EDGE0_MAX_K;
     if (b >= B) return;
-    for (int e = lane; e < E; e += 32) lg[e] = logits[(long long)b * ldl + e];
+    float v[EDGE0_MAX_E / 32];   // all of the warp's loads in flight at once
+#pragma unroll
+    for (int i = 0; i < EDGE0_MAX_E / 32; ++i)
+        if (lane + 32 * i < E) v[i] = logits[(long long)b * ldl + lane + 32 * i];
+#pragma unroll
+    for (int i = 0; i < EDGE0_MAX_E / 32; ++i)
+        if (lane + 32 * i < E) lg[lane + 32 * i] = v[i];
     __syncwarp();
     warp_route(lg, E, K, kind, ng, G, scale, bias, lg + E, rid, rw, lane);
     if (lane < K) {

@@ -706,6 +706,23 @@ __device__ bool make_dist(int l) {
     return ok;
 }
 
+// make_dist by one warp (B K <= 32 ids, lane i holding id i): an id is new if
+// no lower lane holds it; its slot is its rank among the new ids
+__device__ bool make_dist_warp(int l, int lane) {
+    const Ctx& c = ctx();
+    const Prog& p = prg();
+    const int n = p.B * p.K;
+    const int e = lane < n ? ids_of(l)[lane] : -1;
+    const bool bad = lane < n && (e < 0 || e >= p.E);
+    const unsigned act = __ballot_sync(0xffffffffu, lane < n && !bad);
+    const unsigned same = __match_any_sync(0xffffffffu, lane < n && !bad ? e : -1);
+    const bool first = lane < n && !bad && (__ffs(same & act) - 1) == lane;
+    const unsigned firsts = __ballot_sync(0xffffffffu, first);
+    if (first) dist_of(l)[__popc(firsts & ((1u << lane) - 1u))] = e;
+    if (lane == 0) SM<int>(c.pl.ndist)[l] = __popc(firsts);
+    return !__any_sync(0xffffffffu, bad);
+}
+
 // ------------------------------------------------------------ producer -----
 // global source of an item; null: nothing to copy (a routed slot no token uses);
 // (const char*)1: an expert slot outside the stacks
@@ -1202,10 +1219,13 @@ __device__ __noinline__ void route_layer(int l) {
         }
     }
     cbar();
-    if (tid == 0) {
-        if (!make_dist(l)) raise_error(EDGE0_EINVAL);
-        __threadfence_block();
-        SM<volatile int>(c.pl.ready)[l] = 1;
+    if (tid < 32) {
+        const bool ok = make_dist_warp(l, lane);
+        if (lane == 0) {
+            if (!ok) raise_error(EDGE0_EINVAL);
+            __threadfence_block();
+            SM<volatile int>(c.pl.ready)[l] = 1;
+        }
     }
     cbar();
 }
@@ -1856,8 +1876,10 @@ __device__ void consumer() {
         if (router) {
             const bool ok = phase_router(l, T);
             if (cbar_or(!ok || aborted())) break;
+            stamp((l << 8) | 40);   // router units done
             bar_arrive();
             if (!bar_wait(bar_target)) break;
+            stamp((l << 8) | 42);   // the router barrier seen
             route_layer(l);
         }
         if (p.mode == MODE_DECODE && c.cta == 0) {
@@ -1921,7 +1943,10 @@ __device__ void consumer() {
     if (c.cta == 0 && tid == 0 && p.step < 0) c.hdr->step = c.step + 1;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ Prog prog) {
+// The pair shape is part of the kernel (compile-time cluster dimensions): every
+// launch of it, a profiler's replay included, runs in CTA pairs.
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads, 1)
+    engine_kernel(const __grid_constant__ Prog prog) {
     const int tid = threadIdx.x;
     // parameters and context into shared memory
     {
@@ -2088,18 +2113,12 @@ int engine_grid(int* nct) {
         const int dyn = maxsm - (int)fa.sharedSizeBytes;
         if (cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
             return EDGE0_ECUDA;
+        // (the cluster shape comes from the kernel's compile-time dimensions)
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(kClusterCtas);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = dyn;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = kClusterCtas;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
         int ncl = 0;
         if (cudaOccupancyMaxActiveClusters(&ncl, (void*)engine_kernel, &cfg) != cudaSuccess || ncl < 2)
             return EDGE0_ECUDA;
@@ -2256,15 +2275,11 @@ int engine_launch(Prog& p, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute at[2];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = kClusterCtas;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeCooperative;
-    at[1].val.cooperative = 1;
+    cudaLaunchAttribute at[1];   // the cluster shape is compiled into the kernel
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, engine_kernel, p) != cudaSuccess) return EDGE0_ECUDA;
     return EDGE0_OK;
 }

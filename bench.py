@@ -333,6 +333,10 @@ def run_batched(args, rank, world, cfg):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
+    if args.layers:
+        # reduced case for profiler captures only (same per-layer shapes)
+        cfg = cfg.with_(L=args.layers, head_owner_last=min(cfg.head_owner_last, args.layers - 2),
+                        prerouted=tuple(l for l in cfg.prerouted if l < args.layers - 1))
     model = inputs.make_model(cfg, seed=args.seed, device=dev, small_device=dev)
     dm = binding.DeviceModel(model, dev)
     del model
@@ -431,7 +435,8 @@ def run_batched(args, rank, world, cfg):
         "dtype": "int4xf16",
         "data": "synthetic",
         "config": {
-            "workload": f"{cfg.name}: {cfg.description}",
+            "workload": (f"{cfg.name}: {cfg.description}" if not args.layers else
+                         f"REDUCED profiling case: {cfg.L} layers, shapes of {cfg.name}"),
             "layers": cfg.L, "d_model": d, "experts": cfg.E, "top_k": cfg.K, "batch": B, "seq_len": 1,
             "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2 (%.0f MB of weights read per step > 129 MB)" % (step_bytes / 1e6),

@@ -394,17 +394,28 @@ __device__ __forceinline__ bool slot_of(int j, const Disp* D, const LayerP& Ly, 
 // 576-byte int4 slices group by group through a 4-stage ring in shared memory
 // (cp.async for device-resident experts, plain loads for host-tier ones), three
 // groups in flight.
-constexpr int kExpWarps = 8;
-constexpr int kGuTok = 8;     // tokens per gate/up block (one mma column tile)
-constexpr int kDnTok = 16;    // tokens per down block (4 tiles of 4 tokens x hi/lo)
+constexpr int kExpWarps = 8;   // warps of a down CTA
+constexpr int kGuWarps = 16;   // warps of a gate/up CTA
+constexpr int kGuTok = 32;     // tokens per gate/up block (4 mma column tiles)
+constexpr int kGuNt = kGuTok / 8;
+constexpr int kGuStages = 8;   // gate/up ring depth per warp: 7 groups in flight
+constexpr int kDnTok = 16;     // tokens per down block (4 tiles of 4 tokens x hi/lo)
 constexpr int kStages = 4;
 constexpr int kSlice = 576;   // one group of one row tile: 512 B of nibbles + 64 B of (s, b)
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+// four 8x8 b16 matrices from shared memory (lane l gives the row address of
+// matrix l / 8, row l % 8; register i holds matrix i's fragment)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_2() { asm volatile("cp.async.wait_group 2;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_6() { asm volatile("cp.async.wait_group 6;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // one 16-byte piece of a slice into the ring: asynchronous from device memory,
@@ -415,91 +426,137 @@ __device__ __forceinline__ void piece(void* dst, const char* src, bool host) {
 }
 
 // --------------------------------------------------------------- k_gu -------
-// gate/up of one expert for all of its tokens: warp w of CTA x takes the
-// interleaved 16-row tile 8 x + w (gate rows of act rows 8 (8 x + w) .. + 7 and
-// the same up rows) over all of d, 8 tokens per block.  act[position][row] =
-// silu(gate) up (the shared expert's gate and up with their LoRA terms
-// (alpha/r) B (A x), A x precomputed in la).
+// gate/up of one expert for a block of up to 32 of its tokens: warp w of CTA x
+// takes the interleaved 16-row tile 16 x + w (gate rows of act rows
+// 8 (16 x + w) .. + 7 and the same up rows) over all of d, and runs each int4
+// fragment against the block's 4 token column tiles (the nibble masks are taken
+// once per fragment).  act[position][row] = silu(gate) up (the shared expert's
+// gate and up with their LoRA terms (alpha/r) B (A x), A x precomputed in la).
+// Each warp streams its tile's 576-byte slices group by group through an
+// 8-stage ring (7 groups in flight), started before the token rows are staged.
 // Dynamic shared memory: x rows [kGuTok][d + 8] fp16 (padded: conflict-free
-// fragment reads), x group sums [kGuTok][d/64], ring [8 warps][4][576 B].
-__global__ void __launch_bounds__(256) k_gu(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
-                                            const __half* __restrict__ x, const float* __restrict__ xsum,
-                                            const float* la, int lora, int r, int B, int K, int d, int I, int Is,
-                                            int Imax, float* act, WsHeader* hdr) {
+// fragment reads), x group sums [kGuTok][d/64], ring [16 warps][8][576 B].
+__global__ void __launch_bounds__(kGuWarps * 32) k_gu(const LayerP Ly, const Disp* D, const int* tok,
+                                                      const float* wt, const __half* __restrict__ x,
+                                                      const float* __restrict__ xsum, const float* la, int lora,
+                                                      int r, int B, int K, int d, int I, int Is, int Imax,
+                                                      float* act, WsHeader* hdr) {
     extern __shared__ __align__(16) char gsm[];
-    if ((int)blockIdx.y >= D->n_gu) return;   // CTA-uniform
-    const int2 item = D->it_gu[blockIdx.y];
-    Slot S;
-    if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
+    auto run_item = [&](const int2 item, const Slot& S) {
+    constexpr int NT = kGuWarps * 32;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
     const int n_gd = d / kGroup, hn = n_gd / 2, RTI = S.I / kHalfRow, ld = d + 8;
     __half* xrow = reinterpret_cast<__half*>(gsm);
     float* xss = reinterpret_cast<float*>(gsm + kGuTok * ld * 2);
-    char* ring = gsm + kGuTok * ld * 2 + kGuTok * n_gd * 4 + wid * kStages * kSlice;
-    const int rt = blockIdx.x * kExpWarps + wid;
+    char* ring = gsm + kGuTok * ld * 2 + kGuTok * n_gd * 4 + wid * kGuStages * kSlice;
+    const int rt = blockIdx.x * kGuWarps + wid;
     const bool live = rt < RTI;
-    auto unit_of = [&](int gg) {
-        const int h = gg / hn, gl = gg - h * hn;
-        return S.gu + ((long long)(h * RTI + rt) * hn + gl) * kQ4Unit;
-    };
-    auto fill = [&](int gg) {
-        if (gg < n_gd) {
-            char* dst = ring + (gg & (kStages - 1)) * kSlice;
-            const char* src = unit_of(gg);
-            piece(dst + 16 * lane, src + 16 * lane, S.host);
-            if (lane < 4) piece(dst + 512 + 16 * lane, src + 512 + 16 * lane, S.host);
+    // the tile's units in group order: half 0's groups, then half 1's (the source
+    // advances by one unit, and jumps to the other half once)
+    const char* nxt = S.gu + (long long)rt * hn * kQ4Unit;
+    int gn = 0;   // groups filled so far
+    auto fill = [&]() {
+        if (gn < n_gd) {
+            char* dst = ring + (gn & (kGuStages - 1)) * kSlice;
+            piece(dst + 16 * lane, nxt + 16 * lane, S.host);
+            if (lane < 4) piece(dst + 512 + 16 * lane, nxt + 512 + 16 * lane, S.host);
+            nxt += kQ4Unit;
+            if (++gn == hn) nxt += (long long)(RTI - 1) * hn * kQ4Unit;
         }
         cp_commit();
     };
+    // the weight stream first: it does not depend on the token rows
+    if (live)
+        for (int j = 0; j < kGuStages - 1; ++j) fill();
+    const int tb = item.y;
     {
-        const int tb = item.y;
-        for (int e = tid; e < kGuTok * (d / 8); e += 256) {
-            const int q = e / (d / 8), c = e - q * (d / 8), p = tb + q;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (p < S.m) v = __ldg(reinterpret_cast<const uint4*>(x + (long long)(S.toks ? S.toks[p] : p) * d) + c);
-            *reinterpret_cast<uint4*>(xrow + q * ld + c * 8) = v;
-        }
-        for (int e = tid; e < kGuTok * n_gd; e += 256) {
-            const int q = e / n_gd, gg = e - q * n_gd, p = tb + q;
-            xss[e] = p < S.m ? __ldg(xsum + (long long)(S.toks ? S.toks[p] : p) * n_gd + gg) : 0.f;
-        }
-        __syncthreads();
-        if (!live) return;
-        float racc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < kStages - 1; ++j) fill(j);
-        const __half* xg = xrow + g * ld + 2 * t;
-        for (int gg = 0; gg < n_gd; ++gg) {
-            cp_wait_2();
-            __syncwarp();
-            const char* u = ring + (gg & (kStages - 1)) * kSlice;
-            const uint4 wv = *reinterpret_cast<const uint4*>(u + 16 * lane);
-            const uint2 sc = *reinterpret_cast<const uint2*>(u + 512 + 8 * g);
-            __syncwarp();
-            fill(gg + kStages - 1);
-            const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // the block's token rows and group sums: 16 threads per token, every load
+        // of a pass issued before any store (one round trip per pass)
+        static_assert(kGuTok * 16 == NT, "16 threads per token");
+        const int q = tid >> 4, j = tid & 15, p = tb + q;
+        const bool valid = p < S.m;
+        const long long row = valid ? (S.toks ? S.toks[p] : p) : 0;
+        const uint4* src = reinterpret_cast<const uint4*>(x + row * d);
+        const int nc = d / 8;
+        for (int c0 = 0; c0 < nc; c0 += 16 * 16) {
+            uint4 v[16];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                uint32_t A[4];
-                q4_masks(wq[s], A);
-                const __half* xp = xg + gg * kGroup + s * 16;
-                mma_16816(acc, A, *reinterpret_cast<const uint32_t*>(xp), *reinterpret_cast<const uint32_t*>(xp + 8));
+            for (int i = 0; i < 16; ++i) {
+                const int c = c0 + j + 16 * i;
+                v[i] = valid && c < nc ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
             }
-            const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) of row g
-            const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) of row g + 8
-            const float xs0 = xss[(2 * t) * n_gd + gg], xs1 = xss[(2 * t + 1) * n_gd + gg];
-            racc[0] += __low2float(s0) * kTwo24 * acc[0] + __high2float(s0) * xs0;
-            racc[1] += __low2float(s0) * kTwo24 * acc[1] + __high2float(s0) * xs1;
-            racc[2] += __low2float(s1) * (kTwo24 / 16.0f) * acc[2] + __high2float(s1) * xs0;
-            racc[3] += __low2float(s1) * (kTwo24 / 16.0f) * acc[3] + __high2float(s1) * xs1;
+            float xv[2] = {0.f, 0.f};
+            if (c0 == 0)
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (valid && j + 16 * i < n_gd) xv[i] = __ldg(xsum + row * n_gd + j + 16 * i);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c = c0 + j + 16 * i;
+                if (c < nc) *reinterpret_cast<uint4*>(xrow + q * ld + c * 8) = v[i];
+            }
+            if (c0 == 0)
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (j + 16 * i < n_gd) xss[q * n_gd + j + 16 * i] = xv[i];
         }
-        cp_wait_0();
-        const int arow = rt * kHalfRow + g;
+        for (int gg = j + 32; gg < n_gd; gg += 16)   // d > 2048 only
+            xss[q * n_gd + gg] = valid ? __ldg(xsum + row * n_gd + gg) : 0.f;
+    }
+    __syncthreads();
+    if (!live) return;
+    float racc[kGuNt][4];
+#pragma unroll
+    for (int n = 0; n < kGuNt; ++n) racc[n][0] = racc[n][1] = racc[n][2] = racc[n][3] = 0.f;
+    // B fragments by ldmatrix: lane l addresses row l % 8 of 8x8 matrix l / 8;
+    // matrices (tokens 8 n .. + 7) x (k 0..7 | 8..15) for n-tile pairs
+    const uint32_t xl = smem_u32(xrow + (8 * ((lane >> 3) >> 1) + (lane & 7)) * ld + 8 * ((lane >> 3) & 1));
+    for (int gg = 0; gg < n_gd; ++gg) {
+        cp_wait_6();
+        __syncwarp();
+        const char* u = ring + (gg & (kGuStages - 1)) * kSlice;
+        const uint4 wv = *reinterpret_cast<const uint4*>(u + 16 * lane);
+        const uint2 sc = *reinterpret_cast<const uint2*>(u + 512 + 8 * g);
+        __syncwarp();
+        fill();
+        const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+        float acc[kGuNt][4];
+#pragma unroll
+        for (int n = 0; n < kGuNt; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            uint32_t A[4];
+            q4_masks(wq[s], A);
+#pragma unroll
+            for (int n2 = 0; n2 < kGuNt / 2; ++n2) {
+                uint32_t b[4];
+                ldsm_x4(xl + (uint32_t)((16 * n2 * ld + gg * kGroup + s * 16) * 2), b);
+                mma_16816(acc[2 * n2], A, b[0], b[1]);
+                mma_16816(acc[2 * n2 + 1], A, b[2], b[3]);
+            }
+        }
+        const __half2 s0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) of row g
+        const __half2 s1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) of row g + 8
+        const float a0 = __low2float(s0) * kTwo24, b0 = __high2float(s0);
+        const float a1 = __low2float(s1) * (kTwo24 / 16.0f), b1 = __high2float(s1);
+#pragma unroll
+        for (int n = 0; n < kGuNt; ++n) {
+            const float xs0 = xss[(8 * n + 2 * t) * n_gd + gg], xs1 = xss[(8 * n + 2 * t + 1) * n_gd + gg];
+            racc[n][0] += a0 * acc[n][0] + b0 * xs0;
+            racc[n][1] += a0 * acc[n][1] + b0 * xs1;
+            racc[n][2] += a1 * acc[n][2] + b1 * xs0;
+            racc[n][3] += a1 * acc[n][3] + b1 * xs1;
+        }
+    }
+    cp_wait_0();
+    const int arow = rt * kHalfRow + g;
+#pragma unroll
+    for (int n = 0; n < kGuNt; ++n)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            const int q = tb + 2 * t + c;
+            const int q = tb + 8 * n + 2 * t + c;
             if (q >= S.m) continue;
-            float gate = racc[c], up = racc[2 + c];
+            float gate = racc[n][c], up = racc[n][2 + c];
             if (S.shared && lora) {
                 const int b = S.toks ? S.toks[q] : q;
                 const __half* bg = Ly.lora_Bg + (long long)arow * r;
@@ -514,6 +571,15 @@ __global__ void __launch_bounds__(256) k_gu(const LayerP Ly, const Disp* D, cons
             }
             act[(long long)(S.pos0 + q) * Imax + arow] = silu_f(gate) * up;
         }
+    };
+    // the CTAs of a column take the work items in turn (the grid is sized to the
+    // GPU, not to the most items a layer can have)
+    for (int yi = blockIdx.y; yi < D->n_gu; yi += gridDim.y) {   // CTA-uniform
+        Slot S;
+        const int2 item = D->it_gu[yi];
+        if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) continue;
+        run_item(item, S);
+        __syncthreads();   // the staged token rows are reused by the next item
     }
 }
 
@@ -525,14 +591,11 @@ __global__ void __launch_bounds__(256) k_gu(const LayerP Ly, const Disp* D, cons
 // 64 B of scales) is gathered into the ring in the unit layout of gate/up.
 // Dynamic shared memory: act fragments [I/64][4 steps][4 tiles][32 lanes] uint2,
 // act group sums [kDnTok][I/64], ring [8 warps][4][576 B].
-__global__ void __launch_bounds__(256) k_down(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
+__global__ void __launch_bounds__(256, 3) k_down(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
                                               const float* __restrict__ act, int B, int K, int d, int I, int Is,
                                               int Imax, float* y, WsHeader* hdr) {
     extern __shared__ __align__(16) char dsm[];
-    if ((int)blockIdx.y >= D->n_dn) return;   // CTA-uniform
-    const int2 item = D->it_dn[blockIdx.y];
-    Slot S;
-    if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) return;
+    auto run_item = [&](const int2 item, const Slot& S) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
     const int n_rtd = d / kRowTile, nh = n_rtd / 2, ngi = S.I / kGroup, ngmax = Imax / kGroup;
     uint2* afr = reinterpret_cast<uint2*>(dsm);
@@ -550,27 +613,44 @@ __global__ void __launch_bounds__(256) k_down(const LayerP Ly, const Disp* D, co
         }
         cp_commit();
     };
+    // the weight stream first: it does not depend on the act rows
+    if (live)
+        for (int j = 0; j < kStages - 1; ++j) fill(j);
     {
         const int tb = item.y;
-        for (int e = tid; e < ngi * 512; e += 256) {
-            const int ln = e & 31, n = (e >> 5) & 3, s = (e >> 7) & 3, gg = e >> 9;
-            const int p = tb + n * 4 + (ln >> 3), part = (ln >> 2) & 1;
-            uint2 v = make_uint2(0u, 0u);
-            if (p < S.m) {
-                const float* ar = act + (long long)(S.pos0 + p) * Imax + gg * kGroup + s * 16 + 2 * (ln & 3);
-                const float2 a0 = *reinterpret_cast<const float2*>(ar);
-                const float2 a1 = *reinterpret_cast<const float2*>(ar + 8);
-                const __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a1.x, a1.y);
+        // act fragments, 8 per thread and pass with every load of a pass issued
+        // before any conversion (one round trip per pass)
+        for (int e0 = 0; e0 < ngi * 512; e0 += 8 * 256) {
+            float2 a0[8], a1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + tid + 256 * i;
+                const int ln = e & 31, n = (e >> 5) & 3, s = (e >> 7) & 3, gg = e >> 9;
+                const int p = tb + n * 4 + (ln >> 3);
+                a0[i] = a1[i] = make_float2(0.f, 0.f);
+                if (e < ngi * 512 && p < S.m) {
+                    const float* ar = act + (long long)(S.pos0 + p) * Imax + gg * kGroup + s * 16 + 2 * (ln & 3);
+                    a0[i] = *reinterpret_cast<const float2*>(ar);
+                    a1[i] = *reinterpret_cast<const float2*>(ar + 8);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + tid + 256 * i;
+                if (e >= ngi * 512) continue;
+                const int part = ((e & 31) >> 2) & 1;
+                const __half2 h0 = __floats2half2_rn(a0[i].x, a0[i].y), h1 = __floats2half2_rn(a1[i].x, a1[i].y);
+                uint2 v;
                 if (!part) {
                     v.x = *reinterpret_cast<const uint32_t*>(&h0);
                     v.y = *reinterpret_cast<const uint32_t*>(&h1);
                 } else {
                     const float2 r0 = __half22float2(h0), r1 = __half22float2(h1);
-                    v.x = pack_h2((a0.x - r0.x) * kLoScale, (a0.y - r0.y) * kLoScale);
-                    v.y = pack_h2((a1.x - r1.x) * kLoScale, (a1.y - r1.y) * kLoScale);
+                    v.x = pack_h2((a0[i].x - r0.x) * kLoScale, (a0[i].y - r0.y) * kLoScale);
+                    v.y = pack_h2((a1[i].x - r1.x) * kLoScale, (a1[i].y - r1.y) * kLoScale);
                 }
+                afr[e] = v;
             }
-            afr[e] = v;
         }
         for (int e = tid; e < kDnTok * ngi; e += 256) {
             const int q = e / ngi, gg = e - q * ngi, p = tb + q;
@@ -589,7 +669,6 @@ __global__ void __launch_bounds__(256) k_down(const LayerP Ly, const Disp* D, co
         float o[4][2];
 #pragma unroll
         for (int n = 0; n < 4; ++n) o[n][0] = o[n][1] = 0.f;
-        for (int j = 0; j < kStages - 1; ++j) fill(j);
         for (int gg = 0; gg < ngi; ++gg) {
             cp_wait_2();
             __syncwarp();
@@ -637,6 +716,14 @@ __global__ void __launch_bounds__(256) k_down(const LayerP Ly, const Disp* D, co
             red_add_f32(y + (long long)b * d + row, w * o[n][0]);
             red_add_f32(y + (long long)b * d + row + 8, w * o[n][1]);
         }
+    }
+    };
+    for (int yi = blockIdx.y; yi < D->n_dn; yi += gridDim.y) {   // CTA-uniform, as in k_gu
+        Slot S;
+        const int2 item = D->it_dn[yi];
+        if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) continue;
+        run_item(item, S);
+        __syncthreads();   // the staged act fragments are reused by the next item
     }
 }
 
@@ -740,10 +827,25 @@ int batch_decode(const Prog& p, cudaStream_t st) {
     auto ok = [] { return cudaGetLastError() == cudaSuccess; };
     // staged B fragments (+ group sums) of one token block
     const size_t ring = (size_t)kExpWarps * kStages * kSlice;
-    const size_t smem_gu = (size_t)kGuTok * (d + 8) * 2 + (size_t)kGuTok * (d / kGroup) * 4 + ring;
+    const size_t smem_gu = (size_t)kGuTok * (d + 8) * 2 + (size_t)kGuTok * (d / kGroup) * 4 +
+                           (size_t)kGuWarps * kGuStages * kSlice;
     const size_t smem_dn = (size_t)(Imax / kGroup) * 512 * 8 + (size_t)kDnTok * (Imax / kGroup) * 4 + ring;
+    int dev = 0, smem_max = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return EDGE0_ECUDA;
+    if (smem_gu > (size_t)smem_max || smem_dn > (size_t)smem_max) return EDGE0_EUNSUPPORTED;   // d or I too large
     static size_t done_gu = 0, done_dn = 0;
     if (!smem_opt_in(k_gu, smem_gu, &done_gu) || !smem_opt_in(k_down, smem_dn, &done_dn)) return EDGE0_ECUDA;
+    // expert grids: the CTAs that fit on the GPU at once, each looping over items
+    int nsm = 0, occ_gu = 0, occ_dn = 0;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_gu, k_gu, kGuWarps * 32, smem_gu) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_dn, k_down, 256, smem_dn) != cudaSuccess)
+        return EDGE0_ECUDA;
+    const int gu_x = (Imax / kHalfRow + kGuWarps - 1) / kGuWarps, dn_x = (d / kRowTile + kExpWarps - 1) / kExpWarps;
+    const int gu_y = std::max(1, std::min(items_gu, nsm * std::max(occ_gu, 1) / gu_x));
+    const int dn_y = std::max(1, std::min(items_dn, nsm * std::max(occ_dn, 1) / dn_x));
     int rc = EDGE0_OK;
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
         const LayerP& Ly = p.layers[l];
@@ -776,10 +878,10 @@ int batch_decode(const Prog& p, cudaStream_t st) {
             if (rc == EDGE0_OK) rc = dense<false>(Ly.lora_Au, 0, r, d, x, nullptr, d, B, la + 16, 32, false, st);
             if (rc) return rc;
         }
-        k_gu<<<dim3((Imax / kHalfRow + kExpWarps - 1) / kExpWarps, items_gu), 256, smem_gu, st>>>(
+        k_gu<<<dim3(gu_x, gu_y), kGuWarps * 32, smem_gu, st>>>(
             Ly, D, tok, wt, x, xsum, la, lora, r, B, K, d, I, Is, Imax, act, hdr);
         if (!ok()) return EDGE0_ECUDA;
-        k_down<<<dim3((d / kRowTile + kExpWarps - 1) / kExpWarps, items_dn), 256, smem_dn, st>>>(
+        k_down<<<dim3(dn_x, dn_y), 256, smem_dn, st>>>(
             Ly, D, tok, wt, act, B, K, d, I, Is, Imax, y, hdr);
         if (!ok()) return EDGE0_ECUDA;
         if (lora) {

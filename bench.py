@@ -63,11 +63,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+ENGINE_SOURCES = ("int4_routed_expert_prerouter_gb300/csrc/engine.cu",
+                  "int4_routed_expert_prerouter_gb300/csrc/internal.cuh",
+                  "int4_routed_expert_prerouter_gb300/csrc/common.cuh",
+                  "include/edge0.h")
+
+
 def kernel_source_hash():
+    """Hash of the sources the engine kernel is compiled from."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "int4_routed_expert_prerouter_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ENGINE_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -70,10 +71,14 @@ ENGINE_SOURCES = ("int4_routed_expert_prerouter_gb300/csrc/engine.cu",
 
 
 def kernel_source_hash():
-    """Hash of the sources the engine kernel is compiled from."""
+    """Hash of the code the engine kernel is compiled from: its sources with the
+    comments and whitespace taken out (a comment edit does not change the kernel)."""
     h = hashlib.sha256()
     for f in ENGINE_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        text = open(os.path.join(ROOT, f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -24,9 +24,9 @@
 //   * the shared expert's LoRA runs inside the pairs that own shared rows: A x
 //     and v = A_down act are summed in small global accumulators, and the
 //     same pairs apply B_down (split over the output rows) once v is complete;
-//   * the prerouter head of layer l runs after the CTA has arrived at layer l's
-//     barrier, in the time the barrier takes; its logits accumulate in global
-//     memory and the last CTA to finish computes the top-K.
+//   * every prerouter head of the step runs in one flush after the last layer
+//     (a head's prediction is consumed one token later); its logits accumulate
+//     in global memory and the last CTA to finish its tasks computes the top-K.
 // The producer warp streams each CTA's weight slices into a byte ring of shared
 // memory with bulk copies as soon as the routing that selects them is known
 // (prerouted layers: at step start, so the stream runs ahead across barriers).

@@ -72,12 +72,16 @@ ENGINE_SOURCES = ("int4_routed_expert_prerouter_gb300/csrc/engine.cu",
 
 def kernel_source_hash():
     """Hash of the code the engine kernel is compiled from: its sources with the
-    comments and whitespace taken out (a comment edit does not change the kernel)."""
+    comments and whitespace taken out (a comment edit does not change the
+    kernel), and of the public header only the constants (#define lines) that
+    the kernel uses (a new host-side declaration does not change it either)."""
     h = hashlib.sha256()
     for f in ENGINE_SOURCES:
         text = open(os.path.join(ROOT, f), encoding="utf-8").read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
+        if f.endswith("edge0.h"):
+            text = "\n".join(line for line in text.splitlines() if line.lstrip().startswith("#define"))
         h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
@@ -368,10 +372,42 @@ def run_batched(args, rank, world, cfg):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    def step(t, prefetch=True):
-        binding.decode_step(dm, st, h_all[t], t)
-        if pool is not None and prefetch:
+    # host-tier arms: copy-engine prefetch of the prerouted layers' predictions
+    # (the product path), least-recently-used caching of every layer's executed
+    # experts without a prediction, or no copies at all (resident set frozen)
+    def step(t, prefetch="prediction"):
+        binding.decode_step(dm, st, h_all[t % n_in], t)
+        if pool is not None and prefetch == "prediction":
             pool.prefetch(st, t, prerouted)
+        elif pool is not None and prefetch == "executed":
+            pool.prefetch(st, t, range(cfg.L), source="executed")
+
+    def cold_pass(prefetch, n):
+        """Untimed steps, each synchronised: the share of (layer, executed
+        expert) pairs that the step found outside HBM (read from host memory),
+        over all layers and over the prerouted ones."""
+        nonlocal t
+        cold = [0, 0]
+        tot = [0, 0]
+        for _ in range(n):
+            res = [pool.resident(l) for l in range(cfg.L)]   # the map this step runs with
+            step(t, prefetch=None)
+            ex = st.exec_ids[t & 1].cpu().numpy()
+            if prefetch == "prediction":
+                pool.prefetch(st, t, prerouted)
+            elif prefetch == "executed":
+                pool.prefetch(st, t, range(cfg.L), source="executed")
+            for l in range(cfg.L):
+                ids = np.unique(ex[l])
+                c = int((res[l][ids] < 0).sum())
+                cold[0] += c
+                tot[0] += len(ids)
+                if l in prerouted:
+                    cold[1] += c
+                    tot[1] += len(ids)
+            t += 1
+        barrier()
+        return round(cold[0] / max(tot[0], 1), 4), round(cold[1] / max(tot[1], 1), 4), tot[0] / n
 
     t = 0
     for _ in range(args.warmup):
@@ -381,7 +417,7 @@ def run_batched(args, rank, world, cfg):
     err = st.error()
     assert err == 0, f"kernel error during warm-up: {binding.status_string(err)}"
 
-    def timed(prefetch=True):
+    def timed(prefetch="prediction"):
         nonlocal t
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
@@ -403,7 +439,27 @@ def run_batched(args, rank, world, cfg):
     ex = st.exec_ids.cpu().numpy()
     own = cfg.L - len(cfg.prerouted)
     step_bytes = statistics.mean(batched_bytes_per_step(cfg, ex[p], own) for p in (0, 1))
-    off_ms = timed(prefetch=False) if pool is not None else None
+    arms = {}
+    if pool is not None:
+        ebytes = pool.gu_bytes + pool.dn_bytes
+        for arm in ("prediction", "executed", None):
+            for _ in range(args.warmup):   # the arm's steady state
+                step(t, arm)
+                t += 1
+            c0 = pool.stats()[1]
+            ms = region_ms if arm == "prediction" else timed(prefetch=arm)
+            if arm == "prediction":
+                c0 = copies0
+                c1 = copies1
+            else:
+                c1 = pool.stats()[1]
+            cold_all, cold_pre, active = cold_pass(arm, 8)
+            arms[arm or "frozen"] = {
+                "tokens_per_s": round(B * args.steps / (ms / 1e3), 2),
+                "cold_fraction": cold_all, "cold_fraction_prerouted_layers": cold_pre,
+                "copied_mb_per_step": round((c1 - c0) / args.steps * ebytes / 1e6, 1),
+                "host_read_mb_per_step": round(cold_all * active * ebytes / 1e6, 1)}
+        assert st.error() == 0
 
     # end to end: pinned host input -> device, decode step, device -> host, every step
     h_host = torch.empty(args.steps, B, d, dtype=torch.float16).pin_memory()
@@ -472,8 +528,14 @@ def run_batched(args, rank, world, cfg):
         line["pool"] = {"slots_per_layer": pool.n_slots, "experts": cfg.E,
                         "prefetch_hit_rate": round((hits1 - hits0) / max(req, 1), 4),
                         "experts_copied_per_step": round((copies1 - copies0) / args.steps, 2),
-                        "prefetch_off_tokens_per_s": round(tokens / (off_ms / 1e3), 2),
-                        "prefetch_off": "no copies: resident set frozen, misses read from host memory"}
+                        "prefetch_off_tokens_per_s": arms["frozen"]["tokens_per_s"],
+                        "prefetch_off": "no copies: resident set frozen, misses read from host memory",
+                        "arms": arms,
+                        "arms_note": ("prediction: copy-engine prefetch of the prerouted layers' predicted "
+                                      "experts (the timed line); executed: LRU caching of every layer's "
+                                      "executed experts, no prediction; frozen: no copies. cold_fraction: "
+                                      "executed (layer, expert) pairs read from host memory, from 8 "
+                                      "synchronised steps after each arm's timed region")}
     return line
 
 

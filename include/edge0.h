@@ -269,7 +269,11 @@ int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
  *                          between this call and the completion of its copies:
  *                          record an event on `stream` after it and pass it as
  *                          the layer's `ready` event.
- *   edge0_pool_stats       requested experts found resident / copied, so far. */
+ *   edge0_pool_stats       requested experts found resident / copied, so far.
+ *   edge0_pool_resident    the planner's map of layer l: slot_of[e] = the slot
+ *                          of expert e, or -1 (host tier), E entries written to
+ *                          host memory.  After a prefetch it is the map the
+ *                          layer's next decode uses once its copies are done. */
 typedef struct edge0_pool edge0_pool;
 int edge0_pool_create(int L, int E, int n_slots, size_t gu_bytes, size_t dn_bytes, edge0_pool** out);
 int edge0_pool_set_layer(edge0_pool* pool, int l, const void* host_gu, const void* host_dn, void* dev_gu,
@@ -279,6 +283,7 @@ int edge0_pool_plan(edge0_pool* pool, int l, const int32_t* ids, int n, int32_t*
 int edge0_pool_prefetch(edge0_pool* pool, int l, const int32_t* ids, int n, cudaStream_t stream,
                         int* copied);
 int edge0_pool_stats(const edge0_pool* pool, long long* hits, long long* copies);
+int edge0_pool_resident(const edge0_pool* pool, int l, int32_t* slot_of);
 void edge0_pool_destroy(edge0_pool* pool);
 
 /* ---- allocation-free variant (the paper has no counterpart to this call) ----

@@ -9,6 +9,7 @@ from __future__ import annotations
 import ctypes as C
 import os
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -97,6 +98,7 @@ def _declare(L):
     L.edge0_pool_plan.argtypes = [P, C.c_int, P, C.c_int, P, P, C.POINTER(C.c_int)]
     L.edge0_pool_prefetch.argtypes = [P, C.c_int, P, C.c_int, P, C.POINTER(C.c_int)]
     L.edge0_pool_stats.argtypes = [P, C.POINTER(C.c_longlong), C.POINTER(C.c_longlong)]
+    L.edge0_pool_resident.argtypes = [P, C.c_int, P]
     L.edge0_pool_destroy.argtypes = [P]
     L.edge0_pool_destroy.restype = None
     L.edge0_state_init.argtypes = [C.POINTER(RouteState), P]
@@ -125,7 +127,7 @@ EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_
             "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
             "edge0_moe_int4_forward_noalloc", "edge0_pool_create", "edge0_pool_set_layer",
-            "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_destroy"]
+            "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_resident", "edge0_pool_destroy"]
 
 
 def status_string(code: int) -> str:
@@ -361,12 +363,15 @@ class ExpertPool:
             dm.stacks[l] = None
         torch.cuda.synchronize(dev)
 
-    def prefetch(self, st: "DecodeState", t: int, layers):
+    def prefetch(self, st: "DecodeState", t: int, layers, source: str = "prediction"):
         """After step t has completed: make resident, per layer in `layers`, the
         experts its prediction for step t + 1 names (union over the batch), on the
-        copy stream; the layer's next decode waits for its copies.  Returns the
-        number of experts copied."""
-        pred = st.pred_ids[t & 1].cpu()
+        copy stream; the layer's next decode waits for its copies.  With
+        source="executed", the experts step t ran instead (least-recently-used
+        caching without a prediction).  Returns the number of experts copied."""
+        if source not in ("prediction", "executed"):
+            raise ValueError(source)
+        pred = (st.pred_ids if source == "prediction" else st.exec_ids)[t & 1].cpu()
         total = 0
         for l in layers:
             ids = torch.unique(pred[l]).to(torch.int32).contiguous()
@@ -383,6 +388,12 @@ class ExpertPool:
         hits, copies = C.c_longlong(0), C.c_longlong(0)
         _check(lib().edge0_pool_stats(self.pool, C.byref(hits), C.byref(copies)), "edge0_pool_stats")
         return hits.value, copies.value
+
+    def resident(self, l: int) -> np.ndarray:
+        """The planner's map of layer l: slot of each expert, -1 for the host tier."""
+        out = np.empty(self.dm.cfg.E, dtype=np.int32)
+        _check(lib().edge0_pool_resident(self.pool, l, C.c_void_p(out.ctypes.data)), "edge0_pool_resident")
+        return out
 
     def __del__(self):
         if getattr(self, "pool", None):

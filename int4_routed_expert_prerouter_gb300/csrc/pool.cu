@@ -148,6 +148,12 @@ extern "C" int edge0_pool_prefetch(edge0_pool* P, int l, const int32_t* ids, int
     return EDGE0_OK;
 }
 
+extern "C" int edge0_pool_resident(const edge0_pool* P, int l, int32_t* slot_of) {
+    if (!P || l < 0 || l >= P->L || !slot_of) return EDGE0_EINVAL;
+    for (int e = 0; e < P->E; ++e) slot_of[e] = P->layers[l].slot_of[e];
+    return EDGE0_OK;
+}
+
 extern "C" int edge0_pool_stats(const edge0_pool* P, long long* hits, long long* copies) {
     if (!P) return EDGE0_EINVAL;
     if (hits) *hits = P->hits;

@@ -37,6 +37,11 @@ class Pool:
         assert self.lib.edge0_pool_stats(self.p, C.byref(h), C.byref(c)) == 0
         return h.value, c.value
 
+    def resident(self, l):
+        out = np.zeros(self.E, dtype=np.int32)
+        assert self.lib.edge0_pool_resident(self.p, l, out.ctypes.data_as(C.c_void_p)) == 0
+        return out.tolist()
+
     def __del__(self):
         self.lib.edge0_pool_destroy(self.p)
 
@@ -88,10 +93,20 @@ def test_pool_matches_a_plain_lru_restatement(lib, E, n_slots):
     reqs = [rng.choices(range(E), weights=w, k=rng.randint(1, 3 * n_slots // 2)) for _ in range(60)]
     p = Pool(lib, 2, E, n_slots)
     ref = _reference(n_slots, reqs)
+    slot_of = [-1] * E
     for req, exp in zip(reqs, ref):
         rc, got = p.plan(1, req)
         assert rc == 0 and got == exp
+        # the resident map follows the copies: a copied expert evicts the slot's
+        # previous one
+        for e, sl in got:
+            for e2 in range(E):
+                if slot_of[e2] == sl:
+                    slot_of[e2] = -1
+            slot_of[e] = sl
+        assert p.resident(1) == slot_of
     # layer 0 untouched by layer 1's plans
+    assert p.resident(0) == [-1] * E
     assert p.plan(0, [0])[1] == [(0, 0)]
 
 

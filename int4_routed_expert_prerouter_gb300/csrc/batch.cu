@@ -10,8 +10,8 @@
 //   k_dispatch  tokens grouped by expert: the active experts in id order, each
 //               with its token list and routing weights
 //   k_dense     LoRA A_gate x, A_up x (shared expert)
-//   k_gu        gate/up of every active expert and the shared expert, once per
-//               expert for all of its tokens -> act = silu(g) up (fp32)
+//   k_gu        gate/up of every active expert and the shared expert over
+//               blocks of up to 32 of its tokens -> act = silu(g) up (fp32)
 //   k_down      down of the same -> y += w act (fp32 reductions)
 //   k_lora_vd   y += (alpha/r) B_down (A_down act_shared)
 // and after the last layer h = fp16(h + y), then every head of the step (one
@@ -22,8 +22,9 @@
 // The weights are the same packed layouts as the persistent engine's (int4
 // nibbles enter mma.sync as fp16 subnormals q 2^-24, the epilogue rescales by
 // s 2^24 and adds b times the group sum of the input; fp32 inputs enter as a
-// hi + lo pair of fp16).  An expert's weights are read once per step however
-// many tokens it serves: the contraction becomes a skinny GEMM over its tokens.
+// hi + lo pair of fp16).  An expert's weights are read once per block of its
+// tokens (32 for gate/up, 16 for down), not once per token: the contraction
+// becomes a skinny GEMM over the block.
 #include <string.h>
 
 #include "internal.cuh"

@@ -225,7 +225,11 @@ def run_gpu(args, rank, world):
         t += 1
         st.set_trace(False)
         tr = st.read_trace()
-        print_trace(tr, torch.cuda.get_device_properties(dev).multi_processor_count)
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        print_trace(tr, nsm)
+        own = [l for l in range(cfg.L) if l not in cfg.prerouted]
+        pre = list(cfg.prerouted)
+        print_trace_roles(tr, nsm, cfg, ([pre[len(pre) // 2]] if pre else []) + (own[-1:] if own else []))
         if args.trace_file:
             np.savez_compressed(args.trace_file, consumer=tr[0].numpy(), producer=tr[1].numpy())
     # device-resident timed region: one event pair per launch for the kernel
@@ -612,6 +616,51 @@ def print_trace(tr, nct, sm_mhz=2070.0):
             for i, n in enumerate(fn)) + " us (mean/max over CTAs)")
     sys.stderr.write("\n".join(lines) + "\n")
     sys.stderr.write("total (mean over CTAs): " + " ".join(f"{n} {a:.1f}" for n, a in zip(names, tot)) + " us\n")
+
+
+def _shared_pairs(P, n_sh, n_rt, lora):
+    """How many CTA pairs own shared-expert rows: a restatement of the engine's
+    cost model, used here only to label the trace's CTAs by role."""
+    if n_sh <= 0:
+        return 0
+    if n_rt <= 0:
+        return P
+    best, pick = 1 << 30, 1
+    for ps in range(1, P):
+        cs = -(-n_sh // ps) * 24 + (20 if lora else 0)
+        cr = -(-n_rt // (P - ps)) * 24
+        if max(cs, cr) <= best:
+            best, pick = max(cs, cr), ps
+    return pick
+
+
+def print_trace_roles(tr, nct, cfg, layers, sm_mhz=2070.0):
+    """For the given layers, the mean duration (SM cycle counter) of each phase
+    from the grid barrier seen to the next arrival, separately for the CTAs of
+    the pairs that own shared-expert rows (and carry the LoRA) and the routed
+    pairs; own-routed layers also split their router phase."""
+    cons = tr[0]
+    P = nct // 2
+    ps = _shared_pairs(P, cfg.Is // 8, min(cfg.B * cfg.K, cfg.E) * (cfg.I // 8), True)
+    seq = ((24, "bar seen"), (1, "x"), (40, "router units"), (42, "router barrier"), (2, "routing"),
+           (8, "first item"), (3, "gate/up"), (4, "xchg"), (10, "act wait"), (11, "act rows"), (5, "act"),
+           (9, "down wait"), (12, "down rows"), (6, "arrive"))
+    lines = []
+    for l in layers:
+        for role, ctas in (("shared pairs", range(0, 2 * ps)), ("routed pairs", range(2 * ps, nct))):
+            dur = {}
+            for c in ctas:
+                ev = {}
+                for tag, tm, cy in cons[c].tolist():
+                    if tm != 0:
+                        ev[tag] = cy
+                pts = [(name, ev[(l << 8) | k]) for k, name in seq if (l << 8) | k in ev]
+                for (_, a), (name, b) in zip(pts, pts[1:]):
+                    dur.setdefault(name, []).append((b - a) / sm_mhz)
+            if dur:
+                lines.append(f"layer {l:2d} {role} ({len(ctas)} CTAs): " +
+                             " ".join(f"{n} {statistics.mean(v):.2f}" for n, v in dur.items()) + " us")
+    sys.stderr.write("\n".join(lines) + "\n")
 
 
 def _host_layers(model, n):

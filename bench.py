@@ -64,7 +64,7 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-ENGINE_SOURCES = ("int4_routed_expert_prerouter_gb300/csrc/engine.cu",
+ENGINE_SOURCES = ("int4_routed_expert_prerouter_gb300/csrc/decode1.cu",
                   "int4_routed_expert_prerouter_gb300/csrc/internal.cuh",
                   "int4_routed_expert_prerouter_gb300/csrc/common.cuh",
                   "include/edge0.h")
@@ -314,7 +314,7 @@ def run_gpu(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if traffic is None else int(traffic),
-                     "kernel": "edge0::engine_kernel (one launch per decode step)",
+                     "kernel": "edge0::d1::decode1_kernel (one launch per decode step)",
                      "algorithmic_bytes_per_launch": bytes_tok,
                      "mean_launch_us": round(mean_kern_s * 1e6, 2),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},

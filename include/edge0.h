@@ -164,6 +164,14 @@ typedef struct {
     int32_t* exec_ids;
     void* workspace;
     size_t workspace_bytes;
+    /* Optional records of a batch-1 decode call (B == 1; NULL: not recorded;
+     * ignored for B > 1).  For checking a whole decode step against a reference
+     * layer by layer, and for diagnosis.
+     *   record_h      fp16 [L][d]: row l = the output h of the call's layer l;
+     *   record_logits fp32 [L][E]: row l = the logits of the head owned by the
+     *                 call's layer l (rows of layers without a head untouched). */
+    uint16_t* record_h;
+    float* record_logits;
 } edge0_route_state;
 
 /* ---- packing (device -> device, enqueued on stream) ---- */
@@ -197,8 +205,17 @@ size_t edge0_decode_workspace_bytes(int L, int B, int d, int E, int K, int I, in
 /* zero pred/exec/workspace; must precede the first decode call on a state */
 int edge0_state_init(edge0_route_state* st, cudaStream_t stream);
 /* HOST call: synchronises `stream`, returns the kernels' recorded status (EDGE0_OK,
- * EDGE0_ETIMEOUT) in *status and clears it. */
+ * EDGE0_ETIMEOUT, EDGE0_EINVAL for a routing id outside [0, E) in the state,
+ * EDGE0_EUNSUPPORTED for a launch without its cluster shape) in *status.  After
+ * a non-zero status the state is re-initialised as by edge0_state_init (a launch
+ * that gave up leaves its accumulators part-way), which also resets the wait
+ * limit. */
 int edge0_state_error(const edge0_route_state* st, cudaStream_t stream, int* status);
+/* HOST call (synchronises `stream`): the limit, in nanoseconds, of every bounded
+ * wait of the persistent kernels on this state (0: the default of 2 s).  A wait
+ * that runs out records EDGE0_ETIMEOUT, every CTA of the launch leaves, and the
+ * next edge0_state_error reports it. */
+int edge0_state_set_wait_limit(edge0_route_state* st, unsigned long long wait_ns, cudaStream_t stream);
 
 /* ---- the four operations of the path ---- */
 
@@ -240,13 +257,18 @@ int edge0_decode_layer(const edge0_layer_desc* layer, uint16_t* h_inout, edge0_r
                        int B, int step, cudaStream_t stream);
 
 /* All L layers of one decode step (same semantics as L successive
- * edge0_decode_layer calls).  B <= EDGE0_MAX_BATCH: one persistent launch;
+ * edge0_decode_layer calls).  B == 1: one launch of the batch-1 kernel when the
+ * shapes are within its limits (d <= 2048, d % 128 == 0, every layer with the
+ * same shared-expert / LoRA parts, no slot table), else of the persistent
+ * engine; B <= EDGE0_MAX_BATCH: one persistent launch;
  * EDGE0_MAX_BATCH < B <= EDGE0_MAX_BATCHED: the batched path, a sequence of
  * kernels per layer in which every active expert's weights are read once for
  * all of its tokens, then every head of the step; it needs step >= 0 and a
  * workspace of edge0_decode_workspace_bytes. */
 int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
                       edge0_route_state* st, int B, int step, cudaStream_t stream);
+/* Calls on one state step through the step parities in order (step, step + 1,
+ * ...): a call clears the accumulators of the other parity for the next one. */
 
 /* ---- expert pool with a host tier [S3.1 "SSD Streaming Expert Layers", S3.2
  * "Motivation", S5.3]: n_slots device slots per layer in front of every

@@ -72,7 +72,7 @@ class LayerDesc(C.Structure):
 class RouteState(C.Structure):
     _fields_ = [("L", C.c_int), ("B", C.c_int), ("K", C.c_int),
                 ("pred_ids", P), ("pred_w", P), ("exec_ids", P), ("workspace", P),
-                ("workspace_bytes", C.c_size_t)]
+                ("workspace_bytes", C.c_size_t), ("record_h", P), ("record_logits", P)]
 
 
 def _declare(L):
@@ -103,6 +103,7 @@ def _declare(L):
     L.edge0_pool_destroy.restype = None
     L.edge0_state_init.argtypes = [C.POINTER(RouteState), P]
     L.edge0_state_error.argtypes = [C.POINTER(RouteState), P, C.POINTER(C.c_int)]
+    L.edge0_state_set_wait_limit.argtypes = [C.POINTER(RouteState), C.c_ulonglong, P]
     L.edge0_prerouter_topk.argtypes = [C.POINTER(HeadDesc), P, P, P, C.c_int, P, P, P, P,
                                        C.c_size_t, P]
     L.edge0_moe_int4_forward.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P, C.c_size_t, P]
@@ -116,7 +117,7 @@ def _declare(L):
                  "edge0_pack_f16_kmajor", "edge0_pack_cols_T", "edge0_state_init",
                  "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
                  "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
-                 "edge0_moe_int4_forward_noalloc"):
+                 "edge0_moe_int4_forward_noalloc", "edge0_state_set_wait_limit"):
         getattr(L, name).restype = C.c_int
 
 
@@ -124,7 +125,7 @@ EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_
             "edge0_q4_down_packed_bytes", "edge0_pack_q4_down", "edge0_f16_packed_bytes",
             "edge0_pack_f16", "edge0_pack_f16_kmajor", "edge0_pack_cols_T",
             "edge0_workspace_bytes", "edge0_decode_workspace_bytes", "edge0_state_init",
-            "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
+            "edge0_state_error", "edge0_state_set_wait_limit", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
             "edge0_moe_int4_forward_noalloc", "edge0_pool_create", "edge0_pool_set_layer",
             "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_resident", "edge0_pool_destroy"]
@@ -283,6 +284,8 @@ class DecodeState:
         B = cfg.B if B is None else B
         dev = torch.device(device)
         self.B = B
+        self.d, self.E = cfg.d, cfg.E
+        self.rec_h = self.rec_logits = None
         self.pred_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
         self.pred_w = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.float32, device=dev)
         self.exec_ids = torch.zeros(2, cfg.L, B, cfg.K, dtype=torch.int32, device=dev)
@@ -290,8 +293,32 @@ class DecodeState:
         assert nbytes > 0, f"no decode path for B = {B}"
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         self.st = RouteState(cfg.L, B, cfg.K, _ptr(self.pred_ids), _ptr(self.pred_w),
-                             _ptr(self.exec_ids), _ptr(self.workspace), nbytes)
+                             _ptr(self.exec_ids), _ptr(self.workspace), nbytes, None, None)
         _check(lib().edge0_state_init(C.byref(self.st), _stream(stream)), "edge0_state_init")
+
+    def record(self, on=True):
+        """Batch-1 calls record each layer's output h ([L, d] fp16) and each head's
+        logits ([L, E] fp32, at the owner layer's row) into self.rec_h /
+        self.rec_logits (None: off)."""
+        dev = self.workspace.device
+        if on:
+            self.rec_h = torch.zeros(self.st.L, self.d, dtype=torch.float16, device=dev)
+            self.rec_logits = torch.full((self.st.L, self.E), float("nan"), dtype=torch.float32, device=dev)
+            self.st.record_h, self.st.record_logits = _ptr(self.rec_h), _ptr(self.rec_logits)
+        else:
+            self.rec_h = self.rec_logits = None
+            self.st.record_h = self.st.record_logits = None
+
+    def set_wait_limit(self, wait_ns, stream=None):
+        _check(lib().edge0_state_set_wait_limit(C.byref(self.st), int(wait_ns), _stream(stream)),
+               "edge0_state_set_wait_limit")
+
+    def hold_first_barrier(self, n):
+        """Test hook (workspace header field `hold`): the next launch's first grid
+        barrier waits for n arrivals beyond the grid, so it cannot complete."""
+        torch.cuda.synchronize(self.workspace.device)
+        self.workspace[28:32].copy_(torch.tensor([int(n)], dtype=torch.int32).view(torch.uint8))
+        torch.cuda.synchronize(self.workspace.device)
 
     TRACE_CTAS, TRACE_SLOTS, TRACE_PRODUCER = 160, 4096, 3072
 

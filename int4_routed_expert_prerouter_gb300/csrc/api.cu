@@ -1,5 +1,6 @@
 // C ABI entry points of libedge0: argument validation on the host, translation
 // of the public descriptors into the engine's kernel parameter block, launch.
+#include <stddef.h>
 #include <string.h>
 
 #include "internal.cuh"
@@ -185,8 +186,17 @@ int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_rout
     p->exec_ids = st->exec_ids;
     p->Ls = st->L;
     p->ws = (char*)st->workspace;
+    p->ws_bytes = (long long)st->workspace_bytes;
+    if (B == 1) {
+        p->dbg_h = (__half*)st->record_h;
+        p->dbg_logits = st->record_logits;
+    }
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) rc = fill_layer(layers[l], D, st->L, p->layers[l]);
-    if (rc == EDGE0_OK) rc = batched ? batch_decode(*p, stream) : engine_launch(*p, stream);
+    if (rc == EDGE0_OK) {
+        if (batched) rc = batch_decode(*p, stream);
+        else if (B == 1 && decode1_check(*p) == EDGE0_OK) rc = decode1_launch(*p, stream);
+        else rc = engine_launch(*p, stream);
+    }
     delete p;
     return rc;
 }
@@ -204,14 +214,24 @@ extern "C" const char* edge0_status_string(int status) {
     }
 }
 
+// one sequence: room for the batch-1 kernel's layout too
+static long long persistent_ws_bytes(int L, int B, int d, int E) {
+    long long n = ws_layout(L, B, d, E).total;
+    if (B == 1) {
+        const long long n1 = decode1_ws_bytes(L, d, E);
+        if (n1 > n) n = n1;
+    }
+    return n;
+}
+
 extern "C" size_t edge0_workspace_bytes(int L, int B, int d, int E) {
     if (L <= 0 || B <= 0 || d <= 0 || E <= 0) return 0;
-    return (size_t)ws_layout(L, B, d, E).total;
+    return (size_t)persistent_ws_bytes(L, B, d, E);
 }
 
 extern "C" size_t edge0_decode_workspace_bytes(int L, int B, int d, int E, int K, int I, int Is, int H) {
     if (L <= 0 || B <= 0 || d <= 0 || E <= 0 || K <= 0 || I <= 0 || Is <= 0 || H <= 0) return 0;
-    if (B <= EDGE0_MAX_BATCH) return (size_t)ws_layout(L, B, d, E).total;
+    if (B <= EDGE0_MAX_BATCH) return (size_t)persistent_ws_bytes(L, B, d, E);
     if (B > EDGE0_MAX_BATCHED) return 0;
     return (size_t)batch_ws_layout(L, B, d, E, K, I > Is ? I : Is, H).total;
 }
@@ -236,15 +256,21 @@ extern "C" int edge0_state_error(const edge0_route_state* st, cudaStream_t strea
         return EDGE0_ECUDA;
     *status = h.error;
     if (h.error || h.abort) {
-        // clear the error; the barrier counter is re-aligned by the next launch's base
-        // computation only when every CTA left through the same barrier, so reset it too
-        WsHeader z = h;
-        z.error = 0;
-        z.abort = 0;
-        z.barrier = 0;
-        if (cudaMemcpy(st->workspace, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess)
-            return EDGE0_ECUDA;
+        // a launch that gave up leaves its accumulators, counters and barrier
+        // count part-way: the whole state starts again from zero
+        edge0_route_state s2 = *st;
+        if (edge0_state_init(&s2, stream) != EDGE0_OK) return EDGE0_ECUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return EDGE0_ECUDA;
     }
+    return EDGE0_OK;
+}
+
+extern "C" int edge0_state_set_wait_limit(edge0_route_state* st, unsigned long long wait_ns,
+                                          cudaStream_t stream) {
+    if (!st || !st->workspace || st->workspace_bytes < sizeof(WsHeader)) return EDGE0_EINVAL;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return EDGE0_ECUDA;
+    char* dst = (char*)st->workspace + offsetof(WsHeader, wait_ns);
+    if (cudaMemcpy(dst, &wait_ns, sizeof(wait_ns), cudaMemcpyHostToDevice) != cudaSuccess) return EDGE0_ECUDA;
     return EDGE0_OK;
 }
 

@@ -50,7 +50,6 @@ constexpr int kMaxChunks = 4;      // 4-element chunks of [B, d] per consumer th
 constexpr int kVWarp = 15;         // consumer warp that forms the LoRA v of a CTA with shared rows
 constexpr int kMaxD = 2048;
 constexpr int kMinRing = 2 * kItemMax;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;   // bounded waits: 2 s
 
 // Copy items.  Unit items (router, gate/up, LoRA A, fc1, linear_init) copy a run
 // of n consecutive units of the CTA's half of the input groups, from unit b of
@@ -430,6 +429,7 @@ __host__ __device__ __noinline__ bool build_flush_items(const Prog& p, int hl, i
 struct Ctl {
     int trace, tslot, abort, step, cdone, issued, last, ptslot;
     unsigned long long bar_seen;   // grid-barrier count right after this CTA's last arrival
+    unsigned long long tmo;        // limit of every bounded wait (ns)
 };
 constexpr int kTraceProducer = 3072;   // first trace word of the producer's stamps
 
@@ -536,7 +536,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 63) {
             if (should_abort()) return false;
-            if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); return false; }
+            if (now_ns() - t0 > ctx().ctl->tmo) { raise_error(EDGE0_ETIMEOUT); return false; }
         }
     }
 }
@@ -554,7 +554,7 @@ __device__ __noinline__ bool wait_flag(volatile int* flag, int want) {
         __nanosleep(32);
         if ((it & 63) == 63) {
             if (should_abort()) return false;
-            if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); return false; }
+            if (now_ns() - t0 > ctx().ctl->tmo) { raise_error(EDGE0_ETIMEOUT); return false; }
         }
     }
     return true;
@@ -928,7 +928,7 @@ __device__ __noinline__ bool bar_wait(unsigned long long& target) {
             for (unsigned it = 0; ld_acquire_u64(&c.hdr->barrier) < target; ++it) {
                 if ((it & 15) == 15) {
                     if (should_abort()) { *(volatile int*)&c.ctl->abort = 1; break; }
-                    if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); break; }
+                    if (now_ns() - t0 > ctx().ctl->tmo) { raise_error(EDGE0_ETIMEOUT); break; }
                 }
             }
         }
@@ -1238,7 +1238,7 @@ __device__ __noinline__ bool wait_count(const unsigned* cnt, unsigned want) {
     for (unsigned it = 0; ld_acquire_u32(cnt) < want; ++it) {
         if ((it & 15) == 15) {
             if (should_abort()) return false;
-            if (now_ns() - t0 > kTimeoutNs) { raise_error(EDGE0_ETIMEOUT); return false; }
+            if (now_ns() - t0 > ctx().ctl->tmo) { raise_error(EDGE0_ETIMEOUT); return false; }
         }
     }
     return true;
@@ -1994,6 +1994,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads,
         ctl->bar_seen = 0;
         ctl->step = p.step >= 0 ? p.step : ld_volatile_s32(&c.hdr->step);
         ctl->trace = c.cta < kTraceCtas ? ld_volatile_s32(&c.hdr->trace) : 0;
+        const unsigned long long wn = ld_relaxed_u64(&c.hdr->wait_ns);
+        ctl->tmo = wn ? wn : kDefaultWaitNs;
         ctl->tslot = 0;
         ctl->ptslot = kTraceProducer;
         for (int s = 0; s < kSlots; ++s) {

@@ -106,18 +106,28 @@ struct Prog {
     int hr_max, q_max;        // most half-row tiles / act quarters one CTA pair owns
     int ring_bytes;           // shared-memory ring of streamed weights
     int ft;                   // most head tasks in one table of the head flush
+    // batch-1 decode kernel (decode1.cu), filled by decode1_check
+    int pairs1[4];            // CTA pairs: all, routed, shared, LoRA
+    int ring1;                // bytes of its shared-memory ring
+    long long ws_bytes;       // workspace bytes (the trace area is at its end)
+    __half* dbg_h;            // [L][d] or null: each layer's output h (batch 1)
+    float* dbg_logits;        // [L][E] or null: each head's logits, at its owner layer's row
     LayerP layers[EDGE0_MAX_LAYERS];
 };
 
 // Workspace header (first 256 bytes)
 struct WsHeader {
     unsigned long long barrier;   // monotonically increasing arrival counter
-    unsigned int spare;
+    unsigned int serial;          // launches of the batch-1 kernel on this workspace
     int step;                     // auto step counter
     int error;                    // EDGE0_* status recorded by a kernel
     int abort;                    // set with error: every wait gives up
     int trace;                    // non-zero: record phase timestamps in the trace area
+    int hold;                     // test hook: arrivals the first grid barrier of a launch
+                                  // waits for beyond the grid (> 0: it cannot complete)
+    unsigned long long wait_ns;   // limit of every bounded wait (0: kDefaultWaitNs)
 };
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
 constexpr int kWsHeaderBytes = 256;
 // trace area (at the end of the workspace): per CTA kTraceSlots u64
 constexpr int kTraceCtas = 160;
@@ -249,6 +259,25 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rb
         ::"r"(raddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
         : "memory");
 }
+// 4-byte store into another CTA's shared memory that completes 4 bytes on its mbarrier
+__device__ __forceinline__ void st_async_b32(uint32_t raddr, float v, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n"
+                 ::"r"(raddr), "r"(__float_as_uint(v)), "r"(rbar)
+                 : "memory");
+}
+// generic-proxy accesses of shared memory ordered before later bulk copies into it
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+// single-copy-atomic 64-bit global accesses at GPU scope (value and tag travel together)
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" :::
                      "memory");
@@ -311,6 +340,14 @@ __device__ __forceinline__ float warp_sum(float s) {
 constexpr float kLoScale = 2048.0f;
 constexpr float kLoInv = 1.0f / 2048.0f;
 constexpr float kTwo24 = 16777216.0f;   // int4 nibbles enter the tensor cores as q * 2^-24
+
+// batch-1 decode kernel (decode1.cu): one launch per decode step of B = 1
+// workspace bytes it needs for Ls state rows (0 if the shapes exceed its limits)
+long long decode1_ws_bytes(int Ls, int d, int E);
+// fills p's batch-1 fields for the current device and checks that the kernel
+// takes the call (EDGE0_OK) or not (EDGE0_EUNSUPPORTED: use the engine)
+int decode1_check(Prog& p);
+int decode1_launch(Prog& p, cudaStream_t stream);
 
 // engine (engine.cu)
 __global__ void engine_kernel(const __grid_constant__ Prog prog);

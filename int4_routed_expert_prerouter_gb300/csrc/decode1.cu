@@ -53,8 +53,8 @@ constexpr int kCT = kCW * 32;            // consumer threads
 constexpr int kT1 = kCT + 32;            // + the producer warp
 constexpr int kMaxHr1 = 8;               // hr of one pair
 constexpr int kMaxSeg1 = 3;              // expert runs of one pair
-constexpr int kMaxSig = 8;               // 16-row act steps of one pair
-constexpr int kMaxPc = 16;               // copies of one block
+constexpr int kMaxSig = 9;               // 16-row act steps of one pair (+ the last slot: LoRA v)
+constexpr int kMaxPc = 24;               // copies of one block
 constexpr int kMaxParts = 8;             // (expert run, group) parts of a pair's down block
 constexpr int kBlocks = 16;              // block barriers
 constexpr int kPieceMax = 32768;         // bytes of one bulk copy
@@ -63,6 +63,7 @@ constexpr int kMaxG1 = kMaxD1 / kGroup;  // groups of d
 constexpr int kMaxTw = kMaxD1 / 2 / kRowTile / kCW;   // down row tiles of one warp
 constexpr int kMsg = kMaxHr1 * 16;       // partial sums a pair exchanges
 constexpr int kMaxK1 = EDGE0_MAX_K;
+constexpr int kNY = 1;                   // copies of each layer's y: pair p adds into copy p % kNY
 
 __host__ __device__ inline void split1(int n, int parts, int i, int* a, int* b) {
     *a = (int)((long long)n * i / parts);
@@ -166,7 +167,8 @@ __host__ inline int choose_pairs(Shape1& S) {
 // rows B_gate, B_up, A_down^T of the pair's act rows and B_down of this CTA's
 // output half); one block per head-flush task.
 enum PieceKind1 : int {
-    K1_ROUTER = 0, K1_GU, K1_DOWN, K1_LA, K1_LU, K1_BG, K1_BU, K1_ADT, K1_BD, K1_FC1, K1_FC2, K1_LINIT
+    K1_ROUTER = 0, K1_GU, K1_DOWN, K1_LA, K1_LU, K1_BG, K1_BU, K1_ADT, K1_BD, K1_FC1, K1_FC2, K1_LINIT,
+    K1_OHF, K1_OHL
 };
 struct Piece1 {
     int kind, seg;
@@ -221,12 +223,10 @@ __host__ __device__ inline bool layout1(const Shape1& S, const Plan1& p, int ran
                         (long long)rank * (S.E / kRowTile) * ng0 * kF16Unit + (long long)p.ru0 * kF16Unit,
                         (long long)(p.ru1 - p.ru0) * kF16Unit);
     if (p.role == R1_LORA) {
-        // LoRA A_gate, A_up (packed fp16 [r x d], one row tile): this CTA's half
-        const long long half0 = (long long)ng0 * kF16Unit;
-        L.la = L.b1.bytes;
-        ok &= add_piece(L.b1, K1_LA, 0, rank * half0, (long long)ngh * kF16Unit);
-        L.lu = L.b1.bytes;
-        ok &= add_piece(L.b1, K1_LU, 0, rank * half0, (long long)ngh * kF16Unit);
+        // LoRA A (packed fp16 [r x d], one row tile: its two halves back to back
+        // are the row tile's groups in order): rank 0 A_gate, rank 1 A_up, all of d
+        L.la = 0;
+        ok &= add_piece(L.b1, rank ? K1_LU : K1_LA, 0, 0, (long long)ng * kF16Unit);
         return ok;
     }
     // P1: gate/up units [hr][group of the half] of each run, back to back
@@ -252,7 +252,7 @@ __host__ __device__ inline bool layout1(const Shape1& S, const Plan1& p, int ran
         const int sa = sg.hr0 / 2, sb = (sg.hr1 - 1) / 2;
         const int sig0 = L.nsig;
         for (int st = sa; st <= sb; ++st) {
-            if (L.nsig >= kMaxSig) return false;
+            if (L.nsig >= kMaxSig - 1) return false;
             L.sig_seg[L.nsig] = s;
             L.sig_step[L.nsig] = st;
             ++L.nsig;
@@ -296,41 +296,100 @@ __host__ __device__ inline bool layout1(const Shape1& S, const Plan1& p, int ran
     return ok;
 }
 
-// head-flush task j of a head: fc1 row tile j (j < H/16) with its fc2 column
-// block, else linear_init row tile j - H/16; dense parts over all of d
-__host__ __device__ inline bool flush_block(const Shape1& S, int j, Block1& B) {
-    B.n = B.bytes = 0;
+// Head-flush task j of a head: fc1 row tile j (j < H/16) with its fc2 column
+// block, else linear_init row tile j - H/16, dense parts over all of d; and the
+// 16 entries of the row tile in each of the n2 one-hot columns the head's
+// features select (rows of the transposed columns, 32 bytes each: ids[k2] is
+// column e for executed expert e, E + e for previous expert e).  Two blocks:
+//   half 0: the row tile's groups of the first half of d;
+//   half 1: the groups of the second half, then (fc1) the fc2 block, then the
+//           one-hot rows.
+// flush_piece(., half, i, ...) is copy i of a block; false past its last.
+__host__ __device__ inline bool flush_piece(const Shape1& S, int j, int half, int i, const int* ids, int n2,
+                                            Piece1& pc) {
     const int ng = S.d / kGroup, ng0 = ng / 2, ng1 = ng - ng0, nH = S.H / kRowTile, nE = S.E / kRowTile;
-    bool ok = true;
-    if (j < nH) {
-        ok &= add_piece(B, K1_FC1, 0, (long long)j * ng0 * kF16Unit, (long long)ng0 * kF16Unit);
-        ok &= add_piece(B, K1_FC1, 0, (long long)nH * ng0 * kF16Unit + (long long)j * ng1 * kF16Unit,
-                        (long long)ng1 * kF16Unit);
-        ok &= add_piece(B, K1_FC2, 0, (long long)j * nE * kF16Step, (long long)nE * kF16Step);
-    } else {
-        j -= nH;
-        ok &= add_piece(B, K1_LINIT, 0, (long long)j * ng0 * kF16Unit, (long long)ng0 * kF16Unit);
-        ok &= add_piece(B, K1_LINIT, 0, (long long)nE * ng0 * kF16Unit + (long long)j * ng1 * kF16Unit,
-                        (long long)ng1 * kF16Unit);
+    const bool fc1 = j < nH;
+    const int jr = fc1 ? j : j - nH;
+    const int rows = fc1 ? nH : nE;   // row tiles of the dense matrix
+    pc.seg = 0;
+    if (half == 0) {
+        if (i != 0) return false;
+        pc.kind = fc1 ? K1_FC1 : K1_LINIT;
+        pc.src = (long long)jr * ng0 * kF16Unit;
+        pc.bytes = ng0 * kF16Unit;
+        pc.dst = 0;
+        return true;
     }
-    return ok;
+    int dst = 0;
+    if (i == 0) {
+        pc.kind = fc1 ? K1_FC1 : K1_LINIT;
+        pc.src = (long long)rows * ng0 * kF16Unit + (long long)jr * ng1 * kF16Unit;
+        pc.bytes = ng1 * kF16Unit;
+        pc.dst = 0;
+        return true;
+    }
+    dst = ng1 * kF16Unit;
+    if (fc1) {
+        if (i == 1) {
+            pc.kind = K1_FC2;
+            pc.src = (long long)jr * nE * kF16Step;
+            pc.bytes = nE * kF16Step;
+            pc.dst = dst;
+            return true;
+        }
+        dst += nE * kF16Step;
+        --i;
+    }
+    const int k2 = i - 1;
+    if (k2 >= n2) return false;
+    pc.kind = fc1 ? K1_OHF : K1_OHL;
+    pc.src = ((long long)(ids ? ids[k2] : 0) * (fc1 ? S.H : S.E) + 16LL * jr) * 2;
+    pc.bytes = 32;
+    pc.dst = dst + 32 * k2;
+    return true;
+}
+// the block as a copy list
+__host__ __device__ inline bool flush_block(const Shape1& S, int j, int half, Block1& B, const int* ids = nullptr,
+                                            int n2 = 0) {
+    B.n = B.bytes = 0;
+    Piece1 pc;
+    for (int i = 0; flush_piece(S, j, half, i, ids, n2, pc); ++i) {
+        if (B.n >= kMaxPc || pc.bytes > kPieceMax) return false;
+        B.pc[B.n++] = pc;
+        B.bytes = pc.dst + pc.bytes;
+    }
+    return true;
 }
 
-// ring placement shared by the producer and the consumers: a block starts at
-// `pos` unless it would cross the ring's end, then at the next lap
-__host__ __device__ inline long long place1(long long pos, int bytes, int ring, int* off) {
-    int o = (int)(pos % ring);
-    if (o + bytes > ring) {
-        pos += ring - o;
-        o = 0;
+// bytes of flush_block(S, j, half, ., ., n2), without building it
+__host__ __device__ inline int flush_bytes(const Shape1& S, int j, int half, int n2) {
+    const int ng = S.d / kGroup, ng0 = ng / 2;
+    if (half == 0) return ng0 * kF16Unit;
+    return (ng - ng0) * kF16Unit + (j < S.H / kRowTile ? (S.E / kRowTile) * kF16Step : 0) + n2 * 32;
+}
+
+// ring placement shared by the producer and the consumers: a block starts at the
+// ring offset `off` unless it would cross the ring's end, then at offset 0 of
+// the next lap; `pos` counts ring bytes passed (skipped tails included)
+struct Ring1 {
+    int pos, off;
+};
+__host__ __device__ inline int place1(Ring1& r, int bytes, int ring) {
+    if (r.off + bytes > ring) {
+        r.pos += ring - r.off;
+        r.off = 0;
     }
-    *off = o;
-    return pos;
+    const int at = r.off;
+    r.pos += bytes;
+    r.off += bytes;
+    if (r.off == ring) r.off = 0;
+    return at;
 }
 
 // --------------------------------------------------------------- workspace ----
 // After the header, per step parity p and state row s:
-//   y      [2][Ls][d]   fp32  layer output (vector reductions)
+//   y      [2][Ls][kNY][d] fp32  layer output (vector reductions; kNY copies spread
+//                                the reductions, their sum is the output)
 //   logr   [2][Ls][E]   fp32  own-router logits
 //   logh   [2][Ls][E]   fp32  head logits (row of the head's owner)
 //   lax    [2][Ls][32]  u64   A_gate x, A_up x as (fp32 bits, launch tag)
@@ -343,7 +402,7 @@ struct Ws1 {
 __host__ __device__ inline Ws1 ws1(int Ls, int d, int E) {
     Ws1 w;
     long long o = kWsHeaderBytes;
-    w.y = o;    o += 2LL * Ls * d * 4;
+    w.y = o;    o += 2LL * Ls * kNY * d * 4;
     w.logr = o; o += 2LL * Ls * E * 4;
     w.logh = o; o += 2LL * Ls * E * 4;
     w.lax = o;  o += 2LL * Ls * 32 * 8;
@@ -362,17 +421,17 @@ struct Sm1 {
     int topk;                             // flush: this CTA completed the current head
     int issued;                           // blocks issued by the producer
     int released_blocks;                  // blocks the consumers are done with
-    long long released;                   // ring position up to which blocks are free
+    int released;                         // ring position up to which blocks are free
     unsigned long long wait_ns;
     int trace, tslot, ptslot;
-    int fnpv;
+    int flush_after;                      // the head flush follows this layer (-1: no heads)
+    unsigned gu_warps;                    // consumer warps with gate/up (or LoRA A) partials
+    unsigned fl_warps;                    // consumer warps with head-flush dense partials
     // arrays: each 16-byte aligned (some are read and written as vectors)
     __align__(16) int route_ready[EDGE0_MAX_LAYERS];
     __align__(16) int ids[EDGE0_MAX_LAYERS][kMaxK1];
     __align__(16) float w[EDGE0_MAX_LAYERS][kMaxK1];
     __align__(16) int heads[EDGE0_MAX_LAYERS];
-    __align__(16) int fex[kMaxK1];
-    __align__(16) int fpv[kMaxK1];
     __align__(16) Shape1 S;
     __align__(16) Plan1 plan;
     __align__(16) Lay1 lay;
@@ -384,8 +443,6 @@ struct Sm1 {
     __align__(16) float mine[kMsg];
     __align__(16) float recv[kMsg];
     __align__(16) float actw[kMaxHr1 * 8];
-    __align__(16) float oh[2 * kMaxK1][16];
-    __align__(16) float yacc[kMaxD1 / 2];
     __align__(16) float part[kCW][kMsg];
     __align__(16) float logits[EDGE0_MAX_E];
     __align__(16) float rscr[2 * EDGE0_MAX_E];
@@ -394,7 +451,7 @@ struct Sm1 {
     __align__(16) uint2 af[kMaxSig * 8];  // [act step][lane < 8]: act hi (lanes 0-3), lo (4-7)
     __align__(16) uint2 gf[8];            // GELU(z) of a flush task, same form
 };
-static_assert(offsetof(Sm1, yacc) % 16 == 0 && offsetof(Sm1, h) % 16 == 0 && offsetof(Sm1, xf) % 16 == 0 &&
+static_assert(offsetof(Sm1, h) % 16 == 0 && offsetof(Sm1, xf) % 16 == 0 &&
                   offsetof(Sm1, part) % 16 == 0 && offsetof(Sm1, mine) % 16 == 0,
               "vector-accessed shared arrays are 16-byte aligned");
 constexpr int kSm1Bytes = (int)((sizeof(Sm1) + 127) / 128 * 128);
@@ -456,7 +513,29 @@ __device__ __noinline__ void stamp_slow1(const Prog& p, int tag, bool producer) 
     *slot += 3;
 }
 __device__ __forceinline__ void stamp1(const Prog& p, int tag) {
-    if (sm().trace && threadIdx.x == 0) stamp_slow1(p, tag, false);
+    Sm1& s = sm();
+    if (s.trace && threadIdx.x == 0 && s.tslot + 3 <= 3072) {
+        unsigned long long* tr = reinterpret_cast<unsigned long long*>(p.ws + p.ws_bytes - kTraceBytes) +
+                                 (long long)blockIdx.x * kTraceSlots + s.tslot;
+        long long c;
+        asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+        tr[0] = (unsigned long long)tag;
+        tr[1] = now1();
+        tr[2] = (unsigned long long)c;
+        s.tslot += 3;
+    }
+}
+
+// parity wait with CTA-scope acquire (the bulk copies into this CTA's ring)
+__device__ __forceinline__ bool mbar_try_wait_cta(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 // bounded wait on a block or exchange barrier phase; false on abort/timeout
@@ -475,19 +554,26 @@ __device__ __noinline__ bool mbar_wait1(WsHeader* hdr, uint64_t* bar, uint32_t p
     }
 }
 
-// grid barrier: thread 0 arrives after the caller's consumer barrier (all of
-// the CTA's global writes before it are ordered by the fence)
-__device__ __forceinline__ void grid_arrive1(WsHeader* hdr) {
+// Grid barriers.  Two counters: `barrier` counts layer-end arrivals (one per CTA
+// and layer), `barrier_r` router arrivals (one per CTA and layer that routes
+// itself).  Every CTA arrives at a layer's router barrier before its end
+// barrier and waits for the end barrier before the next layer, so neither
+// counter can reach a barrier's count while a CTA has yet to arrive at it (CTAs
+// that do not wait for the router barrier arrive at the end one right away; on
+// a shared counter their arrivals could complete the router barrier early).
+// thread 0 arrives after the caller's consumer barrier (all of the CTA's global
+// writes before it are ordered by the fence)
+__device__ __forceinline__ void grid_arrive1(unsigned long long* ctr) {
     if (threadIdx.x == 0) {
         __threadfence();
-        red_release_add_u64(&hdr->barrier, 1ull);
+        red_release_add_u64(ctr, 1ull);
     }
 }
 // thread 0 polls, then a consumer barrier; false on abort/timeout (uniform)
-__device__ __noinline__ bool grid_wait1(WsHeader* hdr, unsigned long long target) {
-    if (threadIdx.x == 0 && ld_acquire_u64(&hdr->barrier) < target) {
+__device__ __noinline__ bool grid_wait1(WsHeader* hdr, const unsigned long long* ctr, unsigned long long target) {
+    if (threadIdx.x == 0 && ld_acquire_u64(ctr) < target) {
         const unsigned long long t0 = now1();
-        for (unsigned it = 0; ld_acquire_u64(&hdr->barrier) < target; ++it) {
+        for (unsigned it = 0; ld_acquire_u64(ctr) < target; ++it) {
             if ((it & 15) == 15) {
                 if (gone1(hdr)) {
                     *(volatile int*)&sm().abort = 1;
@@ -541,32 +627,35 @@ __device__ const char* piece_src1(const Prog& p, const Piece1& pc, int l) {
         case K1_BD: return reinterpret_cast<const char*>(Ly.lora_Bd) + pc.src;
         case K1_FC1: return Ly.fc1 + pc.src;
         case K1_FC2: return Ly.fc2 + pc.src;
+        case K1_OHF: return reinterpret_cast<const char*>(Ly.fc1_oh) + pc.src;
+        case K1_OHL: return reinterpret_cast<const char*>(Ly.linit_oh) + pc.src;
         default: return Ly.linit + pc.src;
     }
 }
 
 struct Stream1 {
-    long long pos;
+    Ring1 r;
     int nb;
 };
+// one flush block (task j of head layer l, half h): as issue1, with copy i made
+// by lane i straight from flush_piece
+__device__ bool issue_flush1(const Prog& p, WsHeader* hdr, Stream1& q, int j, int h, const int* ids, int n2, int l,
+                             uint64_t pol, int tag);
 
 // the whole producer warp: place a block, wait for its room, arm its barrier,
 // issue its copies (one lane per copy)
-__device__ bool issue1(const Prog& p, WsHeader* hdr, Stream1& q, const Block1& B, int l, uint64_t pol) {
+__device__ bool issue1(const Prog& p, WsHeader* hdr, Stream1& q, const Block1& B, int l, uint64_t pol, int tag) {
     Sm1& s = sm();
     const int lane = threadIdx.x & 31;
     if (B.bytes == 0) return true;
-    int off;
-    const long long start = place1(q.pos, B.bytes, p.ring1, &off);
-    const long long end = start + B.bytes;
+    const int off = place1(q.r, B.bytes, p.ring1);
+    const int end = q.r.pos;
     int ok = 1;
     if (lane == 0) {
         const unsigned long long t0 = now1();
         for (unsigned it = 0;; ++it) {
-            const long long rel = *(volatile long long*)&s.released;
-            if (end - rel <= p.ring1 && q.nb - vload(&s.released_blocks) < kBlocks) break;
-            __nanosleep(64);
-            if ((it & 15) == 15) {
+            if (end - vload(&s.released) <= p.ring1 && q.nb - vload(&s.released_blocks) < kBlocks) break;
+            if ((it & 63) == 63) {
                 if (gone1(hdr)) { ok = 0; break; }
                 if (now1() - t0 > s.wait_ns) { fail1(hdr, EDGE0_ETIMEOUT); ok = 0; break; }
             }
@@ -582,29 +671,110 @@ __device__ bool issue1(const Prog& p, WsHeader* hdr, Stream1& q, const Block1& B
         const Piece1& pc = B.pc[i];
         bulk_g2s(ring() + off + pc.dst, piece_src1(p, pc, l), (uint32_t)pc.bytes, &s.full[q.nb % kBlocks], pol);
     }
-    q.pos = end;
     ++q.nb;
-    if (lane == 0) *(volatile int*)&s.issued = q.nb;
+    if (lane == 0) {
+        *(volatile int*)&s.issued = q.nb;
+        if (s.trace) stamp_slow1(p, tag, true);
+    }
     __syncwarp();
     return true;
 }
 
-__device__ void producer1(const Prog& p, WsHeader* hdr, int step) {
+__device__ bool issue_flush1(const Prog& p, WsHeader* hdr, Stream1& q, int j, int h, const int* ids, int n2, int l,
+                             uint64_t pol, int tag) {
+    Sm1& s = sm();
+    const int lane = threadIdx.x & 31;
+    const int bytes = flush_bytes(s.S, j, h, n2);
+    const int off = place1(q.r, bytes, p.ring1);
+    const int end = q.r.pos;
+    int ok = 1;
+    if (lane == 0) {
+        const unsigned long long t0 = now1();
+        for (unsigned it = 0;; ++it) {
+            if (end - vload(&s.released) <= p.ring1 && q.nb - vload(&s.released_blocks) < kBlocks) break;
+            if ((it & 63) == 63) {
+                if (gone1(hdr)) { ok = 0; break; }
+                if (now1() - t0 > s.wait_ns) { fail1(hdr, EDGE0_ETIMEOUT); ok = 0; break; }
+            }
+        }
+        if (ok) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&s.full[q.nb % kBlocks], (uint32_t)bytes);
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) return false;
+    Piece1 pc;
+    if (flush_piece(s.S, j, h, lane, ids, n2, pc))
+        bulk_g2s(ring() + off + pc.dst, piece_src1(p, pc, l), (uint32_t)pc.bytes, &s.full[q.nb % kBlocks], pol);
+    ++q.nb;
+    if (lane == 0) {
+        *(volatile int*)&s.issued = q.nb;
+        if (s.trace) stamp_slow1(p, tag, true);
+    }
+    __syncwarp();
+    return true;
+}
+
+// the head flush's blocks: a task's one-hot rows are gathered by the head layer's
+// executed (this step) and previous (last step) ids, read once the barrier that
+// ends that layer has passed
+__device__ bool produce_flush1(const Prog& p, WsHeader* hdr, Stream1& q, int step, int par, unsigned long long base,
+                               uint64_t pol) {
+    Sm1& s = sm();
+    const int lane = threadIdx.x & 31;
+    const int tph = p.H / kRowTile + p.E / kRowTile;
+    const int n2 = p.K + (step > 0 ? p.K : 0);
+    int cur = -1;
+    __shared__ int fids[2 * kMaxK1];
+    for (int t = s.plan.t0; t < s.plan.t1; ++t) {
+        const int l = s.heads[t / tph];
+        if (l != cur) {
+            const unsigned long long need = base + (unsigned long long)gridDim.x * ((unsigned long long)l + 1);
+            int ok = 1;
+            if (lane == 0 && ld_acquire_u64(&hdr->barrier) < need) {
+                const unsigned long long t0 = now1();
+                for (unsigned it = 0; ld_acquire_u64(&hdr->barrier) < need; ++it) {
+                    if ((it & 15) == 15) {
+                        if (gone1(hdr)) { ok = 0; break; }
+                        if (now1() - t0 > s.wait_ns) { fail1(hdr, EDGE0_ETIMEOUT); ok = 0; break; }
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+            const int sidx = p.layers[l].sidx;
+            if (lane < n2) {
+                const int k = lane < p.K ? lane : lane - p.K;
+                const int32_t* src = p.exec_ids + ((long long)((lane < p.K ? par : par ^ 1)) * p.Ls + sidx) * p.K;
+                int e = ld_volatile_s32(src + k);
+                e = e < 0 || e >= p.E ? 0 : e;
+                fids[lane] = lane < p.K ? e : p.E + e;
+            }
+            __syncwarp();
+            cur = l;
+        }
+        const int j = t % tph, tg = 0xF000 | (t - s.plan.t0);
+        if (!issue_flush1(p, hdr, q, j, 0, fids, n2, l, pol, tg)) return false;
+        if (!issue_flush1(p, hdr, q, j, 1, fids, n2, l, pol, tg)) return false;
+    }
+    return true;
+}
+
+__device__ void producer1(const Prog& p, WsHeader* hdr, int step, int par, unsigned long long base) {
     Sm1& s = sm();
     const int lane = threadIdx.x & 31;
     const uint64_t pol = policy_evict_first();
-    Stream1 q{0, 0};
+    Stream1 q{{0, 0}, 0};
     for (int l = 0; l < p.L; ++l) {
         const bool own = own_routed1(p, l, step);
-        if (own && !issue1(p, hdr, q, s.lay.b0, l, pol)) return;
+        if (own && !issue1(p, hdr, q, s.lay.b0, l, pol, (l << 8) | 0x80)) return;
         if (own && s.plan.role == R1_ROUTED && s.plan.nseg > 0) {
             // the routed weights of a layer that routes itself follow its routing
             int ok = 1;
             if (lane == 0) {
                 const unsigned long long t0 = now1();
                 for (unsigned it = 0; !vload(&s.route_ready[l]); ++it) {
-                    __nanosleep(32);
-                    if ((it & 15) == 15) {
+                    if ((it & 63) == 63) {
                         if (gone1(hdr)) { ok = 0; break; }
                         if (now1() - t0 > s.wait_ns) { fail1(hdr, EDGE0_ETIMEOUT); ok = 0; break; }
                     }
@@ -612,31 +782,28 @@ __device__ void producer1(const Prog& p, WsHeader* hdr, int step) {
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) return;
         }
-        if (!issue1(p, hdr, q, s.lay.b1, l, pol)) return;
-        if (!issue1(p, hdr, q, s.lay.b2, l, pol)) return;
-    }
-    const int tph = p.H / kRowTile + p.E / kRowTile;
-    for (int t = s.plan.t0; t < s.plan.t1; ++t) {
-        Block1 B;
-        flush_block(s.S, t % tph, B);
-        if (!issue1(p, hdr, q, B, s.heads[t / tph], pol)) return;
+        if (!issue1(p, hdr, q, s.lay.b1, l, pol, (l << 8) | 0x81)) return;
+        if (!issue1(p, hdr, q, s.lay.b2, l, pol, (l << 8) | 0x82)) return;
+        // the head flush runs right after the last layer that owns a head
+        if (l == s.flush_after && !produce_flush1(p, hdr, q, step, par, base, pol)) return;
     }
 }
 
 // ---------------------------------------------------------------- consumers ----
 struct Cons1 {
-    long long pos;             // ring position (same sequence as the producer's)
+    Ring1 r;                   // ring placement (same sequence as the producer's)
     int nb;                    // blocks taken
     int off;                   // ring offset of the current block
-    long long end;
+    int end;                   // ring position after it
 };
 // next block: its ring offset; waits for its data (every consumer thread)
 __device__ __forceinline__ bool take1(const Prog& p, WsHeader* hdr, Cons1& c, int bytes) {
-    const long long start = place1(c.pos, bytes, p.ring1, &c.off);
-    c.end = start + bytes;
-    c.pos = c.end;
+    c.off = place1(c.r, bytes, p.ring1);
+    c.end = c.r.pos;
     Sm1& s = sm();
-    const bool ok = mbar_wait1(hdr, &s.full[c.nb % kBlocks], (uint32_t)((c.nb / kBlocks) & 1));
+    uint64_t* bar = &s.full[c.nb % kBlocks];
+    const uint32_t par = (uint32_t)((c.nb / kBlocks) & 1);
+    const bool ok = mbar_try_wait_cta(bar, par) || mbar_wait1(hdr, bar, par);
     ++c.nb;
     return ok;
 }
@@ -644,7 +811,7 @@ __device__ __forceinline__ bool take1(const Prog& p, WsHeader* hdr, Cons1& c, in
 __device__ __forceinline__ void give1(const Cons1& c) {
     if (threadIdx.x == 0) {
         Sm1& s = sm();
-        *(volatile long long*)&s.released = c.end;
+        *(volatile int*)&s.released = c.end;
         *(volatile int*)&s.released_blocks = c.nb;
     }
 }
@@ -673,7 +840,12 @@ __device__ void build_x1(const Prog& p, int l, const __half* h_in, const float* 
                               : *reinterpret_cast<const uint2*>(&s.h[4 * tid]);
         __half2 h01 = *reinterpret_cast<const __half2*>(&hv.x), h23 = *reinterpret_cast<const __half2*>(&hv.y);
         if (y) {
-            const float4 yv = __ldcg(reinterpret_cast<const float4*>(y + 4 * tid));
+            float4 yv = __ldcg(reinterpret_cast<const float4*>(y + 4 * tid));
+#pragma unroll
+            for (int q = 1; q < kNY; ++q) {
+                const float4 u = __ldcg(reinterpret_cast<const float4*>(y + (long long)q * p.d + 4 * tid));
+                yv.x += u.x; yv.y += u.y; yv.z += u.z; yv.w += u.w;
+            }
             h01 = __floats2half2_rn(__low2float(h01) + yv.x, __high2float(h01) + yv.y);
             h23 = __floats2half2_rn(__low2float(h23) + yv.z, __high2float(h23) + yv.w);
         }
@@ -723,7 +895,7 @@ __device__ void build_x1(const Prog& p, int l, const __half* h_in, const float* 
 }
 
 // own-router units of this CTA: partial logits summed into logr
-__device__ void router_units1(const Prog& p, const char* blk, float* logr) {
+__device__ void router_units1(const Prog& p, const char* blk, float* logr, int xg0) {
     const Sm1& s = sm();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, g8 = lane >> 2;
     const int ngh = ngh1(p.d, cluster_ctarank());
@@ -731,7 +903,7 @@ __device__ void router_units1(const Prog& p, const char* blk, float* logr) {
         const int rt = u / ngh, g = u - rt * ngh;
         const char* unit = blk + (long long)(u - s.plan.ru0) * kF16Unit;
         uint4 xa, xb;
-        xfrag(s, g, lane, xa, xb);
+        xfrag(s, xg0 + g, lane, xa, xb);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t xbv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
@@ -794,16 +966,14 @@ __device__ void gateup1(const char* blk, int ngh, int n_hr) {
     }
 }
 
-// LoRA A_gate x and A_up x over this CTA's half (the LoRA pair): rows 0-15 of
-// A_gate then of A_up, partial sums into part (warp w takes units w, w + 16, ...)
-__device__ void lora_a1(const char* blk, int la, int lu, int ngh) {
+// LoRA A x of one matrix over all of d (the LoRA pair: rank 0 A_gate, rank 1
+// A_up): partial sums of its 16 rows into part (warp w takes groups w, w + 16, ...)
+__device__ void lora_a1(const char* blk, int ng) {
     Sm1& s = sm();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    bool any = false;
-    for (int u = wid; u < 2 * ngh; u += kCW) {
-        const int m = u >= ngh, g = u - m * ngh;
-        const char* unit = blk + (m ? lu : la) + (long long)g * kF16Unit;
+    float a0 = 0.f, a1 = 0.f;
+    for (int g = wid; g < ng; g += kCW) {
+        const char* unit = blk + (long long)g * kF16Unit;
         uint4 xa, xb;
         xfrag(s, g, lane, xa, xb);
         const uint32_t xbv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
@@ -814,24 +984,15 @@ __device__ void lora_a1(const char* blk, int la, int lu, int ngh) {
             const uint32_t A[4] = {a.x, a.y, a.z, a.w};
             mma_16816(c, A, xbv[2 * st], xbv[2 * st + 1]);
         }
-        if (m) {
-            acc[1][0] += c[0];
-            acc[1][1] += c[2];
-        } else {
-            acc[0][0] += c[0];
-            acc[0][1] += c[2];
-        }
-        any = true;
+        a0 += c[0];
+        a1 += c[2];
     }
     if ((lane & 3) == 0) {
         const int g8 = lane >> 2;
-        s.part[wid][g8] = any ? acc[0][0] : 0.f;
-        s.part[wid][g8 + 8] = any ? acc[0][1] : 0.f;
-        s.part[wid][16 + g8] = any ? acc[1][0] : 0.f;
-        s.part[wid][16 + g8 + 8] = any ? acc[1][1] : 0.f;
+        s.part[wid][g8] = a0;
+        s.part[wid][g8 + 8] = a1;
     }
 }
-
 
 // act of every act row of the pair, weighted by its routing weight, as hi/lo B
 // fragments per 16-row step, with per-step sums; thread (sigma, k) owns row k of
@@ -862,9 +1023,24 @@ __device__ void act1(const Prog& p, int l, const float* m0, const float* m1, con
             const __half* bg = reinterpret_cast<const __half*>(blk2 + L.bg) + (long long)i * r;
             const __half* bu = reinterpret_cast<const __half*>(blk2 + L.bu) + (long long)i * r;
             float dg = 0.f, du = 0.f;
-            for (int j = 0; j < r; ++j) {
-                dg += __half2float(bg[j]) * s.lax[j];
-                du += __half2float(bu[j]) * s.lax[16 + j];
+            if ((r & 7) == 0) {
+                for (int j = 0; j < r; j += 8) {
+                    const uint4 gv = *reinterpret_cast<const uint4*>(bg + j);
+                    const uint4 uv = *reinterpret_cast<const uint4*>(bu + j);
+                    const __half2* g2 = reinterpret_cast<const __half2*>(&gv);
+                    const __half2* u2 = reinterpret_cast<const __half2*>(&uv);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 gf = __half22float2(g2[q]), uf = __half22float2(u2[q]);
+                        dg += gf.x * s.lax[j + 2 * q] + gf.y * s.lax[j + 2 * q + 1];
+                        du += uf.x * s.lax[16 + j + 2 * q] + uf.y * s.lax[16 + j + 2 * q + 1];
+                    }
+                }
+            } else {
+                for (int j = 0; j < r; ++j) {
+                    dg += __half2float(bg[j]) * s.lax[j];
+                    du += __half2float(bu[j]) * s.lax[16 + j];
+                }
             }
             const float ls = p.layers[l].lora_scale;
             gt += ls * dg;
@@ -889,7 +1065,10 @@ __device__ void act1(const Prog& p, int l, const float* m0, const float* m1, con
 
 // down of the pair's act over this CTA's half of the output row tiles: warp w
 // takes row tiles [nh w / 16, nh (w + 1) / 16); results into yacc
-__device__ void down1(const char* blk2, int nh) {
+// With `lora` (a shared pair): + (alpha / r) B_down v_pair on the same rows, one
+// MMA per row tile with B_down's rows as the A operand (k = the rank, zero
+// beyond r) and v_pair as hi/lo columns.
+__device__ void down1(const Prog& p, int l, const char* blk2, int nh, bool lora, float* yout) {
     Sm1& s = sm();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const Lay1& L = s.lay;
@@ -898,6 +1077,34 @@ __device__ void down1(const char* blk2, int nh) {
     float y[kMaxTw][2];
 #pragma unroll
     for (int j = 0; j < kMaxTw; ++j) y[j][0] = y[j][1] = 0.f;
+    if (lora) {
+        const int r = p.r, g8 = lane >> 2, t = lane & 3;
+        const float ls = p.layers[l].lora_scale;
+        uint2 bv = make_uint2(0u, 0u);
+        if (lane < 8) bv = s.af[kMaxSig * 8 - 8 + lane];   // v_pair hi/lo (written by lora_v1)
+        const __half* bd = reinterpret_cast<const __half*>(blk2 + L.bd);
+        const __half zero = __float2half_rn(0.f);
+#pragma unroll
+        for (int j = 0; j < kMaxTw; ++j) {
+            const int rt = ta + j;
+            if (rt < tb) {
+                // A fragment: rows rt*16 + g8 (+ 8), k = 2t, 2t+1 (+ 8)
+                const __half* r0 = bd + (long long)(rt * 16 + g8) * r;
+                const __half* r1 = r0 + 8LL * r;
+                auto at = [&](const __half* row, int k) { return k < r ? row[k] : zero; };
+                __half2 a0 = __halves2half2(at(r0, 2 * t), at(r0, 2 * t + 1));
+                __half2 a1 = __halves2half2(at(r1, 2 * t), at(r1, 2 * t + 1));
+                __half2 a2 = __halves2half2(at(r0, 2 * t + 8), at(r0, 2 * t + 9));
+                __half2 a3 = __halves2half2(at(r1, 2 * t + 8), at(r1, 2 * t + 9));
+                const uint32_t A[4] = {*reinterpret_cast<uint32_t*>(&a0), *reinterpret_cast<uint32_t*>(&a1),
+                                       *reinterpret_cast<uint32_t*>(&a2), *reinterpret_cast<uint32_t*>(&a3)};
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_16816(c, A, bv.x, bv.y);
+                y[j][0] += ls * (c[0] + c[1] * kLoInv);
+                y[j][1] += ls * (c[2] + c[3] * kLoInv);
+            }
+        }
+    }
     for (int pi = 0; pi < L.nparts; ++pi) {
         const Part1& P = L.part[pi];
         const int nst = P.sb - P.sa + 1;
@@ -934,14 +1141,21 @@ __device__ void down1(const char* blk2, int nh) {
             }
         }
     }
-    if ((lane & 3) == 0) {
-        const int g8 = lane >> 2;
+    // rows g (y[j][0]) and g + 8 (y[j][1]) sit in lanes 4g: lane q < 4 gathers rows
+    // 4q .. 4q+3 of the tile and adds them into the layer's y with one vector reduction
 #pragma unroll
-        for (int j = 0; j < kMaxTw; ++j)
-            if (ta + j < tb) {
-                s.yacc[(ta + j) * 16 + g8] = y[j][0];
-                s.yacc[(ta + j) * 16 + g8 + 8] = y[j][1];
+    for (int j = 0; j < kMaxTw; ++j) {
+        if (ta + j < tb) {
+            float v[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int src = (lane & 1) * 16 + 4 * m;
+                const float a = __shfl_sync(0xffffffffu, y[j][0], src);
+                const float b = __shfl_sync(0xffffffffu, y[j][1], src);
+                v[m] = (lane & 2) ? b : a;
             }
+            if (lane < 4) red_add_v4_f32(yout + (ta + j) * 16 + 4 * lane, v[0], v[1], v[2], v[3]);
+        }
     }
 }
 
@@ -959,39 +1173,21 @@ __device__ void lora_v1(const char* blk2, int r, int rows) {
     }
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
-    if (c == 0 && rr < 16) s.v[rr] = v;
-}
-
-// this CTA's output half into the layer's y: thread i adds rows 4i .. 4i+3 (with
-// the shared pair's (alpha / r) B_down v on them)
-__device__ void red1(const Prog& p, int l, float* y, const char* blk2, int nh, bool lora) {
-    Sm1& s = sm();
-    const int tid = threadIdx.x;
-    if (tid >= nh * 4) return;
-    float4 v = *reinterpret_cast<const float4*>(&s.yacc[4 * tid]);
-    if (lora) {
-        const int r = p.r;
-        const float ls = p.layers[l].lora_scale;
-        const __half* bd = reinterpret_cast<const __half*>(blk2 + s.lay.bd) + (long long)4 * tid * r;
-        float d4[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < r; ++j) {
-            const float vj = s.v[j];
-            d4[0] += __half2float(bd[j]) * vj;
-            d4[1] += __half2float(bd[r + j]) * vj;
-            d4[2] += __half2float(bd[2 * r + j]) * vj;
-            d4[3] += __half2float(bd[3 * r + j]) * vj;
-        }
-        v.x += ls * d4[0];
-        v.y += ls * d4[1];
-        v.z += ls * d4[2];
-        v.w += ls * d4[3];
+    if (c == 0 && rr < 16) {
+        s.v[rr] = v;
+        // as the B operand of down1's LoRA MMA (k = rr): lanes 0-3 hi, 4-7 lo
+        const __half hi = __float2half_rn(v);
+        const __half lo = __float2half_rn((v - __half2float(hi)) * kLoScale);
+        __half* bf = reinterpret_cast<__half*>(&s.af[kMaxSig * 8 - 8]);
+        const int kk = rr & 7, t = kk >> 1, wv = rr >> 3, hh = kk & 1;
+        bf[(t * 2 + wv) * 2 + hh] = hi;
+        bf[((4 + t) * 2 + wv) * 2 + hh] = lo;
     }
-    red_add_v4_f32(y + 4 * tid, v.x, v.y, v.z, v.w);
 }
 
 // ------------------------------------------------------------ head flush ----
-// x of head layer l over all of d as B fragments, its executed and previous ids
-__device__ void flush_head1(const Prog& p, int l, const __half* xs, const int32_t* ex, const int32_t* pv) {
+// x of head layer l over all of d as B fragments
+__device__ void flush_head1(const Prog& p, const __half* xs) {
     Sm1& s = sm();
     const int tid = threadIdx.x, n4 = p.d / 4;
     if (tid < n4) {
@@ -1002,26 +1198,18 @@ __device__ void flush_head1(const Prog& p, int l, const __half* xs, const int32_
         xw[((g * 4 + t) * 4 + st) * 2 + wv] = v.x;
         xw[((g * 4 + t + 1) * 4 + st) * 2 + wv] = v.y;
     }
-    if (tid < p.K) {
-        int e = __ldcg(ex + tid);
-        s.fex[tid] = e < 0 || e >= p.E ? 0 : e;
-        if (pv) {
-            e = __ldcg(pv + tid);
-            s.fpv[tid] = e < 0 || e >= p.E ? 0 : e;
-        }
-    }
-    if (tid == 0) s.fnpv = pv ? p.K : 0;
     cbar1();
 }
 
 // one task of head layer l (see flush_block); its logits summed into lg
-__device__ void flush_task1(const Prog& p, int l, int j, const char* blk, float* lg) {
+__device__ void flush_task1(const Prog& p, int l, int j, int n2, const char* blkA, const char* blkB, float* lg) {
     Sm1& s = sm();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g8 = lane >> 2;
     const LayerP& Ly = p.layers[l];
     const int nH = p.H / kRowTile, nE = p.E / kRowTile, ng = p.d / kGroup;
     const bool fc1 = j < nH;
     const int row0 = 16 * (fc1 ? j : j - nH);
+    (void)Ly;
     // dense part: warp w takes groups [ng w / 16, ng (w + 1) / 16) of the row tile
     int ga, gb;
     split1(ng, kCW, wid, &ga, &gb);
@@ -1030,7 +1218,7 @@ __device__ void flush_task1(const Prog& p, int l, int j, const char* blk, float*
         uint4 xa, xb;
         xfrag(s, g, lane, xa, xb);
         const uint32_t xbv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-        const char* unit = blk + (long long)g * kF16Unit;
+        const char* unit = g < ng / 2 ? blkA + (long long)g * kF16Unit : blkB + (long long)(g - ng / 2) * kF16Unit;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
@@ -1045,24 +1233,17 @@ __device__ void flush_task1(const Prog& p, int l, int j, const char* blk, float*
         s.part[wid][g8] = acc0;
         s.part[wid][g8 + 8] = acc1;
     }
-    // one-hot columns of the executed and previous masks [S3.2 "Head"]: the rows
-    // of the transposed columns, gathered (never a materialised concat)
-    const int n2 = p.K + s.fnpv;
-    if (tid < n2 * 16) {
-        const int k2 = tid >> 4, i = tid & 15;
-        const int e = k2 < p.K ? s.fex[k2] : p.E + s.fpv[k2 - p.K];
-        const __half* oh = fc1 ? Ly.fc1_oh + (long long)e * p.H : Ly.linit_oh + (long long)e * p.E;
-        s.oh[k2][i] = __half2float(oh[row0 + i]);
-    }
     cbar1();
     if (tid < 16) {
         float z = 0.f;
-        for (int w = 0; w < kCW; ++w) {
-            int a, b;
-            split1(ng, kCW, w, &a, &b);
-            if (a < b) z += s.part[w][tid];
-        }
-        for (int k2 = 0; k2 < n2; ++k2) z += s.oh[k2][tid];
+        for (int w = 0; w < kCW; ++w)
+            if ((s.fl_warps >> w) & 1u) z += s.part[w][tid];
+        // one-hot columns of the executed and previous masks [S3.2 "Head"]: the
+        // rows of the transposed columns that the producer gathered into the block
+        // (the concatenated features are never materialised)
+        const __half* oh = reinterpret_cast<const __half*>(blkB + (long long)(ng - ng / 2) * kF16Unit +
+                                                           (fc1 ? (long long)nE * kF16Step : 0LL));
+        for (int k2 = 0; k2 < n2; ++k2) z += __half2float(oh[k2 * 16 + tid]);
         if (fc1) {
             // erf-GELU [S3.2 "Head"], then fc2 columns row0 .. row0+15 below
             const float gl = 0.5f * z * (1.f + erff(z * 0.70710678118654752f));
@@ -1079,7 +1260,7 @@ __device__ void flush_task1(const Prog& p, int l, int j, const char* blk, float*
     if (fc1) {
         cbar1();
         const uint2 b = lane < 8 ? s.gf[lane] : make_uint2(0u, 0u);
-        const char* fc2 = blk + (long long)ng * kF16Unit;
+        const char* fc2 = blkB + (long long)(ng - ng / 2) * kF16Unit;
         for (int rt = wid; rt < nE; rt += kCW) {
             const uint4 a = *reinterpret_cast<const uint4*>(fc2 + (long long)rt * kF16Step + 16 * lane);
             const uint32_t A[4] = {a.x, a.y, a.z, a.w};
@@ -1105,7 +1286,7 @@ __device__ void route_row1(const float* lg, int E, int K, int kind, int ng, int 
 
 // ---------------------------------------------------------------- consumers ----
 __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, int par, unsigned tag,
-                          unsigned long long base) {
+                          unsigned long long base, unsigned long long base_r) {
     Sm1& s = sm();
     const int tid = threadIdx.x;
     const int rank = (int)cluster_ctarank();
@@ -1116,20 +1297,23 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
     const int nh = nrth1(p.d, rank), row0 = rank ? 16 * (p.d / kRowTile / 2) : 0;
     const bool lora = s.S.lora && pl.role == R1_SHARED && pl.nseg > 0;
     const int hold = ld_volatile_s32(&hdr->hold);
-    unsigned long long nbar = 0;   // grid barriers arrived at
+    unsigned long long nend = 0, nrt = 0;   // layer-end and router barriers arrived at
     bool first_wait = true;
-    auto target = [&](unsigned long long k) {   // count after barrier k (0-based) completes
-        unsigned long long t = base + (unsigned long long)nct * (k + 1);
+    // counter value once `n` barriers of a counter with launch base `b` completed
+    auto target = [&](unsigned long long b, unsigned long long n) {
+        unsigned long long t = b + (unsigned long long)nct * n;
         if (first_wait) t += (unsigned long long)(hold > 0 ? hold : 0);
         return t;
     };
-    Cons1 c{0, 0, 0, 0};
+    Cons1 c{{0, 0}, 0, 0, 0};
     int nx = 0;   // pair exchanges so far
     const uint32_t peer = (uint32_t)rank ^ 1u;
     const uint32_t rbar = mapa_shared(smem_u32(&s.xbar), peer);
     const uint32_t rrecv = mapa_shared(smem_u32(s.recv), peer);
-    const bool xch = pl.n_hr > 0 || pl.role == R1_LORA;
-    const int msg = pl.role == R1_LORA ? 32 : pl.n_hr * 16;
+    const bool xch = pl.n_hr > 0;
+    const int msg = pl.n_hr * 16;
+    // x fragments held: this CTA's half of d, or all of d on the LoRA pair
+    const int xa0 = pl.role == R1_LORA ? 0 : g0, xa1 = pl.role == R1_LORA ? ng : g0 + ngh;
     // RMSNorm gain of layer 0 (then of the next layer, loaded a layer ahead)
     const int n4 = p.d / 4;
     auto gain = [&](int l) {
@@ -1139,6 +1323,57 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
         return g;
     };
     uint2 gam = gain(0);
+    // ---- head flush (after the last layer that owns a head): x of a head layer
+    // is final once the barrier that ends the layer has passed.  A CTA adds its
+    // finished tasks of a head to the head's count once; the one that completes
+    // the count routes.  false: the launch gave up (uniform).
+    auto flush = [&]() -> bool {
+        const int tph = p.H / kRowTile + p.E / kRowTile;
+        const int n2 = p.K + (step > 0 ? p.K : 0);
+        int xl = -1, ndone = 0;
+        for (int t = pl.t0; t < pl.t1; ++t) {
+            const int hi = t / tph, j = t % tph, l = s.heads[hi];
+            const LayerP& Ly = p.layers[l];
+            const int sidx = Ly.sidx;
+            if (l != xl) {
+                if (!grid_wait1(hdr, &hdr->barrier, target(base, (unsigned long long)l + 1))) return false;
+                first_wait = false;
+                flush_head1(p, reinterpret_cast<const __half*>(p.ws + W.xs) + (long long)sidx * p.d);
+                xl = l;
+            }
+            float* lg = reinterpret_cast<float*>(p.ws + W.logh) + ((long long)par * p.Ls + sidx) * p.E;
+            stamp1(p, 0xF100 | (t - pl.t0));
+            bool ok = take1(p, hdr, c, flush_bytes(s.S, j, 0, n2));
+            const char* blkA = ring() + c.off;
+            ok = take1(p, hdr, c, flush_bytes(s.S, j, 1, n2)) && ok;
+            const char* blkB = ring() + c.off;
+            stamp1(p, 0xF200 | (t - pl.t0));
+            if (ok) flush_task1(p, l, j, n2, blkA, blkB, lg);
+            if (cbar_or1(!ok || vload(&s.abort))) return false;
+            give1(c);
+            stamp1(p, 0xF300 | (t - pl.t0));
+            ++ndone;
+            const bool head_end = t + 1 == pl.t1 || (t + 1) / tph != hi;
+            if (!head_end) continue;
+            if (tid == 0) {
+                __threadfence();
+                unsigned* cnt = reinterpret_cast<unsigned*>(p.ws + W.cnt) + ((long long)par * p.Ls + sidx);
+                s.topk = atom_acq_rel_add_u32(cnt, (unsigned)ndone) + (unsigned)ndone == (unsigned)tph;
+            }
+            ndone = 0;
+            cbar1();
+            if (s.topk && tid < 32) {
+                // the head's prediction for its target layer at the next token [S3.2]
+                const long long o = ((long long)par * p.Ls + Ly.head_target) * p.K;
+                route_row1(lg, p.E, p.K, Ly.head_route_kind, Ly.head_n_groups, Ly.head_topk_groups,
+                           Ly.head_route_scale, Ly.head_bias, p.pred_ids + o, p.pred_w + o);
+                if (p.dbg_logits)
+                    for (int e = tid; e < p.E; e += 32) p.dbg_logits[(long long)l * p.E + e] = s.logits[e];
+            }
+            cbar1();
+        }
+        return true;
+    };
     bool broke = true;   // left the layer loop early (set false when it completes)
     for (int l = 0;; ++l) {
         if (l == p.L) {
@@ -1148,20 +1383,22 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
         const LayerP& Ly = p.layers[l];
         const bool own = own_routed1(p, l, step);
         const int sidx = Ly.sidx;
-        float* y = reinterpret_cast<float*>(p.ws + W.y) + ((long long)par * p.Ls + sidx) * p.d;
+        float* y = reinterpret_cast<float*>(p.ws + W.y) + (((long long)par * p.Ls + sidx) * kNY + (cta >> 1) % kNY) * p.d;
         stamp1(p, (l << 8) | 0);
-        if (xch && tid == 0) mbar_arrive_expect_tx(&s.xbar, (uint32_t)(msg * 4));
+        // the exchange barrier of this layer is armed before the peer can send:
+        // layer 0's here, the next layer's before this layer's grid arrival
+        if (l == 0 && xch && tid == 0) mbar_arrive_expect_tx(&s.xbar, (uint32_t)(msg * 4));
         // ---- x: the previous layer's y is complete after its barrier
         const float* yprev = nullptr;
         if (l > 0) {
-            if (!grid_wait1(hdr, target(nbar - 1))) break;
+            if (!grid_wait1(hdr, &hdr->barrier, target(base, nend))) break;
             first_wait = false;
-            yprev = reinterpret_cast<const float*>(p.ws + W.y) + ((long long)par * p.Ls + p.layers[l - 1].sidx) * p.d;
+            yprev = reinterpret_cast<const float*>(p.ws + W.y) + ((long long)par * p.Ls + p.layers[l - 1].sidx) * kNY * p.d;
         }
         stamp1(p, (l << 8) | 1);
         __half* xs_out = cta < 2 ? reinterpret_cast<__half*>(p.ws + W.xs) + (long long)sidx * p.d : nullptr;
         __half* dbg = (p.dbg_h && cta == 0 && l > 0) ? p.dbg_h + (long long)(l - 1) * p.d : nullptr;
-        build_x1(p, l, l == 0 ? p.h_io : nullptr, yprev, gam, g0, g0 + ngh, xs_out, dbg);
+        build_x1(p, l, l == 0 ? p.h_io : nullptr, yprev, gam, xa0, xa1, xs_out, dbg);
         gam = gain(l + 1);
         stamp1(p, (l << 8) | 2);
         // ---- routing
@@ -1170,14 +1407,15 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
             bool ok = true;
             if (L.b0.bytes) {
                 ok = take1(p, hdr, c, L.b0.bytes);
-                if (ok) router_units1(p, ring() + c.off, logr);
+                if (ok) router_units1(p, ring() + c.off, logr, g0 - xa0);
             }
             if (cbar_or1(!ok || vload(&s.abort))) break;
             if (L.b0.bytes) give1(c);
-            grid_arrive1(hdr);
-            ++nbar;
+            stamp1(p, (l << 8) | 11);
+            grid_arrive1(&hdr->barrier_r);
+            ++nrt;
             if (pl.role == R1_ROUTED && (pl.nseg > 0 || cta == 0)) {
-                if (!grid_wait1(hdr, target(nbar - 1))) break;
+                if (!grid_wait1(hdr, &hdr->barrier_r, target(base_r, nrt))) break;
                 first_wait = false;
                 stamp1(p, (l << 8) | 3);
                 if (tid < 32)
@@ -1192,9 +1430,10 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
         // ---- gate/up (or LoRA A) partial sums over this CTA's half, swapped with the peer
         if (L.b1.bytes) {
             const bool ok = take1(p, hdr, c, L.b1.bytes);
+            stamp1(p, (l << 8) | 9);
             const char* blk1 = ring() + c.off;
             if (ok) {
-                if (pl.role == R1_LORA) lora_a1(blk1, L.la, L.lu, ngh);
+                if (pl.role == R1_LORA) lora_a1(blk1, ng);
                 else gateup1(blk1, ngh, pl.n_hr);
             }
             if (cbar_or1(!ok || vload(&s.abort))) break;
@@ -1204,12 +1443,8 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
         if (xch) {
             if (tid < msg) {
                 float v = 0.f;
-                for (int w = 0; w < kCW; ++w) {
-                    int a, b;
-                    if (pl.role == R1_LORA) { a = w; b = w < 2 * ngh ? w + 1 : w; }
-                    else split1(ngh, kCW, w, &a, &b);
-                    if (a < b) v += s.part[w][tid];
-                }
+                for (int w = 0; w < kCW; ++w)
+                    if ((s.gu_warps >> w) & 1u) v += s.part[w][tid];
                 s.mine[tid] = v;
                 st_async_b32(rrecv + 4u * tid, v, rbar);
             }
@@ -1233,7 +1468,10 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
                 }
                 s.lax[ln] = __uint_as_float((unsigned)(v & 0xFFFFFFFFu));
             }
-            if (tid == 0 && !mbar_wait1(hdr, &s.xbar, (uint32_t)(nx & 1))) *(volatile int*)&s.abort = 1;
+            if (tid == 0) {
+                if (!mbar_wait1(hdr, &s.xbar, (uint32_t)(nx & 1))) *(volatile int*)&s.abort = 1;
+                else if (l + 1 < p.L) mbar_arrive_expect_tx(&s.xbar, (uint32_t)(msg * 4));
+            }
             ++nx;
             if (cbar_or1(vload(&s.abort) != 0)) break;
         }
@@ -1241,89 +1479,58 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
         const float* m1 = rank ? s.mine : s.recv;
         stamp1(p, (l << 8) | 6);
         if (pl.role == R1_LORA) {
-            if (rank == 0 && tid < 32) {
+            // (value, tag) words: rank 0 A_gate x (words 0-15), rank 1 A_up x (16-31)
+            if (tid < 16) {
+                float v = 0.f;
+                for (int w = 0; w < kCW; ++w)
+                    if ((s.gu_warps >> w) & 1u) v += s.part[w][tid];
                 unsigned long long* dst =
                     reinterpret_cast<unsigned long long*>(p.ws + W.lax) + ((long long)par * p.Ls + sidx) * 32;
-                const float v = m0[tid] + m1[tid];
-                st_relaxed_u64(dst + tid, ((unsigned long long)tag << 32) | __float_as_uint(v));
+                st_relaxed_u64(dst + 16 * rank + tid, ((unsigned long long)tag << 32) | __float_as_uint(v));
             }
-            grid_arrive1(hdr);
-            ++nbar;
+            cbar1();
+            grid_arrive1(&hdr->barrier);
+            ++nend;
+            if (l == s.flush_after && !flush()) break;
             continue;
         }
         // ---- act, down, y
         if (L.b2.bytes) {
             const bool ok = take1(p, hdr, c, L.b2.bytes);
+            stamp1(p, (l << 8) | 10);
             const char* blk2 = ring() + c.off;
             if (ok) act1(p, l, m0, m1, blk2, lora);
             if (cbar_or1(!ok || vload(&s.abort))) break;
             stamp1(p, (l << 8) | 7);
-            down1(blk2, nh);
-            if (lora) lora_v1(blk2, p.r, 8 * pl.n_hr);
-            cbar1();
-            red1(p, l, y + row0, blk2, nh, lora);
+            if (lora) {
+                lora_v1(blk2, p.r, 8 * pl.n_hr);
+                cbar1();
+            }
+            down1(p, l, blk2, nh, lora, y + row0);
             cbar1();
             give1(c);
         } else {
             cbar1();
         }
         stamp1(p, (l << 8) | 8);
-        grid_arrive1(hdr);
-        ++nbar;
+        grid_arrive1(&hdr->barrier);
+        ++nend;
+        if (l == s.flush_after && !flush()) break;
     }
     if (broke) {
         if (tid == 0) *(volatile int*)&s.abort = 1;
         return;
     }
-    // ---- head flush: x, executed and previous ids of every head layer are final
-    // once the layer's barrier passed (the last layer's: after the final one)
-    const int tph = p.H / kRowTile + p.E / kRowTile;
-    bool final_seen = false;
-    int xl = -1;
-    for (int t = pl.t0; t < pl.t1; ++t) {
-        const int hi = t / tph, j = t % tph, l = s.heads[hi];
-        const LayerP& Ly = p.layers[l];
-        const int sidx = Ly.sidx;
-        if (l != xl) {
-            if (l == p.L - 1 && !final_seen) {
-                if (!grid_wait1(hdr, target(nbar - 1))) return;
-                final_seen = true;
-            }
-            const int32_t* ex = p.exec_ids + ((long long)par * p.Ls + sidx) * p.K;
-            const int32_t* pv = step > 0 ? p.exec_ids + ((long long)(par ^ 1) * p.Ls + sidx) * p.K : nullptr;
-            flush_head1(p, l, reinterpret_cast<const __half*>(p.ws + W.xs) + (long long)sidx * p.d, ex, pv);
-            xl = l;
-        }
-        float* lg = reinterpret_cast<float*>(p.ws + W.logh) + ((long long)par * p.Ls + sidx) * p.E;
-        Block1 B;
-        flush_block(s.S, j, B);
-        const bool ok = take1(p, hdr, c, B.bytes);
-        if (ok) flush_task1(p, l, j, ring() + c.off, lg);
-        if (cbar_or1(!ok || vload(&s.abort))) return;
-        give1(c);
-        if (tid == 0) {
-            __threadfence();
-            unsigned* cnt = reinterpret_cast<unsigned*>(p.ws + W.cnt) + ((long long)par * p.Ls + sidx);
-            s.topk = atom_acq_rel_add_u32(cnt, 1u) == (unsigned)(tph - 1);
-        }
-        cbar1();
-        if (s.topk && tid < 32) {
-            // the head's prediction for its target layer at the next token [S3.2]
-            const long long o = ((long long)par * p.Ls + Ly.head_target) * p.K;
-            route_row1(lg, p.E, p.K, Ly.head_route_kind, Ly.head_n_groups, Ly.head_topk_groups,
-                       Ly.head_route_scale, Ly.head_bias, p.pred_ids + o, p.pred_w + o);
-            if (p.dbg_logits)
-                for (int e = tid; e < p.E; e += 32) p.dbg_logits[(long long)l * p.E + e] = s.logits[e];
-        }
-        cbar1();
-    }
     stamp1(p, 0xFF00);
     // ---- the last layer's output
-    if (!final_seen && !grid_wait1(hdr, target(nbar - 1))) return;
-    const float* ylast = reinterpret_cast<const float*>(p.ws + W.y) + ((long long)par * p.Ls + p.layers[p.L - 1].sidx) * p.d;
+    if (!grid_wait1(hdr, &hdr->barrier, target(base, nend))) return;
+    const float* ylast = reinterpret_cast<const float*>(p.ws + W.y) + ((long long)par * p.Ls + p.layers[p.L - 1].sidx) * kNY * p.d;
     const int a = p.d * cta / nct, b = p.d * (cta + 1) / nct;
     for (int i = a + tid; i < b; i += kCT) {
-        const __half h = __float2half_rn(__half2float(s.h[i]) + __ldcg(ylast + i));
+        float yv = 0.f;
+#pragma unroll
+        for (int q = 0; q < kNY; ++q) yv += __ldcg(ylast + (long long)q * p.d + i);
+        const __half h = __float2half_rn(__half2float(s.h[i]) + yv);
         p.h_io[i] = h;
         if (p.dbg_h) p.dbg_h[(long long)(p.L - 1) * p.d + i] = h;
     }
@@ -1350,7 +1557,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kT1, 1)
     }
     const int rank = (int)cluster_ctarank(), pair = blockIdx.x / 2;
     const Ws1 W = ws1(p.Ls, p.d, p.E);
-    __shared__ unsigned long long s_base;
+    __shared__ unsigned long long s_base, s_base_r;
     __shared__ int s_step;
     __shared__ unsigned s_tag;
     if (tid == 0) {
@@ -1369,6 +1576,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kT1, 1)
         fence_mbar_init();
         const unsigned long long v = ld_acquire_u64(&hdr->barrier);
         s_base = v - v % (unsigned long long)gridDim.x;
+        const unsigned long long vr = ld_acquire_u64(&hdr->barrier_r);
+        s_base_r = vr - vr % (unsigned long long)gridDim.x;
         s_step = p.step >= 0 ? p.step : ld_volatile_s32(&hdr->step);
         s_tag = (ld_volatile_s32(reinterpret_cast<const int*>(&hdr->serial)) & 0x3FFFFFFF) + 1;
         // the plan of this CTA and the layout of its blocks
@@ -1378,28 +1587,45 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kT1, 1)
         S.lora = (p.layers[0].flags & LF_LORA) != 0;
         S.P = p.pairs1[0]; S.Pr = p.pairs1[1]; S.Ps = p.pairs1[2]; S.Pl = p.pairs1[3];
         int nh = 0;
+        s.flush_after = -1;
         for (int l = 0; l < p.L; ++l)
-            if (p.layers[l].flags & LF_HEAD) s.heads[nh++] = l;
+            if (p.layers[l].flags & LF_HEAD) {
+                s.heads[nh++] = l;
+                s.flush_after = l;
+            }
         S.n_heads = nh;
         s.S = S;
         if (!plan1(S, pair, rank, s.plan) || !layout1(S, s.plan, rank, s.lay)) fail1(hdr, EDGE0_EUNSUPPORTED);
+        // warps that write partial sums (the others' part rows are not read)
+        const int ngh = ngh1(p.d, rank), ng = p.d / kGroup;
+        unsigned gm = 0, fm = 0;
+        for (int w = 0; w < kCW; ++w) {
+            int a, b;
+            split1(ngh, kCW, w, &a, &b);
+            if (s.plan.role == R1_LORA ? w < ng : a < b) gm |= 1u << w;
+            split1(ng, kCW, w, &a, &b);
+            if (a < b) fm |= 1u << w;
+        }
+        s.gu_warps = gm;
+        s.fl_warps = fm;
     }
     __syncthreads();
     const int step = s_step, par = step & 1;
     // clear the other step parity of this launch's layers for the next step
     {
         const int op = par ^ 1;
-        const long long per = (long long)p.d + 2LL * p.E + 64;   // floats: y, logr, logh, lax (32 u64)
+        const long long dy = (long long)kNY * p.d;
+        const long long per = dy + 2LL * p.E + 64;   // floats: y copies, logr, logh, lax (32 u64)
         const long long tot = (long long)p.L * per;
         const long long a = tot * blockIdx.x / gridDim.x, b = tot * (blockIdx.x + 1) / gridDim.x;
         for (long long i = a + tid; i < b; i += kT1) {
             const long long l = i / per, o = i % per;
             const long long row = (long long)op * p.Ls + p.layers[l].sidx;
             float* dst;
-            if (o < p.d) dst = reinterpret_cast<float*>(p.ws + W.y) + row * p.d + o;
-            else if (o < p.d + p.E) dst = reinterpret_cast<float*>(p.ws + W.logr) + row * p.E + (o - p.d);
-            else if (o < p.d + 2LL * p.E) dst = reinterpret_cast<float*>(p.ws + W.logh) + row * p.E + (o - p.d - p.E);
-            else dst = reinterpret_cast<float*>(p.ws + W.lax) + row * 64 + (o - p.d - 2LL * p.E);
+            if (o < dy) dst = reinterpret_cast<float*>(p.ws + W.y) + row * dy + o;
+            else if (o < dy + p.E) dst = reinterpret_cast<float*>(p.ws + W.logr) + row * p.E + (o - dy);
+            else if (o < dy + 2LL * p.E) dst = reinterpret_cast<float*>(p.ws + W.logh) + row * p.E + (o - dy - p.E);
+            else dst = reinterpret_cast<float*>(p.ws + W.lax) + row * 64 + (o - dy - 2LL * p.E);
             *dst = 0.f;
         }
         if (blockIdx.x == 0)
@@ -1425,8 +1651,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kT1, 1)
     // the peer's barriers exist before any exchange
     cluster_sync_all();
     if (!vload(&s.abort)) {
-        if (tid >= kCT) producer1(p, hdr, step);
-        else consumer1(p, hdr, W, step, par, s_tag, s_base);
+        if (tid >= kCT) producer1(p, hdr, step, par, s_base);
+        else consumer1(p, hdr, W, step, par, s_tag, s_base, s_base_r);
     }
     __syncthreads();
     if (tid == 0 && vload(&s.abort)) {
@@ -1516,11 +1742,15 @@ int derive1(Key1& k) {
             biggest = L.b2.bytes > biggest ? L.b2.bytes : biggest;
         }
     const int tph = S.H / kRowTile + S.E / kRowTile;
-    for (int j = 0; j < tph && S.n_heads > 0; ++j) {
-        Block1 B;
-        if (!flush_block(S, j, B)) return EDGE0_EUNSUPPORTED;
-        biggest = B.bytes > biggest ? B.bytes : biggest;
-    }
+    for (int j = 0; j < tph && S.n_heads > 0; ++j)
+        for (int h = 0; h < 2; ++h) {
+            Block1 B;
+            if (!flush_block(S, j, h, B, nullptr, 2 * S.K) || B.n > 32) return EDGE0_EUNSUPPORTED;
+            biggest = B.bytes > biggest ? B.bytes : biggest;
+        }
+    // a task's two blocks are held together
+    if (S.n_heads > 0 && flush_bytes(S, 0, 0, 2 * S.K) + 2 * flush_bytes(S, 0, 1, 2 * S.K) > ring)
+        return EDGE0_EUNSUPPORTED;
     if (biggest > ring) return EDGE0_EUNSUPPORTED;
     k.P = S.P; k.Pr = S.Pr; k.Ps = S.Ps; k.Pl = S.Pl;
     k.ring = ring;

@@ -126,6 +126,7 @@ struct WsHeader {
     int hold;                     // test hook: arrivals the first grid barrier of a launch
                                   // waits for beyond the grid (> 0: it cannot complete)
     unsigned long long wait_ns;   // limit of every bounded wait (0: kDefaultWaitNs)
+    unsigned long long barrier_r; // arrival counter of the batch-1 kernel's router barriers
 };
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
 constexpr int kWsHeaderBytes = 256;

@@ -39,6 +39,8 @@ static long long src_size(const Shape1& S, const Plan1& pl, const Piece1& pc) {
         case K1_FC1: return f16_bytes(S.H, S.d);
         case K1_FC2: return f16_bytes(S.E, S.H);
         case K1_LINIT: return f16_bytes(S.E, S.d);
+        case K1_OHF: return 2LL * 2 * S.E * S.H;
+        case K1_OHL: return 2LL * 2 * S.E * S.E;
     }
     return -1;
 }
@@ -138,7 +140,7 @@ static void check_shape(const char* name, int d, int E, int K, int I, int Is, in
             // gate/up units of the block: n_hr x groups of the half, 576 bytes each
             if (pl.role != R1_LORA) CHECK(L.b1.bytes == pl.n_hr * ngh1(d, rank) * 576, "P1 bytes");
             if (pl.role == R1_LORA)
-                CHECK(L.b1.bytes == 2 * ngh1(d, rank) * 2048 && L.b2.bytes == 0, "LoRA pair blocks");
+                CHECK(L.b1.bytes == (d / 64) * 2048 && L.b2.bytes == 0, "LoRA pair blocks");
         }
     for (size_t i = 0; i < cov_rt.size(); ++i) CHECK(cov_rt[i] == 1, "%s routed hr %zu covered %d", name, i, cov_rt[i]);
     for (size_t i = 0; i < cov_sh.size(); ++i) CHECK(cov_sh[i] == 1, "%s shared hr %zu covered %d", name, i, cov_sh[i]);
@@ -146,12 +148,28 @@ static void check_shape(const char* name, int d, int E, int K, int I, int Is, in
         for (size_t i = 0; i < cov_ru[h].size(); ++i) CHECK(cov_ru[h][i] == 1, "router unit %d/%zu: %d", h, i, cov_ru[h][i]);
     for (size_t i = 0; i < cov_task.size(); ++i) CHECK(cov_task[i] == 1, "task %zu: %d", i, cov_task[i]);
     CHECK(n_lora == (lora ? 1 : 0), "LoRA pairs %d", n_lora);
-    for (int j = 0; j < tph && n_heads; ++j) {
-        Block1 B;
-        CHECK(flush_block(S, j, B), "flush block %d", j);
-        Plan1 pl;
-        plan1(S, 0, 0, pl);
-        check_block(S, pl, B, k.ring, "flush");
+    // flush blocks with the one-hot rows of the extreme columns (0 and 2E - 1)
+    std::vector<int> ids(2 * K);
+    for (int q = 0; q < 2; ++q) {
+        for (int i = 0; i < 2 * K; ++i) ids[i] = q ? (i < K ? E - 1 - i : 2 * E - 1 - (i - K)) : (i < K ? i : E + i - K);
+        for (int j = 0; j < tph && n_heads; ++j)
+            for (int h = 0; h < 2; ++h) {
+                Block1 B;
+                CHECK(flush_block(S, j, h, B, ids.data(), 2 * K), "flush block %d/%d", j, h);
+                CHECK(flush_bytes(S, j, h, 2 * K) == B.bytes, "flush_bytes %d != %d", flush_bytes(S, j, h, 2 * K), B.bytes);
+                CHECK(h == 0 || flush_bytes(S, j, h, K) == B.bytes - 32 * K, "flush_bytes without previous ids");
+                CHECK(B.n <= 32, "more copies than producer lanes");
+                Plan1 pl;
+                plan1(S, 0, 0, pl);
+                check_block(S, pl, B, k.ring, "flush");
+            }
+    }
+    // the two blocks of an fc1 task read the whole row tile of fc1 once
+    if (n_heads) {
+        Block1 A, B;
+        flush_block(S, 0, 0, A);
+        flush_block(S, 0, 1, B);
+        CHECK(A.pc[0].bytes + B.pc[0].bytes == 32 * d, "fc1 row tile bytes");
     }
 }
 

@@ -21,7 +21,9 @@
  * Conventions for every call
  *   - Pointers are DEVICE pointers unless the argument says HOST.  The caller
  *     owns every buffer; the library borrows them for the call, never frees them
- *     and keeps no global state.
+ *     and keeps no global state -- except edge0_moe_int4_forward_noalloc, whose
+ *     scratch is a fixed array inside the library (see its section) and whose
+ *     device-side status is read with edge0_noalloc_error.
  *   - fp16 tensors are IEEE binary16 (passed as uint16_t); fp32 as float.
  *   - Every call enqueues work on `stream` and returns without synchronising.
  *     Arguments are validated on the host before anything is launched; an
@@ -324,11 +326,25 @@ void edge0_pool_destroy(edge0_pool* pool);
  *     device (cudaGetSymbolAddress); make that first call before any stream
  *     capture.
  *   - All calls share the array: two calls whose kernels overlap on the GPU (for
- *     instance on different streams) race and give wrong results. */
+ *     instance on different streams) race and give wrong results.
+ *   - The cached address belongs to the device's primary context: it is no longer
+ *     valid after cudaDeviceReset on that device.
+ *   - The call builds the kernel's parameter block (up to 32 KB) on the calling
+ *     thread's stack: threads with small stacks must allow for it.
+ *   - A shape refused on the host (EDGE0_EINVAL, EDGE0_EUNSUPPORTED) queues
+ *     nothing.  What the kernel itself records (EDGE0_EINVAL for a slot_table
+ *     entry outside [0, n_slots), EDGE0_ETIMEOUT for a wait that ran out) stays
+ *     in the array's header until the next call clears it: read it with
+ *     edge0_noalloc_error before that call. */
 #define EDGE0_NOALLOC_SCRATCH_BYTES (1 << 17)
 int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const uint16_t* x,
                                    const int32_t* ids, const float* w, int B, uint16_t* y,
                                    cudaStream_t stream);
+/* HOST call: synchronises `stream`, writes the status the last
+ * edge0_moe_int4_forward_noalloc kernel on the current device recorded
+ * (EDGE0_OK, EDGE0_EINVAL, EDGE0_ETIMEOUT) to *status and clears it.  Allocates
+ * nothing. */
+int edge0_noalloc_error(cudaStream_t stream, int* status);
 
 #ifdef __cplusplus
 }

@@ -108,6 +108,7 @@ def _declare(L):
                                        C.c_size_t, P]
     L.edge0_moe_int4_forward.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P, C.c_size_t, P]
     L.edge0_moe_int4_forward_noalloc.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P]
+    L.edge0_noalloc_error.argtypes = [P, C.POINTER(C.c_int)]
     L.edge0_lora_delta.argtypes = [C.POINTER(LoraDesc), P, C.c_int, P, P]
     L.edge0_decode_layer.argtypes = [C.POINTER(LayerDesc), P, C.POINTER(RouteState), C.c_int,
                                      C.c_int, P]
@@ -117,7 +118,7 @@ def _declare(L):
                  "edge0_pack_f16_kmajor", "edge0_pack_cols_T", "edge0_state_init",
                  "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
                  "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
-                 "edge0_moe_int4_forward_noalloc", "edge0_state_set_wait_limit"):
+                 "edge0_moe_int4_forward_noalloc", "edge0_state_set_wait_limit", "edge0_noalloc_error"):
         getattr(L, name).restype = C.c_int
 
 
@@ -127,7 +128,7 @@ EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_
             "edge0_workspace_bytes", "edge0_decode_workspace_bytes", "edge0_state_init",
             "edge0_state_error", "edge0_state_set_wait_limit", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
-            "edge0_moe_int4_forward_noalloc", "edge0_pool_create", "edge0_pool_set_layer",
+            "edge0_moe_int4_forward_noalloc", "edge0_noalloc_error", "edge0_pool_create", "edge0_pool_set_layer",
             "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_resident", "edge0_pool_destroy"]
 
 

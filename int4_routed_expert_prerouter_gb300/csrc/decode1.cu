@@ -921,7 +921,7 @@ __device__ void router_units1(const Prog& p, const char* blk, float* logr, int x
 
 // gate/up partial sums of the pair's hr over this CTA's half of d: warp w takes
 // groups [ngh w / 16, ngh (w + 1) / 16) of every hr
-__device__ void gateup1(const char* blk, int ngh, int n_hr) {
+__device__ void gateup1(const Prog& p, const char* blk, int ngh, int n_hr) {
     Sm1& s = sm();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int ga, gb;
@@ -955,6 +955,7 @@ __device__ void gateup1(const char* blk, int ngh, int n_hr) {
             }
         }
     }
+    stamp1(p, 0xE010);
     if ((lane & 3) == 0) {
         const int g8 = lane >> 2;
 #pragma unroll
@@ -1141,6 +1142,7 @@ __device__ void down1(const Prog& p, int l, const char* blk2, int nh, bool lora,
             }
         }
     }
+    stamp1(p, 0xE020);
     // rows g (y[j][0]) and g + 8 (y[j][1]) sit in lanes 4g: lane q < 4 gathers rows
     // 4q .. 4q+3 of the tile and adds them into the layer's y with one vector reduction
 #pragma unroll
@@ -1157,6 +1159,7 @@ __device__ void down1(const Prog& p, int l, const char* blk2, int nh, bool lora,
             if (lane < 4) red_add_v4_f32(yout + (ta + j) * 16 + 4 * lane, v[0], v[1], v[2], v[3]);
         }
     }
+    stamp1(p, 0xE021);
 }
 
 // the shared pair's partial v = A_down^T-rows . act of its own rows (64 threads:
@@ -1434,7 +1437,7 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
             const char* blk1 = ring() + c.off;
             if (ok) {
                 if (pl.role == R1_LORA) lora_a1(blk1, ng);
-                else gateup1(blk1, ngh, pl.n_hr);
+                else gateup1(p, blk1, ngh, pl.n_hr);
             }
             if (cbar_or1(!ok || vload(&s.abort))) break;
             give1(c);
@@ -1508,6 +1511,7 @@ __device__ void consumer1(const Prog& p, WsHeader* hdr, const Ws1& W, int step, 
             }
             down1(p, l, blk2, nh, lora, y + row0);
             cbar1();
+            stamp1(p, 0xE022);
             give1(c);
         } else {
             cbar1();

@@ -2131,6 +2131,13 @@ int engine_grid(int* nct) {
     return EDGE0_OK;
 }
 
+int engine_smem_max() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(g_grid_mutex);
+    return g_smem_max[dev];
+}
+
 // Derived launch fields for one set of shapes and grid: the pair-plan maxima over
 // every kind of layer (shared expert, LoRA, own router: all 8 combinations), the
 // ring that fits next to the fixed buffers, and the head flush's table size.

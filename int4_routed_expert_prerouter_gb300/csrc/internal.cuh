@@ -357,6 +357,8 @@ int engine_grid(int* nct);
 // fills p's derived fields for a grid of nct CTAs and checks the shapes against the
 // engine's limits; *smem_bytes <- dynamic shared memory.  0 or an EDGE0_* status.
 int engine_check(Prog& p, int nct, int smem_max, int* smem_bytes);
+// dynamic shared memory the engine can use on the current device (after engine_grid)
+int engine_smem_max();
 // launch the engine for `p` on `stream` (cooperative, CTA pairs); fills p's derived
 // fields.  Allocates nothing.
 int engine_launch(Prog& p, cudaStream_t stream);

@@ -76,9 +76,6 @@ extern "C" int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const u
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc) return rc;
-    // every call starts from a cleared header and cleared accumulators: the
-    // previous call may have used other shapes
-    if (cudaMemsetAsync(scratch, 0, (size_t)need, stream) != cudaSuccess) return EDGE0_ECUDA;
 
     Prog p;   // kernel parameter block, on the stack
     memset(&p, 0, sizeof(p));
@@ -110,5 +107,34 @@ extern "C" int edge0_moe_int4_forward_noalloc(const edge0_moe_desc* moe, const u
         P.flags = LF_SHARED;
     }
     P.n_groups = P.topk_groups = P.head_n_groups = P.head_topk_groups = 1;
+    // the shapes are checked before anything is queued: a refused call leaves
+    // the array (and a kernel still using it) alone
+    int nct = 0, smem = 0;
+    rc = engine_grid(&nct);
+    if (rc) return rc;
+    rc = engine_check(p, nct, engine_smem_max(), &smem);
+    if (rc) return rc;
+    // every call starts from a cleared header and cleared accumulators: the
+    // previous call may have used other shapes
+    if (cudaMemsetAsync(scratch, 0, (size_t)need, stream) != cudaSuccess) return EDGE0_ECUDA;
     return engine_launch(p, stream);
+}
+
+extern "C" int edge0_noalloc_error(cudaStream_t stream, int* status) {
+    if (!status) return EDGE0_EINVAL;
+    void* scratch = nullptr;
+    int rc = scratch_address(&scratch);
+    if (rc) return rc;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return EDGE0_ECUDA;
+    WsHeader h;
+    if (cudaMemcpyFromSymbol(&h, g_noalloc_scratch, sizeof(h), 0, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return EDGE0_ECUDA;
+    *status = h.error;
+    if (h.error || h.abort) {
+        h.error = 0;
+        h.abort = 0;
+        if (cudaMemcpyToSymbol(g_noalloc_scratch, &h, sizeof(h), 0, cudaMemcpyHostToDevice) != cudaSuccess)
+            return EDGE0_ECUDA;
+    }
+    return EDGE0_OK;
 }

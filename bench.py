@@ -18,6 +18,7 @@ Multi-GPU runs are independent replicas (no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import platform
 import hashlib
 import json
 import os
@@ -684,6 +685,26 @@ def _host_layers(model, n):
     return m
 
 
+def host_cpu():
+    """The host's hardware threads and CPU model (for the CPU-side records)."""
+    model = platform.processor() or platform.machine()
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+        names = [l.split(":", 1)[1].strip() for l in info if l.lower().startswith("model name")]
+        if names:
+            model = names[0]
+        else:   # Arm: implementer and part numbers
+            impl = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU implementer")]
+            part = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU part")]
+            known = {("0x41", "0xd4f"): "Arm Neoverse-V2", ("0x41", "0xd40"): "Arm Neoverse-V1",
+                     ("0x41", "0xd0c"): "Arm Neoverse-N1"}
+            if impl and part:
+                model = known.get((impl[0], part[0]), f"Arm implementer {impl[0]} part {part[0]}")
+    except OSError:
+        pass
+    return {"host_threads": os.cpu_count(), "cpu_model": f"{model} ({platform.machine()})"}
+
+
 def cpu_baseline(cpu_model, args):
     """The CPU oracle (single-threaded C++, fp64) on a bounded sample: decode
     steps of `cpu_layers` 35B-shaped layers (each with a head, prerouted from
@@ -700,7 +721,7 @@ def cpu_baseline(cpu_model, args):
         per_layer.append((time.perf_counter() - t0) / cfg.L)
     sec_per_layer = statistics.mean(per_layer[1:] if len(per_layer) > 1 else per_layer)
     tok_s = 1.0 / (sec_per_layer * CFG.L)
-    return {"value": round(tok_s, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return {"value": round(tok_s, 5), "unit": "tokens/s", "cores": 1, "kind": "oracle", **host_cpu(),
             "sample": f"{args.cpu_steps} decode steps of {cfg.L} 35B-tier layers (layers 6..{5 + cfg.L} "
                       f"of the stack, each with its head; first step excluded), "
                       f"{sec_per_layer:.3f} s per layer, scaled to {CFG.L} layers per token"}
@@ -738,7 +759,7 @@ def run_reference(args, rank):
             "config": {"workload": f"{CFG.name}: {CFG.description}", "batch": 1, "seq_len": 1,
                        "parallelism": "single host thread"},
             "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", **host_cpu(), "sample": sample},
             "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

@@ -108,6 +108,10 @@ typedef struct {
                                   device can read; an expert whose slot_table entry is -1
                                   is read from here.  NULL: no host tier.              */
     const void* host_down;
+    const void* down_rows;     /* down again in row-tile major units (edge0_pack_q4_rows),
+                                  experts stacked, or NULL: the batch-1 kernel reads
+                                  down by output row tiles from here               */
+    const void* sh_down_rows;  /* the shared expert's down, same layout, or NULL    */
 } edge0_moe_desc;
 
 /* ---- one unmerged LoRA projection [S3.3]: y += (alpha/r) B (A v) ---- */
@@ -115,7 +119,9 @@ typedef struct {
     int r, in, out;            /* rank (at most 16), input and output width            */
     float alpha;
     const void* A;             /* packed fp16 [r x in]  (edge0_pack_f16); used for the
-                                  shared expert's gate and up projections              */
+                                  shared expert's gate and up projections, and for its
+                                  down projection by the batch-1 decode kernel (which
+                                  is not used when lora_down.A is NULL)                */
     const uint16_t* A_T;       /* fp16 [in, r] = A transposed, row-major; used for the
                                   shared expert's down projection and edge0_lora_delta */
     const uint16_t* B;         /* fp16 [out, r] row-major                              */
@@ -154,8 +160,8 @@ typedef struct {
  *   (consumed at t + 1); exec_ids [2][L][B][K]: slot (t & 1) holds the ids each
  *   layer executed at step t (the head's executed mask at t, previous mask at t+1).
  * workspace: device scratch of edge0_workspace_bytes(L, B, d, E) bytes, zeroed by
- *   edge0_state_init before first use; it holds the layer-output and logit
- *   accumulators of two step parities, the grid barrier and the error word.  A
+ *   edge0_state_init before first use; it holds the layer outputs and logits of
+ *   two step parities, the launch counters and the error word.  A
  *   workspace belongs to one kind of call (decode on this state,
  *   edge0_moe_int4_forward, or edge0_prerouter_topk): calls of different kinds
  *   must not share one. */
@@ -185,6 +191,10 @@ int edge0_pack_q4_gate_up(const uint32_t* q_gate, const uint16_t* s_gate, const 
 size_t edge0_q4_down_packed_bytes(int E, int out, int in);
 /* q [E, out, in/8] uint32, s/b [E, out, in/64] fp16 -> K-major packed int4 */
 int edge0_pack_q4_down(const uint32_t* q, const uint16_t* s, const uint16_t* b, int E, int out,
+                       int in, void* packed, cudaStream_t stream);
+/* q [E, out, in/8] uint32, s/b [E, out, in/64] fp16 -> row-tile major int4 units
+ * [E][out/16][in/64][576] (edge0_q4_down_packed_bytes(E, out, in) bytes) */
+int edge0_pack_q4_rows(const uint32_t* q, const uint16_t* s, const uint16_t* b, int E, int out,
                        int in, void* packed, cudaStream_t stream);
 size_t edge0_f16_packed_bytes(int out, int in);
 /* W [out, in] fp16 with row stride ld elements (use ld > in for a column slice) */
@@ -260,9 +270,10 @@ int edge0_decode_layer(const edge0_layer_desc* layer, uint16_t* h_inout, edge0_r
 
 /* All L layers of one decode step (same semantics as L successive
  * edge0_decode_layer calls).  B == 1: one launch of the batch-1 kernel when the
- * shapes are within its limits (d <= 2048, d % 128 == 0, every layer with the
- * same shared-expert / LoRA parts, no slot table), else of the persistent
- * engine; B <= EDGE0_MAX_BATCH: one persistent launch;
+ * shapes are within its limits (d <= 2048, d % 128 == 0, K I + Is <= 4608,
+ * every layer with the same shared-expert / LoRA parts, down_rows (and
+ * sh_down_rows, lora_down.A) given, no slot table, one layer per state row),
+ * else of the persistent engine; B <= EDGE0_MAX_BATCH: one persistent launch;
  * EDGE0_MAX_BATCH < B <= EDGE0_MAX_BATCHED: the batched path, a sequence of
  * kernels per layer in which every active expert's weights are read once for
  * all of its tokens, then every head of the step; it needs step >= 0 and a

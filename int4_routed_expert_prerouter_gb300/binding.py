@@ -48,7 +48,8 @@ class Route(C.Structure):
 class MoeDesc(C.Structure):
     _fields_ = [("d", C.c_int), ("E", C.c_int), ("K", C.c_int), ("I", C.c_int), ("Is", C.c_int),
                 ("gate_up", P), ("down", P), ("sh_gate_up", P), ("sh_down", P),
-                ("slot_table", P), ("n_slots", C.c_int), ("host_gate_up", P), ("host_down", P)]
+                ("slot_table", P), ("n_slots", C.c_int), ("host_gate_up", P), ("host_down", P),
+                ("down_rows", P), ("sh_down_rows", P)]
 
 
 class LoraDesc(C.Structure):
@@ -84,6 +85,7 @@ def _declare(L):
     L.edge0_q4_down_packed_bytes.argtypes = [C.c_int] * 3
     L.edge0_q4_down_packed_bytes.restype = C.c_size_t
     L.edge0_pack_q4_down.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, P, P]
+    L.edge0_pack_q4_rows.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, P, P]
     L.edge0_f16_packed_bytes.argtypes = [C.c_int] * 2
     L.edge0_f16_packed_bytes.restype = C.c_size_t
     L.edge0_pack_f16.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
@@ -114,7 +116,7 @@ def _declare(L):
                                      C.c_int, P]
     L.edge0_decode_step.argtypes = [C.POINTER(LayerDesc), C.c_int, P, C.POINTER(RouteState),
                                     C.c_int, C.c_int, P]
-    for name in ("edge0_pack_q4_gate_up", "edge0_pack_q4_down", "edge0_pack_f16",
+    for name in ("edge0_pack_q4_gate_up", "edge0_pack_q4_down", "edge0_pack_q4_rows", "edge0_pack_f16",
                  "edge0_pack_f16_kmajor", "edge0_pack_cols_T", "edge0_state_init",
                  "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
                  "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
@@ -123,7 +125,7 @@ def _declare(L):
 
 
 EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_q4_gate_up",
-            "edge0_q4_down_packed_bytes", "edge0_pack_q4_down", "edge0_f16_packed_bytes",
+            "edge0_q4_down_packed_bytes", "edge0_pack_q4_down", "edge0_pack_q4_rows", "edge0_f16_packed_bytes",
             "edge0_pack_f16", "edge0_pack_f16_kmajor", "edge0_pack_cols_T",
             "edge0_workspace_bytes", "edge0_decode_workspace_bytes", "edge0_state_init",
             "edge0_state_error", "edge0_state_set_wait_limit", "edge0_prerouter_topk", "edge0_moe_int4_forward",
@@ -174,6 +176,18 @@ def pack_q4_down(trip, stream=None) -> torch.Tensor:
     dst = torch.empty(n, dtype=torch.uint8, device=q.device)
     _check(lib().edge0_pack_q4_down(_ptr(q), _ptr(s), _ptr(b), E, out, inp, _ptr(dst), _stream(stream)),
            "edge0_pack_q4_down")
+    return dst
+
+
+def pack_q4_rows(trip, stream=None) -> torch.Tensor:
+    """(q [E, out, in/8] int32, s, b [E, out, in/64] fp16) -> row-tile major int4 units (uint8)."""
+    q, s, b = (t.contiguous() for t in trip)
+    E, out, w8 = q.shape
+    inp = w8 * 8
+    n = lib().edge0_q4_down_packed_bytes(E, out, inp)
+    dst = torch.empty(n, dtype=torch.uint8, device=q.device)
+    _check(lib().edge0_pack_q4_rows(_ptr(q), _ptr(s), _ptr(b), E, out, inp, _ptr(dst), _stream(stream)),
+           "edge0_pack_q4_rows")
     return dst
 
 
@@ -248,7 +262,10 @@ class DeviceModel:
                         _ptr(self.stacks[l][1]),
                         self._k(pack_q4_gate_up(gt(lw.sh_gate), gt(lw.sh_up), stream)),
                         self._k(pack_q4_down(gt(lw.sh_down), stream)),
-                        None, 0)
+                        None, 0, None, None,
+                        # down by output row tiles, for the batch-1 decode kernel
+                        self._k(pack_q4_rows(gt(lw.down), stream)),
+                        self._k(pack_q4_rows(gt(lw.sh_down), stream)))
         lo = lw.lora
         alpha = float(cfg.alpha)
         lora = lambda A, Bm, inp, out: LoraDesc(

@@ -9,7 +9,7 @@ using namespace edge0;
 
 namespace {
 
-bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }   // (null counts as aligned)
 
 struct Dims {
     int d, E, K, I, Is, H, r;
@@ -59,6 +59,9 @@ int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P)
     if (m.host_gate_up && (!m.slot_table || !al16(m.host_gate_up) || !al16(m.host_down))) return EDGE0_EINVAL;
     P.gu_host = (const char*)m.host_gate_up;
     P.down_host = (const char*)m.host_down;
+    if (!al16(m.down_rows) || !al16(m.sh_down_rows)) return EDGE0_EINVAL;
+    P.down_rows = (const char*)m.down_rows;
+    P.sh_down_rows = (const char*)m.sh_down_rows;
     P.ready = (void*)Ld.ready;
     P.router = (const char*)Ld.router;
     P.gamma = (const __half*)Ld.gamma;
@@ -85,11 +88,13 @@ int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P)
             ld.out != D.d)
             return EDGE0_EINVAL;
         if (lg.alpha != lu.alpha || lg.alpha != ld.alpha) return EDGE0_EINVAL;
-        if (!al16(lg.A) || !al16(lu.A) || !al16(ld.A_T) || !al16(lg.B) || !al16(lu.B) || !al16(ld.B))
+        if (!al16(lg.A) || !al16(lu.A) || !al16(ld.A_T) || !al16(lg.B) || !al16(lu.B) || !al16(ld.B) ||
+            !al16(ld.A))
             return EDGE0_EINVAL;
         P.lora_Ag = (const char*)lg.A;
         P.lora_Au = (const char*)lu.A;
         P.lora_AdT = (const __half*)ld.A_T;
+        P.lora_Ad = (const char*)ld.A;   // optional: the batch-1 kernel needs it
         P.lora_Bg = (const __half*)lg.B;
         P.lora_Bu = (const __half*)lu.B;
         P.lora_Bd = (const __half*)ld.B;
@@ -214,24 +219,19 @@ extern "C" const char* edge0_status_string(int status) {
     }
 }
 
-// one sequence: room for the batch-1 kernel's layout too
-static long long persistent_ws_bytes(int L, int B, int d, int E) {
-    long long n = ws_layout(L, B, d, E).total;
-    if (B == 1) {
-        const long long n1 = decode1_ws_bytes(L, d, E);
-        if (n1 > n) n = n1;
-    }
-    return n;
-}
-
 extern "C" size_t edge0_workspace_bytes(int L, int B, int d, int E) {
     if (L <= 0 || B <= 0 || d <= 0 || E <= 0) return 0;
-    return (size_t)persistent_ws_bytes(L, B, d, E);
+    return (size_t)ws_layout(L, B, d, E).total;
 }
 
 extern "C" size_t edge0_decode_workspace_bytes(int L, int B, int d, int E, int K, int I, int Is, int H) {
     if (L <= 0 || B <= 0 || d <= 0 || E <= 0 || K <= 0 || I <= 0 || Is <= 0 || H <= 0) return 0;
-    if (B <= EDGE0_MAX_BATCH) return (size_t)persistent_ws_bytes(L, B, d, E);
+    if (B == 1) {
+        // one sequence: room for the batch-1 kernel's layout too
+        const long long n = ws_layout(L, B, d, E).total, n1 = decode1_ws_bytes(L, d, E, K, I, Is);
+        return (size_t)(n > n1 ? n : n1);
+    }
+    if (B <= EDGE0_MAX_BATCH) return (size_t)ws_layout(L, B, d, E).total;
     if (B > EDGE0_MAX_BATCHED) return 0;
     return (size_t)batch_ws_layout(L, B, d, E, K, I > Is ? I : Is, H).total;
 }

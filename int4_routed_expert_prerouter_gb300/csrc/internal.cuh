@@ -52,10 +52,13 @@ struct LayerP {
     int n_slots;
     const char* gu_host;     // host tier: all experts (slot -1), batched path only
     const char* down_host;
+    const char* down_rows;   // down in row-tile major units (batch-1 kernel), or null
+    const char* sh_down_rows;
     void* ready;             // host: event the batched path waits for before the layer
     const char* router;      // packed fp16 [E x d]
     const char* lora_Ag;     // packed fp16 [r x d] (one row tile)
     const char* lora_Au;
+    const char* lora_Ad;     // packed fp16 [r x Is] (one row tile), or null
     const __half* lora_AdT;  // [Is, r]: A_down transposed
     const __half* lora_Bg;   // [Is, r]
     const __half* lora_Bu;
@@ -123,8 +126,10 @@ struct WsHeader {
     int error;                    // EDGE0_* status recorded by a kernel
     int abort;                    // set with error: every wait gives up
     int trace;                    // non-zero: record phase timestamps in the trace area
-    int hold;                     // test hook: arrivals the first grid barrier of a launch
-                                  // waits for beyond the grid (> 0: it cannot complete)
+    int hold;                     // test hook (> 0): the first wait of each CTA of a launch
+                                  // cannot complete (the engine's first grid barrier waits
+                                  // for arrivals beyond the grid, the batch-1 kernel's first
+                                  // poll for a tag that is never written)
     unsigned long long wait_ns;   // limit of every bounded wait (0: kDefaultWaitNs)
     unsigned long long barrier_r; // arrival counter of the batch-1 kernel's router barriers
 };
@@ -279,6 +284,12 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// two single-copy-atomic 64-bit loads at GPU scope (16-byte aligned pair)
+__device__ __forceinline__ ulonglong2 ld_relaxed_u64x2(const unsigned long long* p) {
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];\n" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" :::
                      "memory");
@@ -343,8 +354,8 @@ constexpr float kLoInv = 1.0f / 2048.0f;
 constexpr float kTwo24 = 16777216.0f;   // int4 nibbles enter the tensor cores as q * 2^-24
 
 // batch-1 decode kernel (decode1.cu): one launch per decode step of B = 1
-// workspace bytes it needs for Ls state rows (0 if the shapes exceed its limits)
-long long decode1_ws_bytes(int Ls, int d, int E);
+// workspace bytes it needs for Ls state rows
+long long decode1_ws_bytes(int Ls, int d, int E, int K, int I, int Is);
 // fills p's batch-1 fields for the current device and checks that the kernel
 // takes the call (EDGE0_OK) or not (EDGE0_EUNSUPPORTED: use the engine)
 int decode1_check(Prog& p);

@@ -26,6 +26,8 @@
 //            per row tile of the half (step major), then the half's 64-byte
 //            scale/bias blocks; one 16-input slice of the intermediate over a
 //            half of the output rows is contiguous.
+//   rows     [E][out/16 row tiles][in/64 groups][576]: the gate/up unit format with
+//            the rows in order (down, for the batch-1 kernel's output row tiles).
 //   fp16     [half][out/16 row tiles][groups of the half][4 steps][512] (row
 //            tiles x input groups; every matrix that multiplies x) or
 //            [in/16 steps][out/16 row tiles][512] (K-major, for the head's fc2).
@@ -122,6 +124,43 @@ __global__ void pack_down_kernel(const uint32_t* __restrict__ q, const uint16_t*
     }
 }
 
+// int4 row-tile major: [E][row tile][group][576] (the unit format of gate/up,
+// rows in order); one thread per (expert, row tile, group, lane)
+__global__ void pack_rows_kernel(const uint32_t* __restrict__ q, const uint16_t* __restrict__ s,
+                                 const uint16_t* __restrict__ b, int E, int out, int in,
+                                 char* __restrict__ dst) {
+    const int n_rt = ceil_div(out, kRowTile), n_g = in / kGroup;
+    const long long units = (long long)E * n_rt * n_g;
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid >= units * 32) return;
+    const int lane = (int)(tid & 31);
+    const long long unit = tid >> 5;
+    const int c = (int)(unit % n_g);
+    const int i = (int)((unit / n_g) % n_rt);
+    const int e = (int)(unit / ((long long)n_g * n_rt));
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = i * kRowTile + g, r1 = r0 + 8;
+    const long long wpr = in / 8, gpr = in / kGroup;
+    const uint32_t* w0 = r0 < out ? q + ((long long)e * out + r0) * wpr : nullptr;
+    const uint32_t* w1 = r1 < out ? q + ((long long)e * out + r1) * wpr : nullptr;
+    uint4 v;
+    v.x = step_word(w0, w1, kGroup * c + 0, t);
+    v.y = step_word(w0, w1, kGroup * c + 16, t);
+    v.z = step_word(w0, w1, kGroup * c + 32, t);
+    v.w = step_word(w0, w1, kGroup * c + 48, t);
+    char* u = dst + unit * kQ4Unit;
+    *reinterpret_cast<uint4*>(u + 16 * lane) = v;
+    if (t == 0) {
+        ushort4 sb;
+        const long long o0 = ((long long)e * out + r0) * gpr + c, o1 = ((long long)e * out + r1) * gpr + c;
+        sb.x = r0 < out ? s[o0] : 0;
+        sb.y = r0 < out ? b[o0] : 0;
+        sb.z = r1 < out ? s[o1] : 0;
+        sb.w = r1 < out ? b[o1] : 0;
+        *reinterpret_cast<ushort4*>(u + 512 + 8 * g) = sb;
+    }
+}
+
 // fp16 step block of lane (g, t) for row tile i, inputs k0 + {2t, 2t+1, 2t+8, 2t+9}
 __device__ __forceinline__ uint4 f16_block(const uint16_t* W, int out, int ld, int i, int k0, int g, int t) {
     const int r0 = i * kRowTile + g, r1 = r0 + 8, k = k0 + 2 * t;
@@ -210,6 +249,17 @@ extern "C" int edge0_pack_q4_down(const uint32_t* q, const uint16_t* s, const ui
         return EDGE0_EINVAL;
     const long long threads = (long long)E * (in / kGroup) * ceil_div(out, kRowTile) * 32;
     pack_down_kernel<<<launch_1d(threads), 256, 0, stream>>>(q, s, b, E, out, in, (char*)packed);
+    return cudaGetLastError() == cudaSuccess ? EDGE0_OK : EDGE0_ECUDA;
+}
+
+extern "C" int edge0_pack_q4_rows(const uint32_t* q, const uint16_t* s, const uint16_t* b, int E,
+                                  int out, int in, void* packed, cudaStream_t stream) {
+    if (!q || !s || !b || !packed || E <= 0 || out <= 0 || in <= 0 || in % kGroup)
+        return EDGE0_EINVAL;
+    if (!aligned(q, 4) || !aligned(s, 2) || !aligned(b, 2) || !aligned(packed, 16))
+        return EDGE0_EINVAL;
+    const long long threads = (long long)E * ceil_div(out, kRowTile) * (in / kGroup) * 32;
+    pack_rows_kernel<<<launch_1d(threads), 256, 0, stream>>>(q, s, b, E, out, in, (char*)packed);
     return cudaGetLastError() == cudaSuccess ? EDGE0_OK : EDGE0_ECUDA;
 }
 

@@ -1,11 +1,13 @@
 // Host-side check of the batch-1 decode kernel's work split (no GPU needed): for
 // several shapes and grids, every CTA's plan and block layouts as the kernel
-// builds them.  Checked: every half-row tile of every routed slot and of the
-// shared expert is owned by exactly one pair; every router unit of each half of
-// d and every head-flush task by exactly one CTA; every copy lies inside its
-// source matrix, starts and ends on 16 bytes and stays inside its block; every
-// block fits the ring; the act steps of each run cover its rows; the down parts
-// of each run cover its steps once, inside their group.
+// builds them.  Checked: every pair but the LoRA pair owns half-row tiles, and
+// every half-row tile of every routed slot and of the shared expert is owned by
+// exactly one pair; the act rows the two CTAs of the pairs publish cover the
+// layer's act vector exactly once; every output row tile and router row tile
+// has exactly one CTA, every head-flush task exactly one; every copy lies
+// inside its source matrix, starts and ends on 16 bytes and stays inside its
+// block; the down block holds one unit per act group, in act order; every block
+// fits the ring.
 // Compiled and run by tests/test_decode1_plan.py; exits non-zero on a failure.
 #include "decode1.cu"
 
@@ -32,9 +34,10 @@ static long long src_size(const Shape1& S, const Plan1& pl, const Piece1& pc) {
     switch (pc.kind) {
         case K1_ROUTER: return f16_bytes(S.E, S.d);
         case K1_GU: return q4_bytes(2 * (pl.seg[pc.seg].slot < 0 ? S.Is : S.I), S.d);
-        case K1_DOWN: return q4_bytes(S.d, pl.seg[pc.seg].slot < 0 ? S.Is : S.I);
+        case K1_DOWN: return q4_bytes(S.d, pc.seg < 0 ? S.Is : S.I);
         case K1_LA: case K1_LU: return f16_bytes(S.r, S.d);
-        case K1_BG: case K1_BU: case K1_ADT: return 2LL * S.Is * S.r;
+        case K1_BG: case K1_BU: return 2LL * S.Is * S.r;
+        case K1_AD: return f16_bytes(S.r, S.Is);
         case K1_BD: return 2LL * S.d * S.r;
         case K1_FC1: return f16_bytes(S.H, S.d);
         case K1_FC2: return f16_bytes(S.E, S.H);
@@ -61,25 +64,25 @@ static void check_block(const Shape1& S, const Plan1& pl, const Block1& B, int r
 }
 
 static void check_shape(const char* name, int d, int E, int K, int I, int Is, int H, int r, bool shared, bool lora,
-                        int n_heads, int nct) {
+                        int n_heads, int nct, bool must) {
     Key1 k;
     memset(&k, 0, sizeof(k));
     k.d = d; k.I = I; k.Is = Is; k.E = E; k.K = K; k.H = H; k.r = r;
     k.shared = shared; k.lora = lora; k.n_heads = n_heads; k.nct = nct;
     k.smem = 232448 - 1024;
     const int rc = derive1(k);
-    printf("%-30s nct=%d rc=%d pairs %d = %d routed + %d shared + %d lora, ring %d\n", name, nct, rc, k.P, k.Pr,
+    printf("%-30s grid %3d rc=%d pairs %d = %d routed + %d shared + %d lora, ring %d\n", name, nct, rc, k.P, k.Pr,
            k.Ps, k.Pl, k.ring);
-    CHECK(rc == 0 || nct < 148, "%s: the full grid must take the shape (rc %d)", name, rc);
+    CHECK(rc == 0 || !must, "%s: the grid must take the shape (rc %d)", name, rc);
     if (rc) return;
+    CHECK(k.P <= nct / 2, "%s: more pairs than the grid", name);
     Shape1 S;
     S.d = d; S.I = I; S.Is = Is; S.E = E; S.K = K; S.H = H; S.r = r;
     S.shared = shared; S.lora = lora; S.n_heads = n_heads;
     S.P = k.P; S.Pr = k.Pr; S.Ps = k.Ps; S.Pl = k.Pl;
-    const int hpe = I / 8, n_sh = shared ? Is / 8 : 0;
-    std::vector<int> cov_rt(K * hpe, 0), cov_sh(n_sh, 0);
-    std::vector<int> cov_ru[2] = {std::vector<int>((E / 16) * ngh1(d, 0), 0),
-                                  std::vector<int>((E / 16) * ngh1(d, 1), 0)};
+    S.nct = 2 * k.P;
+    const int hpe = I / 8, n_sh = shared ? Is / 8 : 0, NA = n_act1(S);
+    std::vector<int> cov_rt(K * hpe, 0), cov_sh(n_sh, 0), cov_act(NA, 0), cov_dt(d / 16, 0), cov_r(E / 16, 0);
     const int tph = H / 16 + E / 16;
     std::vector<int> cov_task(n_heads * tph, 0);
     int n_lora = 0;
@@ -91,6 +94,7 @@ static void check_shape(const char* name, int d, int E, int K, int I, int Is, in
             CHECK(ok, "%s pair %d rank %d: plan/layout refused", name, pair, rank);
             if (!ok) continue;
             if (pl.role == R1_LORA) n_lora += rank == 0;
+            CHECK(pl.role == R1_LORA || pl.n_hr >= 1, "%s pair %d owns no hr", name, pair);
             CHECK(pl.n_hr <= kMaxHr1, "n_hr %d", pl.n_hr);
             int nh = 0;
             for (int s = 0; s < pl.nseg; ++s) {
@@ -103,49 +107,56 @@ static void check_shape(const char* name, int d, int E, int K, int I, int Is, in
                     if (sg.slot < 0) { CHECK(h < n_sh, "shared hr %d", h); if (h < n_sh) ++cov_sh[h]; }
                     else { CHECK(sg.slot < K && h < hpe, "slot %d hr %d", sg.slot, h); if (sg.slot < K && h < hpe) ++cov_rt[sg.slot * hpe + h]; }
                 }
-                // act steps of the run: its steps in order, consecutive
-                int first = -1, cnt = 0;
-                for (int sg2 = 0; sg2 < L.nsig; ++sg2)
-                    if (L.sig_seg[sg2] == s) {
-                        if (first < 0) first = sg2;
-                        CHECK(L.sig_step[sg2] == sg.hr0 / 2 + cnt, "sigma step");
-                        ++cnt;
-                    }
-                CHECK(cnt == (sg.hr1 - 1) / 2 - sg.hr0 / 2 + 1, "sigma count");
-                // down parts of the run: its steps once, each part inside one group
-                std::vector<int> seen(cnt, 0);
-                for (int pi = 0; pi < L.nparts; ++pi) {
-                    const Part1& P = L.part[pi];
-                    if (P.seg != s) continue;
-                    CHECK(P.sa / 4 == P.sb / 4 && P.sa <= P.sb, "part crosses a group");
-                    CHECK(P.sig0 == first + (P.sa - sg.hr0 / 2), "part sigma");
-                    for (int st = P.sa; st <= P.sb; ++st) {
-                        const int j = st - sg.hr0 / 2;
-                        CHECK(j >= 0 && j < cnt, "part step");
-                        if (j >= 0 && j < cnt) ++seen[j];
-                    }
-                    const int nhr = nrth1(d, rank);
-                    CHECK(P.words + (P.sb - P.sa + 1) * nhr * 128 <= L.b2.bytes, "part words outside the block");
-                    CHECK(P.scales + nhr * 64 <= L.b2.bytes, "part scales outside the block");
-                }
-                for (int j = 0; j < cnt; ++j) CHECK(seen[j] == 1, "down step covered %d times", seen[j]);
             }
             CHECK(nh == pl.n_hr, "n_hr");
-            CHECK(8 * pl.n_hr <= 64, "act rows");
-            for (int u = pl.ru0; u < pl.ru1; ++u) ++cov_ru[rank][u];
+            // the act rows this CTA publishes (as act1 maps its threads)
+            for (int i = 0; i < 8 * pl.n_hr; ++i) {
+                if ((i & 1) != rank) continue;
+                int sg = 0;
+                while (sg + 1 < pl.nseg && i >= L.seg_base[sg + 1]) ++sg;
+                const Seg1& seg = pl.seg[sg];
+                const int row = 8 * seg.hr0 + i - L.seg_base[sg];
+                const long long gi = (seg.slot >= 0 ? (long long)seg.slot * I : (long long)K * I) + row;
+                CHECK(gi >= 0 && gi < NA, "act index %lld", gi);
+                if (gi >= 0 && gi < NA) ++cov_act[gi];
+            }
+            const int cta = 2 * pair + rank;
+            if (pl.dt >= 0) { CHECK(pl.dt == cta && pl.dt < d / 16, "dt %d", pl.dt); ++cov_dt[pl.dt]; }
+            if (pl.rt >= 0) { CHECK(pl.rt < E / 16, "rt %d", pl.rt); ++cov_r[pl.rt]; }
             for (int t = pl.t0; t < pl.t1; ++t) ++cov_task[t];
-            check_block(S, pl, L.b0, k.ring, "P0");
-            check_block(S, pl, L.b1, k.ring, "P1");
-            check_block(S, pl, L.b2, k.ring, "P2");
-            // gate/up units of the block: n_hr x groups of the half, 576 bytes each
-            if (pl.role != R1_LORA) CHECK(L.b1.bytes == pl.n_hr * ngh1(d, rank) * 576, "P1 bytes");
-            if (pl.role == R1_LORA)
-                CHECK(L.b1.bytes == (d / 64) * 2048 && L.b2.bytes == 0, "LoRA pair blocks");
+            check_block(S, pl, L.b0, k.ring, "b0");
+            check_block(S, pl, L.b1, k.ring, "b1");
+            check_block(S, pl, L.b3, k.ring, "b3");
+            check_block(S, pl, L.b2, k.ring, "b2");
+            CHECK(L.b0.bytes == (pl.rt >= 0 ? (d / 64) * 2048 : 0), "b0 bytes");
+            if (pl.role != R1_LORA) CHECK(L.b1.bytes == pl.n_hr * ngh1(d, rank) * 576, "b1 bytes");
+            else CHECK(L.b1.bytes == (d / 64) * 2048 && L.b3.bytes == 0, "LoRA pair blocks");
+            CHECK(L.b3.bytes == ((pl.role == R1_SHARED && lora) ? 2 * 16 * r * pl.n_hr : 0), "b3 bytes");
+            if (pl.dt >= 0) {
+                // one unit per act group, in act order, then (LoRA) A_down and B_down rows
+                int u = 0;
+                for (int i = 0; i < L.b2.n; ++i) {
+                    const Piece1& pc = L.b2.pc[i];
+                    if (pc.kind != K1_DOWN) continue;
+                    CHECK(pc.dst == u * 576, "down unit %d at %d", u, pc.dst);
+                    const int per = (pc.seg < 0 ? Is : I) / 64;
+                    CHECK(pc.src == (long long)pl.dt * per * 576, "down tile source");
+                    CHECK(pc.seg == (u < K * (I / 64) ? u / (I / 64) : -1), "down unit %d slot %d", u, pc.seg);
+                    u += pc.bytes / 576;
+                }
+                CHECK(u == NA / 64, "down units %d != %d", u, NA / 64);
+                if (lora) CHECK(L.ad == u * 576 && L.bd == L.ad + (Is / 64) * 2048 && L.b2.bytes == L.bd + 32 * r,
+                                "LoRA down parts");
+                else CHECK(L.b2.bytes == u * 576, "b2 bytes");
+            } else {
+                CHECK(L.b2.bytes == 0, "b2 without a tile");
+            }
         }
     for (size_t i = 0; i < cov_rt.size(); ++i) CHECK(cov_rt[i] == 1, "%s routed hr %zu covered %d", name, i, cov_rt[i]);
     for (size_t i = 0; i < cov_sh.size(); ++i) CHECK(cov_sh[i] == 1, "%s shared hr %zu covered %d", name, i, cov_sh[i]);
-    for (int h = 0; h < 2; ++h)
-        for (size_t i = 0; i < cov_ru[h].size(); ++i) CHECK(cov_ru[h][i] == 1, "router unit %d/%zu: %d", h, i, cov_ru[h][i]);
+    for (size_t i = 0; i < cov_act.size(); ++i) CHECK(cov_act[i] == 1, "%s act %zu published %d times", name, i, cov_act[i]);
+    for (size_t i = 0; i < cov_dt.size(); ++i) CHECK(cov_dt[i] == 1, "%s output tile %zu: %d", name, i, cov_dt[i]);
+    for (size_t i = 0; i < cov_r.size(); ++i) CHECK(cov_r[i] == 1, "%s router tile %zu: %d", name, i, cov_r[i]);
     for (size_t i = 0; i < cov_task.size(); ++i) CHECK(cov_task[i] == 1, "task %zu: %d", i, cov_task[i]);
     CHECK(n_lora == (lora ? 1 : 0), "LoRA pairs %d", n_lora);
     // flush blocks with the one-hot rows of the extreme columns (0 and 2E - 1)
@@ -174,16 +185,19 @@ static void check_shape(const char* name, int d, int E, int K, int I, int Is, in
 }
 
 int main() {
+    printf("shared-memory state %d bytes\n", kSm1Bytes);
     const int grids[] = {152, 148, 76, 32};
     for (int nct : grids) {
-        check_shape("35B stack (33 heads)", 2048, 256, 4, 512, 512, 512, 16, true, true, 33, nct);
-        check_shape("35B layer ring", 2048, 256, 4, 512, 512, 512, 16, true, true, 1, nct);
-        check_shape("toy", 256, 16, 2, 128, 128, 64, 4, true, true, 1, nct);
-        check_shape("35B no LoRA", 2048, 256, 4, 512, 512, 512, 16, true, false, 2, nct);
-        check_shape("35B no shared", 2048, 256, 4, 512, 512, 512, 16, false, false, 0, nct);
-        check_shape("8B shapes E=32 K=8", 1536, 32, 8, 512, 512, 512, 16, true, true, 2, nct);
-        check_shape("d=1536 K=2", 1536, 64, 2, 512, 256, 256, 8, true, true, 3, nct);
-        check_shape("35B E=16 (small)", 2048, 16, 4, 512, 512, 512, 16, true, true, 1, nct);
+        const bool big = nct >= 128;
+        check_shape("35B stack (33 heads)", 2048, 256, 4, 512, 512, 512, 16, true, true, 33, nct, big);
+        check_shape("35B layer ring", 2048, 256, 4, 512, 512, 512, 16, true, true, 1, nct, big);
+        check_shape("toy", 256, 16, 2, 128, 128, 64, 4, true, true, 1, nct, true);
+        check_shape("35B no LoRA", 2048, 256, 4, 512, 512, 512, 16, true, false, 2, nct, big);
+        check_shape("35B no shared", 2048, 256, 4, 512, 512, 512, 16, false, false, 0, nct, big);
+        check_shape("8B shapes E=32 K=8", 1536, 32, 8, 512, 512, 512, 16, true, true, 2, nct, nct >= 96);
+        check_shape("d=1536 K=2", 1536, 64, 2, 512, 256, 256, 8, true, true, 3, nct, nct >= 96);
+        check_shape("35B E=16 (small)", 2048, 16, 4, 512, 512, 512, 16, true, true, 1, nct, big);
+        check_shape("35B E=32 L=1 (no heads)", 2048, 32, 4, 512, 512, 512, 16, true, true, 0, nct, big);
     }
     if (fails) {
         printf("%d FAILURES\n", fails);

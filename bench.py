@@ -227,10 +227,9 @@ def run_gpu(args, rank, world):
         st.set_trace(False)
         tr = st.read_trace()
         nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-        print_trace(tr, nsm)
         own = [l for l in range(cfg.L) if l not in cfg.prerouted]
         pre = list(cfg.prerouted)
-        print_trace_roles(tr, nsm, cfg, ([pre[len(pre) // 2]] if pre else []) + (own[-1:] if own else []))
+        print_trace(tr, nsm, ([pre[len(pre) // 2]] if pre else []) + (own[1:2] if len(own) > 1 else own))
         if args.trace_file:
             np.savez_compressed(args.trace_file, consumer=tr[0].numpy(), producer=tr[1].numpy())
     # device-resident timed region: one event pair per launch for the kernel
@@ -544,123 +543,53 @@ def run_batched(args, rank, world, cfg):
     return line
 
 
-def print_trace(tr, nct, sm_mhz=2070.0):
-    """Per-layer split of one traced decode step, averaged over CTAs (durations
-    from each SM's cycle counter): barrier wait and x, own routing, gate/up,
-    pair exchange, act, down (to the barrier arrival); the act and down phases
-    split further; the producer's timeline relative to the consumer's layer
-    start (globaltimer); then the head flush after the last layer (x fragments,
-    fc1/linear_init units, fc2, count and top-K, summed over a CTA's tables)."""
-    import collections
-    cons, prod = tr
-    names = ("wait+x", "route", "gate/up", "xchg", "act", "down")
-    acc = collections.defaultdict(list)
-    sub = collections.defaultdict(list)
-    rel = collections.defaultdict(list)
-    flush = []
-    us = lambda cyc: cyc / sm_mhz
-    for c in range(nct):
-        ev, evt = {}, {}
-        for tag, tm, cy in cons[c].tolist():
-            if tm != 0:
-                ev[tag] = cy
-                evt[tag] = tm
-        pev = {}
-        for tag, tm, cy in prod[c].tolist():
-            if tm != 0:
-                pev[tag] = tm
-        for l in sorted({k >> 8 for k in ev if (k & 0xFF) == 0}):
-            pts = [ev.get((l << 8) | i) for i in range(7)]
-            if None in pts:
-                continue
-            acc[l].append(tuple(us(pts[i + 1] - pts[i]) for i in range(6)))
-            x = [ev.get((l << 8) | k) for k in (4, 10, 11, 5, 9, 12, 6)]
-            if None not in x:
-                sub[l].append(tuple(us(x[i + 1] - x[i]) for i in range(6)))
-            t0 = evt[(l << 8) | 0]
-            r = [pev.get((l << 8) | k) for k in (0x80, 0x81, 0x83)]
-            if None not in r:
-                rel[l].append(tuple((v - t0) / 1e3 for v in r))
-        tails = [k for k in ev if (k & 0xFF) == 7]
-        tabs = sorted({k >> 8 for k in ev if (k & 0xFF) == 23})
-        if tails and tabs:
-            prev = ev[max(tails)]
-            parts = [0.0] * 4
-            for t in tabs:
-                pts = [ev.get((t << 8) | k) for k in (20, 21, 22, 23)]
-                if None in pts:
-                    continue
-                seg = [pts[0] - prev] + [pts[i + 1] - pts[i] for i in range(3)]
-                parts = [a + us(b) for a, b in zip(parts, seg)]
-                prev = pts[3]
-            flush.append(parts + [sum(parts)])
-    tot = [0.0] * 6
-    lines = []
-    subn = ("act:zero", "act:rows", "act:tail", "dn:wait", "dn:rows", "dn:release")
-    for l in sorted(acc):
-        v = acc[l]
-        m = [statistics.mean(x[i] for x in v) for i in range(6)]
-        mx = [max(x[i] for x in v) for i in range(6)]
-        tot = [a + b for a, b in zip(tot, m)]
-        extra = ""
-        if sub[l]:
-            extra += " | " + " ".join(f"{n} {statistics.mean(x[i] for x in sub[l]):.2f}" for i, n in enumerate(subn))
-        if rel[l]:
-            extra += " | producer " + " ".join(f"{n} {statistics.mean(x[i] for x in rel[l]):+.1f}"
-                                              for i, n in enumerate(("tab0", "tab1", "issued")))
-        lines.append(f"layer {l:2d}: " + " ".join(f"{n} {a:5.2f}/{b:5.2f}" for n, a, b in zip(names, m, mx))
-                     + " us (mean/max)" + extra)
-    if flush:
-        fn = ("x", "units", "fc2", "count+topk", "total")
-        lines.append("head flush: " + " ".join(
-            f"{n} {statistics.mean(f[i] for f in flush):5.2f}/{max(f[i] for f in flush):5.2f}"
-            for i, n in enumerate(fn)) + " us (mean/max over CTAs)")
-    sys.stderr.write("\n".join(lines) + "\n")
-    sys.stderr.write("total (mean over CTAs): " + " ".join(f"{n} {a:.1f}" for n, a in zip(names, tot)) + " us\n")
+TRACE_POINTS = {0: "start", 0x21: "y in", 2: "x", 4: "routing", 9: "b1 ready", 0x27: "gate/up MMAs",
+                5: "gate/up", 7: "act out", 10: "b2 ready", 0x25: "down MMAs", 8: "y out"}
 
 
-def _shared_pairs(P, n_sh, n_rt, lora):
-    """How many CTA pairs own shared-expert rows: a restatement of the engine's
-    cost model, used here only to label the trace's CTAs by role."""
-    if n_sh <= 0:
-        return 0
-    if n_rt <= 0:
-        return P
-    best, pick = 1 << 30, 1
-    for ps in range(1, P):
-        cs = -(-n_sh // ps) * 24 + (20 if lora else 0)
-        cr = -(-n_rt // (P - ps)) * 24
-        if max(cs, cr) <= best:
-            best, pick = max(cs, cr), ps
-    return pick
-
-
-def print_trace_roles(tr, nct, cfg, layers, sm_mhz=2070.0):
-    """For the given layers, the mean duration (SM cycle counter) of each phase
-    from the grid barrier seen to the next arrival, separately for the CTAs of
-    the pairs that own shared-expert rows (and carry the LoRA) and the routed
-    pairs; own-routed layers also split their router phase."""
+def print_trace(tr, nct, layers, sm_mhz=2070.0):
+    """One traced decode step of the batch-1 kernel.  For the given layers, the
+    segments between consecutive trace points of each CTA (SM cycle counter),
+    mean and max over the CTAs that pass both points; the period of every layer
+    (globaltimer at CTA 0's layer starts); the head flush per task (blocks
+    waited for, task computed) summed over a CTA's tasks."""
     cons = tr[0]
-    P = nct // 2
-    ps = _shared_pairs(P, cfg.Is // 8, min(cfg.B * cfg.K, cfg.E) * (cfg.I // 8), True)
-    seq = ((24, "bar seen"), (1, "x"), (40, "router units"), (42, "router barrier"), (2, "routing"),
-           (8, "first item"), (3, "gate/up"), (4, "xchg"), (10, "act wait"), (11, "act rows"), (5, "act"),
-           (9, "down wait"), (12, "down rows"), (6, "arrive"))
     lines = []
+    us = lambda cyc: cyc / sm_mhz
+    starts = {}
+    seg = {l: {} for l in layers}
+    flush = []
+    for c in range(nct):
+        ev = {}
+        for tag, tm, cy in cons[c].tolist():
+            if tm != 0 and tag not in ev:
+                ev[tag] = (tm, cy)
+        if c == 0:
+            starts = {k >> 8: v[0] for k, v in ev.items() if k < 0xF000 and (k & 0xFF) == 0}
+        for l in layers:
+            pts = sorted(((v[1], k & 0xFF) for k, v in ev.items() if k < 0xF000 and k >> 8 == l))
+            nxt = ev.get((l + 1) << 8)
+            if nxt:
+                pts.append((nxt[1], 0x100))
+            for (ca, ka), (cb, kb) in zip(pts, pts[1:]):
+                name = f"{TRACE_POINTS.get(ka, hex(ka))} -> {TRACE_POINTS.get(kb, 'next layer') if kb != 0x100 else 'next layer'}"
+                seg[l].setdefault(name, []).append(us(cb - ca))
+        tasks = sorted({k & 0xFF for k in ev if 0xF100 <= k < 0xF200})
+        if tasks:
+            wait = sum(us(ev[0xF200 | t][1] - ev[0xF100 | t][1]) for t in tasks if 0xF200 | t in ev)
+            work = sum(us(ev[0xF300 | t][1] - ev[0xF200 | t][1]) for t in tasks if 0xF300 | t in ev)
+            first = ev[0xF100 | tasks[0]][0]
+            last = max(ev[0xF300 | t][0] for t in tasks if 0xF300 | t in ev)
+            flush.append((len(tasks), wait, work, (last - first) / 1e3))
     for l in layers:
-        for role, ctas in (("shared pairs", range(0, 2 * ps)), ("routed pairs", range(2 * ps, nct))):
-            dur = {}
-            for c in ctas:
-                ev = {}
-                for tag, tm, cy in cons[c].tolist():
-                    if tm != 0:
-                        ev[tag] = cy
-                pts = [(name, ev[(l << 8) | k]) for k, name in seq if (l << 8) | k in ev]
-                for (_, a), (name, b) in zip(pts, pts[1:]):
-                    dur.setdefault(name, []).append((b - a) / sm_mhz)
-            if dur:
-                lines.append(f"layer {l:2d} {role} ({len(ctas)} CTAs): " +
-                             " ".join(f"{n} {statistics.mean(v):.2f}" for n, v in dur.items()) + " us")
+        lines.append(f"layer {l}: " + "; ".join(
+            f"{n} {statistics.mean(v):.2f}/{max(v):.2f}" for n, v in seg[l].items()) + " us (mean/max over CTAs)")
+    ls = sorted(starts)
+    per = [(l, (starts[l + 1] - starts[l]) / 1e3) for l in ls if l + 1 in starts]
+    lines.append("layer periods (CTA 0, us): " + " ".join(f"{l}:{v:.1f}" for l, v in per))
+    if flush:
+        lines.append("head flush per CTA: tasks %.1f, block waits %.2f us, compute %.2f us, span %.2f us (mean)" % tuple(
+            statistics.mean(f[i] for f in flush) for i in range(4)))
     sys.stderr.write("\n".join(lines) + "\n")
 
 

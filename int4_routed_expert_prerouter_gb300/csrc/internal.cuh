@@ -110,8 +110,12 @@ struct Prog {
     int ring_bytes;           // shared-memory ring of streamed weights
     int ft;                   // most head tasks in one table of the head flush
     // batch-1 decode kernel (decode1.cu), filled by decode1_check
-    int pairs1[4];            // CTA pairs: all, routed, shared, LoRA
+    int grid1[2];             // CTAs of the launch, LoRA-A CTAs per LoRA matrix
     int ring1;                // bytes of its shared-memory ring
+    const char* tab1;         // device table of every CTA's plan and block layout
+    const LayerP* ly1;        // device copy of layers[0..L) (the batch-1 kernel reads it there)
+    int n_heads1;             // layers that own a head, in order (batch-1 kernel)
+    int heads1[EDGE0_MAX_LAYERS];
     long long ws_bytes;       // workspace bytes (the trace area is at its end)
     __half* dbg_h;            // [L][d] or null: each layer's output h (batch 1)
     float* dbg_logits;        // [L][E] or null: each head's logits, at its owner layer's row

@@ -65,19 +65,21 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-ENGINE_SOURCES = ("int4_routed_expert_prerouter_gb300/csrc/decode1.cu",
+KERNEL_SOURCES = ("int4_routed_expert_prerouter_gb300/csrc/decode1.cu",
                   "int4_routed_expert_prerouter_gb300/csrc/internal.cuh",
                   "int4_routed_expert_prerouter_gb300/csrc/common.cuh",
                   "include/edge0.h")
+# the committed DRAM-traffic record of the benched kernel (from an ncu capture)
+TRAFFIC_RECORD = "decode1_35b_stack_traffic.txt"
 
 
 def kernel_source_hash():
-    """Hash of the code the engine kernel is compiled from: its sources with the
+    """Hash of the code the benched kernel is compiled from: its sources with the
     comments and whitespace taken out (a comment edit does not change the
     kernel), and of the public header only the constants (#define lines) that
     the kernel uses (a new host-side declaration does not change it either)."""
     h = hashlib.sha256()
-    for f in ENGINE_SOURCES:
+    for f in KERNEL_SOURCES:
         text = open(os.path.join(ROOT, f), encoding="utf-8").read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
@@ -88,9 +90,9 @@ def kernel_source_hash():
 
 
 def profiled_traffic():
-    """DRAM bytes per token of the engine kernel from the committed ncu summary,
+    """DRAM bytes per token of the benched kernel from the committed ncu summary,
     if it was taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "engine_decode_35b_stack_traffic.txt")
+    p = os.path.join(ROOT, "profiles", TRAFFIC_RECORD)
     if not os.path.exists(p):
         return None
     kv = {}

@@ -695,6 +695,65 @@ def run_reference(args, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------- prefill -----
+def run_prefill(args, rank):
+    """The whole-layer prefill of a prompt of args.prefill tokens through the 40
+    layers of the 35B-tier stack, every layer on its own router: tokens/s, with
+    the roofline of the step's algorithmic bytes (every expert the prompt
+    activates read once per layer, the shared expert, LoRA factors, router)
+    over the measured HBM peak.  Its own JSON line (not the decode bench line)."""
+    from int4_routed_expert_prerouter_gb300 import binding, inputs
+    cfg = configs.CONFIGS[args.config]
+    T = args.prefill
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    model = inputs.make_model(cfg, seed=args.seed, device=dev, small_device=dev)
+    dm = binding.DeviceModel(model, dev)
+    ws = torch.empty(binding.prefill_workspace_bytes(cfg, T), dtype=torch.uint8, device=dev)
+    ids = torch.zeros(cfg.L, T, cfg.K, dtype=torch.int32, device=dev)
+    h0 = inputs.hidden(cfg.with_(B=T), 0, seed=args.seed, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = args.steps or 5
+    warm = args.warmup if args.warmup is not None else 3
+    h = h0.clone()
+    for _ in range(warm):
+        h.copy_(h0)
+        binding.prefill(dm, h, ws, ids_out=ids)
+    torch.cuda.synchronize(dev)
+    # algorithmic bytes of one prefill: the experts each layer's routing activates
+    active = sum(int(torch.unique(ids[l]).numel()) for l in range(cfg.L))
+    expert, shared = configs.expert_bytes(cfg.d, cfg.I), configs.expert_bytes(cfg.d, cfg.Is)
+    lora = (2 * (cfg.r * cfg.d + cfg.Is * cfg.r) + (cfg.r * cfg.Is + cfg.d * cfg.r)) * 2
+    router = cfg.E * cfg.d * 2
+    step_bytes = active * expert + cfg.L * (shared + lora + router) + 2 * T * cfg.d * 2
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            h.copy_(h0)
+            ev[i][0].record(stream)
+            binding.prefill(dm, h, ws, ids_out=ids)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    peak, src = measured_peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    line = {"metric": f"prefill tokens/s (1 GB300, 35B-tier 40-layer stack, prompt of {T} tokens)",
+            "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": warm,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int4xf16", "data": "synthetic",
+            "config": {"workload": f"{cfg.name} prefill: {T} prompt tokens through {cfg.L} layers, own routing",
+                       "tokens": T, "layers": cfg.L, "active_experts_per_layer": round(active / cfg.L, 1),
+                       "l2": "inputs larger than L2 (every prefill reads the layers' experts from HBM)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "algorithmic_bytes_per_step": int(step_bytes), "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -707,6 +766,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="reduced case for profiler captures")
     ap.add_argument("--experts", type=int, default=0, help="reduced case for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="time the whole-layer prefill of a prompt of this many tokens instead")
     ap.add_argument("--trace", action="store_true", help="print a per-phase split of one step")
     ap.add_argument("--trace-file", default=None, help="with --trace: save the raw per-CTA trace (.npz)")
     ap.add_argument("--config", default=CFG.name, choices=sorted(configs.CONFIGS),
@@ -714,6 +775,9 @@ def main():
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.prefill:
+        run_prefill(args, rank)
+        return
     if args.impl == "reference":
         args.steps = 12 if args.steps is None else args.steps
         args.warmup = 3 if args.warmup is None else args.warmup

@@ -283,6 +283,26 @@ int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
 /* Calls on one state step through the step parities in order (step, step + 1,
  * ...): a call clears the accumulators of the other parity for the next one. */
 
+/* ---- whole-layer prefill [S3.1 "Executor paths" (whole-layer), S5.1 Table 1
+ * caption: prompt processing reads every expert of a layer once for all the
+ * prompt's tokens; the prerouter is not used at prefill] ----
+ * The L layers over a prompt of T tokens (1 <= T <= 8192): h_inout [T, d] fp16
+ * (device, 16-byte aligned, updated in place).  Every layer routes every token
+ * with its own router and routing rule (App. A) -- heads and route state are
+ * not used -- then runs the routed experts grouped by expert (each active
+ * expert's weights read once per block of its tokens) and the shared expert
+ * with its LoRA over all tokens; h = fp16(h + y) per layer, as in
+ * edge0_decode_step.  ids_out: NULL, or [L][T][K] int32 (device) that receives
+ * every layer's executed ids.  workspace: device scratch of at least
+ * edge0_prefill_workspace_bytes(T, ...) bytes (16-byte aligned, owned by the
+ * caller, not zeroed beforehand; the call clears what it needs).  The shapes of
+ * every layer are those of layers[0]; d % 128 == 0.  No slot table, no host
+ * tier.  Returns EDGE0_EINVAL on bad arguments, EDGE0_ECUDA when a launch
+ * fails; enqueued on `stream` (asynchronous). */
+size_t edge0_prefill_workspace_bytes(int T, int d, int E, int K, int I, int Is);
+int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h_inout, int T, int32_t* ids_out,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ---- expert pool with a host tier [S3.1 "SSD Streaming Expert Layers", S3.2
  * "Motivation", S5.3]: n_slots device slots per layer in front of every
  * expert's packed weights in pinned host memory.  The device slot table

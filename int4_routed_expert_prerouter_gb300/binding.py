@@ -111,6 +111,9 @@ def _declare(L):
     L.edge0_moe_int4_forward.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P, C.c_size_t, P]
     L.edge0_moe_int4_forward_noalloc.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P]
     L.edge0_noalloc_error.argtypes = [P, C.POINTER(C.c_int)]
+    L.edge0_prefill_workspace_bytes.argtypes = [C.c_int] * 6
+    L.edge0_prefill_workspace_bytes.restype = C.c_size_t
+    L.edge0_prefill.argtypes = [C.POINTER(LayerDesc), C.c_int, P, C.c_int, P, P, C.c_size_t, P]
     L.edge0_lora_delta.argtypes = [C.POINTER(LoraDesc), P, C.c_int, P, P]
     L.edge0_decode_layer.argtypes = [C.POINTER(LayerDesc), P, C.POINTER(RouteState), C.c_int,
                                      C.c_int, P]
@@ -120,7 +123,8 @@ def _declare(L):
                  "edge0_pack_f16_kmajor", "edge0_pack_cols_T", "edge0_state_init",
                  "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
                  "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
-                 "edge0_moe_int4_forward_noalloc", "edge0_state_set_wait_limit", "edge0_noalloc_error"):
+                 "edge0_moe_int4_forward_noalloc", "edge0_state_set_wait_limit", "edge0_noalloc_error",
+                 "edge0_prefill"):
         getattr(L, name).restype = C.c_int
 
 
@@ -130,7 +134,8 @@ EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_
             "edge0_workspace_bytes", "edge0_decode_workspace_bytes", "edge0_state_init",
             "edge0_state_error", "edge0_state_set_wait_limit", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
-            "edge0_moe_int4_forward_noalloc", "edge0_noalloc_error", "edge0_pool_create", "edge0_pool_set_layer",
+            "edge0_moe_int4_forward_noalloc", "edge0_noalloc_error", "edge0_prefill_workspace_bytes",
+            "edge0_prefill", "edge0_pool_create", "edge0_pool_set_layer",
             "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_resident", "edge0_pool_destroy"]
 
 
@@ -452,6 +457,24 @@ def decode_step(dm: DeviceModel, st: DecodeState, h: torch.Tensor, step: int, st
     assert h.is_cuda and h.dtype == torch.float16 and h.is_contiguous()
     _check(lib().edge0_decode_step(dm.layers, dm.cfg.L, _ptr(h), C.byref(st.st), st.B, step,
                                    _stream(stream)), "edge0_decode_step")
+
+
+def prefill_workspace_bytes(cfg: Config, T: int) -> int:
+    return int(lib().edge0_prefill_workspace_bytes(T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is))
+
+
+def prefill(dm: DeviceModel, h: torch.Tensor, workspace: torch.Tensor, ids_out=None, layers=None, stream=None):
+    """The model's layers (or layers[a:b] given as a slice) over a prompt h [T, d]
+    fp16 (device, in place); every layer on its own router.  ids_out: None or
+    [L][T][K] int32 (device)."""
+    assert h.is_cuda and h.dtype == torch.float16 and h.is_contiguous() and h.dim() == 2
+    arr, L = dm.layers, dm.cfg.L
+    if layers is not None:
+        idx = list(range(L))[layers]
+        arr = (LayerDesc * len(idx))(*[dm.layers[i] for i in idx])
+        L = len(idx)
+    _check(lib().edge0_prefill(arr, L, _ptr(h), h.shape[0], _ptr(ids_out), _ptr(workspace),
+                               workspace.numel(), _stream(stream)), "edge0_prefill")
 
 
 def decode_layer(dm: DeviceModel, l: int, st: DecodeState, h: torch.Tensor, step: int, stream=None):

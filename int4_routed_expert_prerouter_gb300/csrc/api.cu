@@ -284,6 +284,59 @@ extern "C" int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t
     return decode_common(layers, L, h_inout, st, B, step, stream);
 }
 
+extern "C" size_t edge0_prefill_workspace_bytes(int T, int d, int E, int K, int I, int Is) {
+    if (T <= 0 || T > kMaxPrefill || d <= 0 || E <= 0 || K <= 0 || I <= 0 || Is <= 0) return 0;
+    return (size_t)batch_ws_layout(1, T, d, E, K, I > Is ? I : Is, 16).total;
+}
+
+extern "C" int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h, int T, int32_t* ids_out,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!layers || !h || L <= 0 || L > EDGE0_MAX_LAYERS || T <= 0 || T > kMaxPrefill) return EDGE0_EINVAL;
+    if (!al16(h) || !workspace || !al16(workspace) || ((uintptr_t)ids_out & 3)) return EDGE0_EINVAL;
+    Dims D;
+    D.d = layers[0].moe.d;
+    D.E = layers[0].moe.E;
+    D.K = layers[0].moe.K;
+    D.I = layers[0].moe.I;
+    D.Is = layers[0].moe.Is;
+    D.H = 64;
+    D.r = 16;
+    for (int l = 0; l < L; ++l)
+        if (layers[l].lora_gate.A) { D.r = layers[l].lora_gate.r; break; }
+    int rc = check_dims(D, T, kMaxPrefill);
+    if (rc) return rc;
+    if (D.d % 128) return EDGE0_EINVAL;
+    const size_t need = edge0_prefill_workspace_bytes(T, D.d, D.E, D.K, D.I, D.Is);
+    if (need == 0 || workspace_bytes < need) return EDGE0_EINVAL;
+    Prog* p = new Prog;
+    memset(p, 0, sizeof(Prog));
+    p->mode = MODE_PREFILL;
+    p->L = L;
+    set_dims(*p, D, T);
+    p->h_io = (__half*)h;
+    p->Ls = L;
+    p->ws = (char*)workspace;
+    p->ws_bytes = (long long)workspace_bytes;
+    for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
+        // a prefill reads no route state: a layer's state row is not used
+        edge0_layer_desc Ld = layers[l];
+        Ld.index = 0;
+        Ld.has_head = 0;     // nor a head: the prerouter is not used at prefill
+        rc = fill_layer(Ld, D, 1, p->layers[l]);
+        if (rc == EDGE0_OK && (p->layers[l].slot_table || p->layers[l].gu_host)) rc = EDGE0_EINVAL;
+    }
+    if (rc == EDGE0_OK) {
+        // the header (error word) and the layer-output accumulators start at zero
+        const BatchWs W = batch_ws_layout(1, T, D.d, D.E, D.K, D.I > D.Is ? D.I : D.Is, 16);
+        if (cudaMemsetAsync(workspace, 0, kWsHeaderBytes, stream) != cudaSuccess ||
+            cudaMemsetAsync((char*)workspace + W.y, 0, (size_t)T * D.d * 4, stream) != cudaSuccess)
+            rc = EDGE0_ECUDA;
+    }
+    if (rc == EDGE0_OK) rc = batch_prefill(*p, ids_out, stream);
+    delete p;
+    return rc;
+}
+
 extern "C" int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t* x,
                                       const int32_t* ids, const float* w, int B, uint16_t* y,
                                       void* workspace, size_t workspace_bytes,

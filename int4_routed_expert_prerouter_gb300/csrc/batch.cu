@@ -33,8 +33,14 @@
 namespace edge0 {
 
 // ---------------------------------------------------------------- layout ----
-// work items of the expert kernels in the dispatch record (see Disp)
-constexpr int kDispItems = EDGE0_MAX_BATCHED * EDGE0_MAX_K / 8 + EDGE0_MAX_E + EDGE0_MAX_BATCHED / 8 + 2;
+// work items of the expert kernels in the dispatch record (see Disp): at most
+// B K / 8 (blocks of at least 8 positions) + one partial block per active
+// expert + the shared expert's blocks, per kernel
+__host__ __device__ inline int disp_cap(int B, int K, int E) {
+    return (B * K + 7) / 8 + (B * K < E ? B * K : E) + (B + 7) / 8 + 2;
+}
+// bytes of the dispatch record's fixed part (Disp); the work items follow it
+constexpr long long kDispHead = 6400;
 BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
     BatchWs w;
     auto al = [](long long x) { return (x + 255) / 256 * 256; };
@@ -46,7 +52,8 @@ BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
     w.z = o;     o += al((long long)B * H * 4);
     w.la = o;    o += al((long long)B * 32 * 4);
     w.wsel = o;  o += al((long long)B * K * 4);
-    w.disp = o;  o += al((long long)(4 * (EDGE0_MAX_E + 1) + 4 + 4 * kDispItems) * 4);
+    w.exec = o;  o += al((long long)B * K * 4);
+    w.disp = o;  o += al(kDispHead + 2LL * disp_cap(B, K, E) * 8);
     w.tok = o;   o += al((long long)B * K * 4);
     w.wt = o;    o += al((long long)B * K * 4);
     w.act = o;   o += al((long long)(B * K + B) * I * 4);
@@ -56,18 +63,25 @@ BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
 
 namespace {
 
-// work items of the expert kernels: (slot, first token of a block); at most
-// B K / blk + (active experts) + B / blk + 1 per kernel
-constexpr int kMaxItems = kDispItems;
-
 struct Disp {   // dispatch of one layer (device); fits the workspace's dispatch record
     int nact;
     int sexp[EDGE0_MAX_E + 1];
     int soff[EDGE0_MAX_E + 1];
     int scnt[EDGE0_MAX_E + 1];
     int n_gu, n_dn;                   // work items of k_gu / k_down
-    int2 it_gu[kMaxItems], it_dn[kMaxItems];
+    int cap;                          // room for the items of each kernel
+    // then, kDispHead bytes from the record's start, the work items (slot, first
+    // position of a block): cap for k_gu, cap for k_down
 };
+static_assert(sizeof(Disp) <= kDispHead && kDispHead % 16 == 0, "the work items start 16-byte aligned after Disp");
+__device__ __forceinline__ int2* gu_items(Disp* D) {
+    return reinterpret_cast<int2*>(reinterpret_cast<char*>(D) + kDispHead);
+}
+__device__ __forceinline__ int2* dn_items(Disp* D) { return gu_items(D) + D->cap; }
+__device__ __forceinline__ const int2* gu_items(const Disp* D) {
+    return reinterpret_cast<const int2*>(reinterpret_cast<const char*>(D) + kDispHead);
+}
+__device__ __forceinline__ const int2* dn_items(const Disp* D) { return gu_items(D) + D->cap; }
 
 __device__ __forceinline__ void record_error(WsHeader* hdr, int code) {
     atomicCAS(&hdr->error, 0, code);
@@ -255,10 +269,11 @@ __global__ void __launch_bounds__(256) k_route(const float* logits, int ldl, int
 // (token, weight) pairs; one CTA.  An id outside [0, E) records EDGE0_EINVAL
 // and counts as expert 0.
 __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const float* w, int B, int K, int E,
-                                                   int shared, int blk_gu, int blk_dn, Disp* D, int* tok, float* wt,
-                                                   WsHeader* hdr) {
+                                                   int shared, int blk_gu, int blk_dn, int cap, Disp* D, int* tok,
+                                                   float* wt, WsHeader* hdr) {
     __shared__ int cnt[EDGE0_MAX_E], off[EDGE0_MAX_E], fill[EDGE0_MAX_E];
     const int tid = threadIdx.x, n = B * K;
+    if (tid == 0) D->cap = cap;
     for (int e = tid; e < E; e += blockDim.x) cnt[e] = fill[e] = 0;
     __syncthreads();
     for (int p = tid; p < n; p += blockDim.x) {
@@ -310,16 +325,16 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const flo
             D->sexp[j] = e;
             D->soff[j] = ex[0];
             D->scnt[j] = c_e;
-            for (int i = 0; i < v[2]; ++i) D->it_gu[ex[2] + i] = make_int2(j, i * blk_gu);
-            for (int i = 0; i < v[3]; ++i) D->it_dn[ex[3] + i] = make_int2(j, i * blk_dn);
+            for (int i = 0; i < v[2]; ++i) gu_items(D)[ex[2] + i] = make_int2(j, i * blk_gu);
+            for (int i = 0; i < v[3]; ++i) dn_items(D)[ex[3] + i] = make_int2(j, i * blk_dn);
         }
     }
     if (tid == 0) {
         // the shared expert's work items after the routed ones (slot a)
         int ng = sc_wsum[2][nwarps - 1], nd = sc_wsum[3][nwarps - 1];
         if (shared) {
-            for (int tb = 0; tb < B; tb += blk_gu) D->it_gu[ng++] = make_int2(a, tb);
-            for (int tb = 0; tb < B; tb += blk_dn) D->it_dn[nd++] = make_int2(a, tb);
+            for (int tb = 0; tb < B; tb += blk_gu) gu_items(D)[ng++] = make_int2(a, tb);
+            for (int tb = 0; tb < B; tb += blk_dn) dn_items(D)[nd++] = make_int2(a, tb);
         }
         D->nact = a;
         D->n_gu = ng;
@@ -577,7 +592,7 @@ __global__ void __launch_bounds__(kGuWarps * 32) k_gu(const LayerP Ly, const Dis
     // GPU, not to the most items a layer can have)
     for (int yi = blockIdx.y; yi < D->n_gu; yi += gridDim.y) {   // CTA-uniform
         Slot S;
-        const int2 item = D->it_gu[yi];
+        const int2 item = gu_items(D)[yi];
         if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) continue;
         run_item(item, S);
         __syncthreads();   // the staged token rows are reused by the next item
@@ -721,7 +736,7 @@ __global__ void __launch_bounds__(256, 3) k_down(const LayerP Ly, const Disp* D,
     };
     for (int yi = blockIdx.y; yi < D->n_dn; yi += gridDim.y) {   // CTA-uniform, as in k_gu
         Slot S;
-        const int2 item = D->it_dn[yi];
+        const int2 item = dn_items(D)[yi];
         if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S)) continue;
         run_item(item, S);
         __syncthreads();   // the staged act fragments are reused by the next item
@@ -802,12 +817,17 @@ int route(const float* lg, int B, int E, int K, int kind, int ng, int G, float s
 
 }  // namespace
 
-// One decode step of L layers for B > EDGE0_MAX_BATCH sequences (host: validates
-// nothing beyond what the caller checked; enqueues on `st`).
-int batch_decode(const Prog& p, cudaStream_t st) {
+namespace {
+// One decode step of L layers for B > EDGE0_MAX_BATCH sequences, or (prefill)
+// the L layers over a prompt of B tokens, every layer on its own router and no
+// head (the prerouter is not used at prefill), the executed ids into ids_out
+// ([L][B][K], or the workspace when null).  Validates nothing beyond what the
+// caller checked; enqueues on `st`.
+int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
+    const bool prefill = p.mode == MODE_PREFILL;
     const int L = p.L, B = p.B, K = p.K, d = p.d, E = p.E, I = p.I, Is = p.Is, H = p.H, r = p.r;
     const int Imax = I > Is ? I : Is;
-    const BatchWs W = batch_ws_layout(p.Ls, B, d, E, K, Imax, H);
+    const BatchWs W = prefill ? batch_ws_layout(1, B, d, E, K, Imax, 16) : batch_ws_layout(p.Ls, B, d, E, K, Imax, H);
     char* ws = p.ws;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     float* y = reinterpret_cast<float*>(ws + W.y);
@@ -821,8 +841,9 @@ int batch_decode(const Prog& p, cudaStream_t st) {
     int* tok = reinterpret_cast<int*>(ws + W.tok);
     float* wt = reinterpret_cast<float*>(ws + W.wt);
     float* act = reinterpret_cast<float*>(ws + W.act);
-    const int step = p.step, par = step & 1;
+    const int step = prefill ? 0 : p.step, par = step & 1;
     const int slots = (B * K < E ? B * K : E) + 1;
+    const int cap = disp_cap(B, K, E);
     const int items_gu = (B * K + kGuTok - 1) / kGuTok + slots + (B + kGuTok - 1) / kGuTok;
     const int items_dn = (B * K + kDnTok - 1) / kDnTok + slots + (B + kDnTok - 1) / kDnTok;
     auto ok = [] { return cudaGetLastError() == cudaSuccess; };
@@ -851,13 +872,14 @@ int batch_decode(const Prog& p, cudaStream_t st) {
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
         const LayerP& Ly = p.layers[l];
         const long long srow = (long long)Ly.sidx * B * K;
-        __half* x = xs + (long long)Ly.sidx * B * d;
+        __half* x = xs + (prefill ? 0LL : (long long)Ly.sidx * B * d);
         if (Ly.ready && cudaStreamWaitEvent(st, (cudaEvent_t)Ly.ready, 0) != cudaSuccess) return EDGE0_ECUDA;
         k_norm<<<B, 256, 0, st>>>(p.h_io, y, l > 0, Ly.gamma, Ly.eps, d, x, xsum, 1);
         if (!ok()) return EDGE0_ECUDA;
-        int32_t* exec = p.exec_ids + (long long)par * p.Ls * B * K + srow;
+        int32_t* exec = prefill ? (ids_out ? ids_out + (long long)l * B * K : reinterpret_cast<int32_t*>(ws + W.exec))
+                                : p.exec_ids + (long long)par * p.Ls * B * K + srow;
         const float* w;
-        if ((Ly.flags & LF_PREROUTED) && step > 0) {
+        if (!prefill && (Ly.flags & LF_PREROUTED) && step > 0) {
             const long long o = (long long)(par ^ 1) * p.Ls * B * K + srow;
             if (cudaMemcpyAsync(exec, p.pred_ids + o, (size_t)B * K * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
                 return EDGE0_ECUDA;
@@ -870,7 +892,7 @@ int batch_decode(const Prog& p, cudaStream_t st) {
             w = wsel;
         }
         if (rc) return rc;
-        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, kGuTok, kDnTok, D, tok, wt, hdr);
+        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, kGuTok, kDnTok, cap, D, tok, wt, hdr);
         if (!ok()) return EDGE0_ECUDA;
         const int lora = (Ly.flags & LF_LORA) ? 1 : 0;
         if (lora) {
@@ -894,6 +916,7 @@ int batch_decode(const Prog& p, cudaStream_t st) {
     // the last layer's output
     k_norm<<<B, 256, 0, st>>>(p.h_io, y, 1, nullptr, 0.f, d, nullptr, nullptr, 0);
     if (!ok()) return EDGE0_ECUDA;
+    if (prefill) return rc;
     // head flush: every head of the step, from its layer's x and routing
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
         const LayerP& Ly = p.layers[l];
@@ -916,6 +939,14 @@ int batch_decode(const Prog& p, cudaStream_t st) {
                    Ly.head_bias, p.pred_ids + o, p.pred_w + o, st);
     }
     return rc;
+}
+}  // namespace
+
+int batch_decode(const Prog& p, cudaStream_t st) { return run_batched(p, nullptr, st); }
+
+int batch_prefill(const Prog& p, int32_t* ids_out, cudaStream_t st) {
+    if (p.mode != MODE_PREFILL || p.B < 1 || p.B > kMaxPrefill) return EDGE0_EINVAL;
+    return run_batched(p, ids_out, st);
 }
 
 }  // namespace edge0

@@ -34,7 +34,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one producer warp
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kClusterCtas = 2;                        // CTA pairs share gate/up partial sums
 
-enum Mode : int { MODE_DECODE = 0, MODE_MOE = 1, MODE_HEAD = 2 };
+enum Mode : int { MODE_DECODE = 0, MODE_MOE = 1, MODE_HEAD = 2, MODE_PREFILL = 3 };
 
 enum LayerFlags : int {
     LF_PREROUTED = 1,
@@ -179,9 +179,14 @@ inline __host__ __device__ WsLayout ws_layout(int Ls, int B, int d, int E) {
 //   la [B][32] LoRA A x, wsel [B][K] own-router weights, disp (dispatch of a
 //   layer), tok / wt [B K] (token, weight) per position, act [B K + B][Imax].
 struct BatchWs {
-    long long y, xs, xsum, lg, z, la, wsel, disp, tok, wt, act, total;
+    long long y, xs, xsum, lg, z, la, wsel, exec, disp, tok, wt, act, total;
 };
 BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H);
+// prompt tokens of one whole-layer prefill call
+constexpr int kMaxPrefill = 8192;
+// the layers of a prompt of p.B tokens (p.mode == MODE_PREFILL), every layer on
+// its own router; enqueued on `st`
+int batch_prefill(const Prog& p, int32_t* ids_out, cudaStream_t st);
 
 // --------------------------------------------------------------- PTX -----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

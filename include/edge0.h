@@ -258,6 +258,15 @@ int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t* x, const i
 int edge0_lora_delta(const edge0_lora_desc* lora, const uint16_t* v, int B, uint16_t* y_inout,
                      cudaStream_t stream);
 
+/* Dense fp16 GEMM on the fifth-generation tensor cores (tcgen05.mma with a TMEM
+ * accumulator): D [M, N] fp32 = A [M, K] fp16 x B [N, K]^T fp16, all row-major
+ * and 16-byte aligned on the device; M % 128 == 0, 16 <= N <= 256 with N % 16
+ * == 0, K % 64 == 0.  *status (device int, set to 0 by the caller) receives
+ * EDGE0_ETIMEOUT if a tensor-core wait ran past its limit.  The building block
+ * of the grouped int4 kernels; enqueued on `stream`. */
+int edge0_tc_gemm_f16(const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K, int* status,
+                      cudaStream_t stream);
+
 /* One decode layer at step `step` for B sequences: h_inout [B, d] fp16 is the
  * layer input (residual stream) and receives the layer output
  *   h + routed experts + shared expert (with LoRA),

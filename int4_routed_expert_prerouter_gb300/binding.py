@@ -111,6 +111,7 @@ def _declare(L):
     L.edge0_moe_int4_forward.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P, C.c_size_t, P]
     L.edge0_moe_int4_forward_noalloc.argtypes = [C.POINTER(MoeDesc), P, P, P, C.c_int, P, P]
     L.edge0_noalloc_error.argtypes = [P, C.POINTER(C.c_int)]
+    L.edge0_tc_gemm_f16.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, P, P]
     L.edge0_prefill_workspace_bytes.argtypes = [C.c_int] * 6
     L.edge0_prefill_workspace_bytes.restype = C.c_size_t
     L.edge0_prefill.argtypes = [C.POINTER(LayerDesc), C.c_int, P, C.c_int, P, P, C.c_size_t, P]
@@ -124,7 +125,7 @@ def _declare(L):
                  "edge0_state_error", "edge0_prerouter_topk", "edge0_moe_int4_forward",
                  "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
                  "edge0_moe_int4_forward_noalloc", "edge0_state_set_wait_limit", "edge0_noalloc_error",
-                 "edge0_prefill"):
+                 "edge0_prefill", "edge0_tc_gemm_f16"):
         getattr(L, name).restype = C.c_int
 
 
@@ -135,7 +136,7 @@ EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_
             "edge0_state_error", "edge0_state_set_wait_limit", "edge0_prerouter_topk", "edge0_moe_int4_forward",
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
             "edge0_moe_int4_forward_noalloc", "edge0_noalloc_error", "edge0_prefill_workspace_bytes",
-            "edge0_prefill", "edge0_pool_create", "edge0_pool_set_layer",
+            "edge0_prefill", "edge0_tc_gemm_f16", "edge0_pool_create", "edge0_pool_set_layer",
             "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_resident", "edge0_pool_destroy"]
 
 
@@ -457,6 +458,22 @@ def decode_step(dm: DeviceModel, st: DecodeState, h: torch.Tensor, step: int, st
     assert h.is_cuda and h.dtype == torch.float16 and h.is_contiguous()
     _check(lib().edge0_decode_step(dm.layers, dm.cfg.L, _ptr(h), C.byref(st.st), st.B, step,
                                    _stream(stream)), "edge0_decode_step")
+
+
+def tc_gemm_f16(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
+    """A [M, K] fp16 x B [N, K]^T fp16 -> fp32 [M, N] on tcgen05 (device tensors)."""
+    A, B = A.contiguous(), B.contiguous()
+    M, K = A.shape
+    N = B.shape[0]
+    D = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    status = torch.zeros(1, dtype=torch.int32, device=A.device)
+    _check(lib().edge0_tc_gemm_f16(_ptr(A), _ptr(B), _ptr(D), M, N, K, _ptr(status), _stream(stream)),
+           "edge0_tc_gemm_f16")
+    torch.cuda.synchronize(A.device)
+    code = int(status.item())
+    if code:
+        raise RuntimeError(f"edge0_tc_gemm_f16: {status_string(code)}")
+    return D
 
 
 def prefill_workspace_bytes(cfg: Config, T: int) -> int:

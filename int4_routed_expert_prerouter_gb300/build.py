@@ -15,7 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libedge0.so")
-SOURCES = ["decode1.cu", "engine.cu", "batch.cu", "pool.cu", "api.cu", "pack.cu", "lora.cu", "noalloc.cu"]
+SOURCES = ["decode1.cu", "engine.cu", "batch.cu", "pool.cu", "api.cu", "pack.cu", "lora.cu", "noalloc.cu",
+           "tcgemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

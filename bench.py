@@ -704,6 +704,9 @@ def run_prefill(args, rank):
     over the measured HBM peak.  Its own JSON line (not the decode bench line)."""
     from int4_routed_expert_prerouter_gb300 import binding, inputs
     cfg = configs.CONFIGS[args.config]
+    if args.layers:   # reduced case for profiler captures
+        cfg = cfg.with_(L=args.layers, head_owner_last=min(cfg.head_owner_last, args.layers - 2),
+                        prerouted=tuple(l for l in cfg.prerouted if l < args.layers - 1))
     T = args.prefill
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
@@ -715,12 +718,13 @@ def run_prefill(args, rank):
     ids = torch.zeros(cfg.L, T, cfg.K, dtype=torch.int32, device=dev)
     h0 = inputs.hidden(cfg.with_(B=T), 0, seed=args.seed, device=dev)
     stream = torch.cuda.current_stream(dev)
+    flags = binding.PREFILL_TCGEN05_GATE_UP if args.prefill_tcgen05 else 0
     steps = args.steps or 5
     warm = args.warmup if args.warmup is not None else 3
     h = h0.clone()
     for _ in range(warm):
         h.copy_(h0)
-        binding.prefill(dm, h, ws, ids_out=ids)
+        binding.prefill(dm, h, ws, ids_out=ids, flags=flags)
     torch.cuda.synchronize(dev)
     # algorithmic bytes of one prefill: the experts each layer's routing activates
     active = sum(int(torch.unique(ids[l]).numel()) for l in range(cfg.L))
@@ -734,7 +738,7 @@ def run_prefill(args, rank):
         for i in range(steps):
             h.copy_(h0)
             ev[i][0].record(stream)
-            binding.prefill(dm, h, ws, ids_out=ids)
+            binding.prefill(dm, h, ws, ids_out=ids, flags=flags)
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
@@ -745,7 +749,8 @@ def run_prefill(args, rank):
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int4xf16", "data": "synthetic",
             "config": {"workload": f"{cfg.name} prefill: {T} prompt tokens through {cfg.L} layers, own routing",
-                       "tokens": T, "layers": cfg.L, "active_experts_per_layer": round(active / cfg.L, 1),
+                       "tokens": T, "layers": cfg.L,
+                       "gate_up_kernel": "tcgen05" if flags else "mma.sync", "active_experts_per_layer": round(active / cfg.L, 1),
                        "l2": "inputs larger than L2 (every prefill reads the layers' experts from HBM)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
@@ -768,6 +773,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", type=int, default=0,
                     help="time the whole-layer prefill of a prompt of this many tokens instead")
+    ap.add_argument("--prefill-tcgen05", action="store_true", help="with --prefill: the tcgen05 gate/up kernel")
     ap.add_argument("--trace", action="store_true", help="print a per-phase split of one step")
     ap.add_argument("--trace-file", default=None, help="with --trace: save the raw per-CTA trace (.npz)")
     ap.add_argument("--config", default=CFG.name, choices=sorted(configs.CONFIGS),

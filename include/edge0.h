@@ -309,8 +309,13 @@ int edge0_decode_step(const edge0_layer_desc* layers, int L, uint16_t* h_inout,
  * tier.  Returns EDGE0_EINVAL on bad arguments, EDGE0_ECUDA when a launch
  * fails; enqueued on `stream` (asynchronous). */
 size_t edge0_prefill_workspace_bytes(int T, int d, int E, int K, int I, int Is);
+#define EDGE0_PREFILL_TCGEN05_GATE_UP 1u  /* flags: gate/up on the tcgen05 kernel (dequantized
+                                             fp16 tiles, TMEM accumulator) instead of the
+                                             mma.sync kernel (int4 nibbles as fp16
+                                             subnormals, scales in the epilogue); the
+                                             results agree within the parity tolerance */
 int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h_inout, int T, int32_t* ids_out,
-                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                  unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---- expert pool with a host tier [S3.1 "SSD Streaming Expert Layers", S3.2
  * "Motivation", S5.3]: n_slots device slots per layer in front of every

@@ -114,7 +114,7 @@ def _declare(L):
     L.edge0_tc_gemm_f16.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, P, P]
     L.edge0_prefill_workspace_bytes.argtypes = [C.c_int] * 6
     L.edge0_prefill_workspace_bytes.restype = C.c_size_t
-    L.edge0_prefill.argtypes = [C.POINTER(LayerDesc), C.c_int, P, C.c_int, P, P, C.c_size_t, P]
+    L.edge0_prefill.argtypes = [C.POINTER(LayerDesc), C.c_int, P, C.c_int, P, C.c_uint, P, C.c_size_t, P]
     L.edge0_lora_delta.argtypes = [C.POINTER(LoraDesc), P, C.c_int, P, P]
     L.edge0_decode_layer.argtypes = [C.POINTER(LayerDesc), P, C.POINTER(RouteState), C.c_int,
                                      C.c_int, P]
@@ -480,17 +480,22 @@ def prefill_workspace_bytes(cfg: Config, T: int) -> int:
     return int(lib().edge0_prefill_workspace_bytes(T, cfg.d, cfg.E, cfg.K, cfg.I, cfg.Is))
 
 
-def prefill(dm: DeviceModel, h: torch.Tensor, workspace: torch.Tensor, ids_out=None, layers=None, stream=None):
+PREFILL_TCGEN05_GATE_UP = 1
+
+
+def prefill(dm: DeviceModel, h: torch.Tensor, workspace: torch.Tensor, ids_out=None, layers=None, flags=0,
+            stream=None):
     """The model's layers (or layers[a:b] given as a slice) over a prompt h [T, d]
     fp16 (device, in place); every layer on its own router.  ids_out: None or
-    [L][T][K] int32 (device)."""
+    [L][T][K] int32 (device); flags: PREFILL_TCGEN05_GATE_UP for the tcgen05
+    gate/up kernel."""
     assert h.is_cuda and h.dtype == torch.float16 and h.is_contiguous() and h.dim() == 2
     arr, L = dm.layers, dm.cfg.L
     if layers is not None:
         idx = list(range(L))[layers]
         arr = (LayerDesc * len(idx))(*[dm.layers[i] for i in idx])
         L = len(idx)
-    _check(lib().edge0_prefill(arr, L, _ptr(h), h.shape[0], _ptr(ids_out), _ptr(workspace),
+    _check(lib().edge0_prefill(arr, L, _ptr(h), h.shape[0], _ptr(ids_out), flags, _ptr(workspace),
                                workspace.numel(), _stream(stream)), "edge0_prefill")
 
 

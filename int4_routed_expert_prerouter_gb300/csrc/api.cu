@@ -290,7 +290,8 @@ extern "C" size_t edge0_prefill_workspace_bytes(int T, int d, int E, int K, int 
 }
 
 extern "C" int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h, int T, int32_t* ids_out,
-                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                             unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (flags & ~EDGE0_PREFILL_TCGEN05_GATE_UP) return EDGE0_EINVAL;
     if (!layers || !h || L <= 0 || L > EDGE0_MAX_LAYERS || T <= 0 || T > kMaxPrefill) return EDGE0_EINVAL;
     if (!al16(h) || !workspace || !al16(workspace) || ((uintptr_t)ids_out & 3)) return EDGE0_EINVAL;
     Dims D;
@@ -332,6 +333,7 @@ extern "C" int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h,
             cudaMemsetAsync((char*)workspace + W.y, 0, (size_t)T * D.d * 4, stream) != cudaSuccess)
             rc = EDGE0_ECUDA;
     }
+    p->tc_gu = (flags & EDGE0_PREFILL_TCGEN05_GATE_UP) ? 1 : 0;
     if (rc == EDGE0_OK) rc = batch_prefill(*p, ids_out, stream);
     delete p;
     return rc;

@@ -29,6 +29,7 @@
 
 #include "internal.cuh"
 #include "common.cuh"
+#include "tc05.cuh"
 
 namespace edge0 {
 
@@ -430,6 +431,7 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
                  : "r"(addr));
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_2() { asm volatile("cp.async.wait_group 2;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_6() { asm volatile("cp.async.wait_group 6;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
@@ -599,6 +601,230 @@ __global__ void __launch_bounds__(kGuWarps * 32) k_gu(const LayerP Ly, const Dis
     }
 }
 
+// ------------------------------------------------------------ k_gu_tc -------
+// gate/up of one expert for a block of up to 128 of its tokens on the fifth-
+// generation tensor cores (prefill): CTA x takes the expert's 128-row tile x of
+// interleaved gate/up rows (8 packed 16-row tiles: the gate rows of act rows
+// 8 p .. 8 p + 7, then the same up rows, for p = 8 x .. 8 x + 7) over all of
+// d, one group of 64 inputs (one K chunk) at a time:
+//   * cp.async brings the chunk's 8 packed units and the block's token rows of
+//     x (straight into the canonical K-major layout, zero rows past the
+//     block's tokens) into one of three slots, two chunks ahead;
+//   * every thread dequantizes one unit's lane slice (s q + b, rounded to fp16
+//     once) from the slot into one of two A stages (canonical K-major layout);
+//   * one thread issues four tcgen05.mma K-steps (M 128, N = the block's tokens
+//     rounded up to 16, K 16) into a TMEM accumulator and commits to the A
+//     stage's mbarrier, which frees the stage and the slot.
+// The epilogue reads the accumulator (lane = row, column = token), pairs each
+// gate row with its up row (8 lanes apart) and writes act[position][row] =
+// silu(gate) up (the shared expert with its LoRA terms (alpha/r) B (A x), A x
+// precomputed in la).
+constexpr int kTcTok = 128;                  // tokens per block (MMA N at most)
+constexpr int kTcThreads = 256;
+constexpr int kTcA = 4 * 128 * 32;           // dequantized A of one K chunk (4 K-steps x 128 rows x 32 B)
+constexpr int kTcB = 4 * kTcTok * 32;        // B of one K chunk
+constexpr int kTcRaw = 8 * kQ4Unit;          // the chunk's 8 packed units
+constexpr int kTcSlots = 4;                  // raw + B slots (chunks in flight)
+constexpr int kTcSlot = kTcB + kTcRaw;       // B first: 1 KB aligned
+constexpr int kTcSmem = kTcSlots * kTcSlot + 2 * kTcA;
+constexpr unsigned long long kTcWait = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long tc_time() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// every thread: the barrier's phase of parity `par` has completed (bounded)
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t par) {
+    if (mbar_try_wait(bar, par)) return true;
+    const unsigned long long t0 = tc_time();
+    while (!mbar_try_wait(bar, par))
+        if (tc_time() - t0 > kTcWait) return false;
+    return true;
+}
+// 16 bytes by cp.async, or 16 zero bytes (src_size 0)
+__device__ __forceinline__ void cp16z(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+// (s q + b) for the nibble pair (bits 0-3 and 16-19 of v): each nibble with
+// exponent bits of 1024 is the fp16 1024 + q, exact; minus 1024 gives q; one
+// fused multiply-add with the row's (s, b) rounds s q + b to fp16 once
+__device__ __forceinline__ uint32_t deq2(uint32_t v, __half2 s2, __half2 b2) {
+    const uint32_t m = (v & 0x000F000Fu) | 0x64006400u;
+    const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&m), __float2half2_rn(1024.f));
+    const __half2 h = __hfma2(q, s2, b2);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kTcThreads) k_gu_tc(const LayerP Ly, const Disp* D, const int* tok, const float* wt,
+                                                      const __half* __restrict__ x, const float* la, int lora, int r,
+                                                      int B, int K, int d, int I, int Is, int Imax, float* act,
+                                                      WsHeader* hdr) {
+    extern __shared__ __align__(1024) char tsm[];
+    __shared__ uint64_t bar[2];
+    __shared__ uint32_t taddr_s;
+    __shared__ int bad;
+    const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+    const int mt = blockIdx.x, n_gd = d / kGroup, ng0 = n_gd / 2, ng1 = n_gd - ng0;
+    char* slots = tsm;
+    char* astage = tsm + kTcSlots * kTcSlot;
+    if (wid == 0) {
+        tc::tmem_alloc(&taddr_s, kTcTok);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        bad = 0;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t taddr = taddr_s;
+    int cc = 0;   // K chunks whose MMAs this CTA issued (A stage = cc & 1; commit count of bar[s] = cc >> 1)
+    for (int yi = blockIdx.y; yi < D->n_gu && !bad; yi += gridDim.y) {   // CTA-uniform
+        Slot S;
+        const int2 item = gu_items(D)[yi];
+        if (!slot_of(item.x, D, Ly, B, K, d, I, Is, tok, wt, hdr, S) || S.host) continue;
+        const int RT = S.I / kHalfRow;          // packed 16-row tiles of the expert
+        if (mt * 8 >= RT) continue;             // this row tile lies beyond a narrower expert
+        const int tb = item.y, m = min(kTcTok, S.m - tb), nb = (m + 15) & ~15;
+        const uint32_t idesc = tc::idesc_f16(128, nb);
+        // this thread's token pieces: token q = tid / 8 + 32 j, inputs 8 (tid % 8)
+        // of the chunk; their x rows (fixed for the item) and shared-memory places
+        const int c8 = tid & 7;
+        long long xrow[4];
+        uint32_t boff[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = (tid >> 3) + 32 * j;
+            xrow[j] = q < m ? (long long)(S.toks ? S.toks[tb + q] : tb + q) * d : -1;
+            boff[j] = (uint32_t)((c8 >> 1) * kTcTok * 32) + tc::kstep_off(q, (c8 & 1) * 8);
+        }
+        // the prefetch of chunk kc into slot kc % kTcSlots: the 8 units (288
+        // pieces of 16 bytes) and the block's token rows (zeros past them)
+        auto prefetch = [&](int kc) {
+            if (kc < n_gd) {
+                char* sl = slots + (kc % kTcSlots) * kTcSlot;
+                const int h = kc >= ng0, gh = kc - h * ng0, ngh = h ? ng1 : ng0;
+                const char* u0 = S.gu + (h ? (long long)RT * ng0 * kQ4Unit : 0LL) +
+                                 ((long long)(mt * 8) * ngh + gh) * kQ4Unit;
+                for (int i = tid; i < kTcRaw / 16; i += kTcThreads) {
+                    const int uu = i / (kQ4Unit / 16), o = (i - uu * (kQ4Unit / 16)) * 16;
+                    cp16(sl + kTcB + uu * kQ4Unit + o, u0 + (long long)uu * ngh * kQ4Unit + o);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int q = (tid >> 3) + 32 * j;
+                    if (q < nb)
+                        cp16z(sl + boff[j], x + (xrow[j] < 0 ? 0 : xrow[j]) + kc * kGroup + c8 * 8, xrow[j] >= 0);
+                }
+            }
+            cp_commit();
+        };
+        prefetch(0);
+        prefetch(1);
+        const int u = tid >> 5, g8 = lane >> 2, t = lane & 3;
+        const int row0 = u * 16 + g8, row1 = row0 + 8;
+        const uint32_t o00 = tc::kstep_off(row0, 2 * t), o01 = tc::kstep_off(row0, 2 * t + 8);
+        const uint32_t o10 = tc::kstep_off(row1, 2 * t), o11 = tc::kstep_off(row1, 2 * t + 8);
+        for (int kc = 0; kc < n_gd; ++kc, ++cc) {
+            const int st = cc & 1;
+            char* sl = slots + (kc % kTcSlots) * kTcSlot;
+            char* sA = astage + st * kTcA;
+            // chunk kc's copies landed (every thread's, after the barrier); the A
+            // stage and the slot of chunk kc + 2 (that of chunk kc - 2) are free
+            // once the MMAs of the chunk two before completed (one thread waits)
+            cp_wait_1();
+            if (tid == 0 && cc >= 2 && !tc_wait(&bar[st], (uint32_t)(((cc - 2) >> 1) & 1))) bad = 1;
+            __syncthreads();
+            if (bad) break;
+            {
+                const char* unit = sl + kTcB + u * kQ4Unit;
+                const uint4 wv = *reinterpret_cast<const uint4*>(unit + 16 * lane);
+                const uint2 sc = *reinterpret_cast<const uint2*>(unit + 512 + 8 * g8);
+                const __half2 sb0 = *reinterpret_cast<const __half2*>(&sc.x);   // (s, b) row g8
+                const __half2 sb1 = *reinterpret_cast<const __half2*>(&sc.y);   // (s, b) row g8 + 8
+                const __half2 s20 = __low2half2(sb0), b20 = __high2half2(sb0);
+                const __half2 s21 = __low2half2(sb1), b21 = __high2half2(sb1);
+                const uint32_t wq[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    char* a = sA + ks * 128 * 32;
+                    const uint32_t w = wq[ks];
+                    *reinterpret_cast<uint32_t*>(a + o00) = deq2(w, s20, b20);          // k 2t, 2t+1 of row g8
+                    *reinterpret_cast<uint32_t*>(a + o01) = deq2(w >> 8, s20, b20);     // k 2t+8, 2t+9
+                    *reinterpret_cast<uint32_t*>(a + o10) = deq2(w >> 4, s21, b21);     // row g8 + 8
+                    *reinterpret_cast<uint32_t*>(a + o11) = deq2(w >> 12, s21, b21);
+                }
+            }
+            tc::fence_async_smem();   // the generic-proxy writes (A) and the copies (B) to the tensor core
+            prefetch(kc + 2);
+            __syncthreads();
+            if (tid == 0) {
+                tc::fence_after_sync();
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sl);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_f16(taddr, tc::smem_desc(a0 + ks * 128 * 32), tc::smem_desc(b0 + ks * kTcTok * 32), idesc,
+                                kc > 0 || ks > 0);
+                tc::mma_commit(&bar[st]);
+            }
+        }
+        cp_wait_0();   // the item's trailing (empty) copy groups
+        if (bad) break;
+        // the accumulator is complete once the last chunk's commit arrived
+        if (tid == 0 && !tc_wait(&bar[(cc - 1) & 1], (uint32_t)(((cc - 1) >> 1) & 1))) bad = 1;
+        __syncthreads();
+        if (bad) break;
+        tc::fence_after_sync();
+        {
+            // warp w: TMEM lanes 32 (w % 4) .. (rows: packed tiles 2 (w % 4), + 1),
+            // columns (tokens) of half w / 4 of the block
+            const int qd = wid & 3, c_lo = (wid >> 2) * (kTcTok / 2);
+            const int tile = mt * 8 + 2 * qd + (lane >> 4);
+            const int arow = tile * kHalfRow + (lane & 7);
+            const bool gate_lane = (lane & 8) == 0;
+            for (int c0 = c_lo; c0 < c_lo + kTcTok / 2 && c0 < nb; c0 += 8) {
+                float v[8];
+                tc::tmem_ld8(taddr + ((uint32_t)(32 * qd) << 16) + (uint32_t)c0, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float other = __shfl_xor_sync(0xffffffffu, v[j], 8);
+                    const int q = c0 + j;
+                    if (!gate_lane || q >= m) continue;
+                    float gate = v[j], up = other;
+                    if (S.shared && lora) {
+                        const int b = S.toks ? S.toks[tb + q] : tb + q;
+                        const __half* bg = Ly.lora_Bg + (long long)arow * r;
+                        const __half* bu = Ly.lora_Bu + (long long)arow * r;
+                        float dg = 0.f, du = 0.f;
+                        for (int qq = 0; qq < r; ++qq) {
+                            dg += __half2float(bg[qq]) * la[b * 32 + qq];
+                            du += __half2float(bu[qq]) * la[b * 32 + 16 + qq];
+                        }
+                        gate += Ly.lora_scale * dg;
+                        up += Ly.lora_scale * du;
+                    }
+                    act[(long long)(S.pos0 + tb + q) * Imax + arow] = silu_f(gate) * up;
+                }
+            }
+        }
+        // every read of the accumulator done before the next item's MMAs overwrite it
+        tc::fence_before_sync();
+        __syncthreads();
+    }
+    cp_wait_0();
+    if (bad && tid == 0) record_error(hdr, EDGE0_ETIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (wid == 0) tc::tmem_dealloc(taddr, kTcTok);
+}
+
 // ------------------------------------------------------------- k_down -------
 // down of one expert for all of its tokens: warp w of CTA x takes the 16 output
 // rows of row tile 8 x + w over all of the expert's act rows, 16 tokens per
@@ -744,39 +970,47 @@ __global__ void __launch_bounds__(256, 3) k_down(const LayerP Ly, const Disp* D,
 }
 
 // ---------------------------------------------------------- k_lora_vd -------
-// One CTA per (token, 256 output rows): v = A_down act_shared (r values, each
-// CTA of the token recomputes them), y += (alpha/r) B_down v for its rows.
+// One CTA per block of 8 tokens: warp j forms v = A_down act_shared of token j
+// of the block (r values), then every thread takes output rows tid, tid + 256,
+// ... and adds (alpha/r) B_down[row] v to the block's tokens (one read of a
+// B_down row serves the 8 tokens).
+constexpr int kLoraTok = 8;
 __global__ void __launch_bounds__(256) k_lora_vd(const float* act, int Imax, int pos0, const __half* AdT,
-                                                 const __half* Bd, int r, int Is, int d, float scale, float* y) {
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    __shared__ float red[8][16];
-    __shared__ float vs[16];
-    float acc[16];
+                                                 const __half* Bd, int r, int Is, int d, int B, float scale, float* y) {
+    const int b0 = blockIdx.x * kLoraTok, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    __shared__ float vs[kLoraTok][16];
+    {
+        const int b = b0 + wid;
+        float acc[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-    const float* a = act + (long long)(pos0 + b) * Imax;
-    for (int k = tid; k < Is; k += 256) {
-        const float av = a[k];
+        for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+        if (b < B) {
+            const float* a = act + (long long)(pos0 + b) * Imax;
+            for (int k = lane; k < Is; k += 32) {
+                const float av = a[k];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (q < r) acc[q] += __half2float(AdT[(long long)k * r + q]) * av;
-    }
+                for (int q = 0; q < 16; ++q)
+                    if (q < r) acc[q] += __half2float(AdT[(long long)k * r + q]) * av;
+            }
+        }
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const float s = warp_sum(acc[q]);
-        if (lane == 0) red[wid][q] = s;
-    }
-    __syncthreads();
-    if (tid < 16) {
-        float s = 0.f;
-        for (int w = 0; w < 8; ++w) s += red[w][tid];
-        vs[tid] = s;
+        for (int q = 0; q < 16; ++q) {
+            const float sq = warp_sum(acc[q]);
+            if (lane == 0) vs[wid][q] = sq;
+        }
     }
     __syncthreads();
-    for (int row = blockIdx.y * 256 + tid; row < d && row < (int)(blockIdx.y + 1) * 256; row += 256) {
-        float s = 0.f;
-        for (int q = 0; q < r; ++q) s += __half2float(Bd[(long long)row * r + q]) * vs[q];
-        y[(long long)b * d + row] += scale * s;
+    const int nb = min(kLoraTok, B - b0);
+    for (int row = tid; row < d; row += 256) {
+        float bd[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) bd[q] = q < r ? __half2float(Bd[(long long)row * r + q]) : 0.f;
+        for (int j = 0; j < nb; ++j) {
+            float sj = 0.f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) sj += bd[q] * vs[j][q];
+            y[(long long)(b0 + j) * d + row] += scale * sj;
+        }
     }
 }
 
@@ -824,7 +1058,7 @@ namespace {
 // ([L][B][K], or the workspace when null).  Validates nothing beyond what the
 // caller checked; enqueues on `st`.
 int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
-    const bool prefill = p.mode == MODE_PREFILL;
+    const bool prefill = p.mode == MODE_PREFILL, tcgu = prefill && p.tc_gu;
     const int L = p.L, B = p.B, K = p.K, d = p.d, E = p.E, I = p.I, Is = p.Is, H = p.H, r = p.r;
     const int Imax = I > Is ? I : Is;
     const BatchWs W = prefill ? batch_ws_layout(1, B, d, E, K, Imax, 16) : batch_ws_layout(p.Ls, B, d, E, K, Imax, H);
@@ -844,7 +1078,9 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
     const int step = prefill ? 0 : p.step, par = step & 1;
     const int slots = (B * K < E ? B * K : E) + 1;
     const int cap = disp_cap(B, K, E);
-    const int items_gu = (B * K + kGuTok - 1) / kGuTok + slots + (B + kGuTok - 1) / kGuTok;
+    // gate/up on the tcgen05 kernel (prefill, when asked): blocks of kTcTok tokens
+    const int blk_gu = tcgu ? kTcTok : kGuTok;
+    const int items_gu = (B * K + blk_gu - 1) / blk_gu + slots + (B + blk_gu - 1) / blk_gu;
     const int items_dn = (B * K + kDnTok - 1) / kDnTok + slots + (B + kDnTok - 1) / kDnTok;
     auto ok = [] { return cudaGetLastError() == cudaSuccess; };
     // staged B fragments (+ group sums) of one token block
@@ -857,16 +1093,21 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
         cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return EDGE0_ECUDA;
     if (smem_gu > (size_t)smem_max || smem_dn > (size_t)smem_max) return EDGE0_EUNSUPPORTED;   // d or I too large
-    static size_t done_gu = 0, done_dn = 0;
+    static size_t done_gu = 0, done_dn = 0, done_tc = 0;
     if (!smem_opt_in(k_gu, smem_gu, &done_gu) || !smem_opt_in(k_down, smem_dn, &done_dn)) return EDGE0_ECUDA;
+    if (tcgu && !smem_opt_in(k_gu_tc, kTcSmem, &done_tc)) return EDGE0_ECUDA;
     // expert grids: the CTAs that fit on the GPU at once, each looping over items
     int nsm = 0, occ_gu = 0, occ_dn = 0;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_gu, k_gu, kGuWarps * 32, smem_gu) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_dn, k_down, 256, smem_dn) != cudaSuccess)
         return EDGE0_ECUDA;
-    const int gu_x = (Imax / kHalfRow + kGuWarps - 1) / kGuWarps, dn_x = (d / kRowTile + kExpWarps - 1) / kExpWarps;
-    const int gu_y = std::max(1, std::min(items_gu, nsm * std::max(occ_gu, 1) / gu_x));
+    int occ_tc = 1;
+    if (tcgu && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_tc, k_gu_tc, kTcThreads, kTcSmem) != cudaSuccess)
+        return EDGE0_ECUDA;
+    const int gu_x = tcgu ? Imax / (8 * kHalfRow) : (Imax / kHalfRow + kGuWarps - 1) / kGuWarps;
+    const int dn_x = (d / kRowTile + kExpWarps - 1) / kExpWarps;
+    const int gu_y = std::max(1, std::min(items_gu, nsm * std::max(tcgu ? occ_tc : occ_gu, 1) / gu_x));
     const int dn_y = std::max(1, std::min(items_dn, nsm * std::max(occ_dn, 1) / dn_x));
     int rc = EDGE0_OK;
     for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
@@ -892,7 +1133,7 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
             w = wsel;
         }
         if (rc) return rc;
-        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, kGuTok, kDnTok, cap, D, tok, wt, hdr);
+        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, blk_gu, kDnTok, cap, D, tok, wt, hdr);
         if (!ok()) return EDGE0_ECUDA;
         const int lora = (Ly.flags & LF_LORA) ? 1 : 0;
         if (lora) {
@@ -901,15 +1142,19 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
             if (rc == EDGE0_OK) rc = dense<false>(Ly.lora_Au, 0, r, d, x, nullptr, d, B, la + 16, 32, false, st);
             if (rc) return rc;
         }
-        k_gu<<<dim3(gu_x, gu_y), kGuWarps * 32, smem_gu, st>>>(
-            Ly, D, tok, wt, x, xsum, la, lora, r, B, K, d, I, Is, Imax, act, hdr);
+        if (tcgu)
+            k_gu_tc<<<dim3(gu_x, gu_y), kTcThreads, kTcSmem, st>>>(Ly, D, tok, wt, x, la, lora, r, B, K, d, I, Is,
+                                                                 Imax, act, hdr);
+        else
+            k_gu<<<dim3(gu_x, gu_y), kGuWarps * 32, smem_gu, st>>>(
+                Ly, D, tok, wt, x, xsum, la, lora, r, B, K, d, I, Is, Imax, act, hdr);
         if (!ok()) return EDGE0_ECUDA;
         k_down<<<dim3(dn_x, dn_y), 256, smem_dn, st>>>(
             Ly, D, tok, wt, act, B, K, d, I, Is, Imax, y, hdr);
         if (!ok()) return EDGE0_ECUDA;
         if (lora) {
-            k_lora_vd<<<dim3(B, (d + 255) / 256), 256, 0, st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is, d,
-                                                               Ly.lora_scale, y);
+            k_lora_vd<<<(B + kLoraTok - 1) / kLoraTok, 256, 0, st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is,
+                                                                      d, B, Ly.lora_scale, y);
             if (!ok()) return EDGE0_ECUDA;
         }
     }

@@ -114,6 +114,7 @@ struct Prog {
     int ring1;                // bytes of its shared-memory ring
     const char* tab1;         // device table of every CTA's plan and block layout
     const LayerP* ly1;        // device copy of layers[0..L) (the batch-1 kernel reads it there)
+    int tc_gu;                // prefill: gate/up on the tcgen05 kernel
     int n_heads1;             // layers that own a head, in order (batch-1 kernel)
     int heads1[EDGE0_MAX_LAYERS];
     long long ws_bytes;       // workspace bytes (the trace area is at its end)

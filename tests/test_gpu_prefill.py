@@ -37,7 +37,7 @@ def _routing_kw(cfg):
                 G=cfg.topk_groups if cfg.route_kind else None)
 
 
-def _prefill_teacher_forced(cfg, T, seed):
+def _prefill_teacher_forced(cfg, T, seed, flags=0):
     model = inputs.make_model(cfg, seed=seed, gamma="random")
     dm = binding.DeviceModel(model, DEV)
     ref = oracle.Stack(model, B=T)
@@ -47,7 +47,7 @@ def _prefill_teacher_forced(cfg, T, seed):
     ties = []
     for l in range(cfg.L):
         h = h_ref.to(DEV).contiguous()
-        binding.prefill(dm, h, ws, ids_out=ids, layers=slice(l, l + 1))
+        binding.prefill(dm, h, ws, ids_out=ids, layers=slice(l, l + 1), flags=flags)
         h_in = h_ref.clone()
         rec = ref.step(h_ref, 0, layers=[l])       # h_ref becomes the oracle's output of layer l
         torch.cuda.synchronize()
@@ -68,20 +68,28 @@ def _prefill_teacher_forced(cfg, T, seed):
     return ties
 
 
+KERNELS = [0, binding.PREFILL_TCGEN05_GATE_UP]
+KERNEL_IDS = ["mma_sync", "tcgen05"]
+
+
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("T", [1, 100, 257])
-def test_prefill_toy_teacher_forced(T):
-    ties = _prefill_teacher_forced(configs.TOY.with_(L=2), T, seed=21)
+def test_prefill_toy_teacher_forced(T, flags):
+    ties = _prefill_teacher_forced(configs.TOY.with_(L=2), T, seed=21, flags=flags)
     print("near-ties (layer, token):", ties)
 
 
-def test_prefill_35b_shapes_teacher_forced():
-    ties = _prefill_teacher_forced(configs.STACK35.with_(L=2, prerouted=(1,), head_owner_last=0), 48, seed=22)
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
+def test_prefill_35b_shapes_teacher_forced(flags):
+    ties = _prefill_teacher_forced(configs.STACK35.with_(L=2, prerouted=(1,), head_owner_last=0), 48, seed=22,
+                                   flags=flags)
     print("near-ties (layer, token):", ties)
 
 
-def test_prefill_8b_sigmoid_group_teacher_forced():
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
+def test_prefill_8b_sigmoid_group_teacher_forced(flags):
     cfg = configs.STACK8.with_(L=2, E=64, prerouted=(1,), head_owner_first=0, head_owner_last=0)
-    ties = _prefill_teacher_forced(cfg, 40, seed=23)
+    ties = _prefill_teacher_forced(cfg, 40, seed=23, flags=flags)
     print("near-ties (layer, token):", ties)
 
 
@@ -115,9 +123,10 @@ def test_prefill_rejects_bad_arguments():
     h = torch.zeros(T, cfg.d, dtype=torch.float16, device=DEV)
     lib = binding.lib()
     P = binding._ptr
-    assert lib.edge0_prefill(dm.layers, cfg.L, P(h), 0, None, P(ws), ws.numel(), None) == binding.EDGE0_EINVAL
-    assert lib.edge0_prefill(dm.layers, cfg.L, P(h), T, None, P(ws), ws.numel() - 1, None) == binding.EDGE0_EINVAL
-    assert lib.edge0_prefill(dm.layers, cfg.L, P(h), 8193, None, P(ws), ws.numel(), None) == binding.EDGE0_EINVAL
+    assert lib.edge0_prefill(dm.layers, cfg.L, P(h), 0, None, 0, P(ws), ws.numel(), None) == binding.EDGE0_EINVAL
+    assert lib.edge0_prefill(dm.layers, cfg.L, P(h), T, None, 0, P(ws), ws.numel() - 1, None) == binding.EDGE0_EINVAL
+    assert lib.edge0_prefill(dm.layers, cfg.L, P(h), 8193, None, 0, P(ws), ws.numel(), None) == binding.EDGE0_EINVAL
+    assert lib.edge0_prefill(dm.layers, cfg.L, P(h), T, None, 2, P(ws), ws.numel(), None) == binding.EDGE0_EINVAL
     assert binding.prefill_workspace_bytes(cfg, 8193) == 0
 
 

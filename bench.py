@@ -378,43 +378,25 @@ def run_batched(args, rank, world, cfg):
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    # host-tier arms: copy-engine prefetch of the prerouted layers' predictions
-    # (the product path), least-recently-used caching of every layer's executed
-    # experts without a prediction, or no copies at all (resident set frozen)
+    # host-tier arms: the device-planned prefetch of the prerouted layers'
+    # predictions, with least-recently-used caching of the executed experts on
+    # the layers that route themselves (the product path); least-recently-used
+    # caching of every layer's executed experts, no prediction; or no copies at
+    # all (resident set frozen).  The plan is enqueued after the step's head flush on
+    # the compute stream; the copies run on the pool's copy stream; nothing waits.
+    own_layers = [l for l in range(cfg.L) if l not in prerouted]
+
     def step(t, prefetch="prediction"):
         binding.decode_step(dm, st, h_all[t % n_in], t)
         if pool is not None and prefetch == "prediction":
-            pool.prefetch(st, t, prerouted)
+            pool.prefetch(st, t, predicted=prerouted, cached=own_layers)
         elif pool is not None and prefetch == "executed":
-            pool.prefetch(st, t, range(cfg.L), source="executed")
+            pool.prefetch(st, t, cached=range(cfg.L))
 
-    def cold_pass(prefetch, n):
-        """Untimed steps, each synchronised: the share of (layer, executed
-        expert) pairs that the step found outside HBM (read from host memory),
-        over all layers and over the prerouted ones."""
-        nonlocal t
-        cold = [0, 0]
-        tot = [0, 0]
-        for _ in range(n):
-            res = [pool.resident(l) for l in range(cfg.L)]   # the map this step runs with
-            step(t, prefetch=None)
-            ex = st.exec_ids[t & 1].cpu().numpy()
-            if prefetch == "prediction":
-                pool.prefetch(st, t, prerouted)
-            elif prefetch == "executed":
-                pool.prefetch(st, t, range(cfg.L), source="executed")
-            for l in range(cfg.L):
-                ids = np.unique(ex[l])
-                c = int((res[l][ids] < 0).sum())
-                cold[0] += c
-                tot[0] += len(ids)
-                if l in prerouted:
-                    cold[1] += c
-                    tot[1] += len(ids)
-            t += 1
-        barrier()
-        return round(cold[0] / max(tot[0], 1), 4), round(cold[1] / max(tot[1], 1), 4), tot[0] / n
-
+    if pool is not None:
+        # an empty pool fills at ~200 copies per step: 64 slots x 40 layers take
+        # a dozen steps or more before the arm reaches its steady state
+        args.warmup = max(args.warmup, 24)
     t = 0
     for _ in range(args.warmup):
         step(t)
@@ -435,36 +417,54 @@ def run_batched(args, rank, world, cfg):
         barrier()
         return a.elapsed_time(b)
 
-    hits0, copies0 = pool.stats() if pool is not None else (0, 0)
+    def arm_record(ms, s0, s1, c0, c1):
+        """The arm's residency over its timed steps, from the device counters:
+        cold fraction = executed (layer, expert) pairs read from host memory;
+        loads = whole-expert transfers from host memory, either copies made off
+        the critical path or reads inside the expert kernels."""
+        ebytes = pool.gu_bytes + pool.dn_bytes
+        dt = c1 - c0                                     # [L, 2]
+        pre = np.array(prerouted, dtype=np.int64)
+        act, cold = dt[:, 0].sum(), dt[:, 1].sum()
+        copies = s1["published"] - s0["published"]
+        return {
+            "tokens_per_s": round(B * args.steps / (ms / 1e3), 2),
+            "ms_per_step": round(ms / args.steps, 3),
+            "cold_fraction": round(cold / max(act, 1), 4),
+            "cold_fraction_prerouted_layers": round(dt[pre, 1].sum() / max(dt[pre, 0].sum(), 1), 4),
+            "active_experts_per_step": round(act / args.steps, 1),
+            "copies_per_step": round(copies / args.steps, 2),
+            "copied_mb_per_step": round((s1["bytes"] - s0["bytes"]) / args.steps / 1e6, 1),
+            "host_reads_per_step": round(cold / args.steps, 2),
+            "host_read_mb_per_step": round(cold * ebytes / args.steps / 1e6, 1),
+            "loads_per_step": round((copies + cold) / args.steps, 2),
+            "mib_per_load": round(ebytes / 2 ** 20, 3),
+            "failed_copies": s1["failed"] - s0["failed"],
+            "plans_skipped": s1["skipped"] - s0["skipped"],
+            "hit_rate": round((s1["hits"] - s0["hits"]) / max(s1["requests"] - s0["requests"], 1), 4),
+        }
+
+    if pool is not None:
+        s0, c0 = pool.stats(), pool.tiers()
     with ClockSampler(dev.index) as clk:
         region_ms = timed()
     err = st.error()
     assert err == 0, f"kernel error in the timed region: {binding.status_string(err)}"
-    hits1, copies1 = pool.stats() if pool is not None else (0, 0)
     # bytes from the routing of the last two timed steps
     ex = st.exec_ids.cpu().numpy()
     own = cfg.L - len(cfg.prerouted)
     step_bytes = statistics.mean(batched_bytes_per_step(cfg, ex[p], own) for p in (0, 1))
     arms = {}
     if pool is not None:
-        ebytes = pool.gu_bytes + pool.dn_bytes
-        for arm in ("prediction", "executed", None):
+        arms["prediction"] = arm_record(region_ms, s0, pool.stats(), c0, pool.tiers())
+        for arm in ("executed", None):
             for _ in range(args.warmup):   # the arm's steady state
                 step(t, arm)
                 t += 1
-            c0 = pool.stats()[1]
-            ms = region_ms if arm == "prediction" else timed(prefetch=arm)
-            if arm == "prediction":
-                c0 = copies0
-                c1 = copies1
-            else:
-                c1 = pool.stats()[1]
-            cold_all, cold_pre, active = cold_pass(arm, 8)
-            arms[arm or "frozen"] = {
-                "tokens_per_s": round(B * args.steps / (ms / 1e3), 2),
-                "cold_fraction": cold_all, "cold_fraction_prerouted_layers": cold_pre,
-                "copied_mb_per_step": round((c1 - c0) / args.steps * ebytes / 1e6, 1),
-                "host_read_mb_per_step": round(cold_all * active * ebytes / 1e6, 1)}
+            barrier()
+            s0, c0 = pool.stats(), pool.tiers()
+            ms = timed(prefetch=arm)
+            arms[arm or "frozen"] = arm_record(ms, s0, pool.stats(), c0, pool.tiers())
         assert st.error() == 0
 
     # end to end: pinned host input -> device, decode step, device -> host, every step
@@ -479,7 +479,7 @@ def run_batched(args, rank, world, cfg):
         h.copy_(h_host[i], non_blocking=True)
         binding.decode_step(dm, st, h, t)
         if pool is not None:
-            pool.prefetch(st, t, prerouted)
+            pool.prefetch(st, t, predicted=prerouted, cached=own_layers)
         h_host[i].copy_(h, non_blocking=True)
         t += 1
     b.record(stream)
@@ -517,10 +517,12 @@ def run_batched(args, rank, world, cfg):
         },
         "e2e": {"value": round(tokens / (e2e_ms / 1e3), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": B * d * 2, "d2h_bytes_per_step": B * d * 2},
-        # per layer: norm, dispatch, gate/up, down, LoRA A (2), LoRA down; + router
-        # and top-K on own-routed layers; final residual; per head: fc1, one-hot +
-        # GELU, fc2, linear_init, one-hot, top-K
-        "gpu_launches": args.steps * (7 * cfg.L + 2 * own + 1 + 6 * len(cfg.head_owners())),
+        # per layer: norm, dispatch, LoRA A (both matrices), gate/up, down, LoRA
+        # down; + router and top-K on own-routed layers; final residual; the head
+        # flush: fc1, one-hot + GELU, fc2, linear_init, one-hot, top-K, each one
+        # launch over all heads; + the pool's planner and copy kernel
+        "gpu_launches": args.steps * (6 * cfg.L + 2 * own + 1 + (6 if cfg.head_owners() else 0)
+                                      + (2 if pool is not None else 0)),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": "batched decode step (per layer: norm, routing, dispatch, gate/up, down, LoRA; "
@@ -530,18 +532,22 @@ def run_batched(args, rank, world, cfg):
         "clocks": clk.summary(),
     }
     if pool is not None:
-        req = (hits1 - hits0) + (copies1 - copies0)
         line["pool"] = {"slots_per_layer": pool.n_slots, "experts": cfg.E,
-                        "prefetch_hit_rate": round((hits1 - hits0) / max(req, 1), 4),
-                        "experts_copied_per_step": round((copies1 - copies0) / args.steps, 2),
+                        "prefetch_hit_rate": arms["prediction"]["hit_rate"],
+                        "experts_copied_per_step": arms["prediction"]["copies_per_step"],
                         "prefetch_off_tokens_per_s": arms["frozen"]["tokens_per_s"],
                         "prefetch_off": "no copies: resident set frozen, misses read from host memory",
                         "arms": arms,
-                        "arms_note": ("prediction: copy-engine prefetch of the prerouted layers' predicted "
-                                      "experts (the timed line); executed: LRU caching of every layer's "
-                                      "executed experts, no prediction; frozen: no copies. cold_fraction: "
-                                      "executed (layer, expert) pairs read from host memory, from 8 "
-                                      "synchronised steps after each arm's timed region")}
+                        "arms_note": ("prediction: device-planned prefetch of the prerouted layers' predicted "
+                                      "experts, LRU caching of the executed experts on the self-routed "
+                                      "layers, copies on a second stream, nothing waits (the timed line); "
+                                      "executed: the same pool caching every layer's executed experts (LRU, "
+                                      "no prediction); frozen: no copies. Each arm measured over its own "
+                                      "timed steps from the device counters: cold_fraction = executed "
+                                      "(layer, expert) pairs read from host memory when their layer "
+                                      "dispatched; a load = one expert's packed gate/up + down moved from "
+                                      "host memory, by a copy off the critical path or by the expert "
+                                      "kernels' own reads")}
     return line
 
 

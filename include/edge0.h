@@ -112,6 +112,10 @@ typedef struct {
                                   experts stacked, or NULL: the batch-1 kernel reads
                                   down by output row tiles from here               */
     const void* sh_down_rows;  /* the shared expert's down, same layout, or NULL    */
+    unsigned long long* tier_counts; /* batched path with a slot table: device [2] u64,
+                                  or NULL.  Each layer adds its active routed experts
+                                  to [0] and those of them read from the host tier
+                                  (published slot -1 when the layer dispatched) to [1] */
 } edge0_moe_desc;
 
 /* ---- one unmerged LoRA projection [S3.3]: y += (alpha/r) B (A v) ---- */
@@ -319,38 +323,71 @@ int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h_inout, int 
 
 /* ---- expert pool with a host tier [S3.1 "SSD Streaming Expert Layers", S3.2
  * "Motivation", S5.3]: n_slots device slots per layer in front of every
- * expert's packed weights in pinned host memory.  The device slot table
- * (edge0_moe_desc.slot_table, [E] int32) maps an expert to its slot or -1 (read
- * from the host tier).  Host-side object; not thread-safe.
- *   edge0_pool_create      L layers of E experts; one expert's packed gate/up and
- *                          down take gu_bytes and dn_bytes.
- *   edge0_pool_set_layer   the layer's host stacks [E][..] (pinned), its device
- *                          slot stacks [n_slots][..] and its device slot table.
- *   edge0_pool_plan        marks ids[0..n) (duplicates allowed) as requested and
- *                          assigns each requested expert that is not resident a
- *                          slot: a free one, else the least recently requested
- *                          slot whose expert is not requested now; experts left
- *                          without a slot stay in the host tier.  Returns the
- *                          copies to make (expert, slot) without making them.
- *   edge0_pool_prefetch    plan + one cudaMemcpyAsync per copied matrix on
- *                          `stream`, then the slot table; *copied = experts
- *                          copied.  Kernels that read the layer must not run
- *                          between this call and the completion of its copies:
- *                          record an event on `stream` after it and pass it as
- *                          the layer's `ready` event.
- *   edge0_pool_stats       requested experts found resident / copied, so far.
- *   edge0_pool_resident    the planner's map of layer l: slot_of[e] = the slot
- *                          of expert e, or -1 (host tier), E entries written to
- *                          host memory.  After a prefetch it is the map the
- *                          layer's next decode uses once its copies are done. */
+ * expert's packed weights in pinned host memory.  The published slot table
+ * (edge0_moe_desc.slot_table, [E] int32, device) maps an expert to its slot or
+ * -1; the batched kernels read an expert whose entry is -1 from the host tier.
+ *
+ * Policy (edge0_pool_plan): a request marks experts as requested now; each
+ * requested expert that is not in the planner's map takes a free slot, else the
+ * least recently requested slot whose expert is not requested now (lowest
+ * index on equal recency); experts left without a slot stay in the host tier.
+ *
+ * edge0_pool_create: L <= EDGE0_MAX_LAYERS layers of E <= EDGE0_MAX_E experts,
+ *   1 <= n_slots <= E; one expert's packed gate/up and down take gu_bytes and
+ *   dn_bytes (multiples of 16).  edge0_pool_set_layer: the layer's host stacks
+ *   [E][..], its slot stacks [n_slots][..] and its slot table (16-byte aligned).
+ * Device mode (the product path), after edge0_pool_device_init (every layer set;
+ *   allocates the pool's device state, empties every slot table):
+ *   edge0_pool_prefetch_async(ids, n, stream, copy_stream): ids[l] is a device
+ *     pointer to n expert ids of layer l (e.g. its prediction for the next
+ *     step), or NULL to leave layer l alone.  Enqueues on `stream` one planner
+ *     CTA per layer; an evicted expert leaves the published table before any
+ *     later work of `stream` reads it.  Then on `copy_stream` (after the
+ *     planner) one copy kernel moves the planned experts from host memory into
+ *     their slots and publishes each (release store of its table entry) once
+ *     all of its bytes are in place.  Neither the host nor `stream` waits for a
+ *     copy: an expert whose copy has not been published is read from the host
+ *     tier.  A layer whose previous copies are still in flight skips this plan
+ *     (counted).  Asynchronous; returns EDGE0_EINVAL on bad arguments.
+ *   edge0_pool_wait(timeout_ns): polls from the host until the last copy pass
+ *     enqueued has ended, at most timeout_ns; EDGE0_ETIMEOUT when it has not
+ *     (the copies go on; nothing is cancelled).  For callers that want the
+ *     published map settled, e.g. before reading it; the decode path never
+ *     calls it.
+ *   edge0_pool_inject(fail_every, delay_ns): host-side fault injection for the
+ *     following copy passes: copy number q fails when fail_every > 0 and
+ *     q % fail_every == fail_every - 1 (its bytes are not moved, it is not
+ *     published, the next plan frees its slot); every copy pass first waits
+ *     delay_ns (at most 1e9, else EDGE0_EINVAL).  0, 0 turns both off.
+ *   edge0_pool_stats_ex / edge0_pool_stats / edge0_pool_resident wait for the
+ *     device (cudaDeviceSynchronize) and read the device counters and the
+ *     published table of layer l.
+ * Host mode (no GPU: the same planner and publication steps over host
+ * buffers; set_layer then takes host buffers for the slots and the table):
+ *   edge0_pool_plan           one request of layer l; returns the copies to make
+ *                             (expert, slot) without making them.
+ *   edge0_pool_host_prefetch  as edge0_pool_prefetch_async's planner: ids[l] host
+ *                             pointers, evicted experts leave the table.
+ *   edge0_pool_host_copy      as the copy kernel: completes every copy in flight
+ *                             (memcpy, publish, or mark failed under injection).
+ * Counters (edge0_pool_stats_ex, out[8]): requests, hits, copies planned,
+ * copies published, copies failed, layer plans skipped, bytes published,
+ * requested ids outside [0, E).  edge0_pool_stats gives hits and copies planned.
+ * Not thread-safe; one pool per device. */
 typedef struct edge0_pool edge0_pool;
 int edge0_pool_create(int L, int E, int n_slots, size_t gu_bytes, size_t dn_bytes, edge0_pool** out);
 int edge0_pool_set_layer(edge0_pool* pool, int l, const void* host_gu, const void* host_dn, void* dev_gu,
                          void* dev_dn, int32_t* dev_slot_table);
 int edge0_pool_plan(edge0_pool* pool, int l, const int32_t* ids, int n, int32_t* out_expert,
                     int32_t* out_slot, int* n_copy);
-int edge0_pool_prefetch(edge0_pool* pool, int l, const int32_t* ids, int n, cudaStream_t stream,
-                        int* copied);
+int edge0_pool_host_prefetch(edge0_pool* pool, const int32_t* const* ids, int n);
+int edge0_pool_host_copy(edge0_pool* pool);
+int edge0_pool_device_init(edge0_pool* pool);
+int edge0_pool_prefetch_async(edge0_pool* pool, const int32_t* const* ids, int n, cudaStream_t stream,
+                              cudaStream_t copy_stream);
+int edge0_pool_wait(edge0_pool* pool, unsigned long long timeout_ns);
+int edge0_pool_inject(edge0_pool* pool, int fail_every, unsigned long long delay_ns);
+int edge0_pool_stats_ex(const edge0_pool* pool, long long* out, int n);
 int edge0_pool_stats(const edge0_pool* pool, long long* hits, long long* copies);
 int edge0_pool_resident(const edge0_pool* pool, int l, int32_t* slot_of);
 void edge0_pool_destroy(edge0_pool* pool);

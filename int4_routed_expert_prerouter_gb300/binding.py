@@ -49,7 +49,7 @@ class MoeDesc(C.Structure):
     _fields_ = [("d", C.c_int), ("E", C.c_int), ("K", C.c_int), ("I", C.c_int), ("Is", C.c_int),
                 ("gate_up", P), ("down", P), ("sh_gate_up", P), ("sh_down", P),
                 ("slot_table", P), ("n_slots", C.c_int), ("host_gate_up", P), ("host_down", P),
-                ("down_rows", P), ("sh_down_rows", P)]
+                ("down_rows", P), ("sh_down_rows", P), ("tier_counts", P)]
 
 
 class LoraDesc(C.Structure):
@@ -98,7 +98,13 @@ def _declare(L):
     L.edge0_pool_create.argtypes = [C.c_int, C.c_int, C.c_int, C.c_size_t, C.c_size_t, C.POINTER(P)]
     L.edge0_pool_set_layer.argtypes = [P, C.c_int, P, P, P, P, P]
     L.edge0_pool_plan.argtypes = [P, C.c_int, P, C.c_int, P, P, C.POINTER(C.c_int)]
-    L.edge0_pool_prefetch.argtypes = [P, C.c_int, P, C.c_int, P, C.POINTER(C.c_int)]
+    L.edge0_pool_host_prefetch.argtypes = [P, P, C.c_int]
+    L.edge0_pool_host_copy.argtypes = [P]
+    L.edge0_pool_device_init.argtypes = [P]
+    L.edge0_pool_prefetch_async.argtypes = [P, P, C.c_int, P, P]
+    L.edge0_pool_inject.argtypes = [P, C.c_int, C.c_ulonglong]
+    L.edge0_pool_wait.argtypes = [P, C.c_ulonglong]
+    L.edge0_pool_stats_ex.argtypes = [P, P, C.c_int]
     L.edge0_pool_stats.argtypes = [P, C.POINTER(C.c_longlong), C.POINTER(C.c_longlong)]
     L.edge0_pool_resident.argtypes = [P, C.c_int, P]
     L.edge0_pool_destroy.argtypes = [P]
@@ -137,7 +143,9 @@ EXPORTED = ["edge0_status_string", "edge0_q4_gate_up_packed_bytes", "edge0_pack_
             "edge0_lora_delta", "edge0_decode_layer", "edge0_decode_step",
             "edge0_moe_int4_forward_noalloc", "edge0_noalloc_error", "edge0_prefill_workspace_bytes",
             "edge0_prefill", "edge0_tc_gemm_f16", "edge0_pool_create", "edge0_pool_set_layer",
-            "edge0_pool_plan", "edge0_pool_prefetch", "edge0_pool_stats", "edge0_pool_resident", "edge0_pool_destroy"]
+            "edge0_pool_plan", "edge0_pool_host_prefetch", "edge0_pool_host_copy", "edge0_pool_device_init",
+            "edge0_pool_prefetch_async", "edge0_pool_wait", "edge0_pool_inject", "edge0_pool_stats_ex", "edge0_pool_stats",
+            "edge0_pool_resident", "edge0_pool_destroy"]
 
 
 def status_string(code: int) -> str:
@@ -377,12 +385,15 @@ class DecodeState:
 
 
 class ExpertPool:
-    """Host tier for a DeviceModel's routed experts (edge0_pool_*): every layer's
-    packed experts move to pinned host memory the device can read, and the layer
-    keeps `n_slots` device slots, filled by copy-engine prefetch from the
-    prerouter's prediction one token ahead.  The model's descriptors are pointed
-    at the slots, the slot table and the host stacks; the full device stacks are
+    """Host tier for a DeviceModel's routed experts (edge0_pool_*, device mode):
+    every layer's packed experts move to pinned host memory the device can read,
+    and the layer keeps `n_slots` device slots, filled from the prerouter's
+    prediction one token ahead by the pool's device planner and copy kernel.
+    The model's descriptors are pointed at the slots, the published slot table,
+    the host stacks and a pair of residency counters; the full device stacks are
     released."""
+
+    STATS = ("requests", "hits", "planned", "published", "failed", "skipped", "bytes", "bad_ids")
 
     def __init__(self, dm: "DeviceModel", n_slots: int, copy_stream=None):
         cfg = dm.cfg
@@ -394,7 +405,8 @@ class ExpertPool:
         _check(lib().edge0_pool_create(cfg.L, cfg.E, n_slots, self.gu_bytes, self.dn_bytes,
                                        C.byref(self.pool)), "edge0_pool_create")
         self.copy_stream = copy_stream or torch.cuda.Stream(dev)
-        self.events = [torch.cuda.Event() for _ in range(cfg.L)]
+        # per layer [0]: active routed experts summed over steps, [1]: of them read from host memory
+        self.tier_counts = torch.zeros(cfg.L, 2, dtype=torch.int64, device=dev)
         self.keep = []
         for l in range(cfg.L):
             gu, dn = dm.stacks[l]
@@ -410,38 +422,57 @@ class ExpertPool:
             m = dm.layers[l].moe
             m.gate_up, m.down, m.slot_table, m.n_slots = _ptr(sg), _ptr(sd), _ptr(tb), n_slots
             m.host_gate_up, m.host_down = _ptr(hg), _ptr(hd)
+            m.tier_counts = C.c_void_p(self.tier_counts[l].data_ptr())
             self.keep += [hg, hd, sg, sd, tb]
             dm.stacks[l] = None
+        self.slots = [(self.keep[5 * l + 2], self.keep[5 * l + 3], self.keep[5 * l + 4]) for l in range(cfg.L)]
+        self.host = [(self.keep[5 * l], self.keep[5 * l + 1]) for l in range(cfg.L)]
         torch.cuda.synchronize(dev)
+        _check(lib().edge0_pool_device_init(self.pool), "edge0_pool_device_init")
 
-    def prefetch(self, st: "DecodeState", t: int, layers, source: str = "prediction"):
-        """After step t has completed: make resident, per layer in `layers`, the
-        experts its prediction for step t + 1 names (union over the batch), on the
-        copy stream; the layer's next decode waits for its copies.  With
-        source="executed", the experts step t ran instead (least-recently-used
-        caching without a prediction).  Returns the number of experts copied."""
-        if source not in ("prediction", "executed"):
-            raise ValueError(source)
-        pred = (st.pred_ids if source == "prediction" else st.exec_ids)[t & 1].cpu()
-        total = 0
-        for l in layers:
-            ids = torch.unique(pred[l]).to(torch.int32).contiguous()
-            n = C.c_int(0)
-            _check(lib().edge0_pool_prefetch(self.pool, l, C.c_void_p(ids.data_ptr()), ids.numel(),
-                                             C.c_void_p(self.copy_stream.cuda_stream), C.byref(n)),
-                   "edge0_pool_prefetch")
-            self.events[l].record(self.copy_stream)
-            self.dm.layers[l].ready = C.c_void_p(self.events[l].cuda_event)
-            total += n.value
-        return total
+    def prefetch(self, st: "DecodeState", t: int, predicted=(), cached=(), stream=None):
+        """Enqueue, after step t's work on `stream`, the residency plan of each
+        layer in `predicted` from the experts its prediction for step t + 1 names
+        (union over the batch), and of each layer in `cached` from the experts
+        step t ran (least-recently-used caching, for layers without a
+        prediction); the copies go on the copy stream.  Nothing waits: no host
+        read-back, and the next step reads experts whose copies are still in
+        flight from host memory."""
+        L = self.dm.cfg.L
+        ids = (C.c_void_p * L)()
+        for l in cached:
+            ids[l] = st.exec_ids[t & 1, l].data_ptr()
+        for l in predicted:
+            ids[l] = st.pred_ids[t & 1, l].data_ptr()
+        _check(lib().edge0_pool_prefetch_async(self.pool, ids, st.B * self.dm.cfg.K, _stream(stream),
+                                               C.c_void_p(self.copy_stream.cuda_stream)),
+               "edge0_pool_prefetch_async")
 
-    def stats(self):
-        hits, copies = C.c_longlong(0), C.c_longlong(0)
-        _check(lib().edge0_pool_stats(self.pool, C.byref(hits), C.byref(copies)), "edge0_pool_stats")
-        return hits.value, copies.value
+    def wait(self, timeout_ns) -> int:
+        """Bounded host poll for the last copy pass: EDGE0_OK or EDGE0_ETIMEOUT."""
+        rc = lib().edge0_pool_wait(self.pool, int(timeout_ns))
+        if rc not in (EDGE0_OK, EDGE0_ETIMEOUT):
+            _check(rc, "edge0_pool_wait")
+        return rc
+
+    def inject(self, fail_every=0, delay_ns=0):
+        _check(lib().edge0_pool_inject(self.pool, int(fail_every), int(delay_ns)), "edge0_pool_inject")
+
+    def stats(self) -> dict:
+        """The pool's counters (waits for the device)."""
+        out = (C.c_longlong * 8)()
+        _check(lib().edge0_pool_stats_ex(self.pool, out, 8), "edge0_pool_stats_ex")
+        return dict(zip(self.STATS, list(out)))
+
+    def tiers(self) -> np.ndarray:
+        """[L, 2]: per layer, active routed experts and those of them read from
+        host memory, summed over the steps run so far (waits for the device)."""
+        torch.cuda.synchronize(self.tier_counts.device)
+        return self.tier_counts.cpu().numpy().copy()
 
     def resident(self, l: int) -> np.ndarray:
-        """The planner's map of layer l: slot of each expert, -1 for the host tier."""
+        """The published map of layer l: slot of each expert, -1 for the host tier
+        (waits for the device)."""
         out = np.empty(self.dm.cfg.E, dtype=np.int32)
         _check(lib().edge0_pool_resident(self.pool, l, C.c_void_p(out.ctypes.data)), "edge0_pool_resident")
         return out

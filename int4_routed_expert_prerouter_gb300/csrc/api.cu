@@ -59,6 +59,8 @@ int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P)
     if (m.host_gate_up && (!m.slot_table || !al16(m.host_gate_up) || !al16(m.host_down))) return EDGE0_EINVAL;
     P.gu_host = (const char*)m.host_gate_up;
     P.down_host = (const char*)m.host_down;
+    if (m.tier_counts && ((uintptr_t)m.tier_counts & 7)) return EDGE0_EINVAL;
+    P.tier_counts = m.tier_counts;
     if (!al16(m.down_rows) || !al16(m.sh_down_rows)) return EDGE0_EINVAL;
     P.down_rows = (const char*)m.down_rows;
     P.sh_down_rows = (const char*)m.sh_down_rows;

@@ -9,7 +9,7 @@
 //               (k_dense + k_route)
 //   k_dispatch  tokens grouped by expert: the active experts in id order, each
 //               with its token list and routing weights
-//   k_dense     LoRA A_gate x, A_up x (shared expert)
+//   k_dense_pair  LoRA A_gate x, A_up x (shared expert), one launch
 //   k_gu        gate/up of every active expert and the shared expert over
 //               blocks of up to 32 of its tokens -> act = silu(g) up (fp32)
 //   k_down      down of the same -> y += w act (fp32 reductions)
@@ -17,7 +17,9 @@
 // and after the last layer h = fp16(h + y), then every head of the step (one
 // flush per step: a head's prediction is consumed only at the next token):
 //   z = fc1 x + executed / previous one-hot columns, GELU, logits = fc2 g +
-//   linear_init x + its one-hot columns, top-K -> prediction for the next step.
+//   linear_init x + its one-hot columns, top-K -> prediction for the next step,
+// each stage one launch over all heads (k_dense_heads, k_onehot_heads,
+// k_route_heads).
 //
 // The weights are the same packed layouts as the persistent engine's (int4
 // nibbles enter mma.sync as fp16 subnormals q 2^-24, the epilogue rescales by
@@ -26,6 +28,8 @@
 // tokens (32 for gate/up, 16 for down), not once per token: the contraction
 // becomes a skinny GEMM over the block.
 #include <string.h>
+
+#include <vector>
 
 #include "internal.cuh"
 #include "common.cuh"
@@ -41,7 +45,9 @@ __host__ __device__ inline int disp_cap(int B, int K, int E) {
     return (B * K + 7) / 8 + (B * K < E ? B * K : E) + (B + 7) / 8 + 2;
 }
 // bytes of the dispatch record's fixed part (Disp); the work items follow it
-constexpr long long kDispHead = 6400;
+constexpr long long kDispHead = 8448;
+// room for one head's job of the head flush (HeadJob)
+constexpr long long kHeadJobBytes = 128;
 BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
     BatchWs w;
     auto al = [](long long x) { return (x + 255) / 256 * 256; };
@@ -50,7 +56,9 @@ BatchWs batch_ws_layout(int L, int B, int d, int E, int K, int I, int H) {
     w.xs = o;    o += al((long long)L * B * d * 2);
     w.xsum = o;  o += al((long long)B * (d / kGroup) * 4);
     w.lg = o;    o += al((long long)B * E * 4);
-    w.z = o;     o += al((long long)B * H * 4);
+    // head flush: per head its fc1 output [B][H] then its logits [B][E] (the
+    // heads of a step one run: one memset), then the heads' job table
+    w.z = o;     o += al((long long)L * B * (H + E) * 4) + al((long long)L * kHeadJobBytes);
     w.la = o;    o += al((long long)B * 32 * 4);
     w.wsel = o;  o += al((long long)B * K * 4);
     w.exec = o;  o += al((long long)B * K * 4);
@@ -69,6 +77,7 @@ struct Disp {   // dispatch of one layer (device); fits the workspace's dispatch
     int sexp[EDGE0_MAX_E + 1];
     int soff[EDGE0_MAX_E + 1];
     int scnt[EDGE0_MAX_E + 1];
+    int sslot[EDGE0_MAX_E + 1];       // slot of each active expert (-1: host tier), read once per layer
     int n_gu, n_dn;                   // work items of k_gu / k_down
     int cap;                          // room for the items of each kernel
     // then, kDispHead bytes from the record's start, the work items (slot, first
@@ -154,10 +163,9 @@ __global__ void __launch_bounds__(256) k_norm(__half* h, float* y, int add_y, co
 // (xf, entered as hi + lo fp16).  One CTA per (row tile, 32 tokens, 256-input
 // chunk); its 4 warps split the chunk's 16 steps; fp32 reductions into out.
 template <bool F32IN>
-__global__ void __launch_bounds__(128) k_dense(const char* __restrict__ W, int kmajor, int N, int Kin,
-                                               const __half* __restrict__ xh, const float* __restrict__ xf,
-                                               int ldx, int B, float* out, int ldo) {
-    const int rt = blockIdx.x, tb = blockIdx.y * 32, kc = blockIdx.z;
+__device__ __forceinline__ void dense_tile(const char* __restrict__ W, int kmajor, int N, int Kin,
+                                           const __half* __restrict__ xh, const float* __restrict__ xf, int ldx,
+                                           int B, float* out, int ldo, int rt, int tb, int kc) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, t = lane & 3;
     const int nks = Kin / 16, RT = (N + 15) / 16, hn = Kin / kGroup / 2;
     const int ks1 = nks < kc * 16 + 16 ? nks : kc * 16 + 16;
@@ -220,13 +228,65 @@ __global__ void __launch_bounds__(128) k_dense(const char* __restrict__ W, int k
     }
 }
 
+
+template <bool F32IN>
+__global__ void __launch_bounds__(128) k_dense(const char* __restrict__ W, int kmajor, int N, int Kin,
+                                               const __half* __restrict__ xh, const float* __restrict__ xf,
+                                               int ldx, int B, float* out, int ldo) {
+    dense_tile<F32IN>(W, kmajor, N, Kin, xh, xf, ldx, B, out, ldo, blockIdx.x, blockIdx.y * 32, blockIdx.z);
+}
+
+// Two fp16-input matrices of the same shape against the same x in one launch:
+// row tiles [0, RT) of W0 into out, row tiles [RT, 2 RT) of W1 into out + off1
+// (the shared expert's A_gate x and A_up x).
+__global__ void __launch_bounds__(128) k_dense_pair(const char* __restrict__ W0, const char* __restrict__ W1,
+                                                    int N, int Kin, const __half* __restrict__ xh, int ldx, int B,
+                                                    float* out, int ldo, int off1) {
+    const int RT = (N + 15) / 16, second = blockIdx.x >= RT;
+    dense_tile<false>(second ? W1 : W0, 0, N, Kin, xh, nullptr, ldx, B, second ? out + off1 : out, ldo,
+                      blockIdx.x - (second ? RT : 0), blockIdx.y * 32, blockIdx.z);
+}
+
+// ------------------------------------------------------------ head flush ----
+// Every head of a step runs in one launch per stage (fc1, one-hot + GELU, fc2,
+// linear_init, one-hot, routing): blockIdx.z (or .y) selects the head's job.
+struct HeadJob;
+struct HeadJob {
+    const char* fc1;
+    const __half* fc1_oh;
+    const char* fc2;
+    const char* linit;
+    const __half* linit_oh;
+    const __half* x;           // the head layer's x [B][d]
+    const int32_t* exec;       // its executed ids [B][K]
+    const int32_t* prev;       // the previous step's (or null)
+    int32_t* pred_ids;         // the prediction's rows [B][K]
+    float* pred_w;
+    const float* bias;         // the target layer's routing bias (or null)
+    float scale;
+    int kind, ng, G;
+};
+static_assert(sizeof(HeadJob) <= kHeadJobBytes, "a head job fits its room in the workspace");
+enum HeadStage : int { HS_FC1 = 0, HS_FC2 = 1, HS_LINIT = 2 };
+template <bool F32IN>
+__global__ void __launch_bounds__(128) k_dense_heads(const HeadJob* __restrict__ jobs, int stage, int nkc, int N,
+                                                     int Kin, int B, const float* zbase, long long zstride,
+                                                     float* obase, int ldo, long long ostride) {
+    const int h = blockIdx.z / nkc, kc = blockIdx.z - h * nkc;
+    const HeadJob& J = jobs[h];
+    const char* W = stage == HS_FC1 ? J.fc1 : stage == HS_FC2 ? J.fc2 : J.linit;
+    dense_tile<F32IN>(W, stage == HS_FC2 ? 1 : 0, N, Kin, F32IN ? nullptr : J.x,
+                      F32IN ? zbase + h * zstride : nullptr, Kin, B, obase + h * ostride, ldo, blockIdx.x,
+                      blockIdx.y * 32, kc);
+}
+
 // ----------------------------------------------------------- k_onehot -------
 // z[b][n] += sum over executed e of M[e][n] + sum over previous e of M[E + e][n]
 // (M = [2E][N] fp16: the one-hot columns of a head matrix, transposed), then
 // GELU (erf form) if `gelu`.
-__global__ void k_onehot(float* z, int ldz, int N, const __half* __restrict__ M, const int32_t* ids,
-                         const int32_t* prev, int K, int E, int gelu) {
-    const int b = blockIdx.y, n = blockIdx.x * blockDim.x + threadIdx.x;
+__device__ __forceinline__ void onehot_col(float* z, int ldz, int N, const __half* __restrict__ M,
+                                           const int32_t* ids, const int32_t* prev, int K, int E, int gelu, int b,
+                                           int n) {
     if (n >= N) return;
     // (ids outside [0, E) were recorded as errors by the dispatch; read column 0)
     auto col = [E](int e) { return e >= 0 && e < E ? e : 0; };
@@ -238,12 +298,18 @@ __global__ void k_onehot(float* z, int ldz, int N, const __half* __restrict__ M,
     if (gelu) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
     z[(long long)b * ldz + n] = v;
 }
+// the heads' one-hot columns: of fc1 with GELU (linit = 0) or of linear_init
+__global__ void k_onehot_heads(const HeadJob* __restrict__ jobs, int linit, float* zbase, long long zstride, int N,
+                               int K, int E) {
+    const HeadJob& J = jobs[blockIdx.z];
+    onehot_col(zbase + blockIdx.z * zstride, N, N, linit ? J.linit_oh : J.fc1_oh, J.exec, J.prev, K, E, !linit,
+               blockIdx.y, blockIdx.x * blockDim.x + threadIdx.x);
+}
 
 // ------------------------------------------------------------ k_route -------
 // Routing rule of App. A, one token per warp, 8 warps per CTA.
-__global__ void __launch_bounds__(256) k_route(const float* logits, int ldl, int B, int E, int K, int kind,
-                                               int ng, int G, float scale, const float* bias, int32_t* ids_out,
-                                               float* w_out) {
+__device__ __forceinline__ void route_rows(const float* logits, int ldl, int B, int E, int K, int kind, int ng,
+                                           int G, float scale, const float* bias, int32_t* ids_out, float* w_out) {
     extern __shared__ float sm[];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, b = blockIdx.x * 8 + wid;
     float* lg = sm + wid * 3 * E;
@@ -264,17 +330,32 @@ __global__ void __launch_bounds__(256) k_route(const float* logits, int ldl, int
         w_out[b * K + lane] = rw[lane];
     }
 }
+__global__ void __launch_bounds__(256) k_route(const float* logits, int ldl, int B, int E, int K, int kind,
+                                               int ng, int G, float scale, const float* bias, int32_t* ids_out,
+                                               float* w_out) {
+    route_rows(logits, ldl, B, E, K, kind, ng, G, scale, bias, ids_out, w_out);
+}
+__global__ void __launch_bounds__(256) k_route_heads(const HeadJob* __restrict__ jobs, const float* lbase,
+                                                     long long lstride, int B, int E, int K) {
+    const HeadJob& J = jobs[blockIdx.y];
+    route_rows(lbase + blockIdx.y * lstride, E, B, E, K, J.kind, J.ng, J.G, J.scale, J.bias, J.pred_ids, J.pred_w);
+}
 
 // --------------------------------------------------------- k_dispatch -------
 // The active experts of a layer in id order, each with the positions of its
 // (token, weight) pairs; one CTA.  An id outside [0, E) records EDGE0_EINVAL
 // and counts as expert 0.
 __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const float* w, int B, int K, int E,
-                                                   int shared, int blk_gu, int blk_dn, int cap, Disp* D, int* tok,
-                                                   float* wt, WsHeader* hdr) {
+                                                   int shared, int blk_gu, int blk_dn, int cap, const int* table,
+                                                   unsigned long long* tier, Disp* D, int* tok, float* wt,
+                                                   WsHeader* hdr) {
     __shared__ int cnt[EDGE0_MAX_E], off[EDGE0_MAX_E], fill[EDGE0_MAX_E];
+    __shared__ int n_host;
     const int tid = threadIdx.x, n = B * K;
-    if (tid == 0) D->cap = cap;
+    if (tid == 0) {
+        D->cap = cap;
+        n_host = 0;
+    }
     for (int e = tid; e < E; e += blockDim.x) cnt[e] = fill[e] = 0;
     __syncthreads();
     for (int p = tid; p < n; p += blockDim.x) {
@@ -326,6 +407,14 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const flo
             D->sexp[j] = e;
             D->soff[j] = ex[0];
             D->scnt[j] = c_e;
+            // the slot table is read once per layer: a copy published later in
+            // the layer does not change where its kernels read the expert
+            int sl = e;
+            if (table) {
+                sl = (int)ld_acquire_u32(reinterpret_cast<const unsigned*>(table + e));
+                if (sl == -1) atomicAdd(&n_host, 1);
+            }
+            D->sslot[j] = sl;
             for (int i = 0; i < v[2]; ++i) gu_items(D)[ex[2] + i] = make_int2(j, i * blk_gu);
             for (int i = 0; i < v[3]; ++i) dn_items(D)[ex[3] + i] = make_int2(j, i * blk_dn);
         }
@@ -342,6 +431,10 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const flo
         D->n_dn = nd;
     }
     __syncthreads();
+    if (tid == 0 && tier && table) {   // residency counters: active routed experts, of them in the host tier
+        atomicAdd(&tier[0], (unsigned long long)a);
+        atomicAdd(&tier[1], (unsigned long long)n_host);
+    }
     for (int p = tid; p < n; p += blockDim.x) {
         int e = ids[p];
         if (e < 0 || e >= E) e = 0;
@@ -368,7 +461,7 @@ __device__ __forceinline__ bool slot_of(int j, const Disp* D, const LayerP& Ly, 
     const int nact = D->nact;
     if (j < nact) {
         const int e = D->sexp[j];
-        const int sl = Ly.slot_table ? Ly.slot_table[e] : e;
+        const int sl = D->sslot[j];
         s.host = false;
         if (sl == -1 && Ly.gu_host) {
             // host tier: the expert's weights are read from pinned host memory
@@ -970,28 +1063,47 @@ __global__ void __launch_bounds__(256, 3) k_down(const LayerP Ly, const Disp* D,
 }
 
 // ---------------------------------------------------------- k_lora_vd -------
-// One CTA per block of 8 tokens: warp j forms v = A_down act_shared of token j
-// of the block (r values), then every thread takes output rows tid, tid + 256,
-// ... and adds (alpha/r) B_down[row] v to the block's tokens (one read of a
-// B_down row serves the 8 tokens).
+// One CTA per block of 8 tokens and 512 output rows.  A_down^T and the block's
+// shared-expert act rows are staged in shared memory (one round trip), warp j
+// forms v = A_down act of token j of the block (r values), then every thread
+// takes output rows and adds (alpha/r) B_down[row] v to the block's tokens (one
+// read of a B_down row serves the 8 tokens).
 constexpr int kLoraTok = 8;
-__global__ void __launch_bounds__(256) k_lora_vd(const float* act, int Imax, int pos0, const __half* AdT,
-                                                 const __half* Bd, int r, int Is, int d, int B, float scale, float* y) {
-    const int b0 = blockIdx.x * kLoraTok, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+constexpr int kLoraRows = 512;
+__host__ __device__ inline size_t lora_vd_smem(int Is, int r) {
+    return (size_t)Is * r * 2 + (size_t)kLoraTok * Is * 4;
+}
+__global__ void __launch_bounds__(256) k_lora_vd(const float* __restrict__ act, int Imax, int pos0,
+                                                 const __half* __restrict__ AdT, const __half* __restrict__ Bd,
+                                                 int r, int Is, int d, int B, float scale, float* __restrict__ y) {
+    extern __shared__ __align__(16) char lsm[];
+    __half* sA = reinterpret_cast<__half*>(lsm);                           // [Is][r]
+    float* sx = reinterpret_cast<float*>(lsm + (size_t)Is * r * 2);       // [kLoraTok][Is]
     __shared__ float vs[kLoraTok][16];
-    {
-        const int b = b0 + wid;
+    const int b0 = blockIdx.x * kLoraTok, row0 = blockIdx.y * kLoraRows;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nb = min(kLoraTok, B - b0);
+    if (((uintptr_t)AdT & 15) == 0 && (Is * r) % 8 == 0) {
+        for (int i = tid; i < Is * r / 8; i += 256)
+            reinterpret_cast<uint4*>(sA)[i] = reinterpret_cast<const uint4*>(AdT)[i];
+    } else {
+        for (int i = tid; i < Is * r; i += 256) sA[i] = AdT[i];
+    }
+    for (int i = tid; i < nb * (Is / 4); i += 256) {
+        const int j = i / (Is / 4), k4 = i - j * (Is / 4);
+        reinterpret_cast<float4*>(sx + j * Is)[k4] =
+            reinterpret_cast<const float4*>(act + (long long)(pos0 + b0 + j) * Imax)[k4];
+    }
+    __syncthreads();
+    if (wid < nb) {
         float acc[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-        if (b < B) {
-            const float* a = act + (long long)(pos0 + b) * Imax;
-            for (int k = lane; k < Is; k += 32) {
-                const float av = a[k];
+        for (int k = lane; k < Is; k += 32) {
+            const float av = sx[wid * Is + k];
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    if (q < r) acc[q] += __half2float(AdT[(long long)k * r + q]) * av;
-            }
+            for (int q = 0; q < 16; ++q)
+                if (q < r) acc[q] += __half2float(sA[k * r + q]) * av;
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -1000,12 +1112,14 @@ __global__ void __launch_bounds__(256) k_lora_vd(const float* act, int Imax, int
         }
     }
     __syncthreads();
-    const int nb = min(kLoraTok, B - b0);
-    for (int row = tid; row < d; row += 256) {
+    const int row1 = min(d, row0 + kLoraRows);
+    for (int row = row0 + tid; row < row1; row += 256) {
         float bd[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) bd[q] = q < r ? __half2float(Bd[(long long)row * r + q]) : 0.f;
-        for (int j = 0; j < nb; ++j) {
+#pragma unroll
+        for (int j = 0; j < kLoraTok; ++j) {
+            if (j >= nb) break;
             float sj = 0.f;
 #pragma unroll
             for (int q = 0; q < 16; ++q) sj += bd[q] * vs[j][q];
@@ -1068,7 +1182,6 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
     __half* xs = reinterpret_cast<__half*>(ws + W.xs);
     float* xsum = reinterpret_cast<float*>(ws + W.xsum);
     float* lg = reinterpret_cast<float*>(ws + W.lg);
-    float* z = reinterpret_cast<float*>(ws + W.z);
     float* la = reinterpret_cast<float*>(ws + W.la);
     float* wsel = reinterpret_cast<float*>(ws + W.wsel);
     Disp* D = reinterpret_cast<Disp*>(ws + W.disp);
@@ -1096,6 +1209,9 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
     static size_t done_gu = 0, done_dn = 0, done_tc = 0;
     if (!smem_opt_in(k_gu, smem_gu, &done_gu) || !smem_opt_in(k_down, smem_dn, &done_dn)) return EDGE0_ECUDA;
     if (tcgu && !smem_opt_in(k_gu_tc, kTcSmem, &done_tc)) return EDGE0_ECUDA;
+    static size_t done_lv = 0;
+    if (lora_vd_smem(Is, r) > (size_t)smem_max) return EDGE0_EUNSUPPORTED;
+    if (!smem_opt_in(k_lora_vd, lora_vd_smem(Is, r), &done_lv)) return EDGE0_ECUDA;
     // expert grids: the CTAs that fit on the GPU at once, each looping over items
     int nsm = 0, occ_gu = 0, occ_dn = 0;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -1133,14 +1249,15 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
             w = wsel;
         }
         if (rc) return rc;
-        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, blk_gu, kDnTok, cap, D, tok, wt, hdr);
+        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, blk_gu, kDnTok, cap, Ly.slot_table,
+                                       Ly.tier_counts, D, tok, wt, hdr);
         if (!ok()) return EDGE0_ECUDA;
         const int lora = (Ly.flags & LF_LORA) ? 1 : 0;
         if (lora) {
             if (cudaMemsetAsync(la, 0, (size_t)B * 32 * 4, st) != cudaSuccess) return EDGE0_ECUDA;
-            rc = dense<false>(Ly.lora_Ag, 0, r, d, x, nullptr, d, B, la, 32, false, st);
-            if (rc == EDGE0_OK) rc = dense<false>(Ly.lora_Au, 0, r, d, x, nullptr, d, B, la + 16, 32, false, st);
-            if (rc) return rc;
+            k_dense_pair<<<dim3(2 * ((r + 15) / 16), (B + 31) / 32, (d / 16 + 15) / 16), 128, 0, st>>>(
+                Ly.lora_Ag, Ly.lora_Au, r, d, x, d, B, la, 32, 16);
+            if (!ok()) return EDGE0_ECUDA;
         }
         if (tcgu)
             k_gu_tc<<<dim3(gu_x, gu_y), kTcThreads, kTcSmem, st>>>(Ly, D, tok, wt, x, la, lora, r, B, K, d, I, Is,
@@ -1153,7 +1270,8 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
             Ly, D, tok, wt, act, B, K, d, I, Is, Imax, y, hdr);
         if (!ok()) return EDGE0_ECUDA;
         if (lora) {
-            k_lora_vd<<<(B + kLoraTok - 1) / kLoraTok, 256, 0, st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is,
+            k_lora_vd<<<dim3((B + kLoraTok - 1) / kLoraTok, (d + kLoraRows - 1) / kLoraRows), 256,
+                        lora_vd_smem(Is, r), st>>>(act, Imax, B * K, Ly.lora_AdT, Ly.lora_Bd, r, Is,
                                                                       d, B, Ly.lora_scale, y);
             if (!ok()) return EDGE0_ECUDA;
         }
@@ -1162,27 +1280,64 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
     k_norm<<<B, 256, 0, st>>>(p.h_io, y, 1, nullptr, 0.f, d, nullptr, nullptr, 0);
     if (!ok()) return EDGE0_ECUDA;
     if (prefill) return rc;
-    // head flush: every head of the step, from its layer's x and routing
-    for (int l = 0; l < L && rc == EDGE0_OK; ++l) {
+    // head flush: every head of the step, from its layer's x and routing, one
+    // launch per stage over all heads (the job table goes to the workspace with
+    // the step's parity and previous-step ids)
+    std::vector<HeadJob> jobs;
+    for (int l = 0; l < L; ++l) {
         const LayerP& Ly = p.layers[l];
         if (!(Ly.flags & LF_HEAD)) continue;
         const long long srow = (long long)Ly.sidx * B * K;
-        const __half* x = xs + (long long)Ly.sidx * B * d;
-        const int32_t* exec = p.exec_ids + (long long)par * p.Ls * B * K + srow;
-        const int32_t* prev = step > 0 ? p.exec_ids + (long long)(par ^ 1) * p.Ls * B * K + srow : nullptr;
-        rc = dense<false>(Ly.fc1, 0, H, d, x, nullptr, d, B, z, H, true, st);
-        if (rc) break;
-        k_onehot<<<dim3((H + 127) / 128, B), 128, 0, st>>>(z, H, H, Ly.fc1_oh, exec, prev, K, E, 1);
-        if (!ok()) return EDGE0_ECUDA;
-        rc = dense<true>(Ly.fc2, 1, E, H, nullptr, z, H, B, lg, E, true, st);
-        if (rc == EDGE0_OK) rc = dense<false>(Ly.linit, 0, E, d, x, nullptr, d, B, lg, E, false, st);
-        if (rc) break;
-        k_onehot<<<dim3((E + 127) / 128, B), 128, 0, st>>>(lg, E, E, Ly.linit_oh, exec, prev, K, E, 0);
-        if (!ok()) return EDGE0_ECUDA;
         const long long o = (long long)par * p.Ls * B * K + (long long)Ly.head_target * B * K;
-        rc = route(lg, B, E, K, Ly.head_route_kind, Ly.head_n_groups, Ly.head_topk_groups, Ly.head_route_scale,
-                   Ly.head_bias, p.pred_ids + o, p.pred_w + o, st);
+        HeadJob J;
+        J.fc1 = Ly.fc1;
+        J.fc1_oh = Ly.fc1_oh;
+        J.fc2 = Ly.fc2;
+        J.linit = Ly.linit;
+        J.linit_oh = Ly.linit_oh;
+        J.x = xs + (long long)Ly.sidx * B * d;
+        J.exec = p.exec_ids + (long long)par * p.Ls * B * K + srow;
+        J.prev = step > 0 ? p.exec_ids + (long long)(par ^ 1) * p.Ls * B * K + srow : nullptr;
+        J.pred_ids = p.pred_ids + o;
+        J.pred_w = p.pred_w + o;
+        J.bias = Ly.head_bias;
+        J.scale = Ly.head_route_scale;
+        J.kind = Ly.head_route_kind;
+        J.ng = Ly.head_n_groups;
+        J.G = Ly.head_topk_groups;
+        jobs.push_back(J);
     }
+    const int nh = (int)jobs.size();
+    if (nh == 0) return rc;
+    if (nh > p.Ls) return EDGE0_EINVAL;
+    // head h: fc1 output at zh + h hs, logits at lgh + h hs; the job table after
+    const long long hs = (long long)B * (H + E);
+    HeadJob* dj = reinterpret_cast<HeadJob*>(ws + W.z + ((long long)p.Ls * hs * 4 + 255) / 256 * 256);
+    float* zh = reinterpret_cast<float*>(ws + W.z);
+    float* lgh = zh + (long long)B * H;
+    const long long zs = hs, ls = hs;
+    if (cudaMemcpyAsync(dj, jobs.data(), sizeof(HeadJob) * nh, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemsetAsync(zh, 0, (size_t)nh * hs * 4, st) != cudaSuccess)
+        return EDGE0_ECUDA;
+    const int nk_d = (d / 16 + 15) / 16, nk_h = (H / 16 + 15) / 16;
+    k_dense_heads<false><<<dim3((H + 15) / 16, (B + 31) / 32, nk_d * nh), 128, 0, st>>>(
+        dj, HS_FC1, nk_d, H, d, B, nullptr, 0, zh, H, zs);
+    if (!ok()) return EDGE0_ECUDA;
+    k_onehot_heads<<<dim3((H + 127) / 128, B, nh), 128, 0, st>>>(dj, 0, zh, zs, H, K, E);
+    if (!ok()) return EDGE0_ECUDA;
+    k_dense_heads<true><<<dim3((E + 15) / 16, (B + 31) / 32, nk_h * nh), 128, 0, st>>>(
+        dj, HS_FC2, nk_h, E, H, B, zh, zs, lgh, E, ls);
+    if (!ok()) return EDGE0_ECUDA;
+    k_dense_heads<false><<<dim3((E + 15) / 16, (B + 31) / 32, nk_d * nh), 128, 0, st>>>(
+        dj, HS_LINIT, nk_d, E, d, B, nullptr, 0, lgh, E, ls);
+    if (!ok()) return EDGE0_ECUDA;
+    k_onehot_heads<<<dim3((E + 127) / 128, B, nh), 128, 0, st>>>(dj, 1, lgh, ls, E, K, E);
+    if (!ok()) return EDGE0_ECUDA;
+    const size_t rsmem = (size_t)8 * 3 * E * 4 + 2 * 8 * EDGE0_MAX_K * 4;
+    static size_t done_rh = 0;
+    if (!smem_opt_in(k_route_heads, rsmem, &done_rh)) return EDGE0_ECUDA;
+    k_route_heads<<<dim3((B + 7) / 8, nh), 256, rsmem, st>>>(dj, lgh, ls, B, E, K);
+    if (!ok()) return EDGE0_ECUDA;
     return rc;
 }
 }  // namespace

@@ -55,6 +55,7 @@ struct LayerP {
     const char* down_rows;   // down in row-tile major units (batch-1 kernel), or null
     const char* sh_down_rows;
     void* ready;             // host: event the batched path waits for before the layer
+    unsigned long long* tier_counts;   // [2] += active routed experts, += of them read from the host tier
     const char* router;      // packed fp16 [E x d]
     const char* lora_Ag;     // packed fp16 [r x d] (one row tile)
     const char* lora_Au;
@@ -338,6 +339,9 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ int ld_volatile_s32(const int* p) {
     int v;

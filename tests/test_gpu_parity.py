@@ -366,17 +366,24 @@ def _check_recorded_step(cfg, model, ref, st, before, h0, t, ties):
     return n_heads
 
 
-def _run_stack(cfg, model, steps, use_layers=False, pool_slots=None, on_pool=None):
+def _run_stack(cfg, model, steps, use_layers=False, pool_slots=None, on_pool=None, inject=None,
+               double_prefetch=False):
     """Decode `steps` steps on the GPU and check each against the oracle (see the
     protocol above).  Returns (steps compared, near-ties seen).  pool_slots: run
     the routed experts from a host tier with that many device slots per layer,
-    prefetched after each step from the predictions (on_pool(pool) at the end)."""
+    prefetched after each step from the predictions (on_pool(pool) at the end);
+    inject: (fail_every, delay_ns) for the pool's copy passes; double_prefetch:
+    request each step's prefetch twice in a row (the second finds the layers'
+    copies in flight).  Only the compute stream is synchronised between steps:
+    the pool's copies run on."""
     dm = binding.DeviceModel(model, DEV)
     st = binding.DecodeState(cfg, device=DEV)
     recorded = cfg.B == 1 and not use_layers
     if recorded:
         st.record(True)
     pool = binding.ExpertPool(dm, pool_slots) if pool_slots else None
+    if inject is not None:
+        pool.inject(*inject)
     prerouted = [l for l in range(cfg.L) if model.layers[l].prerouted]
     ref = oracle.Stack(_cpu_model(model) if model.layers[0].gate[0].is_cuda else model)
     ties = []
@@ -389,10 +396,13 @@ def _run_stack(cfg, model, steps, use_layers=False, pool_slots=None, on_pool=Non
                 binding.decode_layer(dm, l, st, h, t)
         else:
             binding.decode_step(dm, st, h, t)
-        torch.cuda.synchronize()
-        assert st.error() == 0
         if pool is not None:
-            pool.prefetch(st, t, prerouted)
+            own = [l for l in range(cfg.L) if l not in prerouted]
+            pool.prefetch(st, t, predicted=prerouted, cached=own)
+            if double_prefetch:
+                pool.prefetch(st, t, predicted=prerouted, cached=own)
+        torch.cuda.current_stream().synchronize()
+        assert st.error() == 0
         if recorded:
             assert torch.equal(h.cpu()[0], st.rec_h[cfg.L - 1].cpu())
             _check_recorded_step(cfg, model, ref, st, before, h0, t, ties)
@@ -572,6 +582,25 @@ def test_batched_35b_shapes_small_zipf():
     assert _run_stack(cfg, model, 3)[0] == 3
 
 
+def _check_pool(pool, seen):
+    """After the run: counters, residency counters, and every published slot
+    holding its expert's bytes (device compare, bit-exact)."""
+    st = pool.stats()
+    tiers = pool.tiers()
+    seen.update(stats=st, tiers=tiers)
+    for l, ((sg, sd, tb), (hg, hd)) in enumerate(zip(pool.slots, pool.host)):
+        table = tb.cpu().tolist()
+        pub = [s for s in table if s >= 0]
+        assert len(pub) == len(set(pub)), f"layer {l}: a slot published twice"
+        for e, s in enumerate(table):
+            if s < 0:
+                continue
+            g, d = pool.gu_bytes, pool.dn_bytes
+            assert torch.equal(sg[s * g:(s + 1) * g].cpu(), hg[e * g:(e + 1) * g]), (l, e, s)
+            assert torch.equal(sd[s * d:(s + 1) * d].cpu(), hd[e * d:(e + 1) * d]), (l, e, s)
+    print(f"pool: {st}; active / host-tier experts per layer: {tiers.tolist()}")
+
+
 def test_host_tier_batched_decode_matches_oracle():
     # 16 device slots for 64 experts: predicted experts are copied in ahead of
     # their layer, the rest (and own-routed layers) are read from host memory
@@ -579,11 +608,64 @@ def test_host_tier_batched_decode_matches_oracle():
                                prerouted=(1, 2), pool_frac=0.25)
     model = inputs.make_model(cfg, seed=11)
     seen = {}
-    n, _ = _run_stack(cfg, model, 4, pool_slots=16, on_pool=lambda p: seen.update(stats=p.stats()))
+    n, _ = _run_stack(cfg, model, 4, pool_slots=16, on_pool=lambda p: _check_pool(p, seen))
     assert n == 4
-    hits, copies = seen["stats"]
-    print(f"pool: {hits} hits, {copies} experts copied")
-    assert copies > 0 and hits > 0
+    st, tiers = seen["stats"], seen["tiers"]
+    assert st["published"] > 0 and st["hits"] > 0 and st["failed"] == 0 and st["bad_ids"] == 0
+    assert 0 < tiers[:, 1].sum() < tiers[:, 0].sum()
+
+
+def test_host_tier_full_cfg5_shapes_256_sequences():
+    # E = 256 experts, 64 slots per layer, 256 sequences, 35B-tier expert
+    # shapes: the predictions name more experts than there are slots, so each
+    # prerouted layer runs partly from its slots and partly from host memory
+    cfg = configs.HOST35.with_(L=3, head_owner_first=0, head_owner_last=1, prerouted=(1, 2))
+    assert (cfg.E, cfg.B, int(cfg.E * cfg.pool_frac)) == (256, 256, 64)
+    model = inputs.make_model(cfg, seed=13, device=DEV)
+    seen = {}
+    n, _ = _run_stack(cfg, model, 3, pool_slots=64, on_pool=lambda p: _check_pool(p, seen))
+    assert n == 3
+    st, tiers = seen["stats"], seen["tiers"]
+    assert st["published"] > 0 and st["hits"] > 0
+    assert tiers[1:, 1].sum() > 0 and tiers[1:, 1].sum() < tiers[1:, 0].sum()
+
+
+def test_host_tier_delayed_and_failed_copies_keep_results_exact():
+    # Host-side injection: every copy pass starts 0.4 s late and every third
+    # copy fails; each step's prefetch is requested twice.  The steps do not
+    # wait for copies: experts whose copies are late or failed are read from
+    # host memory, plans of layers with copies in flight are skipped, and every
+    # step still matches the oracle.
+    cfg = configs.HOST35.with_(L=3, E=64, B=24, head_owner_first=0, head_owner_last=1,
+                               prerouted=(1, 2), pool_frac=0.25)
+    model = inputs.make_model(cfg, seed=12)
+    seen = {}
+    n, _ = _run_stack(cfg, model, 5, pool_slots=16, inject=(3, 400_000_000), double_prefetch=True,
+                      on_pool=lambda p: _check_pool(p, seen))
+    assert n == 5
+    st, tiers = seen["stats"], seen["tiers"]
+    assert st["skipped"] > 0 and st["failed"] > 0 and st["published"] > 0
+    assert tiers[1:, 1].sum() > 0
+
+
+def test_host_tier_bounded_wait_for_copies():
+    # edge0_pool_wait polls from the host up to its limit: with the copy pass
+    # held back 0.5 s it returns EDGE0_ETIMEOUT after 2 ms, then EDGE0_OK.
+    import time
+    cfg = configs.HOST35.with_(L=3, E=64, B=24, head_owner_first=0, head_owner_last=1,
+                               prerouted=(1, 2), pool_frac=0.25)
+    model = inputs.make_model(cfg, seed=14)
+    dm = binding.DeviceModel(model, DEV)
+    st = binding.DecodeState(cfg, device=DEV)
+    pool = binding.ExpertPool(dm, 16)
+    pool.inject(0, 500_000_000)
+    binding.decode_step(dm, st, inputs.hidden(cfg, 0, seed=14).to(DEV), 0)
+    pool.prefetch(st, 0, cached=[1, 2])
+    t0 = time.time()
+    assert pool.wait(2_000_000) == binding.EDGE0_ETIMEOUT
+    assert time.time() - t0 < 0.4
+    assert pool.wait(5_000_000_000) == binding.EDGE0_OK
+    assert pool.stats()["published"] > 0
 
 
 def test_batched_8b_full_shapes_64_sequences_teacher_forced():

@@ -174,6 +174,7 @@ __device__ __forceinline__ void dense_tile(const char* __restrict__ W, int kmajo
     for (int n = 0; n < 4; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[n][e] = accl[n][e] = 0.f;
+#pragma unroll 4
     for (int ks = kc * 16 + wid; ks < ks1; ks += 4) {
         const char* ap;
         if (kmajor) {
@@ -1063,31 +1064,33 @@ __global__ void __launch_bounds__(256, 3) k_down(const LayerP Ly, const Disp* D,
 }
 
 // ---------------------------------------------------------- k_lora_vd -------
-// One CTA per block of 8 tokens and 512 output rows.  A_down^T and the block's
-// shared-expert act rows are staged in shared memory (one round trip), warp j
-// forms v = A_down act of token j of the block (r values), then every thread
-// takes output rows and adds (alpha/r) B_down[row] v to the block's tokens (one
-// read of a B_down row serves the 8 tokens).
+// One CTA per block of 8 tokens and 128 output rows.  A_down (transposed back
+// to [r][Is], rows padded by one word) and the block's shared-expert act rows
+// are staged in shared memory; warp j forms v = A_down act of token j of the
+// block (r values, lanes over Is without bank conflicts); then thread t takes
+// output row t mod 128 for four of the block's tokens and adds (alpha/r)
+// B_down[row] v (one read of a B_down row serves four tokens).
 constexpr int kLoraTok = 8;
-constexpr int kLoraRows = 512;
+constexpr int kLoraRows = 128;
+__host__ __device__ inline int lora_vd_lda(int Is) { return Is + 2; }
 __host__ __device__ inline size_t lora_vd_smem(int Is, int r) {
-    return (size_t)Is * r * 2 + (size_t)kLoraTok * Is * 4;
+    (void)r;
+    return (size_t)16 * lora_vd_lda(Is) * 2 + (size_t)kLoraTok * Is * 4;
 }
 __global__ void __launch_bounds__(256) k_lora_vd(const float* __restrict__ act, int Imax, int pos0,
                                                  const __half* __restrict__ AdT, const __half* __restrict__ Bd,
                                                  int r, int Is, int d, int B, float scale, float* __restrict__ y) {
     extern __shared__ __align__(16) char lsm[];
-    __half* sA = reinterpret_cast<__half*>(lsm);                           // [Is][r]
-    float* sx = reinterpret_cast<float*>(lsm + (size_t)Is * r * 2);       // [kLoraTok][Is]
+    const int lda = lora_vd_lda(Is);
+    __half* sA = reinterpret_cast<__half*>(lsm);                               // [16][lda]
+    float* sx = reinterpret_cast<float*>(lsm + (size_t)16 * lda * 2);         // [kLoraTok][Is]
     __shared__ float vs[kLoraTok][16];
     const int b0 = blockIdx.x * kLoraTok, row0 = blockIdx.y * kLoraRows;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nb = min(kLoraTok, B - b0);
-    if (((uintptr_t)AdT & 15) == 0 && (Is * r) % 8 == 0) {
-        for (int i = tid; i < Is * r / 8; i += 256)
-            reinterpret_cast<uint4*>(sA)[i] = reinterpret_cast<const uint4*>(AdT)[i];
-    } else {
-        for (int i = tid; i < Is * r; i += 256) sA[i] = AdT[i];
+    for (int i = tid; i < Is * r; i += 256) {
+        const int k = i / r, q = i - k * r;
+        sA[q * lda + k] = AdT[i];
     }
     for (int i = tid; i < nb * (Is / 4); i += 256) {
         const int j = i / (Is / 4), k4 = i - j * (Is / 4);
@@ -1103,7 +1106,7 @@ __global__ void __launch_bounds__(256) k_lora_vd(const float* __restrict__ act, 
             const float av = sx[wid * Is + k];
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                if (q < r) acc[q] += __half2float(sA[k * r + q]) * av;
+                if (q < r) acc[q] += __half2float(sA[q * lda + k]) * av;
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -1112,13 +1115,14 @@ __global__ void __launch_bounds__(256) k_lora_vd(const float* __restrict__ act, 
         }
     }
     __syncthreads();
-    const int row1 = min(d, row0 + kLoraRows);
-    for (int row = row0 + tid; row < row1; row += 256) {
+    const int row = row0 + (tid & (kLoraRows - 1)), j0 = (tid / kLoraRows) * (kLoraTok / 2);
+    if (row < d && j0 < nb) {
         float bd[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) bd[q] = q < r ? __half2float(Bd[(long long)row * r + q]) : 0.f;
 #pragma unroll
-        for (int j = 0; j < kLoraTok; ++j) {
+        for (int jj = 0; jj < kLoraTok / 2; ++jj) {
+            const int j = j0 + jj;
             if (j >= nb) break;
             float sj = 0.f;
 #pragma unroll

@@ -107,8 +107,9 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 // output); want_x: x = fp16(h rsqrt(mean h^2 + eps) gamma) into x_out and the
 // sums of each 64-input group of x into xsum.
 __global__ void __launch_bounds__(256) k_norm(__half* h, float* y, int add_y, const __half* gamma, float eps,
-                                              int d, __half* x_out, float* xsum, int want_x) {
+                                              int d, __half* x_out, float* xsum, int want_x, float* la) {
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (la && tid < 32) la[(long long)b * 32 + tid] = 0.f;   // the layer's LoRA A sums start at zero
     __half* hb = h + (long long)b * d;
     float* yb = y + (long long)b * d;
     float ss = 0.f;
@@ -346,10 +347,10 @@ __global__ void __launch_bounds__(256) k_route_heads(const HeadJob* __restrict__
 // The active experts of a layer in id order, each with the positions of its
 // (token, weight) pairs; one CTA.  An id outside [0, E) records EDGE0_EINVAL
 // and counts as expert 0.
-__global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const float* w, int B, int K, int E,
-                                                   int shared, int blk_gu, int blk_dn, int cap, const int* table,
-                                                   unsigned long long* tier, Disp* D, int* tok, float* wt,
-                                                   WsHeader* hdr) {
+__global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, int32_t* ids_copy, const float* w, int B,
+                                                   int K, int E, int shared, int blk_gu, int blk_dn, int cap,
+                                                   const int* table, unsigned long long* tier, Disp* D, int* tok,
+                                                   float* wt, WsHeader* hdr) {
     __shared__ int cnt[EDGE0_MAX_E], off[EDGE0_MAX_E], fill[EDGE0_MAX_E];
     __shared__ int n_host;
     const int tid = threadIdx.x, n = B * K;
@@ -361,6 +362,7 @@ __global__ void __launch_bounds__(1024) k_dispatch(const int32_t* ids, const flo
     __syncthreads();
     for (int p = tid; p < n; p += blockDim.x) {
         int e = ids[p];
+        if (ids_copy) ids_copy[p] = e;   // a prediction becomes the layer's executed ids
         if (e < 0 || e >= E) { record_error(hdr, EDGE0_EINVAL); e = 0; }
         atomicAdd(&cnt[e], 1);
     }
@@ -1235,15 +1237,18 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
         const long long srow = (long long)Ly.sidx * B * K;
         __half* x = xs + (prefill ? 0LL : (long long)Ly.sidx * B * d);
         if (Ly.ready && cudaStreamWaitEvent(st, (cudaEvent_t)Ly.ready, 0) != cudaSuccess) return EDGE0_ECUDA;
-        k_norm<<<B, 256, 0, st>>>(p.h_io, y, l > 0, Ly.gamma, Ly.eps, d, x, xsum, 1);
+        k_norm<<<B, 256, 0, st>>>(p.h_io, y, l > 0, Ly.gamma, Ly.eps, d, x, xsum, 1,
+                                  (Ly.flags & LF_LORA) ? la : nullptr);
         if (!ok()) return EDGE0_ECUDA;
         int32_t* exec = prefill ? (ids_out ? ids_out + (long long)l * B * K : reinterpret_cast<int32_t*>(ws + W.exec))
                                 : p.exec_ids + (long long)par * p.Ls * B * K + srow;
         const float* w;
+        const int32_t* ids = exec;      // the routing the dispatch reads
+        int32_t* ids_copy = nullptr;    // where it copies a prediction to
         if (!prefill && (Ly.flags & LF_PREROUTED) && step > 0) {
             const long long o = (long long)(par ^ 1) * p.Ls * B * K + srow;
-            if (cudaMemcpyAsync(exec, p.pred_ids + o, (size_t)B * K * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-                return EDGE0_ECUDA;
+            ids = p.pred_ids + o;
+            ids_copy = exec;
             w = p.pred_w + o;
         } else {
             rc = dense<false>(Ly.router, 0, E, d, x, nullptr, d, B, lg, E, true, st);
@@ -1253,12 +1258,11 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
             w = wsel;
         }
         if (rc) return rc;
-        k_dispatch<<<1, 1024, 0, st>>>(exec, w, B, K, E, Ly.sh_gu ? 1 : 0, blk_gu, kDnTok, cap, Ly.slot_table,
-                                       Ly.tier_counts, D, tok, wt, hdr);
+        k_dispatch<<<1, 1024, 0, st>>>(ids, ids_copy, w, B, K, E, Ly.sh_gu ? 1 : 0, blk_gu, kDnTok, cap,
+                                       Ly.slot_table, Ly.tier_counts, D, tok, wt, hdr);
         if (!ok()) return EDGE0_ECUDA;
         const int lora = (Ly.flags & LF_LORA) ? 1 : 0;
         if (lora) {
-            if (cudaMemsetAsync(la, 0, (size_t)B * 32 * 4, st) != cudaSuccess) return EDGE0_ECUDA;
             k_dense_pair<<<dim3(2 * ((r + 15) / 16), (B + 31) / 32, (d / 16 + 15) / 16), 128, 0, st>>>(
                 Ly.lora_Ag, Ly.lora_Au, r, d, x, d, B, la, 32, 16);
             if (!ok()) return EDGE0_ECUDA;
@@ -1281,7 +1285,7 @@ int run_batched(const Prog& p, int32_t* ids_out, cudaStream_t st) {
         }
     }
     // the last layer's output
-    k_norm<<<B, 256, 0, st>>>(p.h_io, y, 1, nullptr, 0.f, d, nullptr, nullptr, 0);
+    k_norm<<<B, 256, 0, st>>>(p.h_io, y, 1, nullptr, 0.f, d, nullptr, nullptr, 0, nullptr);
     if (!ok()) return EDGE0_ECUDA;
     if (prefill) return rc;
     // head flush: every head of the step, from its layer's x and routing, one

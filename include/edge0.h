@@ -20,14 +20,24 @@
  *
  * Conventions for every call
  *   - Pointers are DEVICE pointers unless the argument says HOST.  The caller
- *     owns every buffer; the library borrows them for the call, never frees them
- *     and keeps no global state -- except edge0_moe_int4_forward_noalloc, whose
- *     scratch is a fixed array inside the library (see its section) and whose
- *     device-side status is read with edge0_noalloc_error.
+ *     owns every buffer; the library borrows them for the call and never frees
+ *     them.  Its only state of its own: caches of tables it derives from the
+ *     shapes and descriptors (the batch-1 kernel's per-shape plan table and its
+ *     device copy of the layer descriptors), allocated and uploaded on the first
+ *     call that needs them and kept for the process; the expert pool's device
+ *     state (owned by its handle); and edge0_moe_int4_forward_noalloc's fixed
+ *     scratch array (see its section; its device-side status is read with
+ *     edge0_noalloc_error).
  *   - fp16 tensors are IEEE binary16 (passed as uint16_t); fp32 as float.
- *   - Every call enqueues work on `stream` and returns without synchronising.
- *     Arguments are validated on the host before anything is launched; an
- *     invalid argument returns EDGE0_EINVAL and launches nothing.
+ *   - Every call enqueues work on `stream` and returns without synchronising,
+ *     except where its section says otherwise (edge0_state_error, the pool's
+ *     read-outs and set-up) and the first-use uploads above.  Arguments are
+ *     validated on the host before anything is launched; an invalid argument
+ *     returns EDGE0_EINVAL and launches nothing.
+ *   - Stream capture into CUDA graphs is supported only for the allocation-free
+ *     call (see its section): the first-use uploads above are synchronous, and
+ *     the batched path (B > 4) and prefill upload a small per-call table from
+ *     host memory.
  *   - Kernels never trap: a wait that runs out of time records EDGE0_ETIMEOUT in
  *     the route state's control block (read it with edge0_state_error) and the
  *     kernel returns.

@@ -44,6 +44,14 @@ void route_into(const edge0_route& r, int* kind, int* ng, int* tg, float* sc, co
     *bias = r.bias;
 }
 
+// The kernel parameter block of a call (~32 KB): one per calling thread, reused
+// by every call of that thread (no heap allocation per call; a call holds it
+// only until it has enqueued its launches).
+Prog* call_prog() {
+    static thread_local Prog prog;
+    return &prog;
+}
+
 int fill_layer(const edge0_layer_desc& Ld, const Dims& D, int Lstate, LayerP& P) {
     const edge0_moe_desc& m = Ld.moe;
     if (m.d != D.d || m.E != D.E || m.K != D.K || m.I != D.I || m.Is != D.Is) return EDGE0_EINVAL;
@@ -181,7 +189,7 @@ int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_rout
         if (rc) return rc;
     }
     static_assert(sizeof(Prog) <= 32000, "kernel parameter block too large");
-    Prog* p = new Prog;
+    Prog* p = call_prog();
     memset(p, 0, sizeof(Prog));
     p->mode = MODE_DECODE;
     p->L = L;
@@ -204,7 +212,6 @@ int decode_common(const edge0_layer_desc* layers, int L, uint16_t* h, edge0_rout
         else if (B == 1 && decode1_check(*p) == EDGE0_OK) rc = decode1_launch(*p, stream);
         else rc = engine_launch(*p, stream);
     }
-    delete p;
     return rc;
 }
 
@@ -311,7 +318,7 @@ extern "C" int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h,
     if (D.d % 128) return EDGE0_EINVAL;
     const size_t need = edge0_prefill_workspace_bytes(T, D.d, D.E, D.K, D.I, D.Is);
     if (need == 0 || workspace_bytes < need) return EDGE0_EINVAL;
-    Prog* p = new Prog;
+    Prog* p = call_prog();
     memset(p, 0, sizeof(Prog));
     p->mode = MODE_PREFILL;
     p->L = L;
@@ -337,7 +344,6 @@ extern "C" int edge0_prefill(const edge0_layer_desc* layers, int L, uint16_t* h,
     }
     p->tc_gu = (flags & EDGE0_PREFILL_TCGEN05_GATE_UP) ? 1 : 0;
     if (rc == EDGE0_OK) rc = batch_prefill(*p, ids_out, stream);
-    delete p;
     return rc;
 }
 
@@ -359,7 +365,7 @@ extern "C" int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t*
     L.moe.Is = D.Is;
     L.router = moe->gate_up;   // not used in this mode; satisfies the layer check
     L.route.kind = EDGE0_ROUTE_SOFTMAX_TOPK;
-    Prog* p = new Prog;
+    Prog* p = call_prog();
     memset(p, 0, sizeof(Prog));
     p->mode = MODE_MOE;
     p->L = 1;
@@ -373,7 +379,6 @@ extern "C" int edge0_moe_int4_forward(const edge0_moe_desc* moe, const uint16_t*
     p->ws = (char*)workspace;
     rc = fill_layer(L, D, 1, p->layers[0]);
     if (rc == EDGE0_OK) rc = engine_launch(*p, stream);
-    delete p;
     return rc;
 }
 
@@ -401,7 +406,7 @@ extern "C" int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t*
     L.has_head = 1;
     L.head = *head;
     L.head_target = 0;
-    Prog* p = new Prog;
+    Prog* p = call_prog();
     memset(p, 0, sizeof(Prog));
     p->mode = MODE_HEAD;
     p->L = 1;
@@ -417,6 +422,5 @@ extern "C" int edge0_prerouter_topk(const edge0_head_desc* head, const uint16_t*
     p->ws = (char*)workspace;
     rc = fill_layer(L, D, 1, p->layers[0]);
     if (rc == EDGE0_OK) rc = engine_launch(*p, stream);
-    delete p;
     return rc;
 }

@@ -358,3 +358,17 @@ def test_protocol_matches_a_restatement_under_random_operations(lib, seed):
             assert p.table[l].tolist() == m.table[l], f"layer {l}"
         assert p.stats() == m.st
         p.check_published()
+
+
+def test_device_init_without_a_gpu_leaves_the_host_model_usable(lib):
+    # no GPU here: the device state cannot be allocated; the call reports it
+    # and the pool stays on the host model
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present (the host buffers below are not device memory)")
+    p = HostPool(lib, 1, 8, 2)
+    assert lib.edge0_pool_device_init(p.p) == binding.EDGE0_ECUDA
+    p.prefetch({0: [1, 2]}, 2)
+    p.copy()
+    assert sorted(e for e in range(8) if p.table[0][e] >= 0) == [1, 2]
+    p.check_published()

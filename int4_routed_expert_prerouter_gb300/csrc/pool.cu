@@ -39,7 +39,10 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kCopyVec = 16;                                    // uint4 per thread and chunk
 constexpr int kCopyChunk = kCopyThreads * kCopyVec * 16;       // 64 KB
-constexpr int kCopyCtas = 32;
+// few copy CTAs: a resident copy CTA keeps an expert kernel's CTA off its SM
+// (the expert kernels take whole SMs), so the copies run on 8 SMs at a time;
+// they still end long before the next step (~370 MB per step)
+constexpr int kCopyCtas = 8;
 constexpr unsigned long long kMaxDelayNs = 1000000000ull;
 
 struct PoolLayerDev {
